@@ -1,0 +1,323 @@
+"""Decode throughput of the batch-1 Llama decode pass on GB300.
+
+Workload: Llama-3.2-1B-shaped model with Q8_0 weights (16 layers, d 2048,
+32/8 heads of 64, FFN 8192, vocab 128256, tied output, RoPE base 500000 with
+unit frequency factors), seeded synthetic weights, the F16 KV cache pre-filled
+with 4095 seeded rows, one decode step at pos 4095 (context 4096) per step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line on rank 0.  ``value`` is device-timed decode tok/s (CUDA events
+on the library's stream, inputs resident in HBM; the step reads 1.45 GB, far
+more than the 129 MB L2, so no flush is needed).  ``e2e`` is the same metric
+through the synchronous C-ABI call with pinned host buffers (token in, argmax
+and logits out).  ``roofline`` relates the step kernel's algorithmic bytes to
+the measured HBM copy bandwidth.  With N > 1 every rank runs an independent
+replica (a batch-1 step does not shard); ``value`` sums the ranks.
+``--impl reference`` times the CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "decode tok/s @batch1 (Llama-3.2-1B-shape Q8_0, ctx 4k); % HBM roofline"
+POS = 4095
+CFG = synth.LLAMA1B_Q8
+KERNEL_SOURCES = ["llama_decode_forward_gb300/csrc/decode_step.cu", "llama_decode_forward_gb300/csrc/llm_internal.cuh"]
+
+
+# ------------------------------------------------------- byte accounting --
+def weight_bytes(cfg, n_elems: int) -> int:
+    return {synth.F32: 4 * n_elems, synth.F16: 2 * n_elems, synth.Q8_0: n_elems // 32 * 34}[cfg.wtype]
+
+
+def matrix_elems(cfg) -> tuple[int, int]:
+    """(elements of the layer matrices, elements of the logits matrix)."""
+    d, q, kv, f = cfg.dim, cfg.q_dim, cfg.kv_dim, cfg.ffn_dim
+    per_layer = d * q + 2 * d * kv + q * d + 3 * d * f
+    return cfg.n_layers * per_layer, cfg.vocab * d
+
+
+def algorithmic_bytes(cfg, pos: int) -> int:
+    """Bytes one decode step must move: every matrix once (the logits matrix is
+    the embedding when tied), the F32 norm gains and biases, and the F16 K/V
+    rows 0..pos of every layer."""
+    layers, logits = matrix_elems(cfg)
+    b = weight_bytes(cfg, layers) + weight_bytes(cfg, logits)
+    b += 4 * (2 * cfg.n_layers + 1) * cfg.dim
+    if cfg.bias:
+        b += 4 * cfg.n_layers * (cfg.q_dim + 2 * cfg.kv_dim)
+    b += (pos + 1) * cfg.n_layers * 2 * cfg.kv_dim * 2
+    return b
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for s in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, s), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "decode_step_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_hash") != kernel_hash() or d.get("pos") != POS:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ clocks --
+class ClockSampler:
+    def __init__(self, device_uuid: str | None):
+        self.proc = None
+        self.path = None
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        cmd = ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if device_uuid:
+            cmd += ["-i", device_uuid]
+        try:
+            import tempfile
+            self.path = tempfile.mktemp(suffix=".csv")
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------- CPU baseline --
+def cpu_oracle_sample(W, tok: int, budget_s: float = 12.0, min_steps: int = 1, max_steps: int | None = None):
+    """The oracle (single thread) on the same workload: decode steps at pos
+    4095 after the same 4095 pre-filled rows, as many as fit in the budget."""
+    import oracle
+    ora = oracle.OracleModel(CFG, W, max_seq=POS + 1)
+    for l in range(CFG.n_layers):
+        for which in (0, 1):
+            ora.set_kv_rows_f16(l, which, synth.kv_rows(CFG, l, which, POS))
+    n, t0 = 0, time.perf_counter()
+    while True:
+        ora.forward(tok, POS)
+        n += 1
+        el = time.perf_counter() - t0
+        if (n >= min_steps and el >= budget_s) or (max_steps and n >= max_steps):
+            break
+    ora.close()
+    return n, el
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    W = synth.make_weights(CFG)
+    tok = int(synth.prompt(CFG, 1)[0])
+    warm = min(args.warmup, 1)
+    if warm:
+        cpu_oracle_sample(W, tok, budget_s=0.0, min_steps=warm, max_steps=warm)
+    n, el = cpu_oracle_sample(W, tok, budget_s=min(180.0, 10.0 * max(1, args.steps)), min_steps=1,
+                              max_steps=args.steps)
+    v = n / el
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": args.gpus, "steps": n,
+            "warmup": warm, "ms_per_step": 1000.0 * el / n, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random Q8_0 weights and KV rows)",
+            "config": {"workload": "llama-3.2-1b-shape q8_0 decode, batch 1, step at pos 4095 (ctx 4096)",
+                       "pos": POS, "implementation": "CPU oracle (plain C, single thread)"},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{n} full decode steps at pos 4095, 1 thread"},
+            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- ours --
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import llama_decode_forward_gb300 as L
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.cuda.current_device()
+
+    W = synth.make_weights(CFG)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        dec = L.Decoder(CFG, W, stream=stream.cuda_stream)
+        for l in range(CFG.n_layers):
+            k, v = dec.kv_tensors(l)
+            for which, t in ((0, k), (1, v)):
+                rows = synth.kv_rows(CFG, l, which, POS)
+                t[:POS].copy_(torch.from_numpy(rows.view(np.int16)).to("cuda"))
+    torch.cuda.synchronize()
+    tok = int(synth.prompt(CFG, 1)[0])
+    token_dev = torch.tensor([tok], dtype=torch.int32, device="cuda")
+    argmax_dev = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step():
+        L.llm_decode_step_async(dec.h, token_dev, POS, argmax_dev)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    L.llm_sync(dec.h)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    time.sleep(0.3)
+    launches0 = L.llm_launch_count(dec.h)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = L.llm_launch_count(dec.h) - launches0
+    L.llm_sync(dec.h)
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * args.steps / (total_ms / 1000.0)
+
+    # end to end through the synchronous C-ABI call, pinned host buffers
+    logits_pin = torch.empty(CFG.vocab, dtype=torch.float32, pin_memory=True)
+    logits_np = logits_pin.numpy()
+    for _ in range(max(args.warmup, 3)):
+        L.llm_decode_step(dec.h, tok, POS, logits_np)
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        L.llm_decode_step(dec.h, tok, POS, logits_np)
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = world * args.steps / e2e_s
+
+    nbytes = algorithmic_bytes(CFG, POS)
+    kern_ms = statistics.mean(per_launch)
+    peaks = measured_peaks()
+    achieved = nbytes / (kern_ms / 1000.0) / 1e9
+    traffic = stored_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded random Q8_0 weights and KV rows)",
+        "config": {"workload": "llama-3.2-1b-shape q8_0 decode, batch 1, step at pos 4095 (ctx 4096)",
+                   "n_layers": CFG.n_layers, "dim": CFG.dim, "vocab": CFG.vocab, "pos": POS,
+                   "bytes_per_step": nbytes, "l2": "working set 1.45 GB > 129 MB L2; no flush",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "decode_step_kernel<Q8_0> (whole step, one launch)",
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+                     "frac_of_8tbs_nominal": achieved / 8000.0},
+        "e2e": {"value": e2e, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4 + 4 + 4 * CFG.vocab},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        n, el = cpu_oracle_sample(W, tok, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": n / el, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{n} full decode steps at pos 4095 of the same model, 1 thread, {el:.1f} s"}
+    dec.close()
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,179 @@
+/*
+ * llm.h — C ABI of libllmdecode: batch-1 decode forward pass of a Llama-family
+ * model on one NVIDIA GB300 (sm_103a), plus an F16 batched prefill.
+ *
+ * What the calls compute is the forward pass of "The Forward Pass in Java"
+ * (codeloopback.dev, llm-forward-pass), Example 13 (`Llama.forward`): embedding
+ * lookup, per layer RMSNorm, Q/K/V projections (+ optional biases), RoPE on q
+ * and k (normal or NEOX pairs), K/V appended to an F16 cache at row `pos`,
+ * grouped-query attention over rows 0..pos, output projection + residual,
+ * RMSNorm, SwiGLU feed-forward + residual; then the final RMSNorm, the logits
+ * product (tied to the embedding when there is no output matrix) and the greedy
+ * argmax of Example 9.  "What a Llama model computes, and why" (branes-ai
+ * synapse) §2 gives the same steps with Llama-3.2-1B shapes, §2.4 the per-pair
+ * frequency factors and §4 the batched prefill.
+ *
+ * Conventions for every call:
+ *   - Return value: LLM_OK (0) or a negative llm_status.  On failure nothing is
+ *     enqueued unless the status says so, and llm_last_error(h) holds a one-line
+ *     reason.  No call aborts or prints.
+ *   - Pointers documented as "device" must point to memory of the current CUDA
+ *     device; "host" pointers to ordinary (pageable or pinned) host memory.
+ *   - A handle is not thread-safe: one host thread drives a handle at a time.
+ *   - All device work of a handle is enqueued on the stream given at creation.
+ *     "Synchronous" calls wait for that stream before returning.
+ */
+#ifndef LLM_H
+#define LLM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL means the legacy default stream. */
+typedef struct CUstream_st *llm_stream_t;
+
+/* Weight storage types, numbered as ggml's type ids ("Loading GGUF with the
+ * FFM API", tensor types F32 = 0, F16 = 1, Q8_0 = 8). */
+typedef enum { LLM_F32 = 0, LLM_F16 = 1, LLM_Q8_0 = 8 } llm_dtype;
+
+typedef enum {
+    LLM_OK = 0,
+    LLM_ERR_INVALID_ARG = -1,     /* NULL pointer, inconsistent shape, bad config field */
+    LLM_ERR_UNSUPPORTED = -2,     /* a valid model this build does not handle (dtype, head size, ...) */
+    LLM_ERR_OUT_OF_RANGE = -3,    /* token not in [0, vocab), pos not in [0, max_seq), pos0+n > max_seq */
+    LLM_ERR_CUDA = -4,            /* a CUDA runtime call failed; llm_last_error has its message */
+    LLM_ERR_NO_MEMORY = -5,       /* device allocation failed */
+    LLM_ERR_DEVICE_TIMEOUT = -6,  /* a bounded wait inside a kernel gave up; the step's outputs are invalid */
+    LLM_ERR_STATE = -7            /* call not valid in the handle's state (e.g. after a device error) */
+} llm_status;
+
+/* Model shape ("The Forward Pass in Java", Example 1, Config record).
+ * head_dim * n_heads must equal dim; n_heads must be a multiple of n_kv_heads;
+ * rope_dims is even and <= head_dim (dims beyond it are not rotated);
+ * head_dim is a multiple of 8 and at most 256.  For LLM_Q8_0, dim and ffn_dim
+ * are multiples of 32; for LLM_F16, multiples of 8; for LLM_F32, of 4.
+ * max_seq is the number of KV-cache rows the handle allocates. */
+typedef struct {
+    int n_layers, dim, n_heads, n_kv_heads, head_dim, ffn_dim, vocab, max_seq, rope_dims;
+    float eps;          /* RMSNorm epsilon */
+    float rope_base;    /* RoPE frequency base */
+    int rope_neox;      /* 0: pairs (2i, 2i+1) (llama); 1: pairs (i, i + rope_dims/2) (qwen2) */
+    int wtype;          /* llm_dtype of every matrix, the embedding and the output */
+} llm_config;
+
+/* One layer's tensors, all DEVICE pointers in GGUF layout ("The Forward Pass
+ * in Java", Example 5): a [in -> out] matrix is `out` rows of `in` values
+ * (F32/F16) or of in/32 Q8_0 blocks of 34 bytes (FP16 scale, 32 int8), row r
+ * at r * row_bytes — the same bytes as a PyTorch [out, in] tensor.
+ * attn_norm / ffn_norm: F32 [dim].  bq [n_heads*head_dim], bk / bv
+ * [n_kv_heads*head_dim]: F32 or NULL (no bias).  wq [dim -> n_heads*head_dim],
+ * wk / wv [dim -> n_kv_heads*head_dim], wo [n_heads*head_dim -> dim],
+ * w_gate / w_up [dim -> ffn_dim], w_down [ffn_dim -> dim]. */
+typedef struct {
+    const float *attn_norm, *ffn_norm, *bq, *bk, *bv;
+    const void *wq, *wk, *wv, *wo, *w_gate, *w_up, *w_down;
+} llm_layer_weights;
+
+/* tok_embd: [dim -> vocab] in wtype (DEVICE).  output_norm: F32 [dim] (DEVICE).
+ * output: [dim -> vocab] in wtype, or NULL for tied embeddings ("The Forward
+ * Pass in Java", Example 9).  rope_freqs: F32 [rope_dims/2] per-pair divisors
+ * of the angle ("What a Llama model computes, and why" §2.4), or NULL for 1.
+ * layers: HOST array of n_layers records. */
+typedef struct {
+    const void *tok_embd;
+    const float *output_norm;
+    const void *output;
+    const float *rope_freqs;
+    const llm_layer_weights *layers;
+} llm_weights;
+
+typedef struct llm_handle llm_handle;
+
+/* Creates a handle: validates the config, copies every tensor once into the
+ * library's own device layout (Q8_0 split into 16-byte aligned int8 quants and
+ * FP16 scales; Q/K/V rows and gate/up rows fused), allocates the F16 KV cache
+ * [n_layers][2][max_seq][n_kv_heads][head_dim] and the activations.  The
+ * caller's weight buffers are only read during this call.  Synchronous.
+ * Errors: INVALID_ARG, UNSUPPORTED, NO_MEMORY, CUDA; *out is set to NULL then. */
+int llm_create(const llm_config *cfg, const llm_weights *w, llm_stream_t stream, llm_handle **out);
+
+/* Starts a new sequence (P4 "The Engine": Attention.reset).  Logical only: the
+ * cache is not cleared; rows are overwritten as positions are decoded.  Also
+ * clears a sticky device error.  Synchronous. */
+int llm_reset(llm_handle *h);
+
+/* One decode step, synchronous, HOST in/out: token at position `pos`.  Writes
+ * K/V row `pos` of every layer, attends over rows 0..pos (rows 0..pos-1 must
+ * hold this sequence's K/V, as in Llama.forward), and returns the logits
+ * (vocab floats, copied to logits_host when not NULL) and the greedy argmax
+ * (first index of the maximum, to argmax_host when not NULL).
+ * Errors: OUT_OF_RANGE (token, pos), DEVICE_TIMEOUT, CUDA, STATE. */
+int llm_decode_step(llm_handle *h, int32_t token, int32_t pos, float *logits_host, int32_t *argmax_host);
+
+/* The same step enqueued without waiting.  The token is read on the device
+ * from token_dev (so it can be the previous step's argmax); the argmax is
+ * written to argmax_dev (DEVICE, may equal token_dev + 1 etc.); the logits stay
+ * in the handle's buffer (llm_logits_device).  pos is range-checked on the
+ * host; the token is clamped on the device and an out-of-range token sets the
+ * handle's device error (reported by llm_sync as OUT_OF_RANGE). */
+int llm_decode_step_async(llm_handle *h, const int32_t *token_dev, int32_t pos, int32_t *argmax_dev);
+
+/* Greedy generation with device-side feedback ("The Forward Pass in Java",
+ * Example 12 loop, without the end-of-generation check): n_steps steps at
+ * positions pos..pos+n_steps-1; step 0 consumes `token`, step i > 0 consumes
+ * tokens_dev[i-1]; step i writes its argmax to tokens_dev[i] (DEVICE, n_steps
+ * int32).  Enqueued without waiting; no host round trip between steps. */
+int llm_generate(llm_handle *h, int32_t token, int32_t pos, int32_t n_steps, int32_t *tokens_dev);
+
+/* Batched prefill of tokens_host[0..n) at positions pos0..pos0+n-1 ("What a
+ * Llama model computes, and why" §4): every K/V row is written and token i
+ * attends to rows 0..pos0+i; only the last token's logits are produced (to
+ * logits_host when not NULL; argmax to argmax_host when not NULL).  F16
+ * weights run the projections as tensor-core GEMMs; other types run the decode
+ * step token by token.  Synchronous.  Errors: OUT_OF_RANGE, INVALID_ARG, CUDA. */
+int llm_prefill(llm_handle *h, const int32_t *tokens_host, int32_t n, int32_t pos0,
+                float *logits_host, int32_t *argmax_host);
+
+/* Waits for the handle's stream and reports a device-side error of the
+ * enqueued steps (DEVICE_TIMEOUT, OUT_OF_RANGE) or CUDA. */
+int llm_sync(llm_handle *h);
+
+/* DEVICE pointer to the logits of the latest step (vocab floats); valid until
+ * the next step on the handle and the handle's destruction. */
+const float *llm_logits_device(const llm_handle *h);
+
+/* Test hook: DEVICE pointers to layer `layer`'s K and V cache,
+ * [max_seq][n_kv_heads][head_dim] FP16 each ("The Forward Pass in Java",
+ * Example 7: element pos*kv_dim + kv_head*head_dim + i).  Writable, so a
+ * harness can pre-fill rows of a long context. */
+int llm_kv_view(llm_handle *h, int layer, uint16_t **k_dev, uint16_t **v_dev);
+
+/* Test hook: runs the device KV store on given values — k_dev / v_dev are
+ * DEVICE F32 vectors of n_kv_heads*head_dim already rotated — writing row `pos`
+ * of layer `layer` exactly as the decode step does (FP16, round to nearest
+ * even; "The Forward Pass in Java", Example 10).  Synchronous. */
+int llm_test_kv_store(llm_handle *h, int layer, int32_t pos, const float *k_dev, const float *v_dev);
+
+/* Test hook: decodes rows [row0, row0+n_rows) of one weight matrix from the
+ * library's own layout with the same device routine the matrix-vector kernels
+ * use, into out_dev (DEVICE, n_rows*cols F32).  which: 0 wq, 1 wk, 2 wv, 3 wo,
+ * 4 w_gate, 5 w_up, 6 w_down (of `layer`), 7 tok_embd, 8 output.  Synchronous. */
+int llm_test_dequant_rows(llm_handle *h, int which, int layer, int32_t row0, int32_t n_rows, float *out_dev);
+
+/* Number of kernel launches enqueued on the handle's stream so far (all calls). */
+int64_t llm_launch_count(const llm_handle *h);
+
+/* Releases every device buffer of the handle (after waiting for its stream). */
+void llm_destroy(llm_handle *h);
+
+const char *llm_status_string(int status);
+const char *llm_last_error(const llm_handle *h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LLM_H */

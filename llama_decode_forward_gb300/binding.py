@@ -1,0 +1,267 @@
+"""ctypes binding of libllmdecode with the names of include/llm.h.
+
+Argument marshalling only: every step of the decode pass runs in the CUDA
+library.  PyTorch is used for device memory and streams (``DeviceWeights``
+uploads host arrays into CUDA tensors).  If the library cannot be built or
+loaded, importing this module raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+LLM_F32, LLM_F16, LLM_Q8_0 = 0, 1, 8
+LLM_OK = 0
+LLM_ERR_INVALID_ARG, LLM_ERR_UNSUPPORTED, LLM_ERR_OUT_OF_RANGE = -1, -2, -3
+LLM_ERR_CUDA, LLM_ERR_NO_MEMORY, LLM_ERR_DEVICE_TIMEOUT, LLM_ERR_STATE = -4, -5, -6, -7
+
+
+class llm_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("n_layers", "dim", "n_heads", "n_kv_heads", "head_dim", "ffn_dim",
+                                            "vocab", "max_seq", "rope_dims")] + \
+               [("eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("rope_neox", ctypes.c_int),
+                ("wtype", ctypes.c_int)]
+
+
+class llm_layer_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("attn_norm", "ffn_norm", "bq", "bk", "bv", "wq", "wk", "wv", "wo",
+                                               "w_gate", "w_up", "w_down")]
+
+
+class llm_weights(ctypes.Structure):
+    _fields_ = [("tok_embd", ctypes.c_void_p), ("output_norm", ctypes.c_void_p), ("output", ctypes.c_void_p),
+                ("rope_freqs", ctypes.c_void_p), ("layers", ctypes.POINTER(llm_layer_weights))]
+
+
+_vp, _i32, _int = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int
+_SIGS = {
+    "llm_create": ([ctypes.POINTER(llm_config), ctypes.POINTER(llm_weights), _vp, ctypes.POINTER(_vp)], _int),
+    "llm_reset": ([_vp], _int),
+    "llm_decode_step": ([_vp, _i32, _i32, _vp, _vp], _int),
+    "llm_decode_step_async": ([_vp, _vp, _i32, _vp], _int),
+    "llm_generate": ([_vp, _i32, _i32, _i32, _vp], _int),
+    "llm_prefill": ([_vp, _vp, _i32, _i32, _vp, _vp], _int),
+    "llm_sync": ([_vp], _int),
+    "llm_logits_device": ([_vp], _vp),
+    "llm_kv_view": ([_vp, _int, ctypes.POINTER(_vp), ctypes.POINTER(_vp)], _int),
+    "llm_test_kv_store": ([_vp, _int, _i32, _vp, _vp], _int),
+    "llm_test_dequant_rows": ([_vp, _int, _int, _i32, _i32, _vp], _int),
+    "llm_launch_count": ([_vp], ctypes.c_int64),
+    "llm_destroy": ([_vp], None),
+    "llm_status_string": ([_int], ctypes.c_char_p),
+    "llm_last_error": ([_vp], ctypes.c_char_p),
+}
+
+
+def declared_symbols(header: str | None = None) -> list[str]:
+    """Names of the functions include/llm.h declares."""
+    import re
+    header = header or os.path.join(_build.ROOT, "include", "llm.h")
+    with open(header) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(llm_\w+)\s*\(", text, re.M)))
+
+
+def load_library(path: str | None = None):
+    lib = ctypes.CDLL(path or _build.build())
+    for name, (args, res) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = load_library()
+LIBRARY_PATH = _lib._name
+
+
+class LlmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_lib.llm_status_string(status).decode()} ({status}): {message}")
+        self.status = status
+
+
+def _check(rc: int, h=None):
+    if rc != LLM_OK:
+        msg = _lib.llm_last_error(h).decode() if h else ""
+        raise LlmError(rc, msg)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+# ------------------------------------------------------ the C functions --
+def llm_create(cfg: llm_config, weights: llm_weights, stream=None):
+    h = _vp()
+    _check(_lib.llm_create(ctypes.byref(cfg), ctypes.byref(weights), stream, ctypes.byref(h)))
+    return h.value
+
+
+def llm_reset(h):
+    _check(_lib.llm_reset(h), h)
+
+
+def llm_decode_step(h, token: int, pos: int, logits_host: np.ndarray | None = None) -> int:
+    out = ctypes.c_int32(0)
+    if logits_host is not None:
+        assert logits_host.dtype == np.float32 and logits_host.flags.c_contiguous
+    _check(_lib.llm_decode_step(h, int(token), int(pos), _ptr(logits_host), ctypes.addressof(out)), h)
+    return out.value
+
+
+def llm_decode_step_async(h, token_dev, pos: int, argmax_dev):
+    _check(_lib.llm_decode_step_async(h, _ptr(token_dev), int(pos), _ptr(argmax_dev)), h)
+
+
+def llm_generate(h, token: int, pos: int, n_steps: int, tokens_dev):
+    _check(_lib.llm_generate(h, int(token), int(pos), int(n_steps), _ptr(tokens_dev)), h)
+
+
+def llm_prefill(h, tokens_host, pos0: int, logits_host: np.ndarray | None = None) -> int:
+    t = np.ascontiguousarray(tokens_host, dtype=np.int32)
+    out = ctypes.c_int32(0)
+    _check(_lib.llm_prefill(h, t.ctypes.data, t.size, int(pos0), _ptr(logits_host), ctypes.addressof(out)), h)
+    return out.value
+
+
+def llm_sync(h):
+    _check(_lib.llm_sync(h), h)
+
+
+def llm_logits_device(h) -> int:
+    return _lib.llm_logits_device(h)
+
+
+def llm_kv_view(h, layer: int):
+    k, v = _vp(), _vp()
+    _check(_lib.llm_kv_view(h, layer, ctypes.byref(k), ctypes.byref(v)), h)
+    return k.value, v.value
+
+
+def llm_test_kv_store(h, layer: int, pos: int, k_dev, v_dev):
+    _check(_lib.llm_test_kv_store(h, layer, pos, _ptr(k_dev), _ptr(v_dev)), h)
+
+
+def llm_test_dequant_rows(h, which: int, layer: int, row0: int, n_rows: int, out_dev):
+    _check(_lib.llm_test_dequant_rows(h, which, layer, row0, n_rows, _ptr(out_dev)), h)
+
+
+def llm_launch_count(h) -> int:
+    return _lib.llm_launch_count(h)
+
+
+def llm_destroy(h):
+    _lib.llm_destroy(h)
+
+
+def llm_status_string(status: int) -> str:
+    return _lib.llm_status_string(status).decode()
+
+
+def llm_last_error(h) -> str:
+    return _lib.llm_last_error(h).decode()
+
+
+# ------------------------------------------------------- device plumbing --
+def config_struct(cfg) -> llm_config:
+    return llm_config(n_layers=cfg.n_layers, dim=cfg.dim, n_heads=cfg.n_heads, n_kv_heads=cfg.n_kv_heads,
+                      head_dim=cfg.head_dim, ffn_dim=cfg.ffn_dim, vocab=cfg.vocab, max_seq=cfg.max_seq,
+                      rope_dims=cfg.rope_dims, eps=cfg.eps, rope_base=cfg.rope_base, rope_neox=int(cfg.rope_neox),
+                      wtype=int(cfg.wtype))
+
+
+class DeviceWeights:
+    """Host arrays (GGUF layout) copied into CUDA tensors, and the llm_weights
+    record pointing at them.  ``host`` needs tok_embd, output_norm, output,
+    rope_freqs and ``layers`` (dicts with the llm_layer_weights names)."""
+
+    def __init__(self, host, device="cuda"):
+        import torch
+        self.tensors = []
+
+        def up(a):
+            if a is None:
+                return None
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                a = a.view(np.int16)
+            t = torch.from_numpy(a).to(device)
+            self.tensors.append(t)
+            return t.data_ptr()
+
+        n = len(host.layers)
+        self._layers = (llm_layer_weights * n)()
+        for l, L in enumerate(host.layers):
+            for name, _ in llm_layer_weights._fields_:
+                setattr(self._layers[l], name, up(L.get(name)))
+        self.struct = llm_weights(tok_embd=up(host.tok_embd), output_norm=up(host.output_norm),
+                                  output=up(host.output), rope_freqs=up(host.rope_freqs), layers=self._layers)
+
+    def free(self):
+        self.tensors.clear()
+
+
+class Decoder:
+    """A handle plus its uploaded weights (the weights may be freed after
+    creation: the library keeps its own copy)."""
+
+    def __init__(self, cfg, host_weights, stream=None, keep_weights: bool = False):
+        import torch
+        self.cfg = cfg
+        dw = DeviceWeights(host_weights)
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        self.stream = stream
+        self.h = llm_create(config_struct(cfg), dw.struct, stream)
+        torch.cuda.synchronize()
+        if not keep_weights:
+            dw.free()
+        self.dw = dw
+
+    def close(self):
+        if getattr(self, "h", None):
+            llm_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def kv_tensors(self, layer: int):
+        """(K, V) of one layer as int16 CUDA tensors [max_seq, kv_dim] viewing the cache."""
+        import torch
+        k, v = llm_kv_view(self.h, layer)
+        kv_dim = self.cfg.n_kv_heads * self.cfg.head_dim
+        n = self.cfg.max_seq * kv_dim
+        return (_wrap_device(k, n, torch.int16).view(self.cfg.max_seq, kv_dim),
+                _wrap_device(v, n, torch.int16).view(self.cfg.max_seq, kv_dim))
+
+    def logits_tensor(self):
+        import torch
+        return _wrap_device(llm_logits_device(self.h), self.cfg.vocab, torch.float32)
+
+
+def _wrap_device(ptr: int, n: int, dtype):
+    """A torch view of library-owned device memory (no copy, no ownership)."""
+    import torch
+    itemsize = torch.tensor([], dtype=dtype).element_size()
+
+    class _Holder:
+        __cuda_array_interface__ = {
+            "shape": (n,), "typestr": {torch.int16: "<i2", torch.float32: "<f4", torch.int32: "<i4"}[dtype],
+            "data": (ptr, False), "version": 3, "strides": (itemsize,)}
+
+    return torch.as_tensor(_Holder(), device="cuda")

@@ -1,0 +1,520 @@
+// C ABI of libllmdecode (declared in include/llm.h): handle lifetime, weight
+// repacking, argument validation and step launches.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+#include <vector>
+
+#include "llm_internal.cuh"
+
+namespace llm {
+size_t step_smem_bytes(int dim, int q_dim, int ffn, int n_heads, int n_kv, int hd);
+const void* step_kernel_ptr(int wtype);
+void launch_kv_store(cudaStream_t st, __half* kc, __half* vc, int pos, int kv_dim, const float* k, const float* v);
+void launch_dequant_rows(cudaStream_t st, int wtype, const DMat& m, int row0, int n_rows, float* out);
+}  // namespace llm
+
+using namespace llm;
+
+struct HostPinned {
+    int token_in;
+    int argmax;
+    int err;
+};
+
+struct llm_handle {
+    llm_config cfg;
+    cudaStream_t st = nullptr;
+    int device = 0, sms = 0;
+    int q_dim = 0, kv_dim = 0, max_splits = 1;
+    size_t smem = 0;
+    const void* kernel = nullptr;
+    float theta_scale = 0.f, attn_div = 0.f;
+
+    uint8_t* arena = nullptr;        // weights in the library layout
+    size_t arena_bytes = 0;
+    __half* kv = nullptr;            // [n_layers][2][max_seq][kv_dim]
+    uint8_t* act = nullptr;          // activations, counters, partials
+    std::vector<LayerDev> layers;
+    LayerDev* d_layers = nullptr;
+    DMat embd{}, out{};
+    const float* out_norm = nullptr;
+    const float* rope_freqs = nullptr;
+
+    float *x = nullptr, *qkv = nullptr, *attn = nullptr, *u = nullptr, *logits = nullptr, *attn_part = nullptr;
+    unsigned long long* best = nullptr;
+    unsigned* counters = nullptr;
+    int n_counters = 0;
+    int* err = nullptr;
+    int* tok_in = nullptr;
+    int* tok_out = nullptr;
+    HostPinned* pinned = nullptr;
+
+    int64_t launches = 0;
+    bool broken = false;             // a device error was seen; cleared by llm_reset
+    std::string last_error;
+
+    void* prefill_ws = nullptr;      // prefill workspace (lazily sized)
+    size_t prefill_ws_bytes = 0;
+};
+
+// --------------------------------------------------------------- helpers --
+static int fail(llm_handle* h, int status, const char* fmt, ...) {
+    if (h) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        h->last_error = buf;
+    }
+    return status;
+}
+
+#define CK(h, call)                                                                                   \
+    do {                                                                                              \
+        cudaError_t e_ = (call);                                                                      \
+        if (e_ != cudaSuccess) {                                                                      \
+            cudaGetLastError();                                                                       \
+            return fail((h), e_ == cudaErrorMemoryAllocation ? LLM_ERR_NO_MEMORY : LLM_ERR_CUDA,      \
+                        "%s: %s", #call, cudaGetErrorString(e_));                                     \
+        }                                                                                             \
+    } while (0)
+
+static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+static size_t mat_bytes(int wtype, long long rows, long long cols) {
+    if (wtype == LLM_Q8_0) return (size_t)(rows * cols + rows * (cols / 32) * 2);
+    return (size_t)(rows * cols * (wtype == LLM_F16 ? 2 : 4));
+}
+
+// Q8_0 blocks (34 bytes: FP16 scale, 32 int8) of `rows` rows -> quants and
+// scales of the library layout; source row r goes to destination row
+// dst0 + r*mul + phase.
+__global__ void repack_q8_kernel(const uint8_t* __restrict__ src, int rows, int cols, uint8_t* dq, __half* dd,
+                                 int dst0, int mul, int phase) {
+    const int nb = cols / 32;
+    const long long total = (long long)rows * nb;
+    for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < total;
+         b += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(b / nb), j = (int)(b % nb);
+        const uint8_t* s = src + b * 34;
+        const long long dr = (long long)dst0 + (long long)r * mul + phase;
+        dd[dr * nb + j] = __ushort_as_half((unsigned short)(s[0] | (s[1] << 8)));
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            w[k] = (uint32_t)s[2 + 4 * k] | ((uint32_t)s[3 + 4 * k] << 8) | ((uint32_t)s[4 + 4 * k] << 16) |
+                   ((uint32_t)s[5 + 4 * k] << 24);
+        uint4* d = reinterpret_cast<uint4*>(dq + dr * cols + (long long)j * 32);
+        d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
+// Copy one matrix from the caller's GGUF layout into destination rows.
+static int put_matrix(llm_handle* h, const void* src, int rows, int cols, const DMat& dst, int dst0, int mul,
+                      int phase) {
+    const int wt = h->cfg.wtype;
+    if (!src) return fail(h, LLM_ERR_INVALID_ARG, "a weight pointer is NULL");
+    if (wt == LLM_Q8_0) {
+        const long long total = (long long)rows * (cols / 32);
+        const int blocks = (int)((total + 255) / 256 < 65535 * 8 ? (total + 255) / 256 : 65535 * 8);
+        repack_q8_kernel<<<blocks, 256, 0, h->st>>>((const uint8_t*)src, rows, cols, (uint8_t*)dst.q,
+                                                    (__half*)dst.d, dst0, mul, phase);
+        h->launches++;
+        CK(h, cudaGetLastError());
+    } else {
+        const size_t rb = (size_t)cols * (wt == LLM_F16 ? 2 : 4);
+        CK(h, cudaMemcpy2DAsync((uint8_t*)dst.q + ((size_t)dst0 + phase) * rb, rb * mul, src, rb, rb, rows,
+                                cudaMemcpyDeviceToDevice, h->st));
+    }
+    return LLM_OK;
+}
+
+static DMat carve_mat(llm_handle* h, size_t& off, int rows, int cols) {
+    DMat m{};
+    m.rows = rows;
+    m.cols = cols;
+    if (h->cfg.wtype == LLM_Q8_0) {
+        m.q = h->arena + off;
+        off += align256((size_t)rows * cols);
+        m.d = reinterpret_cast<const __half*>(h->arena + off);
+        off += align256((size_t)rows * (cols / 32) * 2);
+    } else {
+        m.q = h->arena + off;
+        off += align256(mat_bytes(h->cfg.wtype, rows, cols));
+        m.d = nullptr;
+    }
+    return m;
+}
+
+static int validate(const llm_config* c, const llm_weights* w, llm_handle* h) {
+    if (!c || !w) return fail(h, LLM_ERR_INVALID_ARG, "config or weights is NULL");
+    if (c->n_layers <= 0 || c->dim <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
+        c->ffn_dim <= 0 || c->vocab <= 0 || c->max_seq <= 0)
+        return fail(h, LLM_ERR_INVALID_ARG, "every size must be positive");
+    if (c->n_heads % c->n_kv_heads) return fail(h, LLM_ERR_INVALID_ARG, "n_heads %% n_kv_heads != 0");
+    if (c->head_dim * c->n_heads != c->dim) return fail(h, LLM_ERR_INVALID_ARG, "head_dim * n_heads != dim");
+    if (c->rope_dims <= 0 || c->rope_dims % 2 || c->rope_dims > c->head_dim)
+        return fail(h, LLM_ERR_INVALID_ARG, "rope_dims must be even and in (0, head_dim]");
+    if (!(c->eps >= 0.f) || !(c->rope_base > 0.f)) return fail(h, LLM_ERR_INVALID_ARG, "bad eps or rope_base");
+    if (c->wtype != LLM_F32 && c->wtype != LLM_F16 && c->wtype != LLM_Q8_0)
+        return fail(h, LLM_ERR_UNSUPPORTED, "weight type %d not supported", c->wtype);
+    const int mult = c->wtype == LLM_Q8_0 ? 32 : (c->wtype == LLM_F16 ? 8 : 4);
+    if (c->dim % mult || c->ffn_dim % mult)
+        return fail(h, c->wtype == LLM_Q8_0 ? LLM_ERR_INVALID_ARG : LLM_ERR_UNSUPPORTED,
+                    "dim and ffn_dim must be multiples of %d for this weight type", mult);
+    if (c->head_dim % 8 || c->head_dim > 256) return fail(h, LLM_ERR_UNSUPPORTED, "head_dim must be a multiple of 8, <= 256");
+    const int gq = c->n_heads / c->n_kv_heads;
+    if (gq > kWarps || gq * c->head_dim > kMaxGroupDim)
+        return fail(h, LLM_ERR_UNSUPPORTED, "query heads per kv head too large");
+    if (!w->tok_embd || !w->output_norm || !w->layers) return fail(h, LLM_ERR_INVALID_ARG, "a weight pointer is NULL");
+    for (int l = 0; l < c->n_layers; l++) {
+        const llm_layer_weights& L = w->layers[l];
+        if (!L.attn_norm || !L.ffn_norm || !L.wq || !L.wk || !L.wv || !L.wo || !L.w_gate || !L.w_up || !L.w_down)
+            return fail(h, LLM_ERR_INVALID_ARG, "layer %d: a weight pointer is NULL", l);
+    }
+    return LLM_OK;
+}
+
+static void free_handle(llm_handle* h) {
+    if (!h) return;
+    if (h->st) cudaStreamSynchronize(h->st);
+    cudaFree(h->arena);
+    cudaFree(h->kv);
+    cudaFree(h->act);
+    cudaFree(h->d_layers);
+    cudaFree(h->prefill_ws);
+    if (h->pinned) cudaFreeHost(h->pinned);
+    cudaGetLastError();
+    delete h;
+}
+
+// ------------------------------------------------------------------ ABI --
+extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_stream_t stream, llm_handle** out) {
+    if (!out) return LLM_ERR_INVALID_ARG;
+    *out = nullptr;
+    llm_handle* h = new llm_handle();
+    int rc = validate(cfg, w, h);
+    if (rc) { delete h; return rc; }
+    const llm_config& c = *cfg;
+    h->cfg = c;
+    h->st = (cudaStream_t)stream;
+    h->q_dim = c.n_heads * c.head_dim;
+    h->kv_dim = c.n_kv_heads * c.head_dim;
+#define CKC(call)                                \
+    do {                                         \
+        cudaError_t e_ = (call);                 \
+        if (e_ != cudaSuccess) {                 \
+            cudaGetLastError();                  \
+            free_handle(h);                      \
+            return e_ == cudaErrorMemoryAllocation ? LLM_ERR_NO_MEMORY : LLM_ERR_CUDA; \
+        }                                        \
+    } while (0)
+    CKC(cudaGetDevice(&h->device));
+    CKC(cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device));
+    int coop = 0;
+    CKC(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device));
+    if (!coop) { free_handle(h); return LLM_ERR_UNSUPPORTED; }
+
+    // ---- weight arena
+    const int L = c.n_layers, d = c.dim, q = h->q_dim, kv = h->kv_dim, f = c.ffn_dim;
+    const bool has_bias = false;
+    (void)has_bias;
+    size_t bytes = 0;
+    for (int l = 0; l < L; l++) {
+        bytes += align256(mat_bytes(c.wtype, q + 2 * kv, d)) + 256 * 2;
+        bytes += align256(mat_bytes(c.wtype, d, q)) + 256 * 2;
+        bytes += align256(mat_bytes(c.wtype, 2 * f, d)) + 256 * 2;
+        bytes += align256(mat_bytes(c.wtype, d, f)) + 256 * 2;
+        bytes += 2 * align256((size_t)d * 4) + align256((size_t)(q + 2 * kv) * 4);
+    }
+    bytes += align256(mat_bytes(c.wtype, c.vocab, d)) + 512;
+    if (w->output) bytes += align256(mat_bytes(c.wtype, c.vocab, d)) + 512;
+    bytes += align256((size_t)d * 4) + align256((size_t)c.rope_dims * 2 + 4);
+    h->arena_bytes = bytes;
+    CKC(cudaMalloc(&h->arena, bytes));
+
+    size_t off = 0;
+    h->layers.resize(L);
+    for (int l = 0; l < L; l++) {
+        const llm_layer_weights& W = w->layers[l];
+        LayerDev& D = h->layers[l];
+        D.qkv = carve_mat(h, off, q + 2 * kv, d);
+        D.o = carve_mat(h, off, d, q);
+        D.gu = carve_mat(h, off, 2 * f, d);
+        D.down = carve_mat(h, off, d, f);
+        float* an = (float*)(h->arena + off); off += align256((size_t)d * 4);
+        float* fn = (float*)(h->arena + off); off += align256((size_t)d * 4);
+        float* bias = (float*)(h->arena + off); off += align256((size_t)(q + 2 * kv) * 4);
+        D.attn_norm = an;
+        D.ffn_norm = fn;
+        D.qkv_bias = (W.bq || W.bk || W.bv) ? bias : nullptr;
+        if ((rc = put_matrix(h, W.wq, q, d, D.qkv, 0, 1, 0)) ||
+            (rc = put_matrix(h, W.wk, kv, d, D.qkv, q, 1, 0)) ||
+            (rc = put_matrix(h, W.wv, kv, d, D.qkv, q + kv, 1, 0)) ||
+            (rc = put_matrix(h, W.wo, d, q, D.o, 0, 1, 0)) ||
+            (rc = put_matrix(h, W.w_gate, f, d, D.gu, 0, 2, 0)) ||
+            (rc = put_matrix(h, W.w_up, f, d, D.gu, 0, 2, 1)) ||
+            (rc = put_matrix(h, W.w_down, d, f, D.down, 0, 1, 0))) {
+            free_handle(h);
+            return rc;
+        }
+        CKC(cudaMemcpyAsync(an, W.attn_norm, (size_t)d * 4, cudaMemcpyDeviceToDevice, h->st));
+        CKC(cudaMemcpyAsync(fn, W.ffn_norm, (size_t)d * 4, cudaMemcpyDeviceToDevice, h->st));
+        if (D.qkv_bias) {
+            CKC(cudaMemsetAsync(bias, 0, (size_t)(q + 2 * kv) * 4, h->st));
+            if (W.bq) CKC(cudaMemcpyAsync(bias, W.bq, (size_t)q * 4, cudaMemcpyDeviceToDevice, h->st));
+            if (W.bk) CKC(cudaMemcpyAsync(bias + q, W.bk, (size_t)kv * 4, cudaMemcpyDeviceToDevice, h->st));
+            if (W.bv) CKC(cudaMemcpyAsync(bias + q + kv, W.bv, (size_t)kv * 4, cudaMemcpyDeviceToDevice, h->st));
+        }
+    }
+    h->embd = carve_mat(h, off, c.vocab, d);
+    if ((rc = put_matrix(h, w->tok_embd, c.vocab, d, h->embd, 0, 1, 0))) { free_handle(h); return rc; }
+    if (w->output) {
+        h->out = carve_mat(h, off, c.vocab, d);
+        if ((rc = put_matrix(h, w->output, c.vocab, d, h->out, 0, 1, 0))) { free_handle(h); return rc; }
+    } else {
+        h->out = h->embd;                                      // tied embeddings
+    }
+    float* onorm = (float*)(h->arena + off); off += align256((size_t)d * 4);
+    CKC(cudaMemcpyAsync(onorm, w->output_norm, (size_t)d * 4, cudaMemcpyDeviceToDevice, h->st));
+    h->out_norm = onorm;
+    if (w->rope_freqs) {
+        float* fr = (float*)(h->arena + off); off += align256((size_t)c.rope_dims * 2 + 4);
+        CKC(cudaMemcpyAsync(fr, w->rope_freqs, (size_t)(c.rope_dims / 2) * 4, cudaMemcpyDeviceToDevice, h->st));
+        h->rope_freqs = fr;
+    }
+
+    // ---- KV cache
+    const size_t kv_bytes = (size_t)L * 2 * c.max_seq * kv * sizeof(__half);
+    CKC(cudaMalloc(&h->kv, kv_bytes));
+    CKC(cudaMemsetAsync(h->kv, 0, kv_bytes, h->st));
+    for (int l = 0; l < L; l++) {
+        h->layers[l].kc = h->kv + (size_t)(2 * l) * c.max_seq * kv;
+        h->layers[l].vc = h->layers[l].kc + (size_t)c.max_seq * kv;
+    }
+    CKC(cudaMalloc(&h->d_layers, sizeof(LayerDev) * L));
+    CKC(cudaMemcpyAsync(h->d_layers, h->layers.data(), sizeof(LayerDev) * L, cudaMemcpyHostToDevice, h->st));
+
+    // ---- activations
+    h->max_splits = h->sms / c.n_kv_heads > 1 ? h->sms / c.n_kv_heads : 1;
+    h->n_counters = n_phase_counters(L) + L * c.n_kv_heads;
+    size_t a = 0;
+    auto take = [&](size_t b) { size_t o = a; a += align256(b); return o; };
+    const size_t o_x = take((size_t)d * 4), o_qkv = take((size_t)(q + 2 * kv) * 4), o_attn = take((size_t)q * 4),
+                 o_u = take((size_t)f * 4), o_logits = take((size_t)c.vocab * 4),
+                 o_part = take((size_t)c.n_heads * h->max_splits * (c.head_dim + 2) * 4), o_best = take(8),
+                 o_ctr = take((size_t)h->n_counters * 4), o_err = take(4), o_tin = take(4), o_tout = take(4);
+    CKC(cudaMalloc(&h->act, a));
+    CKC(cudaMemsetAsync(h->act, 0, a, h->st));
+    h->x = (float*)(h->act + o_x);
+    h->qkv = (float*)(h->act + o_qkv);
+    h->attn = (float*)(h->act + o_attn);
+    h->u = (float*)(h->act + o_u);
+    h->logits = (float*)(h->act + o_logits);
+    h->attn_part = (float*)(h->act + o_part);
+    h->best = (unsigned long long*)(h->act + o_best);
+    h->counters = (unsigned*)(h->act + o_ctr);
+    h->err = (int*)(h->act + o_err);
+    h->tok_in = (int*)(h->act + o_tin);
+    h->tok_out = (int*)(h->act + o_tout);
+    CKC(cudaMallocHost(&h->pinned, sizeof(HostPinned)));
+
+    h->theta_scale = (float)pow((double)c.rope_base, -2.0 / (double)c.rope_dims);
+    h->attn_div = (float)sqrt((double)c.head_dim);
+    h->kernel = step_kernel_ptr(c.wtype);
+    h->smem = step_smem_bytes(d, q, f, c.n_heads, c.n_kv_heads, c.head_dim);
+    CKC(cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem));
+    int per_sm = 0;
+    CKC(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->kernel, kThreads, h->smem));
+    if (per_sm < 1) { free_handle(h); return LLM_ERR_UNSUPPORTED; }
+    CKC(cudaStreamSynchronize(h->st));
+    *out = h;
+    return LLM_OK;
+#undef CKC
+}
+
+static int launch_step(llm_handle* h, const int* token_dev, int pos, int* argmax_dev) {
+    const llm_config& c = h->cfg;
+    StepParams p{};
+    p.layers = h->d_layers;
+    p.embd = h->embd;
+    p.out = h->out;
+    p.out_norm = h->out_norm;
+    p.rope_freqs = h->rope_freqs;
+    p.wtype = c.wtype;
+    p.n_layers = c.n_layers; p.dim = c.dim; p.n_heads = c.n_heads; p.n_kv = c.n_kv_heads; p.hd = c.head_dim;
+    p.ffn = c.ffn_dim; p.vocab = c.vocab; p.max_seq = c.max_seq; p.rope_dims = c.rope_dims; p.neox = c.rope_neox;
+    p.q_dim = h->q_dim; p.kv_dim = h->kv_dim;
+    p.eps = c.eps; p.theta_scale = h->theta_scale; p.attn_div = h->attn_div;
+    p.x = h->x; p.qkv = h->qkv; p.attn = h->attn; p.u = h->u; p.logits = h->logits; p.attn_part = h->attn_part;
+    p.max_splits = h->max_splits; p.best = h->best; p.counters = h->counters; p.err = h->err;
+    p.token_in = token_dev; p.token_out = argmax_dev; p.pos = pos;
+    int s = (pos + 1 + 15) / 16;
+    p.splits = s < 1 ? 1 : (s > h->max_splits ? h->max_splits : s);
+    void* args[] = {&p};
+    CK(h, cudaLaunchCooperativeKernel(h->kernel, dim3(h->sms), dim3(kThreads), args, h->smem, h->st));
+    h->launches++;
+    return LLM_OK;
+}
+
+static int read_device_error(llm_handle* h) {
+    CK(h, cudaMemcpyAsync(&h->pinned->err, h->err, 4, cudaMemcpyDeviceToHost, h->st));
+    CK(h, cudaStreamSynchronize(h->st));
+    const int e = h->pinned->err;
+    if (e & kErrTimeout) { h->broken = true; return fail(h, LLM_ERR_DEVICE_TIMEOUT, "a bounded device wait expired"); }
+    if (e & kErrToken) { h->broken = true; return fail(h, LLM_ERR_OUT_OF_RANGE, "a device-side token was out of range"); }
+    return LLM_OK;
+}
+
+extern "C" int llm_reset(llm_handle* h) {
+    if (!h) return LLM_ERR_INVALID_ARG;
+    CK(h, cudaStreamSynchronize(h->st));
+    CK(h, cudaMemsetAsync(h->err, 0, 4, h->st));
+    CK(h, cudaMemsetAsync(h->counters, 0, (size_t)h->n_counters * 4, h->st));
+    CK(h, cudaMemsetAsync(h->best, 0, 8, h->st));
+    CK(h, cudaStreamSynchronize(h->st));
+    h->broken = false;
+    return LLM_OK;
+}
+
+extern "C" int llm_decode_step(llm_handle* h, int32_t token, int32_t pos, float* logits_host, int32_t* argmax_host) {
+    if (!h) return LLM_ERR_INVALID_ARG;
+    if (h->broken) return fail(h, LLM_ERR_STATE, "handle has a device error; call llm_reset");
+    if (token < 0 || token >= h->cfg.vocab) return fail(h, LLM_ERR_OUT_OF_RANGE, "token %d not in [0, %d)", token, h->cfg.vocab);
+    if (pos < 0 || pos >= h->cfg.max_seq) return fail(h, LLM_ERR_OUT_OF_RANGE, "pos %d not in [0, %d)", pos, h->cfg.max_seq);
+    h->pinned->token_in = token;
+    CK(h, cudaMemcpyAsync(h->tok_in, &h->pinned->token_in, 4, cudaMemcpyHostToDevice, h->st));
+    int rc = launch_step(h, h->tok_in, pos, h->tok_out);
+    if (rc) return rc;
+    CK(h, cudaMemcpyAsync(&h->pinned->argmax, h->tok_out, 4, cudaMemcpyDeviceToHost, h->st));
+    if (logits_host)
+        CK(h, cudaMemcpyAsync(logits_host, h->logits, (size_t)h->cfg.vocab * 4, cudaMemcpyDeviceToHost, h->st));
+    if ((rc = read_device_error(h))) return rc;
+    if (argmax_host) *argmax_host = h->pinned->argmax;
+    return LLM_OK;
+}
+
+extern "C" int llm_decode_step_async(llm_handle* h, const int32_t* token_dev, int32_t pos, int32_t* argmax_dev) {
+    if (!h || !token_dev || !argmax_dev) return fail(h, LLM_ERR_INVALID_ARG, "NULL argument");
+    if (h->broken) return fail(h, LLM_ERR_STATE, "handle has a device error; call llm_reset");
+    if (pos < 0 || pos >= h->cfg.max_seq) return fail(h, LLM_ERR_OUT_OF_RANGE, "pos %d not in [0, %d)", pos, h->cfg.max_seq);
+    return launch_step(h, token_dev, pos, argmax_dev);
+}
+
+extern "C" int llm_generate(llm_handle* h, int32_t token, int32_t pos, int32_t n_steps, int32_t* tokens_dev) {
+    if (!h || !tokens_dev || n_steps < 0) return fail(h, LLM_ERR_INVALID_ARG, "bad argument");
+    if (h->broken) return fail(h, LLM_ERR_STATE, "handle has a device error; call llm_reset");
+    if (token < 0 || token >= h->cfg.vocab) return fail(h, LLM_ERR_OUT_OF_RANGE, "token %d not in [0, %d)", token, h->cfg.vocab);
+    if (pos < 0 || (long long)pos + n_steps > h->cfg.max_seq)
+        return fail(h, LLM_ERR_OUT_OF_RANGE, "positions %d..%d exceed max_seq %d", pos, pos + n_steps - 1, h->cfg.max_seq);
+    if (n_steps == 0) return LLM_OK;
+    h->pinned->token_in = token;
+    CK(h, cudaMemcpyAsync(h->tok_in, &h->pinned->token_in, 4, cudaMemcpyHostToDevice, h->st));
+    for (int i = 0; i < n_steps; i++) {
+        int rc = launch_step(h, i == 0 ? h->tok_in : tokens_dev + i - 1, pos + i, tokens_dev + i);
+        if (rc) return rc;
+    }
+    return LLM_OK;
+}
+
+extern "C" int llm_prefill(llm_handle* h, const int32_t* tokens_host, int32_t n, int32_t pos0, float* logits_host,
+                           int32_t* argmax_host) {
+    if (!h || !tokens_host || n <= 0) return fail(h, LLM_ERR_INVALID_ARG, "bad argument");
+    if (h->broken) return fail(h, LLM_ERR_STATE, "handle has a device error; call llm_reset");
+    if (pos0 < 0 || (long long)pos0 + n > h->cfg.max_seq)
+        return fail(h, LLM_ERR_OUT_OF_RANGE, "positions %d..%d exceed max_seq %d", pos0, pos0 + n - 1, h->cfg.max_seq);
+    for (int i = 0; i < n; i++)
+        if (tokens_host[i] < 0 || tokens_host[i] >= h->cfg.vocab)
+            return fail(h, LLM_ERR_OUT_OF_RANGE, "token %d not in [0, %d)", tokens_host[i], h->cfg.vocab);
+    int rc;
+    for (int i = 0; i < n - 1; i++) {
+        h->pinned->token_in = tokens_host[i];
+        CK(h, cudaMemcpyAsync(h->tok_in, &h->pinned->token_in, 4, cudaMemcpyHostToDevice, h->st));
+        if ((rc = launch_step(h, h->tok_in, pos0 + i, h->tok_out))) return rc;
+        CK(h, cudaStreamSynchronize(h->st));    // the pinned token slot is reused
+    }
+    return llm_decode_step(h, tokens_host[n - 1], pos0 + n - 1, logits_host, argmax_host);
+}
+
+extern "C" int llm_sync(llm_handle* h) {
+    if (!h) return LLM_ERR_INVALID_ARG;
+    CK(h, cudaStreamSynchronize(h->st));
+    return read_device_error(h);
+}
+
+extern "C" const float* llm_logits_device(const llm_handle* h) { return h ? h->logits : nullptr; }
+
+extern "C" int llm_kv_view(llm_handle* h, int layer, uint16_t** k_dev, uint16_t** v_dev) {
+    if (!h || !k_dev || !v_dev) return LLM_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers) return fail(h, LLM_ERR_OUT_OF_RANGE, "layer %d", layer);
+    *k_dev = reinterpret_cast<uint16_t*>(h->layers[layer].kc);
+    *v_dev = reinterpret_cast<uint16_t*>(h->layers[layer].vc);
+    return LLM_OK;
+}
+
+extern "C" int llm_test_kv_store(llm_handle* h, int layer, int32_t pos, const float* k_dev, const float* v_dev) {
+    if (!h || !k_dev || !v_dev) return LLM_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= h->cfg.n_layers || pos < 0 || pos >= h->cfg.max_seq)
+        return fail(h, LLM_ERR_OUT_OF_RANGE, "layer %d / pos %d", layer, pos);
+    launch_kv_store(h->st, h->layers[layer].kc, h->layers[layer].vc, pos, h->kv_dim, k_dev, v_dev);
+    h->launches++;
+    CK(h, cudaGetLastError());
+    CK(h, cudaStreamSynchronize(h->st));
+    return LLM_OK;
+}
+
+extern "C" int llm_test_dequant_rows(llm_handle* h, int which, int layer, int32_t row0, int32_t n_rows, float* out_dev) {
+    if (!h || !out_dev || n_rows < 0) return LLM_ERR_INVALID_ARG;
+    if (which < 7 && (layer < 0 || layer >= h->cfg.n_layers)) return fail(h, LLM_ERR_OUT_OF_RANGE, "layer %d", layer);
+    const llm_config& c = h->cfg;
+    DMat m{};
+    int first = 0, mul = 1, phase = 0, rows = 0;
+    const int nb_bytes = 1;
+    (void)nb_bytes;
+    switch (which) {
+        case 0: m = h->layers[layer].qkv; first = 0; rows = h->q_dim; break;
+        case 1: m = h->layers[layer].qkv; first = h->q_dim; rows = h->kv_dim; break;
+        case 2: m = h->layers[layer].qkv; first = h->q_dim + h->kv_dim; rows = h->kv_dim; break;
+        case 3: m = h->layers[layer].o; rows = c.dim; break;
+        case 4: m = h->layers[layer].gu; mul = 2; phase = 0; rows = c.ffn_dim; break;
+        case 5: m = h->layers[layer].gu; mul = 2; phase = 1; rows = c.ffn_dim; break;
+        case 6: m = h->layers[layer].down; rows = c.dim; break;
+        case 7: m = h->embd; rows = c.vocab; break;
+        case 8: m = h->out; rows = c.vocab; break;
+        default: return fail(h, LLM_ERR_INVALID_ARG, "which = %d", which);
+    }
+    if (row0 < 0 || (long long)row0 + n_rows > rows) return fail(h, LLM_ERR_OUT_OF_RANGE, "rows %d..%d", row0, row0 + n_rows);
+    for (int r = 0; r < n_rows; r++) {
+        launch_dequant_rows(h->st, c.wtype, m, first + (row0 + r) * mul + phase, 1, out_dev + (size_t)r * m.cols);
+        h->launches++;
+    }
+    CK(h, cudaGetLastError());
+    CK(h, cudaStreamSynchronize(h->st));
+    return LLM_OK;
+}
+
+extern "C" int64_t llm_launch_count(const llm_handle* h) { return h ? h->launches : 0; }
+
+extern "C" void llm_destroy(llm_handle* h) { free_handle(h); }
+
+extern "C" const char* llm_status_string(int s) {
+    switch (s) {
+        case LLM_OK: return "ok";
+        case LLM_ERR_INVALID_ARG: return "invalid argument";
+        case LLM_ERR_UNSUPPORTED: return "unsupported configuration";
+        case LLM_ERR_OUT_OF_RANGE: return "token or position out of range";
+        case LLM_ERR_CUDA: return "CUDA error";
+        case LLM_ERR_NO_MEMORY: return "device allocation failed";
+        case LLM_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case LLM_ERR_STATE: return "invalid handle state";
+        default: return "unknown status";
+    }
+}
+
+extern "C" const char* llm_last_error(const llm_handle* h) { return h ? h->last_error.c_str() : ""; }
