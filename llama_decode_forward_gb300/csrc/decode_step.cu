@@ -1,247 +1,377 @@
-// The batch-1 decode step as one persistent kernel.
+// The batch-1 decode step as one persistent, warp-specialised kernel.
 //
-// One CTA per SM (cooperative launch, so all CTAs are resident).  The step is
-// a chain of phases; every phase reads the whole activation vector produced by
-// the previous one, so phases are separated by grid-wide counters:
+// One CTA per SM (cooperative launch, so all CTAs are resident).  Warps 0-14
+// compute ("consumers"); warp 15 ("producer") streams everything the CTA will
+// read from HBM (its rows of every weight matrix and its KV-cache tiles) in a
+// fixed order through a ring of 32 KB shared-memory slots, with cp.async.bulk
+// (weights) and 2-D TMA tiles (K/V), completing on mbarriers.  The producer
+// never waits on other CTAs: nothing it loads depends on this step's results
+// (KV row `pos`, which does, is patched in by the consumers), so HBM keeps
+// streaming while the consumers wait at the grid-wide phase counters.
 //
 //   per layer l:  QKV   rows of [Wq;Wk;Wv] . RMSNorm(x)        -> qkv (+ bias)
 //                 ATTN  (kv head, position split) units: RoPE(q), RoPE(k),
 //                       K/V row `pos` stored as F16, partial softmax;
 //                       the last split of a kv head merges the partials -> attn
 //                 O     rows of Wo . attn                       -> x += ...
-//                 GU    rows of [Wgate|Wup] . RMSNorm(x)        -> u = silu(g) * up
+//                 GU    rows of [Wgate|Wup] . RMSNorm(x)        -> u = silu(gate) * up
 //                 DOWN  rows of Wdown . u                       -> x += ...
 //   LOGITS  rows of Wout . RMSNorm(x) -> logits, argmax (first index of the max)
 //
-// Steps follow "The Forward Pass in Java", Example 13 (Llama.forward); the
+// Steps follow "The Forward Pass in Java", Example 13 (Llama.forward).  The
 // attention split and merge is the flash-decoding rearrangement of the same
 // softmax (max-subtracted partial sums combined with exp(m_s - M) weights).
-// Every wait is bounded: on expiry the CTA records kErrTimeout and returns.
+//
+// A matrix row is reduced by a "team" of lanes, each holding 32 elements of
+// the activation vector in registers (loaded straight from L2 at the start of
+// the phase, normalised in registers); rows up to 1024 elements are part of a
+// warp, longer rows whole warps that meet at their own named barrier and take
+// two rows per pass.  Each CTA keeps the residual-stream rows it owns in
+// shared memory, so no phase reads back what it wrote.
+//
+// Every wait is bounded; on expiry the error word is set, the producer drains
+// its copies in flight, and the CTA exits.
 #include "llm_internal.cuh"
 
 namespace llm {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+// Spin until ready() holds.  The deadline (SM cycle counter) and the error
+// word (a global load) are checked only every 256 polls, so a wait that ends
+// reacts within a few hundred cycles.  Returns false on expiry (after setting
+// the error word) or when another CTA has already reported a timeout.
+constexpr long long kWaitLimitCycles = 4000000000ll;   // about 2 s at 2 GHz
 
-// ------------------------------------------------------------ grid sync --
-__device__ __forceinline__ bool wait_counter(const StepParams& p, const unsigned* c, unsigned target,
-                                             volatile int* s_flag) {
-    if (threadIdx.x == 0) {
-        int ok = 1;
-        if (ld_acquire(c) < target) {
-            const uint64_t t0 = global_timer_ns();
-            while (ld_acquire(c) < target) {
-                __nanosleep(32);
-                if (*(volatile int*)p.err & kErrTimeout) { ok = 0; break; }
-                if (global_timer_ns() - t0 > kWaitLimitNs) { atomicOr(p.err, kErrTimeout); ok = 0; break; }
+template <class Ready>
+__device__ __forceinline__ bool bounded_wait(Ready ready, int* err) {
+    if (ready()) return true;
+    const long long t0 = clock64();
+    for (unsigned i = 1;; i++) {
+        if (ready()) return true;
+        if ((i & 255u) == 0) {
+            if (*(volatile int*)err & kErrTimeout) return false;
+            if (clock64() - t0 > kWaitLimitCycles) {
+                atomicOr(err, kErrTimeout);
+                return false;
             }
         }
-        *s_flag = ok;
-    }
-    __syncthreads();
-    return *s_flag != 0;
-}
-
-__device__ __forceinline__ void signal_counter(unsigned* c) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(c, 1u);
     }
 }
 
-// ------------------------------------------------------- block reductions --
-__device__ double block_sum_double(double v, double* red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        double s = 0.0;
-        for (int w = 0; w < kWarps; w++) s += red[w];
-        red[kWarps] = s;
+// Shared-memory regions, addressed from the dynamic smem base with the
+// offsets in the (constant-bank) parameters, so no region pointer stays live.
+struct Smem {
+    unsigned char* base;
+    const StepParams& p;
+    __device__ Smem(unsigned char* b, const StepParams& p_) : base(b), p(p_) {}
+    __device__ __forceinline__ uint8_t* ring() const { return base; }
+    // attention scratch and the merge gather buffer (scratch_floats floats)
+    __device__ __forceinline__ float* xs() const { return reinterpret_cast<float*>(base + p.off_xs); }
+    // [kMaxTeams][2][kConsumerWarps][2] partial dots of multi-warp teams
+    __device__ __forceinline__ float* tpart() const { return reinterpret_cast<float*>(base + p.off_red); }
+    __device__ __forceinline__ float* rope_c() const { return reinterpret_cast<float*>(base + p.off_rope); }
+    __device__ __forceinline__ float* rope_s() const { return rope_c() + 128; }
+    // [2 * kConsumers] attention split combine
+    __device__ __forceinline__ float* comb() const { return reinterpret_cast<float*>(base + p.off_comb); }
+    // [kOwnFloats] residual rows this CTA owns, then [kOwnFloats] its QKV bias rows
+    __device__ __forceinline__ float* xown() const { return reinterpret_cast<float*>(base + p.off_own); }
+    __device__ __forceinline__ float* bias() const { return xown() + kOwnFloats; }
+    __device__ __forceinline__ uint64_t* full() const { return reinterpret_cast<uint64_t*>(base + p.off_bar); }
+    __device__ __forceinline__ uint64_t* empty() const { return full() + p.ns; }
+    __device__ __forceinline__ int* misc() const { return reinterpret_cast<int*>(base + p.off_misc); }   // [0] abort, [1] flag
+    __device__ __forceinline__ float* fred() const { return reinterpret_cast<float*>(base + p.off_misc + 64); }
+    __device__ __forceinline__ unsigned long long* best() const {
+        return reinterpret_cast<unsigned long long*>(base + p.off_misc + 64 + 8 * (kConsumerWarps + 2));
     }
-    __syncthreads();
-    double r = red[kWarps];
-    __syncthreads();
-    return r;
+};
+
+// ------------------------------------------------------------ schedule --
+// Both roles walk the same sequence of chunks; these helpers define it.
+__device__ __forceinline__ void cta_rows(int rows, int& r0, int& r1) {
+    const long long b = blockIdx.x, G = gridDim.x;
+    r0 = (int)(rows * b / G);
+    r1 = (int)(rows * (b + 1) / G);
 }
 
-// xs <- RMSNorm(src) * g ("The Forward Pass in Java", Example 4): the sum of
-// squares in double, scale = (float)(1/sqrt(ss/n + eps)), y = (x*scale)*g.
-__device__ void load_normed(float* xs, const float* src, const float* g, int n, float eps, double* red) {
-    double ss = 0.0;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-        const float v = __ldcg(src + i);
-        xs[i] = v;
-        ss += (double)v * (double)v;
-    }
-    const double tot = block_sum_double(ss, red);
-    const float scale = (float)(1.0 / sqrt(tot / (double)n + (double)eps));
-    for (int i = threadIdx.x; i < n; i += kThreads) xs[i] = __fmul_rn(__fmul_rn(xs[i], scale), __ldg(g + i));
-    __syncthreads();
+__device__ __forceinline__ void unit_range(const StepParams& p, int unit, int S, int& g, int& s, int& t0, int& t1) {
+    g = unit / S;
+    s = unit % S;
+    const int n_pos = p.pos + 1, chunk = (n_pos + S - 1) / S;
+    t0 = min(n_pos, s * chunk);
+    t1 = min(n_pos, t0 + chunk);
 }
 
-__device__ void load_plain(float* xs, const float* src, int n) {
-    for (int i = threadIdx.x; i < n; i += kThreads) xs[i] = __ldcg(src + i);
-    __syncthreads();
+__device__ __forceinline__ int row_qbytes(const DMat& m, int wtype) {
+    return wtype == LLM_Q8_0 ? m.cols : m.cols * (wtype == LLM_F16 ? 2 : 4);
 }
+
+// Position in the ring: slot index and the parity of its current use.
+struct RingPos {
+    int slot = 0;
+    uint32_t phase = 0;      // flips each time the slot index wraps
+    int count = 0;           // chunks passed (saturates at ns: "ring filled once")
+    __device__ __forceinline__ void advance(int ns) {
+        if (++slot == ns) { slot = 0; phase ^= 1u; }
+        if (count < ns) count++;
+    }
+};
+
+// ------------------------------------------------------------ producer --
+struct Producer {
+    const StepParams& p;
+    Smem& sm;
+    RingPos rp;
+    long long it = 0;
+    bool dead = false;
+
+    __device__ Producer(const StepParams& p_, Smem& s_) : p(p_), sm(s_) {}
+
+    // Next free slot, or nullptr after an error.  A slot's first fill needs no
+    // wait; later fills wait for the consumers' release of the previous use.
+    __device__ uint8_t* acquire(int& slot) {
+        slot = rp.slot;
+        if (rp.count >= p.ns) {
+            const uint32_t par = rp.phase ^ 1u;
+            uint64_t* bar = &sm.empty()[slot];
+            if (!bounded_wait([&] { return mbar_try_wait(bar, par); }, p.err)) {
+                dead = true;
+                return nullptr;
+            }
+        }
+        return sm.ring() + (size_t)slot * kSlotBytes;
+    }
+
+    __device__ __forceinline__ void issued() {
+        rp.advance(p.ns);
+        it++;
+    }
+
+    __device__ void gemv(const DMat& m, int wtype) {
+        if (dead) return;
+        int r0, r1;                                   // rows, or super-rows when m.pair
+        cta_rows(m.rows, r0, r1);
+        const int per = m.pair ? 2 : 1;
+        const size_t rowq = (size_t)row_qbytes(m, wtype);
+        const int rowd = wtype == LLM_Q8_0 ? 2 * m.dstride : 0;
+        for (int r = r0; r < r1; r += m.rpc) {
+            const int n = min(m.rpc, r1 - r) * per;  // matrix rows in this chunk
+            int slot;
+            uint8_t* dst = acquire(slot);
+            if (!dst) return;
+            const uint32_t bq = (uint32_t)(n * rowq), bd = (uint32_t)(n * rowd);
+            mbar_arrive_expect_tx(&sm.full()[slot], bq + bd);
+            bulk_g2s(dst, m.q + (size_t)r * per * rowq, bq, &sm.full()[slot]);
+            if (bd)
+                bulk_g2s(dst + bq, reinterpret_cast<const uint8_t*>(m.d) + (size_t)r * per * rowd, bd,
+                         &sm.full()[slot]);
+            issued();
+        }
+    }
+
+    __device__ void attention(int layer) {
+        if (dead) return;
+        const int S = p.splits, units = p.n_kv * S, P = p.attn_rows;
+        const char* maps = reinterpret_cast<const char*>(p.kv_maps);
+        const void* kmap = maps + (size_t)(2 * layer) * 128;
+        const void* vmap = maps + (size_t)(2 * layer + 1) * 128;
+        const uint32_t half_bytes = (uint32_t)(P * p.hd * 2);
+        for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+            int g, s, t0, t1;
+            unit_range(p, unit, S, g, s, t0, t1);
+            for (int c0 = t0; c0 < t1; c0 += P) {
+                int slot;
+                uint8_t* dst = acquire(slot);
+                if (!dst) return;
+                mbar_arrive_expect_tx(&sm.full()[slot], 2 * half_bytes);
+                tma_2d_g2s(dst, kmap, g * p.hd, c0, &sm.full()[slot]);
+                tma_2d_g2s(dst + half_bytes, vmap, g * p.hd, c0, &sm.full()[slot]);
+                issued();
+            }
+        }
+    }
+
+    __device__ void drain() {
+        // the last min(it, ns) copies: slots rp.slot-1, rp.slot-2, ... backwards
+        const int n = it < p.ns ? (int)it : p.ns;
+        int slot = rp.slot;
+        uint32_t phase = rp.phase;
+        for (int k = 0; k < n; k++) {
+            if (slot == 0) { slot = p.ns; phase ^= 1u; }
+            slot--;
+            uint64_t* bar = &sm.full()[slot];
+            const long long t0 = clock64();
+            while (!mbar_try_wait(bar, phase))
+                if (clock64() - t0 > kWaitLimitCycles) break;
+        }
+    }
+};
+
+// ------------------------------------------------------------ consumers --
+struct Consumer {
+    const StepParams& p;
+    Smem& sm;
+    RingPos rp;            // next slot to consume
+    int tid, warp, lane;
+    int own0, own1;        // residual rows this CTA owns (rows of Wo and Wdown)
+
+    __device__ Consumer(const StepParams& p_, Smem& s_) : p(p_), sm(s_) {
+        tid = threadIdx.x;
+        warp = tid >> 5;
+        lane = tid & 31;
+        cta_rows(p.dim, own0, own1);
+    }
+
+    __device__ bool aborted() const { return *(volatile int*)&sm.misc()[0] != 0; }
+
+    // Wait for the next slot.  A timeout is recorded in the abort flag; the
+    // caller checks it only at a point all consumer threads reach together.
+    __device__ uint8_t* next_slot(int& slot) {
+        slot = rp.slot;
+        const uint32_t par = rp.phase;
+        uint64_t* bar = &sm.full()[slot];
+        if (!bounded_wait([&] { return mbar_try_wait(bar, par); }, p.err)) sm.misc()[0] = 1;
+        return sm.ring() + (size_t)slot * kSlotBytes;
+    }
+
+    __device__ void release(int slot) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty()[slot]);
+        rp.advance(p.ns);
+    }
+
+    // Grid-wide dependency: thread 0 waits for counter >= target.
+    __device__ bool wait_counter(const unsigned* c, unsigned target) {
+        if (tid == 0 && !bounded_wait([&] { return ld_acquire(c) >= target; }, p.err)) sm.misc()[0] = 1;
+        consumer_sync();
+        return !aborted();
+    }
+
+    __device__ void signal(unsigned* c) {
+        consumer_sync();
+        if (tid == 0) {
+            __threadfence();
+            red_release_add(c, 1u);
+        }
+    }
+
+    // Sum of one value per warp (warps may pass 0), identical in every thread.
+    __device__ float warps_total(float v) {
+        v = warp_sum(v);
+        if (lane == 0) sm.fred()[warp] = v;
+        consumer_sync();
+        float s = 0.f;
+        for (int w = 0; w < kConsumerWarps; w++) s += sm.fred()[w];
+        return s;
+    }
+};
 
 // --------------------------------------------------------- weight decode --
 // Element i of row r, decoded exactly as the format defines it: Q8_0
-// d * qs (an exact float product), F16 widened, F32 as stored.
+// d * qs (an exact float product; quants stored as qs + 128), F16 widened,
+// F32 as stored.
 template <int DT>
 __device__ __forceinline__ float weight_at(const DMat& m, int r, int i) {
-    if (DT == LLM_Q8_0) {
-        const float d = __half2float(m.d[(size_t)r * (m.cols / 32) + i / 32]);
-        return __fmul_rn(d, (float)(int8_t)m.q[(size_t)r * m.cols + i]);
-    } else if (DT == LLM_F16) {
+    if constexpr (DT == LLM_Q8_0) {
+        const float d = __half2float(m.d[(size_t)r * m.dstride + i / 32]);
+        return __fmul_rn(d, (float)((int)m.q[(size_t)r * m.cols + i] - 128));
+    } else if constexpr (DT == LLM_F16) {
         return __half2float(reinterpret_cast<const __half*>(m.q)[(size_t)r * m.cols + i]);
     } else {
         return reinterpret_cast<const float*>(m.q)[(size_t)r * m.cols + i];
     }
 }
 
-// ------------------------------------------------------------------ GEMV --
-// Elements per 16-byte segment.
-template <int DT> struct Seg { static constexpr int n = DT == LLM_Q8_0 ? 16 : (DT == LLM_F16 ? 8 : 4); };
-
-// Dot of one 16-byte weight segment with the matching x values (from smem).
+// ------------------------------------------------------------ lane dots --
+// A lane's 32 elements of one row (in the slot) against its x registers.
+// Q8_0: one 32-element block; each biased quant byte is placed in the low
+// mantissa of 2^23 and 2^23 + 128 is subtracted, which yields the exact
+// integer qs as a float, then the block's FP16 scale multiplies the sum.
 template <int DT>
-__device__ __forceinline__ float seg_dot(const uint4 w, const float* xs) {
-    if (DT == LLM_Q8_0) {
-        const float4* xp = reinterpret_cast<const float4*>(xs);
-        const uint32_t ws[4] = {w.x ^ 0x80808080u, w.y ^ 0x80808080u, w.z ^ 0x80808080u, w.w ^ 0x80808080u};
-        float s0 = 0.f, s1 = 0.f;
+struct LaneDot;
+
+template <>
+struct LaneDot<LLM_Q8_0> {
+    static constexpr int kSeg = 2;           // 16-byte words per lane and row
+    __device__ __forceinline__ static void acc(const uint4* w, const float2 (&x2)[16], float2& c0, float2& c1) {
+        const float2 off = make_float2(-8388736.0f, -8388736.0f);
+        const uint32_t u[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
 #pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const float4 xv = xp[k];
-            s0 = fmaf(i8_to_f32(ws[k], 0), xv.x, s0);
-            s1 = fmaf(i8_to_f32(ws[k], 1), xv.y, s1);
-            s0 = fmaf(i8_to_f32(ws[k], 2), xv.z, s0);
-            s1 = fmaf(i8_to_f32(ws[k], 3), xv.w, s1);
+        for (int k = 0; k < 8; k++) {
+            float2 lo = make_float2(__uint_as_float(__byte_perm(u[k], 0x4B000000u, 0x7540u)),
+                                    __uint_as_float(__byte_perm(u[k], 0x4B000000u, 0x7541u)));
+            float2 hi = make_float2(__uint_as_float(__byte_perm(u[k], 0x4B000000u, 0x7542u)),
+                                    __uint_as_float(__byte_perm(u[k], 0x4B000000u, 0x7543u)));
+            c0 = __ffma2_rn(__fadd2_rn(lo, off), x2[2 * k], c0);
+            c1 = __ffma2_rn(__fadd2_rn(hi, off), x2[2 * k + 1], c1);
         }
-        return s0 + s1;
-    } else if (DT == LLM_F16) {
-        const float4* xp = reinterpret_cast<const float4*>(xs);
-        const float4 xa = xp[0], xb = xp[1];
-        const __half2* h = reinterpret_cast<const __half2*>(&w);
-        const float2 a = __half22float2(h[0]), b = __half22float2(h[1]), c = __half22float2(h[2]),
-                     d = __half22float2(h[3]);
-        float s0 = a.x * xa.x, s1 = a.y * xa.y;
-        s0 = fmaf(b.x, xa.z, s0); s1 = fmaf(b.y, xa.w, s1);
-        s0 = fmaf(c.x, xb.x, s0); s1 = fmaf(c.y, xb.y, s1);
-        s0 = fmaf(d.x, xb.z, s0); s1 = fmaf(d.y, xb.w, s1);
-        return s0 + s1;
-    } else {
-        const float4 xv = *reinterpret_cast<const float4*>(xs);
-        float s0 = __uint_as_float(w.x) * xv.x, s1 = __uint_as_float(w.y) * xv.y;
-        s0 = fmaf(__uint_as_float(w.z), xv.z, s0);
-        s1 = fmaf(__uint_as_float(w.w), xv.w, s1);
-        return s0 + s1;
     }
+};
+
+template <>
+struct LaneDot<LLM_F16> {
+    static constexpr int kSeg = 4;
+    __device__ __forceinline__ static float2 h2f(uint32_t v) {
+        return __half22float2(__halves2half2(__ushort_as_half((unsigned short)(v & 0xffffu)),
+                                             __ushort_as_half((unsigned short)(v >> 16))));
+    }
+    __device__ __forceinline__ static void acc(const uint4* w, const float2 (&x2)[16], float2& c0, float2& c1) {
+#pragma unroll
+        for (int s = 0; s < 4; s++) {
+            c0 = __ffma2_rn(h2f(w[s].x), x2[4 * s], c0);
+            c1 = __ffma2_rn(h2f(w[s].y), x2[4 * s + 1], c1);
+            c0 = __ffma2_rn(h2f(w[s].z), x2[4 * s + 2], c0);
+            c1 = __ffma2_rn(h2f(w[s].w), x2[4 * s + 3], c1);
+        }
+    }
+};
+
+template <>
+struct LaneDot<LLM_F32> {
+    static constexpr int kSeg = 8;
+    __device__ __forceinline__ static void acc(const uint4* w, const float2 (&x2)[16], float2& c0, float2& c1) {
+#pragma unroll
+        for (int s = 0; s < 8; s++) {
+            c0 = __ffma2_rn(make_float2(__uint_as_float(w[s].x), __uint_as_float(w[s].y)), x2[2 * s], c0);
+            c1 = __ffma2_rn(make_float2(__uint_as_float(w[s].z), __uint_as_float(w[s].w)), x2[2 * s + 1], c1);
+        }
+    }
+};
+
+// One row: words of the lane (nseg of them valid, the rest read as zero).
+template <int DT>
+__device__ __forceinline__ float lane_row(const uint8_t* w, const uint8_t* scale, const float2 (&x2)[16], int nseg) {
+    constexpr int NS = LaneDot<DT>::kSeg;
+    uint4 v[NS];
+#pragma unroll
+    for (int s = 0; s < NS; s++) v[s] = s < nseg ? reinterpret_cast<const uint4*>(w)[s] : make_uint4(0u, 0u, 0u, 0u);
+    float2 c0 = make_float2(0.f, 0.f), c1 = c0;
+    LaneDot<DT>::acc(v, x2, c0, c1);
+    const float t = (c0.x + c0.y) + (c1.x + c1.y);
+    if constexpr (DT == LLM_Q8_0) return nseg ? __half2float(*reinterpret_cast<const __half*>(scale)) * t : 0.f;
+    return t;
 }
 
-// Lane-partial dots of NR consecutive rows starting at r0 (lane strides over
-// 16-byte segments; loads issued four segments ahead per row).
-template <int DT, int NR>
-__device__ __forceinline__ void rows_dot(const DMat& m, int r0, const float* xs, float acc[NR]) {
-    constexpr int E = Seg<DT>::n;
-    constexpr int ES = DT == LLM_Q8_0 ? 1 : (DT == LLM_F16 ? 2 : 4);   // bytes per element
-    const int lane = threadIdx.x & 31;
-    const int nseg = m.cols / E;
-    const size_t row_bytes = (size_t)m.cols * ES;
-    const uint8_t* rowp[NR];
-    const __half* drow[NR];
-#pragma unroll
-    for (int r = 0; r < NR; r++) {
-        acc[r] = 0.f;
-        rowp[r] = m.q + (size_t)(r0 + r) * row_bytes;
-        drow[r] = DT == LLM_Q8_0 ? m.d + (size_t)(r0 + r) * (m.cols / 32) : nullptr;
-    }
-    int seg = lane;
-    for (; seg + 96 < nseg; seg += 128) {
-        uint4 w[NR][4];
-        unsigned short dd[NR][4];
-#pragma unroll
-        for (int r = 0; r < NR; r++)
-#pragma unroll
-            for (int u = 0; u < 4; u++) {
-                w[r][u] = ld_stream(rowp[r] + (size_t)(seg + 32 * u) * 16);
-                if (DT == LLM_Q8_0) dd[r][u] = ld_stream_u16(drow[r] + (seg + 32 * u) / 2);
-            }
-#pragma unroll
-        for (int u = 0; u < 4; u++) {
-            const float* xp = xs + (seg + 32 * u) * E;
-#pragma unroll
-            for (int r = 0; r < NR; r++) {
-                const float s = seg_dot<DT>(w[r][u], xp);
-                if (DT == LLM_Q8_0) acc[r] = fmaf(__half2float(__ushort_as_half(dd[r][u])), s, acc[r]);
-                else acc[r] += s;
-            }
-        }
-    }
-    for (; seg < nseg; seg += 32) {
-        uint4 w[NR];
-        unsigned short dd[NR];
-#pragma unroll
-        for (int r = 0; r < NR; r++) {
-            w[r] = ld_stream(rowp[r] + (size_t)seg * 16);
-            if (DT == LLM_Q8_0) dd[r] = ld_stream_u16(drow[r] + seg / 2);
-        }
-#pragma unroll
-        for (int r = 0; r < NR; r++) {
-            const float s = seg_dot<DT>(w[r], xs + seg * E);
-            if (DT == LLM_Q8_0) acc[r] = fmaf(__half2float(__ushort_as_half(dd[r])), s, acc[r]);
-            else acc[r] += s;
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < NR; r++) acc[r] = warp_sum(acc[r]);
-}
-
-// Rows of m split evenly over every warp of the grid; epi.row(r, v) is called
-// by lane 0 with the full dot of row r.  pair=true: rows come in (2i, 2i+1)
-// pairs and epi.pair(i, v0, v1) is called instead.
-template <int DT, bool PAIR, class Epi>
-__device__ __forceinline__ void gemv_phase(const DMat& m, const float* xs, Epi& epi) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long gw = (long long)blockIdx.x * kWarps + warp, GW = (long long)gridDim.x * kWarps;
-    const int units = PAIR ? m.rows / 2 : m.rows;
-    const int u0 = (int)(units * gw / GW), u1 = (int)(units * (gw + 1) / GW);
-    if constexpr (PAIR) {
-        for (int u = u0; u < u1; u++) {
-            float a[2];
-            rows_dot<DT, 2>(m, 2 * u, xs, a);
-            if (lane == 0) epi.pair(u, a[0], a[1]);
-        }
-    } else {
-        int r = u0;
-        for (; r + 1 < u1; r += 2) {
-            float a[2];
-            rows_dot<DT, 2>(m, r, xs, a);
-            if (lane == 0) { epi.row(r, a[0]); epi.row(r + 1, a[1]); }
-        }
-        if (r < u1) {
-            float a[1];
-            rows_dot<DT, 1>(m, r, xs, a);
-            if (lane == 0) epi.row(r, a[0]);
-        }
-    }
-}
-
-struct EpiStore {                 // out[r] = v (+ bias[r])
+// ------------------------------------------------------------------ GEMV --
+struct EpiStore {                 // out[r] = v (+ bias of this CTA's row r)
     float* out;
-    const float* bias;
-    __device__ void row(int r, float v) { __stcg(out + r, bias ? v + __ldg(bias + r) : v); }
+    const float* bias;            // smem, indexed from the CTA's first row, or nullptr
+    int r0;
+    __device__ void row(int r, float v) { __stcg(out + r, bias ? v + bias[r - r0] : v); }
+    __device__ void pair(int, float, float) {}
 };
-struct EpiResidual {              // x[r] += v
+struct EpiResidual {              // x[r] += v, the owned row kept in smem
     float* x;
-    __device__ void row(int r, float v) { __stcg(x + r, __ldcg(x + r) + v); }
+    float* own;
+    int own0;
+    __device__ void row(int r, float v) {
+        const float y = own[r - own0] + v;
+        own[r - own0] = y;
+        __stcg(x + r, y);
+    }
+    __device__ void pair(int, float, float) {}
 };
-struct EpiSwiGLU {                // u[i] = silu(gate) * up ("The Forward Pass in Java", Example 8)
+struct EpiSwiGLU {                // u[i] = silu(gate_i) * up_i ("The Forward Pass in Java", Example 8)
     float* u;
+    __device__ void row(int, float) {}
     __device__ void pair(int i, float g, float up) {
         const float e = expf(-g);
         __stcg(u + i, __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), up));
@@ -255,289 +385,594 @@ struct EpiLogits {                // logits[r] = v, keep this lane's best (value
         const unsigned long long k = argmax_key(v, r);
         best = k > best ? k : best;
     }
+    __device__ void pair(int, float, float) {}
 };
+
+// Where a GEMV phase takes its activation vector: a global vector (written
+// by this step) or the embedding row of `token`, optionally RMSNormed with
+// gains g ("The Forward Pass in Java", Example 4: y = (x * scale) * g with
+// scale = 1/sqrt(mean(x^2) + eps), the sum of squares a float tree sum).
+struct XSrc {
+    const float* x;               // nullptr: the embedding row
+    const float* g;               // nullptr: no norm
+    int n;                        // length of the vector
+};
+
+// Lane layout of a plan: team, lane index within the team, row half (pair).
+struct Lanes {
+    int team, lit, hsel, clit, col0, nseg;
+    bool active;
+};
+
+template <int DT, bool PAIR>
+__device__ __forceinline__ Lanes lane_layout(const Consumer& c, const DMat& m) {
+    constexpr int ES = DT == LLM_Q8_0 ? 1 : (DT == LLM_F16 ? 2 : 4);
+    Lanes L;
+    const int tw = m.tw;
+    if (tw <= 32) {
+        L.team = c.warp * (32 / tw) + c.lane / tw;
+        L.lit = c.lane % tw;
+    } else {
+        const int wpr = tw / 32;
+        L.team = c.warp / wpr;
+        L.lit = (c.warp % wpr) * 32 + c.lane;
+    }
+    const int half = PAIR ? tw / 2 : tw;
+    L.hsel = PAIR ? L.lit / half : 0;
+    L.clit = L.lit - L.hsel * half;
+    L.active = L.team < m.teams;
+    L.col0 = L.clit * kLaneElems;
+    L.nseg = L.active && L.col0 < m.cols ? min(kLaneElems, m.cols - L.col0) * ES / 16 : 0;
+    return L;
+}
+
+// x2 <- the lane's 32 activation values (zero past the vector's end), normed
+// when src.g is set.  Every consumer thread must call this (it synchronises).
+template <int DT, bool PAIR>
+__device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& L, const XSrc& src, int token,
+                                       float2 (&x2)[16]) {
+    const int col0 = L.col0;
+    const bool have = L.active && col0 < src.n;
+    if (src.x) {
+        const float4* s4 = reinterpret_cast<const float4*>(src.x + col0);
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const float4 v = have && col0 + 4 * k < src.n ? __ldcg(s4 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+            x2[2 * k] = make_float2(v.x, v.y);
+            x2[2 * k + 1] = make_float2(v.z, v.w);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 16; k++) {
+            const int e = col0 + 2 * k;
+            x2[k] = have && e < src.n ? make_float2(weight_at<DT>(c.p.embd, token, e), weight_at<DT>(c.p.embd, token, e + 1))
+                                      : make_float2(0.f, 0.f);
+        }
+    }
+    if (src.g) {
+        // each column counted once: the lanes of team 0 (first half for pairs)
+        float ss = 0.f;
+        if (L.team == 0 && L.hsel == 0 && have) {
+#pragma unroll
+            for (int k = 0; k < 16; k++) ss += x2[k].x * x2[k].x + x2[k].y * x2[k].y;
+        }
+        const float tot = c.warps_total(ss);
+        const float scale = 1.0f / sqrtf(tot / (float)src.n + c.p.eps);
+        const float4* g4 = reinterpret_cast<const float4*>(src.g + col0);
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const float4 g = have && col0 + 4 * k < src.n ? __ldg(g4 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+            x2[2 * k] = make_float2(__fmul_rn(__fmul_rn(x2[2 * k].x, scale), g.x),
+                                    __fmul_rn(__fmul_rn(x2[2 * k].y, scale), g.y));
+            x2[2 * k + 1] = make_float2(__fmul_rn(__fmul_rn(x2[2 * k + 1].x, scale), g.z),
+                                        __fmul_rn(__fmul_rn(x2[2 * k + 1].y, scale), g.w));
+        }
+    }
+}
+
+// The CTA's rows of m, chunk by chunk from the ring (the plan in DMat).
+// Multi-warp teams take two rows per pass: their partial dots are reduced with
+// one butterfly (lanes 0-15 for the first row, 16-31 for the second), then the
+// team meets at its named barrier and lane 0 of the team adds the warps' parts.
+template <int DT, bool PAIR, class Epi>
+__device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const XSrc& src, int token, Epi& epi) {
+    constexpr int ES = DT == LLM_Q8_0 ? 1 : (DT == LLM_F16 ? 2 : 4);
+    const Lanes L = lane_layout<DT, PAIR>(c, m);
+    float2 x2[16];
+    lane_x<DT, PAIR>(c, m, L, src, token, x2);
+    const int tw = m.tw, teams = m.teams;
+    int r0, r1;
+    cta_rows(m.rows, r0, r1);
+    const int per = PAIR ? 2 : 1;
+    const int rowq = row_qbytes(m, DT);
+    const int rowd = DT == LLM_Q8_0 ? 2 * m.dstride : 0;
+    const int xoff = L.col0 * ES, soff = L.clit * 2;
+    int pass = 0;
+    for (int r = r0; r < r1; r += m.rpc) {
+        const int n = min(m.rpc, r1 - r);           // rows (super-rows) in this chunk
+        int slot;
+        const uint8_t* buf = c.next_slot(slot);
+        const uint8_t* sbase = buf + (size_t)n * per * rowq;
+        if (tw <= 32) {
+            // part-of-a-warp teams: one row per pass, segmented butterfly
+            const int half = PAIR ? tw / 2 : tw;
+            const int wteam = c.warp * (32 / tw);
+            for (int j = 0; wteam + j * teams < n; j++) {
+                const int rr = L.team + j * teams;
+                const bool real = L.active && rr < n;
+                const int mrow = (real ? rr : 0) * per + L.hsel;
+                float v = real ? lane_row<DT>(buf + (size_t)mrow * rowq + xoff, sbase + mrow * rowd + soff, x2, L.nseg)
+                               : 0.f;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    if (o < half) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if constexpr (PAIR) {
+                    const float up = __shfl_down_sync(0xffffffffu, v, half);
+                    if (real && L.lit == 0) epi.pair(r + rr, v, up);
+                } else {
+                    if (real && L.lit == 0) epi.row(r + rr, v);
+                }
+            }
+        } else if (L.active) {
+            // whole-warp teams: two rows per pass
+            const int wpr = tw / 32;
+            for (int j = 0; L.team + 2 * j * teams < n; j++) {
+                const int ra = L.team + 2 * j * teams, rb = ra + teams;
+                const bool hasb = rb < n;
+                const int ma = ra * per + L.hsel, mb = (hasb ? rb : ra) * per + L.hsel;
+                float va = lane_row<DT>(buf + (size_t)ma * rowq + xoff, sbase + ma * rowd + soff, x2, L.nseg);
+                float vb = lane_row<DT>(buf + (size_t)mb * rowq + xoff, sbase + mb * rowd + soff, x2, L.nseg);
+                float keep = c.lane < 16 ? va : vb;
+                const float send = c.lane < 16 ? vb : va;
+                keep += __shfl_xor_sync(0xffffffffu, send, 16);
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+                float* tp = c.sm.tpart() + ((L.team * 2 + (pass & 1)) * kConsumerWarps) * 2;
+                if ((c.lane & 15) == 0) tp[(c.warp % wpr) * 2 + (c.lane >> 4)] = keep;
+                asm volatile("bar.sync %0, %1;" ::"r"(3 + L.team), "r"(tw) : "memory");
+                if (L.lit == 0) {
+                    if constexpr (PAIR) {
+                        float ga = 0.f, ua = 0.f, gb = 0.f, ub = 0.f;
+                        for (int k = 0; k < wpr / 2; k++) { ga += tp[2 * k]; gb += tp[2 * k + 1]; }
+                        for (int k = wpr / 2; k < wpr; k++) { ua += tp[2 * k]; ub += tp[2 * k + 1]; }
+                        epi.pair(r + ra, ga, ua);
+                        if (hasb) epi.pair(r + rb, gb, ub);
+                    } else {
+                        float ta = 0.f, tb = 0.f;
+                        for (int k = 0; k < wpr; k++) { ta += tp[2 * k]; tb += tp[2 * k + 1]; }
+                        epi.row(r + ra, ta);
+                        if (hasb) epi.row(r + rb, tb);
+                    }
+                }
+                pass++;
+            }
+        }
+        c.release(slot);
+    }
+}
 
 // ------------------------------------------------------------------ RoPE --
 // "The Forward Pass in Java", Example 6 and "What a Llama model computes, and
 // why" §2.4: pair i turns by theta_i, where theta starts at pos and is
 // multiplied by theta_scale once per pair in float (the same chain as ggml's
-// rope cache), then divided by the pair's frequency factor.
-__device__ __forceinline__ void rope_pair(float* v, int head_dim, int rope_dims, int neox, int i, int pos,
-                                          float theta_scale, const float* freqs) {
-    float th = (float)pos;
-    for (int j = 0; j < i; j++) th = __fmul_rn(th, theta_scale);
-    if (freqs) th = __fdiv_rn(th, __ldg(freqs + i));
-    const float c = (float)cos((double)th), s = (float)sin((double)th);
-    const int a = neox ? i : 2 * i, b = neox ? i + rope_dims / 2 : 2 * i + 1;
+// rope cache), then divided by the pair's frequency factor.  cos/sin are taken
+// in double and rounded to float.  One table per step, shared by q and k.
+__device__ void rope_table(const StepParams& p, Smem& sm, int tid) {
+    for (int i = tid; i < p.rope_dims / 2; i += kConsumers) {
+        float th = (float)p.pos;
+        for (int j = 0; j < i; j++) th = __fmul_rn(th, p.theta_scale);
+        if (p.rope_freqs) th = __fdiv_rn(th, __ldg(p.rope_freqs + i));
+        double s, c;
+        sincos((double)th, &s, &c);
+        sm.rope_c()[i] = (float)c;
+        sm.rope_s()[i] = (float)s;
+    }
+}
+
+__device__ __forceinline__ void rope_apply(const StepParams& p, const Smem& sm, float* v, int i) {
+    const float c = sm.rope_c()[i], s = sm.rope_s()[i];
+    const int a = p.neox ? i : 2 * i, b = p.neox ? i + p.rope_dims / 2 : 2 * i + 1;
     const float x0 = v[a], x1 = v[b];
     v[a] = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
     v[b] = __fadd_rn(__fmul_rn(x0, s), __fmul_rn(x1, c));
-    (void)head_dim;
 }
 
 // K/V row `pos` of one kv head, rounded to F16 to nearest even ("The Forward
 // Pass in Java", Example 10), at element pos*kv_dim + off + i (Example 7).
-__device__ __forceinline__ void store_kv(__half* kc, __half* vc, int pos, int kv_dim, int off, int i, float k,
-                                         float v) {
+__device__ __forceinline__ void store_kv(__half* kc, __half* vc, int pos, int kv_dim, int off, int i, __half k,
+                                         __half v) {
     const size_t e = (size_t)pos * kv_dim + off + i;
-    kc[e] = __float2half_rn(k);
-    vc[e] = __float2half_rn(v);
+    kc[e] = k;
+    vc[e] = v;
 }
 
 // ------------------------------------------------------------- attention --
-struct AttnSmem {
-    float* q;      // [gq][hd] rotated queries of the group
-    float* kpos;   // [hd] rotated k of this position (writer split only)
-    float* sc;     // [gq][kAttnChunk] scores, then exp weights
-    float* mlc;    // [3][gq]: running max, running sum, correction
-    __half* ks;    // [kAttnChunk][hd]
-    __half* vs;    // [kAttnChunk][hd]
-};
+__device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int unit) {
+    const StepParams& p = c.p;
+    Smem& sm = c.sm;
+    const int tid = c.tid, warp = c.warp, lane = c.lane;
+    const int hd = p.hd, gq = p.n_heads / p.n_kv, P = p.attn_rows, S = p.splits;
+    int g, s, t0, t1;
+    unit_range(p, unit, S, g, s, t0, t1);
+    const int h0 = g * gq, GD = gq * hd;
+    // scratch
+    float* q_s = sm.xs();                                          // [gq][hd]
+    float* kf = q_s + GD;                                          // [hd] f32 k of this position
+    float* sc = kf + hd;                                           // [gq][P]
+    float* mlc = sc + gq * P;                                      // [3][gq]
+    __half* kp = reinterpret_cast<__half*>(mlc + 3 * gq);          // [hd]
+    __half* vp = kp + hd;                                          // [hd]
 
-__device__ void attention_unit(const StepParams& p, const LayerDev& L, int layer, int g, int s, int S,
-                               const AttnSmem& sm, volatile int* s_flag) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int hd = p.hd, gq = p.n_heads / p.n_kv, h0 = g * gq, n_pos = p.pos + 1;
-    const int chunk = (n_pos + S - 1) / S;
-    const int t0 = min(n_pos, s * chunk), t1 = min(n_pos, t0 + chunk);
-
-    // queries of the group, rotated
-    for (int i = tid; i < gq * hd; i += kThreads) sm.q[i] = __ldcg(p.qkv + h0 * hd + i);
-    __syncthreads();
-    for (int i = tid; i < gq * (p.rope_dims / 2); i += kThreads) {
-        const int h = i / (p.rope_dims / 2), pr = i % (p.rope_dims / 2);
-        rope_pair(sm.q + h * hd, hd, p.rope_dims, p.neox, pr, p.pos, p.theta_scale, p.rope_freqs);
-    }
-    // the split holding `pos` rotates this token's k and stores K/V row pos
     const bool writer = t0 <= p.pos && p.pos < t1;
-    if (writer) {
-        for (int i = tid; i < hd; i += kThreads) sm.kpos[i] = __ldcg(p.qkv + p.q_dim + g * hd + i);
-        __syncthreads();
-        for (int i = tid; i < p.rope_dims / 2; i += kThreads)
-            rope_pair(sm.kpos, hd, p.rope_dims, p.neox, i, p.pos, p.theta_scale, p.rope_freqs);
-        __syncthreads();
-        for (int i = tid; i < hd; i += kThreads)
-            store_kv(L.kc, L.vc, p.pos, p.kv_dim, g * hd, i, sm.kpos[i],
-                     __ldcg(p.qkv + p.q_dim + p.kv_dim + g * hd + i));
-        __threadfence_block();
-    }
-    if (tid < gq) { sm.mlc[tid] = -INFINITY; sm.mlc[gq + tid] = 0.f; }
-    __syncthreads();
-
-    // online softmax over [t0, t1) in chunks staged in shared memory
-    constexpr int kAcc = kMaxGroupDim / kThreads;
-    float acc[kAcc];
+    {
+        float qv[2], kv = 0.f, vv = 0.f;
 #pragma unroll
-    for (int a = 0; a < kAcc; a++) acc[a] = 0.f;
-    const int per_row = hd / 8;
-    for (int c0 = t0; c0 < t1; c0 += kAttnChunk) {
-        const int np = min(kAttnChunk, t1 - c0);
-        for (int idx = tid; idx < np * per_row; idx += kThreads) {
-            const int row = idx / per_row, w = idx % per_row;
-            const size_t e = (size_t)(c0 + row) * p.kv_dim + g * hd + w * 8;
-            reinterpret_cast<uint4*>(sm.ks)[row * per_row + w] = __ldcg(reinterpret_cast<const uint4*>(L.kc + e));
-            reinterpret_cast<uint4*>(sm.vs)[row * per_row + w] = __ldcg(reinterpret_cast<const uint4*>(L.vc + e));
+        for (int k = 0; k < 2; k++) {
+            const int i = tid + k * kConsumers;
+            qv[k] = i < GD ? __ldcg(p.qkv + h0 * hd + i) : 0.f;
         }
-        __syncthreads();
-        for (int idx = tid; idx < gq * np; idx += kThreads) {
+        if (writer && tid < hd) {
+            kv = __ldcg(p.qkv + p.q_dim + g * hd + tid);
+            vv = __ldcg(p.qkv + p.q_dim + p.kv_dim + g * hd + tid);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+            const int i = tid + k * kConsumers;
+            if (i < GD) q_s[i] = qv[k];
+        }
+        if (writer && tid < hd) {
+            kf[tid] = kv;
+            vp[tid] = __float2half_rn(vv);
+        }
+    }
+    consumer_sync();
+    for (int i = tid; i < gq * (p.rope_dims / 2); i += kConsumers)
+        rope_apply(p, sm, q_s + (i / (p.rope_dims / 2)) * hd, i % (p.rope_dims / 2));
+    if (writer)
+        for (int i = tid; i < p.rope_dims / 2; i += kConsumers) rope_apply(p, sm, kf, i);
+    if (tid < gq) { mlc[tid] = -INFINITY; mlc[gq + tid] = 0.f; }
+    consumer_sync();
+    if (writer && tid < hd) {
+        const __half kh = __float2half_rn(kf[tid]);
+        kp[tid] = kh;
+        store_kv(L.kc, L.vc, p.pos, p.kv_dim, g * hd, tid, kh, vp[tid]);
+    }
+    // PV work split: thread t accumulates the output pair o2 = t % (GD/2)
+    // (elements 2*o2, 2*o2+1) over positions with index % NSPLIT == t / (GD/2).
+    const int GD2 = GD / 2;
+    const int NSPLIT = kConsumers / GD2;
+    const int o2 = tid % GD2, sp = tid / GD2;
+    const bool pv_active = sp < NSPLIT;
+    const int oh = (2 * o2) / hd, oi = (2 * o2) % hd;
+    float2 acc = make_float2(0.f, 0.f);
+
+    for (int c0 = t0; c0 < t1; c0 += P) {
+        const int np = min(P, t1 - c0);
+        int slot;
+        uint8_t* buf = c.next_slot(slot);
+        __half* ks = reinterpret_cast<__half*>(buf);
+        __half* vs = ks + (size_t)P * hd;
+        consumer_sync();                                            // kp/vp ready; every thread saw the slot land
+        if (writer && p.pos >= c0 && p.pos < c0 + np && tid < hd) { // this step's row, not the stale copy
+            ks[(p.pos - c0) * hd + tid] = kp[tid];
+            vs[(p.pos - c0) * hd + tid] = vp[tid];
+        }
+        consumer_sync();
+        if (c.aborted()) return false;
+        // scores: thread (h, position); the start column rotates with the lane
+        // so that a warp's reads fall in different banks
+        for (int idx = tid; idx < gq * np; idx += kConsumers) {
             const int h = idx / np, pp = idx % np;
-            const float* qh = sm.q + h * hd;
-            const __half2* kr = reinterpret_cast<const __half2*>(sm.ks + pp * hd);
-            float s0 = 0.f, s1 = 0.f;
-            for (int i = 0; i < hd / 2; i++) {
-                const float2 kv = __half22float2(kr[i]);
-                s0 = fmaf(qh[2 * i], kv.x, s0);
-                s1 = fmaf(qh[2 * i + 1], kv.y, s1);
+            const float2* q2 = reinterpret_cast<const float2*>(q_s + h * hd);
+            const __half2* k2 = reinterpret_cast<const __half2*>(ks + (size_t)pp * hd);
+            const int nh2 = hd / 2;
+            float2 a = make_float2(0.f, 0.f);
+            int j = lane % nh2;
+            for (int k = 0; k < nh2; k++) {
+                a = __ffma2_rn(__half22float2(k2[j]), q2[j], a);
+                j = j + 1 == nh2 ? 0 : j + 1;
             }
-            sm.sc[h * kAttnChunk + pp] = __fdiv_rn(s0 + s1, p.attn_div);
+            sc[h * P + pp] = __fdiv_rn(a.x + a.y, p.attn_div);
         }
-        __syncthreads();
+        consumer_sync();
         if (warp < gq) {
             const int h = warp;
             float mloc = -INFINITY;
-            for (int pp = lane; pp < np; pp += 32) mloc = fmaxf(mloc, sm.sc[h * kAttnChunk + pp]);
+            for (int pp = lane; pp < np; pp += 32) mloc = fmaxf(mloc, sc[h * P + pp]);
             mloc = warp_max(mloc);
-            const float mold = sm.mlc[h], mnew = fmaxf(mold, mloc);
+            const float mold = mlc[h], mnew = fmaxf(mold, mloc);
             float sum = 0.f;
             for (int pp = lane; pp < np; pp += 32) {
-                const float e = expf(sm.sc[h * kAttnChunk + pp] - mnew);
-                sm.sc[h * kAttnChunk + pp] = e;
+                const float e = expf(sc[h * P + pp] - mnew);
+                sc[h * P + pp] = e;
                 sum += e;
             }
             sum = warp_sum(sum);
             if (lane == 0) {
                 const float corr = expf(mold - mnew);     // 0 on the first chunk (mold = -inf)
-                sm.mlc[h] = mnew;
-                sm.mlc[gq + h] = sm.mlc[gq + h] * corr + sum;
-                sm.mlc[2 * gq + h] = corr;
+                mlc[h] = mnew;
+                mlc[gq + h] = mlc[gq + h] * corr + sum;
+                mlc[2 * gq + h] = corr;
             }
         }
-        __syncthreads();
-#pragma unroll
-        for (int a = 0; a < kAcc; a++) {
-            const int o = tid + a * kThreads;
-            if (o < gq * hd) {
-                const int h = o / hd, i = o % hd;
-                float v = acc[a] * sm.mlc[2 * gq + h];
-                const float* e = sm.sc + h * kAttnChunk;
-                for (int pp = 0; pp < np; pp++) v = fmaf(e[pp], __half2float(sm.vs[pp * hd + i]), v);
-                acc[a] = v;
+        consumer_sync();
+        if (pv_active) {
+            const float corr = mlc[2 * gq + oh];
+            float2 v = make_float2(acc.x * corr, acc.y * corr);
+            const float* e = sc + oh * P;
+            for (int pp = sp; pp < np; pp += NSPLIT) {
+                const float2 vv = __half22float2(*reinterpret_cast<const __half2*>(vs + (size_t)pp * hd + oi));
+                v = __ffma2_rn(make_float2(e[pp], e[pp]), vv, v);
             }
+            acc = v;
         }
-        __syncthreads();
+        c.release(slot);
     }
-    // partial of this split: (m, l, acc) per head
+    // combine the position splits, write this split's (m, l, acc)
+    if (pv_active) {
+        sm.comb()[sp * GD + 2 * o2] = acc.x;
+        sm.comb()[sp * GD + 2 * o2 + 1] = acc.y;
+    }
+    consumer_sync();
     const int stride = hd + 2;
-#pragma unroll
-    for (int a = 0; a < kAcc; a++) {
-        const int o = tid + a * kThreads;
-        if (o < gq * hd) {
-            const int h = o / hd, i = o % hd;
-            float* part = p.attn_part + ((size_t)(h0 + h) * p.max_splits + s) * stride;
-            __stcg(part + 2 + i, acc[a]);
-            if (i == 0) { __stcg(part, sm.mlc[h]); __stcg(part + 1, sm.mlc[gq + h]); }
-        }
+    for (int oo = tid; oo < GD; oo += kConsumers) {
+        float v = 0.f;
+        for (int k = 0; k < NSPLIT; k++) v += sm.comb()[k * GD + oo];
+        const int hh = oo / hd, ii = oo % hd;
+        float* part = p.attn_part + ((size_t)(h0 + hh) * p.max_splits + s) * stride;
+        __stcg(part + 2 + ii, v);
+        if (ii == 0) { __stcg(part, mlc[hh]); __stcg(part + 1, mlc[gq + hh]); }
     }
     // the last split to finish merges: M = max m_s, L = sum e^(m_s-M) l_s,
     // out = sum e^(m_s-M) acc_s / L
     unsigned* mc = p.counters + n_phase_counters(p.n_layers) + layer * p.n_kv + g;
-    __syncthreads();
+    consumer_sync();
     if (tid == 0) {
         __threadfence();
         const unsigned old = atomicAdd(mc, 1u);
-        *s_flag = (old == (unsigned)(S - 1));
+        sm.misc()[1] = (old == (unsigned)(S - 1));
     }
-    __syncthreads();
-    if (*s_flag) {
+    consumer_sync();
+    if (sm.misc()[1]) {
         __threadfence();
-        for (int o = tid; o < gq * hd; o += kThreads) {
-            const int h = o / hd, i = o % hd;
-            const float* base = p.attn_part + (size_t)(h0 + h) * p.max_splits * stride;
-            float M = -INFINITY;
-            for (int ss = 0; ss < S; ss++) M = fmaxf(M, __ldcg(base + ss * stride));
-            float Lsum = 0.f, v = 0.f;
-            for (int ss = 0; ss < S; ss++) {
-                const float ms = __ldcg(base + ss * stride);
-                const float w = ms == -INFINITY ? 0.f : expf(ms - M);
-                Lsum = fmaf(w, __ldcg(base + ss * stride + 1), Lsum);
-                v = fmaf(w, __ldcg(base + ss * stride + 2 + i), v);
+        float* gat = sm.xs();                                      // [S][stride] of one head
+        const int total = S * stride;
+        for (int h = 0; h < gq; h++) {
+            const float* src = p.attn_part + (size_t)(h0 + h) * p.max_splits * stride;
+            for (int base = tid; base < total; base += 4 * kConsumers) {
+                float v[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+                    if (base + k * kConsumers < total) v[k] = __ldcg(src + base + k * kConsumers);
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+                    if (base + k * kConsumers < total) gat[base + k * kConsumers] = v[k];
             }
-            __stcg(p.attn + (h0 + h) * hd + i, v / Lsum);
+            consumer_sync();
+            for (int i = tid; i < hd; i += kConsumers) {
+                float M = -INFINITY;
+                for (int ss = 0; ss < S; ss++) M = fmaxf(M, gat[ss * stride]);
+                float Lsum = 0.f, v = 0.f;
+                for (int ss = 0; ss < S; ss++) {
+                    const float ms = gat[ss * stride];
+                    const float w = ms == -INFINITY ? 0.f : expf(ms - M);
+                    Lsum = fmaf(w, gat[ss * stride + 1], Lsum);
+                    v = fmaf(w, gat[ss * stride + 2 + i], v);
+                }
+                __stcg(p.attn + (h0 + h) * hd + i, v / Lsum);
+            }
+            consumer_sync();
         }
-        signal_counter(p.counters + 5 * layer + 1);
+        c.signal(p.counters + 5 * layer + 1);
     }
-    __syncthreads();
+    consumer_sync();
+    return true;
 }
 
 // ----------------------------------------------------------------- kernel --
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const StepParams p) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    __shared__ double red[kWarps + 1];
-    __shared__ int s_flag;
-    __shared__ unsigned long long s_best[kWarps];
-    float* xs = reinterpret_cast<float*>(smem_raw);
-    const int G = gridDim.x, tid = threadIdx.x;
-    volatile int* flag = &s_flag;
-
+__device__ bool consumer_main(const StepParams& p, Smem& sm) {
+    Consumer c(p, sm);
+    const int tid = c.tid, G = gridDim.x;
     int token = __ldcg(p.token_in);
     if (token < 0 || token >= p.vocab) {
         if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, kErrToken);
         token = 0;
     }
-
-    // attention scratch aliases the x buffer (phases never overlap)
-    const int gq = p.n_heads / p.n_kv;
-    AttnSmem am;
-    am.q = xs;
-    am.kpos = am.q + gq * p.hd;
-    am.sc = am.kpos + p.hd;
-    am.mlc = am.sc + gq * kAttnChunk;
-    am.ks = reinterpret_cast<__half*>(am.mlc + ((3 * gq + 3) / 4) * 4);
-    am.vs = am.ks + kAttnChunk * p.hd;
-
+    rope_table(p, sm, tid);
+    // this CTA's residual rows start as the embedding row's values
+    for (int i = c.own0 + tid; i < c.own1; i += kConsumers) {
+        const float v = weight_at<DT>(p.embd, token, i);
+        sm.xown()[i - c.own0] = v;
+        __stcg(p.x + i, v);
+    }
     for (int l = 0; l < p.n_layers; l++) {
         const LayerDev& L = p.layers[l];
         unsigned* ctr = p.counters + 5 * l;
         // ---- QKV
-        if (l == 0) {
-            double ss = 0.0;
-            for (int i = tid; i < p.dim; i += kThreads) {
-                const float v = weight_at<DT>(p.embd, token, i);
-                xs[i] = v;
-                ss += (double)v * (double)v;
-                if (blockIdx.x == 0) __stcg(p.x + i, v);
-            }
-            const double tot = block_sum_double(ss, red);
-            const float scale = (float)(1.0 / sqrt(tot / (double)p.dim + (double)p.eps));
-            for (int i = tid; i < p.dim; i += kThreads) xs[i] = __fmul_rn(__fmul_rn(xs[i], scale), __ldg(L.attn_norm + i));
-            __syncthreads();
-        } else {
-            if (!wait_counter(p, ctr - 1, G, flag)) return;
-            load_normed(xs, p.x, L.attn_norm, p.dim, p.eps, red);
-        }
-        { EpiStore e{p.qkv, L.qkv_bias}; gemv_phase<DT, false>(L.qkv, xs, e); }
-        signal_counter(ctr + 0);
-        // ---- ATTN
-        if (!wait_counter(p, ctr + 0, G, flag)) return;
+        int q0, q1;
+        cta_rows(L.qkv.rows, q0, q1);
+        if (L.qkv_bias)
+            for (int i = tid; i < q1 - q0; i += kConsumers) sm.bias()[i] = __ldg(L.qkv_bias + q0 + i);
+        if (l > 0 && !c.wait_counter(ctr - 1, G)) return false;
         {
-            const int S = p.splits, units = p.n_kv * S;
+            const XSrc src{l == 0 ? nullptr : p.x, L.attn_norm, p.dim};
+            EpiStore e{p.qkv, L.qkv_bias ? sm.bias() : nullptr, q0};
+            gemv_consume<DT, false>(c, L.qkv, src, token, e);
+        }
+        c.signal(ctr + 0);
+        // ---- ATTN
+        if (!c.wait_counter(ctr + 0, G)) return false;
+        {
+            const int units = p.n_kv * p.splits;
             for (int unit = blockIdx.x; unit < units; unit += G)
-                attention_unit(p, L, l, unit / S, unit % S, S, am, flag);
+                if (!attention_unit(c, L, l, unit)) return false;
         }
         // ---- O
-        if (!wait_counter(p, ctr + 1, p.n_kv, flag)) return;
-        load_plain(xs, p.attn, p.q_dim);
-        { EpiResidual e{p.x}; gemv_phase<DT, false>(L.o, xs, e); }
-        signal_counter(ctr + 2);
+        if (!c.wait_counter(ctr + 1, p.n_kv)) return false;
+        {
+            const XSrc src{p.attn, nullptr, p.q_dim};
+            EpiResidual e{p.x, sm.xown(), c.own0};
+            gemv_consume<DT, false>(c, L.o, src, token, e);
+        }
+        c.signal(ctr + 2);
         // ---- GU
-        if (!wait_counter(p, ctr + 2, G, flag)) return;
-        load_normed(xs, p.x, L.ffn_norm, p.dim, p.eps, red);
-        { EpiSwiGLU e{p.u}; gemv_phase<DT, true>(L.gu, xs, e); }
-        signal_counter(ctr + 3);
+        if (!c.wait_counter(ctr + 2, G)) return false;
+        {
+            const XSrc src{p.x, L.ffn_norm, p.dim};
+            EpiSwiGLU e{p.u};
+            gemv_consume<DT, true>(c, L.gu, src, token, e);
+        }
+        c.signal(ctr + 3);
         // ---- DOWN
-        if (!wait_counter(p, ctr + 3, G, flag)) return;
-        load_plain(xs, p.u, p.ffn);
-        { EpiResidual e{p.x}; gemv_phase<DT, false>(L.down, xs, e); }
-        signal_counter(ctr + 4);
+        if (!c.wait_counter(ctr + 3, G)) return false;
+        {
+            const XSrc src{p.u, nullptr, p.ffn};
+            EpiResidual e{p.x, sm.xown(), c.own0};
+            gemv_consume<DT, false>(c, L.down, src, token, e);
+        }
+        c.signal(ctr + 4);
     }
     // ---- LOGITS + argmax
     unsigned* fin = p.counters + 5 * p.n_layers;
-    if (!wait_counter(p, fin - 1, G, flag)) return;
-    load_normed(xs, p.x, p.out_norm, p.dim, p.eps, red);
+    if (!c.wait_counter(fin - 1, G)) return false;
     EpiLogits e{p.logits, 0ull};
-    gemv_phase<DT, false>(p.out, xs, e);
-    if ((tid & 31) == 0) s_best[tid >> 5] = e.best;
-    __syncthreads();
+    {
+        const XSrc src{p.x, p.out_norm, p.dim};
+        gemv_consume<DT, false>(c, p.out, src, token, e);
+    }
+    unsigned long long b = e.best;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, b, o);
+        b = other > b ? other : b;
+    }
+    if (c.lane == 0) sm.best()[c.warp] = b;
+    consumer_sync();
     if (tid == 0) {
-        unsigned long long b = 0ull;
-        for (int w = 0; w < kWarps; w++) b = s_best[w] > b ? s_best[w] : b;
-        atomicMax(p.best, b);
+        unsigned long long bb = 0ull;
+        for (int w = 0; w < kConsumerWarps; w++) bb = sm.best()[w] > bb ? sm.best()[w] : bb;
+        atomicMax(p.best, bb);
         __threadfence();
         const unsigned old = atomicAdd(fin, 1u);
-        s_flag = (old == (unsigned)(G - 1));
+        sm.misc()[1] = (old == (unsigned)(G - 1));
     }
-    __syncthreads();
-    if (s_flag) {
+    consumer_sync();
+    if (sm.misc()[1]) {
         // every CTA has passed its last wait: publish the argmax, re-arm the counters
         __threadfence();
-        if (tid == 0) {
-            const unsigned long long b = atomicExch(p.best, 0ull);
-            *p.token_out = argmax_key_index(b);
-        }
+        if (tid == 0) *p.token_out = argmax_key_index(atomicExch(p.best, 0ull));
         const int nc = n_phase_counters(p.n_layers) + p.n_layers * p.n_kv;
-        for (int i = tid; i < nc; i += kThreads) p.counters[i] = 0u;
+        for (int i = tid; i < nc; i += kConsumers) p.counters[i] = 0u;
     }
+    return true;
 }
 
-// Shared memory of the step kernel for a model (bytes).
-size_t step_smem_bytes(int dim, int q_dim, int ffn, int n_heads, int n_kv, int hd) {
+template <int DT>
+__device__ void producer_main(const StepParams& p, Smem& sm) {
+    Producer pr(p, sm);
+    for (int l = 0; l < p.n_layers && !pr.dead; l++) {
+        const LayerDev& L = p.layers[l];
+        pr.gemv(L.qkv, DT);
+        pr.attention(l);
+        pr.gemv(L.o, DT);
+        pr.gemv(L.gu, DT);
+        pr.gemv(L.down, DT);
+    }
+    pr.gemv(p.out, DT);
+    pr.drain();   // on success every chunk was consumed and the waits return at once
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kBlock, 1) decode_step_kernel(const __grid_constant__ StepParams p) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    Smem sm(smem_raw, p);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.ns; i++) {
+            mbar_init(&sm.full()[i], 1);
+            mbar_init(&sm.empty()[i], kConsumerWarps);
+        }
+        sm.misc()[0] = 0;
+        sm.misc()[1] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x >= kConsumers) {
+        if (threadIdx.x == kConsumers) producer_main<DT>(p, sm);
+        __syncwarp();
+    } else {
+        consumer_main<DT>(p, sm);
+    }
+    block_join();
+}
+
+// ------------------------------------------------------ host-side helpers --
+// Streaming plan of one matrix (rows per slot, team width, team count).  For
+// a pair matrix the plan counts super-rows (two matrix rows each).  Rows per
+// chunk are a multiple of the rows all teams take in one pass.
+bool matrix_plan(DMat& m, int wtype, bool pair) {
+    const int lpr = (m.cols + kLaneElems - 1) / kLaneElems;
+    int half = 1;
+    if (lpr <= 32) {
+        while (half < lpr) half *= 2;
+    } else {
+        half = 32 * ((lpr + 31) / 32);
+    }
+    const int tw = pair ? 2 * half : half;
+    int teams, rows_per_pass;
+    if (tw <= 32) {
+        teams = kConsumerWarps * (32 / tw);
+        rows_per_pass = teams;
+    } else {
+        if (tw / 32 > kConsumerWarps) return false;
+        teams = kConsumerWarps / (tw / 32);
+        if (teams > kMaxTeams) teams = kMaxTeams;
+        rows_per_pass = 2 * teams;
+    }
+    const int per = pair ? 2 : 1;
+    const int slot_rows = kSlotBytes / (per * slot_row_bytes(wtype, m.cols, m.dstride));
+    if (slot_rows < 1) return false;
+    m.pair = pair ? 1 : 0;
+    m.tw = tw;
+    m.teams = teams;
+    m.rpc = slot_rows >= rows_per_pass ? (slot_rows / rows_per_pass) * rows_per_pass
+                                       : (slot_rows >= teams ? (slot_rows / teams) * teams : slot_rows);
+    return true;
+}
+
+// Shared-memory geometry of the step kernel for a model.  Returns false if the
+// model does not fit the kernel's limits.
+bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int n_kv, int hd, int rope_dims,
+                   int max_splits, size_t* smem_bytes) {
+    (void)dim; (void)q_dim; (void)ffn;
     const int gq = n_heads / n_kv;
-    size_t xbytes = sizeof(float) * (size_t)max(max(dim, q_dim), ffn);
-    size_t abytes = sizeof(float) * (size_t)(gq * hd + hd + gq * kAttnChunk + ((3 * gq + 3) / 4) * 4) +
-                    2 * sizeof(__half) * (size_t)kAttnChunk * hd;
-    size_t b = xbytes > abytes ? xbytes : abytes;
-    return (b + 15) & ~(size_t)15;
+    int P = 8192 / hd;
+    if (P > 256) P = 256;
+    P &= ~7;
+    const int GD = gq * hd;
+    const size_t attn_scratch = sizeof(float) * (size_t)(GD + hd + gq * P + 3 * gq) + 2 * sizeof(__half) * hd;
+    const size_t merge = sizeof(float) * (size_t)max_splits * (hd + 2);
+    size_t xs = attn_scratch > merge ? attn_scratch : merge;
+    auto al = [](size_t b) { return (b + 127) & ~(size_t)127; };
+    const size_t tpart = sizeof(float) * kMaxTeams * 2 * kConsumerWarps * 2;
+    const size_t fixed = al(xs) + al(tpart) + al(2 * 128 * 4) + al(2 * kConsumers * 4) + al(2 * kOwnFloats * 4) + 1024;
+    if (rope_dims / 2 > 128 || GD > 2 * kConsumers || GD % 2) return false;
+    long long ns = ((long long)kMaxSmem - (long long)fixed) / kSlotBytes;
+    if (ns > 8) ns = 8;
+    if (ns < 2) return false;
+    size_t off = (size_t)ns * kSlotBytes;
+    p.ns = (int)ns;
+    p.attn_rows = P;
+    p.scratch_floats = (int)(xs / sizeof(float));
+    p.off_xs = (int)off; off += al(xs);
+    p.off_red = (int)off; off += al(tpart);
+    p.off_rope = (int)off; off += al(2 * 128 * 4);
+    p.off_comb = (int)off; off += al(2 * kConsumers * 4);
+    p.off_own = (int)off; off += al(2 * kOwnFloats * 4);
+    p.off_bar = (int)off; off += al(2 * ns * 8);
+    p.off_misc = (int)off; off += 64 + 8 * (kConsumerWarps + 2) + 8 * kConsumerWarps;
+    *smem_bytes = al(off);
+    return *smem_bytes <= (size_t)kMaxSmem;
 }
 
 const void* step_kernel_ptr(int wtype) {
@@ -551,7 +986,7 @@ const void* step_kernel_ptr(int wtype) {
 // ------------------------------------------------------------ test hooks --
 __global__ void kv_store_kernel(__half* kc, __half* vc, int pos, int kv_dim, const float* k, const float* v) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < kv_dim; i += gridDim.x * blockDim.x)
-        store_kv(kc, vc, pos, kv_dim, 0, i, k[i], v[i]);
+        store_kv(kc, vc, pos, kv_dim, 0, i, __float2half_rn(k[i]), __float2half_rn(v[i]));
 }
 
 template <int DT>

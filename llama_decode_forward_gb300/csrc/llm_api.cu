@@ -8,10 +8,15 @@
 #include <string>
 #include <vector>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "llm_internal.cuh"
 
 namespace llm {
-size_t step_smem_bytes(int dim, int q_dim, int ffn, int n_heads, int n_kv, int hd);
+bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int n_kv, int hd, int rope_dims,
+                   int max_splits, size_t* smem_bytes);
+bool matrix_plan(DMat& m, int wtype, bool pair);
 const void* step_kernel_ptr(int wtype);
 void launch_kv_store(cudaStream_t st, __half* kc, __half* vc, int pos, int kv_dim, const float* k, const float* v);
 void launch_dequant_rows(cudaStream_t st, int wtype, const DMat& m, int row0, int n_rows, float* out);
@@ -32,6 +37,8 @@ struct llm_handle {
     int q_dim = 0, kv_dim = 0, max_splits = 1;
     size_t smem = 0;
     const void* kernel = nullptr;
+    StepParams geo{};                // shared-memory geometry of the step kernel
+    CUtensorMap* kv_maps = nullptr;  // device array [2 * n_layers]
     float theta_scale = 0.f, attn_div = 0.f;
 
     uint8_t* arena = nullptr;        // weights in the library layout
@@ -86,16 +93,18 @@ static int fail(llm_handle* h, int status, const char* fmt, ...) {
 
 static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
+static int scale_stride(int cols) { return ((cols / 32) + 7) & ~7; }
+
 static size_t mat_bytes(int wtype, long long rows, long long cols) {
-    if (wtype == LLM_Q8_0) return (size_t)(rows * cols + rows * (cols / 32) * 2);
+    if (wtype == LLM_Q8_0) return (size_t)(rows * cols + rows * scale_stride((int)cols) * 2);
     return (size_t)(rows * cols * (wtype == LLM_F16 ? 2 : 4));
 }
 
-// Q8_0 blocks (34 bytes: FP16 scale, 32 int8) of `rows` rows -> quants and
-// scales of the library layout; source row r goes to destination row
-// dst0 + r*mul + phase.
+// Q8_0 blocks (34 bytes: FP16 scale, 32 int8) of `rows` rows -> biased
+// quants (qs + 128) and scales of the library layout; source row r goes to
+// destination row dst0 + r*mul + phase.
 __global__ void repack_q8_kernel(const uint8_t* __restrict__ src, int rows, int cols, uint8_t* dq, __half* dd,
-                                 int dst0, int mul, int phase) {
+                                 int dstride, int dst0, int mul, int phase) {
     const int nb = cols / 32;
     const long long total = (long long)rows * nb;
     for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < total;
@@ -103,13 +112,15 @@ __global__ void repack_q8_kernel(const uint8_t* __restrict__ src, int rows, int 
         const int r = (int)(b / nb), j = (int)(b % nb);
         const uint8_t* s = src + b * 34;
         const long long dr = (long long)dst0 + (long long)r * mul + phase;
-        dd[dr * nb + j] = __ushort_as_half((unsigned short)(s[0] | (s[1] << 8)));
+        dd[dr * dstride + j] = __ushort_as_half((unsigned short)(s[0] | (s[1] << 8)));
         uint32_t w[8];
 #pragma unroll
         for (int k = 0; k < 8; k++)
             w[k] = (uint32_t)s[2 + 4 * k] | ((uint32_t)s[3 + 4 * k] << 8) | ((uint32_t)s[4 + 4 * k] << 16) |
                    ((uint32_t)s[5 + 4 * k] << 24);
         uint4* d = reinterpret_cast<uint4*>(dq + dr * cols + (long long)j * 32);
+#pragma unroll
+        for (int k = 0; k < 8; k++) w[k] ^= 0x80808080u;          // stored biased: qs + 128
         d[0] = make_uint4(w[0], w[1], w[2], w[3]);
         d[1] = make_uint4(w[4], w[5], w[6], w[7]);
     }
@@ -124,7 +135,7 @@ static int put_matrix(llm_handle* h, const void* src, int rows, int cols, const 
         const long long total = (long long)rows * (cols / 32);
         const int blocks = (int)((total + 255) / 256 < 65535 * 8 ? (total + 255) / 256 : 65535 * 8);
         repack_q8_kernel<<<blocks, 256, 0, h->st>>>((const uint8_t*)src, rows, cols, (uint8_t*)dst.q,
-                                                    (__half*)dst.d, dst0, mul, phase);
+                                                    (__half*)dst.d, dst.dstride, dst0, mul, phase);
         h->launches++;
         CK(h, cudaGetLastError());
     } else {
@@ -135,20 +146,25 @@ static int put_matrix(llm_handle* h, const void* src, int rows, int cols, const 
     return LLM_OK;
 }
 
-static DMat carve_mat(llm_handle* h, size_t& off, int rows, int cols) {
+// A matrix of `rows` rows in the arena.  pair: rows 2i and 2i+1 are one
+// super-row of the streaming plan (m.rows then counts super-rows).
+static DMat carve_mat(llm_handle* h, size_t& off, int rows, int cols, bool pair = false) {
     DMat m{};
     m.rows = rows;
     m.cols = cols;
     if (h->cfg.wtype == LLM_Q8_0) {
         m.q = h->arena + off;
         off += align256((size_t)rows * cols);
+        m.dstride = scale_stride(cols);
         m.d = reinterpret_cast<const __half*>(h->arena + off);
-        off += align256((size_t)rows * (cols / 32) * 2);
+        off += align256((size_t)rows * m.dstride * 2);
     } else {
         m.q = h->arena + off;
         off += align256(mat_bytes(h->cfg.wtype, rows, cols));
         m.d = nullptr;
     }
+    if (pair) m.rows = rows / 2;
+    if (!matrix_plan(m, h->cfg.wtype, pair)) m.rpc = 0;
     return m;
 }
 
@@ -170,8 +186,16 @@ static int validate(const llm_config* c, const llm_weights* w, llm_handle* h) {
                     "dim and ffn_dim must be multiples of %d for this weight type", mult);
     if (c->head_dim % 8 || c->head_dim > 256) return fail(h, LLM_ERR_UNSUPPORTED, "head_dim must be a multiple of 8, <= 256");
     const int gq = c->n_heads / c->n_kv_heads;
-    if (gq > kWarps || gq * c->head_dim > kMaxGroupDim)
+    if (gq > kConsumerWarps || gq * c->head_dim > kMaxGroupDim)
         return fail(h, LLM_ERR_UNSUPPORTED, "query heads per kv head too large");
+    // the step kernel keeps a phase's activation vector in shared memory and
+    // each lane 64 of its elements in registers; rows must fit a ring slot
+    const int q_dim = c->n_heads * c->head_dim;
+    if (c->dim > 5760 || c->ffn_dim > 16384 || q_dim > 5760)
+        return fail(h, LLM_ERR_UNSUPPORTED, "dim must be at most 5760 and ffn_dim at most 16384");
+    if ((long long)slot_row_bytes(c->wtype, c->ffn_dim, scale_stride(c->ffn_dim)) > kSlotBytes ||
+        (long long)slot_row_bytes(c->wtype, c->dim, scale_stride(c->dim)) > kSlotBytes)
+        return fail(h, LLM_ERR_UNSUPPORTED, "matrix rows too long for the streaming ring");
     if (!w->tok_embd || !w->output_norm || !w->layers) return fail(h, LLM_ERR_INVALID_ARG, "a weight pointer is NULL");
     for (int l = 0; l < c->n_layers; l++) {
         const llm_layer_weights& L = w->layers[l];
@@ -188,6 +212,7 @@ static void free_handle(llm_handle* h) {
     cudaFree(h->kv);
     cudaFree(h->act);
     cudaFree(h->d_layers);
+    cudaFree(h->kv_maps);
     cudaFree(h->prefill_ws);
     if (h->pinned) cudaFreeHost(h->pinned);
     cudaGetLastError();
@@ -246,7 +271,7 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
         LayerDev& D = h->layers[l];
         D.qkv = carve_mat(h, off, q + 2 * kv, d);
         D.o = carve_mat(h, off, d, q);
-        D.gu = carve_mat(h, off, 2 * f, d);
+        D.gu = carve_mat(h, off, 2 * f, d, true);
         D.down = carve_mat(h, off, d, f);
         float* an = (float*)(h->arena + off); off += align256((size_t)d * 4);
         float* fn = (float*)(h->arena + off); off += align256((size_t)d * 4);
@@ -302,7 +327,15 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
     CKC(cudaMemcpyAsync(h->d_layers, h->layers.data(), sizeof(LayerDev) * L, cudaMemcpyHostToDevice, h->st));
 
     // ---- activations
-    h->max_splits = h->sms / c.n_kv_heads > 1 ? h->sms / c.n_kv_heads : 1;
+    // position splits per kv head: enough units to cover every SM, but the
+    // partials of one kv head must fit the merging CTA's 32 KB gather buffer
+    {
+        const int gq = c.n_heads / c.n_kv_heads;
+        int ms = h->sms / c.n_kv_heads;
+        const int cap = 32768 / (gq * (c.head_dim + 2) * 4);
+        if (ms > cap) ms = cap;
+        h->max_splits = ms > 1 ? ms : 1;
+    }
     h->n_counters = n_phase_counters(L) + L * c.n_kv_heads;
     size_t a = 0;
     auto take = [&](size_t b) { size_t o = a; a += align256(b); return o; };
@@ -328,11 +361,51 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
     h->theta_scale = (float)pow((double)c.rope_base, -2.0 / (double)c.rope_dims);
     h->attn_div = (float)sqrt((double)c.head_dim);
     h->kernel = step_kernel_ptr(c.wtype);
-    h->smem = step_smem_bytes(d, q, f, c.n_heads, c.n_kv_heads, c.head_dim);
+    if (!step_geometry(h->geo, d, q, f, c.n_heads, c.n_kv_heads, c.head_dim, c.rope_dims, h->max_splits,
+                       &h->smem)) {
+        free_handle(h);
+        return LLM_ERR_UNSUPPORTED;
+    }
+    // per-CTA shares that live in shared memory, and every matrix's plan
+    if ((d + h->sms - 1) / h->sms > kOwnFloats || (q + 2 * kv + h->sms - 1) / h->sms > kOwnFloats) {
+        free_handle(h);
+        return LLM_ERR_UNSUPPORTED;
+    }
+    for (int l = 0; l < L; l++) {
+        const LayerDev& D = h->layers[l];
+        if (!D.qkv.rpc || !D.o.rpc || !D.gu.rpc || !D.down.rpc) { free_handle(h); return LLM_ERR_UNSUPPORTED; }
+    }
+    if (!h->embd.rpc || !h->out.rpc) { free_handle(h); return LLM_ERR_UNSUPPORTED; }
     CKC(cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem));
     int per_sm = 0;
-    CKC(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->kernel, kThreads, h->smem));
+    CKC(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->kernel, kBlock, h->smem));
     if (per_sm < 1) { free_handle(h); return LLM_ERR_UNSUPPORTED; }
+
+    // 2-D tensor maps of every layer's K and V cache: [max_seq][kv_dim] F16,
+    // box [attn_rows][head_dim], read by the step kernel's TMA tile loads
+    {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q_res;
+        CKC(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q_res));
+        if (!fn || q_res != cudaDriverEntryPointSuccess) { free_handle(h); return LLM_ERR_CUDA; }
+        auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        std::vector<CUtensorMap> maps((size_t)2 * L);
+        for (int l = 0; l < L; l++)
+            for (int which = 0; which < 2; which++) {
+                void* base = which ? (void*)h->layers[l].vc : (void*)h->layers[l].kc;
+                cuuint64_t gdim[2] = {(cuuint64_t)kv, (cuuint64_t)c.max_seq};
+                cuuint64_t gstride[1] = {(cuuint64_t)kv * 2};
+                cuuint32_t box[2] = {(cuuint32_t)c.head_dim, (cuuint32_t)h->geo.attn_rows};
+                cuuint32_t estride[2] = {1, 1};
+                CUresult r = encode(&maps[(size_t)2 * l + which], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, gdim,
+                                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                if (r != CUDA_SUCCESS) { free_handle(h); return LLM_ERR_CUDA; }
+            }
+        CKC(cudaMalloc(&h->kv_maps, sizeof(CUtensorMap) * maps.size()));
+        CKC(cudaMemcpyAsync(h->kv_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice,
+                            h->st));
+    }
     CKC(cudaStreamSynchronize(h->st));
     *out = h;
     return LLM_OK;
@@ -341,13 +414,13 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
 
 static int launch_step(llm_handle* h, const int* token_dev, int pos, int* argmax_dev) {
     const llm_config& c = h->cfg;
-    StepParams p{};
+    StepParams p = h->geo;
     p.layers = h->d_layers;
+    p.kv_maps = h->kv_maps;
     p.embd = h->embd;
     p.out = h->out;
     p.out_norm = h->out_norm;
     p.rope_freqs = h->rope_freqs;
-    p.wtype = c.wtype;
     p.n_layers = c.n_layers; p.dim = c.dim; p.n_heads = c.n_heads; p.n_kv = c.n_kv_heads; p.hd = c.head_dim;
     p.ffn = c.ffn_dim; p.vocab = c.vocab; p.max_seq = c.max_seq; p.rope_dims = c.rope_dims; p.neox = c.rope_neox;
     p.q_dim = h->q_dim; p.kv_dim = h->kv_dim;
@@ -358,7 +431,7 @@ static int launch_step(llm_handle* h, const int* token_dev, int pos, int* argmax
     int s = (pos + 1 + 15) / 16;
     p.splits = s < 1 ? 1 : (s > h->max_splits ? h->max_splits : s);
     void* args[] = {&p};
-    CK(h, cudaLaunchCooperativeKernel(h->kernel, dim3(h->sms), dim3(kThreads), args, h->smem, h->st));
+    CK(h, cudaLaunchCooperativeKernel(h->kernel, dim3(h->sms), dim3(kBlock), args, h->smem, h->st));
     h->launches++;
     return LLM_OK;
 }

@@ -9,21 +9,37 @@
 
 namespace llm {
 
-constexpr int kThreads = 512;          // threads per CTA of the decode step kernel
-constexpr int kWarps = kThreads / 32;
-constexpr int kAttnChunk = 64;         // KV positions staged in shared memory at a time
-constexpr int kMaxGroupDim = 1024;     // (n_heads / n_kv_heads) * head_dim handled per attention unit
+// Decode step kernel: one CTA per SM, 15 consumer warps + 1 producer warp
+// (16 warps: 4 per SM sub-partition, so up to 128 registers per thread).
+constexpr int kConsumerWarps = 15;
+constexpr int kConsumers = kConsumerWarps * 32;   // 480
+constexpr int kBlock = kConsumers + 32;           // 512
+constexpr int kSlotBytes = 32768;                 // one ring slot (a chunk of weight rows or KV rows)
+constexpr int kRedFloats = 1024;                  // row partials of one chunk
+constexpr int kMaxGroupDim = 2 * kConsumers;      // (n_heads / n_kv_heads) * head_dim per attention unit
+// 32-byte column blocks of a row one consumer thread owns: 2 for F16, else 1.
+__host__ __device__ inline int max_blocks_per_thread(int wtype) { return wtype == LLM_F16 ? 2 : 1; }
+constexpr int kMaxSmem = 232448;                  // 227 KB opt-in dynamic shared memory per CTA
 
-// Device error word values (sticky until llm_reset).
+// Device error word bits (sticky until llm_reset).
 enum : int { kErrNone = 0, kErrTimeout = 1, kErrToken = 2 };
 
-// A weight matrix in the library's layout.  Row r of a Q8_0 matrix is `cols`
-// int8 quants at q + r*cols and cols/32 FP16 scales at d + r*(cols/32); F16 and
-// F32 matrices are `rows` rows of `cols` values at q (d unused).
+// A weight matrix in the library's layout.  Q8_0: row r is `cols` quants at
+// q + r*cols, each stored biased as the unsigned byte qs + 128, and cols/32
+// FP16 scales at d + r*dstride (dstride = cols/32 rounded up to a multiple of
+// 8, so every row of scales is 16-byte aligned).
+// F16 / F32: `rows` rows of `cols` values at q.
+// Streaming plan (set at creation): a ring slot carries `rpc` rows; a row is
+// reduced by a team of `tw` lanes (32 elements per lane; tw <= 32 is a part
+// of one warp, tw > 32 is tw/32 whole warps) and `teams` teams work side by side.
+// pair = 1 (gate/up): rows 2i and 2i+1 form one "super-row" reduced by one
+// team whose two halves share the same activation lanes; rows/rpc then count
+// super-rows.
 struct DMat {
     const uint8_t* q;
     const __half* d;
-    int rows, cols;
+    int rows, cols, dstride;
+    int rpc, tw, teams, pair;
 };
 
 struct LayerDev {
@@ -42,18 +58,18 @@ struct LayerDev {
 // counter per (layer, kv head).  All zero between steps.
 struct StepParams {
     const LayerDev* layers;
+    const void* kv_maps;      // CUtensorMap[2 * n_layers]: K and V cache of each layer, box [attn_rows][hd]
     DMat embd;
     DMat out;
     const float* out_norm;
     const float* rope_freqs;  // [rope_dims/2] or nullptr
-    int wtype;
     int n_layers, dim, n_heads, n_kv, hd, ffn, vocab, max_seq, rope_dims, neox, q_dim, kv_dim;
     float eps, theta_scale, attn_div;
 
     float* x;                 // residual stream [dim]
     float* qkv;               // [q_dim + 2 kv_dim]
     float* attn;              // attention output [q_dim]
-    float* u;                 // SwiGLU output [ffn]
+    float* u;                 // silu(gate) * up [ffn]
     float* logits;            // [vocab]
     float* attn_part;         // [n_heads][max_splits][hd + 2]
     int max_splits;
@@ -65,28 +81,40 @@ struct StepParams {
     int* token_out;
     int pos;
     int splits;               // attention splits per kv head for this pos
+
+    // shared-memory geometry (bytes from the dynamic smem base)
+    int ns;                   // ring slots
+    int attn_rows;            // KV rows per ring slot
+    int off_xs, off_red, off_rope, off_comb, off_bar, off_misc, off_own;
+    int scratch_floats;       // floats of the attention scratch region (xs)
 };
 
 __host__ __device__ inline int n_phase_counters(int n_layers) { return 5 * n_layers + 1; }
 
-// ---------------------------------------------------------------- loads --
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-    return r;
+__host__ __device__ inline int dtype_bytes_x16(int wtype) {   // bytes per element, times 16
+    return wtype == LLM_Q8_0 ? 16 : (wtype == LLM_F16 ? 32 : 64);
 }
 
-__device__ __forceinline__ unsigned short ld_stream_u16(const void* p) {
-    unsigned short r;
-    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
-    return r;
+constexpr int kLaneElems = 32;                     // matrix columns one lane covers per row
+constexpr int kMaxTeams = 7;                       // multi-warp teams (named barriers 3..9)
+constexpr int kOwnFloats = 256;                    // residual rows a CTA owns, and its QKV bias rows
+
+// Bytes of one row in a ring slot (quants/values plus Q8_0 scales).
+__host__ __device__ inline int slot_row_bytes(int wtype, int cols, int dstride) {
+    return wtype == LLM_Q8_0 ? cols + 2 * dstride : cols * (wtype == LLM_F16 ? 2 : 4);
 }
+
+// ---------------------------------------------------------------- PTX --
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
@@ -95,12 +123,50 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-// int8 (as a byte of w) -> exact float: the byte, offset by 128, is placed in
-// the low mantissa bits of 2^23 and the offset float 2^23 + 128 subtracted.
-__device__ __forceinline__ float i8_to_f32(uint32_t w_xor80, int k) {
-    const uint32_t sel = 0x7540u | (uint32_t)k;
-    return __uint_as_float(__byte_perm(w_xor80, 0x4B000000u, sel)) - 8388736.0f;
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` on the mbarrier.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// 2-D tiled tensor copy global -> shared (box of the tensor map at (x, y)).
+__device__ __forceinline__ void tma_2d_g2s(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_addr(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+__device__ __forceinline__ void block_join() { asm volatile("bar.sync 2, %0;" ::"n"(kBlock) : "memory"); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
