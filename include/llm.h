@@ -164,6 +164,13 @@ int llm_test_kv_store(llm_handle *h, int layer, int32_t pos, const float *k_dev,
  * 4 w_gate, 5 w_up, 6 w_down (of `layer`), 7 tok_embd, 8 output.  Synchronous. */
 int llm_test_dequant_rows(llm_handle *h, int which, int layer, int32_t row0, int32_t n_rows, float *out_dev);
 
+/* Phase trace of the last decode step: copies sms * 1024 %globaltimer stamps
+ * (nanoseconds, uint64, per CTA: the start and end of every phase of every
+ * layer, as laid out in the library's trace table) to `host` (HOST, caller
+ * owned).  `sms` receives the CTA count.  Only libraries compiled with
+ * LLM_TRACE record stamps; others return LLM_ERR_UNSUPPORTED.  Synchronous. */
+int llm_trace_read(llm_handle *h, uint64_t *host, int32_t *sms);
+
 /* Number of kernel launches enqueued on the handle's stream so far (all calls). */
 int64_t llm_launch_count(const llm_handle *h);
 

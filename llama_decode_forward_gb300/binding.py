@@ -50,6 +50,7 @@ _SIGS = {
     "llm_kv_view": ([_vp, _int, ctypes.POINTER(_vp), ctypes.POINTER(_vp)], _int),
     "llm_test_kv_store": ([_vp, _int, _i32, _vp, _vp], _int),
     "llm_test_dequant_rows": ([_vp, _int, _int, _i32, _i32, _vp], _int),
+    "llm_trace_read": ([_vp, _vp, ctypes.POINTER(_i32)], _int),
     "llm_launch_count": ([_vp], ctypes.c_int64),
     "llm_destroy": ([_vp], None),
     "llm_status_string": ([_int], ctypes.c_char_p),
@@ -155,6 +156,14 @@ def llm_test_kv_store(h, layer: int, pos: int, k_dev, v_dev):
 
 def llm_test_dequant_rows(h, which: int, layer: int, row0: int, n_rows: int, out_dev):
     _check(_lib.llm_test_dequant_rows(h, which, layer, row0, n_rows, _ptr(out_dev)), h)
+
+
+def llm_trace_read(h) -> np.ndarray:
+    """Phase stamps of the last step, [sms][1024] uint64 ns (LLM_TRACE builds only)."""
+    n = _i32()
+    buf = np.zeros(1024 * 1024, np.uint64)
+    _check(_lib.llm_trace_read(h, buf.ctypes.data, ctypes.byref(n)), h)
+    return buf[: n.value * 1024].reshape(n.value, 1024).copy()
 
 
 def llm_launch_count(h) -> int:

@@ -35,6 +35,14 @@
 
 namespace llm {
 
+#ifdef LLM_TRACE
+__device__ __forceinline__ void trace_mark(const StepParams& p, int k) {
+    if (p.trace) p.trace[(size_t)blockIdx.x * kTraceSlots + k] = global_timer_ns();
+}
+#else
+__device__ __forceinline__ void trace_mark(const StepParams&, int) {}
+#endif
+
 // Spin until ready() holds.  The deadline (SM cycle counter) and the error
 // word (a global load) are checked only every 256 polls, so a wait that ends
 // reacts within a few hundred cycles.  Returns false on expiry (after setting
@@ -122,6 +130,7 @@ struct Producer {
     RingPos rp;
     long long it = 0;
     bool dead = false;
+    long long waited = 0;  // trace builds: cycles spent waiting for free slots
 
     __device__ Producer(const StepParams& p_, Smem& s_) : p(p_), sm(s_) {}
 
@@ -132,10 +141,16 @@ struct Producer {
         if (rp.count >= p.ns) {
             const uint32_t par = rp.phase ^ 1u;
             uint64_t* bar = &sm.empty()[slot];
-            if (!bounded_wait([&] { return mbar_try_wait(bar, par); }, p.err)) {
+#ifdef LLM_TRACE
+            const long long tw0 = clock64();
+#endif
+            if (!bounded_wait([&] { return mbar_test_wait(bar, par); }, p.err)) {
                 dead = true;
                 return nullptr;
             }
+#ifdef LLM_TRACE
+            waited += clock64() - tw0;
+#endif
         }
         return sm.ring() + (size_t)slot * kSlotBytes;
     }
@@ -145,8 +160,9 @@ struct Producer {
         it++;
     }
 
-    __device__ void gemv(const DMat& m, int wtype) {
+    __device__ void gemv(const DMat& m, int wtype, int tk) {
         if (dead) return;
+        trace_mark(p, tk);
         int r0, r1;                                   // rows, or super-rows when m.pair
         cta_rows(m.rows, r0, r1);
         const int per = m.pair ? 2 : 1;
@@ -163,12 +179,19 @@ struct Producer {
             if (bd)
                 bulk_g2s(dst + bq, reinterpret_cast<const uint8_t*>(m.d) + (size_t)r * per * rowd, bd,
                          &sm.full()[slot]);
+            if (r == r0 && tk < 448) trace_mark(p, 640 + (tk - 256) / 8 * 4 + ((tk - 256) % 8 == 0 ? 0 : (tk - 256) % 8 - 1));
             issued();
         }
+#ifdef LLM_TRACE
+        if (p.trace && tk < 448)
+            p.trace[(size_t)blockIdx.x * kTraceSlots + 896 + (tk - 256) / 8 * 4 + ((tk - 256) % 8 == 0 ? 0 : (tk - 256) % 8 - 1)] = waited;
+        waited = 0;
+#endif
     }
 
     __device__ void attention(int layer) {
         if (dead) return;
+        trace_mark(p, 256 + 8 * layer + 1);
         const int S = p.splits, units = p.n_kv * S, P = p.attn_rows;
         const char* maps = reinterpret_cast<const char*>(p.kv_maps);
         const void* kmap = maps + (size_t)(2 * layer) * 128;
@@ -212,6 +235,8 @@ struct Consumer {
     RingPos rp;            // next slot to consume
     int tid, warp, lane;
     int own0, own1;        // residual rows this CTA owns (rows of Wo and Wdown)
+    int tk = -1;           // trace slot of the current GEMV's first chunk
+    long long waited = 0;  // trace builds: cycles spent waiting for ring slots
 
     __device__ Consumer(const StepParams& p_, Smem& s_) : p(p_), sm(s_) {
         tid = threadIdx.x;
@@ -228,7 +253,13 @@ struct Consumer {
         slot = rp.slot;
         const uint32_t par = rp.phase;
         uint64_t* bar = &sm.full()[slot];
-        if (!bounded_wait([&] { return mbar_try_wait(bar, par); }, p.err)) sm.misc()[0] = 1;
+#ifdef LLM_TRACE
+        const long long tw0 = clock64();
+#endif
+        if (!bounded_wait([&] { return mbar_test_wait(bar, par); }, p.err)) sm.misc()[0] = 1;
+#ifdef LLM_TRACE
+        waited += clock64() - tw0;
+#endif
         return sm.ring() + (size_t)slot * kSlotBytes;
     }
 
@@ -350,6 +381,38 @@ __device__ __forceinline__ float lane_row(const uint8_t* w, const uint8_t* scale
     return t;
 }
 
+// Two rows at once: every shared-memory word of both rows is loaded before
+// the arithmetic starts, so the load latency is paid once.
+template <int DT>
+__device__ __forceinline__ void lane_row2(const uint8_t* wa, const uint8_t* sa, const uint8_t* wb, const uint8_t* sb,
+                                          const float2 (&x2)[16], int nseg, float& va, float& vb) {
+    constexpr int NS = LaneDot<DT>::kSeg;
+    uint4 a[NS], b[NS];
+#pragma unroll
+    for (int s = 0; s < NS; s++) {
+        a[s] = s < nseg ? reinterpret_cast<const uint4*>(wa)[s] : make_uint4(0u, 0u, 0u, 0u);
+        b[s] = s < nseg ? reinterpret_cast<const uint4*>(wb)[s] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float da = 1.f, db = 1.f;
+    if constexpr (DT == LLM_Q8_0) {
+        if (nseg) {
+            da = __half2float(*reinterpret_cast<const __half*>(sa));
+            db = __half2float(*reinterpret_cast<const __half*>(sb));
+        }
+    }
+    float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
+    LaneDot<DT>::acc(a, x2, a0, a1);
+    LaneDot<DT>::acc(b, x2, b0, b1);
+    const float ta = (a0.x + a0.y) + (a1.x + a1.y), tb = (b0.x + b0.y) + (b1.x + b1.y);
+    if constexpr (DT == LLM_Q8_0) {
+        va = nseg ? da * ta : 0.f;
+        vb = nseg ? db * tb : 0.f;
+    } else {
+        va = ta;
+        vb = tb;
+    }
+}
+
 // ------------------------------------------------------------------ GEMV --
 struct EpiStore {                 // out[r] = v (+ bias of this CTA's row r)
     float* out;
@@ -357,6 +420,7 @@ struct EpiStore {                 // out[r] = v (+ bias of this CTA's row r)
     int r0;
     __device__ void row(int r, float v) { __stcg(out + r, bias ? v + bias[r - r0] : v); }
     __device__ void pair(int, float, float) {}
+    __device__ void finish(Consumer&) {}
 };
 struct EpiResidual {              // x[r] += v, the owned row kept in smem
     float* x;
@@ -368,13 +432,28 @@ struct EpiResidual {              // x[r] += v, the owned row kept in smem
         __stcg(x + r, y);
     }
     __device__ void pair(int, float, float) {}
+    __device__ void finish(Consumer&) {}
 };
-struct EpiSwiGLU {                // u[i] = silu(gate_i) * up_i ("The Forward Pass in Java", Example 8)
+// u[i] = silu(gate_i) * up_i ("The Forward Pass in Java", Example 8).  The
+// (gate, up) sums are parked in shared memory as the rows complete and the
+// nonlinearity is applied to all of the CTA's rows at once at the end of the
+// phase, off the rows' critical path.
+struct EpiSwiGLU {
     float* u;
+    float* gs;                    // smem [2 * rows of this CTA]
+    int i0, i1;                   // this CTA's super-rows
     __device__ void row(int, float) {}
     __device__ void pair(int i, float g, float up) {
-        const float e = expf(-g);
-        __stcg(u + i, __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), up));
+        gs[2 * (i - i0)] = g;
+        gs[2 * (i - i0) + 1] = up;
+    }
+    __device__ void finish(Consumer& c) {
+        consumer_sync();
+        for (int k = c.tid; k < i1 - i0; k += kConsumers) {
+            const float g = gs[2 * k], up = gs[2 * k + 1];
+            const float e = expf(-g);
+            __stcg(u + i0 + k, __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), up));
+        }
     }
 };
 struct EpiLogits {                // logits[r] = v, keep this lane's best (value, first index)
@@ -386,6 +465,7 @@ struct EpiLogits {                // logits[r] = v, keep this lane's best (value
         best = k > best ? k : best;
     }
     __device__ void pair(int, float, float) {}
+    __device__ void finish(Consumer&) {}
 };
 
 // Where a GEMV phase takes its activation vector: a global vector (written
@@ -428,36 +508,75 @@ __device__ __forceinline__ Lanes lane_layout(const Consumer& c, const DMat& m) {
 
 // x2 <- the lane's 32 activation values (zero past the vector's end), normed
 // when src.g is set.  Every consumer thread must call this (it synchronises).
+// A vector that fits the scratch region is first staged there once per CTA
+// with coalesced loads (each 16-byte word w of the 128-byte slice s at word
+// s*8 + (w ^ (s & 7)), so that the lanes' reads of their own slices fall in
+// distinct banks); every lane then reads its slice from shared memory.  This
+// keeps the L2 requests per line of the (freshly written, grid-wide read)
+// vector at one per CTA.  Longer vectors are read by the lanes directly.
 template <int DT, bool PAIR>
 __device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& L, const XSrc& src, int token,
                                        float2 (&x2)[16]) {
     const int col0 = L.col0;
     const bool have = L.active && col0 < src.n;
-    if (src.x) {
-        const float4* s4 = reinterpret_cast<const float4*>(src.x + col0);
+    float scale = 1.0f;
+    if (((src.n + 31) & ~31) <= c.p.scratch_floats) {   // whole 32-float slices fit
+        float4* xv = reinterpret_cast<float4*>(c.sm.xs());
+        float ss = 0.f;
+        for (int i = c.tid; i < src.n / 4; i += kConsumers) {
+            float4 v;
+            if (src.x) {
+                v = __ldcg(reinterpret_cast<const float4*>(src.x) + i);
+            } else {
+                v = make_float4(weight_at<DT>(c.p.embd, token, 4 * i), weight_at<DT>(c.p.embd, token, 4 * i + 1),
+                                weight_at<DT>(c.p.embd, token, 4 * i + 2), weight_at<DT>(c.p.embd, token, 4 * i + 3));
+            }
+            ss += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
+            xv[(i & ~7) + ((i & 7) ^ ((i >> 3) & 7))] = v;
+        }
+        if (src.g) {
+            const float tot = c.warps_total(ss);        // synchronises the consumers
+            scale = 1.0f / sqrtf(tot / (float)src.n + c.p.eps);
+        } else {
+            consumer_sync();
+        }
+        const float4* x4 = xv + L.clit * 8;
 #pragma unroll
         for (int k = 0; k < 8; k++) {
-            const float4 v = have && col0 + 4 * k < src.n ? __ldcg(s4 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 v = have && col0 + 4 * k < src.n ? x4[k ^ (L.clit & 7)] : make_float4(0.f, 0.f, 0.f, 0.f);
             x2[2 * k] = make_float2(v.x, v.y);
             x2[2 * k + 1] = make_float2(v.z, v.w);
         }
     } else {
+        if (src.x) {
+            const float4* s4 = reinterpret_cast<const float4*>(src.x + col0);
 #pragma unroll
-        for (int k = 0; k < 16; k++) {
-            const int e = col0 + 2 * k;
-            x2[k] = have && e < src.n ? make_float2(weight_at<DT>(c.p.embd, token, e), weight_at<DT>(c.p.embd, token, e + 1))
-                                      : make_float2(0.f, 0.f);
+            for (int k = 0; k < 8; k++) {
+                const float4 v = have && col0 + 4 * k < src.n ? __ldcg(s4 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                x2[2 * k] = make_float2(v.x, v.y);
+                x2[2 * k + 1] = make_float2(v.z, v.w);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; k++) {
+                const int e = col0 + 2 * k;
+                x2[k] = have && e < src.n
+                            ? make_float2(weight_at<DT>(c.p.embd, token, e), weight_at<DT>(c.p.embd, token, e + 1))
+                            : make_float2(0.f, 0.f);
+            }
+        }
+        if (src.g) {
+            // each column counted once: the lanes of team 0 (first half for pairs)
+            float ss = 0.f;
+            if (L.team == 0 && L.hsel == 0 && have) {
+#pragma unroll
+                for (int k = 0; k < 16; k++) ss += x2[k].x * x2[k].x + x2[k].y * x2[k].y;
+            }
+            const float tot = c.warps_total(ss);
+            scale = 1.0f / sqrtf(tot / (float)src.n + c.p.eps);
         }
     }
     if (src.g) {
-        // each column counted once: the lanes of team 0 (first half for pairs)
-        float ss = 0.f;
-        if (L.team == 0 && L.hsel == 0 && have) {
-#pragma unroll
-            for (int k = 0; k < 16; k++) ss += x2[k].x * x2[k].x + x2[k].y * x2[k].y;
-        }
-        const float tot = c.warps_total(ss);
-        const float scale = 1.0f / sqrtf(tot / (float)src.n + c.p.eps);
         const float4* g4 = reinterpret_cast<const float4*>(src.g + col0);
 #pragma unroll
         for (int k = 0; k < 8; k++) {
@@ -473,13 +592,15 @@ __device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& 
 // The CTA's rows of m, chunk by chunk from the ring (the plan in DMat).
 // Multi-warp teams take two rows per pass: their partial dots are reduced with
 // one butterfly (lanes 0-15 for the first row, 16-31 for the second), then the
-// team meets at its named barrier and lane 0 of the team adds the warps' parts.
+// team meets at its named barrier, and lanes 0 and 16 of the team's first warp
+// add the warps' parts of the two rows.
 template <int DT, bool PAIR, class Epi>
 __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const XSrc& src, int token, Epi& epi) {
     constexpr int ES = DT == LLM_Q8_0 ? 1 : (DT == LLM_F16 ? 2 : 4);
     const Lanes L = lane_layout<DT, PAIR>(c, m);
     float2 x2[16];
     lane_x<DT, PAIR>(c, m, L, src, token, x2);
+    if (c.tid == 0 && c.tk >= 0) trace_mark(c.p, c.tk - 160 + 512);
     const int tw = m.tw, teams = m.teams;
     int r0, r1;
     cta_rows(m.rows, r0, r1);
@@ -489,12 +610,12 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
     const int xoff = L.col0 * ES, soff = L.clit * 2;
     int pass = 0;
     for (int r = r0; r < r1; r += m.rpc) {
-        const int n = min(m.rpc, r1 - r);           // rows (super-rows) in this chunk
+        const int n = min(m.rpc, r1 - r);
         int slot;
         const uint8_t* buf = c.next_slot(slot);
+        if (c.tid == 0 && r == r0 && c.tk >= 0) trace_mark(c.p, c.tk);
         const uint8_t* sbase = buf + (size_t)n * per * rowq;
         if (tw <= 32) {
-            // part-of-a-warp teams: one row per pass, segmented butterfly
             const int half = PAIR ? tw / 2 : tw;
             const int wteam = c.warp * (32 / tw);
             for (int j = 0; wteam + j * teams < n; j++) {
@@ -514,14 +635,14 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
                 }
             }
         } else if (L.active) {
-            // whole-warp teams: two rows per pass
             const int wpr = tw / 32;
             for (int j = 0; L.team + 2 * j * teams < n; j++) {
                 const int ra = L.team + 2 * j * teams, rb = ra + teams;
                 const bool hasb = rb < n;
                 const int ma = ra * per + L.hsel, mb = (hasb ? rb : ra) * per + L.hsel;
-                float va = lane_row<DT>(buf + (size_t)ma * rowq + xoff, sbase + ma * rowd + soff, x2, L.nseg);
-                float vb = lane_row<DT>(buf + (size_t)mb * rowq + xoff, sbase + mb * rowd + soff, x2, L.nseg);
+                float va, vb;
+                lane_row2<DT>(buf + (size_t)ma * rowq + xoff, sbase + ma * rowd + soff, buf + (size_t)mb * rowq + xoff,
+                              sbase + mb * rowd + soff, x2, L.nseg, va, vb);
                 float keep = c.lane < 16 ? va : vb;
                 const float send = c.lane < 16 ? vb : va;
                 keep += __shfl_xor_sync(0xffffffffu, send, 16);
@@ -530,18 +651,18 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
                 float* tp = c.sm.tpart() + ((L.team * 2 + (pass & 1)) * kConsumerWarps) * 2;
                 if ((c.lane & 15) == 0) tp[(c.warp % wpr) * 2 + (c.lane >> 4)] = keep;
                 asm volatile("bar.sync %0, %1;" ::"r"(3 + L.team), "r"(tw) : "memory");
-                if (L.lit == 0) {
+                if ((L.lit & ~16) == 0 && (L.lit == 0 || hasb)) {
+                    const int h = L.lit >> 4;
+                    const int row = r + (h ? rb : ra);
                     if constexpr (PAIR) {
-                        float ga = 0.f, ua = 0.f, gb = 0.f, ub = 0.f;
-                        for (int k = 0; k < wpr / 2; k++) { ga += tp[2 * k]; gb += tp[2 * k + 1]; }
-                        for (int k = wpr / 2; k < wpr; k++) { ua += tp[2 * k]; ub += tp[2 * k + 1]; }
-                        epi.pair(r + ra, ga, ua);
-                        if (hasb) epi.pair(r + rb, gb, ub);
+                        float g = 0.f, up = 0.f;
+                        for (int k = 0; k < wpr / 2; k++) g += tp[2 * k + h];
+                        for (int k = wpr / 2; k < wpr; k++) up += tp[2 * k + h];
+                        epi.pair(row, g, up);
                     } else {
-                        float ta = 0.f, tb = 0.f;
-                        for (int k = 0; k < wpr; k++) { ta += tp[2 * k]; tb += tp[2 * k + 1]; }
-                        epi.row(r + ra, ta);
-                        if (hasb) epi.row(r + rb, tb);
+                        float t = 0.f;
+                        for (int k = 0; k < wpr; k++) t += tp[2 * k + h];
+                        epi.row(row, t);
                     }
                 }
                 pass++;
@@ -549,6 +670,11 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
         }
         c.release(slot);
     }
+    epi.finish(c);
+#ifdef LLM_TRACE
+    if (c.tid == 0 && c.tk >= 0 && c.p.trace) c.p.trace[(size_t)blockIdx.x * kTraceSlots + c.tk - 160 + 768] = c.waited;
+    c.waited = 0;
+#endif
 }
 
 // ------------------------------------------------------------------ RoPE --
@@ -795,52 +921,71 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         if (L.qkv_bias)
             for (int i = tid; i < q1 - q0; i += kConsumers) sm.bias()[i] = __ldg(L.qkv_bias + q0 + i);
         if (l > 0 && !c.wait_counter(ctr - 1, G)) return false;
+        if (tid == 0) trace_mark(p, 10 * l);
+        c.tk = 160 + 4 * l;
         {
             const XSrc src{l == 0 ? nullptr : p.x, L.attn_norm, p.dim};
             EpiStore e{p.qkv, L.qkv_bias ? sm.bias() : nullptr, q0};
             gemv_consume<DT, false>(c, L.qkv, src, token, e);
         }
+        if (tid == 0) trace_mark(p, 10 * l + 1);
         c.signal(ctr + 0);
         // ---- ATTN
         if (!c.wait_counter(ctr + 0, G)) return false;
+        if (tid == 0) trace_mark(p, 10 * l + 2);
         {
             const int units = p.n_kv * p.splits;
             for (int unit = blockIdx.x; unit < units; unit += G)
                 if (!attention_unit(c, L, l, unit)) return false;
         }
+        if (tid == 0) trace_mark(p, 10 * l + 3);
         // ---- O
         if (!c.wait_counter(ctr + 1, p.n_kv)) return false;
+        if (tid == 0) trace_mark(p, 10 * l + 4);
+        c.tk = 160 + 4 * l + 1;
         {
             const XSrc src{p.attn, nullptr, p.q_dim};
             EpiResidual e{p.x, sm.xown(), c.own0};
             gemv_consume<DT, false>(c, L.o, src, token, e);
         }
+        if (tid == 0) trace_mark(p, 10 * l + 5);
         c.signal(ctr + 2);
         // ---- GU
         if (!c.wait_counter(ctr + 2, G)) return false;
+        if (tid == 0) trace_mark(p, 10 * l + 6);
+        c.tk = 160 + 4 * l + 2;
         {
             const XSrc src{p.x, L.ffn_norm, p.dim};
-            EpiSwiGLU e{p.u};
+            int i0, i1;
+            cta_rows(L.gu.rows, i0, i1);
+            EpiSwiGLU e{p.u, sm.bias(), i0, i1};
             gemv_consume<DT, true>(c, L.gu, src, token, e);
         }
+        if (tid == 0) trace_mark(p, 10 * l + 7);
         c.signal(ctr + 3);
         // ---- DOWN
         if (!c.wait_counter(ctr + 3, G)) return false;
+        if (tid == 0) trace_mark(p, 10 * l + 8);
+        c.tk = 160 + 4 * l + 3;
         {
             const XSrc src{p.u, nullptr, p.ffn};
             EpiResidual e{p.x, sm.xown(), c.own0};
             gemv_consume<DT, false>(c, L.down, src, token, e);
         }
+        if (tid == 0) trace_mark(p, 10 * l + 9);
         c.signal(ctr + 4);
     }
     // ---- LOGITS + argmax
     unsigned* fin = p.counters + 5 * p.n_layers;
     if (!c.wait_counter(fin - 1, G)) return false;
+    if (tid == 0) trace_mark(p, 240);
+    c.tk = -1;
     EpiLogits e{p.logits, 0ull};
     {
         const XSrc src{p.x, p.out_norm, p.dim};
         gemv_consume<DT, false>(c, p.out, src, token, e);
     }
+    if (tid == 0) trace_mark(p, 241);
     unsigned long long b = e.best;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -862,6 +1007,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         // every CTA has passed its last wait: publish the argmax, re-arm the counters
         __threadfence();
         if (tid == 0) *p.token_out = argmax_key_index(atomicExch(p.best, 0ull));
+        if (tid == 0) trace_mark(p, 242);
         const int nc = n_phase_counters(p.n_layers) + p.n_layers * p.n_kv;
         for (int i = tid; i < nc; i += kConsumers) p.counters[i] = 0u;
     }
@@ -873,13 +1019,15 @@ __device__ void producer_main(const StepParams& p, Smem& sm) {
     Producer pr(p, sm);
     for (int l = 0; l < p.n_layers && !pr.dead; l++) {
         const LayerDev& L = p.layers[l];
-        pr.gemv(L.qkv, DT);
+        pr.gemv(L.qkv, DT, 256 + 8 * l);
         pr.attention(l);
-        pr.gemv(L.o, DT);
-        pr.gemv(L.gu, DT);
-        pr.gemv(L.down, DT);
+        pr.gemv(L.o, DT, 256 + 8 * l + 2);
+        pr.gemv(L.gu, DT, 256 + 8 * l + 3);
+        pr.gemv(L.down, DT, 256 + 8 * l + 4);
+        trace_mark(p, 256 + 8 * l + 5);
     }
-    pr.gemv(p.out, DT);
+    pr.gemv(p.out, DT, 448);
+    trace_mark(p, 449);
     pr.drain();   // on success every chunk was consumed and the waits return at once
 }
 
@@ -944,7 +1092,6 @@ bool matrix_plan(DMat& m, int wtype, bool pair) {
 // model does not fit the kernel's limits.
 bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int n_kv, int hd, int rope_dims,
                    int max_splits, size_t* smem_bytes) {
-    (void)dim; (void)q_dim; (void)ffn;
     const int gq = n_heads / n_kv;
     int P = 8192 / hd;
     if (P > 256) P = 256;
@@ -952,11 +1099,22 @@ bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int 
     const int GD = gq * hd;
     const size_t attn_scratch = sizeof(float) * (size_t)(GD + hd + gq * P + 3 * gq) + 2 * sizeof(__half) * hd;
     const size_t merge = sizeof(float) * (size_t)max_splits * (hd + 2);
+    // the scratch region also stages the activation vectors of the GEMV
+    // phases: always those of length dim and q_dim, the FFN one as well when
+    // that still leaves six ring slots
+    auto slices = [](int n) { return (size_t)((n + 31) & ~31) * sizeof(float); };
+    const size_t stage = slices(dim > q_dim ? dim : q_dim);
     size_t xs = attn_scratch > merge ? attn_scratch : merge;
+    xs = xs > stage ? xs : stage;
     auto al = [](size_t b) { return (b + 127) & ~(size_t)127; };
     const size_t tpart = sizeof(float) * kMaxTeams * 2 * kConsumerWarps * 2;
-    const size_t fixed = al(xs) + al(tpart) + al(2 * 128 * 4) + al(2 * kConsumers * 4) + al(2 * kOwnFloats * 4) + 1024;
+    auto fixed_for = [&](size_t x) {
+        return al(x) + al(tpart) + al(2 * 128 * 4) + al(2 * kConsumers * 4) + al(2 * kOwnFloats * 4) + 1024;
+    };
     if (rope_dims / 2 > 128 || GD > 2 * kConsumers || GD % 2) return false;
+    const size_t xs_ffn = xs > slices(ffn) ? xs : slices(ffn);
+    if (((long long)kMaxSmem - (long long)fixed_for(xs_ffn)) / kSlotBytes >= 6) xs = xs_ffn;
+    const size_t fixed = fixed_for(xs);
     long long ns = ((long long)kMaxSmem - (long long)fixed) / kSlotBytes;
     if (ns > 8) ns = 8;
     if (ns < 2) return false;

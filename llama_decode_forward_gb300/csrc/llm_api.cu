@@ -64,6 +64,7 @@ struct llm_handle {
     bool broken = false;             // a device error was seen; cleared by llm_reset
     std::string last_error;
 
+    unsigned long long* trace = nullptr;   // LLM_TRACE builds: [sms][kTraceSlots]
     void* prefill_ws = nullptr;      // prefill workspace (lazily sized)
     size_t prefill_ws_bytes = 0;
 };
@@ -214,6 +215,7 @@ static void free_handle(llm_handle* h) {
     cudaFree(h->d_layers);
     cudaFree(h->kv_maps);
     cudaFree(h->prefill_ws);
+    cudaFree(h->trace);
     if (h->pinned) cudaFreeHost(h->pinned);
     cudaGetLastError();
     delete h;
@@ -357,6 +359,10 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
     h->tok_in = (int*)(h->act + o_tin);
     h->tok_out = (int*)(h->act + o_tout);
     CKC(cudaMallocHost(&h->pinned, sizeof(HostPinned)));
+#ifdef LLM_TRACE
+    CKC(cudaMalloc(&h->trace, (size_t)h->sms * kTraceSlots * 8));
+    CKC(cudaMemsetAsync(h->trace, 0, (size_t)h->sms * kTraceSlots * 8, h->st));
+#endif
 
     h->theta_scale = (float)pow((double)c.rope_base, -2.0 / (double)c.rope_dims);
     h->attn_div = (float)sqrt((double)c.head_dim);
@@ -367,7 +373,8 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
         return LLM_ERR_UNSUPPORTED;
     }
     // per-CTA shares that live in shared memory, and every matrix's plan
-    if ((d + h->sms - 1) / h->sms > kOwnFloats || (q + 2 * kv + h->sms - 1) / h->sms > kOwnFloats) {
+    if ((d + h->sms - 1) / h->sms > kOwnFloats || (q + 2 * kv + h->sms - 1) / h->sms > kOwnFloats ||
+        2 * ((f + h->sms - 1) / h->sms) > kOwnFloats) {
         free_handle(h);
         return LLM_ERR_UNSUPPORTED;
     }
@@ -417,6 +424,7 @@ static int launch_step(llm_handle* h, const int* token_dev, int pos, int* argmax
     StepParams p = h->geo;
     p.layers = h->d_layers;
     p.kv_maps = h->kv_maps;
+    p.trace = h->trace;
     p.embd = h->embd;
     p.out = h->out;
     p.out_norm = h->out_norm;
@@ -568,6 +576,15 @@ extern "C" int llm_test_dequant_rows(llm_handle* h, int which, int layer, int32_
         h->launches++;
     }
     CK(h, cudaGetLastError());
+    CK(h, cudaStreamSynchronize(h->st));
+    return LLM_OK;
+}
+
+extern "C" int llm_trace_read(llm_handle* h, uint64_t* host, int32_t* sms) {
+    if (!h || !host || !sms) return LLM_ERR_INVALID_ARG;
+    if (!h->trace) return LLM_ERR_UNSUPPORTED;
+    *sms = h->sms;
+    CK(h, cudaMemcpyAsync(host, h->trace, (size_t)h->sms * kTraceSlots * 8, cudaMemcpyDeviceToHost, h->st));
     CK(h, cudaStreamSynchronize(h->st));
     return LLM_OK;
 }

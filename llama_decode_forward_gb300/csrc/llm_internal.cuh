@@ -87,7 +87,21 @@ struct StepParams {
     int attn_rows;            // KV rows per ring slot
     int off_xs, off_red, off_rope, off_comb, off_bar, off_misc, off_own;
     int scratch_floats;       // floats of the attention scratch region (xs)
+
+    unsigned long long* trace;  // [gridDim.x][kTraceSlots] phase stamps, or nullptr (LLM_TRACE builds)
 };
+
+// Phase trace (compiled in with -DLLM_TRACE): per CTA, %globaltimer stamps (ns).
+//   consumer  10*l + {0..9}: start/end of QKV, ATTN, O, GU, DOWN of layer l
+//             160 + 4*l + {0..3}: first chunk of QKV, O, GU, DOWN landed
+//             240, 241, 242: LOGITS start, end, argmax published
+//   producer  256 + 8*l + {0..4}: first issue of QKV, ATTN, O, GU, DOWN; 256 + 8*l + 5: layer issued
+//             448, 449: LOGITS first issue, all issued
+//   consumer  512 + 4*l + {0..3}: activation lanes loaded in QKV, O, GU, DOWN
+//   producer  640 + 4*l + {0..3}: first copy of QKV, O, GU, DOWN issued
+//   consumer  768 + 4*l + {0..3}: SM cycles thread 0 waited for full slots in QKV, O, GU, DOWN
+//   producer  896 + 4*l + {0..3}: SM cycles the producer waited for free slots while issuing them
+constexpr int kTraceSlots = 1024;
 
 __host__ __device__ inline int n_phase_counters(int n_layers) { return 5 * n_layers + 1; }
 
@@ -141,6 +155,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking probe of a phase: never suspends the thread, so a spin on it
+// sees the phase complete as soon as it does.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_addr(bar)), "r"(parity)
