@@ -11,9 +11,9 @@
 //
 //   per layer l:  QKV   rows of [Wq;Wk;Wv] . RMSNorm(x)        -> qkv (+ bias)
 //                 ATTN  (kv head, position split) units: RoPE(q), RoPE(k),
-//                       K/V row `pos` stored as F16, partial softmax;
-//                       the last split of a kv head merges the partials -> attn
+//                       K/V row `pos` stored as F16, partial softmax (m, l, acc)
 //                 O     rows of Wo . attn                       -> x += ...
+//                       (every CTA merges the splits into attn as it stages it)
 //                 GU    rows of [Wgate|Wup] . RMSNorm(x)        -> u = silu(gate) * up
 //                 DOWN  rows of Wdown . u                       -> x += ...
 //   LOGITS  rows of Wout . RMSNorm(x) -> logits, argmax (first index of the max)
@@ -72,7 +72,7 @@ struct Smem {
     const StepParams& p;
     __device__ Smem(unsigned char* b, const StepParams& p_) : base(b), p(p_) {}
     __device__ __forceinline__ uint8_t* ring() const { return base; }
-    // attention scratch and the merge gather buffer (scratch_floats floats)
+    // attention scratch, and the staged activation vector of a GEMV phase (scratch_floats floats)
     __device__ __forceinline__ float* xs() const { return reinterpret_cast<float*>(base + p.off_xs); }
     // [kMaxTeams][2][kConsumerWarps][2] partial dots of multi-warp teams
     __device__ __forceinline__ float* tpart() const { return reinterpret_cast<float*>(base + p.off_red); }
@@ -473,9 +473,10 @@ struct EpiLogits {                // logits[r] = v, keep this lane's best (value
 // gains g ("The Forward Pass in Java", Example 4: y = (x * scale) * g with
 // scale = 1/sqrt(mean(x^2) + eps), the sum of squares a float tree sum).
 struct XSrc {
-    const float* x;               // nullptr: the embedding row
+    const float* x;               // nullptr: the embedding row (unless part is set)
     const float* g;               // nullptr: no norm
     int n;                        // length of the vector
+    const float* part;            // attention partials to merge (the O phase), or nullptr
 };
 
 // Lane layout of a plan: team, lane index within the team, row half (pair).
@@ -523,9 +524,43 @@ __device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& 
     if (((src.n + 31) & ~31) <= c.p.scratch_floats) {   // whole 32-float slices fit
         float4* xv = reinterpret_cast<float4*>(c.sm.xs());
         float ss = 0.f;
+        const int S = c.p.splits, MS = c.p.max_splits, hd = c.p.hd;
+        float* wgt = c.sm.comb();                   // [n_heads][S] merge weights
+        if (src.part) {
+            // Merge the attention splits of every head: M = max_s m_s,
+            // w_s = e^(m_s - M) / sum_s' e^(m_s' - M) l_s', out = sum_s w_s acc_s.
+            // One warp per head, one split per lane (S <= 32).
+            const float2* mlp = reinterpret_cast<const float2*>(src.part + (size_t)c.p.n_heads * MS * hd);
+            for (int h = c.warp; h < c.p.n_heads; h += kConsumerWarps) {
+                const bool has = c.lane < S;
+                const float2 mv = has ? __ldcg(mlp + (size_t)h * MS + c.lane) : make_float2(-INFINITY, 0.f);
+                const float M = warp_max(mv.x);
+                const float w = has && mv.x != -INFINITY ? expf(mv.x - M) : 0.f;
+                const float Ls = warp_sum(w * mv.y);
+                if (has) wgt[h * S + c.lane] = w / Ls;
+            }
+            consumer_sync();
+        }
         for (int i = c.tid; i < src.n / 4; i += kConsumers) {
             float4 v;
-            if (src.x) {
+            if (src.part) {
+                const int h = (4 * i) / hd, e = (4 * i) % hd;
+                const float4* a4 = reinterpret_cast<const float4*>(src.part + (size_t)h * MS * hd + e);
+                const float* wh = wgt + h * S;
+                v = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int s0 = 0; s0 < S; s0 += 8) {
+                    float4 t[8];
+#pragma unroll
+                    for (int k = 0; k < 8; k++)
+                        t[k] = s0 + k < S ? __ldcg(a4 + (size_t)(s0 + k) * (hd / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int k = 0; k < 8; k++) {
+                        const float w = s0 + k < S ? wh[s0 + k] : 0.f;
+                        v = make_float4(fmaf(w, t[k].x, v.x), fmaf(w, t[k].y, v.y), fmaf(w, t[k].z, v.z),
+                                        fmaf(w, t[k].w, v.w));
+                    }
+                }
+            } else if (src.x) {
                 v = __ldcg(reinterpret_cast<const float4*>(src.x) + i);
             } else {
                 v = make_float4(weight_at<DT>(c.p.embd, token, 4 * i), weight_at<DT>(c.p.embd, token, 4 * i + 1),
@@ -713,7 +748,14 @@ __device__ __forceinline__ void store_kv(__half* kc, __half* vc, int pos, int kv
 }
 
 // ------------------------------------------------------------- attention --
-__device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int unit) {
+// One unit = the positions [t0, t1) of kv head g, for its gq query heads
+// ("The Forward Pass in Java", Example 11: scores q.k / sqrt(hd), softmax over
+// the positions, weighted sum of the V rows).  The unit keeps a running max m
+// and sum l per head across its chunks (online softmax) and writes its partial
+// (m, l, acc): acc[h][d] at attn_part[(h*max_splits + s)*hd + d], (m, l) at
+// attn_part[n_heads*max_splits*hd + 2*(h*max_splits + s)].  The splits are
+// merged where the O phase stages its activation vector.
+__device__ bool attention_unit(Consumer& c, const LayerDev& L, int unit) {
     const StepParams& p = c.p;
     Smem& sm = c.sm;
     const int tid = c.tid, warp = c.warp, lane = c.lane;
@@ -724,10 +766,11 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
     // scratch
     float* q_s = sm.xs();                                          // [gq][hd]
     float* kf = q_s + GD;                                          // [hd] f32 k of this position
-    float* sc = kf + hd;                                           // [gq][P]
-    float* mlc = sc + gq * P;                                      // [3][gq]
-    __half* kp = reinterpret_cast<__half*>(mlc + 3 * gq);          // [hd]
-    __half* vp = kp + hd;                                          // [hd]
+    float* sc = kf + hd;                                           // [2][gq][P] scores, then probabilities
+    float* ml = sc + 2 * gq * P;                                   // [2][gq] running max m, sum l
+    float* corr = ml + 2 * gq;                                     // [2][gq] rescale of the chunk's old sums
+    __half* kp = reinterpret_cast<__half*>(corr + 2 * gq);         // [hd] this position's K row (F16)
+    __half* vp = kp + hd;                                          // [hd] this position's V row (F16)
 
     const bool writer = t0 <= p.pos && p.pos < t1;
     {
@@ -756,13 +799,14 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
         rope_apply(p, sm, q_s + (i / (p.rope_dims / 2)) * hd, i % (p.rope_dims / 2));
     if (writer)
         for (int i = tid; i < p.rope_dims / 2; i += kConsumers) rope_apply(p, sm, kf, i);
-    if (tid < gq) { mlc[tid] = -INFINITY; mlc[gq + tid] = 0.f; }
+    if (tid < gq) { ml[tid] = -INFINITY; ml[gq + tid] = 0.f; }
     consumer_sync();
     if (writer && tid < hd) {
         const __half kh = __float2half_rn(kf[tid]);
         kp[tid] = kh;
         store_kv(L.kc, L.vc, p.pos, p.kv_dim, g * hd, tid, kh, vp[tid]);
     }
+    consumer_sync();                                               // kp visible
     // PV work split: thread t accumulates the output pair o2 = t % (GD/2)
     // (elements 2*o2, 2*o2+1) over positions with index % NSPLIT == t / (GD/2).
     const int GD2 = GD / 2;
@@ -770,128 +814,108 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
     const int o2 = tid % GD2, sp = tid / GD2;
     const bool pv_active = sp < NSPLIT;
     const int oh = (2 * o2) / hd, oi = (2 * o2) % hd;
+    const int nh2 = hd / 2;
+    const int prow = p.pos - t0;                                   // this step's position within the unit
     float2 acc = make_float2(0.f, 0.f);
 
-    for (int c0 = t0; c0 < t1; c0 += P) {
+    int ci = 0;
+    for (int c0 = t0; c0 < t1; c0 += P, ci++) {
         const int np = min(P, t1 - c0);
         int slot;
-        uint8_t* buf = c.next_slot(slot);
-        __half* ks = reinterpret_cast<__half*>(buf);
-        __half* vs = ks + (size_t)P * hd;
-        consumer_sync();                                            // kp/vp ready; every thread saw the slot land
-        if (writer && p.pos >= c0 && p.pos < c0 + np && tid < hd) { // this step's row, not the stale copy
-            ks[(p.pos - c0) * hd + tid] = kp[tid];
-            vs[(p.pos - c0) * hd + tid] = vp[tid];
-        }
-        consumer_sync();
-        if (c.aborted()) return false;
-        // scores: thread (h, position); the start column rotates with the lane
-        // so that a warp's reads fall in different banks
+        const uint8_t* buf = c.next_slot(slot);
+        const __half* ks = reinterpret_cast<const __half*>(buf);
+        const __half* vs = ks + (size_t)P * hd;
+        float* scb = sc + (ci & 1) * gq * P;
+        float* corrb = corr + (ci & 1) * gq;
+        // scores: thread (h, position); the K row of this step's position is
+        // the one just computed, not the copy the tile load may have read.
+        // Four partial sums; the start column rotates with the lane so that a
+        // warp's reads fall in different banks.
         for (int idx = tid; idx < gq * np; idx += kConsumers) {
             const int h = idx / np, pp = idx % np;
             const float2* q2 = reinterpret_cast<const float2*>(q_s + h * hd);
-            const __half2* k2 = reinterpret_cast<const __half2*>(ks + (size_t)pp * hd);
-            const int nh2 = hd / 2;
-            float2 a = make_float2(0.f, 0.f);
+            const __half2* k2 = reinterpret_cast<const __half2*>(
+                writer && c0 + pp - t0 == prow ? kp : ks + (size_t)pp * hd);
+            float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
             int j = lane % nh2;
-            for (int k = 0; k < nh2; k++) {
-                a = __ffma2_rn(__half22float2(k2[j]), q2[j], a);
+            int k = 0;
+            for (; k + 4 <= nh2; k += 4) {
+                const int j1 = j + 1 == nh2 ? 0 : j + 1;
+                const int j2 = j1 + 1 == nh2 ? 0 : j1 + 1;
+                const int j3 = j2 + 1 == nh2 ? 0 : j2 + 1;
+                a0 = __ffma2_rn(__half22float2(k2[j]), q2[j], a0);
+                a1 = __ffma2_rn(__half22float2(k2[j1]), q2[j1], a1);
+                a2 = __ffma2_rn(__half22float2(k2[j2]), q2[j2], a2);
+                a3 = __ffma2_rn(__half22float2(k2[j3]), q2[j3], a3);
+                j = j3 + 1 == nh2 ? 0 : j3 + 1;
+            }
+            for (; k < nh2; k++) {
+                a0 = __ffma2_rn(__half22float2(k2[j]), q2[j], a0);
                 j = j + 1 == nh2 ? 0 : j + 1;
             }
-            sc[h * P + pp] = __fdiv_rn(a.x + a.y, p.attn_div);
+            const float2 a = make_float2((a0.x + a1.x) + (a2.x + a3.x), (a0.y + a1.y) + (a2.y + a3.y));
+            scb[h * P + pp] = __fdiv_rn(a.x + a.y, p.attn_div);
         }
         consumer_sync();
+        if (c.aborted()) return false;
         if (warp < gq) {
             const int h = warp;
             float mloc = -INFINITY;
-            for (int pp = lane; pp < np; pp += 32) mloc = fmaxf(mloc, sc[h * P + pp]);
+            for (int pp = lane; pp < np; pp += 32) mloc = fmaxf(mloc, scb[h * P + pp]);
             mloc = warp_max(mloc);
-            const float mold = mlc[h], mnew = fmaxf(mold, mloc);
+            const float mold = ml[h], mnew = fmaxf(mold, mloc);
             float sum = 0.f;
             for (int pp = lane; pp < np; pp += 32) {
-                const float e = expf(sc[h * P + pp] - mnew);
-                sc[h * P + pp] = e;
+                const float e = expf(scb[h * P + pp] - mnew);
+                scb[h * P + pp] = e;
                 sum += e;
             }
             sum = warp_sum(sum);
             if (lane == 0) {
-                const float corr = expf(mold - mnew);     // 0 on the first chunk (mold = -inf)
-                mlc[h] = mnew;
-                mlc[gq + h] = mlc[gq + h] * corr + sum;
-                mlc[2 * gq + h] = corr;
+                const float cr = expf(mold - mnew);       // 0 on the first chunk (mold = -inf)
+                ml[h] = mnew;
+                ml[gq + h] = ml[gq + h] * cr + sum;
+                corrb[h] = cr;
             }
         }
         consumer_sync();
         if (pv_active) {
-            const float corr = mlc[2 * gq + oh];
-            float2 v = make_float2(acc.x * corr, acc.y * corr);
-            const float* e = sc + oh * P;
-            for (int pp = sp; pp < np; pp += NSPLIT) {
-                const float2 vv = __half22float2(*reinterpret_cast<const __half2*>(vs + (size_t)pp * hd + oi));
-                v = __ffma2_rn(make_float2(e[pp], e[pp]), vv, v);
+            const float cr = corrb[oh];
+            float2 v0 = make_float2(acc.x * cr, acc.y * cr), v1 = make_float2(0.f, 0.f), v2 = v1, v3 = v1;
+            const float* e = scb + oh * P;
+            auto vrow = [&](int pp) {
+                const __half* r = writer && c0 + pp - t0 == prow ? vp : vs + (size_t)pp * hd;
+                return __half22float2(*reinterpret_cast<const __half2*>(r + oi));
+            };
+            int pp = sp;
+            for (; pp + 3 * NSPLIT < np; pp += 4 * NSPLIT) {
+                v0 = __ffma2_rn(make_float2(e[pp], e[pp]), vrow(pp), v0);
+                v1 = __ffma2_rn(make_float2(e[pp + NSPLIT], e[pp + NSPLIT]), vrow(pp + NSPLIT), v1);
+                v2 = __ffma2_rn(make_float2(e[pp + 2 * NSPLIT], e[pp + 2 * NSPLIT]), vrow(pp + 2 * NSPLIT), v2);
+                v3 = __ffma2_rn(make_float2(e[pp + 3 * NSPLIT], e[pp + 3 * NSPLIT]), vrow(pp + 3 * NSPLIT), v3);
             }
-            acc = v;
+            for (; pp < np; pp += NSPLIT) v0 = __ffma2_rn(make_float2(e[pp], e[pp]), vrow(pp), v0);
+            acc = make_float2((v0.x + v1.x) + (v2.x + v3.x), (v0.y + v1.y) + (v2.y + v3.y));
         }
         c.release(slot);
     }
-    // combine the position splits, write this split's (m, l, acc)
+    // combine the PV position splits and write this unit's partial
     if (pv_active) {
         sm.comb()[sp * GD + 2 * o2] = acc.x;
         sm.comb()[sp * GD + 2 * o2 + 1] = acc.y;
     }
     consumer_sync();
-    const int stride = hd + 2;
+    float* part_acc = p.attn_part;
+    float* part_ml = p.attn_part + (size_t)p.n_heads * p.max_splits * hd;
     for (int oo = tid; oo < GD; oo += kConsumers) {
         float v = 0.f;
         for (int k = 0; k < NSPLIT; k++) v += sm.comb()[k * GD + oo];
         const int hh = oo / hd, ii = oo % hd;
-        float* part = p.attn_part + ((size_t)(h0 + hh) * p.max_splits + s) * stride;
-        __stcg(part + 2 + ii, v);
-        if (ii == 0) { __stcg(part, mlc[hh]); __stcg(part + 1, mlc[gq + hh]); }
+        const size_t hs = (size_t)(h0 + hh) * p.max_splits + s;
+        __stcg(part_acc + hs * hd + ii, v);
+        if (ii == 0) __stcg(reinterpret_cast<float2*>(part_ml) + hs, make_float2(ml[hh], ml[gq + hh]));
     }
-    // the last split to finish merges: M = max m_s, L = sum e^(m_s-M) l_s,
-    // out = sum e^(m_s-M) acc_s / L
-    unsigned* mc = p.counters + n_phase_counters(p.n_layers) + layer * p.n_kv + g;
-    consumer_sync();
-    if (tid == 0) {
-        __threadfence();
-        const unsigned old = atomicAdd(mc, 1u);
-        sm.misc()[1] = (old == (unsigned)(S - 1));
-    }
-    consumer_sync();
-    if (sm.misc()[1]) {
-        __threadfence();
-        float* gat = sm.xs();                                      // [S][stride] of one head
-        const int total = S * stride;
-        for (int h = 0; h < gq; h++) {
-            const float* src = p.attn_part + (size_t)(h0 + h) * p.max_splits * stride;
-            for (int base = tid; base < total; base += 4 * kConsumers) {
-                float v[4];
-#pragma unroll
-                for (int k = 0; k < 4; k++)
-                    if (base + k * kConsumers < total) v[k] = __ldcg(src + base + k * kConsumers);
-#pragma unroll
-                for (int k = 0; k < 4; k++)
-                    if (base + k * kConsumers < total) gat[base + k * kConsumers] = v[k];
-            }
-            consumer_sync();
-            for (int i = tid; i < hd; i += kConsumers) {
-                float M = -INFINITY;
-                for (int ss = 0; ss < S; ss++) M = fmaxf(M, gat[ss * stride]);
-                float Lsum = 0.f, v = 0.f;
-                for (int ss = 0; ss < S; ss++) {
-                    const float ms = gat[ss * stride];
-                    const float w = ms == -INFINITY ? 0.f : expf(ms - M);
-                    Lsum = fmaf(w, gat[ss * stride + 1], Lsum);
-                    v = fmaf(w, gat[ss * stride + 2 + i], v);
-                }
-                __stcg(p.attn + (h0 + h) * hd + i, v / Lsum);
-            }
-            consumer_sync();
-        }
-        c.signal(p.counters + 5 * layer + 1);
-    }
-    consumer_sync();
+    consumer_sync();                                               // comb, scratch free for the next unit
     return true;
 }
 
@@ -924,7 +948,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         if (tid == 0) trace_mark(p, 10 * l);
         c.tk = 160 + 4 * l;
         {
-            const XSrc src{l == 0 ? nullptr : p.x, L.attn_norm, p.dim};
+            const XSrc src{l == 0 ? nullptr : p.x, L.attn_norm, p.dim, nullptr};
             EpiStore e{p.qkv, L.qkv_bias ? sm.bias() : nullptr, q0};
             gemv_consume<DT, false>(c, L.qkv, src, token, e);
         }
@@ -936,15 +960,16 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         {
             const int units = p.n_kv * p.splits;
             for (int unit = blockIdx.x; unit < units; unit += G)
-                if (!attention_unit(c, L, l, unit)) return false;
+                if (!attention_unit(c, L, unit)) return false;
         }
+        c.signal(ctr + 1);
         if (tid == 0) trace_mark(p, 10 * l + 3);
         // ---- O
-        if (!c.wait_counter(ctr + 1, p.n_kv)) return false;
+        if (!c.wait_counter(ctr + 1, G)) return false;
         if (tid == 0) trace_mark(p, 10 * l + 4);
         c.tk = 160 + 4 * l + 1;
         {
-            const XSrc src{p.attn, nullptr, p.q_dim};
+            const XSrc src{nullptr, nullptr, p.q_dim, p.attn_part};
             EpiResidual e{p.x, sm.xown(), c.own0};
             gemv_consume<DT, false>(c, L.o, src, token, e);
         }
@@ -955,7 +980,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         if (tid == 0) trace_mark(p, 10 * l + 6);
         c.tk = 160 + 4 * l + 2;
         {
-            const XSrc src{p.x, L.ffn_norm, p.dim};
+            const XSrc src{p.x, L.ffn_norm, p.dim, nullptr};
             int i0, i1;
             cta_rows(L.gu.rows, i0, i1);
             EpiSwiGLU e{p.u, sm.bias(), i0, i1};
@@ -968,7 +993,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         if (tid == 0) trace_mark(p, 10 * l + 8);
         c.tk = 160 + 4 * l + 3;
         {
-            const XSrc src{p.u, nullptr, p.ffn};
+            const XSrc src{p.u, nullptr, p.ffn, nullptr};
             EpiResidual e{p.x, sm.xown(), c.own0};
             gemv_consume<DT, false>(c, L.down, src, token, e);
         }
@@ -982,7 +1007,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
     c.tk = -1;
     EpiLogits e{p.logits, 0ull};
     {
-        const XSrc src{p.x, p.out_norm, p.dim};
+        const XSrc src{p.x, p.out_norm, p.dim, nullptr};
         gemv_consume<DT, false>(c, p.out, src, token, e);
     }
     if (tid == 0) trace_mark(p, 241);
@@ -1008,7 +1033,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         __threadfence();
         if (tid == 0) *p.token_out = argmax_key_index(atomicExch(p.best, 0ull));
         if (tid == 0) trace_mark(p, 242);
-        const int nc = n_phase_counters(p.n_layers) + p.n_layers * p.n_kv;
+        const int nc = n_phase_counters(p.n_layers);
         for (int i = tid; i < nc; i += kConsumers) p.counters[i] = 0u;
     }
     return true;
@@ -1097,14 +1122,13 @@ bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int 
     if (P > 256) P = 256;
     P &= ~7;
     const int GD = gq * hd;
-    const size_t attn_scratch = sizeof(float) * (size_t)(GD + hd + gq * P + 3 * gq) + 2 * sizeof(__half) * hd;
-    const size_t merge = sizeof(float) * (size_t)max_splits * (hd + 2);
+    const size_t attn_scratch = sizeof(float) * (size_t)(GD + hd + 2 * gq * P + 4 * gq) + 2 * sizeof(__half) * hd;
     // the scratch region also stages the activation vectors of the GEMV
     // phases: always those of length dim and q_dim, the FFN one as well when
     // that still leaves six ring slots
     auto slices = [](int n) { return (size_t)((n + 31) & ~31) * sizeof(float); };
     const size_t stage = slices(dim > q_dim ? dim : q_dim);
-    size_t xs = attn_scratch > merge ? attn_scratch : merge;
+    size_t xs = attn_scratch;
     xs = xs > stage ? xs : stage;
     auto al = [](size_t b) { return (b + 127) & ~(size_t)127; };
     const size_t tpart = sizeof(float) * kMaxTeams * 2 * kConsumerWarps * 2;

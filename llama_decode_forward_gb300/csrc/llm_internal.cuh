@@ -54,8 +54,8 @@ struct LayerDev {
     __half* vc;
 };
 
-// Counters of one step: 5 phases per layer + the logits phase, then one merge
-// counter per (layer, kv head).  All zero between steps.
+// Counters of one step: 5 phases per layer + the logits phase.  All zero
+// between steps.
 struct StepParams {
     const LayerDev* layers;
     const void* kv_maps;      // CUtensorMap[2 * n_layers]: K and V cache of each layer, box [attn_rows][hd]
@@ -71,7 +71,7 @@ struct StepParams {
     float* attn;              // attention output [q_dim]
     float* u;                 // silu(gate) * up [ffn]
     float* logits;            // [vocab]
-    float* attn_part;         // [n_heads][max_splits][hd + 2]
+    float* attn_part;         // acc [n_heads][max_splits][hd], then (m, l) [n_heads][max_splits][2]
     int max_splits;
     unsigned long long* best; // packed argmax of the step
     unsigned* counters;
