@@ -11,9 +11,9 @@
 //
 //   per layer l:  QKV   rows of [Wq;Wk;Wv] . RMSNorm(x)        -> qkv (+ bias)
 //                 ATTN  (kv head, position split) units: RoPE(q), RoPE(k),
-//                       K/V row `pos` stored as F16, partial softmax (m, l, acc)
+//                       K/V row `pos` stored as F16, partial softmax (m, l, acc);
+//                       the last split of a kv head merges the partials -> attn
 //                 O     rows of Wo . attn                       -> x += ...
-//                       (every CTA merges the splits into attn as it stages it)
 //                 GU    rows of [Wgate|Wup] . RMSNorm(x)        -> u = silu(gate) * up
 //                 DOWN  rows of Wdown . u                       -> x += ...
 //   LOGITS  rows of Wout . RMSNorm(x) -> logits, argmax (first index of the max)
@@ -278,10 +278,9 @@ struct Consumer {
 
     __device__ void signal(unsigned* c) {
         consumer_sync();
-        if (tid == 0) {
-            __threadfence();
-            red_release_add(c, 1u);
-        }
+        // the barrier orders every consumer's writes before thread 0's
+        // release; the release makes them visible at GPU scope
+        if (tid == 0) red_release_add(c, 1u);
     }
 
     // Sum of one value per warp (warps may pass 0), identical in every thread.
@@ -473,10 +472,9 @@ struct EpiLogits {                // logits[r] = v, keep this lane's best (value
 // gains g ("The Forward Pass in Java", Example 4: y = (x * scale) * g with
 // scale = 1/sqrt(mean(x^2) + eps), the sum of squares a float tree sum).
 struct XSrc {
-    const float* x;               // nullptr: the embedding row (unless part is set)
+    const float* x;               // nullptr: the embedding row
     const float* g;               // nullptr: no norm
     int n;                        // length of the vector
-    const float* part;            // attention partials to merge (the O phase), or nullptr
 };
 
 // Lane layout of a plan: team, lane index within the team, row half (pair).
@@ -524,43 +522,9 @@ __device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& 
     if (((src.n + 31) & ~31) <= c.p.scratch_floats) {   // whole 32-float slices fit
         float4* xv = reinterpret_cast<float4*>(c.sm.xs());
         float ss = 0.f;
-        const int S = c.p.splits, MS = c.p.max_splits, hd = c.p.hd;
-        float* wgt = c.sm.comb();                   // [n_heads][S] merge weights
-        if (src.part) {
-            // Merge the attention splits of every head: M = max_s m_s,
-            // w_s = e^(m_s - M) / sum_s' e^(m_s' - M) l_s', out = sum_s w_s acc_s.
-            // One warp per head, one split per lane (S <= 32).
-            const float2* mlp = reinterpret_cast<const float2*>(src.part + (size_t)c.p.n_heads * MS * hd);
-            for (int h = c.warp; h < c.p.n_heads; h += kConsumerWarps) {
-                const bool has = c.lane < S;
-                const float2 mv = has ? __ldcg(mlp + (size_t)h * MS + c.lane) : make_float2(-INFINITY, 0.f);
-                const float M = warp_max(mv.x);
-                const float w = has && mv.x != -INFINITY ? expf(mv.x - M) : 0.f;
-                const float Ls = warp_sum(w * mv.y);
-                if (has) wgt[h * S + c.lane] = w / Ls;
-            }
-            consumer_sync();
-        }
         for (int i = c.tid; i < src.n / 4; i += kConsumers) {
             float4 v;
-            if (src.part) {
-                const int h = (4 * i) / hd, e = (4 * i) % hd;
-                const float4* a4 = reinterpret_cast<const float4*>(src.part + (size_t)h * MS * hd + e);
-                const float* wh = wgt + h * S;
-                v = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int s0 = 0; s0 < S; s0 += 8) {
-                    float4 t[8];
-#pragma unroll
-                    for (int k = 0; k < 8; k++)
-                        t[k] = s0 + k < S ? __ldcg(a4 + (size_t)(s0 + k) * (hd / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int k = 0; k < 8; k++) {
-                        const float w = s0 + k < S ? wh[s0 + k] : 0.f;
-                        v = make_float4(fmaf(w, t[k].x, v.x), fmaf(w, t[k].y, v.y), fmaf(w, t[k].z, v.z),
-                                        fmaf(w, t[k].w, v.w));
-                    }
-                }
-            } else if (src.x) {
+            if (src.x) {
                 v = __ldcg(reinterpret_cast<const float4*>(src.x) + i);
             } else {
                 v = make_float4(weight_at<DT>(c.p.embd, token, 4 * i), weight_at<DT>(c.p.embd, token, 4 * i + 1),
@@ -753,9 +717,10 @@ __device__ __forceinline__ void store_kv(__half* kc, __half* vc, int pos, int kv
 // the positions, weighted sum of the V rows).  The unit keeps a running max m
 // and sum l per head across its chunks (online softmax) and writes its partial
 // (m, l, acc): acc[h][d] at attn_part[(h*max_splits + s)*hd + d], (m, l) at
-// attn_part[n_heads*max_splits*hd + 2*(h*max_splits + s)].  The splits are
-// merged where the O phase stages its activation vector.
-__device__ bool attention_unit(Consumer& c, const LayerDev& L, int unit) {
+// attn_part[n_heads*max_splits*hd + 2*(h*max_splits + s)].  The last unit of
+// a kv head to finish merges its splits: per head M = max_s m_s,
+// w_s = e^(m_s - M) / sum_s' e^(m_s' - M) l_s', attn = sum_s w_s acc_s.
+__device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int unit) {
     const StepParams& p = c.p;
     Smem& sm = c.sm;
     const int tid = c.tid, warp = c.warp, lane = c.lane;
@@ -915,7 +880,43 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int unit) {
         __stcg(part_acc + hs * hd + ii, v);
         if (ii == 0) __stcg(reinterpret_cast<float2*>(part_ml) + hs, make_float2(ml[hh], ml[gq + hh]));
     }
-    consumer_sync();                                               // comb, scratch free for the next unit
+    consumer_sync();                                               // comb, scratch free
+    unsigned* mc = p.counters + n_phase_counters(p.n_layers) + layer * p.n_kv + g;
+    if (tid == 0) sm.misc()[1] = atom_add_acq_rel(mc, 1u) == (unsigned)(S - 1);
+    consumer_sync();
+    if (sm.misc()[1]) {
+        // weights per head, one warp per head and one split per lane (S <= 32)
+        const int MS = p.max_splits;
+        float* wgt = sm.comb();                                    // [gq][S]
+        if (warp < gq) {
+            const bool has = lane < S;
+            const float2 mv = has ? __ldcg(reinterpret_cast<const float2*>(part_ml) + (size_t)(h0 + warp) * MS + lane)
+                                  : make_float2(-INFINITY, 0.f);
+            const float M = warp_max(mv.x);
+            const float w = has && mv.x != -INFINITY ? expf(mv.x - M) : 0.f;
+            const float Ls = warp_sum(w * mv.y);
+            if (has) wgt[warp * S + lane] = w / Ls;
+        }
+        // every thread loads its elements' partial sums meanwhile (all splits at once)
+        for (int e0 = 0; e0 < GD; e0 += kConsumers) {
+            const int e = e0 + tid;
+            const int hh = e < GD ? e / hd : 0, ii = e < GD ? e % hd : 0;
+            const float* src = part_acc + (size_t)(h0 + hh) * MS * hd + ii;
+            float av[32];
+#pragma unroll
+            for (int k = 0; k < 32; k++) av[k] = e < GD && k < S ? __ldcg(src + (size_t)k * hd) : 0.f;
+            consumer_sync();                                       // weights ready
+            if (e < GD) {
+                float v = 0.f;
+#pragma unroll
+                for (int k = 0; k < 32; k++)
+                    if (k < S) v = fmaf(wgt[hh * S + k], av[k], v);
+                __stcg(p.attn + (h0 + hh) * hd + ii, v);
+            }
+        }
+        c.signal(p.counters + 5 * layer + 1);
+    }
+    consumer_sync();
     return true;
 }
 
@@ -948,7 +949,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         if (tid == 0) trace_mark(p, 10 * l);
         c.tk = 160 + 4 * l;
         {
-            const XSrc src{l == 0 ? nullptr : p.x, L.attn_norm, p.dim, nullptr};
+            const XSrc src{l == 0 ? nullptr : p.x, L.attn_norm, p.dim};
             EpiStore e{p.qkv, L.qkv_bias ? sm.bias() : nullptr, q0};
             gemv_consume<DT, false>(c, L.qkv, src, token, e);
         }
@@ -960,16 +961,15 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         {
             const int units = p.n_kv * p.splits;
             for (int unit = blockIdx.x; unit < units; unit += G)
-                if (!attention_unit(c, L, unit)) return false;
+                if (!attention_unit(c, L, l, unit)) return false;
         }
-        c.signal(ctr + 1);
         if (tid == 0) trace_mark(p, 10 * l + 3);
         // ---- O
-        if (!c.wait_counter(ctr + 1, G)) return false;
+        if (!c.wait_counter(ctr + 1, p.n_kv)) return false;
         if (tid == 0) trace_mark(p, 10 * l + 4);
         c.tk = 160 + 4 * l + 1;
         {
-            const XSrc src{nullptr, nullptr, p.q_dim, p.attn_part};
+            const XSrc src{p.attn, nullptr, p.q_dim};
             EpiResidual e{p.x, sm.xown(), c.own0};
             gemv_consume<DT, false>(c, L.o, src, token, e);
         }
@@ -980,7 +980,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         if (tid == 0) trace_mark(p, 10 * l + 6);
         c.tk = 160 + 4 * l + 2;
         {
-            const XSrc src{p.x, L.ffn_norm, p.dim, nullptr};
+            const XSrc src{p.x, L.ffn_norm, p.dim};
             int i0, i1;
             cta_rows(L.gu.rows, i0, i1);
             EpiSwiGLU e{p.u, sm.bias(), i0, i1};
@@ -993,7 +993,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         if (tid == 0) trace_mark(p, 10 * l + 8);
         c.tk = 160 + 4 * l + 3;
         {
-            const XSrc src{p.u, nullptr, p.ffn, nullptr};
+            const XSrc src{p.u, nullptr, p.ffn};
             EpiResidual e{p.x, sm.xown(), c.own0};
             gemv_consume<DT, false>(c, L.down, src, token, e);
         }
@@ -1007,7 +1007,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
     c.tk = -1;
     EpiLogits e{p.logits, 0ull};
     {
-        const XSrc src{p.x, p.out_norm, p.dim, nullptr};
+        const XSrc src{p.x, p.out_norm, p.dim};
         gemv_consume<DT, false>(c, p.out, src, token, e);
     }
     if (tid == 0) trace_mark(p, 241);
@@ -1033,7 +1033,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         __threadfence();
         if (tid == 0) *p.token_out = argmax_key_index(atomicExch(p.best, 0ull));
         if (tid == 0) trace_mark(p, 242);
-        const int nc = n_phase_counters(p.n_layers);
+        const int nc = n_phase_counters(p.n_layers) + p.n_layers * p.n_kv;
         for (int i = tid; i < nc; i += kConsumers) p.counters[i] = 0u;
     }
     return true;

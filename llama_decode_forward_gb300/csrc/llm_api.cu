@@ -330,14 +330,13 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
 
     // ---- activations
     // position splits per kv head: enough units to cover every SM, at most 32
-    // (the merge takes one split per lane) and at most 2*480 merge weights
+    // (the merge takes one split per lane)
     {
         int ms = h->sms / c.n_kv_heads;
         if (ms > 32) ms = 32;
-        if (ms > 2 * kConsumers / c.n_heads) ms = 2 * kConsumers / c.n_heads;
         h->max_splits = ms > 1 ? ms : 1;
     }
-    h->n_counters = n_phase_counters(L);
+    h->n_counters = n_phase_counters(L) + L * c.n_kv_heads;
     size_t a = 0;
     auto take = [&](size_t b) { size_t o = a; a += align256(b); return o; };
     const size_t o_x = take((size_t)d * 4), o_qkv = take((size_t)(q + 2 * kv) * 4), o_attn = take((size_t)q * 4),

@@ -54,8 +54,8 @@ struct LayerDev {
     __half* vc;
 };
 
-// Counters of one step: 5 phases per layer + the logits phase.  All zero
-// between steps.
+// Counters of one step: 5 phases per layer + the logits phase, then one merge
+// counter per (layer, kv head).  All zero between steps.
 struct StepParams {
     const LayerDev* layers;
     const void* kv_maps;      // CUtensorMap[2 * n_layers]: K and V cache of each layer, box [attn_rows][hd]
@@ -129,6 +129,13 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Atomic add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
