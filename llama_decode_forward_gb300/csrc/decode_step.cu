@@ -74,8 +74,8 @@ struct Smem {
     __device__ __forceinline__ uint8_t* ring() const { return base; }
     // attention scratch, and the staged activation vector of a GEMV phase (scratch_floats floats)
     __device__ __forceinline__ float* xs() const { return reinterpret_cast<float*>(base + p.off_xs); }
-    // [kMaxTeams][2][kConsumerWarps][2] partial dots of multi-warp teams
-    __device__ __forceinline__ float* tpart() const { return reinterpret_cast<float*>(base + p.off_red); }
+    // [rows of this CTA][warps of a team] partial dots of multi-warp teams
+    __device__ __forceinline__ float* rowp() const { return reinterpret_cast<float*>(base + p.off_red); }
     __device__ __forceinline__ float* rope_c() const { return reinterpret_cast<float*>(base + p.off_rope); }
     __device__ __forceinline__ float* rope_s() const { return rope_c() + 128; }
     // [2 * kConsumers] attention split combine
@@ -590,9 +590,10 @@ __device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& 
 
 // The CTA's rows of m, chunk by chunk from the ring (the plan in DMat).
 // Multi-warp teams take two rows per pass: their partial dots are reduced with
-// one butterfly (lanes 0-15 for the first row, 16-31 for the second), then the
-// team meets at its named barrier, and lanes 0 and 16 of the team's first warp
-// add the warps' parts of the two rows.
+// one butterfly (lanes 0-15 for the first row, 16-31 for the second) and each
+// warp parks its part of the two rows in shared memory; after the last chunk
+// the consumers finish all rows at once (parts added in warp order, so the
+// result does not depend on timing) and apply the phase's epilogue.
 template <int DT, bool PAIR, class Epi>
 __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const XSrc& src, int token, Epi& epi) {
     constexpr int ES = DT == LLM_Q8_0 ? 1 : (DT == LLM_F16 ? 2 : 4);
@@ -607,7 +608,6 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
     const int rowq = row_qbytes(m, DT);
     const int rowd = DT == LLM_Q8_0 ? 2 * m.dstride : 0;
     const int xoff = L.col0 * ES, soff = L.clit * 2;
-    int pass = 0;
     for (int r = r0; r < r1; r += m.rpc) {
         const int n = min(m.rpc, r1 - r);
         int slot;
@@ -634,7 +634,10 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
                 }
             }
         } else if (L.active) {
-            const int wpr = tw / 32;
+            // whole-warp teams: two rows per pass; each warp parks its part of
+            // the two rows' dots, the rows are finished after the last chunk
+            const int wpr = tw / 32, wi = c.warp % wpr;
+            float* rp = c.sm.rowp() + (size_t)(r - r0) * wpr + wi;
             for (int j = 0; L.team + 2 * j * teams < n; j++) {
                 const int ra = L.team + 2 * j * teams, rb = ra + teams;
                 const bool hasb = rb < n;
@@ -647,27 +650,29 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
                 keep += __shfl_xor_sync(0xffffffffu, send, 16);
 #pragma unroll
                 for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
-                float* tp = c.sm.tpart() + ((L.team * 2 + (pass & 1)) * kConsumerWarps) * 2;
-                if ((c.lane & 15) == 0) tp[(c.warp % wpr) * 2 + (c.lane >> 4)] = keep;
-                asm volatile("bar.sync %0, %1;" ::"r"(3 + L.team), "r"(tw) : "memory");
-                if ((L.lit & ~16) == 0 && (L.lit == 0 || hasb)) {
-                    const int h = L.lit >> 4;
-                    const int row = r + (h ? rb : ra);
-                    if constexpr (PAIR) {
-                        float g = 0.f, up = 0.f;
-                        for (int k = 0; k < wpr / 2; k++) g += tp[2 * k + h];
-                        for (int k = wpr / 2; k < wpr; k++) up += tp[2 * k + h];
-                        epi.pair(row, g, up);
-                    } else {
-                        float t = 0.f;
-                        for (int k = 0; k < wpr; k++) t += tp[2 * k + h];
-                        epi.row(row, t);
-                    }
-                }
-                pass++;
+                if (c.lane == 0) rp[ra * wpr] = keep;
+                if (c.lane == 16 && hasb) rp[rb * wpr] = keep;
             }
         }
         c.release(slot);
+    }
+    if (tw > 32) {
+        // finish every row: the warps' parts added in warp order
+        const int wpr = tw / 32;
+        consumer_sync();
+        const float* rp = c.sm.rowp();
+        for (int i = c.tid; i < r1 - r0; i += kConsumers) {
+            if constexpr (PAIR) {
+                float g = 0.f, up = 0.f;
+                for (int k = 0; k < wpr / 2; k++) g += rp[i * wpr + k];
+                for (int k = wpr / 2; k < wpr; k++) up += rp[i * wpr + k];
+                epi.pair(r0 + i, g, up);
+            } else {
+                float t = 0.f;
+                for (int k = 0; k < wpr; k++) t += rp[i * wpr + k];
+                epi.row(r0 + i, t);
+            }
+        }
     }
     epi.finish(c);
 #ifdef LLM_TRACE
@@ -1116,7 +1121,7 @@ bool matrix_plan(DMat& m, int wtype, bool pair) {
 // Shared-memory geometry of the step kernel for a model.  Returns false if the
 // model does not fit the kernel's limits.
 bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int n_kv, int hd, int rope_dims,
-                   int max_splits, size_t* smem_bytes) {
+                   int rowp_floats, size_t* smem_bytes) {
     const int gq = n_heads / n_kv;
     int P = 8192 / hd;
     if (P > 256) P = 256;
@@ -1131,7 +1136,7 @@ bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int 
     size_t xs = attn_scratch;
     xs = xs > stage ? xs : stage;
     auto al = [](size_t b) { return (b + 127) & ~(size_t)127; };
-    const size_t tpart = sizeof(float) * kMaxTeams * 2 * kConsumerWarps * 2;
+    const size_t tpart = sizeof(float) * (size_t)rowp_floats;
     auto fixed_for = [&](size_t x) {
         return al(x) + al(tpart) + al(2 * 128 * 4) + al(2 * kConsumers * 4) + al(2 * kOwnFloats * 4) + 1024;
     };

@@ -15,7 +15,7 @@
 
 namespace llm {
 bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int n_kv, int hd, int rope_dims,
-                   int max_splits, size_t* smem_bytes);
+                   int rowp_floats, size_t* smem_bytes);
 bool matrix_plan(DMat& m, int wtype, bool pair);
 const void* step_kernel_ptr(int wtype);
 void launch_kv_store(cudaStream_t st, __half* kc, __half* vc, int pos, int kv_dim, const float* k, const float* v);
@@ -365,7 +365,17 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
     h->theta_scale = (float)pow((double)c.rope_base, -2.0 / (double)c.rope_dims);
     h->attn_div = (float)sqrt((double)c.head_dim);
     h->kernel = step_kernel_ptr(c.wtype);
-    if (!step_geometry(h->geo, d, q, f, c.n_heads, c.n_kv_heads, c.head_dim, c.rope_dims, h->max_splits,
+    // row partials a CTA keeps for one GEMV phase: its rows times the warps of a team
+    int rowp_floats = 0;
+    {
+        const DMat* mats[5] = {&h->layers[0].qkv, &h->layers[0].o, &h->layers[0].gu, &h->layers[0].down, &h->out};
+        for (const DMat* m : mats) {
+            const int rows = (m->rows + h->sms - 1) / h->sms;
+            const int parts = m->tw > 32 ? m->tw / 32 : 1;
+            if (rows * parts > rowp_floats) rowp_floats = rows * parts;
+        }
+    }
+    if (!step_geometry(h->geo, d, q, f, c.n_heads, c.n_kv_heads, c.head_dim, c.rope_dims, rowp_floats,
                        &h->smem)) {
         free_handle(h);
         return LLM_ERR_UNSUPPORTED;

@@ -110,7 +110,7 @@ __host__ __device__ inline int dtype_bytes_x16(int wtype) {   // bytes per eleme
 }
 
 constexpr int kLaneElems = 32;                     // matrix columns one lane covers per row
-constexpr int kMaxTeams = 7;                       // multi-warp teams (named barriers 3..9)
+constexpr int kMaxTeams = 7;                       // multi-warp teams of one GEMV phase
 constexpr int kOwnFloats = 256;                    // residual rows a CTA owns, and its QKV bias rows
 
 // Bytes of one row in a ring slot (quants/values plus Q8_0 scales).
