@@ -171,6 +171,32 @@ int llm_test_dequant_rows(llm_handle *h, int which, int layer, int32_t row0, int
  * LLM_TRACE record stamps; others return LLM_ERR_UNSUPPORTED.  Synchronous. */
 int llm_trace_read(llm_handle *h, uint64_t *host, int32_t *sms);
 
+/* One decode step like llm_decode_step_async, but its working memory (the
+ * residual stream, q/k/v, attention partials, FFN activations, grid counters,
+ * argmax and error words) lives in a fixed 4 MiB device array inside the
+ * library rather than in buffers of the handle, so the call allocates no
+ * memory of any kind.  The described decode pass has no counterpart of this
+ * call: it exists for callers that may not allocate device memory while
+ * serving (a process whose remaining device memory is owned by its own pool
+ * and cannot grow after start-up).
+ *   token_dev   DEVICE int32, the input token (read by the kernel).
+ *   pos         position of the token, in [0, max_seq).
+ *   logits_dev  DEVICE float[vocab], written with the step's logits.
+ *   argmax_dev  DEVICE int32, written with the first index of the max logit.
+ * The handle's KV cache row `pos` is written as by llm_decode_step.
+ * Synchronous: returns after the step has finished on the handle's stream.
+ * Errors: LLM_ERR_INVALID_ARG for NULL pointers, LLM_ERR_OUT_OF_RANGE for a
+ * bad pos (or a device-side token out of range, after which the handle needs
+ * llm_reset), LLM_ERR_UNSUPPORTED when the model's step needs more than the
+ * fixed array holds (the message gives both sizes), LLM_ERR_DEVICE_TIMEOUT
+ * if a bounded device wait expired.
+ * The first call on a device looks up the array's address; make it before
+ * any stream capture starts.  The array is shared by every handle on the
+ * device: calls that overlap in time race on it and must be serialised by
+ * the caller. */
+int llm_decode_step_noalloc(llm_handle *h, const int32_t *token_dev, int32_t pos, float *logits_dev,
+                            int32_t *argmax_dev);
+
 /* Number of kernel launches enqueued on the handle's stream so far (all calls). */
 int64_t llm_launch_count(const llm_handle *h);
 

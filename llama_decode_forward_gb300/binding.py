@@ -51,6 +51,7 @@ _SIGS = {
     "llm_test_kv_store": ([_vp, _int, _i32, _vp, _vp], _int),
     "llm_test_dequant_rows": ([_vp, _int, _int, _i32, _i32, _vp], _int),
     "llm_trace_read": ([_vp, _vp, ctypes.POINTER(_i32)], _int),
+    "llm_decode_step_noalloc": ([_vp, _vp, _i32, _vp, _vp], _int),
     "llm_launch_count": ([_vp], ctypes.c_int64),
     "llm_destroy": ([_vp], None),
     "llm_status_string": ([_int], ctypes.c_char_p),
@@ -156,6 +157,13 @@ def llm_test_kv_store(h, layer: int, pos: int, k_dev, v_dev):
 
 def llm_test_dequant_rows(h, which: int, layer: int, row0: int, n_rows: int, out_dev):
     _check(_lib.llm_test_dequant_rows(h, which, layer, row0, n_rows, _ptr(out_dev)), h)
+
+
+def llm_decode_step_noalloc(h, token_dev, pos: int, logits_dev, argmax_dev):
+    """One decode step that allocates nothing: its working memory is a fixed
+    device array of the library (for callers that may not allocate device
+    memory while serving).  All three buffers are device tensors; synchronous."""
+    _check(_lib.llm_decode_step_noalloc(h, _ptr(token_dev), int(pos), _ptr(logits_dev), _ptr(argmax_dev)), h)
 
 
 def llm_trace_read(h) -> np.ndarray:

@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -616,3 +617,119 @@ extern "C" const char* llm_status_string(int s) {
 }
 
 extern "C" const char* llm_last_error(const llm_handle* h) { return h ? h->last_error.c_str() : ""; }
+
+// ------------------------------------------------------- no-alloc step --
+// A decode step whose working memory (residual stream, q/k/v, attention
+// output and split partials, FFN activations, grid counters, argmax and error
+// words) comes from one fixed device array of this library instead of
+// buffers of the handle.  It is for callers that must not allocate device
+// memory while serving: a process that has handed the rest of the device to
+// its own pool (KV pages, other models) and runs out of room or is not
+// allowed to grow after start-up.  The call itself allocates nothing (no
+// cudaMalloc, no cudaFree, no allocating library routine); the handle's
+// weights, KV cache and pinned host words were set up by llm_create.
+//
+// The array is shared by every handle on a device, so calls that overlap in
+// time (other threads, other streams, other handles on the same device) race
+// on it and must be serialised by the caller.  The first call on a device
+// looks up the array's address (cudaGetSymbolAddress, with that device
+// current); make that first call before any stream capture begins.
+constexpr size_t kStaticScratchBytes = (size_t)4 << 20;   // 4 MiB
+static __device__ __align__(256) unsigned char g_step_scratch[kStaticScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+
+size_t scratch_align(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Scratch layout of a handle's step: offsets in bytes, total in *bytes.
+struct ScratchLayout {
+    size_t x, qkv, attn, u, part, best, counters, err, total;
+};
+
+ScratchLayout scratch_layout(const llm_handle* h) {
+    const llm_config& c = h->cfg;
+    ScratchLayout s{};
+    size_t o = 0;
+    auto take = [&](size_t b) { size_t at = o; o += scratch_align(b); return at; };
+    s.x = take((size_t)c.dim * 4);
+    s.qkv = take((size_t)(h->q_dim + 2 * h->kv_dim) * 4);
+    s.attn = take((size_t)h->q_dim * 4);
+    s.u = take((size_t)c.ffn_dim * 4);
+    s.part = take((size_t)c.n_heads * h->max_splits * (c.head_dim + 2) * 4);
+    s.best = take(8);                                   // these three must start at zero
+    s.counters = take((size_t)h->n_counters * 4);
+    s.err = take(4);
+    s.total = o;
+    return s;
+}
+}  // namespace
+
+extern "C" int llm_decode_step_noalloc(llm_handle* h, const int32_t* token_dev, int32_t pos, float* logits_dev,
+                                       int32_t* argmax_dev) {
+    if (!h) return LLM_ERR_INVALID_ARG;
+    if (!token_dev || !logits_dev || !argmax_dev) return fail(h, LLM_ERR_INVALID_ARG, "NULL argument");
+    if (h->broken) return fail(h, LLM_ERR_STATE, "handle has a device error; call llm_reset");
+    if (pos < 0 || pos >= h->cfg.max_seq) return fail(h, LLM_ERR_OUT_OF_RANGE, "pos %d not in [0, %d)", pos, h->cfg.max_seq);
+    if (h->device < 0 || h->device >= kMaxDevices) return fail(h, LLM_ERR_UNSUPPORTED, "device %d", h->device);
+    const ScratchLayout sl = scratch_layout(h);
+    if (sl.total > kStaticScratchBytes)
+        return fail(h, LLM_ERR_UNSUPPORTED, "this model's step needs %zu bytes of scratch; the static scratch holds %zu",
+                    sl.total, kStaticScratchBytes);
+    unsigned char* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        if (!g_scratch_addr[h->device]) {
+            int prev = -1;
+            CK(h, cudaGetDevice(&prev));
+            if (prev != h->device) CK(h, cudaSetDevice(h->device));
+            void* a = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&a, g_step_scratch);
+            if (prev != h->device) cudaSetDevice(prev);
+            if (e != cudaSuccess || !a)
+                return fail(h, LLM_ERR_CUDA, "cudaGetSymbolAddress of the step scratch: %s", cudaGetErrorString(e));
+            g_scratch_addr[h->device] = a;
+        }
+        base = static_cast<unsigned char*>(g_scratch_addr[h->device]);
+    }
+    // argmax key, grid counters and error word start at zero (contiguous)
+    CK(h, cudaMemsetAsync(base + sl.best, 0, sl.err + 4 - sl.best, h->st));
+
+    const llm_config& c = h->cfg;
+    StepParams p = h->geo;
+    p.layers = h->d_layers;
+    p.kv_maps = h->kv_maps;
+    p.trace = nullptr;
+    p.embd = h->embd;
+    p.out = h->out;
+    p.out_norm = h->out_norm;
+    p.rope_freqs = h->rope_freqs;
+    p.n_layers = c.n_layers; p.dim = c.dim; p.n_heads = c.n_heads; p.n_kv = c.n_kv_heads; p.hd = c.head_dim;
+    p.ffn = c.ffn_dim; p.vocab = c.vocab; p.max_seq = c.max_seq; p.rope_dims = c.rope_dims; p.neox = c.rope_neox;
+    p.q_dim = h->q_dim; p.kv_dim = h->kv_dim;
+    p.eps = c.eps; p.theta_scale = h->theta_scale; p.attn_div = h->attn_div;
+    p.x = reinterpret_cast<float*>(base + sl.x);
+    p.qkv = reinterpret_cast<float*>(base + sl.qkv);
+    p.attn = reinterpret_cast<float*>(base + sl.attn);
+    p.u = reinterpret_cast<float*>(base + sl.u);
+    p.logits = logits_dev;
+    p.attn_part = reinterpret_cast<float*>(base + sl.part);
+    p.max_splits = h->max_splits;
+    p.best = reinterpret_cast<unsigned long long*>(base + sl.best);
+    p.counters = reinterpret_cast<unsigned*>(base + sl.counters);
+    p.err = reinterpret_cast<int*>(base + sl.err);
+    p.token_in = token_dev; p.token_out = argmax_dev; p.pos = pos;
+    const int s = (pos + 1 + 15) / 16;
+    p.splits = s < 1 ? 1 : (s > h->max_splits ? h->max_splits : s);
+    void* args[] = {&p};
+    CK(h, cudaLaunchCooperativeKernel(h->kernel, dim3(h->sms), dim3(kBlock), args, h->smem, h->st));
+    h->launches++;
+    CK(h, cudaMemcpyAsync(&h->pinned->err, base + sl.err, 4, cudaMemcpyDeviceToHost, h->st));
+    CK(h, cudaStreamSynchronize(h->st));
+    const int e = h->pinned->err;
+    if (e & kErrTimeout) { h->broken = true; return fail(h, LLM_ERR_DEVICE_TIMEOUT, "a bounded device wait expired"); }
+    if (e & kErrToken) { h->broken = true; return fail(h, LLM_ERR_OUT_OF_RANGE, "the device-side token was out of range"); }
+    return LLM_OK;
+}
