@@ -83,6 +83,8 @@ struct Smem {
     // [kOwnFloats] residual rows this CTA owns, then [kOwnFloats] its QKV bias rows
     __device__ __forceinline__ float* xown() const { return reinterpret_cast<float*>(base + p.off_own); }
     __device__ __forceinline__ float* bias() const { return xown() + kOwnFloats; }
+    // the next RMSNorm's gains, fetched ahead of their phase (swizzled like the staged vector)
+    __device__ __forceinline__ float* gains() const { return reinterpret_cast<float*>(base + p.off_gain); }
     __device__ __forceinline__ uint64_t* full() const { return reinterpret_cast<uint64_t*>(base + p.off_bar); }
     __device__ __forceinline__ uint64_t* empty() const { return full() + p.ns; }
     __device__ __forceinline__ int* misc() const { return reinterpret_cast<int*>(base + p.off_misc); }   // [0] abort, [1] flag
@@ -283,6 +285,16 @@ struct Consumer {
         if (tid == 0) red_release_add(c, 1u);
     }
 
+    // Start copying a norm's gains (n floats, n % 4 == 0) into shared memory;
+    // lane_x waits for them.  Each 16-byte word w lands at the swizzled word
+    // (w & ~7) + ((w & 7) ^ ((w >> 3) & 7)), as the staged vectors do.
+    __device__ void prefetch_gains(const float* g, int n) {
+        float4* dst = reinterpret_cast<float4*>(sm.gains());
+        for (int i = tid; i < n / 4; i += kConsumers)
+            cp_async16(dst + (i & ~7) + ((i & 7) ^ ((i >> 3) & 7)), reinterpret_cast<const float4*>(g) + i);
+        cp_async_commit();
+    }
+
     // Sum of one value per warp (warps may pass 0), identical in every thread.
     __device__ float warps_total(float v) {
         v = warp_sum(v);
@@ -380,35 +392,41 @@ __device__ __forceinline__ float lane_row(const uint8_t* w, const uint8_t* scale
     return t;
 }
 
-// Two rows at once: every shared-memory word of both rows is loaded before
-// the arithmetic starts, so the load latency is paid once.
+// Rows a multi-warp team reduces per pass: four for Q8_0 (two 16-byte words
+// per lane and row), two for the wider F16 and F32 rows (register budget).
 template <int DT>
-__device__ __forceinline__ void lane_row2(const uint8_t* wa, const uint8_t* sa, const uint8_t* wb, const uint8_t* sb,
-                                          const float2 (&x2)[16], int nseg, float& va, float& vb) {
+struct RowsPerPass {
+    static constexpr int value = DT == LLM_Q8_0 ? 4 : 2;
+};
+
+// N rows at once: every shared-memory word of the N rows is loaded before the
+// arithmetic starts, so the load latency is paid once.
+template <int DT, int N>
+__device__ __forceinline__ void lane_rows(const uint8_t* const (&w)[N], const uint8_t* const (&sc)[N],
+                                          const float2 (&x2)[16], int nseg, float (&v)[N]) {
     constexpr int NS = LaneDot<DT>::kSeg;
-    uint4 a[NS], b[NS];
+    uint4 a[N][NS];
 #pragma unroll
-    for (int s = 0; s < NS; s++) {
-        a[s] = s < nseg ? reinterpret_cast<const uint4*>(wa)[s] : make_uint4(0u, 0u, 0u, 0u);
-        b[s] = s < nseg ? reinterpret_cast<const uint4*>(wb)[s] : make_uint4(0u, 0u, 0u, 0u);
-    }
-    float da = 1.f, db = 1.f;
+    for (int r = 0; r < N; r++)
+#pragma unroll
+        for (int s = 0; s < NS; s++)
+            a[r][s] = s < nseg ? reinterpret_cast<const uint4*>(w[r])[s] : make_uint4(0u, 0u, 0u, 0u);
+    float dsc[N];
+#pragma unroll
+    for (int r = 0; r < N; r++) dsc[r] = 1.f;
     if constexpr (DT == LLM_Q8_0) {
         if (nseg) {
-            da = __half2float(*reinterpret_cast<const __half*>(sa));
-            db = __half2float(*reinterpret_cast<const __half*>(sb));
+#pragma unroll
+            for (int r = 0; r < N; r++) dsc[r] = __half2float(*reinterpret_cast<const __half*>(sc[r]));
         }
     }
-    float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
-    LaneDot<DT>::acc(a, x2, a0, a1);
-    LaneDot<DT>::acc(b, x2, b0, b1);
-    const float ta = (a0.x + a0.y) + (a1.x + a1.y), tb = (b0.x + b0.y) + (b1.x + b1.y);
-    if constexpr (DT == LLM_Q8_0) {
-        va = nseg ? da * ta : 0.f;
-        vb = nseg ? db * tb : 0.f;
-    } else {
-        va = ta;
-        vb = tb;
+#pragma unroll
+    for (int r = 0; r < N; r++) {
+        float2 c0 = make_float2(0.f, 0.f), c1 = c0;
+        LaneDot<DT>::acc(a[r], x2, c0, c1);
+        const float t = (c0.x + c0.y) + (c1.x + c1.y);
+        if constexpr (DT == LLM_Q8_0) v[r] = nseg ? dsc[r] * t : 0.f;
+        else v[r] = t;
     }
 }
 
@@ -534,6 +552,7 @@ __device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& 
             xv[(i & ~7) + ((i & 7) ^ ((i >> 3) & 7))] = v;
         }
         if (src.g) {
+            cp_async_wait_all();                         // this thread's part of the gains (fetched ahead)
             const float tot = c.warps_total(ss);        // synchronises the consumers
             scale = 1.0f / sqrtf(tot / (float)src.n + c.p.eps);
         } else {
@@ -545,6 +564,17 @@ __device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& 
             const float4 v = have && col0 + 4 * k < src.n ? x4[k ^ (L.clit & 7)] : make_float4(0.f, 0.f, 0.f, 0.f);
             x2[2 * k] = make_float2(v.x, v.y);
             x2[2 * k + 1] = make_float2(v.z, v.w);
+        }
+        if (src.g) {
+            const float4* g4 = reinterpret_cast<const float4*>(c.sm.gains()) + L.clit * 8;
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                const float4 g = have && col0 + 4 * k < src.n ? g4[k ^ (L.clit & 7)] : make_float4(0.f, 0.f, 0.f, 0.f);
+                x2[2 * k] = make_float2(__fmul_rn(__fmul_rn(x2[2 * k].x, scale), g.x),
+                                        __fmul_rn(__fmul_rn(x2[2 * k].y, scale), g.y));
+                x2[2 * k + 1] = make_float2(__fmul_rn(__fmul_rn(x2[2 * k + 1].x, scale), g.z),
+                                            __fmul_rn(__fmul_rn(x2[2 * k + 1].y, scale), g.w));
+            }
         }
     } else {
         if (src.x) {
@@ -571,12 +601,12 @@ __device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& 
 #pragma unroll
                 for (int k = 0; k < 16; k++) ss += x2[k].x * x2[k].x + x2[k].y * x2[k].y;
             }
+            cp_async_wait_all();
             const float tot = c.warps_total(ss);
             scale = 1.0f / sqrtf(tot / (float)src.n + c.p.eps);
         }
-    }
-    if (src.g) {
-        const float4* g4 = reinterpret_cast<const float4*>(src.g + col0);
+        if (src.g) {
+            const float4* g4 = reinterpret_cast<const float4*>(src.g + col0);
 #pragma unroll
         for (int k = 0; k < 8; k++) {
             const float4 g = have && col0 + 4 * k < src.n ? __ldg(g4 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -584,6 +614,7 @@ __device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& 
                                     __fmul_rn(__fmul_rn(x2[2 * k].y, scale), g.y));
             x2[2 * k + 1] = make_float2(__fmul_rn(__fmul_rn(x2[2 * k + 1].x, scale), g.z),
                                         __fmul_rn(__fmul_rn(x2[2 * k + 1].y, scale), g.w));
+            }
         }
     }
 }
@@ -634,24 +665,44 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
                 }
             }
         } else if (L.active) {
-            // whole-warp teams: two rows per pass; each warp parks its part of
-            // the two rows' dots, the rows are finished after the last chunk
+            // whole-warp teams: RPP consecutive rows per pass; each warp parks
+            // its part of the rows' dots, the rows are finished after the last
+            // chunk.  A transposed butterfly reduces the RPP values at once:
+            // lanes 8k..8k+7 (RPP 4) or 16k..16k+15 (RPP 2) end with row k.
+            constexpr int RPP = RowsPerPass<DT>::value;
             const int wpr = tw / 32, wi = c.warp % wpr;
             float* rp = c.sm.rowp() + (size_t)(r - r0) * wpr + wi;
-            for (int j = 0; L.team + 2 * j * teams < n; j++) {
-                const int ra = L.team + 2 * j * teams, rb = ra + teams;
-                const bool hasb = rb < n;
-                const int ma = ra * per + L.hsel, mb = (hasb ? rb : ra) * per + L.hsel;
-                float va, vb;
-                lane_row2<DT>(buf + (size_t)ma * rowq + xoff, sbase + ma * rowd + soff, buf + (size_t)mb * rowq + xoff,
-                              sbase + mb * rowd + soff, x2, L.nseg, va, vb);
-                float keep = c.lane < 16 ? va : vb;
-                const float send = c.lane < 16 ? vb : va;
-                keep += __shfl_xor_sync(0xffffffffu, send, 16);
+            for (int j = 0;; j++) {
+                const int rbase = (L.team + j * teams) * RPP;
+                if (rbase >= n) break;
+                const uint8_t* wq[RPP];
+                const uint8_t* ws[RPP];
 #pragma unroll
-                for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
-                if (c.lane == 0) rp[ra * wpr] = keep;
-                if (c.lane == 16 && hasb) rp[rb * wpr] = keep;
+                for (int k = 0; k < RPP; k++) {
+                    const int mr = min(rbase + k, n - 1) * per + L.hsel;
+                    wq[k] = buf + (size_t)mr * rowq + xoff;
+                    ws[k] = sbase + mr * rowd + soff;
+                }
+                float v[RPP];
+                lane_rows<DT, RPP>(wq, ws, x2, L.nseg, v);
+                float keep;
+                if constexpr (RPP == 4) {
+                    const bool u16 = (c.lane & 16) != 0;
+                    const float a0 = (u16 ? v[2] : v[0]) + __shfl_xor_sync(0xffffffffu, u16 ? v[0] : v[2], 16);
+                    const float a1 = (u16 ? v[3] : v[1]) + __shfl_xor_sync(0xffffffffu, u16 ? v[1] : v[3], 16);
+                    const bool u8 = (c.lane & 8) != 0;
+                    keep = (u8 ? a1 : a0) + __shfl_xor_sync(0xffffffffu, u8 ? a0 : a1, 8);
+#pragma unroll
+                    for (int o = 4; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+                } else {
+                    keep = c.lane < 16 ? v[0] : v[1];
+                    keep += __shfl_xor_sync(0xffffffffu, c.lane < 16 ? v[1] : v[0], 16);
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+                }
+                constexpr int G = 32 / RPP;                    // lanes holding one row's sum
+                const int k = RPP == 4 ? (c.lane >> 4) * 2 + ((c.lane >> 3) & 1) : c.lane >> 4;
+                if ((c.lane & (G - 1)) == 0 && rbase + k < n) rp[(rbase + k) * wpr] = keep;
             }
         }
         c.release(slot);
@@ -935,6 +986,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, kErrToken);
         token = 0;
     }
+    c.prefetch_gains(p.layers[0].attn_norm, p.dim);
     rope_table(p, sm, tid);
     // this CTA's residual rows start as the embedding row's values
     for (int i = c.own0 + tid; i < c.own1; i += kConsumers) {
@@ -960,6 +1012,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         }
         if (tid == 0) trace_mark(p, 10 * l + 1);
         c.signal(ctr + 0);
+        c.prefetch_gains(L.ffn_norm, p.dim);             // QKV has read its gains
         // ---- ATTN
         if (!c.wait_counter(ctr + 0, G)) return false;
         if (tid == 0) trace_mark(p, 10 * l + 2);
@@ -993,6 +1046,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         }
         if (tid == 0) trace_mark(p, 10 * l + 7);
         c.signal(ctr + 3);
+        c.prefetch_gains(l + 1 < p.n_layers ? p.layers[l + 1].attn_norm : p.out_norm, p.dim);
         // ---- DOWN
         if (!c.wait_counter(ctr + 3, G)) return false;
         if (tid == 0) trace_mark(p, 10 * l + 8);
@@ -1105,7 +1159,7 @@ bool matrix_plan(DMat& m, int wtype, bool pair) {
         if (tw / 32 > kConsumerWarps) return false;
         teams = kConsumerWarps / (tw / 32);
         if (teams > kMaxTeams) teams = kMaxTeams;
-        rows_per_pass = 2 * teams;
+        rows_per_pass = (wtype == LLM_Q8_0 ? 4 : 2) * teams;
     }
     const int per = pair ? 2 : 1;
     const int slot_rows = kSlotBytes / (per * slot_row_bytes(wtype, m.cols, m.dstride));
@@ -1123,26 +1177,32 @@ bool matrix_plan(DMat& m, int wtype, bool pair) {
 bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int n_kv, int hd, int rope_dims,
                    int rowp_floats, size_t* smem_bytes) {
     const int gq = n_heads / n_kv;
-    int P = 8192 / hd;
+    // KV rows per slot: K and V tiles of P rows fill a slot, at most 256 (a TMA
+    // box side), and the unit's scores (2 * gq * P floats) stay within 8 KB
+    int P = kSlotBytes / (4 * hd);
     if (P > 256) P = 256;
+    if (P > 1024 / gq) P = 1024 / gq;
     P &= ~7;
+    if (P < 8) return false;
     const int GD = gq * hd;
     const size_t attn_scratch = sizeof(float) * (size_t)(GD + hd + 2 * gq * P + 4 * gq) + 2 * sizeof(__half) * hd;
     // the scratch region also stages the activation vectors of the GEMV
     // phases: always those of length dim and q_dim, the FFN one as well when
-    // that still leaves six ring slots
+    // that still leaves a 192 KB ring
     auto slices = [](int n) { return (size_t)((n + 31) & ~31) * sizeof(float); };
     const size_t stage = slices(dim > q_dim ? dim : q_dim);
     size_t xs = attn_scratch;
     xs = xs > stage ? xs : stage;
     auto al = [](size_t b) { return (b + 127) & ~(size_t)127; };
     const size_t tpart = sizeof(float) * (size_t)rowp_floats;
+    const size_t gain_bytes = slices(dim);
     auto fixed_for = [&](size_t x) {
-        return al(x) + al(tpart) + al(2 * 128 * 4) + al(2 * kConsumers * 4) + al(2 * kOwnFloats * 4) + 1024;
+        return al(x) + al(tpart) + al(2 * 128 * 4) + al(2 * kConsumers * 4) + al(2 * kOwnFloats * 4) + al(gain_bytes) +
+               1024;
     };
     if (rope_dims / 2 > 128 || GD > 2 * kConsumers || GD % 2) return false;
     const size_t xs_ffn = xs > slices(ffn) ? xs : slices(ffn);
-    if (((long long)kMaxSmem - (long long)fixed_for(xs_ffn)) / kSlotBytes >= 6) xs = xs_ffn;
+    if (((long long)kMaxSmem - (long long)fixed_for(xs_ffn)) / kSlotBytes * kSlotBytes >= 196608) xs = xs_ffn;
     const size_t fixed = fixed_for(xs);
     long long ns = ((long long)kMaxSmem - (long long)fixed) / kSlotBytes;
     if (ns > 8) ns = 8;
@@ -1156,6 +1216,7 @@ bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int 
     p.off_rope = (int)off; off += al(2 * 128 * 4);
     p.off_comb = (int)off; off += al(2 * kConsumers * 4);
     p.off_own = (int)off; off += al(2 * kOwnFloats * 4);
+    p.off_gain = (int)off; off += al(gain_bytes);
     p.off_bar = (int)off; off += al(2 * ns * 8);
     p.off_misc = (int)off; off += 64 + 8 * (kConsumerWarps + 2) + 8 * kConsumerWarps;
     *smem_bytes = al(off);

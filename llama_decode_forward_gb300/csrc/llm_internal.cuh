@@ -14,7 +14,7 @@ namespace llm {
 constexpr int kConsumerWarps = 15;
 constexpr int kConsumers = kConsumerWarps * 32;   // 480
 constexpr int kBlock = kConsumers + 32;           // 512
-constexpr int kSlotBytes = 32768;                 // one ring slot (a chunk of weight rows or KV rows)
+constexpr int kSlotBytes = 65536;                 // one ring slot (a chunk of weight rows or KV rows)
 constexpr int kRedFloats = 1024;                  // row partials of one chunk
 constexpr int kMaxGroupDim = 2 * kConsumers;      // (n_heads / n_kv_heads) * head_dim per attention unit
 // 32-byte column blocks of a row one consumer thread owns: 2 for F16, else 1.
@@ -85,7 +85,7 @@ struct StepParams {
     // shared-memory geometry (bytes from the dynamic smem base)
     int ns;                   // ring slots
     int attn_rows;            // KV rows per ring slot
-    int off_xs, off_red, off_rope, off_comb, off_bar, off_misc, off_own;
+    int off_xs, off_red, off_rope, off_comb, off_bar, off_misc, off_own, off_gain;
     int scratch_floats;       // floats of the attention scratch region (xs)
 
     unsigned long long* trace;  // [gridDim.x][kTraceSlots] phase stamps, or nullptr (LLM_TRACE builds)
@@ -182,6 +182,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+
+// 16-byte asynchronous copy global -> shared (completes at cp_async_wait_all).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // 1-D bulk copy global -> shared, completing `bytes` on the mbarrier.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
