@@ -523,6 +523,38 @@ extern "C" int llm_prefill(llm_handle* h, const int32_t* tokens_host, int32_t n,
         if (tokens_host[i] < 0 || tokens_host[i] >= h->cfg.vocab)
             return fail(h, LLM_ERR_OUT_OF_RANGE, "token %d not in [0, %d)", tokens_host[i], h->cfg.vocab);
     int rc;
+    PrefillCtx pc{};
+    pc.st = h->st; pc.sms = h->sms; pc.wtype = h->cfg.wtype;
+    pc.n_layers = h->cfg.n_layers; pc.dim = h->cfg.dim; pc.n_heads = h->cfg.n_heads; pc.n_kv = h->cfg.n_kv_heads;
+    pc.hd = h->cfg.head_dim; pc.ffn = h->cfg.ffn_dim; pc.vocab = h->cfg.vocab; pc.rope_dims = h->cfg.rope_dims;
+    pc.neox = h->cfg.rope_neox; pc.q_dim = h->q_dim; pc.kv_dim = h->kv_dim;
+    pc.eps = h->cfg.eps; pc.theta_scale = h->theta_scale; pc.attn_div = h->attn_div;
+    pc.layers = h->layers.data(); pc.embd = h->embd; pc.out = h->out; pc.out_norm = h->out_norm;
+    pc.rope_freqs = h->rope_freqs; pc.logits = h->logits; pc.argmax_dev = h->tok_out; pc.best = h->best; pc.err = h->err;
+    if (prefill_supported(pc)) {
+        // F16 weights: tensor-core batches of up to kPrefillRows tokens
+        const size_t need = prefill_workspace_bytes(pc);
+        if (h->prefill_ws_bytes < need) {
+            cudaFree(h->prefill_ws);
+            h->prefill_ws = nullptr;
+            h->prefill_ws_bytes = 0;
+            CK(h, cudaMalloc(&h->prefill_ws, need));
+            h->prefill_ws_bytes = need;
+        }
+        const char* what = "";
+        const cudaError_t e = prefill_f16(pc, h->prefill_ws, tokens_host, n, pos0, &what);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(h, LLM_ERR_CUDA, "prefill (%s): %s", what, cudaGetErrorString(e));
+        }
+        h->launches += 1 + (int64_t)h->cfg.n_layers * 8 + 3;
+        CK(h, cudaMemcpyAsync(&h->pinned->argmax, h->tok_out, 4, cudaMemcpyDeviceToHost, h->st));
+        if (logits_host)
+            CK(h, cudaMemcpyAsync(logits_host, h->logits, (size_t)h->cfg.vocab * 4, cudaMemcpyDeviceToHost, h->st));
+        if ((rc = read_device_error(h))) return rc;
+        if (argmax_host) *argmax_host = h->pinned->argmax;
+        return LLM_OK;
+    }
     for (int i = 0; i < n - 1; i++) {
         h->pinned->token_in = tokens_host[i];
         CK(h, cudaMemcpyAsync(h->tok_in, &h->pinned->token_in, 4, cudaMemcpyHostToDevice, h->st));

@@ -105,6 +105,26 @@ constexpr int kTraceSlots = 1024;
 
 __host__ __device__ inline int n_phase_counters(int n_layers) { return 5 * n_layers + 1; }
 
+// Batched prefill (F16 weights): what it needs of a handle.
+constexpr int kPrefillRows = 512;            // tokens per tensor-core batch
+struct PrefillCtx {
+    cudaStream_t st;
+    int sms, wtype;
+    int n_layers, dim, n_heads, n_kv, hd, ffn, vocab, rope_dims, neox, q_dim, kv_dim;
+    float eps, theta_scale, attn_div;
+    const LayerDev* layers;                  // host array [n_layers] of device layouts
+    DMat embd, out;
+    const float* out_norm;
+    const float* rope_freqs;
+    float* logits;                           // [vocab]: the last token's logits
+    int* argmax_dev;                         // the last token's argmax
+    unsigned long long* best;                // argmax key, zero before and after
+    int* err;                                // device error word
+};
+bool prefill_supported(const PrefillCtx& c);
+size_t prefill_workspace_bytes(const PrefillCtx& c);
+cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_host, int n, int pos0, const char** msg);
+
 __host__ __device__ inline int dtype_bytes_x16(int wtype) {   // bytes per element, times 16
     return wtype == LLM_Q8_0 ? 16 : (wtype == LLM_F16 ? 32 : 64);
 }

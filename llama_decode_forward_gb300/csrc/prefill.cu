@@ -1,0 +1,499 @@
+// Batched prefill for F16 weights ("What a Llama model computes, and why",
+// §4: the same pass as the decode step, applied to n tokens at once; every
+// K/V row is written, token i attends to rows 0..pos0+i, and only the last
+// token's logits are produced).
+//
+// The projections are tensor-core GEMMs on the 5th-generation tensor cores:
+// C[M][N] = A[M][K] . W[N][K]^T with A the token rows (F16, rounded to
+// nearest even from the F32 activations) and W a weight matrix in the
+// library's row layout (F16, K contiguous), F32 accumulation in tensor
+// memory.  One CTA computes one 128 x 128 tile: thread 0 streams 128 x 64
+// tiles of A and W into a 4-stage ring with 2-D TMA (128-byte swizzle) and
+// issues tcgen05.mma (M 128, N 128, K 16) into a TMEM accumulator; the four
+// warps then read their 32 rows back with tcgen05.ld and apply the epilogue
+// (bias, residual add, or SwiGLU over the interleaved gate/up columns).
+//
+// The per-row steps (embedding, RMSNorm, RoPE + KV append, attention over the
+// cache, the last row's logits and argmax) are plain CUDA kernels.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <string>
+#include <vector>
+
+#include "llm_internal.cuh"
+
+namespace llm {
+
+namespace {
+
+constexpr int kGBM = 128, kGBN = 128, kGBK = 64, kGStages = 4;
+constexpr int kGABytes = kGBM * kGBK * 2, kGBBytes = kGBN * kGBK * 2, kGStageBytes = kGABytes + kGBBytes;
+constexpr int kGemmSmem = kGStages * kGStageBytes + 1024 + 256;
+constexpr long long kSpinLimit = 200000000ll;   // mbarrier polls before a wait gives up
+
+__device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t par, int* err) {
+    for (long long i = 0; i < kSpinLimit; i++)
+        if (mbar_test_wait(bar, par)) return true;
+    atomicOr(err, kErrTimeout);
+    return false;
+}
+
+// Shared-memory matrix descriptor of a K-major tile of rows x 64 F16 values
+// stored with the 128-byte swizzle (8-row groups 1024 bytes apart).
+__device__ __forceinline__ uint64_t umma_desc_sw128(const void* p) {
+    const uint64_t addr = smem_addr(p);
+    uint64_t d = (addr >> 4) & 0x3FFFull;       // start address
+    d |= (uint64_t)1 << 16;                      // leading-dimension offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;            // stride-dimension offset: 8 rows x 128 bytes
+    d |= (uint64_t)1 << 46;                      // descriptor version
+    d |= (uint64_t)2 << 61;                      // 128-byte swizzle
+    return d;
+}
+
+enum { kEpiBias = 0, kEpiResidual = 1, kEpiSwiGLU = 2 };
+
+struct GemmOut {
+    float* out;          // kEpiBias: [M][N] f32
+    const float* bias;   // kEpiBias: [N] or nullptr
+    float* resid;        // kEpiResidual: [M][N] f32, += acc
+    __half* hout;        // kEpiSwiGLU: [M][N/2] f16, silu(acc[2i]) * acc[2i+1]
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(128, 1) gemm_f16_kernel(const __grid_constant__ CUtensorMap ma,
+                                                          const __grid_constant__ CUtensorMap mb, GemmOut o, int M,
+                                                          int N, int K, int* err) {
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + kGStages * kGStageBytes);
+    uint64_t* empty = full + kGStages;
+    uint64_t* done = empty + kGStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * kGBM, n0 = blockIdx.x * kGBN;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGStages; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(kGBN));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    const uint32_t tmem = *tmem_slot;
+    // instruction descriptor: F32 accumulator, F16 A and B, both K-major, N = 128, M = 128
+    const uint32_t idesc = (1u << 4) | ((uint32_t)(kGBN >> 3) << 17) | ((uint32_t)(kGBM >> 4) << 24);
+    const int nk = K / kGBK;
+    if (threadIdx.x == 0) {
+        bool ok = true;
+        for (int kt = 0; kt < nk + kGStages && ok; kt++) {
+            if (kt < nk) {                                          // load k-tile kt
+                const int s = kt % kGStages;
+                if (kt >= kGStages) ok = wait_parity(&empty[s], ((kt / kGStages) - 1) & 1, err);
+                if (!ok) break;
+                uint8_t* st = sm + s * kGStageBytes;
+                mbar_arrive_expect_tx(&full[s], kGStageBytes);
+                tma_2d_g2s(st, &ma, kt * kGBK, m0, &full[s]);
+                tma_2d_g2s(st + kGABytes, &mb, kt * kGBK, n0, &full[s]);
+            }
+            const int kc = kt - (kGStages - 1);                    // multiply k-tile kc
+            if (kc >= 0 && kc < nk) {
+                const int s = kc % kGStages;
+                ok = wait_parity(&full[s], (kc / kGStages) & 1, err);
+                if (!ok) break;
+                asm volatile("tcgen05.fence::after_thread_sync;");
+                uint8_t* st = sm + s * kGStageBytes;
+                const uint64_t da = umma_desc_sw128(st), db = umma_desc_sw128(st + kGABytes);
+#pragma unroll
+                for (int kk = 0; kk < kGBK / 16; kk++) {
+                    const uint32_t accumulate = (kc > 0 || kk > 0) ? 1u : 0u;
+                    asm volatile(
+                        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+                        "l"(da + 2 * kk), "l"(db + 2 * kk), "r"(idesc), "r"(accumulate));
+                }
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                 smem_addr(&empty[s]))
+                             : "memory");
+            }
+        }
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                         smem_addr(done))
+                     : "memory");
+    }
+    __syncwarp();
+    wait_parity(done, 0, err);
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    // epilogue: warp w owns TMEM lanes (rows) 32w..32w+31, 32 columns per load
+    const int row = m0 + warp * 32 + lane;
+    for (int c0 = 0; c0 < kGBN; c0 += 32) {
+        uint32_t v[32];
+        const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0;
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+              "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
+              "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+              "=r"(v[30]), "=r"(v[31])
+            : "r"(taddr));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (row < M) {
+            const int cb = n0 + c0;
+            if constexpr (EPI == kEpiBias) {
+#pragma unroll
+                for (int j = 0; j < 32; j++)
+                    if (cb + j < N) o.out[(size_t)row * N + cb + j] = __uint_as_float(v[j]) + (o.bias ? o.bias[cb + j] : 0.f);
+            } else if constexpr (EPI == kEpiResidual) {
+#pragma unroll
+                for (int j = 0; j < 32; j++)
+                    if (cb + j < N) o.resid[(size_t)row * N + cb + j] += __uint_as_float(v[j]);
+            } else {
+                // columns 2i (gate) and 2i+1 (up) of the interleaved matrix
+#pragma unroll
+                for (int j = 0; j < 32; j += 2)
+                    if (cb + j + 1 < N) {
+                        const float g = __uint_as_float(v[j]), up = __uint_as_float(v[j + 1]);
+                        const float e = expf(-g);
+                        o.hout[(size_t)row * (N / 2) + (cb + j) / 2] =
+                            __float2half_rn(__fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), up));
+                    }
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kGBN));
+}
+
+// Embedding rows of the batch (F16 weights widened exactly).
+__global__ void embed_rows_kernel(const int* tok, int n, DMat embd, int dim, float* X) {
+    const int i = blockIdx.x;
+    if (i >= n) return;
+    const __half* row = reinterpret_cast<const __half*>(embd.q) + (size_t)tok[i] * embd.cols;
+    for (int d = threadIdx.x; d < dim; d += blockDim.x) X[(size_t)i * dim + d] = __half2float(row[d]);
+}
+
+// RMSNorm of every row ("The Forward Pass in Java", Example 4: y = (x*scale)*g,
+// scale = 1/sqrt(mean(x^2) + eps)); the GEMM operand is y rounded to F16.
+__global__ void rmsnorm_rows_f16_kernel(const float* X, int n, int dim, const float* g, float eps, __half* Y) {
+    const int i = blockIdx.x;
+    if (i >= n) return;
+    const float* x = X + (size_t)i * dim;
+    float ss = 0.f;
+    for (int d = threadIdx.x; d < dim; d += blockDim.x) ss += x[d] * x[d];
+    __shared__ float red[32];
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += red[w];
+    const float scale = 1.0f / sqrtf(tot / (float)dim + eps);
+    for (int d = threadIdx.x; d < dim; d += blockDim.x)
+        Y[(size_t)i * dim + d] = __float2half_rn(__fmul_rn(__fmul_rn(x[d], scale), g[d]));
+}
+
+// RoPE of q and k of row i at position pos0+i with the decode step's float
+// angle chain ("The Forward Pass in Java", Example 6; frequency factors per
+// "What a Llama model computes, and why" §2.4), then the F16 K and V rows of
+// that position ("The Forward Pass in Java", Examples 7 and 10).
+__global__ void rope_kv_rows_kernel(float* QKV, int n, int pos0, int n_heads, int n_kv, int hd, int rope_dims, int neox,
+                                    float theta_scale, const float* freqs, __half* kc, __half* vc) {
+    const int i = blockIdx.x;
+    if (i >= n) return;
+    const int pos = pos0 + i;
+    const int q_dim = n_heads * hd, kv_dim = n_kv * hd, half = rope_dims / 2;
+    float* row = QKV + (size_t)i * (q_dim + 2 * kv_dim);
+    __shared__ float cs[128], sn[128];
+    for (int j = threadIdx.x; j < half; j += blockDim.x) {
+        float th = (float)pos;
+        for (int k = 0; k < j; k++) th = __fmul_rn(th, theta_scale);
+        if (freqs) th = __fdiv_rn(th, freqs[j]);
+        double s, c;
+        sincos((double)th, &s, &c);
+        cs[j] = (float)c;
+        sn[j] = (float)s;
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < (n_heads + n_kv) * half; t += blockDim.x) {
+        const int head = t / half, j = t % half;
+        float* v = head < n_heads ? row + head * hd : row + q_dim + (head - n_heads) * hd;
+        const int a = neox ? j : 2 * j, b = neox ? j + half : 2 * j + 1;
+        const float x0 = v[a], x1 = v[b];
+        v[a] = __fsub_rn(__fmul_rn(x0, cs[j]), __fmul_rn(x1, sn[j]));
+        v[b] = __fadd_rn(__fmul_rn(x0, sn[j]), __fmul_rn(x1, cs[j]));
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < kv_dim; e += blockDim.x) {
+        kc[(size_t)pos * kv_dim + e] = __float2half_rn(row[q_dim + e]);
+        vc[(size_t)pos * kv_dim + e] = __float2half_rn(row[q_dim + kv_dim + e]);
+    }
+}
+
+// Attention of row i (query position pos0+i) for the query heads of kv head g
+// over cache rows 0..pos0+i ("The Forward Pass in Java", Example 7), in tiles
+// of 128 positions with a running max and sum per head; output rounded to F16
+// for the O projection.
+constexpr int kAttnTile = 128;
+__global__ void __launch_bounds__(128) attention_rows_kernel(const float* QKV, int n, int pos0, int n_heads, int n_kv,
+                                                             int hd, float attn_div, const __half* kc,
+                                                             const __half* vc, __half* A) {
+    const int i = blockIdx.x, g = blockIdx.y;
+    if (i >= n) return;
+    const int gq = n_heads / n_kv, q_dim = n_heads * hd, kv_dim = n_kv * hd, GD = gq * hd;
+    const int n_pos = pos0 + i + 1;
+    extern __shared__ float asm_[];
+    float* q = asm_;                                   // [gq][hd]
+    float* sc = q + GD;                                // [gq][tile]
+    float* ml = sc + gq * kAttnTile;                   // [3][gq]: m, l, corr
+    const float* qrow = QKV + (size_t)i * (q_dim + 2 * kv_dim) + g * gq * hd;
+    for (int e = threadIdx.x; e < GD; e += blockDim.x) q[e] = qrow[e];
+    if (threadIdx.x < gq) { ml[threadIdx.x] = -INFINITY; ml[gq + threadIdx.x] = 0.f; }
+    float acc[8];                                      // GD <= 960 -> at most 8 elements per thread
+#pragma unroll
+    for (int k = 0; k < 8; k++) acc[k] = 0.f;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t0 = 0; t0 < n_pos; t0 += kAttnTile) {
+        const int nt = min(kAttnTile, n_pos - t0);
+        // scores: thread t takes position t0+t for every head
+        if ((int)threadIdx.x < nt) {
+            const __half* krow = kc + (size_t)(t0 + threadIdx.x) * kv_dim + g * hd;
+            for (int h = 0; h < gq; h++) {
+                float s = 0.f;
+                for (int d = 0; d < hd; d += 2) {
+                    const float2 kv2 = __half22float2(*reinterpret_cast<const __half2*>(krow + d));
+                    s = fmaf(q[h * hd + d], kv2.x, s);
+                    s = fmaf(q[h * hd + d + 1], kv2.y, s);
+                }
+                sc[h * kAttnTile + threadIdx.x] = __fdiv_rn(s, attn_div);
+            }
+        }
+        __syncthreads();
+        for (int h = warp; h < gq; h += (int)(blockDim.x >> 5)) {
+            float mloc = -INFINITY;
+            for (int t = lane; t < nt; t += 32) mloc = fmaxf(mloc, sc[h * kAttnTile + t]);
+            mloc = warp_max(mloc);
+            const float mold = ml[h], mnew = fmaxf(mold, mloc);
+            float sum = 0.f;
+            for (int t = lane; t < nt; t += 32) {
+                const float e = expf(sc[h * kAttnTile + t] - mnew);
+                sc[h * kAttnTile + t] = e;
+                sum += e;
+            }
+            sum = warp_sum(sum);
+            if (lane == 0) {
+                const float corr = expf(mold - mnew);
+                ml[h] = mnew;
+                ml[gq + h] = ml[gq + h] * corr + sum;
+                ml[2 * gq + h] = corr;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const int e = threadIdx.x + k * 128;
+            if (e < GD) {
+                const int h = e / hd, d = e % hd;
+                float a = acc[k] * ml[2 * gq + h];
+                const __half* vcol = vc + (size_t)t0 * kv_dim + g * hd + d;
+                for (int t = 0; t < nt; t++) a = fmaf(sc[h * kAttnTile + t], __half2float(vcol[(size_t)t * kv_dim]), a);
+                acc[k] = a;
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        const int e = threadIdx.x + k * 128;
+        if (e < GD) A[(size_t)i * q_dim + g * gq * hd + e] = __float2half_rn(acc[k] / ml[gq + e / hd]);
+    }
+}
+
+// The last row: RMSNorm in F32 (as the decode step), logits of every vocabulary
+// row (F16 output matrix), argmax key of each warp's rows.
+__global__ void final_norm_kernel(const float* x, int dim, const float* g, float eps, float* y) {
+    float ss = 0.f;
+    for (int d = threadIdx.x; d < dim; d += blockDim.x) ss += x[d] * x[d];
+    __shared__ float red[32];
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += red[w];
+    const float scale = 1.0f / sqrtf(tot / (float)dim + eps);
+    for (int d = threadIdx.x; d < dim; d += blockDim.x) y[d] = __fmul_rn(__fmul_rn(x[d], scale), g[d]);
+}
+
+__global__ void logits_f16_kernel(DMat out, const float* y, int dim, int vocab, float* logits, unsigned long long* best) {
+    extern __shared__ float ys[];
+    for (int d = threadIdx.x; d < dim; d += blockDim.x) ys[d] = y[d];
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
+    unsigned long long key = 0ull;
+    for (int r = blockIdx.x * wpb + warp; r < vocab; r += gridDim.x * wpb) {
+        const __half* w = reinterpret_cast<const __half*>(out.q) + (size_t)r * out.cols;
+        float s = 0.f;
+        for (int d = 2 * lane; d < dim; d += 64) {
+            const float2 wv = __half22float2(*reinterpret_cast<const __half2*>(w + d));
+            s = fmaf(wv.x, ys[d], s);
+            s = fmaf(wv.y, ys[d + 1], s);
+        }
+        s = warp_sum(s);
+        if (lane == 0) {
+            logits[r] = s;
+            const unsigned long long k = argmax_key(s, r);
+            key = k > key ? k : key;
+        }
+    }
+    if (lane == 0 && key) atomicMax(best, key);
+}
+
+__global__ void argmax_publish_kernel(unsigned long long* best, int* out) {
+    *out = argmax_key_index(*best);
+    *best = 0ull;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D map of a [rows][K] F16 matrix, box 64 x 128, 128-byte swizzle.
+bool gemm_map(CUtensorMap* m, const void* base, int K, int rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kGBK, 128};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI>
+cudaError_t gemm(cudaStream_t st, const CUtensorMap& ma, const CUtensorMap& mb, const GemmOut& o, int M, int N, int K,
+                 int* err) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_f16_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    dim3 grid((N + kGBN - 1) / kGBN, (M + kGBM - 1) / kGBM);
+    gemm_f16_kernel<EPI><<<grid, 128, kGemmSmem, st>>>(ma, mb, o, M, N, K, err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_supported(const PrefillCtx& c) {
+    return c.wtype == LLM_F16 && c.dim % kGBK == 0 && c.q_dim % kGBK == 0 && c.ffn % kGBK == 0 &&
+           c.n_heads / c.n_kv * c.hd <= 8 * 128 && c.rope_dims / 2 <= 128;
+}
+
+size_t prefill_workspace_bytes(const PrefillCtx& c) {
+    const size_t M = kPrefillRows;
+    auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
+    return al(M * 4) + al(M * c.dim * 4) + al(M * c.dim * 2) + al(M * (c.q_dim + 2 * c.kv_dim) * 4) +
+           al(M * c.q_dim * 2) + al(M * c.ffn * 2) + al((size_t)c.dim * 4);
+}
+
+// Runs the batch; `ws` holds prefill_workspace_bytes(c).  Returns a CUDA error
+// or cudaSuccess; *msg names the failing step.
+cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_host, int n, int pos0, const char** msg) {
+    auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
+    const size_t M = kPrefillRows;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    int* tok = reinterpret_cast<int*>(w); w += al(M * 4);
+    float* X = reinterpret_cast<float*>(w); w += al(M * c.dim * 4);
+    __half* Xh = reinterpret_cast<__half*>(w); w += al(M * c.dim * 2);
+    float* QKV = reinterpret_cast<float*>(w); w += al(M * (c.q_dim + 2 * c.kv_dim) * 4);
+    __half* Ah = reinterpret_cast<__half*>(w); w += al(M * c.q_dim * 2);
+    __half* Hh = reinterpret_cast<__half*>(w); w += al(M * c.ffn * 2);
+    float* ylast = reinterpret_cast<float*>(w);
+    cudaError_t e;
+#define PF_CK(call, what)                 \
+    do {                                  \
+        if ((e = (call)) != cudaSuccess) { \
+            *msg = what;                  \
+            return e;                     \
+        }                                 \
+    } while (0)
+    CUtensorMap mXh, mAh, mHh;
+    if (!gemm_map(&mXh, Xh, c.dim, (int)M) || !gemm_map(&mAh, Ah, c.q_dim, (int)M) || !gemm_map(&mHh, Hh, c.ffn, (int)M)) {
+        *msg = "tensor map of an activation operand";
+        return cudaErrorInvalidValue;
+    }
+    std::vector<CUtensorMap> mw((size_t)4 * c.n_layers);
+    for (int l = 0; l < c.n_layers; l++) {
+        const LayerDev& L = c.layers[l];
+        if (!gemm_map(&mw[4 * l + 0], L.qkv.q, c.dim, L.qkv.rows) || !gemm_map(&mw[4 * l + 1], L.o.q, c.q_dim, L.o.rows) ||
+            !gemm_map(&mw[4 * l + 2], L.gu.q, c.dim, 2 * L.gu.rows) ||
+            !gemm_map(&mw[4 * l + 3], L.down.q, c.ffn, L.down.rows)) {
+            *msg = "tensor map of a weight matrix";
+            return cudaErrorInvalidValue;
+        }
+    }
+    const int attn_smem = (int)(sizeof(float) * ((size_t)c.n_heads / c.n_kv * c.hd +
+                                                 (size_t)c.n_heads / c.n_kv * kAttnTile + 3 * (c.n_heads / c.n_kv)));
+    for (int b0 = 0; b0 < n; b0 += kPrefillRows) {
+        const int nb = n - b0 < kPrefillRows ? n - b0 : kPrefillRows;
+        const int p0 = pos0 + b0;
+        PF_CK(cudaMemcpyAsync(tok, tokens_host + b0, (size_t)nb * 4, cudaMemcpyHostToDevice, c.st), "token upload");
+        embed_rows_kernel<<<nb, 256, 0, c.st>>>(tok, nb, c.embd, c.dim, X);
+        PF_CK(cudaGetLastError(), "embedding");
+        for (int l = 0; l < c.n_layers; l++) {
+            const LayerDev& L = c.layers[l];
+            rmsnorm_rows_f16_kernel<<<nb, 256, 0, c.st>>>(X, nb, c.dim, L.attn_norm, c.eps, Xh);
+            PF_CK(cudaGetLastError(), "attention RMSNorm");
+            GemmOut oq{QKV, L.qkv_bias, nullptr, nullptr};
+            PF_CK(gemm<kEpiBias>(c.st, mXh, mw[4 * l + 0], oq, nb, L.qkv.rows, c.dim, c.err), "QKV GEMM");
+            rope_kv_rows_kernel<<<nb, 128, 0, c.st>>>(QKV, nb, p0, c.n_heads, c.n_kv, c.hd, c.rope_dims, c.neox,
+                                                      c.theta_scale, c.rope_freqs, L.kc, L.vc);
+            PF_CK(cudaGetLastError(), "RoPE and KV append");
+            attention_rows_kernel<<<dim3(nb, c.n_kv), 128, attn_smem, c.st>>>(QKV, nb, p0, c.n_heads, c.n_kv, c.hd,
+                                                                              c.attn_div, L.kc, L.vc, Ah);
+            PF_CK(cudaGetLastError(), "attention");
+            GemmOut oo{nullptr, nullptr, X, nullptr};
+            PF_CK(gemm<kEpiResidual>(c.st, mAh, mw[4 * l + 1], oo, nb, c.dim, c.q_dim, c.err), "O GEMM");
+            rmsnorm_rows_f16_kernel<<<nb, 256, 0, c.st>>>(X, nb, c.dim, L.ffn_norm, c.eps, Xh);
+            PF_CK(cudaGetLastError(), "FFN RMSNorm");
+            GemmOut og{nullptr, nullptr, nullptr, Hh};
+            PF_CK(gemm<kEpiSwiGLU>(c.st, mXh, mw[4 * l + 2], og, nb, 2 * L.gu.rows, c.dim, c.err), "gate/up GEMM");
+            GemmOut od{nullptr, nullptr, X, nullptr};
+            PF_CK(gemm<kEpiResidual>(c.st, mHh, mw[4 * l + 3], od, nb, c.dim, c.ffn, c.err), "down GEMM");
+        }
+        if (b0 + nb == n) {
+            final_norm_kernel<<<1, 256, 0, c.st>>>(X + (size_t)(nb - 1) * c.dim, c.dim, c.out_norm, c.eps, ylast);
+            PF_CK(cudaGetLastError(), "final RMSNorm");
+            logits_f16_kernel<<<c.sms * 4, 256, (size_t)c.dim * 4, c.st>>>(c.out, ylast, c.dim, c.vocab, c.logits,
+                                                                           c.best);
+            PF_CK(cudaGetLastError(), "logits");
+            argmax_publish_kernel<<<1, 1, 0, c.st>>>(c.best, c.argmax_dev);
+            PF_CK(cudaGetLastError(), "argmax");
+        }
+    }
+#undef PF_CK
+    return cudaSuccess;
+}
+
+}  // namespace llm
