@@ -305,6 +305,60 @@ def run_ours(args):
     return 0
 
 
+# ------------------------------------------------------------- prefill --
+PREFILL_CFG = synth.QWEN2_F16
+PREFILL_N = 512
+
+
+def prefill_flops(cfg, n: int) -> float:
+    """FLOPs of one n-token prefill from position 0: the layer GEMMs (2 per
+    multiply-add), causal attention (q.k and p.v over positions 0..i for every
+    row i), and the last row's logits."""
+    layers, _ = matrix_elems(cfg)
+    gemm = 2.0 * layers * n
+    attn = cfg.n_layers * cfg.n_heads * cfg.head_dim * 4.0 * (n * (n + 1) / 2)
+    logits = 2.0 * cfg.vocab * cfg.dim
+    return gemm + attn + logits
+
+
+def run_prefill(args):
+    """Optional line (not the headline): the Qwen2-style F16 model's 512-token
+    batched prefill, tokens per second and tensor-core TFLOP/s."""
+    import torch
+    import llama_decode_forward_gb300 as L
+    cfg = PREFILL_CFG.scaled(max_seq=PREFILL_N + 128)
+    W = synth.make_weights(cfg)
+    dec = L.Decoder(cfg, W)
+    toks = synth.prompt(cfg, PREFILL_N)
+    logits = np.empty(cfg.vocab, np.float32)
+    for _ in range(max(args.warmup, 3)):
+        L.llm_prefill(dec.h, toks, 0, logits)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        L.llm_prefill(dec.h, toks, 0, logits)
+    el = time.perf_counter() - t0
+    fl = prefill_flops(cfg, PREFILL_N)
+    tflops = fl * args.steps / el / 1e12
+    peak = None
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            peak = json.load(f).get("bf16_tflops")
+    line = {"metric": "prefill tok/s (Qwen2-style 1B-shape F16, 512 tokens from pos 0)",
+            "value": PREFILL_N * args.steps / el, "unit": "tok/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": 1000.0 * el / args.steps, "higher_is_better": True,
+            "dtype": "f16 operands, f32 accumulate", "data": "synthetic (seeded random F16 weights and tokens)",
+            "config": {"workload": "qwen2-style 1b-shape f16 prefill, 512 tokens", "flops_per_prefill": fl},
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak if peak else None,
+                         "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops; f16 taken equal)"},
+            "timing": "host wall clock around synchronous llm_prefill calls (each includes the token upload and the logits copy)"}
+    dec.close()
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -313,9 +367,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode",
+                    help="decode (the headline line) or the optional batched-prefill line")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "prefill":
+        return run_prefill(args)
     return run_ours(args)
 
 

@@ -242,7 +242,9 @@ __global__ void rope_kv_rows_kernel(float* QKV, int n, int pos0, int n_heads, in
 // Attention of row i (query position pos0+i) for the query heads of kv head g
 // over cache rows 0..pos0+i ("The Forward Pass in Java", Example 7), in tiles
 // of 128 positions with a running max and sum per head; output rounded to F16
-// for the O projection.
+// for the O projection.  Each tile's K and V rows are staged in shared memory
+// with 16-byte loads; a thread's score loop starts at a column that rotates
+// with its position so that the K reads fall in different banks.
 constexpr int kAttnTile = 128;
 __global__ void __launch_bounds__(128) attention_rows_kernel(const float* QKV, int n, int pos0, int n_heads, int n_kv,
                                                              int hd, float attn_div, const __half* kc,
@@ -251,8 +253,10 @@ __global__ void __launch_bounds__(128) attention_rows_kernel(const float* QKV, i
     if (i >= n) return;
     const int gq = n_heads / n_kv, q_dim = n_heads * hd, kv_dim = n_kv * hd, GD = gq * hd;
     const int n_pos = pos0 + i + 1;
-    extern __shared__ float asm_[];
-    float* q = asm_;                                   // [gq][hd]
+    extern __shared__ __align__(16) float asm_[];
+    __half* ks = reinterpret_cast<__half*>(asm_);      // [tile][hd]
+    __half* vs = ks + kAttnTile * hd;                  // [tile][hd]
+    float* q = reinterpret_cast<float*>(vs + kAttnTile * hd);   // [gq][hd]
     float* sc = q + GD;                                // [gq][tile]
     float* ml = sc + gq * kAttnTile;                   // [3][gq]: m, l, corr
     const float* qrow = QKV + (size_t)i * (q_dim + 2 * kv_dim) + g * gq * hd;
@@ -261,21 +265,30 @@ __global__ void __launch_bounds__(128) attention_rows_kernel(const float* QKV, i
     float acc[8];                                      // GD <= 960 -> at most 8 elements per thread
 #pragma unroll
     for (int k = 0; k < 8; k++) acc[k] = 0.f;
-    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int w16 = hd / 8;                            // 16-byte words per row
     for (int t0 = 0; t0 < n_pos; t0 += kAttnTile) {
         const int nt = min(kAttnTile, n_pos - t0);
-        // scores: thread t takes position t0+t for every head
+        __syncthreads();                               // previous tile fully used
+        for (int e = threadIdx.x; e < nt * w16; e += blockDim.x) {
+            const int t = e / w16, w = e % w16;
+            const size_t src = (size_t)(t0 + t) * kv_dim + g * hd + w * 8;
+            reinterpret_cast<uint4*>(ks)[e] = *reinterpret_cast<const uint4*>(kc + src);
+            reinterpret_cast<uint4*>(vs)[e] = *reinterpret_cast<const uint4*>(vc + src);
+        }
+        __syncthreads();
         if ((int)threadIdx.x < nt) {
-            const __half* krow = kc + (size_t)(t0 + threadIdx.x) * kv_dim + g * hd;
+            const int t = threadIdx.x, nh2 = hd / 2;
+            const __half2* k2 = reinterpret_cast<const __half2*>(ks + t * hd);
             for (int h = 0; h < gq; h++) {
-                float s = 0.f;
-                for (int d = 0; d < hd; d += 2) {
-                    const float2 kv2 = __half22float2(*reinterpret_cast<const __half2*>(krow + d));
-                    s = fmaf(q[h * hd + d], kv2.x, s);
-                    s = fmaf(q[h * hd + d + 1], kv2.y, s);
+                const float2* q2 = reinterpret_cast<const float2*>(q + h * hd);
+                float2 a = make_float2(0.f, 0.f);
+                int j = t % nh2;
+                for (int k = 0; k < nh2; k++) {
+                    a = __ffma2_rn(__half22float2(k2[j]), q2[j], a);
+                    j = j + 1 == nh2 ? 0 : j + 1;
                 }
-                sc[h * kAttnTile + threadIdx.x] = __fdiv_rn(s, attn_div);
+                sc[h * kAttnTile + t] = __fdiv_rn(a.x + a.y, attn_div);
             }
         }
         __syncthreads();
@@ -305,12 +318,11 @@ __global__ void __launch_bounds__(128) attention_rows_kernel(const float* QKV, i
             if (e < GD) {
                 const int h = e / hd, d = e % hd;
                 float a = acc[k] * ml[2 * gq + h];
-                const __half* vcol = vc + (size_t)t0 * kv_dim + g * hd + d;
-                for (int t = 0; t < nt; t++) a = fmaf(sc[h * kAttnTile + t], __half2float(vcol[(size_t)t * kv_dim]), a);
+                const float* p = sc + h * kAttnTile;
+                for (int t = 0; t < nt; t++) a = fmaf(p[t], __half2float(vs[t * hd + d]), a);
                 acc[k] = a;
             }
         }
-        __syncthreads();
     }
 #pragma unroll
     for (int k = 0; k < 8; k++) {
@@ -453,8 +465,12 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
             return cudaErrorInvalidValue;
         }
     }
-    const int attn_smem = (int)(sizeof(float) * ((size_t)c.n_heads / c.n_kv * c.hd +
-                                                 (size_t)c.n_heads / c.n_kv * kAttnTile + 3 * (c.n_heads / c.n_kv)));
+    const int gq = c.n_heads / c.n_kv;
+    const int attn_smem = (int)(2 * sizeof(__half) * kAttnTile * c.hd +
+                                sizeof(float) * ((size_t)gq * c.hd + (size_t)gq * kAttnTile + 3 * gq));
+    if (attn_smem > 48 * 1024)
+        PF_CK(cudaFuncSetAttribute(attention_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem),
+              "attention shared memory");
     for (int b0 = 0; b0 < n; b0 += kPrefillRows) {
         const int nb = n - b0 < kPrefillRows ? n - b0 : kPrefillRows;
         const int p0 = pos0 + b0;
