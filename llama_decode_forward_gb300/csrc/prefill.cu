@@ -7,9 +7,10 @@
 // C[M][N] = A[M][K] . W[N][K]^T with A the token rows (F16, rounded to
 // nearest even from the F32 activations) and W a weight matrix in the
 // library's row layout (F16, K contiguous), F32 accumulation in tensor
-// memory.  One CTA computes one 128 x 128 tile: thread 0 streams 128 x 64
-// tiles of A and W into a 4-stage ring with 2-D TMA (128-byte swizzle) and
-// issues tcgen05.mma (M 128, N 128, K 16) into a TMEM accumulator; the four
+// memory.  One CTA computes one 128 x BN tile (BN 64 for the narrow outputs,
+// 128 for the wide gate/up one; two CTAs per SM): thread 0 streams 128 x 64
+// tiles of A and BN x 64 tiles of W into a ring with 2-D TMA (128-byte
+// swizzle) and issues tcgen05.mma (M 128, N BN, K 16) into a TMEM accumulator; the four
 // warps then read their 32 rows back with tcgen05.ld and apply the epilogue
 // (bias, residual add, or SwiGLU over the interleaved gate/up columns).
 //
@@ -27,9 +28,15 @@ namespace llm {
 
 namespace {
 
-constexpr int kGBM = 128, kGBN = 128, kGBK = 64, kGStages = 4;
-constexpr int kGABytes = kGBM * kGBK * 2, kGBBytes = kGBN * kGBK * 2, kGStageBytes = kGABytes + kGBBytes;
-constexpr int kGemmSmem = kGStages * kGStageBytes + 1024 + 256;
+constexpr int kGBM = 128, kGBK = 64;
+constexpr int kGABytes = kGBM * kGBK * 2;
+// Tile width BN and ring depth: 96 KB of stages, so two CTAs share an SM.
+template <int BN>
+struct GemmTile {
+    static constexpr int kStages = BN == 64 ? 4 : 3;
+    static constexpr int kStageBytes = kGABytes + BN * kGBK * 2;
+    static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
+};
 constexpr long long kSpinLimit = 200000000ll;   // mbarrier polls before a wait gives up
 
 __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t par, int* err) {
@@ -60,10 +67,11 @@ struct GemmOut {
     __half* hout;        // kEpiSwiGLU: [M][N/2] f16, silu(acc[2i]) * acc[2i+1]
 };
 
-template <int EPI>
-__global__ void __launch_bounds__(128, 1) gemm_f16_kernel(const __grid_constant__ CUtensorMap ma,
+template <int BN, int EPI>
+__global__ void __launch_bounds__(128, 2) gemm_f16_kernel(const __grid_constant__ CUtensorMap ma,
                                                           const __grid_constant__ CUtensorMap mb, GemmOut o, int M,
                                                           int N, int K, int* err) {
+    constexpr int kGStages = GemmTile<BN>::kStages, kGStageBytes = GemmTile<BN>::kStageBytes, kGBN = BN;
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + kGStages * kGStageBytes);
@@ -388,30 +396,31 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 2-D map of a [rows][K] F16 matrix, box 64 x 128, 128-byte swizzle.
-bool gemm_map(CUtensorMap* m, const void* base, int K, int rows) {
+// 2-D map of a [rows][K] F16 matrix, box 64 x box_rows, 128-byte swizzle.
+bool gemm_map(CUtensorMap* m, const void* base, int K, int rows, int box_rows = 128) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kGBK, 128};
+    cuuint32_t box[2] = {(cuuint32_t)kGBK, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int EPI>
+template <int BN, int EPI>
 cudaError_t gemm(cudaStream_t st, const CUtensorMap& ma, const CUtensorMap& mb, const GemmOut& o, int M, int N, int K,
                  int* err) {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_f16_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+        cudaError_t e = cudaFuncSetAttribute(gemm_f16_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             GemmTile<BN>::kSmem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    dim3 grid((N + kGBN - 1) / kGBN, (M + kGBM - 1) / kGBM);
-    gemm_f16_kernel<EPI><<<grid, 128, kGemmSmem, st>>>(ma, mb, o, M, N, K, err);
+    dim3 grid((N + BN - 1) / BN, (M + kGBM - 1) / kGBM);
+    gemm_f16_kernel<BN, EPI><<<grid, 128, GemmTile<BN>::kSmem, st>>>(ma, mb, o, M, N, K, err);
     return cudaGetLastError();
 }
 
@@ -458,9 +467,10 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
     std::vector<CUtensorMap> mw((size_t)4 * c.n_layers);
     for (int l = 0; l < c.n_layers; l++) {
         const LayerDev& L = c.layers[l];
-        if (!gemm_map(&mw[4 * l + 0], L.qkv.q, c.dim, L.qkv.rows) || !gemm_map(&mw[4 * l + 1], L.o.q, c.q_dim, L.o.rows) ||
-            !gemm_map(&mw[4 * l + 2], L.gu.q, c.dim, 2 * L.gu.rows) ||
-            !gemm_map(&mw[4 * l + 3], L.down.q, c.ffn, L.down.rows)) {
+        if (!gemm_map(&mw[4 * l + 0], L.qkv.q, c.dim, L.qkv.rows, 64) ||
+            !gemm_map(&mw[4 * l + 1], L.o.q, c.q_dim, L.o.rows, 64) ||
+            !gemm_map(&mw[4 * l + 2], L.gu.q, c.dim, 2 * L.gu.rows, 128) ||
+            !gemm_map(&mw[4 * l + 3], L.down.q, c.ffn, L.down.rows, 64)) {
             *msg = "tensor map of a weight matrix";
             return cudaErrorInvalidValue;
         }
@@ -482,7 +492,7 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
             rmsnorm_rows_f16_kernel<<<nb, 256, 0, c.st>>>(X, nb, c.dim, L.attn_norm, c.eps, Xh);
             PF_CK(cudaGetLastError(), "attention RMSNorm");
             GemmOut oq{QKV, L.qkv_bias, nullptr, nullptr};
-            PF_CK(gemm<kEpiBias>(c.st, mXh, mw[4 * l + 0], oq, nb, L.qkv.rows, c.dim, c.err), "QKV GEMM");
+            PF_CK((gemm<64, kEpiBias>(c.st, mXh, mw[4 * l + 0], oq, nb, L.qkv.rows, c.dim, c.err)), "QKV GEMM");
             rope_kv_rows_kernel<<<nb, 128, 0, c.st>>>(QKV, nb, p0, c.n_heads, c.n_kv, c.hd, c.rope_dims, c.neox,
                                                       c.theta_scale, c.rope_freqs, L.kc, L.vc);
             PF_CK(cudaGetLastError(), "RoPE and KV append");
@@ -490,13 +500,13 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
                                                                               c.attn_div, L.kc, L.vc, Ah);
             PF_CK(cudaGetLastError(), "attention");
             GemmOut oo{nullptr, nullptr, X, nullptr};
-            PF_CK(gemm<kEpiResidual>(c.st, mAh, mw[4 * l + 1], oo, nb, c.dim, c.q_dim, c.err), "O GEMM");
+            PF_CK((gemm<64, kEpiResidual>(c.st, mAh, mw[4 * l + 1], oo, nb, c.dim, c.q_dim, c.err)), "O GEMM");
             rmsnorm_rows_f16_kernel<<<nb, 256, 0, c.st>>>(X, nb, c.dim, L.ffn_norm, c.eps, Xh);
             PF_CK(cudaGetLastError(), "FFN RMSNorm");
             GemmOut og{nullptr, nullptr, nullptr, Hh};
-            PF_CK(gemm<kEpiSwiGLU>(c.st, mXh, mw[4 * l + 2], og, nb, 2 * L.gu.rows, c.dim, c.err), "gate/up GEMM");
+            PF_CK((gemm<128, kEpiSwiGLU>(c.st, mXh, mw[4 * l + 2], og, nb, 2 * L.gu.rows, c.dim, c.err)), "gate/up GEMM");
             GemmOut od{nullptr, nullptr, X, nullptr};
-            PF_CK(gemm<kEpiResidual>(c.st, mHh, mw[4 * l + 3], od, nb, c.dim, c.ffn, c.err), "down GEMM");
+            PF_CK((gemm<64, kEpiResidual>(c.st, mHh, mw[4 * l + 3], od, nb, c.dim, c.ffn, c.err)), "down GEMM");
         }
         if (b0 + nb == n) {
             final_norm_kernel<<<1, 256, 0, c.st>>>(X + (size_t)(nb - 1) * c.dim, c.dim, c.out_norm, c.eps, ylast);
