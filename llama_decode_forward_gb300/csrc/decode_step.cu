@@ -167,7 +167,8 @@ struct Producer {
         trace_mark(p, tk);
         int r0, r1;                                   // rows, or super-rows when m.pair
         cta_rows(m.rows, r0, r1);
-        const int per = m.pair ? 2 : 1;
+        if (m.pair == 2) { r0 *= 2; r1 *= 2; }        // pairs streamed as single rows
+        const int per = m.pair == 1 ? 2 : 1;
         const size_t rowq = (size_t)row_qbytes(m, wtype);
         const int rowd = wtype == LLM_Q8_0 ? 2 * m.dstride : 0;
         for (int r = r0; r < r1; r += m.rpc) {
@@ -459,7 +460,8 @@ struct EpiSwiGLU {
     float* u;
     float* gs;                    // smem [2 * rows of this CTA]
     int i0, i1;                   // this CTA's super-rows
-    __device__ void row(int, float) {}
+    // row r of the interleaved matrix: gate (even) or up (odd) of super-row r / 2
+    __device__ void row(int r, float v) { gs[r - 2 * i0] = v; }
     __device__ void pair(int i, float g, float up) {
         gs[2 * (i - i0)] = g;
         gs[2 * (i - i0) + 1] = up;
@@ -635,6 +637,7 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
     const int tw = m.tw, teams = m.teams;
     int r0, r1;
     cta_rows(m.rows, r0, r1);
+    if (m.pair == 2) { r0 *= 2; r1 *= 2; }            // pairs reduced as single rows
     const int per = PAIR ? 2 : 1;
     const int rowq = row_qbytes(m, DT);
     const int rowd = DT == LLM_Q8_0 ? 2 * m.dstride : 0;
@@ -1042,7 +1045,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
             int i0, i1;
             cta_rows(L.gu.rows, i0, i1);
             EpiSwiGLU e{p.u, sm.bias(), i0, i1};
-            gemv_consume<DT, true>(c, L.gu, src, token, e);
+            gemv_consume<DT, false>(c, L.gu, src, token, e);
         }
         if (tid == 0) trace_mark(p, 10 * l + 7);
         c.signal(ctr + 3);
@@ -1139,9 +1142,11 @@ __global__ void __launch_bounds__(kBlock, 1) decode_step_kernel(const __grid_con
 }
 
 // ------------------------------------------------------ host-side helpers --
-// Streaming plan of one matrix (rows per slot, team width, team count).  For
-// a pair matrix the plan counts super-rows (two matrix rows each).  Rows per
-// chunk are a multiple of the rows all teams take in one pass.
+// Streaming plan of one matrix (rows per slot, team width, team count).  Rows
+// per chunk are a multiple of the rows all teams take in one pass.  A pair
+// matrix (interleaved gate/up rows) is split across CTAs by super-rows, so a
+// gate row and its up row stay in one CTA, and is streamed and reduced as
+// single rows (pair = 2); the rows are paired when the phase finishes.
 bool matrix_plan(DMat& m, int wtype, bool pair) {
     const int lpr = (m.cols + kLaneElems - 1) / kLaneElems;
     int half = 1;
@@ -1150,7 +1155,7 @@ bool matrix_plan(DMat& m, int wtype, bool pair) {
     } else {
         half = 32 * ((lpr + 31) / 32);
     }
-    const int tw = pair ? 2 * half : half;
+    const int tw = half;
     int teams, rows_per_pass;
     if (tw <= 32) {
         teams = kConsumerWarps * (32 / tw);
@@ -1161,10 +1166,9 @@ bool matrix_plan(DMat& m, int wtype, bool pair) {
         if (teams > kMaxTeams) teams = kMaxTeams;
         rows_per_pass = (wtype == LLM_Q8_0 ? 4 : 2) * teams;
     }
-    const int per = pair ? 2 : 1;
-    const int slot_rows = kSlotBytes / (per * slot_row_bytes(wtype, m.cols, m.dstride));
+    const int slot_rows = kSlotBytes / slot_row_bytes(wtype, m.cols, m.dstride);
     if (slot_rows < 1) return false;
-    m.pair = pair ? 1 : 0;
+    m.pair = pair ? 2 : 0;
     m.tw = tw;
     m.teams = teams;
     m.rpc = slot_rows >= rows_per_pass ? (slot_rows / rows_per_pass) * rows_per_pass

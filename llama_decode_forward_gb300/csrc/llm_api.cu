@@ -371,7 +371,7 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
     {
         const DMat* mats[5] = {&h->layers[0].qkv, &h->layers[0].o, &h->layers[0].gu, &h->layers[0].down, &h->out};
         for (const DMat* m : mats) {
-            const int rows = (m->rows + h->sms - 1) / h->sms;
+            const int rows = (m->rows + h->sms - 1) / h->sms * (m->pair == 2 ? 2 : 1);
             const int parts = m->tw > 32 ? m->tw / 32 : 1;
             if (rows * parts > rowp_floats) rowp_floats = rows * parts;
         }

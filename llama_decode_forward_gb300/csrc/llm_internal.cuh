@@ -32,9 +32,9 @@ enum : int { kErrNone = 0, kErrTimeout = 1, kErrToken = 2 };
 // Streaming plan (set at creation): a ring slot carries `rpc` rows; a row is
 // reduced by a team of `tw` lanes (32 elements per lane; tw <= 32 is a part
 // of one warp, tw > 32 is tw/32 whole warps) and `teams` teams work side by side.
-// pair = 1 (gate/up): rows 2i and 2i+1 form one "super-row" reduced by one
-// team whose two halves share the same activation lanes; rows/rpc then count
-// super-rows.
+// pair = 2 (gate/up): rows 2i and 2i+1 form one "super-row"; `rows` counts
+// super-rows (CTAs split the matrix by super-rows, so a gate row and its up
+// row stay in one CTA) while the plan (tw, teams, rpc) counts single rows.
 struct DMat {
     const uint8_t* q;
     const __half* d;
