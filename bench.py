@@ -306,7 +306,7 @@ def run_ours(args):
 
 
 # ------------------------------------------------------------- prefill --
-PREFILL_CFG = synth.QWEN2_F16
+PREFILL_CFGS = {"f16": synth.QWEN2_F16, "q8_0": synth.LLAMA1B_Q8}
 PREFILL_N = 512
 
 
@@ -322,11 +322,14 @@ def prefill_flops(cfg, n: int) -> float:
 
 
 def run_prefill(args):
-    """Optional line (not the headline): the Qwen2-style F16 model's 512-token
-    batched prefill, tokens per second and tensor-core TFLOP/s."""
+    """Optional line (not the headline): a 1B-shape model's 512-token batched
+    prefill (the Qwen2-style F16 model, or Llama 3.2 Q8_0 whose matrices are
+    expanded to F16 before each GEMM), tokens per second and tensor-core
+    TFLOP/s."""
     import torch
     import llama_decode_forward_gb300 as L
-    cfg = PREFILL_CFG.scaled(max_seq=PREFILL_N + 128)
+    base = PREFILL_CFGS[args.prefill_weights]
+    cfg = base.scaled(max_seq=PREFILL_N + 128)
     W = synth.make_weights(cfg)
     dec = L.Decoder(cfg, W)
     toks = synth.prompt(cfg, PREFILL_N)
@@ -345,11 +348,13 @@ def run_prefill(args):
     if os.path.exists(p):
         with open(p) as f:
             peak = json.load(f).get("bf16_tflops")
-    line = {"metric": "prefill tok/s (Qwen2-style 1B-shape F16, 512 tokens from pos 0)",
+    what = {"f16": "Qwen2-style 1B-shape F16", "q8_0": "Llama-3.2-1B-shape Q8_0"}[args.prefill_weights]
+    line = {"metric": f"prefill tok/s ({what}, 512 tokens from pos 0)",
             "value": PREFILL_N * args.steps / el, "unit": "tok/s", "n_gpus": 1, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": 1000.0 * el / args.steps, "higher_is_better": True,
-            "dtype": "f16 operands, f32 accumulate", "data": "synthetic (seeded random F16 weights and tokens)",
-            "config": {"workload": "qwen2-style 1b-shape f16 prefill, 512 tokens", "flops_per_prefill": fl},
+            "dtype": "f16 operands, f32 accumulate",
+            "data": f"synthetic (seeded random {args.prefill_weights.upper()} weights and tokens)",
+            "config": {"workload": f"{base.name} prefill, 512 tokens", "flops_per_prefill": fl},
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak if peak else None,
                          "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops; f16 taken equal)"},
@@ -369,6 +374,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["decode", "prefill"], default="decode",
                     help="decode (the headline line) or the optional batched-prefill line")
+    ap.add_argument("--prefill-weights", choices=sorted(PREFILL_CFGS), default="f16",
+                    help="weight type of the prefill line's model")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

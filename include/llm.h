@@ -1,6 +1,6 @@
 /*
  * llm.h — C ABI of libllmdecode: batch-1 decode forward pass of a Llama-family
- * model on one NVIDIA GB300 (sm_103a), plus an F16 batched prefill.
+ * model on one NVIDIA GB300 (sm_103a), plus a tensor-core batched prefill.
  *
  * What the calls compute is the forward pass of "The Forward Pass in Java"
  * (codeloopback.dev, llm-forward-pass), Example 13 (`Llama.forward`): embedding
@@ -132,9 +132,12 @@ int llm_generate(llm_handle *h, int32_t token, int32_t pos, int32_t n_steps, int
 /* Batched prefill of tokens_host[0..n) at positions pos0..pos0+n-1 ("What a
  * Llama model computes, and why" §4): every K/V row is written and token i
  * attends to rows 0..pos0+i; only the last token's logits are produced (to
- * logits_host when not NULL; argmax to argmax_host when not NULL).  F16
- * weights run the projections as tensor-core GEMMs; other types run the decode
- * step token by token.  Synchronous.  Errors: OUT_OF_RANGE, INVALID_ARG, CUDA. */
+ * logits_host when not NULL; argmax to argmax_host when not NULL).  F16 and
+ * Q8_0 weights run the projections as tensor-core GEMMs on F16 operands (a
+ * Q8_0 matrix is expanded to F16, d*q rounded to nearest even, just before its
+ * GEMM) when dim, n_heads*head_dim and ffn_dim are multiples of 64; otherwise,
+ * and for F32 weights, the decode step runs token by token.  Synchronous.
+ * Errors: OUT_OF_RANGE, INVALID_ARG, CUDA. */
 int llm_prefill(llm_handle *h, const int32_t *tokens_host, int32_t n, int32_t pos0,
                 float *logits_host, int32_t *argmax_host);
 

@@ -1,4 +1,4 @@
-// Batched prefill for F16 weights ("What a Llama model computes, and why",
+// Batched prefill for F16 and Q8_0 weights ("What a Llama model computes, and why",
 // §4: the same pass as the decode step, applied to n tokens at once; every
 // K/V row is written, token i attends to rows 0..pos0+i, and only the last
 // token's logits are produced).
@@ -6,7 +6,8 @@
 // The projections are tensor-core GEMMs on the 5th-generation tensor cores:
 // C[M][N] = A[M][K] . W[N][K]^T with A the token rows (F16, rounded to
 // nearest even from the F32 activations) and W a weight matrix in the
-// library's row layout (F16, K contiguous), F32 accumulation in tensor
+// library's row layout (F16, K contiguous; a Q8_0 matrix is first expanded
+// to F16, d * qs rounded to nearest even), F32 accumulation in tensor
 // memory.  One CTA computes one 128 x BN tile (BN 64 for the narrow outputs,
 // 128 for the wide gate/up one; two CTAs per SM): thread 0 streams 128 x 64
 // tiles of A and BN x 64 tiles of W into a ring with 2-D TMA (128-byte
@@ -19,6 +20,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <string>
 #include <vector>
 
@@ -183,12 +185,43 @@ __global__ void __launch_bounds__(128, 2) gemm_f16_kernel(const __grid_constant_
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kGBN));
 }
 
-// Embedding rows of the batch (F16 weights widened exactly).
-__global__ void embed_rows_kernel(const int* tok, int n, DMat embd, int dim, float* X) {
+// Embedding rows of the batch: F16 widened, or Q8_0 decoded as d * qs (both
+// exact in F32; Q8_0 quants are stored as qs + 128).
+__global__ void embed_rows_kernel(const int* tok, int n, DMat embd, int wtype, int dim, float* X) {
     const int i = blockIdx.x;
     if (i >= n) return;
-    const __half* row = reinterpret_cast<const __half*>(embd.q) + (size_t)tok[i] * embd.cols;
-    for (int d = threadIdx.x; d < dim; d += blockDim.x) X[(size_t)i * dim + d] = __half2float(row[d]);
+    const size_t r = (size_t)tok[i];
+    for (int d = threadIdx.x; d < dim; d += blockDim.x) {
+        float v;
+        if (wtype == LLM_Q8_0)
+            v = __fmul_rn(__half2float(embd.d[r * embd.dstride + d / 32]), (float)((int)embd.q[r * embd.cols + d] - 128));
+        else
+            v = __half2float(reinterpret_cast<const __half*>(embd.q)[r * embd.cols + d]);
+        X[(size_t)i * dim + d] = v;
+    }
+}
+
+// A Q8_0 matrix (library layout) expanded to F16 for the tensor-core GEMMs:
+// d * qs, exact in F32, rounded to nearest even (the prefill's operand
+// precision; the decode step keeps the exact values).  8 values per thread.
+__global__ void q8_to_f16_kernel(DMat m, int rows, __half* out) {
+    const long long groups = (long long)rows * m.cols / 8;
+    for (long long gidx = blockIdx.x * (long long)blockDim.x + threadIdx.x; gidx < groups;
+         gidx += (long long)gridDim.x * blockDim.x) {
+        const long long e = gidx * 8;
+        const long long r = e / m.cols;
+        const int c = (int)(e - r * m.cols);
+        const float d = __half2float(m.d[r * m.dstride + c / 32]);
+        const uint2 qv = *reinterpret_cast<const uint2*>(m.q + e);
+        const uint32_t w[2] = {qv.x, qv.y};
+        __half h[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const int q = (int)((w[k / 4] >> (8 * (k % 4))) & 0xFFu) - 128;
+            h[k] = __float2half_rn(__fmul_rn(d, (float)q));
+        }
+        *reinterpret_cast<uint4*>(out + e) = *reinterpret_cast<const uint4*>(h);
+    }
 }
 
 // RMSNorm of every row ("The Forward Pass in Java", Example 4: y = (x*scale)*g,
@@ -354,19 +387,34 @@ __global__ void final_norm_kernel(const float* x, int dim, const float* g, float
     for (int d = threadIdx.x; d < dim; d += blockDim.x) y[d] = __fmul_rn(__fmul_rn(x[d], scale), g[d]);
 }
 
-__global__ void logits_f16_kernel(DMat out, const float* y, int dim, int vocab, float* logits, unsigned long long* best) {
+__global__ void logits_kernel(DMat out, int wtype, const float* y, int dim, int vocab, float* logits,
+                              unsigned long long* best) {
     extern __shared__ float ys[];
     for (int d = threadIdx.x; d < dim; d += blockDim.x) ys[d] = y[d];
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
     unsigned long long key = 0ull;
     for (int r = blockIdx.x * wpb + warp; r < vocab; r += gridDim.x * wpb) {
-        const __half* w = reinterpret_cast<const __half*>(out.q) + (size_t)r * out.cols;
         float s = 0.f;
-        for (int d = 2 * lane; d < dim; d += 64) {
-            const float2 wv = __half22float2(*reinterpret_cast<const __half2*>(w + d));
-            s = fmaf(wv.x, ys[d], s);
-            s = fmaf(wv.y, ys[d + 1], s);
+        if (wtype == LLM_Q8_0) {
+            // lane takes 32-element blocks lane, lane + 32, ...: the block sum times its scale
+            const uint8_t* q = out.q + (size_t)r * out.cols;
+            for (int b = lane; b < dim / 32; b += 32) {
+                float t = 0.f;
+                for (int k = 0; k < 32; k += 4) {
+                    const uint32_t w4 = *reinterpret_cast<const uint32_t*>(q + b * 32 + k);
+#pragma unroll
+                    for (int j = 0; j < 4; j++) t = fmaf((float)((int)((w4 >> (8 * j)) & 0xFFu) - 128), ys[b * 32 + k + j], t);
+                }
+                s = fmaf(__half2float(out.d[(size_t)r * out.dstride + b]), t, s);
+            }
+        } else {
+            const __half* w = reinterpret_cast<const __half*>(out.q) + (size_t)r * out.cols;
+            for (int d = 2 * lane; d < dim; d += 64) {
+                const float2 wv = __half22float2(*reinterpret_cast<const __half2*>(w + d));
+                s = fmaf(wv.x, ys[d], s);
+                s = fmaf(wv.y, ys[d + 1], s);
+            }
         }
         s = warp_sum(s);
         if (lane == 0) {
@@ -427,15 +475,25 @@ cudaError_t gemm(cudaStream_t st, const CUtensorMap& ma, const CUtensorMap& mb, 
 }  // namespace
 
 bool prefill_supported(const PrefillCtx& c) {
-    return c.wtype == LLM_F16 && c.dim % kGBK == 0 && c.q_dim % kGBK == 0 && c.ffn % kGBK == 0 &&
+    return (c.wtype == LLM_F16 || c.wtype == LLM_Q8_0) && c.dim % kGBK == 0 && c.q_dim % kGBK == 0 && c.ffn % kGBK == 0 &&
            c.n_heads / c.n_kv * c.hd <= 8 * 128 && c.rope_dims / 2 <= 128;
+}
+
+// The largest layer matrix (elements): the F16 expansion of a Q8_0 one.
+static size_t prefill_expand_elems(const PrefillCtx& c) {
+    size_t m = (size_t)(c.q_dim + 2 * c.kv_dim) * c.dim;
+    m = std::max(m, (size_t)c.dim * c.q_dim);
+    m = std::max(m, (size_t)2 * c.ffn * c.dim);
+    m = std::max(m, (size_t)c.dim * c.ffn);
+    return m;
 }
 
 size_t prefill_workspace_bytes(const PrefillCtx& c) {
     const size_t M = kPrefillRows;
     auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
+    const size_t expand = c.wtype == LLM_Q8_0 ? al(prefill_expand_elems(c) * 2) : 0;
     return al(M * 4) + al(M * c.dim * 4) + al(M * c.dim * 2) + al(M * (c.q_dim + 2 * c.kv_dim) * 4) +
-           al(M * c.q_dim * 2) + al(M * c.ffn * 2) + al((size_t)c.dim * 4);
+           al(M * c.q_dim * 2) + al(M * c.ffn * 2) + al((size_t)c.dim * 4) + expand;
 }
 
 // Runs the batch; `ws` holds prefill_workspace_bytes(c).  Returns a CUDA error
@@ -450,7 +508,8 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
     float* QKV = reinterpret_cast<float*>(w); w += al(M * (c.q_dim + 2 * c.kv_dim) * 4);
     __half* Ah = reinterpret_cast<__half*>(w); w += al(M * c.q_dim * 2);
     __half* Hh = reinterpret_cast<__half*>(w); w += al(M * c.ffn * 2);
-    float* ylast = reinterpret_cast<float*>(w);
+    float* ylast = reinterpret_cast<float*>(w); w += al((size_t)c.dim * 4);
+    __half* Wx = c.wtype == LLM_Q8_0 ? reinterpret_cast<__half*>(w) : nullptr;   // F16 expansion of a Q8_0 matrix
     cudaError_t e;
 #define PF_CK(call, what)                 \
     do {                                  \
@@ -464,8 +523,10 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
         *msg = "tensor map of an activation operand";
         return cudaErrorInvalidValue;
     }
-    std::vector<CUtensorMap> mw((size_t)4 * c.n_layers);
-    for (int l = 0; l < c.n_layers; l++) {
+    // weight operands: the F16 matrices themselves, or (Q8_0) each matrix
+    // expanded to F16 into Wx just before its GEMM
+    std::vector<CUtensorMap> mw(c.wtype == LLM_F16 ? (size_t)4 * c.n_layers : 0);
+    for (int l = 0; l < (int)mw.size() / 4; l++) {
         const LayerDev& L = c.layers[l];
         if (!gemm_map(&mw[4 * l + 0], L.qkv.q, c.dim, L.qkv.rows, 64) ||
             !gemm_map(&mw[4 * l + 1], L.o.q, c.q_dim, L.o.rows, 64) ||
@@ -475,6 +536,15 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
             return cudaErrorInvalidValue;
         }
     }
+    CUtensorMap mq;
+    auto weights = [&](int l, int which, const DMat& m, int rows, int K, int box) -> const CUtensorMap* {
+        if (c.wtype == LLM_F16) return &mw[4 * l + which];
+        const long long groups = (long long)rows * K / 8;
+        const int blocks = (int)std::min<long long>((groups + 255) / 256, (long long)c.sms * 16);
+        q8_to_f16_kernel<<<blocks, 256, 0, c.st>>>(m, rows, Wx);
+        if (cudaGetLastError() != cudaSuccess || !gemm_map(&mq, Wx, K, rows, box)) return nullptr;
+        return &mq;
+    };
     const int gq = c.n_heads / c.n_kv;
     const int attn_smem = (int)(2 * sizeof(__half) * kAttnTile * c.hd +
                                 sizeof(float) * ((size_t)gq * c.hd + (size_t)gq * kAttnTile + 3 * gq));
@@ -485,14 +555,16 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
         const int nb = n - b0 < kPrefillRows ? n - b0 : kPrefillRows;
         const int p0 = pos0 + b0;
         PF_CK(cudaMemcpyAsync(tok, tokens_host + b0, (size_t)nb * 4, cudaMemcpyHostToDevice, c.st), "token upload");
-        embed_rows_kernel<<<nb, 256, 0, c.st>>>(tok, nb, c.embd, c.dim, X);
+        embed_rows_kernel<<<nb, 256, 0, c.st>>>(tok, nb, c.embd, c.wtype, c.dim, X);
         PF_CK(cudaGetLastError(), "embedding");
         for (int l = 0; l < c.n_layers; l++) {
             const LayerDev& L = c.layers[l];
             rmsnorm_rows_f16_kernel<<<nb, 256, 0, c.st>>>(X, nb, c.dim, L.attn_norm, c.eps, Xh);
             PF_CK(cudaGetLastError(), "attention RMSNorm");
+            const CUtensorMap* wm;
             GemmOut oq{QKV, L.qkv_bias, nullptr, nullptr};
-            PF_CK((gemm<64, kEpiBias>(c.st, mXh, mw[4 * l + 0], oq, nb, L.qkv.rows, c.dim, c.err)), "QKV GEMM");
+            if (!(wm = weights(l, 0, L.qkv, L.qkv.rows, c.dim, 64))) { *msg = "QKV weights"; return cudaErrorInvalidValue; }
+            PF_CK((gemm<64, kEpiBias>(c.st, mXh, *wm, oq, nb, L.qkv.rows, c.dim, c.err)), "QKV GEMM");
             rope_kv_rows_kernel<<<nb, 128, 0, c.st>>>(QKV, nb, p0, c.n_heads, c.n_kv, c.hd, c.rope_dims, c.neox,
                                                       c.theta_scale, c.rope_freqs, L.kc, L.vc);
             PF_CK(cudaGetLastError(), "RoPE and KV append");
@@ -500,19 +572,22 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
                                                                               c.attn_div, L.kc, L.vc, Ah);
             PF_CK(cudaGetLastError(), "attention");
             GemmOut oo{nullptr, nullptr, X, nullptr};
-            PF_CK((gemm<64, kEpiResidual>(c.st, mAh, mw[4 * l + 1], oo, nb, c.dim, c.q_dim, c.err)), "O GEMM");
+            if (!(wm = weights(l, 1, L.o, L.o.rows, c.q_dim, 64))) { *msg = "O weights"; return cudaErrorInvalidValue; }
+            PF_CK((gemm<64, kEpiResidual>(c.st, mAh, *wm, oo, nb, c.dim, c.q_dim, c.err)), "O GEMM");
             rmsnorm_rows_f16_kernel<<<nb, 256, 0, c.st>>>(X, nb, c.dim, L.ffn_norm, c.eps, Xh);
             PF_CK(cudaGetLastError(), "FFN RMSNorm");
             GemmOut og{nullptr, nullptr, nullptr, Hh};
-            PF_CK((gemm<128, kEpiSwiGLU>(c.st, mXh, mw[4 * l + 2], og, nb, 2 * L.gu.rows, c.dim, c.err)), "gate/up GEMM");
+            if (!(wm = weights(l, 2, L.gu, 2 * L.gu.rows, c.dim, 128))) { *msg = "gate/up weights"; return cudaErrorInvalidValue; }
+            PF_CK((gemm<128, kEpiSwiGLU>(c.st, mXh, *wm, og, nb, 2 * L.gu.rows, c.dim, c.err)), "gate/up GEMM");
             GemmOut od{nullptr, nullptr, X, nullptr};
-            PF_CK((gemm<64, kEpiResidual>(c.st, mHh, mw[4 * l + 3], od, nb, c.dim, c.ffn, c.err)), "down GEMM");
+            if (!(wm = weights(l, 3, L.down, L.down.rows, c.ffn, 64))) { *msg = "down weights"; return cudaErrorInvalidValue; }
+            PF_CK((gemm<64, kEpiResidual>(c.st, mHh, *wm, od, nb, c.dim, c.ffn, c.err)), "down GEMM");
         }
         if (b0 + nb == n) {
             final_norm_kernel<<<1, 256, 0, c.st>>>(X + (size_t)(nb - 1) * c.dim, c.dim, c.out_norm, c.eps, ylast);
             PF_CK(cudaGetLastError(), "final RMSNorm");
-            logits_f16_kernel<<<c.sms * 4, 256, (size_t)c.dim * 4, c.st>>>(c.out, ylast, c.dim, c.vocab, c.logits,
-                                                                           c.best);
+            logits_kernel<<<c.sms * 4, 256, (size_t)c.dim * 4, c.st>>>(c.out, c.wtype, ylast, c.dim, c.vocab, c.logits,
+                                                                       c.best);
             PF_CK(cudaGetLastError(), "logits");
             argmax_publish_kernel<<<1, 1, 0, c.st>>>(c.best, c.argmax_dev);
             PF_CK(cudaGetLastError(), "argmax");

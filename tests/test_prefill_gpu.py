@@ -1,9 +1,10 @@
-"""Batched prefill (F16 weights, tensor-core GEMMs) against the oracle and
-against the decode step run token by token ("What a Llama model computes, and
-why" §4: prefill equals token-by-token).  The GEMM operands are rounded to F16
-(the reading of the prefill precision), so the comparison is within the F16
-logit tolerance; the K/V rows it writes are compared element-wise within the
-same tolerance."""
+"""Batched prefill (F16 and Q8_0 weights, tensor-core GEMMs) against the
+oracle and against the decode step run token by token ("What a Llama model
+computes, and why" §4: prefill equals token-by-token).  The GEMM operands are
+rounded to F16 (the reading of the prefill precision; a Q8_0 weight becomes
+d * q rounded to F16), so the comparison is within the F16/Q8_0 logit
+tolerance; the K/V rows it writes are compared element-wise within the same
+tolerance."""
 import numpy as np
 import pytest
 
@@ -33,7 +34,9 @@ def kv_as_float(dec, layer, which, rows):
     return t.cpu().numpy().view(np.float16).astype(np.float64)
 
 
-@pytest.mark.parametrize("kw", [{}, dict(rope_neox=0, bias=False, tied=False, number=72)])
+@pytest.mark.parametrize("kw", [{}, dict(rope_neox=0, bias=False, tied=False, number=72),
+                                dict(wtype=synth.Q8_0, rope_neox=0, bias=False, number=73),
+                                dict(wtype=synth.Q8_0, tied=False, rope_freqs=True, number=74)])
 def test_prefill_matches_oracle_and_continues(lib, kw):
     cfg = f16cfg(**kw)
     W = synth.make_weights(cfg)
@@ -64,10 +67,12 @@ def test_prefill_matches_oracle_and_continues(lib, kw):
     dec.close()
 
 
-def test_prefill_512_full_width_equals_token_by_token(lib):
-    """The 1B-shaped Qwen2-style F16 model (NEOX, biases, tied): a 512-token
-    batched prefill against 512 decode steps of the library's decode path."""
-    cfg = synth.QWEN2_F16.scaled(max_seq=600)
+@pytest.mark.parametrize("base", [synth.QWEN2_F16, synth.LLAMA1B_Q8], ids=["qwen2-1b-f16", "llama-3.2-1b-q8_0"])
+def test_prefill_512_full_width_equals_token_by_token(lib, base):
+    """The 1B-shaped models (Qwen2-style F16: NEOX, biases, tied; Llama 3.2
+    Q8_0: normal pairs, frequency factors, tied): a 512-token batched prefill
+    against 512 decode steps of the library's decode path."""
+    cfg = base.scaled(max_seq=600)
     W = synth.make_weights(cfg)
     toks = synth.prompt(cfg, 512)
     a = lib.Decoder(cfg, W)
