@@ -175,8 +175,8 @@ int llm_test_dequant_rows(llm_handle *h, int which, int layer, int32_t row0, int
 int llm_trace_read(llm_handle *h, uint64_t *host, int32_t *sms);
 
 /* One decode step like llm_decode_step_async, but its working memory (the
- * residual stream, q/k/v, attention partials, FFN activations, grid counters,
- * argmax and error words) lives in a fixed 4 MiB device array inside the
+ * tagged activation vectors of every layer, attention partials, grid
+ * counters, argmax and error words) lives in a fixed 16 MiB device array inside the
  * library rather than in buffers of the handle, so the call allocates no
  * memory of any kind.  The described decode pass has no counterpart of this
  * call: it exists for callers that may not allocate device memory while

@@ -65,6 +65,31 @@ __device__ __forceinline__ bool bounded_wait(Ready ready, int* err) {
     }
 }
 
+// Tagged elements once they carry `tag` (the step's): four consecutive ones
+// (16-byte aligned), or one.  After a timeout (the error word is set) the
+// values read as zero; every later wait of the step then gives up at once.
+__device__ __forceinline__ float4 poll4(const unsigned long long* a, unsigned tag, int* err) {
+    ulonglong2 w0, w1;
+    const auto ready = [&] {
+        w0 = ld_tagged2(a);
+        w1 = ld_tagged2(a + 2);
+        return ((unsigned)(w0.x >> 32) == tag) & ((unsigned)(w0.y >> 32) == tag) & ((unsigned)(w1.x >> 32) == tag) &
+               ((unsigned)(w1.y >> 32) == tag);
+    };
+    if (!bounded_wait(ready, err)) return make_float4(0.f, 0.f, 0.f, 0.f);
+    return make_float4(__uint_as_float((unsigned)w0.x), __uint_as_float((unsigned)w0.y),
+                       __uint_as_float((unsigned)w1.x), __uint_as_float((unsigned)w1.y));
+}
+__device__ __forceinline__ float poll1(const unsigned long long* a, unsigned tag, int* err) {
+    unsigned long long w;
+    const auto ready = [&] {
+        asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(a) : "memory");
+        return (unsigned)(w >> 32) == tag;
+    };
+    if (!bounded_wait(ready, err)) return 0.f;
+    return __uint_as_float((unsigned)w);
+}
+
 // Shared-memory regions, addressed from the dynamic smem base with the
 // offsets in the (constant-bank) parameters, so no region pointer stays live.
 struct Smem {
@@ -238,6 +263,8 @@ struct Consumer {
     RingPos rp;            // next slot to consume
     int tid, warp, lane;
     int own0, own1;        // residual rows this CTA owns (rows of Wo and Wdown)
+    unsigned tag;          // this step's tag of the tagged vectors
+    TvLayout tl;
     int tk = -1;           // trace slot of the current GEMV's first chunk
     long long waited = 0;  // trace builds: cycles spent waiting for ring slots
 
@@ -246,6 +273,13 @@ struct Consumer {
         warp = tid >> 5;
         lane = tid & 31;
         cta_rows(p.dim, own0, own1);
+        tag = __ldcg(p.epoch) + 1u;
+        tl = tv_layout(p.dim, p.q_dim, p.kv_dim, p.ffn);
+    }
+
+    // layer l's tagged vector at element offset `off` of its set
+    __device__ __forceinline__ unsigned long long* tv(int l, long long off) const {
+        return p.tv + (long long)l * tl.stride + off;
     }
 
     __device__ bool aborted() const { return *(volatile int*)&sm.misc()[0] != 0; }
@@ -270,20 +304,6 @@ struct Consumer {
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty()[slot]);
         rp.advance(p.ns);
-    }
-
-    // Grid-wide dependency: thread 0 waits for counter >= target.
-    __device__ bool wait_counter(const unsigned* c, unsigned target) {
-        if (tid == 0 && !bounded_wait([&] { return ld_acquire(c) >= target; }, p.err)) sm.misc()[0] = 1;
-        consumer_sync();
-        return !aborted();
-    }
-
-    __device__ void signal(unsigned* c) {
-        consumer_sync();
-        // the barrier orders every consumer's writes before thread 0's
-        // release; the release makes them visible at GPU scope
-        if (tid == 0) red_release_add(c, 1u);
     }
 
     // Start copying a norm's gains (n floats, n % 4 == 0) into shared memory;
@@ -432,22 +452,24 @@ __device__ __forceinline__ void lane_rows(const uint8_t* const (&w)[N], const ui
 }
 
 // ------------------------------------------------------------------ GEMV --
-struct EpiStore {                 // out[r] = v (+ bias of this CTA's row r)
-    float* out;
+struct EpiStore {                 // out[r] = v (+ bias of this CTA's row r), tagged
+    unsigned long long* out;
     const float* bias;            // smem, indexed from the CTA's first row, or nullptr
     int r0;
-    __device__ void row(int r, float v) { __stcg(out + r, bias ? v + bias[r - r0] : v); }
+    unsigned tag;
+    __device__ void row(int r, float v) { st_tagged(out + r, bias ? v + bias[r - r0] : v, tag); }
     __device__ void pair(int, float, float) {}
     __device__ void finish(Consumer&) {}
 };
-struct EpiResidual {              // x[r] += v, the owned row kept in smem
-    float* x;
+struct EpiResidual {              // x[r] = own[r] + v, the owned row kept in smem; x tagged
+    unsigned long long* x;
     float* own;
     int own0;
+    unsigned tag;
     __device__ void row(int r, float v) {
         const float y = own[r - own0] + v;
         own[r - own0] = y;
-        __stcg(x + r, y);
+        st_tagged(x + r, y, tag);
     }
     __device__ void pair(int, float, float) {}
     __device__ void finish(Consumer&) {}
@@ -457,7 +479,7 @@ struct EpiResidual {              // x[r] += v, the owned row kept in smem
 // nonlinearity is applied to all of the CTA's rows at once at the end of the
 // phase, off the rows' critical path.
 struct EpiSwiGLU {
-    float* u;
+    unsigned long long* u;        // tagged
     float* gs;                    // smem [2 * rows of this CTA]
     int i0, i1;                   // this CTA's super-rows
     // row r of the interleaved matrix: gate (even) or up (odd) of super-row r / 2
@@ -471,7 +493,7 @@ struct EpiSwiGLU {
         for (int k = c.tid; k < i1 - i0; k += kConsumers) {
             const float g = gs[2 * k], up = gs[2 * k + 1];
             const float e = expf(-g);
-            __stcg(u + i0 + k, __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), up));
+            st_tagged(u + i0 + k, __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), up), c.tag);
         }
     }
 };
@@ -487,12 +509,12 @@ struct EpiLogits {                // logits[r] = v, keep this lane's best (value
     __device__ void finish(Consumer&) {}
 };
 
-// Where a GEMV phase takes its activation vector: a global vector (written
+// Where a GEMV phase takes its activation vector: a tagged vector (written
 // by this step) or the embedding row of `token`, optionally RMSNormed with
 // gains g ("The Forward Pass in Java", Example 4: y = (x * scale) * g with
 // scale = 1/sqrt(mean(x^2) + eps), the sum of squares a float tree sum).
 struct XSrc {
-    const float* x;               // nullptr: the embedding row
+    const unsigned long long* x;  // tagged; nullptr: the embedding row
     const float* g;               // nullptr: no norm
     int n;                        // length of the vector
 };
@@ -545,7 +567,7 @@ __device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& 
         for (int i = c.tid; i < src.n / 4; i += kConsumers) {
             float4 v;
             if (src.x) {
-                v = __ldcg(reinterpret_cast<const float4*>(src.x) + i);
+                v = poll4(src.x + 4 * i, c.tag, c.p.err);
             } else {
                 v = make_float4(weight_at<DT>(c.p.embd, token, 4 * i), weight_at<DT>(c.p.embd, token, 4 * i + 1),
                                 weight_at<DT>(c.p.embd, token, 4 * i + 2), weight_at<DT>(c.p.embd, token, 4 * i + 3));
@@ -580,10 +602,10 @@ __device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& 
         }
     } else {
         if (src.x) {
-            const float4* s4 = reinterpret_cast<const float4*>(src.x + col0);
 #pragma unroll
             for (int k = 0; k < 8; k++) {
-                const float4 v = have && col0 + 4 * k < src.n ? __ldcg(s4 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 v = have && col0 + 4 * k < src.n ? poll4(src.x + col0 + 4 * k, c.tag, c.p.err)
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
                 x2[2 * k] = make_float2(v.x, v.y);
                 x2[2 * k + 1] = make_float2(v.z, v.w);
             }
@@ -729,6 +751,9 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
         }
     }
     epi.finish(c);
+    // narrow teams have no finishing barrier: the next phase's staging must
+    // not overwrite the staged vector (or the gains) while a warp still reads it
+    if (tw <= 32) consumer_sync();
 #ifdef LLM_TRACE
     if (c.tid == 0 && c.tk >= 0 && c.p.trace) c.p.trace[(size_t)blockIdx.x * kTraceSlots + c.tk - 160 + 768] = c.waited;
     c.waited = 0;
@@ -797,16 +822,17 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
     __half* vp = kp + hd;                                          // [hd] this position's V row (F16)
 
     const bool writer = t0 <= p.pos && p.pos < t1;
+    const unsigned long long* qkv = c.tv(layer, c.tl.qkv);
     {
         float qv[2], kv = 0.f, vv = 0.f;
 #pragma unroll
         for (int k = 0; k < 2; k++) {
             const int i = tid + k * kConsumers;
-            qv[k] = i < GD ? __ldcg(p.qkv + h0 * hd + i) : 0.f;
+            qv[k] = i < GD ? poll1(qkv + h0 * hd + i, c.tag, p.err) : 0.f;
         }
         if (writer && tid < hd) {
-            kv = __ldcg(p.qkv + p.q_dim + g * hd + tid);
-            vv = __ldcg(p.qkv + p.q_dim + p.kv_dim + g * hd + tid);
+            kv = poll1(qkv + p.q_dim + g * hd + tid, c.tag, p.err);
+            vv = poll1(qkv + p.q_dim + p.kv_dim + g * hd + tid, c.tag, p.err);
         }
 #pragma unroll
         for (int k = 0; k < 2; k++) {
@@ -970,10 +996,9 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
 #pragma unroll
                 for (int k = 0; k < 32; k++)
                     if (k < S) v = fmaf(wgt[hh * S + k], av[k], v);
-                __stcg(p.attn + (h0 + hh) * hd + ii, v);
+                st_tagged(c.tv(layer, c.tl.attn) + (h0 + hh) * hd + ii, v, c.tag);
             }
         }
-        c.signal(p.counters + 5 * layer + 1);
     }
     consumer_sync();
     return true;
@@ -992,32 +1017,26 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
     c.prefetch_gains(p.layers[0].attn_norm, p.dim);
     rope_table(p, sm, tid);
     // this CTA's residual rows start as the embedding row's values
-    for (int i = c.own0 + tid; i < c.own1; i += kConsumers) {
-        const float v = weight_at<DT>(p.embd, token, i);
-        sm.xown()[i - c.own0] = v;
-        __stcg(p.x + i, v);
-    }
+    for (int i = c.own0 + tid; i < c.own1; i += kConsumers) sm.xown()[i - c.own0] = weight_at<DT>(p.embd, token, i);
+    // Phases wait for their inputs through the tags of the vectors they read;
+    // the only counters left are the attention merges and the end of the step.
     for (int l = 0; l < p.n_layers; l++) {
         const LayerDev& L = p.layers[l];
-        unsigned* ctr = p.counters + 5 * l;
         // ---- QKV
         int q0, q1;
         cta_rows(L.qkv.rows, q0, q1);
         if (L.qkv_bias)
             for (int i = tid; i < q1 - q0; i += kConsumers) sm.bias()[i] = __ldg(L.qkv_bias + q0 + i);
-        if (l > 0 && !c.wait_counter(ctr - 1, G)) return false;
         if (tid == 0) trace_mark(p, 10 * l);
         c.tk = 160 + 4 * l;
         {
-            const XSrc src{l == 0 ? nullptr : p.x, L.attn_norm, p.dim};
-            EpiStore e{p.qkv, L.qkv_bias ? sm.bias() : nullptr, q0};
+            const XSrc src{l == 0 ? nullptr : c.tv(l - 1, c.tl.xd), L.attn_norm, p.dim};
+            EpiStore e{c.tv(l, c.tl.qkv), L.qkv_bias ? sm.bias() : nullptr, q0, c.tag};
             gemv_consume<DT, false>(c, L.qkv, src, token, e);
         }
         if (tid == 0) trace_mark(p, 10 * l + 1);
-        c.signal(ctr + 0);
         c.prefetch_gains(L.ffn_norm, p.dim);             // QKV has read its gains
         // ---- ATTN
-        if (!c.wait_counter(ctr + 0, G)) return false;
         if (tid == 0) trace_mark(p, 10 * l + 2);
         {
             const int units = p.n_kv * p.splits;
@@ -1026,50 +1045,43 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         }
         if (tid == 0) trace_mark(p, 10 * l + 3);
         // ---- O
-        if (!c.wait_counter(ctr + 1, p.n_kv)) return false;
         if (tid == 0) trace_mark(p, 10 * l + 4);
         c.tk = 160 + 4 * l + 1;
         {
-            const XSrc src{p.attn, nullptr, p.q_dim};
-            EpiResidual e{p.x, sm.xown(), c.own0};
+            const XSrc src{c.tv(l, c.tl.attn), nullptr, p.q_dim};
+            EpiResidual e{c.tv(l, c.tl.xo), sm.xown(), c.own0, c.tag};
             gemv_consume<DT, false>(c, L.o, src, token, e);
         }
         if (tid == 0) trace_mark(p, 10 * l + 5);
-        c.signal(ctr + 2);
         // ---- GU
-        if (!c.wait_counter(ctr + 2, G)) return false;
         if (tid == 0) trace_mark(p, 10 * l + 6);
         c.tk = 160 + 4 * l + 2;
         {
-            const XSrc src{p.x, L.ffn_norm, p.dim};
+            const XSrc src{c.tv(l, c.tl.xo), L.ffn_norm, p.dim};
             int i0, i1;
             cta_rows(L.gu.rows, i0, i1);
-            EpiSwiGLU e{p.u, sm.bias(), i0, i1};
+            EpiSwiGLU e{c.tv(l, c.tl.u), sm.bias(), i0, i1};
             gemv_consume<DT, false>(c, L.gu, src, token, e);
         }
         if (tid == 0) trace_mark(p, 10 * l + 7);
-        c.signal(ctr + 3);
         c.prefetch_gains(l + 1 < p.n_layers ? p.layers[l + 1].attn_norm : p.out_norm, p.dim);
         // ---- DOWN
-        if (!c.wait_counter(ctr + 3, G)) return false;
         if (tid == 0) trace_mark(p, 10 * l + 8);
         c.tk = 160 + 4 * l + 3;
         {
-            const XSrc src{p.u, nullptr, p.ffn};
-            EpiResidual e{p.x, sm.xown(), c.own0};
+            const XSrc src{c.tv(l, c.tl.u), nullptr, p.ffn};
+            EpiResidual e{c.tv(l, c.tl.xd), sm.xown(), c.own0, c.tag};
             gemv_consume<DT, false>(c, L.down, src, token, e);
         }
         if (tid == 0) trace_mark(p, 10 * l + 9);
-        c.signal(ctr + 4);
     }
     // ---- LOGITS + argmax
-    unsigned* fin = p.counters + 5 * p.n_layers;
-    if (!c.wait_counter(fin - 1, G)) return false;
+    unsigned* fin = p.counters;
     if (tid == 0) trace_mark(p, 240);
     c.tk = -1;
     EpiLogits e{p.logits, 0ull};
     {
-        const XSrc src{p.x, p.out_norm, p.dim};
+        const XSrc src{c.tv(p.n_layers - 1, c.tl.xd), p.out_norm, p.dim};
         gemv_consume<DT, false>(c, p.out, src, token, e);
     }
     if (tid == 0) trace_mark(p, 241);
@@ -1091,9 +1103,11 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
     }
     consumer_sync();
     if (sm.misc()[1]) {
-        // every CTA has passed its last wait: publish the argmax, re-arm the counters
+        // every CTA has passed its last wait: publish the argmax, re-arm the
+        // counters, and make this step's tag the last completed one
         __threadfence();
         if (tid == 0) *p.token_out = argmax_key_index(atomicExch(p.best, 0ull));
+        if (tid == 0) *p.epoch = c.tag;
         if (tid == 0) trace_mark(p, 242);
         const int nc = n_phase_counters(p.n_layers) + p.n_layers * p.n_kv;
         for (int i = tid; i < nc; i += kConsumers) p.counters[i] = 0u;

@@ -52,7 +52,10 @@ struct llm_handle {
     const float* out_norm = nullptr;
     const float* rope_freqs = nullptr;
 
-    float *x = nullptr, *qkv = nullptr, *attn = nullptr, *u = nullptr, *logits = nullptr, *attn_part = nullptr;
+    unsigned long long* tv = nullptr;  // tagged activation vectors of every layer
+    size_t tv_words = 0;
+    unsigned* epoch = nullptr;          // tag of the last completed step
+    float *logits = nullptr, *attn_part = nullptr;
     unsigned long long* best = nullptr;
     unsigned* counters = nullptr;
     int n_counters = 0;
@@ -340,16 +343,14 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
     h->n_counters = n_phase_counters(L) + L * c.n_kv_heads;
     size_t a = 0;
     auto take = [&](size_t b) { size_t o = a; a += align256(b); return o; };
-    const size_t o_x = take((size_t)d * 4), o_qkv = take((size_t)(q + 2 * kv) * 4), o_attn = take((size_t)q * 4),
-                 o_u = take((size_t)f * 4), o_logits = take((size_t)c.vocab * 4),
+    h->tv_words = (size_t)L * (size_t)tv_layout(d, q, kv, f).stride;
+    const size_t o_tv = take(h->tv_words * 8), o_epoch = take(4), o_logits = take((size_t)c.vocab * 4),
                  o_part = take((size_t)c.n_heads * h->max_splits * (c.head_dim + 2) * 4), o_best = take(8),
                  o_ctr = take((size_t)h->n_counters * 4), o_err = take(4), o_tin = take(4), o_tout = take(4);
     CKC(cudaMalloc(&h->act, a));
     CKC(cudaMemsetAsync(h->act, 0, a, h->st));
-    h->x = (float*)(h->act + o_x);
-    h->qkv = (float*)(h->act + o_qkv);
-    h->attn = (float*)(h->act + o_attn);
-    h->u = (float*)(h->act + o_u);
+    h->tv = (unsigned long long*)(h->act + o_tv);
+    h->epoch = (unsigned*)(h->act + o_epoch);
     h->logits = (float*)(h->act + o_logits);
     h->attn_part = (float*)(h->act + o_part);
     h->best = (unsigned long long*)(h->act + o_best);
@@ -442,7 +443,7 @@ static int launch_step(llm_handle* h, const int* token_dev, int pos, int* argmax
     p.ffn = c.ffn_dim; p.vocab = c.vocab; p.max_seq = c.max_seq; p.rope_dims = c.rope_dims; p.neox = c.rope_neox;
     p.q_dim = h->q_dim; p.kv_dim = h->kv_dim;
     p.eps = c.eps; p.theta_scale = h->theta_scale; p.attn_div = h->attn_div;
-    p.x = h->x; p.qkv = h->qkv; p.attn = h->attn; p.u = h->u; p.logits = h->logits; p.attn_part = h->attn_part;
+    p.tv = h->tv; p.epoch = h->epoch; p.logits = h->logits; p.attn_part = h->attn_part;
     p.max_splits = h->max_splits; p.best = h->best; p.counters = h->counters; p.err = h->err;
     p.token_in = token_dev; p.token_out = argmax_dev; p.pos = pos;
     int s = (pos + 1 + 15) / 16;
@@ -468,6 +469,9 @@ extern "C" int llm_reset(llm_handle* h) {
     CK(h, cudaMemsetAsync(h->err, 0, 4, h->st));
     CK(h, cudaMemsetAsync(h->counters, 0, (size_t)h->n_counters * 4, h->st));
     CK(h, cudaMemsetAsync(h->best, 0, 8, h->st));
+    // a step that stopped early may have left words with the next step's tag
+    CK(h, cudaMemsetAsync(h->tv, 0, h->tv_words * 8, h->st));
+    CK(h, cudaMemsetAsync(h->epoch, 0, 4, h->st));
     CK(h, cudaStreamSynchronize(h->st));
     h->broken = false;
     return LLM_OK;
@@ -666,7 +670,7 @@ extern "C" const char* llm_last_error(const llm_handle* h) { return h ? h->last_
 // on it and must be serialised by the caller.  The first call on a device
 // looks up the array's address (cudaGetSymbolAddress, with that device
 // current); make that first call before any stream capture begins.
-constexpr size_t kStaticScratchBytes = (size_t)4 << 20;   // 4 MiB
+constexpr size_t kStaticScratchBytes = (size_t)16 << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char g_step_scratch[kStaticScratchBytes];
 
 namespace {
@@ -678,7 +682,7 @@ size_t scratch_align(size_t b) { return (b + 255) & ~(size_t)255; }
 
 // Scratch layout of a handle's step: offsets in bytes, total in *bytes.
 struct ScratchLayout {
-    size_t x, qkv, attn, u, part, best, counters, err, total;
+    size_t epoch, tv, tv_bytes, part, best, counters, err, total;
 };
 
 ScratchLayout scratch_layout(const llm_handle* h) {
@@ -686,10 +690,9 @@ ScratchLayout scratch_layout(const llm_handle* h) {
     ScratchLayout s{};
     size_t o = 0;
     auto take = [&](size_t b) { size_t at = o; o += scratch_align(b); return at; };
-    s.x = take((size_t)c.dim * 4);
-    s.qkv = take((size_t)(h->q_dim + 2 * h->kv_dim) * 4);
-    s.attn = take((size_t)h->q_dim * 4);
-    s.u = take((size_t)c.ffn_dim * 4);
+    s.epoch = take(4);                                  // shared by every handle: tags only grow
+    s.tv_bytes = h->tv_words * 8;
+    s.tv = take(s.tv_bytes);
     s.part = take((size_t)c.n_heads * h->max_splits * (c.head_dim + 2) * 4);
     s.best = take(8);                                   // these three must start at zero
     s.counters = take((size_t)h->n_counters * 4);
@@ -742,10 +745,8 @@ extern "C" int llm_decode_step_noalloc(llm_handle* h, const int32_t* token_dev, 
     p.ffn = c.ffn_dim; p.vocab = c.vocab; p.max_seq = c.max_seq; p.rope_dims = c.rope_dims; p.neox = c.rope_neox;
     p.q_dim = h->q_dim; p.kv_dim = h->kv_dim;
     p.eps = c.eps; p.theta_scale = h->theta_scale; p.attn_div = h->attn_div;
-    p.x = reinterpret_cast<float*>(base + sl.x);
-    p.qkv = reinterpret_cast<float*>(base + sl.qkv);
-    p.attn = reinterpret_cast<float*>(base + sl.attn);
-    p.u = reinterpret_cast<float*>(base + sl.u);
+    p.tv = reinterpret_cast<unsigned long long*>(base + sl.tv);
+    p.epoch = reinterpret_cast<unsigned*>(base + sl.epoch);
     p.logits = logits_dev;
     p.attn_part = reinterpret_cast<float*>(base + sl.part);
     p.max_splits = h->max_splits;
@@ -761,6 +762,11 @@ extern "C" int llm_decode_step_noalloc(llm_handle* h, const int32_t* token_dev, 
     CK(h, cudaMemcpyAsync(&h->pinned->err, base + sl.err, 4, cudaMemcpyDeviceToHost, h->st));
     CK(h, cudaStreamSynchronize(h->st));
     const int e = h->pinned->err;
+    if (e) {
+        // a step that stopped early may have left words with the next step's tag
+        CK(h, cudaMemsetAsync(base + sl.tv, 0, sl.tv_bytes, h->st));
+        CK(h, cudaStreamSynchronize(h->st));
+    }
     if (e & kErrTimeout) { h->broken = true; return fail(h, LLM_ERR_DEVICE_TIMEOUT, "a bounded device wait expired"); }
     if (e & kErrToken) { h->broken = true; return fail(h, LLM_ERR_OUT_OF_RANGE, "the device-side token was out of range"); }
     return LLM_OK;

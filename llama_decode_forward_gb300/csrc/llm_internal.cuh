@@ -54,8 +54,18 @@ struct LayerDev {
     __half* vc;
 };
 
-// Counters of one step: 5 phases per layer + the logits phase, then one merge
-// counter per (layer, kv head).  All zero between steps.
+// Counters of one step: the logits phase, then one merge counter per
+// (layer, kv head).  All zero between steps.
+//
+// Activation vectors that cross the grid are tagged: each element is one
+// 64-bit word, the float's bits in the low half and the step's tag in the high
+// half, written with one store.  A reader waits until the words it needs carry
+// the current tag, so the data is its own ready flag (no separate counter, no
+// release/acquire round trip).  Each layer has its own set of vectors, each
+// written exactly once per step:
+//   qkv [q_dim + 2 kv_dim], attn [q_dim], xo [dim] (residual after the
+//   attention block), u [ffn] (silu(gate) * up), xd [dim] (residual after the
+//   feed-forward block).
 struct StepParams {
     const LayerDev* layers;
     const void* kv_maps;      // CUtensorMap[2 * n_layers]: K and V cache of each layer, box [attn_rows][hd]
@@ -66,10 +76,8 @@ struct StepParams {
     int n_layers, dim, n_heads, n_kv, hd, ffn, vocab, max_seq, rope_dims, neox, q_dim, kv_dim;
     float eps, theta_scale, attn_div;
 
-    float* x;                 // residual stream [dim]
-    float* qkv;               // [q_dim + 2 kv_dim]
-    float* attn;              // attention output [q_dim]
-    float* u;                 // silu(gate) * up [ffn]
+    unsigned long long* tv;   // tagged vectors, n_layers sets (tv_elems_per_layer words each)
+    unsigned* epoch;          // tag of the last completed step; this step writes epoch + 1
     float* logits;            // [vocab]
     float* attn_part;         // acc [n_heads][max_splits][hd], then (m, l) [n_heads][max_splits][2]
     int max_splits;
@@ -103,7 +111,23 @@ struct StepParams {
 //   producer  896 + 4*l + {0..3}: SM cycles the producer waited for free slots while issuing them
 constexpr int kTraceSlots = 1024;
 
-__host__ __device__ inline int n_phase_counters(int n_layers) { return 5 * n_layers + 1; }
+__host__ __device__ inline int n_phase_counters(int) { return 1; }
+
+// Tagged-vector set of one layer: element offsets of its vectors.
+struct TvLayout {
+    long long qkv, attn, xo, u, xd, stride;
+};
+__host__ __device__ inline TvLayout tv_layout(int dim, int q_dim, int kv_dim, int ffn) {
+    TvLayout t;
+    t.qkv = 0;
+    t.attn = t.qkv + q_dim + 2LL * kv_dim;
+    t.xo = t.attn + q_dim;
+    t.u = t.xo + dim;
+    t.xd = t.u + ffn;
+    t.stride = t.xd + dim;
+    t.stride += t.stride & 1;          // 16-byte aligned sets
+    return t;
+}
 
 // Batched prefill (F16 weights): what it needs of a handle.
 constexpr int kPrefillRows = 512;            // tokens per tensor-core batch
@@ -145,6 +169,19 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// One tagged element: the float's bits and the tag in a single 64-bit store.
+__device__ __forceinline__ void st_tagged(unsigned long long* a, float v, unsigned tag) {
+    const unsigned long long w = ((unsigned long long)tag << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(a), "l"(w) : "memory");
+}
+
+// Two tagged elements (16-byte aligned); each 64-bit word is read whole.
+__device__ __forceinline__ ulonglong2 ld_tagged2(const unsigned long long* a) {
+    ulonglong2 r;
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(r.x), "=l"(r.y) : "l"(a) : "memory");
+    return r;
 }
 
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
