@@ -225,6 +225,7 @@ struct Producer {
         const void* kmap = maps + (size_t)(2 * layer) * 128;
         const void* vmap = maps + (size_t)(2 * layer + 1) * 128;
         const uint32_t half_bytes = (uint32_t)(P * p.hd * 2);
+        const int W = p.attn_w, nsub = p.hd / W;                   // sub-tiles of [P][W] per tile
         for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
             int g, s, t0, t1;
             unit_range(p, unit, S, g, s, t0, t1);
@@ -233,8 +234,10 @@ struct Producer {
                 uint8_t* dst = acquire(slot);
                 if (!dst) return;
                 mbar_arrive_expect_tx(&sm.full()[slot], 2 * half_bytes);
-                tma_2d_g2s(dst, kmap, g * p.hd, c0, &sm.full()[slot]);
-                tma_2d_g2s(dst + half_bytes, vmap, g * p.hd, c0, &sm.full()[slot]);
+                for (int j = 0; j < nsub; j++) {
+                    tma_2d_g2s(dst + (size_t)j * P * W * 2, kmap, g * p.hd + j * W, c0, &sm.full()[slot]);
+                    tma_2d_g2s(dst + half_bytes + (size_t)j * P * W * 2, vmap, g * p.hd + j * W, c0, &sm.full()[slot]);
+                }
                 issued();
             }
         }
@@ -804,24 +807,22 @@ __device__ __forceinline__ void store_kv(__half* kc, __half* vc, int pos, int kv
 // attn_part[n_heads*max_splits*hd + 2*(h*max_splits + s)].  The last unit of
 // a kv head to finish merges its splits: per head M = max_s m_s,
 // w_s = e^(m_s - M) / sum_s' e^(m_s' - M) l_s', attn = sum_s w_s acc_s.
-__device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int unit) {
+//
+// Scratch shared by both forms of the unit: q_s [gq][hd] (rotated q, F32),
+// kf [hd] (this position's k, F32), kp and vp [hd] each (its K and V rows,
+// F16); the scalar form's score buffers follow.
+
+// q of the unit's heads, rotated, into q_s; the writer (the unit that holds
+// this step's position) rotates k, rounds K and V to F16 into kp/vp and
+// stores them in the cache.  Ends with the scratch visible to all consumers.
+__device__ void attention_prologue(Consumer& c, const LayerDev& L, int layer, int g, bool writer) {
     const StepParams& p = c.p;
     Smem& sm = c.sm;
-    const int tid = c.tid, warp = c.warp, lane = c.lane;
-    const int hd = p.hd, gq = p.n_heads / p.n_kv, P = p.attn_rows, S = p.splits;
-    int g, s, t0, t1;
-    unit_range(p, unit, S, g, s, t0, t1);
-    const int h0 = g * gq, GD = gq * hd;
-    // scratch
-    float* q_s = sm.xs();                                          // [gq][hd]
-    float* kf = q_s + GD;                                          // [hd] f32 k of this position
-    float* sc = kf + hd;                                           // [2][gq][P] scores, then probabilities
-    float* ml = sc + 2 * gq * P;                                   // [2][gq] running max m, sum l
-    float* corr = ml + 2 * gq;                                     // [2][gq] rescale of the chunk's old sums
-    __half* kp = reinterpret_cast<__half*>(corr + 2 * gq);         // [hd] this position's K row (F16)
-    __half* vp = kp + hd;                                          // [hd] this position's V row (F16)
-
-    const bool writer = t0 <= p.pos && p.pos < t1;
+    const int tid = c.tid, hd = p.hd, gq = p.n_heads / p.n_kv, h0 = g * gq, GD = gq * hd;
+    float* q_s = sm.xs();
+    float* kf = q_s + GD;
+    __half* kp = reinterpret_cast<__half*>(kf + hd);
+    __half* vp = kp + hd;
     const unsigned long long* qkv = c.tv(layer, c.tl.qkv);
     {
         float qv[2], kv = 0.f, vv = 0.f;
@@ -849,14 +850,83 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
         rope_apply(p, sm, q_s + (i / (p.rope_dims / 2)) * hd, i % (p.rope_dims / 2));
     if (writer)
         for (int i = tid; i < p.rope_dims / 2; i += kConsumers) rope_apply(p, sm, kf, i);
-    if (tid < gq) { ml[tid] = -INFINITY; ml[gq + tid] = 0.f; }
     consumer_sync();
     if (writer && tid < hd) {
         const __half kh = __float2half_rn(kf[tid]);
         kp[tid] = kh;
         store_kv(L.kc, L.vc, p.pos, p.kv_dim, g * hd, tid, kh, vp[tid]);
     }
-    consumer_sync();                                               // kp visible
+    consumer_sync();                                               // kp, vp visible
+}
+
+// After the unit's partial is stored: the last unit of kv head g (an
+// acquire-release counter) merges the splits in one round of loads and
+// writes the heads' tagged output.
+__device__ void attention_merge(Consumer& c, int layer, int g) {
+    const StepParams& p = c.p;
+    Smem& sm = c.sm;
+    const int tid = c.tid, warp = c.warp, lane = c.lane;
+    const int hd = p.hd, gq = p.n_heads / p.n_kv, h0 = g * gq, GD = gq * hd, S = p.splits;
+    const float* part_acc = p.attn_part;
+    const float* part_ml = p.attn_part + (size_t)p.n_heads * p.max_splits * hd;
+    unsigned* mc = p.counters + n_phase_counters(p.n_layers) + layer * p.n_kv + g;
+    if (tid == 0) sm.misc()[1] = atom_add_acq_rel(mc, 1u) == (unsigned)(S - 1);
+    consumer_sync();
+    if (sm.misc()[1]) {
+        // weights per head, one warp per head and one split per lane (S <= 32)
+        const int MS = p.max_splits;
+        float* wgt = sm.comb();                                    // [gq][S]
+        if (warp < gq) {
+            const bool has = lane < S;
+            const float2 mv = has ? __ldcg(reinterpret_cast<const float2*>(part_ml) + (size_t)(h0 + warp) * MS + lane)
+                                  : make_float2(-INFINITY, 0.f);
+            const float M = warp_max(mv.x);
+            const float w = has && mv.x != -INFINITY ? expf(mv.x - M) : 0.f;
+            const float Ls = warp_sum(w * mv.y);
+            if (has) wgt[warp * S + lane] = w / Ls;
+        }
+        // every thread loads its elements' partial sums meanwhile (all splits at once)
+        for (int e0 = 0; e0 < GD; e0 += kConsumers) {
+            const int e = e0 + tid;
+            const int hh = e < GD ? e / hd : 0, ii = e < GD ? e % hd : 0;
+            const float* src = part_acc + (size_t)(h0 + hh) * MS * hd + ii;
+            float av[32];
+#pragma unroll
+            for (int k = 0; k < 32; k++) av[k] = e < GD && k < S ? __ldcg(src + (size_t)k * hd) : 0.f;
+            consumer_sync();                                       // weights ready
+            if (e < GD) {
+                float v = 0.f;
+#pragma unroll
+                for (int k = 0; k < 32; k++)
+                    if (k < S) v = fmaf(wgt[hh * S + k], av[k], v);
+                st_tagged(c.tv(layer, c.tl.attn) + (h0 + hh) * hd + ii, v, c.tag);
+            }
+        }
+    }
+    consumer_sync();
+}
+
+// Scalar form (any head_dim and group size): scores one thread per (head,
+// position), softmax one warp per head, the weighted V sum split over
+// threads by output pair and position stride.
+__device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int unit) {
+    const StepParams& p = c.p;
+    Smem& sm = c.sm;
+    const int tid = c.tid, warp = c.warp, lane = c.lane;
+    const int hd = p.hd, gq = p.n_heads / p.n_kv, P = p.attn_rows, S = p.splits;
+    int g, s, t0, t1;
+    unit_range(p, unit, S, g, s, t0, t1);
+    const int h0 = g * gq, GD = gq * hd;
+    float* q_s = sm.xs();                                          // [gq][hd]
+    __half* kp = reinterpret_cast<__half*>(q_s + GD + hd);         // [hd] this position's K row (F16)
+    __half* vp = kp + hd;                                          // [hd] this position's V row (F16)
+    float* sc = q_s + GD + 2 * hd;                                 // [2][gq][P] scores, then probabilities
+    float* ml = sc + 2 * gq * P;                                   // [2][gq] running max m, sum l
+    float* corr = ml + 2 * gq;                                     // [2][gq] rescale of the chunk's old sums
+
+    const bool writer = t0 <= p.pos && p.pos < t1;
+    attention_prologue(c, L, layer, g, writer);
+    if (tid < gq) { ml[tid] = -INFINITY; ml[gq + tid] = 0.f; }     // read after the first chunk's scores sync
     // PV work split: thread t accumulates the output pair o2 = t % (GD/2)
     // (elements 2*o2, 2*o2+1) over positions with index % NSPLIT == t / (GD/2).
     const int GD2 = GD / 2;
@@ -966,42 +1036,223 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
         if (ii == 0) __stcg(reinterpret_cast<float2*>(part_ml) + hs, make_float2(ml[hh], ml[gq + hh]));
     }
     consumer_sync();                                               // comb, scratch free
-    unsigned* mc = p.counters + n_phase_counters(p.n_layers) + layer * p.n_kv + g;
-    if (tid == 0) sm.misc()[1] = atom_add_acq_rel(mc, 1u) == (unsigned)(S - 1);
-    consumer_sync();
-    if (sm.misc()[1]) {
-        // weights per head, one warp per head and one split per lane (S <= 32)
-        const int MS = p.max_splits;
-        float* wgt = sm.comb();                                    // [gq][S]
-        if (warp < gq) {
-            const bool has = lane < S;
-            const float2 mv = has ? __ldcg(reinterpret_cast<const float2*>(part_ml) + (size_t)(h0 + warp) * MS + lane)
-                                  : make_float2(-INFINITY, 0.f);
-            const float M = warp_max(mv.x);
-            const float w = has && mv.x != -INFINITY ? expf(mv.x - M) : 0.f;
-            const float Ls = warp_sum(w * mv.y);
-            if (has) wgt[warp * S + lane] = w / Ls;
+    attention_merge(c, layer, g);
+    return true;
+}
+
+// Shared-memory address of 16-byte chunk `ch` of row r of a K or V tile: the
+// tile is hd / W sub-tiles of [P][W] F16 (W = 64 when hd is a multiple of
+// 64, else hd), each written by TMA with the swizzle of its row width (128,
+// 64 or 32 bytes: address bits 7.. XORed into the chunk bits 4..; none for
+// other widths).  The ring is 1024-byte aligned, so the pattern computed on
+// the address is the one the copy used.
+template <int HD>
+__device__ __forceinline__ uint32_t kv_chunk(uint32_t tile, int P, int r, int ch) {
+    constexpr int W = HD % 64 == 0 ? 64 : HD;
+    constexpr uint32_t SWZ = W * 2 == 128 ? 7u : W * 2 == 64 ? 3u : W * 2 == 32 ? 1u : 0u;
+    constexpr int CPR = W / 8;
+    const int sub = ch / CPR, cc = ch - sub * CPR;
+    const uint32_t a = tile + (uint32_t)(sub * P + r) * (uint32_t)(W * 2) + (uint32_t)cc * 16u;
+    return a ^ (((a >> 7) & SWZ) << 4);
+}
+
+// The two F16 parts of x: hi = x rounded to F16, lo = the rest rounded to
+// F16, so that hi + lo carries about 22 bits of x and every product of a part
+// with an F16 value is exact in F32.
+__device__ __forceinline__ __half f16_part(float x, int part) {
+    const __half hi = __float2half_rn(x);
+    return part ? __float2half_rn(x - __half2float(hi)) : hi;
+}
+__device__ __forceinline__ uint32_t pack_h2(__half a, __half b) {
+    return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+}
+
+// Tensor-core form (head_dim HD in {32, 48, 64}, gq <= 4): each warp
+// takes 16-position tiles of the chunk.  Scores are one m16n8k16 product per
+// 8 positions and 16 dimensions: A rows 2h and 2h+1 hold the F16 hi and lo
+// parts of head h's q, B the K rows (ldmatrix from the swizzled tile), so the
+// two rows of a head add up to q.k with F32 accumulation.  The warp keeps its
+// own online softmax (m, l per head) over its tiles; the probabilities, again
+// split into hi and lo rows, multiply the V rows (ldmatrix.trans) into the
+// warp's accumulators.  At the end the warps' (m, l, acc) are merged in
+// shared memory into the unit's partial.
+template <int HD>
+__device__ bool attention_unit_mma(Consumer& c, const LayerDev& L, int layer, int unit) {
+    const StepParams& p = c.p;
+    Smem& sm = c.sm;
+    const int tid = c.tid, warp = c.warp, lane = c.lane;
+    const int gq = p.n_heads / p.n_kv, P = p.attn_rows, S = p.splits;
+    int g, s, t0, t1;
+    unit_range(p, unit, S, g, s, t0, t1);
+    const int h0 = g * gq, GD = gq * HD;
+    const float* q_s = sm.xs();
+    const __half* kp = reinterpret_cast<const __half*>(q_s + GD + HD);
+    const __half* vp = kp + HD;
+    const bool writer = t0 <= p.pos && p.pos < t1;
+    attention_prologue(c, L, layer, g, writer);
+
+    // A fragments of q: row r = lane / 4 is part (r & 1) of head r / 2
+    const int r = lane >> 2, t = lane & 3, hq = r >> 1, part = r & 1;
+    uint32_t aq[HD / 16][2];
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ks++)
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const int d = ks * 16 + 8 * j + 2 * t;
+            const float x0 = hq < gq ? q_s[hq * HD + d] : 0.f, x1 = hq < gq ? q_s[hq * HD + d + 1] : 0.f;
+            aq[ks][j] = pack_h2(f16_part(x0, part), f16_part(x1, part));
         }
-        // every thread loads its elements' partial sums meanwhile (all splits at once)
-        for (int e0 = 0; e0 < GD; e0 += kConsumers) {
-            const int e = e0 + tid;
-            const int hh = e < GD ? e / hd : 0, ii = e < GD ? e % hd : 0;
-            const float* src = part_acc + (size_t)(h0 + hh) * MS * hd + ii;
-            float av[32];
+    float m_run = -INFINITY, l_run = 0.f;
+    float acc[HD / 8][2];
 #pragma unroll
-            for (int k = 0; k < 32; k++) av[k] = e < GD && k < S ? __ldcg(src + (size_t)k * hd) : 0.f;
-            consumer_sync();                                       // weights ready
-            if (e < GD) {
-                float v = 0.f;
+    for (int n = 0; n < HD / 8; n++) acc[n][0] = acc[n][1] = 0.f;
+
+    int slot = 0;
+    const uint8_t* buf = nullptr;
+    for (int c0 = t0; c0 < t1; c0 += P) {
+        if (buf) c.release(slot);
+        const int np = min(P, t1 - c0);
+        buf = c.next_slot(slot);
+        const uint32_t kt = smem_addr(buf), vt = kt + (uint32_t)(P * HD * 2);
+        if (writer && c0 <= p.pos && p.pos < c0 + np) {
+            // this step's K and V rows replace the copies the tile load read
+            const int row = p.pos - c0;
+            if (tid < HD / 8) {
+                const uint4 kv = reinterpret_cast<const uint4*>(kp)[tid];
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(kv_chunk<HD>(kt, P, row, tid)),
+                             "r"(kv.x), "r"(kv.y), "r"(kv.z), "r"(kv.w) : "memory");
+            } else if (tid < HD / 4) {
+                const uint4 vv = reinterpret_cast<const uint4*>(vp)[tid - HD / 8];
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(kv_chunk<HD>(vt, P, row, tid - HD / 8)),
+                             "r"(vv.x), "r"(vv.y), "r"(vv.z), "r"(vv.w) : "memory");
+            }
+            fence_proxy_async_smem();
+        }
+        consumer_sync();
+        if (c.aborted()) return false;
+        const int nt = (np + 15) >> 4;
+        for (int tile = warp; tile < nt; tile += kConsumerWarps) {
+            const int pj = tile * 16;
+            // scores of positions pj + 8 * ns + 2t + {0, 1}, rows r (parts of head hq)
+            float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+            {
+                int kr = pj + ((lane >> 4) & 1) * 8 + (lane & 7);
+                if (kr >= np) kr = 0;                                  // masked below
 #pragma unroll
-                for (int k = 0; k < 32; k++)
-                    if (k < S) v = fmaf(wgt[hh * S + k], av[k], v);
-                st_tagged(c.tv(layer, c.tl.attn) + (h0 + hh) * hd + ii, v, c.tag);
+                for (int ks = 0; ks < HD / 16; ks++) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kv_chunk<HD>(kt, P, kr, 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
+                    mma_rows8(sc[0][0], sc[0][1], aq[ks][0], aq[ks][1], b0, b1);
+                    mma_rows8(sc[1][0], sc[1][1], aq[ks][0], aq[ks][1], b2, b3);
+                }
+            }
+            float e[2][2], mt = -INFINITY;
+#pragma unroll
+            for (int ns = 0; ns < 2; ns++)
+#pragma unroll
+                for (int k = 0; k < 2; k++) {
+                    const float v = sc[ns][k] + __shfl_xor_sync(0xffffffffu, sc[ns][k], 4);   // hi + lo
+                    const int pos = pj + 8 * ns + 2 * t + k;
+                    e[ns][k] = pos < np ? __fdiv_rn(v, p.attn_div) : -INFINITY;
+                    mt = fmaxf(mt, e[ns][k]);
+                }
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+            const float m_new = fmaxf(m_run, mt);
+            const float cr = expf(m_run - m_new);                      // 0 on the warp's first tile
+            float ls = 0.f;
+#pragma unroll
+            for (int ns = 0; ns < 2; ns++)
+#pragma unroll
+                for (int k = 0; k < 2; k++) {
+                    e[ns][k] = expf(e[ns][k] - m_new);
+                    ls += e[ns][k];
+                }
+            ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+            ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+            l_run = l_run * cr + ls;
+            m_run = m_new;
+#pragma unroll
+            for (int n = 0; n < HD / 8; n++) {
+                acc[n][0] *= cr;
+                acc[n][1] *= cr;
+            }
+            // probabilities as A: columns 2t, 2t+1 (positions of n-subtile 0) and 2t+8, 2t+9 (subtile 1)
+            const uint32_t pa0 = pack_h2(f16_part(e[0][0], part), f16_part(e[0][1], part));
+            const uint32_t pa2 = pack_h2(f16_part(e[1][0], part), f16_part(e[1][1], part));
+            int vr = pj + ((lane >> 3) & 1) * 8 + (lane & 7);
+            if (vr >= np) vr = 0;                                      // probability 0
+#pragma unroll
+            for (int n = 0; n < HD / 8; n += 2) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(kv_chunk<HD>(vt, P, vr, n + (lane >> 4)), b0, b1, b2, b3);
+                mma_rows8(acc[n][0], acc[n][1], pa0, pa2, b0, b1);
+                mma_rows8(acc[n + 1][0], acc[n + 1][1], pa0, pa2, b2, b3);
             }
         }
     }
+    if (!buf) {                                                    // no positions: an empty partial
+        for (int oo = tid; oo < GD; oo += kConsumers) {
+            const size_t hs = (size_t)(h0 + oo / HD) * p.max_splits + s;
+            __stcg(p.attn_part + hs * HD + oo % HD, 0.f);
+            if (oo % HD == 0)
+                __stcg(reinterpret_cast<float2*>(p.attn_part + (size_t)p.n_heads * p.max_splits * HD) + hs,
+                       make_float2(-INFINITY, 0.f));
+        }
+        consumer_sync();
+        attention_merge(c, layer, g);
+        return true;
+    }
+    // the warps' partials, in the last slot (its tile is no longer read)
     consumer_sync();
+    float* wpart = reinterpret_cast<float*>(const_cast<uint8_t*>(buf));   // [warp][gq][HD + 2]
+    const int WS = gq * (HD + 2);
+#pragma unroll
+    for (int n = 0; n < HD / 8; n++)
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+            const float o = acc[n][k] + __shfl_xor_sync(0xffffffffu, acc[n][k], 4);
+            if (part == 0 && hq < gq) wpart[warp * WS + hq * (HD + 2) + n * 8 + 2 * t + k] = o;
+        }
+    if (part == 0 && hq < gq && t == 0) {
+        wpart[warp * WS + hq * (HD + 2) + HD] = m_run;
+        wpart[warp * WS + hq * (HD + 2) + HD + 1] = l_run;
+    }
+    consumer_sync();
+    float* part_acc = p.attn_part;
+    float* part_ml = p.attn_part + (size_t)p.n_heads * p.max_splits * HD;
+    for (int oo = tid; oo < GD; oo += kConsumers) {
+        const int hh = oo / HD, ii = oo % HD;
+        float M = -INFINITY;
+        for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, wpart[w * WS + hh * (HD + 2) + HD]);
+        float v = 0.f, l = 0.f;
+        for (int w = 0; w < kConsumerWarps; w++) {
+            const float mw = wpart[w * WS + hh * (HD + 2) + HD];
+            const float f = mw == -INFINITY ? 0.f : expf(mw - M);
+            v = fmaf(f, wpart[w * WS + hh * (HD + 2) + ii], v);
+            l = fmaf(f, wpart[w * WS + hh * (HD + 2) + HD + 1], l);
+        }
+        const size_t hs = (size_t)(h0 + hh) * p.max_splits + s;
+        __stcg(part_acc + hs * HD + ii, v);
+        if (ii == 0) __stcg(reinterpret_cast<float2*>(part_ml) + hs, make_float2(M, l));
+    }
+    fence_proxy_async_smem();                                      // the slot's next fill is a TMA write
+    consumer_sync();
+    c.release(slot);
+    attention_merge(c, layer, g);
     return true;
+}
+
+__device__ bool attention_any(Consumer& c, const LayerDev& L, int layer, int unit) {
+    if (c.p.attn_mma) {
+        switch (c.p.hd) {
+            case 32: return attention_unit_mma<32>(c, L, layer, unit);
+            case 48: return attention_unit_mma<48>(c, L, layer, unit);
+            case 64: return attention_unit_mma<64>(c, L, layer, unit);
+            default: break;
+        }
+    }
+    return attention_unit(c, L, layer, unit);
 }
 
 // ----------------------------------------------------------------- kernel --
@@ -1041,7 +1292,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         {
             const int units = p.n_kv * p.splits;
             for (int unit = blockIdx.x; unit < units; unit += G)
-                if (!attention_unit(c, L, l, unit)) return false;
+                if (!attention_any(c, L, l, unit)) return false;
         }
         if (tid == 0) trace_mark(p, 10 * l + 3);
         // ---- O
@@ -1134,8 +1385,9 @@ __device__ void producer_main(const StepParams& p, Smem& sm) {
 
 template <int DT>
 __global__ void __launch_bounds__(kBlock, 1) decode_step_kernel(const __grid_constant__ StepParams p) {
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    Smem sm(smem_raw, p);
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // the ring starts on a 1024-byte boundary (the swizzled KV tiles rely on it)
+    Smem sm(reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023), p);
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.ns; i++) {
             mbar_init(&sm.full()[i], 1);
@@ -1203,7 +1455,13 @@ bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int 
     P &= ~7;
     if (P < 8) return false;
     const int GD = gq * hd;
-    const size_t attn_scratch = sizeof(float) * (size_t)(GD + hd + 2 * gq * P + 4 * gq) + 2 * sizeof(__half) * hd;
+    // tensor-core attention for the head sizes it is instantiated for
+    // (head_dim 128 would need more registers than the kernel has to spare)
+    p.attn_mma = (hd == 32 || hd == 48 || hd == 64) && gq <= 4;
+    p.attn_w = p.attn_mma && hd % 64 == 0 ? 64 : hd;
+    // q_s, kf, kp/vp; the scalar form adds its score buffers
+    const size_t attn_scratch =
+        sizeof(float) * (size_t)(GD + 2 * hd) + (p.attn_mma ? 0 : sizeof(float) * (size_t)(2 * gq * P + 4 * gq));
     // the scratch region also stages the activation vectors of the GEMV
     // phases: always those of length dim and q_dim, the FFN one as well when
     // that still leaves a 192 KB ring
@@ -1216,7 +1474,7 @@ bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int 
     const size_t gain_bytes = slices(dim);
     auto fixed_for = [&](size_t x) {
         return al(x) + al(tpart) + al(2 * 128 * 4) + al(2 * kConsumers * 4) + al(2 * kOwnFloats * 4) + al(gain_bytes) +
-               1024;
+               2048;                                            // barriers and flags; the ring's alignment
     };
     if (rope_dims / 2 > 128 || GD > 2 * kConsumers || GD % 2) return false;
     const size_t xs_ffn = xs > slices(ffn) ? xs : slices(ffn);
@@ -1237,7 +1495,7 @@ bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int 
     p.off_gain = (int)off; off += al(gain_bytes);
     p.off_bar = (int)off; off += al(2 * ns * 8);
     p.off_misc = (int)off; off += 64 + 8 * (kConsumerWarps + 2) + 8 * kConsumerWarps;
-    *smem_bytes = al(off);
+    *smem_bytes = al(off) + 1024;                               // room to align the ring to 1024 bytes
     return *smem_bytes <= (size_t)kMaxSmem;
 }
 

@@ -399,7 +399,9 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
     if (per_sm < 1) { free_handle(h); return LLM_ERR_UNSUPPORTED; }
 
     // 2-D tensor maps of every layer's K and V cache: [max_seq][kv_dim] F16,
-    // box [attn_rows][head_dim], read by the step kernel's TMA tile loads
+    // box [attn_rows][attn_w], read by the step kernel's TMA tile loads; the
+    // tensor-core attention reads its tiles with ldmatrix, so they are
+    // swizzled by their row width (128, 64 or 32 bytes)
     {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q_res;
@@ -412,10 +414,16 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
                 void* base = which ? (void*)h->layers[l].vc : (void*)h->layers[l].kc;
                 cuuint64_t gdim[2] = {(cuuint64_t)kv, (cuuint64_t)c.max_seq};
                 cuuint64_t gstride[1] = {(cuuint64_t)kv * 2};
-                cuuint32_t box[2] = {(cuuint32_t)c.head_dim, (cuuint32_t)h->geo.attn_rows};
+                cuuint32_t box[2] = {(cuuint32_t)h->geo.attn_w, (cuuint32_t)h->geo.attn_rows};
                 cuuint32_t estride[2] = {1, 1};
+                const int row_bytes = h->geo.attn_w * 2;
+                const CUtensorMapSwizzle swz = !h->geo.attn_mma ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                               : row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                               : row_bytes == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : row_bytes == 32  ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                                  : CU_TENSOR_MAP_SWIZZLE_NONE;
                 CUresult r = encode(&maps[(size_t)2 * l + which], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, gdim,
-                                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
                 if (r != CUDA_SUCCESS) { free_handle(h); return LLM_ERR_CUDA; }
             }

@@ -93,6 +93,8 @@ struct StepParams {
     // shared-memory geometry (bytes from the dynamic smem base)
     int ns;                   // ring slots
     int attn_rows;            // KV rows per ring slot
+    int attn_mma;             // attention on tensor cores (mma.sync): head_dim in {32, 48, 64}, gq <= 4
+    int attn_w;               // KV tile sub-tile width (elements): 64 when head_dim % 64 == 0 on the mma path, else head_dim
     int off_xs, off_red, off_rope, off_comb, off_bar, off_misc, off_own, off_gain;
     int scratch_floats;       // floats of the attention scratch region (xs)
 
@@ -253,6 +255,38 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                      smem_addr(dst)),
                  "l"(src), "r"(bytes), "r"(smem_addr(bar))
                  : "memory");
+}
+
+// Orders this thread's generic-proxy writes to shared memory before later
+// async-proxy (TMA) writes to the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Four 8x8 b16 matrices from shared memory (lanes 8i..8i+7 give the row
+// addresses of matrix i); .trans delivers each matrix transposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(a));
+}
+
+// D = A * B + C for one m16n8k16 tile, F16 operands, F32 accumulation, with
+// A's rows 8..15 zero: only the accumulator rows 0..7 (d0 = column 2t, d1 =
+// column 2t + 1 of row lane/4) are carried.
+__device__ __forceinline__ void mma_rows8(float& d0, float& d1, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    float x2, x3;                 // rows 8..15 of D, not used
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %11, %12, %12};"
+        : "=f"(d0), "=f"(d1), "=f"(x2), "=f"(x3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(d0), "f"(d1), "f"(0.f));
+    asm volatile("" ::"f"(x2), "f"(x3));
 }
 
 // 2-D tiled tensor copy global -> shared (box of the tensor map at (x, y)).
