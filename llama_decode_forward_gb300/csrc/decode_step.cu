@@ -455,61 +455,54 @@ __device__ __forceinline__ void lane_rows(const uint8_t* const (&w)[N], const ui
 }
 
 // ------------------------------------------------------------------ GEMV --
-struct EpiStore {                 // out[r] = v (+ bias of this CTA's row r), tagged
-    unsigned long long* out;
-    const float* bias;            // smem, indexed from the CTA's first row, or nullptr
-    int r0;
+// The epilogue of a GEMV phase, chosen at run time (all phases share one
+// copy of the GEMV code):
+//   kStore     out[r] = v (+ bias of this CTA's row r), tagged
+//   kResidual  out[r] = own[r] + v, the owned rows kept in shared memory
+//   kSwiGLU    u[i] = silu(gate_i) * up_i ("The Forward Pass in Java",
+//              Example 8): the (gate, up) sums of interleaved rows 2i, 2i+1
+//              are parked in shared memory and the nonlinearity is applied
+//              to all of the CTA's rows at once when the phase finishes
+//   kLogits    logits[r] = v, keeping this thread's best (value, first index)
+struct Epi {
+    enum : int { kStore, kResidual, kSwiGLU, kLogits };
+    int kind;
+    unsigned long long* out;      // tagged output vector (store, residual, swiglu)
+    const float* bias;            // store: smem bias indexed from `base`, or nullptr
+    float* sm;                    // residual: owned rows; swiglu: (gate, up) sums
+    int base;                     // first row (store), first owned row (residual), first super-row (swiglu)
+    int end;                      // swiglu: end super-row
     unsigned tag;
-    __device__ void row(int r, float v) { st_tagged(out + r, bias ? v + bias[r - r0] : v, tag); }
-    __device__ void pair(int, float, float) {}
-    __device__ void finish(Consumer&) {}
-};
-struct EpiResidual {              // x[r] = own[r] + v, the owned row kept in smem; x tagged
-    unsigned long long* x;
-    float* own;
-    int own0;
-    unsigned tag;
-    __device__ void row(int r, float v) {
-        const float y = own[r - own0] + v;
-        own[r - own0] = y;
-        st_tagged(x + r, y, tag);
-    }
-    __device__ void pair(int, float, float) {}
-    __device__ void finish(Consumer&) {}
-};
-// u[i] = silu(gate_i) * up_i ("The Forward Pass in Java", Example 8).  The
-// (gate, up) sums are parked in shared memory as the rows complete and the
-// nonlinearity is applied to all of the CTA's rows at once at the end of the
-// phase, off the rows' critical path.
-struct EpiSwiGLU {
-    unsigned long long* u;        // tagged
-    float* gs;                    // smem [2 * rows of this CTA]
-    int i0, i1;                   // this CTA's super-rows
-    // row r of the interleaved matrix: gate (even) or up (odd) of super-row r / 2
-    __device__ void row(int r, float v) { gs[r - 2 * i0] = v; }
-    __device__ void pair(int i, float g, float up) {
-        gs[2 * (i - i0)] = g;
-        gs[2 * (i - i0) + 1] = up;
-    }
-    __device__ void finish(Consumer& c) {
-        consumer_sync();
-        for (int k = c.tid; k < i1 - i0; k += kConsumers) {
-            const float g = gs[2 * k], up = gs[2 * k + 1];
-            const float e = expf(-g);
-            st_tagged(u + i0 + k, __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), up), c.tag);
-        }
-    }
-};
-struct EpiLogits {                // logits[r] = v, keep this lane's best (value, first index)
     float* logits;
     unsigned long long best;
     __device__ void row(int r, float v) {
-        __stcg(logits + r, v);
-        const unsigned long long k = argmax_key(v, r);
-        best = k > best ? k : best;
+        if (kind == kStore) {
+            st_tagged(out + r, bias ? v + bias[r - base] : v, tag);
+        } else if (kind == kResidual) {
+            const float y = sm[r - base] + v;
+            sm[r - base] = y;
+            st_tagged(out + r, y, tag);
+        } else if (kind == kSwiGLU) {
+            sm[r - 2 * base] = v;                 // row r: gate (even) or up (odd) of super-row r / 2
+        } else {
+            __stcg(logits + r, v);
+            const unsigned long long k = argmax_key(v, r);
+            best = k > best ? k : best;
+        }
     }
-    __device__ void pair(int, float, float) {}
-    __device__ void finish(Consumer&) {}
+    __device__ void pair(int i, float g, float up) {
+        sm[2 * (i - base)] = g;
+        sm[2 * (i - base) + 1] = up;
+    }
+    __device__ void finish(Consumer& c) {
+        if (kind != kSwiGLU) return;
+        consumer_sync();
+        for (int k = c.tid; k < end - base; k += kConsumers) {
+            const float g = sm[2 * k], up = sm[2 * k + 1];
+            const float e = expf(-g);
+            st_tagged(out + base + k, __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), up), c.tag);
+        }
+    }
 };
 
 // Where a GEMV phase takes its activation vector: a tagged vector (written
@@ -652,7 +645,7 @@ __device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& 
 // warp parks its part of the two rows in shared memory; after the last chunk
 // the consumers finish all rows at once (parts added in warp order, so the
 // result does not depend on timing) and apply the phase's epilogue.
-template <int DT, bool PAIR, class Epi>
+template <int DT, bool PAIR>
 __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const XSrc& src, int token, Epi& epi) {
     constexpr int ES = DT == LLM_Q8_0 ? 1 : (DT == LLM_F16 ? 2 : 4);
     const Lanes L = lane_layout<DT, PAIR>(c, m);
@@ -1271,72 +1264,89 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
     for (int i = c.own0 + tid; i < c.own1; i += kConsumers) sm.xown()[i - c.own0] = weight_at<DT>(p.embd, token, i);
     // Phases wait for their inputs through the tags of the vectors they read;
     // the only counters left are the attention merges and the end of the step.
-    for (int l = 0; l < p.n_layers; l++) {
-        const LayerDev& L = p.layers[l];
-        // ---- QKV
-        int q0, q1;
-        cta_rows(L.qkv.rows, q0, q1);
-        if (L.qkv_bias)
-            for (int i = tid; i < q1 - q0; i += kConsumers) sm.bias()[i] = __ldg(L.qkv_bias + q0 + i);
-        if (tid == 0) trace_mark(p, 10 * l);
-        c.tk = 160 + 4 * l;
-        {
-            const XSrc src{l == 0 ? nullptr : c.tv(l - 1, c.tl.xd), L.attn_norm, p.dim};
-            EpiStore e{c.tv(l, c.tl.qkv), L.qkv_bias ? sm.bias() : nullptr, q0, c.tag};
-            gemv_consume<DT, false>(c, L.qkv, src, token, e);
-        }
-        if (tid == 0) trace_mark(p, 10 * l + 1);
-        c.prefetch_gains(L.ffn_norm, p.dim);             // QKV has read its gains
-        // ---- ATTN
-        if (tid == 0) trace_mark(p, 10 * l + 2);
-        {
+    // Every GEMV phase (QKV, O, GU, DOWN of each layer, then the logits) goes
+    // through the one call site below, so the kernel holds one copy of the
+    // GEMV code.
+    const int nph = 4 * p.n_layers + 1;
+    unsigned long long best = 0ull;
+    for (int ph = 0; ph < nph; ph++) {
+        const int l = ph >> 2, k = ph & 3;
+        const bool last = ph == nph - 1;
+        const LayerDev& L = p.layers[last ? p.n_layers - 1 : l];
+        const DMat* m;
+        XSrc src;
+        Epi e{};
+        e.tag = c.tag;
+        if (last) {
+            // ---- LOGITS + argmax
+            if (tid == 0) trace_mark(p, 240);
+            c.tk = -1;
+            m = &p.out;
+            src = XSrc{c.tv(p.n_layers - 1, c.tl.xd), p.out_norm, p.dim};
+            e.kind = Epi::kLogits;
+            e.logits = p.logits;
+        } else if (k == 0) {
+            // ---- QKV
+            int q0, q1;
+            cta_rows(L.qkv.rows, q0, q1);
+            if (L.qkv_bias)
+                for (int i = tid; i < q1 - q0; i += kConsumers) sm.bias()[i] = __ldg(L.qkv_bias + q0 + i);
+            if (tid == 0) trace_mark(p, 10 * l);
+            c.tk = 160 + 4 * l;
+            m = &L.qkv;
+            src = XSrc{l == 0 ? nullptr : c.tv(l - 1, c.tl.xd), L.attn_norm, p.dim};
+            e.kind = Epi::kStore;
+            e.out = c.tv(l, c.tl.qkv);
+            e.bias = L.qkv_bias ? sm.bias() : nullptr;
+            e.base = q0;
+        } else if (k == 1) {
+            // ---- ATTN, then O
+            if (tid == 0) trace_mark(p, 10 * l + 2);
             const int units = p.n_kv * p.splits;
             for (int unit = blockIdx.x; unit < units; unit += G)
                 if (!attention_any(c, L, l, unit)) return false;
+            if (tid == 0) trace_mark(p, 10 * l + 3);
+            if (tid == 0) trace_mark(p, 10 * l + 4);
+            c.tk = 160 + 4 * l + 1;
+            m = &L.o;
+            src = XSrc{c.tv(l, c.tl.attn), nullptr, p.q_dim};
+            e.kind = Epi::kResidual;
+            e.out = c.tv(l, c.tl.xo);
+            e.sm = sm.xown();
+            e.base = c.own0;
+        } else if (k == 2) {
+            // ---- GU
+            if (tid == 0) trace_mark(p, 10 * l + 6);
+            c.tk = 160 + 4 * l + 2;
+            m = &L.gu;
+            src = XSrc{c.tv(l, c.tl.xo), L.ffn_norm, p.dim};
+            e.kind = Epi::kSwiGLU;
+            e.out = c.tv(l, c.tl.u);
+            e.sm = sm.bias();
+            cta_rows(L.gu.rows, e.base, e.end);
+        } else {
+            // ---- DOWN
+            if (tid == 0) trace_mark(p, 10 * l + 8);
+            c.tk = 160 + 4 * l + 3;
+            m = &L.down;
+            src = XSrc{c.tv(l, c.tl.u), nullptr, p.ffn};
+            e.kind = Epi::kResidual;
+            e.out = c.tv(l, c.tl.xd);
+            e.sm = sm.xown();
+            e.base = c.own0;
         }
-        if (tid == 0) trace_mark(p, 10 * l + 3);
-        // ---- O
-        if (tid == 0) trace_mark(p, 10 * l + 4);
-        c.tk = 160 + 4 * l + 1;
-        {
-            const XSrc src{c.tv(l, c.tl.attn), nullptr, p.q_dim};
-            EpiResidual e{c.tv(l, c.tl.xo), sm.xown(), c.own0, c.tag};
-            gemv_consume<DT, false>(c, L.o, src, token, e);
+        gemv_consume<DT, false>(c, *m, src, token, e);
+        if (last) {
+            best = e.best;
+        } else {
+            if (tid == 0) trace_mark(p, 10 * l + 2 * k + 1 + (k > 0 ? 2 : 0));
+            if (k == 0) c.prefetch_gains(L.ffn_norm, p.dim);       // QKV has read its gains
+            if (k == 2) c.prefetch_gains(l + 1 < p.n_layers ? p.layers[l + 1].attn_norm : p.out_norm, p.dim);
         }
-        if (tid == 0) trace_mark(p, 10 * l + 5);
-        // ---- GU
-        if (tid == 0) trace_mark(p, 10 * l + 6);
-        c.tk = 160 + 4 * l + 2;
-        {
-            const XSrc src{c.tv(l, c.tl.xo), L.ffn_norm, p.dim};
-            int i0, i1;
-            cta_rows(L.gu.rows, i0, i1);
-            EpiSwiGLU e{c.tv(l, c.tl.u), sm.bias(), i0, i1};
-            gemv_consume<DT, false>(c, L.gu, src, token, e);
-        }
-        if (tid == 0) trace_mark(p, 10 * l + 7);
-        c.prefetch_gains(l + 1 < p.n_layers ? p.layers[l + 1].attn_norm : p.out_norm, p.dim);
-        // ---- DOWN
-        if (tid == 0) trace_mark(p, 10 * l + 8);
-        c.tk = 160 + 4 * l + 3;
-        {
-            const XSrc src{c.tv(l, c.tl.u), nullptr, p.ffn};
-            EpiResidual e{c.tv(l, c.tl.xd), sm.xown(), c.own0, c.tag};
-            gemv_consume<DT, false>(c, L.down, src, token, e);
-        }
-        if (tid == 0) trace_mark(p, 10 * l + 9);
     }
-    // ---- LOGITS + argmax
     unsigned* fin = p.counters;
-    if (tid == 0) trace_mark(p, 240);
-    c.tk = -1;
-    EpiLogits e{p.logits, 0ull};
-    {
-        const XSrc src{c.tv(p.n_layers - 1, c.tl.xd), p.out_norm, p.dim};
-        gemv_consume<DT, false>(c, p.out, src, token, e);
-    }
     if (tid == 0) trace_mark(p, 241);
-    unsigned long long b = e.best;
+    unsigned long long b = best;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const unsigned long long other = __shfl_xor_sync(0xffffffffu, b, o);
