@@ -267,7 +267,6 @@ struct Consumer {
     int tid, warp, lane;
     int own0, own1;        // residual rows this CTA owns (rows of Wo and Wdown)
     unsigned tag;          // this step's tag of the tagged vectors
-    TvLayout tl;
     int tk = -1;           // trace slot of the current GEMV's first chunk
     long long waited = 0;  // trace builds: cycles spent waiting for ring slots
 
@@ -277,12 +276,14 @@ struct Consumer {
         lane = tid & 31;
         cta_rows(p.dim, own0, own1);
         tag = __ldcg(p.epoch) + 1u;
-        tl = tv_layout(p.dim, p.q_dim, p.kv_dim, p.ffn);
     }
+
+    // element offsets of the tagged vectors within a layer's set
+    __device__ __forceinline__ TvLayout tl() const { return tv_layout(p.dim, p.q_dim, p.kv_dim, p.ffn); }
 
     // layer l's tagged vector at element offset `off` of its set
     __device__ __forceinline__ unsigned long long* tv(int l, long long off) const {
-        return p.tv + (long long)l * tl.stride + off;
+        return p.tv + (long long)l * tl().stride + off;
     }
 
     __device__ bool aborted() const { return *(volatile int*)&sm.misc()[0] != 0; }
@@ -347,10 +348,16 @@ __device__ __forceinline__ float weight_at(const DMat& m, int r, int i) {
 }
 
 // ------------------------------------------------------------ lane dots --
-// A lane's 32 elements of one row (in the slot) against its x registers.
+// A lane's 32 elements of one row (in the slot) against its 32 activations,
+// held as floats in registers (x2).
 // Q8_0: one 32-element block; each biased quant byte is placed in the low
 // mantissa of 2^23 and 2^23 + 128 is subtracted, which yields the exact
 // integer qs as a float, then the block's FP16 scale multiplies the sum.
+template <int DT>
+struct XReg {
+    float2 x2[16];
+};
+
 template <int DT>
 struct LaneDot;
 
@@ -404,13 +411,13 @@ struct LaneDot<LLM_F32> {
 
 // One row: words of the lane (nseg of them valid, the rest read as zero).
 template <int DT>
-__device__ __forceinline__ float lane_row(const uint8_t* w, const uint8_t* scale, const float2 (&x2)[16], int nseg) {
+__device__ __forceinline__ float lane_row(const uint8_t* w, const uint8_t* scale, const XReg<DT>& xr, int nseg) {
     constexpr int NS = LaneDot<DT>::kSeg;
     uint4 v[NS];
 #pragma unroll
     for (int s = 0; s < NS; s++) v[s] = s < nseg ? reinterpret_cast<const uint4*>(w)[s] : make_uint4(0u, 0u, 0u, 0u);
     float2 c0 = make_float2(0.f, 0.f), c1 = c0;
-    LaneDot<DT>::acc(v, x2, c0, c1);
+    LaneDot<DT>::acc(v, xr.x2, c0, c1);
     const float t = (c0.x + c0.y) + (c1.x + c1.y);
     if constexpr (DT == LLM_Q8_0) return nseg ? __half2float(*reinterpret_cast<const __half*>(scale)) * t : 0.f;
     return t;
@@ -423,34 +430,37 @@ struct RowsPerPass {
     static constexpr int value = DT == LLM_Q8_0 ? 4 : 2;
 };
 
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float lds_half(uint32_t a) {
+    unsigned short h;
+    asm volatile("ld.shared.b16 %0, [%1];" : "=h"(h) : "r"(a));
+    return __half2float(__ushort_as_half(h));
+}
+
 // N rows at once: every shared-memory word of the N rows is loaded before the
-// arithmetic starts, so the load latency is paid once.
+// arithmetic starts, so the load latency is paid once.  Rows are given by
+// their shared-memory addresses (quants or values w, Q8_0 scale sc).
 template <int DT, int N>
-__device__ __forceinline__ void lane_rows(const uint8_t* const (&w)[N], const uint8_t* const (&sc)[N],
-                                          const float2 (&x2)[16], int nseg, float (&v)[N]) {
+__device__ __forceinline__ void lane_rows(const uint32_t (&w)[N], const uint32_t (&sc)[N], const XReg<DT>& xr,
+                                          int nseg, float (&v)[N]) {
     constexpr int NS = LaneDot<DT>::kSeg;
     uint4 a[N][NS];
 #pragma unroll
     for (int r = 0; r < N; r++)
 #pragma unroll
-        for (int s = 0; s < NS; s++)
-            a[r][s] = s < nseg ? reinterpret_cast<const uint4*>(w[r])[s] : make_uint4(0u, 0u, 0u, 0u);
+        for (int s = 0; s < NS; s++) a[r][s] = s < nseg ? lds128(w[r] + 16 * s) : make_uint4(0u, 0u, 0u, 0u);
     float dsc[N];
 #pragma unroll
-    for (int r = 0; r < N; r++) dsc[r] = 1.f;
-    if constexpr (DT == LLM_Q8_0) {
-        if (nseg) {
-#pragma unroll
-            for (int r = 0; r < N; r++) dsc[r] = __half2float(*reinterpret_cast<const __half*>(sc[r]));
-        }
-    }
+    for (int r = 0; r < N; r++) dsc[r] = DT == LLM_Q8_0 && nseg ? lds_half(sc[r]) : 1.f;
 #pragma unroll
     for (int r = 0; r < N; r++) {
         float2 c0 = make_float2(0.f, 0.f), c1 = c0;
-        LaneDot<DT>::acc(a[r], x2, c0, c1);
-        const float t = (c0.x + c0.y) + (c1.x + c1.y);
-        if constexpr (DT == LLM_Q8_0) v[r] = nseg ? dsc[r] * t : 0.f;
-        else v[r] = t;
+        LaneDot<DT>::acc(a[r], xr.x2, c0, c1);
+        v[r] = DT == LLM_Q8_0 && !nseg ? 0.f : dsc[r] * ((c0.x + c0.y) + (c1.x + c1.y));
     }
 }
 
@@ -543,99 +553,81 @@ __device__ __forceinline__ Lanes lane_layout(const Consumer& c, const DMat& m) {
     return L;
 }
 
-// x2 <- the lane's 32 activation values (zero past the vector's end), normed
-// when src.g is set.  Every consumer thread must call this (it synchronises).
-// A vector that fits the scratch region is first staged there once per CTA
-// with coalesced loads (each 16-byte word w of the 128-byte slice s at word
-// s*8 + (w ^ (s & 7)), so that the lanes' reads of their own slices fall in
-// distinct banks); every lane then reads its slice from shared memory.  This
-// keeps the L2 requests per line of the (freshly written, grid-wide read)
-// vector at one per CTA.  Longer vectors are read by the lanes directly.
+// The lane's 32 activations (zero past the vector's end) from 8 float4 words
+// w(k) = elements 4k..4k+3.
+template <int DT, class Word>
+__device__ __forceinline__ void xreg_from_words(Word w, XReg<DT>& xr) {
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        const float4 v = w(k);
+        xr.x2[2 * k] = make_float2(v.x, v.y);
+        xr.x2[2 * k + 1] = make_float2(v.z, v.w);
+    }
+}
+
+// xr <- the lane's 32 activations, normed when src.g is set ("The Forward
+// Pass in Java", Example 4: y = (x * scale) * g, scale = 1/sqrt(mean(x^2) +
+// eps), the sum of squares a float tree sum).  Every consumer thread must call
+// this (it synchronises).  The vector is staged in the scratch region with
+// coalesced loads (each 16-byte word w of the 128-byte slice s at word s*8 +
+// (w ^ (s & 7)), so that the lanes' reads of their own slices fall in distinct
+// banks), normed in place by the threads that staged it, and each lane then
+// reads its slice from shared memory.  This keeps the L2 requests per line of
+// the (freshly written, grid-wide read) vector at one per CTA.  A vector longer
+// than the region is staged in region-sized pieces, one after the other; only
+// the FFN-length input of the down projection is that long (every normed
+// vector and the embedding row have length dim, which always fits).
 template <int DT, bool PAIR>
-__device__ __forceinline__ void lane_x(Consumer& c, const DMat& m, const Lanes& L, const XSrc& src, int token,
-                                       float2 (&x2)[16]) {
+__device__ __forceinline__ void lane_x(Consumer& c, const Lanes& L, const XSrc& src, int token, XReg<DT>& xr) {
     const int col0 = L.col0;
     const bool have = L.active && col0 < src.n;
-    float scale = 1.0f;
-    if (((src.n + 31) & ~31) <= c.p.scratch_floats) {   // whole 32-float slices fit
-        float4* xv = reinterpret_cast<float4*>(c.sm.xs());
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4* xv = reinterpret_cast<float4*>(c.sm.xs());
+    auto sw = [](int i) { return (i & ~7) + ((i & 7) ^ ((i >> 3) & 7)); };
+    const int piece = c.p.scratch_floats & ~31;          // floats per staging pass (whole slices)
+    for (int base = 0; base < src.n; base += piece) {
+        const int len = min(piece, src.n - base), ngr = len / 4;
         float ss = 0.f;
-        for (int i = c.tid; i < src.n / 4; i += kConsumers) {
-            float4 v;
-            if (src.x) {
-                v = poll4(src.x + 4 * i, c.tag, c.p.err);
-            } else {
-                v = make_float4(weight_at<DT>(c.p.embd, token, 4 * i), weight_at<DT>(c.p.embd, token, 4 * i + 1),
-                                weight_at<DT>(c.p.embd, token, 4 * i + 2), weight_at<DT>(c.p.embd, token, 4 * i + 3));
+        if (src.x) {
+            const unsigned long long* xsrc = src.x + base;
+            for (int i = c.tid; i < ngr; i += kConsumers) {
+                const float4 v = poll4(xsrc + 4 * i, c.tag, c.p.err);
+                ss += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
+                xv[sw(i)] = v;
             }
-            ss += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
-            xv[(i & ~7) + ((i & 7) ^ ((i >> 3) & 7))] = v;
+        } else {
+            for (int i = c.tid; i < ngr; i += kConsumers) {
+                const int e = base + 4 * i;
+                const float4 v = make_float4(weight_at<DT>(c.p.embd, token, e), weight_at<DT>(c.p.embd, token, e + 1),
+                                             weight_at<DT>(c.p.embd, token, e + 2), weight_at<DT>(c.p.embd, token, e + 3));
+                ss += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
+                xv[sw(i)] = v;
+            }
         }
         if (src.g) {
+            // (normed vectors are staged in one piece)
             cp_async_wait_all();                         // this thread's part of the gains (fetched ahead)
             const float tot = c.warps_total(ss);        // synchronises the consumers
-            scale = 1.0f / sqrtf(tot / (float)src.n + c.p.eps);
-        } else {
-            consumer_sync();
-        }
-        const float4* x4 = xv + L.clit * 8;
-#pragma unroll
-        for (int k = 0; k < 8; k++) {
-            const float4 v = have && col0 + 4 * k < src.n ? x4[k ^ (L.clit & 7)] : make_float4(0.f, 0.f, 0.f, 0.f);
-            x2[2 * k] = make_float2(v.x, v.y);
-            x2[2 * k + 1] = make_float2(v.z, v.w);
-        }
-        if (src.g) {
-            const float4* g4 = reinterpret_cast<const float4*>(c.sm.gains()) + L.clit * 8;
-#pragma unroll
-            for (int k = 0; k < 8; k++) {
-                const float4 g = have && col0 + 4 * k < src.n ? g4[k ^ (L.clit & 7)] : make_float4(0.f, 0.f, 0.f, 0.f);
-                x2[2 * k] = make_float2(__fmul_rn(__fmul_rn(x2[2 * k].x, scale), g.x),
-                                        __fmul_rn(__fmul_rn(x2[2 * k].y, scale), g.y));
-                x2[2 * k + 1] = make_float2(__fmul_rn(__fmul_rn(x2[2 * k + 1].x, scale), g.z),
-                                            __fmul_rn(__fmul_rn(x2[2 * k + 1].y, scale), g.w));
+            const float scale = 1.0f / sqrtf(tot / (float)src.n + c.p.eps);
+            // each thread norms the groups it staged (their gains are the ones it fetched)
+            const float4* g4 = reinterpret_cast<const float4*>(c.sm.gains());
+            for (int i = c.tid; i < ngr; i += kConsumers) {
+                const float4 x = xv[sw(i)], g = g4[sw(i)];
+                xv[sw(i)] = make_float4(__fmul_rn(__fmul_rn(x.x, scale), g.x), __fmul_rn(__fmul_rn(x.y, scale), g.y),
+                                        __fmul_rn(__fmul_rn(x.z, scale), g.z), __fmul_rn(__fmul_rn(x.w, scale), g.w));
             }
         }
-    } else {
-        if (src.x) {
-#pragma unroll
-            for (int k = 0; k < 8; k++) {
-                const float4 v = have && col0 + 4 * k < src.n ? poll4(src.x + col0 + 4 * k, c.tag, c.p.err)
-                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
-                x2[2 * k] = make_float2(v.x, v.y);
-                x2[2 * k + 1] = make_float2(v.z, v.w);
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < 16; k++) {
-                const int e = col0 + 2 * k;
-                x2[k] = have && e < src.n
-                            ? make_float2(weight_at<DT>(c.p.embd, token, e), weight_at<DT>(c.p.embd, token, e + 1))
-                            : make_float2(0.f, 0.f);
-            }
+        consumer_sync();
+        // lanes whose slice lies in this piece (slices never straddle pieces)
+        const int sl = (col0 - base) >> 5;
+        if (col0 >= base && col0 < base + len) {
+            const float4* x4 = xv + sl * 8;
+            const int rot = sl & 7;
+            xreg_from_words<DT>([&](int k) { return have && col0 + 4 * k < src.n ? x4[k ^ rot] : zero; }, xr);
+        } else if (base == 0 && !have) {
+            xreg_from_words<DT>([&](int) { return zero; }, xr);
         }
-        if (src.g) {
-            // each column counted once: the lanes of team 0 (first half for pairs)
-            float ss = 0.f;
-            if (L.team == 0 && L.hsel == 0 && have) {
-#pragma unroll
-                for (int k = 0; k < 16; k++) ss += x2[k].x * x2[k].x + x2[k].y * x2[k].y;
-            }
-            cp_async_wait_all();
-            const float tot = c.warps_total(ss);
-            scale = 1.0f / sqrtf(tot / (float)src.n + c.p.eps);
-        }
-        if (src.g) {
-            const float4* g4 = reinterpret_cast<const float4*>(src.g + col0);
-#pragma unroll
-        for (int k = 0; k < 8; k++) {
-            const float4 g = have && col0 + 4 * k < src.n ? __ldg(g4 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
-            x2[2 * k] = make_float2(__fmul_rn(__fmul_rn(x2[2 * k].x, scale), g.x),
-                                    __fmul_rn(__fmul_rn(x2[2 * k].y, scale), g.y));
-            x2[2 * k + 1] = make_float2(__fmul_rn(__fmul_rn(x2[2 * k + 1].x, scale), g.z),
-                                        __fmul_rn(__fmul_rn(x2[2 * k + 1].y, scale), g.w));
-            }
-        }
+        if (base + len < src.n) consumer_sync();       // the next piece overwrites the region
     }
 }
 
@@ -649,8 +641,8 @@ template <int DT, bool PAIR>
 __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const XSrc& src, int token, Epi& epi) {
     constexpr int ES = DT == LLM_Q8_0 ? 1 : (DT == LLM_F16 ? 2 : 4);
     const Lanes L = lane_layout<DT, PAIR>(c, m);
-    float2 x2[16];
-    lane_x<DT, PAIR>(c, m, L, src, token, x2);
+    XReg<DT> xr;
+    lane_x<DT, PAIR>(c, L, src, token, xr);
     if (c.tid == 0 && c.tk >= 0) trace_mark(c.p, c.tk - 160 + 512);
     const int tw = m.tw, teams = m.teams;
     int r0, r1;
@@ -666,6 +658,7 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
         const uint8_t* buf = c.next_slot(slot);
         if (c.tid == 0 && r == r0 && c.tk >= 0) trace_mark(c.p, c.tk);
         const uint8_t* sbase = buf + (size_t)n * per * rowq;
+        const uint32_t sbuf = smem_addr(buf), ssc = smem_addr(sbase);
         if (tw <= 32) {
             const int half = PAIR ? tw / 2 : tw;
             const int wteam = c.warp * (32 / tw);
@@ -673,7 +666,7 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
                 const int rr = L.team + j * teams;
                 const bool real = L.active && rr < n;
                 const int mrow = (real ? rr : 0) * per + L.hsel;
-                float v = real ? lane_row<DT>(buf + (size_t)mrow * rowq + xoff, sbase + mrow * rowd + soff, x2, L.nseg)
+                float v = real ? lane_row<DT>(buf + (size_t)mrow * rowq + xoff, sbase + mrow * rowd + soff, xr, L.nseg)
                                : 0.f;
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1)
@@ -696,16 +689,15 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
             for (int j = 0;; j++) {
                 const int rbase = (L.team + j * teams) * RPP;
                 if (rbase >= n) break;
-                const uint8_t* wq[RPP];
-                const uint8_t* ws[RPP];
+                uint32_t wq[RPP], ws[RPP];
 #pragma unroll
                 for (int k = 0; k < RPP; k++) {
                     const int mr = min(rbase + k, n - 1) * per + L.hsel;
-                    wq[k] = buf + (size_t)mr * rowq + xoff;
-                    ws[k] = sbase + mr * rowd + soff;
+                    wq[k] = sbuf + (uint32_t)(mr * rowq + xoff);
+                    ws[k] = ssc + (uint32_t)(mr * rowd + soff);
                 }
                 float v[RPP];
-                lane_rows<DT, RPP>(wq, ws, x2, L.nseg, v);
+                lane_rows<DT, RPP>(wq, ws, xr, L.nseg, v);
                 float keep;
                 if constexpr (RPP == 4) {
                     const bool u16 = (c.lane & 16) != 0;
@@ -816,7 +808,7 @@ __device__ void attention_prologue(Consumer& c, const LayerDev& L, int layer, in
     float* kf = q_s + GD;
     __half* kp = reinterpret_cast<__half*>(kf + hd);
     __half* vp = kp + hd;
-    const unsigned long long* qkv = c.tv(layer, c.tl.qkv);
+    const unsigned long long* qkv = c.tv(layer, c.tl().qkv);
     {
         float qv[2], kv = 0.f, vv = 0.f;
 #pragma unroll
@@ -866,6 +858,7 @@ __device__ void attention_merge(Consumer& c, int layer, int g) {
     if (tid == 0) sm.misc()[1] = atom_add_acq_rel(mc, 1u) == (unsigned)(S - 1);
     consumer_sync();
     if (sm.misc()[1]) {
+        if (tid == 0) trace_mark(p, 576 + 4 * layer + 2);
         // weights per head, one warp per head and one split per lane (S <= 32)
         const int MS = p.max_splits;
         float* wgt = sm.comb();                                    // [gq][S]
@@ -892,9 +885,10 @@ __device__ void attention_merge(Consumer& c, int layer, int g) {
 #pragma unroll
                 for (int k = 0; k < 32; k++)
                     if (k < S) v = fmaf(wgt[hh * S + k], av[k], v);
-                st_tagged(c.tv(layer, c.tl.attn) + (h0 + hh) * hd + ii, v, c.tag);
+                st_tagged(c.tv(layer, c.tl().attn) + (h0 + hh) * hd + ii, v, c.tag);
             }
         }
+        if (tid == 0) trace_mark(p, 576 + 4 * layer + 3);
     }
     consumer_sync();
 }
@@ -1083,6 +1077,7 @@ __device__ bool attention_unit_mma(Consumer& c, const LayerDev& L, int layer, in
     const __half* vp = kp + HD;
     const bool writer = t0 <= p.pos && p.pos < t1;
     attention_prologue(c, L, layer, g, writer);
+    if (tid == 0) trace_mark(p, 576 + 4 * layer);
 
     // A fragments of q: row r = lane / 4 is part (r & 1) of head r / 2
     const int r = lane >> 2, t = lane & 3, hq = r >> 1, part = r & 1;
@@ -1232,6 +1227,7 @@ __device__ bool attention_unit_mma(Consumer& c, const LayerDev& L, int layer, in
     fence_proxy_async_smem();                                      // the slot's next fill is a TMA write
     consumer_sync();
     c.release(slot);
+    if (tid == 0) trace_mark(p, 576 + 4 * layer + 1);
     attention_merge(c, layer, g);
     return true;
 }
@@ -1282,7 +1278,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
             if (tid == 0) trace_mark(p, 240);
             c.tk = -1;
             m = &p.out;
-            src = XSrc{c.tv(p.n_layers - 1, c.tl.xd), p.out_norm, p.dim};
+            src = XSrc{c.tv(p.n_layers - 1, c.tl().xd), p.out_norm, p.dim};
             e.kind = Epi::kLogits;
             e.logits = p.logits;
         } else if (k == 0) {
@@ -1294,9 +1290,9 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
             if (tid == 0) trace_mark(p, 10 * l);
             c.tk = 160 + 4 * l;
             m = &L.qkv;
-            src = XSrc{l == 0 ? nullptr : c.tv(l - 1, c.tl.xd), L.attn_norm, p.dim};
+            src = XSrc{l == 0 ? nullptr : c.tv(l - 1, c.tl().xd), L.attn_norm, p.dim};
             e.kind = Epi::kStore;
-            e.out = c.tv(l, c.tl.qkv);
+            e.out = c.tv(l, c.tl().qkv);
             e.bias = L.qkv_bias ? sm.bias() : nullptr;
             e.base = q0;
         } else if (k == 1) {
@@ -1309,9 +1305,9 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
             if (tid == 0) trace_mark(p, 10 * l + 4);
             c.tk = 160 + 4 * l + 1;
             m = &L.o;
-            src = XSrc{c.tv(l, c.tl.attn), nullptr, p.q_dim};
+            src = XSrc{c.tv(l, c.tl().attn), nullptr, p.q_dim};
             e.kind = Epi::kResidual;
-            e.out = c.tv(l, c.tl.xo);
+            e.out = c.tv(l, c.tl().xo);
             e.sm = sm.xown();
             e.base = c.own0;
         } else if (k == 2) {
@@ -1319,9 +1315,9 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
             if (tid == 0) trace_mark(p, 10 * l + 6);
             c.tk = 160 + 4 * l + 2;
             m = &L.gu;
-            src = XSrc{c.tv(l, c.tl.xo), L.ffn_norm, p.dim};
+            src = XSrc{c.tv(l, c.tl().xo), L.ffn_norm, p.dim};
             e.kind = Epi::kSwiGLU;
-            e.out = c.tv(l, c.tl.u);
+            e.out = c.tv(l, c.tl().u);
             e.sm = sm.bias();
             cta_rows(L.gu.rows, e.base, e.end);
         } else {
@@ -1329,9 +1325,9 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
             if (tid == 0) trace_mark(p, 10 * l + 8);
             c.tk = 160 + 4 * l + 3;
             m = &L.down;
-            src = XSrc{c.tv(l, c.tl.u), nullptr, p.ffn};
+            src = XSrc{c.tv(l, c.tl().u), nullptr, p.ffn};
             e.kind = Epi::kResidual;
-            e.out = c.tv(l, c.tl.xd);
+            e.out = c.tv(l, c.tl().xd);
             e.sm = sm.xown();
             e.base = c.own0;
         }
@@ -1440,7 +1436,7 @@ bool matrix_plan(DMat& m, int wtype, bool pair) {
         if (tw / 32 > kConsumerWarps) return false;
         teams = kConsumerWarps / (tw / 32);
         if (teams > kMaxTeams) teams = kMaxTeams;
-        rows_per_pass = (wtype == LLM_Q8_0 ? 4 : 2) * teams;
+        rows_per_pass = (wtype == LLM_Q8_0 ? RowsPerPass<LLM_Q8_0>::value : 2) * teams;
     }
     const int slot_rows = kSlotBytes / slot_row_bytes(wtype, m.cols, m.dstride);
     if (slot_rows < 1) return false;

@@ -108,6 +108,8 @@ struct StepParams {
 //   producer  256 + 8*l + {0..4}: first issue of QKV, ATTN, O, GU, DOWN; 256 + 8*l + 5: layer issued
 //             448, 449: LOGITS first issue, all issued
 //   consumer  512 + 4*l + {0..3}: activation lanes loaded in QKV, O, GU, DOWN
+//   consumer  576 + 4*l + {0..3}: attention unit: q/k/v read and rotated, partial stored,
+//             chosen to merge (merging unit only), merged output stored (merging unit only)
 //   producer  640 + 4*l + {0..3}: first copy of QKV, O, GU, DOWN issued
 //   consumer  768 + 4*l + {0..3}: SM cycles thread 0 waited for full slots in QKV, O, GU, DOWN
 //   producer  896 + 4*l + {0..3}: SM cycles the producer waited for free slots while issuing them
