@@ -333,13 +333,12 @@ struct Consumer {
 
 // --------------------------------------------------------- weight decode --
 // Element i of row r, decoded exactly as the format defines it: Q8_0
-// d * qs (an exact float product; quants stored as qs + 128), F16 widened,
-// F32 as stored.
+// d * qs (an exact float product), F16 widened, F32 as stored.
 template <int DT>
 __device__ __forceinline__ float weight_at(const DMat& m, int r, int i) {
     if constexpr (DT == LLM_Q8_0) {
         const float d = __half2float(m.d[(size_t)r * m.dstride + i / 32]);
-        return __fmul_rn(d, (float)((int)m.q[(size_t)r * m.cols + i] - 128));
+        return __fmul_rn(d, (float)(int)(int8_t)m.q[(size_t)r * m.cols + i]);
     } else if constexpr (DT == LLM_F16) {
         return __half2float(reinterpret_cast<const __half*>(m.q)[(size_t)r * m.cols + i]);
     } else {
@@ -348,15 +347,92 @@ __device__ __forceinline__ float weight_at(const DMat& m, int r, int i) {
 }
 
 // ------------------------------------------------------------ lane dots --
-// A lane's 32 elements of one row (in the slot) against its 32 activations,
-// held as floats in registers (x2).
-// Q8_0: one 32-element block; each biased quant byte is placed in the low
-// mantissa of 2^23 and 2^23 + 128 is subtracted, which yields the exact
-// integer qs as a float, then the block's FP16 scale multiplies the sum.
+// A lane's 32 elements of one row (in the slot) against its 32 activations.
+//
+// F16 / F32: the activations are floats in registers (x2) and each product is
+// an F32 FMA.
+//
+// Q8_0: the row's block is 32 int8 quants qs and one F16 scale d.  The lane's
+// activations are held as fixed-point integers X_j = round(x_j * 2^e), e
+// chosen from the largest |x_j| of the block so that |X_j| <= 2^22 (a
+// resolution of 2^-22 of the block maximum, about what an F32 sum of the
+// block's products keeps), as three base-256 digits X_j = D0_j + 256 D1_j +
+// 65536 D2_j (D0, D1 unsigned bytes, D2 a signed byte).  The block's dot
+// product is then exact integer arithmetic, four products per dp4a:
+//   sum_j qs_j X_j = sum_k 256^k sum_j qs_j Dk_j,
+// and the row's part is d * 2^-e times that sum, taken in float.  The digits
+// of each 32-element block are made once per CTA while the phase's vector is
+// staged (convert_group), and each lane loads its block's record.
 template <int DT>
 struct XReg {
     float2 x2[16];
 };
+
+template <>
+struct XReg<LLM_Q8_0> {
+    uint32_t d[3][8];   // digit k of elements 4i..4i+3 (byte b = element 4i + b)
+    float inv;          // 2^-e
+};
+
+// d = a . b + c over four byte lanes: a signed, b unsigned / signed.
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// sum_j qs_j X_j of one block (two 16-byte words of quants), in float: each
+// digit's sum is an exact integer below 2^21 in magnitude.
+__device__ __forceinline__ float q8_block_sum(const uint4 (&w)[2], const XReg<LLM_Q8_0>& xr) {
+    const uint32_t u[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
+    int a0 = 0, a1 = 0, a2 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        a0 = dp4a_su(u[i], xr.d[0][i], a0);
+        a1 = dp4a_su(u[i], xr.d[1][i], a1);
+        a2 = dp4a_ss(u[i], xr.d[2][i], a2);
+    }
+    return fmaf(fmaf((float)a2, 256.f, (float)a1), 256.f, (float)a0);
+}
+
+// One staged group (four floats, word w of 32-element block b of the staging
+// region xv) becomes its share of the block's digit record, in place: the
+// record is 16-byte units u = 0..6 at unit u ^ (b & 7) of the block's 128
+// bytes (the same swizzle as the staged words): units 0-1 digit 0 of the
+// block's 32 elements, 2-3 digit 1, 4-5 digit 2, unit 6 {2^-e, 0, 0, 0}.
+// The 8 groups of a block are held by lanes 8j..8j+7 of one warp, which meet
+// in the shuffles for the block maximum after reading their words and before
+// writing; every lane of the warp calls this (valid or not).
+__device__ __forceinline__ void convert_group(float4* xv, int b, int w, bool valid, float4 v) {
+    float m = valid ? fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) : 0.f;
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    // m < 2^(be - 126) for the biased exponent be of m, so e = 148 - be keeps
+    // |x| * 2^e below 2^22; zero and subnormal blocks take the largest e
+    const int be = (int)((__float_as_uint(m) >> 23) & 0xFFu);
+    const int e = be == 0 ? 126 : max(-126, min(126, 148 - be));
+    const float sc = __uint_as_float((uint32_t)(127 + e) << 23);
+    const int X0 = __float2int_rn(__fmul_rn(v.x, sc)), X1 = __float2int_rn(__fmul_rn(v.y, sc));
+    const int X2 = __float2int_rn(__fmul_rn(v.z, sc)), X3 = __float2int_rn(__fmul_rn(v.w, sc));
+    const uint32_t lo = __byte_perm((uint32_t)X0, (uint32_t)X1, 0x5140u);   // bytes 0,1 of X0 and X1
+    const uint32_t hi = __byte_perm((uint32_t)X2, (uint32_t)X3, 0x5140u);
+    const uint32_t b2 = __byte_perm(__byte_perm((uint32_t)X0, (uint32_t)X1, 0x0062u),
+                                    __byte_perm((uint32_t)X2, (uint32_t)X3, 0x0062u), 0x5410u);
+    if (valid) {
+        uint32_t* blk = reinterpret_cast<uint32_t*>(xv + 8 * b);
+        const int r = b & 7;
+        blk[4 * ((0 + (w >> 2)) ^ r) + (w & 3)] = __byte_perm(lo, hi, 0x5410u);   // byte 0 of X0..X3
+        blk[4 * ((2 + (w >> 2)) ^ r) + (w & 3)] = __byte_perm(lo, hi, 0x7632u);   // byte 1
+        blk[4 * ((4 + (w >> 2)) ^ r) + (w & 3)] = b2;                             // byte 2 (signed)
+        if (w == 0) reinterpret_cast<uint4*>(blk)[6 ^ r] = make_uint4((uint32_t)(127 - e) << 23, 0u, 0u, 0u);
+    }
+}
 
 template <int DT>
 struct LaneDot;
@@ -364,19 +440,6 @@ struct LaneDot;
 template <>
 struct LaneDot<LLM_Q8_0> {
     static constexpr int kSeg = 2;           // 16-byte words per lane and row
-    __device__ __forceinline__ static void acc(const uint4* w, const float2 (&x2)[16], float2& c0, float2& c1) {
-        const float2 off = make_float2(-8388736.0f, -8388736.0f);
-        const uint32_t u[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
-#pragma unroll
-        for (int k = 0; k < 8; k++) {
-            float2 lo = make_float2(__uint_as_float(__byte_perm(u[k], 0x4B000000u, 0x7540u)),
-                                    __uint_as_float(__byte_perm(u[k], 0x4B000000u, 0x7541u)));
-            float2 hi = make_float2(__uint_as_float(__byte_perm(u[k], 0x4B000000u, 0x7542u)),
-                                    __uint_as_float(__byte_perm(u[k], 0x4B000000u, 0x7543u)));
-            c0 = __ffma2_rn(__fadd2_rn(lo, off), x2[2 * k], c0);
-            c1 = __ffma2_rn(__fadd2_rn(hi, off), x2[2 * k + 1], c1);
-        }
-    }
 };
 
 template <>
@@ -416,11 +479,14 @@ __device__ __forceinline__ float lane_row(const uint8_t* w, const uint8_t* scale
     uint4 v[NS];
 #pragma unroll
     for (int s = 0; s < NS; s++) v[s] = s < nseg ? reinterpret_cast<const uint4*>(w)[s] : make_uint4(0u, 0u, 0u, 0u);
-    float2 c0 = make_float2(0.f, 0.f), c1 = c0;
-    LaneDot<DT>::acc(v, xr.x2, c0, c1);
-    const float t = (c0.x + c0.y) + (c1.x + c1.y);
-    if constexpr (DT == LLM_Q8_0) return nseg ? __half2float(*reinterpret_cast<const __half*>(scale)) * t : 0.f;
-    return t;
+    if constexpr (DT == LLM_Q8_0) {
+        if (!nseg) return 0.f;
+        return __half2float(*reinterpret_cast<const __half*>(scale)) * (q8_block_sum(v, xr) * xr.inv);
+    } else {
+        float2 c0 = make_float2(0.f, 0.f), c1 = c0;
+        LaneDot<DT>::acc(v, xr.x2, c0, c1);
+        return (c0.x + c0.y) + (c1.x + c1.y);
+    }
 }
 
 // Rows a multi-warp team reduces per pass: four for Q8_0 (two 16-byte words
@@ -453,14 +519,19 @@ __device__ __forceinline__ void lane_rows(const uint32_t (&w)[N], const uint32_t
     for (int r = 0; r < N; r++)
 #pragma unroll
         for (int s = 0; s < NS; s++) a[r][s] = s < nseg ? lds128(w[r] + 16 * s) : make_uint4(0u, 0u, 0u, 0u);
-    float dsc[N];
+    if constexpr (DT == LLM_Q8_0) {
+        float dq[N];
 #pragma unroll
-    for (int r = 0; r < N; r++) dsc[r] = DT == LLM_Q8_0 && nseg ? lds_half(sc[r]) : 1.f;
+        for (int r = 0; r < N; r++) dq[r] = nseg ? lds_half(sc[r]) : 0.f;
 #pragma unroll
-    for (int r = 0; r < N; r++) {
-        float2 c0 = make_float2(0.f, 0.f), c1 = c0;
-        LaneDot<DT>::acc(a[r], xr.x2, c0, c1);
-        v[r] = DT == LLM_Q8_0 && !nseg ? 0.f : dsc[r] * ((c0.x + c0.y) + (c1.x + c1.y));
+        for (int r = 0; r < N; r++) v[r] = dq[r] * (q8_block_sum(a[r], xr) * xr.inv);
+    } else {
+#pragma unroll
+        for (int r = 0; r < N; r++) {
+            float2 c0 = make_float2(0.f, 0.f), c1 = c0;
+            LaneDot<DT>::acc(a[r], xr.x2, c0, c1);
+            v[r] = (c0.x + c0.y) + (c1.x + c1.y);
+        }
     }
 }
 
@@ -617,15 +688,41 @@ __device__ __forceinline__ void lane_x(Consumer& c, const Lanes& L, const XSrc& 
                                         __fmul_rn(__fmul_rn(x.z, scale), g.z), __fmul_rn(__fmul_rn(x.w, scale), g.w));
             }
         }
-        consumer_sync();
         // lanes whose slice lies in this piece (slices never straddle pieces)
         const int sl = (col0 - base) >> 5;
-        if (col0 >= base && col0 < base + len) {
-            const float4* x4 = xv + sl * 8;
-            const int rot = sl & 7;
-            xreg_from_words<DT>([&](int k) { return have && col0 + 4 * k < src.n ? x4[k ^ rot] : zero; }, xr);
-        } else if (base == 0 && !have) {
-            xreg_from_words<DT>([&](int) { return zero; }, xr);
+        const bool mine = col0 >= base && col0 < base + len;
+        if constexpr (DT == LLM_Q8_0) {
+            // every staged group becomes its share of its block's digit record
+            for (int i0 = c.tid - c.lane; i0 < ngr; i0 += kConsumers) {
+                const int i = i0 + c.lane;
+                const bool valid = i < ngr;
+                convert_group(xv, i >> 3, i & 7, valid, valid ? xv[sw(i)] : zero);
+            }
+            consumer_sync();
+            if (mine && have) {
+                const uint4* rec = reinterpret_cast<const uint4*>(xv + sl * 8);
+                const int rot = sl & 7;
+#pragma unroll
+                for (int k = 0; k < 3; k++) {
+                    const uint4 a = rec[(2 * k) ^ rot], b = rec[(2 * k + 1) ^ rot];
+                    xr.d[k][0] = a.x; xr.d[k][1] = a.y; xr.d[k][2] = a.z; xr.d[k][3] = a.w;
+                    xr.d[k][4] = b.x; xr.d[k][5] = b.y; xr.d[k][6] = b.z; xr.d[k][7] = b.w;
+                }
+                xr.inv = __uint_as_float(rec[6 ^ rot].x);
+            } else if (base == 0) {
+#pragma unroll
+                for (int k = 0; k < 8; k++) xr.d[0][k] = xr.d[1][k] = xr.d[2][k] = 0u;
+                xr.inv = 0.f;
+            }
+        } else {
+            consumer_sync();
+            if (mine) {
+                const float4* x4 = xv + sl * 8;
+                const int rot = sl & 7;
+                xreg_from_words<DT>([&](int k) { return have && col0 + 4 * k < src.n ? x4[k ^ rot] : zero; }, xr);
+            } else if (base == 0 && !have) {
+                xreg_from_words<DT>([&](int) { return zero; }, xr);
+            }
         }
         if (base + len < src.n) consumer_sync();       // the next piece overwrites the region
     }

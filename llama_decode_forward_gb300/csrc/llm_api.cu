@@ -105,9 +105,9 @@ static size_t mat_bytes(int wtype, long long rows, long long cols) {
     return (size_t)(rows * cols * (wtype == LLM_F16 ? 2 : 4));
 }
 
-// Q8_0 blocks (34 bytes: FP16 scale, 32 int8) of `rows` rows -> biased
-// quants (qs + 128) and scales of the library layout; source row r goes to
-// destination row dst0 + r*mul + phase.
+// Q8_0 blocks (34 bytes: FP16 scale, 32 int8) of `rows` rows -> the int8
+// quants and the scales of the library layout (two planes); source row r goes
+// to destination row dst0 + r*mul + phase.
 __global__ void repack_q8_kernel(const uint8_t* __restrict__ src, int rows, int cols, uint8_t* dq, __half* dd,
                                  int dstride, int dst0, int mul, int phase) {
     const int nb = cols / 32;
@@ -124,8 +124,6 @@ __global__ void repack_q8_kernel(const uint8_t* __restrict__ src, int rows, int 
             w[k] = (uint32_t)s[2 + 4 * k] | ((uint32_t)s[3 + 4 * k] << 8) | ((uint32_t)s[4 + 4 * k] << 16) |
                    ((uint32_t)s[5 + 4 * k] << 24);
         uint4* d = reinterpret_cast<uint4*>(dq + dr * cols + (long long)j * 32);
-#pragma unroll
-        for (int k = 0; k < 8; k++) w[k] ^= 0x80808080u;          // stored biased: qs + 128
         d[0] = make_uint4(w[0], w[1], w[2], w[3]);
         d[1] = make_uint4(w[4], w[5], w[6], w[7]);
     }

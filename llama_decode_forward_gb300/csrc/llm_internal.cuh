@@ -24,8 +24,8 @@ constexpr int kMaxSmem = 232448;                  // 227 KB opt-in dynamic share
 // Device error word bits (sticky until llm_reset).
 enum : int { kErrNone = 0, kErrTimeout = 1, kErrToken = 2 };
 
-// A weight matrix in the library's layout.  Q8_0: row r is `cols` quants at
-// q + r*cols, each stored biased as the unsigned byte qs + 128, and cols/32
+// A weight matrix in the library's layout.  Q8_0: row r is `cols` int8 quants
+// at q + r*cols, and cols/32
 // FP16 scales at d + r*dstride (dstride = cols/32 rounded up to a multiple of
 // 8, so every row of scales is 16-byte aligned).
 // F16 / F32: `rows` rows of `cols` values at q.

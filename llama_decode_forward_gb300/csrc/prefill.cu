@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(128, 2) gemm_f16_kernel(const __grid_constant_
 }
 
 // Embedding rows of the batch: F16 widened, or Q8_0 decoded as d * qs (both
-// exact in F32; Q8_0 quants are stored as qs + 128).
+// exact in F32; Q8_0 quants are stored as int8).
 __global__ void embed_rows_kernel(const int* tok, int n, DMat embd, int wtype, int dim, float* X) {
     const int i = blockIdx.x;
     if (i >= n) return;
@@ -194,7 +194,7 @@ __global__ void embed_rows_kernel(const int* tok, int n, DMat embd, int wtype, i
     for (int d = threadIdx.x; d < dim; d += blockDim.x) {
         float v;
         if (wtype == LLM_Q8_0)
-            v = __fmul_rn(__half2float(embd.d[r * embd.dstride + d / 32]), (float)((int)embd.q[r * embd.cols + d] - 128));
+            v = __fmul_rn(__half2float(embd.d[r * embd.dstride + d / 32]), (float)(int)(int8_t)embd.q[r * embd.cols + d]);
         else
             v = __half2float(reinterpret_cast<const __half*>(embd.q)[r * embd.cols + d]);
         X[(size_t)i * dim + d] = v;
@@ -217,7 +217,7 @@ __global__ void q8_to_f16_kernel(DMat m, int rows, __half* out) {
         __half h[8];
 #pragma unroll
         for (int k = 0; k < 8; k++) {
-            const int q = (int)((w[k / 4] >> (8 * (k % 4))) & 0xFFu) - 128;
+            const int q = (int)(int8_t)((w[k / 4] >> (8 * (k % 4))) & 0xFFu);
             h[k] = __float2half_rn(__fmul_rn(d, (float)q));
         }
         *reinterpret_cast<uint4*>(out + e) = *reinterpret_cast<const uint4*>(h);
@@ -404,7 +404,7 @@ __global__ void logits_kernel(DMat out, int wtype, const float* y, int dim, int 
                 for (int k = 0; k < 32; k += 4) {
                     const uint32_t w4 = *reinterpret_cast<const uint32_t*>(q + b * 32 + k);
 #pragma unroll
-                    for (int j = 0; j < 4; j++) t = fmaf((float)((int)((w4 >> (8 * j)) & 0xFFu) - 128), ys[b * 32 + k + j], t);
+                    for (int j = 0; j < 4; j++) t = fmaf((float)(int)(int8_t)((w4 >> (8 * j)) & 0xFFu), ys[b * 32 + k + j], t);
                 }
                 s = fmaf(__half2float(out.d[(size_t)r * out.dstride + b]), t, s);
             }
