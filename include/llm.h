@@ -209,6 +209,104 @@ void llm_destroy(llm_handle *h);
 const char *llm_status_string(int status);
 const char *llm_last_error(const llm_handle *h);
 
+/* ------------------------------------------------------------ GGUF files --
+ * A model file in the GGUF version 3 layout of "Loading GGUF with the FFM API"
+ * (codeloopback.dev, llm-gguf-loader-ffm): a 24-byte header (magic "GGUF",
+ * version, tensor count, key-value count; Example 3), key-value metadata
+ * (Examples 4, 13), tensor infos (name, dims innermost first, ggml type,
+ * offset into the data section; Example 5), padding to general.alignment
+ * (UINT32, 32 when absent), then the data section with each tensor padded to
+ * the alignment.  All numbers little-endian.  Host memory only; none of these
+ * calls touches the GPU except llm_create_from_gguf. */
+typedef struct llm_gguf llm_gguf;
+
+/* Metadata value types ("Loading GGUF with the FFM API", Example 13). */
+typedef enum {
+    LLM_GGUF_UINT8 = 0, LLM_GGUF_INT8 = 1, LLM_GGUF_UINT16 = 2, LLM_GGUF_INT16 = 3, LLM_GGUF_UINT32 = 4,
+    LLM_GGUF_INT32 = 5, LLM_GGUF_FLOAT32 = 6, LLM_GGUF_BOOL = 7, LLM_GGUF_STRING = 8, LLM_GGUF_ARRAY = 9,
+    LLM_GGUF_UINT64 = 10, LLM_GGUF_INT64 = 11, LLM_GGUF_FLOAT64 = 12
+} llm_gguf_type;
+
+typedef struct {
+    uint32_t version;
+    int64_t n_tensors, n_kv;
+    uint64_t alignment;      /* general.alignment, or 32 */
+    uint64_t infos_end;      /* file byte where the tensor infos end */
+    uint64_t data_start;     /* infos_end rounded up to the alignment */
+    uint64_t file_size;
+} llm_gguf_layout;
+
+typedef struct {
+    int32_t type;            /* ggml type: LLM_F32, LLM_F16 or LLM_Q8_0 */
+    int32_t n_dims;          /* 1..4 */
+    int64_t dims[4];         /* innermost first; unused ones are 1 */
+    uint64_t offset;         /* from the start of the data section */
+    uint64_t file_offset;    /* data_start + offset */
+    uint64_t bytes;          /* F32 4, F16 2 per value, Q8_0 34 per 32-value block */
+    const void *data;        /* HOST view into the mapped file, valid until llm_gguf_close */
+} llm_gguf_tensor;
+
+/* Opens and maps `path` read-only and checks it in the loader page's order
+ * (Example 11): at least the 24-byte header, the magic, version 3, metadata
+ * and tensor infos within the file, a nonzero UINT32 general.alignment when
+ * present, every tensor of type F32 / F16 / Q8_0 (Q8_0 rows whole 32-value
+ * blocks), each tensor's offset equal to the padded sizes of the tensors
+ * before it, and each tensor's end within the file.  On success *out owns
+ * the mapping (free with llm_gguf_close).  Errors: INVALID_ARG (missing file,
+ * failed check; `err`, when not NULL, receives a one-line reason of at most
+ * err_len bytes, e.g. "magic 0x4C4D4747 is not GGUF"), UNSUPPORTED (version,
+ * tensor type), NO_MEMORY (mapping failed); *out is NULL then. */
+int llm_gguf_open(const char *path, llm_gguf **out, char *err, size_t err_len);
+void llm_gguf_close(llm_gguf *g);
+
+/* The header counts and the layout of the file (Example 5). */
+int llm_gguf_summary(const llm_gguf *g, llm_gguf_layout *s);
+
+/* A tensor by name, or by index in file order (name: HOST string owned by g).
+ * Errors: INVALID_ARG (NULL), OUT_OF_RANGE (no such tensor / index). */
+int llm_gguf_find_tensor(const llm_gguf *g, const char *name, llm_gguf_tensor *t);
+int llm_gguf_tensor_at(const llm_gguf *g, int64_t i, const char **name, llm_gguf_tensor *t);
+
+/* Metadata: the i-th key in file order with its type; a key's type (element
+ * type and count for arrays, byte count for strings, 1 otherwise); an integer
+ * value (any of the integer types and BOOL; UINT64 above INT64_MAX is
+ * OUT_OF_RANGE); a float value (FLOAT32 widened, FLOAT64); a string value (a
+ * HOST pointer into the mapping, `len` bytes of UTF-8, not zero-terminated).
+ * Errors: OUT_OF_RANGE (no such key / index), INVALID_ARG (NULL, other type). */
+int llm_gguf_meta_at(const llm_gguf *g, int64_t i, const char **key, int32_t *type);
+int llm_gguf_meta_type(const llm_gguf *g, const char *key, int32_t *type, int32_t *elem_type, uint64_t *count);
+int llm_gguf_meta_int(const llm_gguf *g, const char *key, int64_t *out);
+int llm_gguf_meta_float(const llm_gguf *g, const char *key, double *out);
+int llm_gguf_meta_string(const llm_gguf *g, const char *key, const char **s, uint64_t *len);
+
+/* The model shape from the metadata ("The Forward Pass in Java", Example 1):
+ * general.architecture "llama" (RoPE pairs (2i, 2i+1)) or "qwen2" (NEOX
+ * pairs); <arch>.embedding_length, block_count, attention.head_count,
+ * feed_forward_length, context_length, attention.layer_norm_rms_epsilon;
+ * optional attention.head_count_kv (default head_count), rope.freq_base
+ * (10000), rope.dimension_count (dim / heads), vocab_size (the length of the
+ * tokenizer.ggml.tokens array); wtype = the type of token_embd.weight.
+ * max_seq > 0 sets the KV-cache rows, else <arch>.context_length is used.
+ * Errors: INVALID_ARG (missing or mistyped key, no token_embd.weight),
+ * UNSUPPORTED (other architecture); `err` as for llm_gguf_open. */
+int llm_gguf_config(const llm_gguf *g, int32_t max_seq, llm_config *cfg, char *err, size_t err_len);
+
+/* A handle for the model in the file: llm_gguf_config, then the tensors of
+ * "The Forward Pass in Java", Example 13, by their llama.cpp names —
+ * token_embd.weight, output_norm.weight, output.weight (absent: tied to the
+ * embedding), rope_freqs.weight (optional), and for each layer N
+ * blk.N.attn_norm, attn_q, attn_k, attn_v, attn_output, ffn_norm, ffn_gate,
+ * ffn_up, ffn_down (.weight) and the optional blk.N.attn_q/k/v.bias — each
+ * checked for its shape (matrices [in, out], vectors [n]) and type (every
+ * matrix the embedding's type, vectors F32), copied once to a temporary
+ * device buffer, given to llm_create on `stream`, and freed before return.
+ * The file stays owned by the caller (the handle keeps no reference to it).
+ * Synchronous.  Errors: those of llm_gguf_config and llm_create, INVALID_ARG
+ * / UNSUPPORTED for a missing or mismatched tensor, NO_MEMORY / CUDA for the
+ * staging buffer; *out is NULL then and `err` holds the reason. */
+int llm_create_from_gguf(const llm_gguf *g, int32_t max_seq, llm_stream_t stream, llm_handle **out, char *err,
+                         size_t err_len);
+
 #ifdef __cplusplus
 }
 #endif

@@ -37,6 +37,18 @@ class llm_weights(ctypes.Structure):
                 ("rope_freqs", ctypes.c_void_p), ("layers", ctypes.POINTER(llm_layer_weights))]
 
 
+class llm_gguf_layout(ctypes.Structure):
+    _fields_ = [("version", ctypes.c_uint32), ("n_tensors", ctypes.c_int64), ("n_kv", ctypes.c_int64),
+                ("alignment", ctypes.c_uint64), ("infos_end", ctypes.c_uint64), ("data_start", ctypes.c_uint64),
+                ("file_size", ctypes.c_uint64)]
+
+
+class llm_gguf_tensor(ctypes.Structure):
+    _fields_ = [("type", ctypes.c_int32), ("n_dims", ctypes.c_int32), ("dims", ctypes.c_int64 * 4),
+                ("offset", ctypes.c_uint64), ("file_offset", ctypes.c_uint64), ("bytes", ctypes.c_uint64),
+                ("data", ctypes.c_void_p)]
+
+
 _vp, _i32, _int = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int
 _SIGS = {
     "llm_create": ([ctypes.POINTER(llm_config), ctypes.POINTER(llm_weights), _vp, ctypes.POINTER(_vp)], _int),
@@ -54,6 +66,20 @@ _SIGS = {
     "llm_decode_step_noalloc": ([_vp, _vp, _i32, _vp, _vp], _int),
     "llm_launch_count": ([_vp], ctypes.c_int64),
     "llm_destroy": ([_vp], None),
+    "llm_gguf_open": ([ctypes.c_char_p, ctypes.POINTER(_vp), ctypes.c_char_p, ctypes.c_size_t], _int),
+    "llm_gguf_close": ([_vp], None),
+    "llm_gguf_summary": ([_vp, ctypes.POINTER(llm_gguf_layout)], _int),
+    "llm_gguf_find_tensor": ([_vp, ctypes.c_char_p, ctypes.POINTER(llm_gguf_tensor)], _int),
+    "llm_gguf_tensor_at": ([_vp, ctypes.c_int64, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(llm_gguf_tensor)],
+                           _int),
+    "llm_gguf_meta_at": ([_vp, ctypes.c_int64, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(_i32)], _int),
+    "llm_gguf_meta_type": ([_vp, ctypes.c_char_p, ctypes.POINTER(_i32), ctypes.POINTER(_i32),
+                            ctypes.POINTER(ctypes.c_uint64)], _int),
+    "llm_gguf_meta_int": ([_vp, ctypes.c_char_p, ctypes.POINTER(ctypes.c_int64)], _int),
+    "llm_gguf_meta_float": ([_vp, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double)], _int),
+    "llm_gguf_meta_string": ([_vp, ctypes.c_char_p, ctypes.POINTER(_vp), ctypes.POINTER(ctypes.c_uint64)], _int),
+    "llm_gguf_config": ([_vp, _i32, ctypes.POINTER(llm_config), ctypes.c_char_p, ctypes.c_size_t], _int),
+    "llm_create_from_gguf": ([_vp, _i32, _vp, ctypes.POINTER(_vp), ctypes.c_char_p, ctypes.c_size_t], _int),
     "llm_status_string": ([_int], ctypes.c_char_p),
     "llm_last_error": ([_vp], ctypes.c_char_p),
 }
@@ -269,6 +295,130 @@ class Decoder:
     def logits_tensor(self):
         import torch
         return _wrap_device(llm_logits_device(self.h), self.cfg.vocab, torch.float32)
+
+
+# ------------------------------------------------------------ GGUF --
+class GgufFile:
+    """A GGUF file opened by the library (llm_gguf_open): checked at open,
+    memory-mapped until close().  Raises LlmError with the library's reason."""
+
+    def __init__(self, path: str):
+        err = ctypes.create_string_buffer(512)
+        g = _vp()
+        rc = _lib.llm_gguf_open(os.fsencode(path), ctypes.byref(g), err, len(err))
+        if rc != LLM_OK:
+            raise LlmError(rc, err.value.decode())
+        self.g = g.value
+
+    def close(self):
+        if getattr(self, "g", None):
+            _lib.llm_gguf_close(self.g)
+            self.g = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def summary(self) -> dict:
+        s = llm_gguf_layout()
+        _check(_lib.llm_gguf_summary(self.g, ctypes.byref(s)))
+        return {n: getattr(s, n) for n, _ in llm_gguf_layout._fields_}
+
+    @staticmethod
+    def _tensor_dict(t: llm_gguf_tensor) -> dict:
+        return {"type": t.type, "dims": [t.dims[i] for i in range(t.n_dims)], "offset": t.offset,
+                "file_offset": t.file_offset, "bytes": t.bytes, "data": t.data}
+
+    def tensor(self, name: str) -> dict | None:
+        t = llm_gguf_tensor()
+        rc = _lib.llm_gguf_find_tensor(self.g, name.encode(), ctypes.byref(t))
+        if rc == LLM_ERR_OUT_OF_RANGE:
+            return None
+        _check(rc)
+        return self._tensor_dict(t)
+
+    def tensors(self) -> list:
+        out, i = [], 0
+        while True:
+            name, t = ctypes.c_char_p(), llm_gguf_tensor()
+            rc = _lib.llm_gguf_tensor_at(self.g, i, ctypes.byref(name), ctypes.byref(t))
+            if rc == LLM_ERR_OUT_OF_RANGE:
+                return out
+            _check(rc)
+            out.append((name.value.decode(), self._tensor_dict(t)))
+            i += 1
+
+    def keys(self) -> list:
+        out, i = [], 0
+        while True:
+            key, t = ctypes.c_char_p(), _i32()
+            rc = _lib.llm_gguf_meta_at(self.g, i, ctypes.byref(key), ctypes.byref(t))
+            if rc == LLM_ERR_OUT_OF_RANGE:
+                return out
+            _check(rc)
+            out.append((key.value.decode(), t.value))
+            i += 1
+
+    def meta_type(self, key: str):
+        t, et, n = _i32(), _i32(), ctypes.c_uint64()
+        _check(_lib.llm_gguf_meta_type(self.g, key.encode(), ctypes.byref(t), ctypes.byref(et), ctypes.byref(n)))
+        return t.value, et.value, n.value
+
+    def meta_int(self, key: str) -> int:
+        v = ctypes.c_int64()
+        _check(_lib.llm_gguf_meta_int(self.g, key.encode(), ctypes.byref(v)))
+        return v.value
+
+    def meta_float(self, key: str) -> float:
+        v = ctypes.c_double()
+        _check(_lib.llm_gguf_meta_float(self.g, key.encode(), ctypes.byref(v)))
+        return v.value
+
+    def meta_string(self, key: str) -> str:
+        p, n = _vp(), ctypes.c_uint64()
+        _check(_lib.llm_gguf_meta_string(self.g, key.encode(), ctypes.byref(p), ctypes.byref(n)))
+        return ctypes.string_at(p.value, n.value).decode("utf-8") if n.value else ""
+
+    def config(self, max_seq: int = 0) -> llm_config:
+        c, err = llm_config(), ctypes.create_string_buffer(512)
+        rc = _lib.llm_gguf_config(self.g, int(max_seq), ctypes.byref(c), err, len(err))
+        if rc != LLM_OK:
+            raise LlmError(rc, err.value.decode())
+        return c
+
+
+def llm_create_from_gguf(gguf: GgufFile, max_seq: int = 0, stream=None):
+    h, err = _vp(), ctypes.create_string_buffer(512)
+    rc = _lib.llm_create_from_gguf(gguf.g, int(max_seq), stream, ctypes.byref(h), err, len(err))
+    if rc != LLM_OK:
+        raise LlmError(rc, err.value.decode())
+    return h.value
+
+
+class GgufDecoder(Decoder):
+    """A handle created from a GGUF file (llm_create_from_gguf); ``cfg`` holds
+    the shape the library derived from the file's metadata."""
+
+    def __init__(self, path: str, max_seq: int = 0, stream=None):
+        import torch
+        from types import SimpleNamespace
+        with GgufFile(path) as g:
+            c = g.config(max_seq)
+            self.cfg = SimpleNamespace(**{n: getattr(c, n) for n, _ in llm_config._fields_})
+            if stream is None:
+                stream = torch.cuda.current_stream().cuda_stream
+            self.stream = stream
+            self.h = llm_create_from_gguf(g, max_seq, stream)
+        torch.cuda.synchronize()
+        self.dw = None
 
 
 def _wrap_device(ptr: int, n: int, dtype):

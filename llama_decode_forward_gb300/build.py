@@ -29,7 +29,7 @@ def _nvcc() -> str:
 
 
 def sources() -> list[str]:
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _inputs() -> list[str]:
@@ -54,7 +54,7 @@ def build(force: bool = False, verbose: bool = False, trace: bool = False) -> st
     defs = ["-DLLM_TRACE"] if trace else []
 
     def compile_one(src):
-        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *defs, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
