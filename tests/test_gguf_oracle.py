@@ -96,6 +96,23 @@ def test_checks_in_order(label, data, reason):
         assert str(e.value) == reason
 
 
+def test_tensor_sizes():
+    # Example 7: a [4, 3] tensor is 12 values, 48 bytes in F32 and 24 in F16;
+    # Example 8: 128 Q8_0 values make 4 blocks of 34 bytes, 136 bytes
+    assert G.tensor_bytes(G.F32, [4, 3]) == 48 and G.tensor_bytes(G.F16, [4, 3]) == 24
+    assert G.tensor_bytes(G.Q8_0, [128]) == 136
+
+
+def test_header_shorter_than_24_bytes():
+    # Example 11: a file shorter than the 24-byte header is rejected before
+    # the counts are read, whatever its length
+    good = _example11_file("GGUF", 3, 0, 32)
+    for n in (0, 4, 8, 16, 20, 23):
+        with pytest.raises(G.GgufError) as e:
+            G.read(good[:n])
+        assert str(e.value) == "shorter than the 24-byte header"
+
+
 def test_decoding_f16_and_q8_0():
     # Example 13 floats(): F16 widened (Example 6's raw bits 0xB400 = -0.25),
     # Q8_0 as d * qs per block; checked against the C oracle's own decoding
@@ -105,6 +122,7 @@ def test_decoding_f16_and_q8_0():
     g = G.read(data)
     h, q = g["tensors"]
     got = G.tensor_floats(data, h)
+    assert h["bytes"] == 8 and got.size == 4 and G.tensor_floats(data, q).size == 64
     assert got[0] == -0.25 and got[1] == 1.0 and got[2] == 65504.0 and got[3] == np.float32(2.0 ** -24)
     np.testing.assert_array_equal(G.tensor_floats(data, q), oracle.dequant_row(q8, oracle.Q8_0, 0, 64))
 
