@@ -328,6 +328,11 @@ extern "C" int llm_gguf_open(const char* path, llm_gguf** out, char* err, size_t
         close(fd);
         return LLM_ERR_INVALID_ARG;
     }
+    if (!S_ISREG(st.st_mode)) {
+        put_err(err, err_len, "%s is not a regular file", path);
+        close(fd);
+        return LLM_ERR_INVALID_ARG;
+    }
     llm_gguf* g = new llm_gguf();
     g->fd = fd;
     g->size = (uint64_t)st.st_size;

@@ -179,3 +179,11 @@ def test_truncations_are_rejected_not_read(lib, tmp_path):
             lib.GgufFile(_save(tmp_path, "t.gguf", data[:n]))
     with lib.GgufFile(_save(tmp_path, "t.gguf", data)) as g:
         assert g.summary()["file_size"] == len(data)
+
+
+def test_open_errors(lib, tmp_path):
+    # a missing path and a directory are rejected with a reason, not mapped
+    for path, words in ((tmp_path / "absent.gguf", "cannot open"), (tmp_path, "not a regular file")):
+        with pytest.raises(lib.LlmError) as e:
+            lib.GgufFile(str(path))
+        assert e.value.status == lib.LLM_ERR_INVALID_ARG and words in str(e.value)
