@@ -45,7 +45,7 @@ class _Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("n_layers", "dim", "n_heads", "n_kv_heads", "head_dim",
                                             "ffn_dim", "vocab", "max_seq", "rope_dims")] + \
                [("eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("rope_neox", ctypes.c_int),
-                ("wtype", ctypes.c_int), ("f16_cache", ctypes.c_int)]
+                ("wtype", ctypes.c_int), ("f16_cache", ctypes.c_int), ("llamacpp_rounding", ctypes.c_int)]
 
 
 class _Layer(ctypes.Structure):
@@ -90,6 +90,8 @@ def load(path: str):
     L.orc_attention.argtypes = [vp, vp, vp, vp, i, i, i, i]
     L.orc_argmax.argtypes = [vp, i]
     L.orc_argmax.restype = i
+    L.orc_matvec_llamacpp.argtypes = [vp, vp, i, vp, i, i]
+    L.orc_attention_llamacpp.argtypes = [vp, vp, vp, vp, i, i, i, i]
     return L
 
 
@@ -145,10 +147,13 @@ def rmsnorm(x, g, eps: float) -> np.ndarray:
     return out
 
 
-def matvec(w, wtype: int, x, rows: int, cols: int) -> np.ndarray:
+def matvec(w, wtype: int, x, rows: int, cols: int, llamacpp: bool = False) -> np.ndarray:
+    """W x; with ``llamacpp`` the activations are rounded as llama.cpp rounds
+    them for the weight type (orc_matvec_llamacpp)."""
     x = _f32(x)
     out = np.empty(rows, dtype=np.float32)
-    lib().orc_matvec(_p(out), _p(np.ascontiguousarray(w)), wtype, _p(x), rows, cols)
+    fn = lib().orc_matvec_llamacpp if llamacpp else lib().orc_matvec
+    fn(_p(out), _p(np.ascontiguousarray(w)), wtype, _p(x), rows, cols)
     return out
 
 
@@ -164,10 +169,14 @@ def silu(z: float) -> float:
     return lib().orc_silu(float(z))
 
 
-def attention(q, kcache, vcache, n_heads: int, n_kv_heads: int, head_dim: int, pos: int) -> np.ndarray:
+def attention(q, kcache, vcache, n_heads: int, n_kv_heads: int, head_dim: int, pos: int,
+              llamacpp: bool = False) -> np.ndarray:
+    """Attention of one position; with ``llamacpp`` q and the probabilities are
+    rounded to F16 (orc_attention_llamacpp)."""
     q, k, v = _f32(q), _f32(kcache), _f32(vcache)
     out = np.empty(n_heads * head_dim, dtype=np.float32)
-    lib().orc_attention(_p(out), _p(q), _p(k), _p(v), n_heads, n_kv_heads, head_dim, pos)
+    fn = lib().orc_attention_llamacpp if llamacpp else lib().orc_attention
+    fn(_p(out), _p(q), _p(k), _p(v), n_heads, n_kv_heads, head_dim, pos)
     return out
 
 
@@ -186,16 +195,20 @@ class OracleModel:
     (None: unit) and ``layers``: a list of dicts with attn_norm, ffn_norm, bq,
     bk, bv (None: no bias), wq, wk, wv, wo, w_gate, w_up, w_down.
     The arrays are referenced, not copied: keep them alive with this object.
+    ``llamacpp_rounding`` adds llama.cpp's rounding points ("What a Llama
+    model computes, and why" §8) to every matrix product and the attention.
     """
 
-    def __init__(self, cfg, tensors, f16_cache: bool = True, max_seq: int | None = None):
+    def __init__(self, cfg, tensors, f16_cache: bool = True, max_seq: int | None = None,
+                 llamacpp_rounding: bool = False):
         self._L = L = lib()
         self.cfg = cfg
         self.max_seq = int(max_seq if max_seq is not None else cfg.max_seq)
         c = _Config(n_layers=cfg.n_layers, dim=cfg.dim, n_heads=cfg.n_heads, n_kv_heads=cfg.n_kv_heads,
                     head_dim=cfg.head_dim, ffn_dim=cfg.ffn_dim, vocab=cfg.vocab, max_seq=self.max_seq,
                     rope_dims=cfg.rope_dims, eps=cfg.eps, rope_base=cfg.rope_base,
-                    rope_neox=int(cfg.rope_neox), wtype=cfg.wtype, f16_cache=int(f16_cache))
+                    rope_neox=int(cfg.rope_neox), wtype=cfg.wtype, f16_cache=int(f16_cache),
+                    llamacpp_rounding=int(llamacpp_rounding))
         self._keep = [tensors]
         layers = (_Layer * cfg.n_layers)()
         for l, T in enumerate(tensors.layers):

@@ -163,16 +163,23 @@ float orc_silu(float z) {
  * reads KV head h / (n_heads/n_kv_heads); s_t = (q . K_t) / sqrt(hd) for
  * t = 0..pos; softmax with the maximum subtracted (exp in double, rounded to
  * float; the sum in float); out = sum_t (e_t/sum) * V_t accumulated over t in
- * ascending order.  Rows after pos are never read (causality). */
-void orc_attention(float *out, const float *q, const float *kcache, const float *vcache,
-                   int n_heads, int n_kv_heads, int head_dim, int pos) {
+ * ascending order.  Rows after pos are never read (causality).
+ * With `llamacpp` set, the two rounding points of "What a Llama model
+ * computes, and why" §8 are added: ggml's F16 matrix products convert their
+ * F32 operand, so q is rounded to F16 before the q.k dots (K is F16) and each
+ * probability e_t/sum is rounded to F16 before it weights V (V is F16). */
+static float round_f16(float v) { return orc_f16_to_f32(orc_f32_to_f16(v)); }
+
+static void attention(float *out, const float *q, const float *kcache, const float *vcache,
+                      int n_heads, int n_kv_heads, int head_dim, int pos, int llamacpp) {
     int kv_dim = n_kv_heads * head_dim, group = n_heads / n_kv_heads;
     float *att = (float *)malloc(sizeof(float) * (size_t)(pos + 1));
+    float *qh = (float *)malloc(sizeof(float) * (size_t)head_dim);
     float sq = (float)sqrt((double)head_dim);
     for (int i = 0; i < n_heads * head_dim; i++) out[i] = 0.0f;
     for (int h = 0; h < n_heads; h++) {
         int kv_off = (h / group) * head_dim;
-        const float *qh = q + h * head_dim;
+        for (int i = 0; i < head_dim; i++) qh[i] = llamacpp ? round_f16(q[h * head_dim + i]) : q[h * head_dim + i];
         float mx = -INFINITY;
         for (int t = 0; t <= pos; t++) {
             const float *kt = kcache + (int64_t)t * kv_dim + kv_off;
@@ -186,11 +193,68 @@ void orc_attention(float *out, const float *q, const float *kcache, const float 
         float *oh = out + h * head_dim;
         for (int t = 0; t <= pos; t++) {
             float a = att[t] / sum;
+            if (llamacpp) a = round_f16(a);
             const float *vt = vcache + (int64_t)t * kv_dim + kv_off;
             for (int i = 0; i < head_dim; i++) { float p = a * vt[i]; oh[i] = oh[i] + p; }
         }
     }
+    free(qh);
     free(att);
+}
+
+void orc_attention(float *out, const float *q, const float *kcache, const float *vcache,
+                   int n_heads, int n_kv_heads, int head_dim, int pos) {
+    attention(out, q, kcache, vcache, n_heads, n_kv_heads, head_dim, pos, 0);
+}
+
+void orc_attention_llamacpp(float *out, const float *q, const float *kcache, const float *vcache,
+                            int n_heads, int n_kv_heads, int head_dim, int pos) {
+    attention(out, q, kcache, vcache, n_heads, n_kv_heads, head_dim, pos, 1);
+}
+
+/* ------------------------------------------- GEMV with llama.cpp rounding --
+ * "What a Llama model computes, and why" §8: ggml converts the activations of
+ * a matrix product to the weight's vector-dot format first.  F32 weights keep
+ * F32 activations (the plain product).  F16 weights get F16-rounded
+ * activations (round to nearest even); each product of two F16 values is
+ * exact in float, and the sum runs in float from i = 0.  Q8_0 weights get the
+ * activations quantized to Q8_0 blocks by the reference quantizer; block b of
+ * row r then contributes its integer dot sumi = sum_j qw[j]*qx[j] (exact in
+ * int) times d_w*d_x (a product of two F16 values, exact in float), so each
+ * block's term is its exact value rounded once to float; the terms are summed
+ * in float from block 0.  The pages fix the rounding points, not this order
+ * of the float operations: it is the plainest reading of "the integer dot". */
+void orc_matvec_llamacpp(float *out, const void *w, int wtype, const float *x, int rows, int cols) {
+    if (wtype == ORC_F32) {
+        orc_matvec(out, w, wtype, x, rows, cols);
+        return;
+    }
+    if (wtype == ORC_F16) {
+        float *xr = (float *)malloc(sizeof(float) * (size_t)cols);
+        for (int i = 0; i < cols; i++) xr[i] = round_f16(x[i]);
+        orc_matvec(out, w, wtype, xr, rows, cols);
+        free(xr);
+        return;
+    }
+    int nb = cols / 32;
+    uint8_t *xq = (uint8_t *)malloc((size_t)nb * 34);
+    orc_quantize_q8_0(x, cols, xq);
+    for (int r = 0; r < rows; r++) {
+        const uint8_t *wr = (const uint8_t *)w + (int64_t)r * nb * 34;
+        float s = 0.0f;
+        for (int b = 0; b < nb; b++) {
+            const uint8_t *wb = wr + (size_t)b * 34, *xb = xq + (size_t)b * 34;
+            int sumi = 0;
+            for (int j = 0; j < 32; j++) sumi += (int)(int8_t)wb[2 + j] * (int)(int8_t)xb[2 + j];
+            float dw = orc_f16_to_f32((uint16_t)(wb[0] | (wb[1] << 8)));
+            float dx = orc_f16_to_f32((uint16_t)(xb[0] | (xb[1] << 8)));
+            float dd = dw * dx;
+            float c = (float)sumi * dd;
+            s = s + c;
+        }
+        out[r] = s;
+    }
+    free(xq);
 }
 
 /* -------------------------------------------------------------- argmax --
@@ -268,6 +332,12 @@ static void trace(orc_model *m, const char *name, int layer, const float *v, int
     if (m->trace) m->trace(name, layer, v, n, m->trace_user);
 }
 
+/* Every matrix product of the pass, with or without the llama.cpp rounding. */
+static void mv(const orc_model *m, float *out, const void *w, const float *x, int rows, int cols) {
+    if (m->c.llamacpp_rounding) orc_matvec_llamacpp(out, w, m->c.wtype, x, rows, cols);
+    else orc_matvec(out, w, m->c.wtype, x, rows, cols);
+}
+
 static void add_bias(float *x, const float *b, int n) {
     if (b) for (int i = 0; i < n; i++) x[i] = x[i] + b[i];
 }
@@ -282,7 +352,10 @@ static float store(const orc_model *m, float v) {
  * position pos.  Embedding lookup; per layer RMSNorm, Q/K/V (+ biases),
  * RoPE on q and k, K/V stored at row pos, attention, output projection and
  * residual, RMSNorm, SwiGLU and residual; final RMSNorm and the logits
- * (output.weight or, when absent, token_embd.weight: Example 9). */
+ * (output.weight or, when absent, token_embd.weight: Example 9).  With
+ * llamacpp_rounding every matrix product and the attention round as
+ * llama.cpp does ("What a Llama model computes, and why" §8); the embedding
+ * row is decoded exactly either way. */
 int orc_forward(orc_model *m, int token, int pos, float *logits) {
     const orc_config *c = &m->c;
     if (token < 0 || token >= c->vocab || pos < 0 || pos >= c->max_seq) return -1;
@@ -302,9 +375,9 @@ int orc_forward(orc_model *m, int token, int pos, float *logits) {
         const orc_layer *L = &m->layers[l];
         orc_rmsnorm(xb, x, L->attn_norm, dim, c->eps);
         trace(m, "attn_norm", l, xb, dim);
-        orc_matvec(q, L->wq, c->wtype, xb, qdim, dim);
-        orc_matvec(k, L->wk, c->wtype, xb, kv_dim, dim);
-        orc_matvec(v, L->wv, c->wtype, xb, kv_dim, dim);
+        mv(m, q, L->wq, xb, qdim, dim);
+        mv(m, k, L->wk, xb, kv_dim, dim);
+        mv(m, v, L->wv, xb, kv_dim, dim);
         add_bias(q, L->bq, qdim);
         add_bias(k, L->bk, kv_dim);
         add_bias(v, L->bv, kv_dim);
@@ -318,28 +391,28 @@ int orc_forward(orc_model *m, int token, int pos, float *logits) {
             kc[(int64_t)pos * kv_dim + i] = store(m, k[i]);
             vc[(int64_t)pos * kv_dim + i] = store(m, v[i]);
         }
-        orc_attention(heads, q, kc, vc, c->n_heads, c->n_kv_heads, hd, pos);
+        attention(heads, q, kc, vc, c->n_heads, c->n_kv_heads, hd, pos, c->llamacpp_rounding);
         trace(m, "kqv_out", l, heads, qdim);
-        orc_matvec(xb, L->wo, c->wtype, heads, dim, qdim);
+        mv(m, xb, L->wo, heads, dim, qdim);
         trace(m, "attn_out", l, xb, dim);
         for (int i = 0; i < dim; i++) x[i] = x[i] + xb[i];
         trace(m, "ffn_inp", l, x, dim);
         orc_rmsnorm(xb, x, L->ffn_norm, dim, c->eps);
         trace(m, "ffn_norm", l, xb, dim);
-        orc_matvec(hb, L->w_gate, c->wtype, xb, c->ffn_dim, dim);
-        orc_matvec(hb2, L->w_up, c->wtype, xb, c->ffn_dim, dim);
+        mv(m, hb, L->w_gate, xb, c->ffn_dim, dim);
+        mv(m, hb2, L->w_up, xb, c->ffn_dim, dim);
         trace(m, "ffn_gate", l, hb, c->ffn_dim);
         trace(m, "ffn_up", l, hb2, c->ffn_dim);
         for (int i = 0; i < c->ffn_dim; i++) hb[i] = orc_silu(hb[i]) * hb2[i];
         trace(m, "ffn_swiglu", l, hb, c->ffn_dim);
-        orc_matvec(xb, L->w_down, c->wtype, hb, dim, c->ffn_dim);
+        mv(m, xb, L->w_down, hb, dim, c->ffn_dim);
         trace(m, "ffn_out", l, xb, dim);
         for (int i = 0; i < dim; i++) x[i] = x[i] + xb[i];
         trace(m, "l_out", l, x, dim);
     }
     orc_rmsnorm(xb, x, m->w.output_norm, dim, c->eps);
     trace(m, "result_norm", -1, xb, dim);
-    orc_matvec(logits, m->w.output ? m->w.output : m->w.tok_embd, c->wtype, xb, c->vocab, dim);
+    mv(m, logits, m->w.output ? m->w.output : m->w.tok_embd, xb, c->vocab, dim);
     trace(m, "result_output", -1, logits, c->vocab);
 
     free(x); free(xb); free(q); free(k); free(v); free(heads); free(hb); free(hb2);

@@ -19,6 +19,10 @@
  *   - Example 10: F16 KV cache (round to nearest even)
  *   - "What a Llama model computes, and why" §2.4: per-pair frequency factors
  *   - "What a Llama model computes, and why" §4: prefill equals token-by-token
+ *   - "What a Llama model computes, and why" §8 ("Where llama.cpp rounds"):
+ *     the optional llama.cpp rounding points (Q8_0 activations of a Q8_0
+ *     product, F16 activations of an F16 product, q and the softmax
+ *     probabilities rounded to F16 in attention)
  *
  * Arithmetic: F32 storage and F32 operations, left to right, no fused
  * multiply-add (compiled with -ffp-contract=off), double only where the pages
@@ -47,6 +51,8 @@ typedef struct {
     int rope_neox;   /* 0: pairs (2i, 2i+1); 1: pairs (i, i + rope_dims/2) */
     int wtype;       /* ORC_F32 / ORC_F16 / ORC_Q8_0 for every matrix incl. the embedding */
     int f16_cache;   /* 1: K/V rounded through F16 before storing (the pages' f16Cache flag) */
+    int llamacpp_rounding;  /* 1: round where llama.cpp's CPU path rounds (orc_matvec_llamacpp,
+                               orc_attention_llamacpp); 0: the Java engine's float arithmetic */
 } orc_config;
 
 /* Host pointers in GGUF layout: a [in -> out] matrix is `out` rows of `in`
@@ -101,6 +107,17 @@ float orc_silu(float z);
 void orc_attention(float *out, const float *q, const float *kcache, const float *vcache,
                    int n_heads, int n_kv_heads, int head_dim, int pos);
 int orc_argmax(const float *v, int n);
+
+/* ---- llama.cpp rounding points ("What a Llama model computes, and why" §8) ----
+ * orc_matvec_llamacpp: as orc_matvec, with the activations rounded as ggml
+ * rounds them for the weight type: unchanged for F32, rounded to F16 for F16,
+ * quantized to Q8_0 blocks (orc_quantize_q8_0) for Q8_0, whose product is
+ * then the integer dot of the two blocks' quants times both scales.
+ * orc_attention_llamacpp: as orc_attention, with q rounded to F16 before the
+ * q.k dots and each probability e_t/sum rounded to F16 before it weights V. */
+void orc_matvec_llamacpp(float *out, const void *w, int wtype, const float *x, int rows, int cols);
+void orc_attention_llamacpp(float *out, const float *q, const float *kcache, const float *vcache,
+                            int n_heads, int n_kv_heads, int head_dim, int pos);
 
 #ifdef __cplusplus
 }
