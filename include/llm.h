@@ -98,7 +98,8 @@ typedef struct llm_handle llm_handle;
  * FP16 scales; Q/K/V rows and gate/up rows fused), allocates the F16 KV cache
  * [n_layers][2][max_seq][n_kv_heads][head_dim] and the activations.  The
  * caller's weight buffers are only read during this call.  Synchronous.
- * Errors: INVALID_ARG, UNSUPPORTED, NO_MEMORY, CUDA; *out is set to NULL then. */
+ * Errors: INVALID_ARG, UNSUPPORTED, NO_MEMORY, CUDA; *out is set to NULL then,
+ * and llm_last_error(NULL) gives the reason. */
 int llm_create(const llm_config *cfg, const llm_weights *w, llm_stream_t stream, llm_handle **out);
 
 /* Starts a new sequence (P4 "The Engine": Attention.reset).  Logical only: the
@@ -207,6 +208,11 @@ int64_t llm_launch_count(const llm_handle *h);
 void llm_destroy(llm_handle *h);
 
 const char *llm_status_string(int status);
+/* The one-line reason of the handle's last failed call.  With h == NULL: the
+ * reason of the calling thread's last failed llm_create, "" after one that
+ * succeeded (llm_create_from_gguf reports through its `err` buffer).  The
+ * string stays valid until the next call on the handle (with NULL: until this
+ * thread's next llm_create). */
 const char *llm_last_error(const llm_handle *h);
 
 /* ------------------------------------------------------------ GGUF files --

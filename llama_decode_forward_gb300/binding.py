@@ -132,7 +132,9 @@ def _ptr(t):
 # ------------------------------------------------------ the C functions --
 def llm_create(cfg: llm_config, weights: llm_weights, stream=None):
     h = _vp()
-    _check(_lib.llm_create(ctypes.byref(cfg), ctypes.byref(weights), stream, ctypes.byref(h)))
+    rc = _lib.llm_create(ctypes.byref(cfg), ctypes.byref(weights), stream, ctypes.byref(h))
+    if rc != LLM_OK:
+        raise LlmError(rc, _lib.llm_last_error(None).decode())     # this thread's failed create
     return h.value
 
 

@@ -669,7 +669,7 @@ extern "C" int llm_create_from_gguf(const llm_gguf* g, int32_t max_seq, llm_stre
     w.rope_freqs = static_cast<const float*>(dev("rope_freqs.weight"));
     w.layers = lw.data();
     rc = llm_create(&cfg, &w, stream, out);
-    if (rc != LLM_OK) put_err(err, err_len, "llm_create: %s", llm_status_string(rc));
+    if (rc != LLM_OK) put_err(err, err_len, "llm_create: %s", llm_last_error(nullptr));
     // llm_create copies every tensor into the handle's own layout before it returns
     cudaStreamSynchronize(st);
     cudaFree(stage);

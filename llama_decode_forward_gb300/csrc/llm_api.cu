@@ -223,37 +223,51 @@ static void free_handle(llm_handle* h) {
     delete h;
 }
 
+// Reason of the calling thread's last failed llm_create: there is no handle
+// to hold it then, so llm_last_error(NULL) returns it.
+static thread_local std::string t_create_error;
+
+// A failed llm_create: keep the handle's reason for llm_last_error(NULL) and
+// release what was allocated so far.
+static int create_failed(llm_handle* h, int rc) {
+    t_create_error = h->last_error.empty() ? llm_status_string(rc) : h->last_error;
+    free_handle(h);
+    return rc;
+}
+
 // ------------------------------------------------------------------ ABI --
 extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_stream_t stream, llm_handle** out) {
     if (!out) return LLM_ERR_INVALID_ARG;
     *out = nullptr;
     llm_handle* h = new llm_handle();
     int rc = validate(cfg, w, h);
-    if (rc) { delete h; return rc; }
+    if (rc) {
+        t_create_error = h->last_error;
+        delete h;                          // nothing allocated yet: no CUDA call
+        return rc;
+    }
     const llm_config& c = *cfg;
     h->cfg = c;
     h->st = (cudaStream_t)stream;
     h->q_dim = c.n_heads * c.head_dim;
     h->kv_dim = c.n_kv_heads * c.head_dim;
-#define CKC(call)                                \
-    do {                                         \
-        cudaError_t e_ = (call);                 \
-        if (e_ != cudaSuccess) {                 \
-            cudaGetLastError();                  \
-            free_handle(h);                      \
-            return e_ == cudaErrorMemoryAllocation ? LLM_ERR_NO_MEMORY : LLM_ERR_CUDA; \
-        }                                        \
+#define CKC(call)                                                                                      \
+    do {                                                                                               \
+        cudaError_t e_ = (call);                                                                       \
+        if (e_ != cudaSuccess) {                                                                       \
+            cudaGetLastError();                                                                        \
+            return create_failed(h, fail(h, e_ == cudaErrorMemoryAllocation ? LLM_ERR_NO_MEMORY : LLM_ERR_CUDA, \
+                                         "%s: %s", #call, cudaGetErrorString(e_)));                    \
+        }                                                                                              \
     } while (0)
     CKC(cudaGetDevice(&h->device));
     CKC(cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device));
     int coop = 0;
     CKC(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device));
-    if (!coop) { free_handle(h); return LLM_ERR_UNSUPPORTED; }
+    if (!coop) return create_failed(h, fail(h, LLM_ERR_UNSUPPORTED, "the device has no cooperative launch"));
 
     // ---- weight arena
     const int L = c.n_layers, d = c.dim, q = h->q_dim, kv = h->kv_dim, f = c.ffn_dim;
-    const bool has_bias = false;
-    (void)has_bias;
     size_t bytes = 0;
     for (int l = 0; l < L; l++) {
         bytes += align256(mat_bytes(c.wtype, q + 2 * kv, d)) + 256 * 2;
@@ -289,10 +303,8 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
             (rc = put_matrix(h, W.wo, d, q, D.o, 0, 1, 0)) ||
             (rc = put_matrix(h, W.w_gate, f, d, D.gu, 0, 2, 0)) ||
             (rc = put_matrix(h, W.w_up, f, d, D.gu, 0, 2, 1)) ||
-            (rc = put_matrix(h, W.w_down, d, f, D.down, 0, 1, 0))) {
-            free_handle(h);
-            return rc;
-        }
+            (rc = put_matrix(h, W.w_down, d, f, D.down, 0, 1, 0)))
+            return create_failed(h, rc);
         CKC(cudaMemcpyAsync(an, W.attn_norm, (size_t)d * 4, cudaMemcpyDeviceToDevice, h->st));
         CKC(cudaMemcpyAsync(fn, W.ffn_norm, (size_t)d * 4, cudaMemcpyDeviceToDevice, h->st));
         if (D.qkv_bias) {
@@ -303,10 +315,10 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
         }
     }
     h->embd = carve_mat(h, off, c.vocab, d);
-    if ((rc = put_matrix(h, w->tok_embd, c.vocab, d, h->embd, 0, 1, 0))) { free_handle(h); return rc; }
+    if ((rc = put_matrix(h, w->tok_embd, c.vocab, d, h->embd, 0, 1, 0))) return create_failed(h, rc);
     if (w->output) {
         h->out = carve_mat(h, off, c.vocab, d);
-        if ((rc = put_matrix(h, w->output, c.vocab, d, h->out, 0, 1, 0))) { free_handle(h); return rc; }
+        if ((rc = put_matrix(h, w->output, c.vocab, d, h->out, 0, 1, 0))) return create_failed(h, rc);
     } else {
         h->out = h->embd;                                      // tied embeddings
     }
@@ -376,25 +388,23 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
         }
     }
     if (!step_geometry(h->geo, d, q, f, c.n_heads, c.n_kv_heads, c.head_dim, c.rope_dims, rowp_floats,
-                       &h->smem)) {
-        free_handle(h);
-        return LLM_ERR_UNSUPPORTED;
-    }
+                       &h->smem))
+        return create_failed(h, fail(h, LLM_ERR_UNSUPPORTED, "the step's shared-memory layout does not fit"));
     // per-CTA shares that live in shared memory, and every matrix's plan
     if ((d + h->sms - 1) / h->sms > kOwnFloats || (q + 2 * kv + h->sms - 1) / h->sms > kOwnFloats ||
-        2 * ((f + h->sms - 1) / h->sms) > kOwnFloats) {
-        free_handle(h);
-        return LLM_ERR_UNSUPPORTED;
-    }
+        2 * ((f + h->sms - 1) / h->sms) > kOwnFloats)
+        return create_failed(h, fail(h, LLM_ERR_UNSUPPORTED, "a CTA's share of a vector exceeds %d floats", kOwnFloats));
     for (int l = 0; l < L; l++) {
         const LayerDev& D = h->layers[l];
-        if (!D.qkv.rpc || !D.o.rpc || !D.gu.rpc || !D.down.rpc) { free_handle(h); return LLM_ERR_UNSUPPORTED; }
+        if (!D.qkv.rpc || !D.o.rpc || !D.gu.rpc || !D.down.rpc)
+            return create_failed(h, fail(h, LLM_ERR_UNSUPPORTED, "layer %d: no streaming plan for a matrix", l));
     }
-    if (!h->embd.rpc || !h->out.rpc) { free_handle(h); return LLM_ERR_UNSUPPORTED; }
+    if (!h->embd.rpc || !h->out.rpc)
+        return create_failed(h, fail(h, LLM_ERR_UNSUPPORTED, "no streaming plan for the vocabulary matrix"));
     CKC(cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem));
     int per_sm = 0;
     CKC(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->kernel, kBlock, h->smem));
-    if (per_sm < 1) { free_handle(h); return LLM_ERR_UNSUPPORTED; }
+    if (per_sm < 1) return create_failed(h, fail(h, LLM_ERR_UNSUPPORTED, "the step kernel cannot be resident"));
 
     // 2-D tensor maps of every layer's K and V cache: [max_seq][kv_dim] F16,
     // box [attn_rows][attn_w], read by the step kernel's TMA tile loads; the
@@ -404,7 +414,8 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q_res;
         CKC(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q_res));
-        if (!fn || q_res != cudaDriverEntryPointSuccess) { free_handle(h); return LLM_ERR_CUDA; }
+        if (!fn || q_res != cudaDriverEntryPointSuccess)
+            return create_failed(h, fail(h, LLM_ERR_CUDA, "cuTensorMapEncodeTiled is not available"));
         auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         std::vector<CUtensorMap> maps((size_t)2 * L);
         for (int l = 0; l < L; l++)
@@ -423,13 +434,16 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
                 CUresult r = encode(&maps[(size_t)2 * l + which], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, gdim,
                                     gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-                if (r != CUDA_SUCCESS) { free_handle(h); return LLM_ERR_CUDA; }
+                if (r != CUDA_SUCCESS)
+                    return create_failed(h, fail(h, LLM_ERR_CUDA, "cuTensorMapEncodeTiled of layer %d: error %d", l,
+                                                 (int)r));
             }
         CKC(cudaMalloc(&h->kv_maps, sizeof(CUtensorMap) * maps.size()));
         CKC(cudaMemcpyAsync(h->kv_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice,
                             h->st));
     }
     CKC(cudaStreamSynchronize(h->st));
+    t_create_error.clear();
     *out = h;
     return LLM_OK;
 #undef CKC
@@ -607,8 +621,6 @@ extern "C" int llm_test_dequant_rows(llm_handle* h, int which, int layer, int32_
     const llm_config& c = h->cfg;
     DMat m{};
     int first = 0, mul = 1, phase = 0, rows = 0;
-    const int nb_bytes = 1;
-    (void)nb_bytes;
     switch (which) {
         case 0: m = h->layers[layer].qkv; first = 0; rows = h->q_dim; break;
         case 1: m = h->layers[layer].qkv; first = h->q_dim; rows = h->kv_dim; break;
@@ -658,7 +670,7 @@ extern "C" const char* llm_status_string(int s) {
     }
 }
 
-extern "C" const char* llm_last_error(const llm_handle* h) { return h ? h->last_error.c_str() : ""; }
+extern "C" const char* llm_last_error(const llm_handle* h) { return h ? h->last_error.c_str() : t_create_error.c_str(); }
 
 // ------------------------------------------------------- no-alloc step --
 // A decode step whose working memory (residual stream, q/k/v, attention

@@ -73,6 +73,25 @@ def test_create_rejects_null_weight():
     assert e.value.status == L.LLM_ERR_INVALID_ARG
 
 
+def test_create_failure_reason_without_a_handle():
+    # no handle exists after a failed create: llm_last_error(NULL) holds the
+    # calling thread's reason, and the Python error carries it
+    with pytest.raises(L.LlmError) as e:
+        L.llm_create(_cfg(rope_dims=15), _weights())
+    assert "rope_dims must be even" in str(e.value)
+    assert "rope_dims must be even" in L.llm_last_error(None)
+    with pytest.raises(L.LlmError) as e:
+        L.llm_create(_cfg(), _weights(null_field="wq"))
+    assert L.llm_last_error(None) == "layer 0: a weight pointer is NULL"
+    # another thread has its own reason
+    import threading
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(L.llm_last_error(None)))
+    t.start()
+    t.join()
+    assert seen == [""]
+
+
 def test_create_without_gpu_fails_loudly():
     try:
         import torch
