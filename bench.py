@@ -140,6 +140,26 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ------------------------------------------------------------ ranks --
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x: the job lasts as long as its slowest
+    rank.  One all-reduce on the process group (NCCL on the GPU machine, gloo in
+    the CPU tests)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, seconds: float) -> float:
+    """Tokens per second of the whole job: each of the `world` ranks decodes
+    `steps` tokens of its own replica, and `seconds` is the slowest rank's time."""
+    return world * steps / seconds
+
+
 # --------------------------------------------------------- CPU baseline --
 def cpu_oracle_sample(W, tok: int, budget_s: float = 12.0, min_steps: int = 1, max_steps: int | None = None):
     """The oracle (single thread) on the same workload: decode steps at pos
@@ -246,11 +266,8 @@ def run_ours(args):
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * args.steps / (total_ms / 1000.0)
+    total_ms = max_over_ranks(total_ms, world, "cuda")
+    value = job_throughput(world, args.steps, total_ms / 1000.0)
 
     # end to end through the synchronous C-ABI call, pinned host buffers
     logits_pin = torch.empty(CFG.vocab, dtype=torch.float32, pin_memory=True)
@@ -263,11 +280,8 @@ def run_ours(args):
     for _ in range(args.steps):
         L.llm_decode_step(dec.h, tok, POS, logits_np)
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = world * args.steps / e2e_s
+    e2e_s = max_over_ranks(e2e_s, world, "cuda")
+    e2e = job_throughput(world, args.steps, e2e_s)
 
     nbytes = algorithmic_bytes(CFG, POS)
     kern_ms = statistics.mean(per_launch)
