@@ -59,6 +59,8 @@ def _lib():
             lib.syn_normal_f16.argtypes = [u64, u64, i64, dbl, dbl, vp]
             lib.syn_uniform_i32.argtypes = [u64, u64, i64, ctypes.c_int32, ctypes.c_int32, vp]
             lib.syn_q8_0.argtypes = [u64, u64, i64, dbl, vp]
+            lib.syn_splitmix64_at.argtypes = [u64, u64]
+            lib.syn_splitmix64_at.restype = u64
             lib.syn_draw.argtypes = [u64, u64, u64]
             lib.syn_draw.restype = u64
             lib.syn_normal_at.argtypes = [u64, u64, u64]
@@ -251,3 +253,13 @@ def kv_rows(cfg: ModelConfig, layer: int, which: int, n_rows: int, seed: int | N
 
 def draw(seed: int, stream: int, i: int) -> int:
     return int(_lib().syn_draw(seed, stream, i))
+
+
+def splitmix64_at(state: int, i: int) -> int:
+    """Value i of the SplitMix64 sequence whose state starts at ``state``."""
+    return int(_lib().syn_splitmix64_at(state, i))
+
+
+def normal_at(seed: int, stream: int, i: int) -> float:
+    """Normal i of a stream (float64, before any rounding to the stored type)."""
+    return float(_lib().syn_normal_at(seed, stream, i))

@@ -44,6 +44,11 @@ static inline uint16_t to_f16_bits(float v) {
     return b;
 }
 
+/* Value i of the SplitMix64 sequence whose state starts at `state` (the
+ * published generator itself, so that it can be checked against its
+ * reference outputs); value i of stream s under seed k is this sequence at
+ * state key(k, s). */
+uint64_t syn_splitmix64_at(uint64_t state, uint64_t i) { return draw(state, i); }
 uint64_t syn_draw(uint64_t seed, uint64_t stream, uint64_t i) { return draw(key_of(seed, stream), i); }
 double syn_normal_at(uint64_t seed, uint64_t stream, uint64_t i) { return normal_at(key_of(seed, stream), i); }
 
