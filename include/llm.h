@@ -150,6 +150,11 @@ int llm_sync(llm_handle *h);
  * the next step on the handle and the handle's destruction. */
 const float *llm_logits_device(const llm_handle *h);
 
+/* The handle's model shape (the llm_config it was created with; for a handle
+ * from llm_create_from_gguf, the shape read from the file), copied to *out.
+ * Host only, no device work.  Errors: INVALID_ARG (NULL). */
+int llm_get_config(const llm_handle *h, llm_config *out);
+
 /* Test hook: DEVICE pointers to layer `layer`'s K and V cache,
  * [max_seq][n_kv_heads][head_dim] FP16 each ("The Forward Pass in Java",
  * Example 7: element pos*kv_dim + kv_head*head_dim + i).  Writable, so a

@@ -59,6 +59,7 @@ _SIGS = {
     "llm_prefill": ([_vp, _vp, _i32, _i32, _vp, _vp], _int),
     "llm_sync": ([_vp], _int),
     "llm_logits_device": ([_vp], _vp),
+    "llm_get_config": ([_vp, ctypes.POINTER(llm_config)], _int),
     "llm_kv_view": ([_vp, _int, ctypes.POINTER(_vp), ctypes.POINTER(_vp)], _int),
     "llm_test_kv_store": ([_vp, _int, _i32, _vp, _vp], _int),
     "llm_test_dequant_rows": ([_vp, _int, _int, _i32, _i32, _vp], _int),
@@ -142,10 +143,28 @@ def llm_reset(h):
     _check(_lib.llm_reset(h), h)
 
 
+def llm_get_config(h) -> llm_config:
+    c = llm_config()
+    _check(_lib.llm_get_config(h, ctypes.byref(c)), h)
+    return c
+
+
+def _check_logits_buffer(h, logits_host):
+    """The C call writes vocab floats to logits_host: refuse a buffer that
+    cannot hold them instead of letting the library write past its end."""
+    if logits_host is None:
+        return
+    if not isinstance(logits_host, np.ndarray) or logits_host.dtype != np.float32 or \
+            not logits_host.flags.c_contiguous or not logits_host.flags.writeable:
+        raise TypeError("logits_host must be a writable C-contiguous float32 numpy array")
+    vocab = llm_get_config(h).vocab
+    if logits_host.size < vocab:
+        raise ValueError(f"logits_host holds {logits_host.size} floats; the model's vocab is {vocab}")
+
+
 def llm_decode_step(h, token: int, pos: int, logits_host: np.ndarray | None = None) -> int:
     out = ctypes.c_int32(0)
-    if logits_host is not None:
-        assert logits_host.dtype == np.float32 and logits_host.flags.c_contiguous
+    _check_logits_buffer(h, logits_host)
     _check(_lib.llm_decode_step(h, int(token), int(pos), _ptr(logits_host), ctypes.addressof(out)), h)
     return out.value
 
@@ -161,6 +180,7 @@ def llm_generate(h, token: int, pos: int, n_steps: int, tokens_dev):
 def llm_prefill(h, tokens_host, pos0: int, logits_host: np.ndarray | None = None) -> int:
     t = np.ascontiguousarray(tokens_host, dtype=np.int32)
     out = ctypes.c_int32(0)
+    _check_logits_buffer(h, logits_host)
     _check(_lib.llm_prefill(h, t.ctypes.data, t.size, int(pos0), _ptr(logits_host), ctypes.addressof(out)), h)
     return out.value
 

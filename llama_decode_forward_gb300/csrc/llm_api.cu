@@ -596,6 +596,12 @@ extern "C" int llm_sync(llm_handle* h) {
 
 extern "C" const float* llm_logits_device(const llm_handle* h) { return h ? h->logits : nullptr; }
 
+extern "C" int llm_get_config(const llm_handle* h, llm_config* out) {
+    if (!h || !out) return LLM_ERR_INVALID_ARG;
+    *out = h->cfg;
+    return LLM_OK;
+}
+
 extern "C" int llm_kv_view(llm_handle* h, int layer, uint16_t** k_dev, uint16_t** v_dev) {
     if (!h || !k_dev || !v_dev) return LLM_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.n_layers) return fail(h, LLM_ERR_OUT_OF_RANGE, "layer %d", layer);

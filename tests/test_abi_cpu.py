@@ -109,4 +109,5 @@ def test_null_handle_calls_are_rejected():
     assert L.binding._lib.llm_sync(None) == L.LLM_ERR_INVALID_ARG
     assert L.binding._lib.llm_decode_step(None, 0, 0, None, None) == L.LLM_ERR_INVALID_ARG
     assert L.binding._lib.llm_launch_count(None) == 0
+    assert L.binding._lib.llm_get_config(None, None) == L.LLM_ERR_INVALID_ARG
     L.binding._lib.llm_destroy(None)

@@ -146,6 +146,14 @@ def test_decode_step_edge_tokens_and_errors(lib):
         with pytest.raises(lib.LlmError) as e:
             lib.llm_decode_step(dec.h, tok, pos)
         assert e.value.status == lib.LLM_ERR_OUT_OF_RANGE
+    # the handle's shape; host buffers that cannot take vocab floats are refused before the call
+    c = lib.llm_get_config(dec.h)
+    assert (c.n_layers, c.dim, c.vocab, c.max_seq, c.wtype) == (cfg.n_layers, cfg.dim, cfg.vocab, cfg.max_seq,
+                                                               cfg.wtype)
+    with pytest.raises(ValueError):
+        lib.llm_decode_step(dec.h, 3, 2, np.empty(cfg.vocab - 1, np.float32))
+    with pytest.raises(TypeError):
+        lib.llm_decode_step(dec.h, 3, 2, np.empty(cfg.vocab, np.float64))
 
 
 def test_device_side_bad_token_is_reported(lib):
