@@ -20,6 +20,10 @@
 
 #include "../../include/llm.h"
 
+namespace llm {
+int check_shape(const llm_config* c, std::string* why);   // llm_api.cu: llm_create's shape checks
+}
+
 namespace {
 
 constexpr uint32_t kMagic = 0x46554747;        // "GGUF" read as a little-endian uint32 (Example 1)
@@ -564,6 +568,15 @@ extern "C" int llm_create_from_gguf(const llm_gguf* g, int32_t max_seq, llm_stre
     llm_config cfg;
     int rc = llm_gguf_config(g, max_seq, &cfg, err, err_len);
     if (rc != LLM_OK) return rc;
+    {
+        // a shape the kernels cannot run is rejected before any tensor is staged on the device
+        std::string why;
+        rc = llm::check_shape(&cfg, &why);
+        if (rc != LLM_OK) {
+            put_err(err, err_len, "llm_create: %s", why.c_str());
+            return rc;
+        }
+    }
     const int wt = cfg.wtype;
     const int64_t q_dim = (int64_t)cfg.n_heads * cfg.head_dim, kv_dim = (int64_t)cfg.n_kv_heads * cfg.head_dim;
     struct Need {

@@ -171,8 +171,9 @@ static DMat carve_mat(llm_handle* h, size_t& off, int rows, int cols, bool pair 
     return m;
 }
 
-static int validate(const llm_config* c, const llm_weights* w, llm_handle* h) {
-    if (!c || !w) return fail(h, LLM_ERR_INVALID_ARG, "config or weights is NULL");
+// The model shape alone: what the kernels support (no weight pointers).
+static int validate_config(const llm_config* c, llm_handle* h) {
+    if (!c) return fail(h, LLM_ERR_INVALID_ARG, "config is NULL");
     if (c->n_layers <= 0 || c->dim <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
         c->ffn_dim <= 0 || c->vocab <= 0 || c->max_seq <= 0)
         return fail(h, LLM_ERR_INVALID_ARG, "every size must be positive");
@@ -199,6 +200,13 @@ static int validate(const llm_config* c, const llm_weights* w, llm_handle* h) {
     if ((long long)slot_row_bytes(c->wtype, c->ffn_dim, scale_stride(c->ffn_dim)) > kSlotBytes ||
         (long long)slot_row_bytes(c->wtype, c->dim, scale_stride(c->dim)) > kSlotBytes)
         return fail(h, LLM_ERR_UNSUPPORTED, "matrix rows too long for the streaming ring");
+    return LLM_OK;
+}
+
+static int validate(const llm_config* c, const llm_weights* w, llm_handle* h) {
+    if (!c || !w) return fail(h, LLM_ERR_INVALID_ARG, "config or weights is NULL");
+    const int rc = validate_config(c, h);
+    if (rc) return rc;
     if (!w->tok_embd || !w->output_norm || !w->layers) return fail(h, LLM_ERR_INVALID_ARG, "a weight pointer is NULL");
     for (int l = 0; l < c->n_layers; l++) {
         const llm_layer_weights& L = w->layers[l];
@@ -222,6 +230,17 @@ static void free_handle(llm_handle* h) {
     cudaGetLastError();
     delete h;
 }
+
+namespace llm {
+// The shape checks of llm_create, for callers that want them before moving
+// any weights (llm_create_from_gguf): LLM_OK, or a status and *why.
+int check_shape(const llm_config* c, std::string* why) {
+    llm_handle tmp;
+    const int rc = validate_config(c, &tmp);
+    if (why) *why = tmp.last_error;
+    return rc;
+}
+}  // namespace llm
 
 // Reason of the calling thread's last failed llm_create: there is no handle
 // to hold it then, so llm_last_error(NULL) returns it.

@@ -167,6 +167,22 @@ def test_rejected_models(lib, tmp_path):
     assert info["bytes"] > 0
 
 
+def test_unsupported_shape_is_rejected_before_staging(lib, tmp_path):
+    # a well-formed file whose shape the kernels cannot run (head_dim 320):
+    # rejected with llm_create's reason before any tensor reaches the device,
+    # so the same answer comes back on a machine without a GPU
+    cfg = synth.ModelConfig("g-hd320", n_layers=1, dim=1280, n_heads=4, n_kv_heads=4, head_dim=320, ffn_dim=64,
+                            vocab=40, max_seq=16, eps=1e-5, rope_base=10000.0, rope_neox=0, wtype=synth.F32,
+                            tied=True, number=84)
+    data = W.model_file(cfg, synth.make_weights(cfg))
+    with lib.GgufFile(_save(tmp_path, "m.gguf", data)) as g:
+        assert g.config().head_dim == 320
+        with pytest.raises(lib.LlmError) as e:
+            lib.llm_create_from_gguf(g)
+    assert e.value.status == lib.LLM_ERR_UNSUPPORTED
+    assert "head_dim must be a multiple of 8, <= 256" in str(e.value)
+
+
 def test_truncations_are_rejected_not_read(lib, tmp_path):
     # every prefix of a valid file is either rejected with a reason or (only
     # the whole file) accepted: no read past the end
