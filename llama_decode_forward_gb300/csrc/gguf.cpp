@@ -577,6 +577,14 @@ extern "C" int llm_create_from_gguf(const llm_gguf* g, int32_t max_seq, llm_stre
             return rc;
         }
     }
+    // every block needs 9 tensors (norms, q/k/v/o, gate/up/down) and the model
+    // 2 more: a block count the file's tensors cannot back is refused before
+    // the list of wanted tensors is built
+    if ((int64_t)cfg.n_layers * 9 + 2 > (int64_t)g->tensors.size()) {
+        put_err(err, err_len, "block_count %d needs at least %lld tensors; the file has %zu", cfg.n_layers,
+                (long long)cfg.n_layers * 9 + 2, g->tensors.size());
+        return LLM_ERR_INVALID_ARG;
+    }
     const int wt = cfg.wtype;
     const int64_t q_dim = (int64_t)cfg.n_heads * cfg.head_dim, kv_dim = (int64_t)cfg.n_kv_heads * cfg.head_dim;
     struct Need {

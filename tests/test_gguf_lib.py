@@ -183,6 +183,22 @@ def test_unsupported_shape_is_rejected_before_staging(lib, tmp_path):
     assert "head_dim must be a multiple of 8, <= 256" in str(e.value)
 
 
+def test_block_count_beyond_the_tensors_is_refused(lib, tmp_path):
+    # a 2-block model whose metadata claims a million blocks: refused from the
+    # tensor count, before any per-block work
+    cfg = SMALL[0]
+    data = W.model_file(cfg, synth.make_weights(cfg))
+    g0 = G.read(data)
+    md = [(k, t, 1_000_000 if k == "llama.block_count" else v) for k, (t, v) in g0["metadata"].items()]
+    tens = [(t["name"], t["type"], t["dims"], data[t["file_offset"]:t["file_offset"] + t["bytes"]])
+            for t in g0["tensors"]]
+    with lib.GgufFile(_save(tmp_path, "m.gguf", W.write(md, tens))) as g:
+        assert g.config().n_layers == 1_000_000
+        with pytest.raises(lib.LlmError) as e:
+            lib.llm_create_from_gguf(g)
+    assert e.value.status == lib.LLM_ERR_INVALID_ARG and "block_count 1000000" in str(e.value)
+
+
 def test_truncations_are_rejected_not_read(lib, tmp_path):
     # every prefix of a valid file is either rejected with a reason or (only
     # the whole file) accepted: no read past the end
