@@ -48,7 +48,10 @@ typedef enum {
     LLM_ERR_CUDA = -4,            /* a CUDA runtime call failed; llm_last_error has its message */
     LLM_ERR_NO_MEMORY = -5,       /* device allocation failed */
     LLM_ERR_DEVICE_TIMEOUT = -6,  /* a bounded wait inside a kernel gave up; the step's outputs are invalid */
-    LLM_ERR_STATE = -7            /* call not valid in the handle's state (e.g. after a device error) */
+    LLM_ERR_STATE = -7,           /* call not valid in the handle's state (e.g. after a device error) */
+    LLM_ERR_NONFINITE = -8        /* a residual-stream update was NaN, infinite or not below 2^15 in
+                                     magnitude (the decode step's fixed-point accumulators); the step's
+                                     outputs are invalid and the handle needs llm_reset */
 } llm_status;
 
 /* Model shape ("The Forward Pass in Java", Example 1, Config record).

@@ -17,7 +17,7 @@ from . import build as _build
 LLM_F32, LLM_F16, LLM_Q8_0 = 0, 1, 8
 LLM_OK = 0
 LLM_ERR_INVALID_ARG, LLM_ERR_UNSUPPORTED, LLM_ERR_OUT_OF_RANGE = -1, -2, -3
-LLM_ERR_CUDA, LLM_ERR_NO_MEMORY, LLM_ERR_DEVICE_TIMEOUT, LLM_ERR_STATE = -4, -5, -6, -7
+LLM_ERR_CUDA, LLM_ERR_NO_MEMORY, LLM_ERR_DEVICE_TIMEOUT, LLM_ERR_STATE, LLM_ERR_NONFINITE = -4, -5, -6, -7, -8
 
 
 class llm_config(ctypes.Structure):

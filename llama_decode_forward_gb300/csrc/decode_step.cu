@@ -3,34 +3,44 @@
 // One CTA per SM (cooperative launch, so all CTAs are resident).  Warps 0-14
 // compute ("consumers"); warp 15 ("producer") streams everything the CTA will
 // read from HBM (its rows of every weight matrix and its KV-cache tiles) in a
-// fixed order through a ring of 32 KB shared-memory slots, with cp.async.bulk
-// (weights) and 2-D TMA tiles (K/V), completing on mbarriers.  The producer
-// never waits on other CTAs: nothing it loads depends on this step's results
-// (KV row `pos`, which does, is patched in by the consumers), so HBM keeps
-// streaming while the consumers wait at the grid-wide phase counters.
+// fixed order through a ring of 64 KB shared-memory slots, with cp.async.bulk
+// (whole weight rows) and TMA tensor tiles (KV tiles, column blocks of Wo and
+// Wdown), completing on mbarriers.  The producer never waits on other CTAs:
+// nothing it loads depends on this step's results (KV row `pos`, which does,
+// is patched in by the consumers), so HBM keeps streaming while the consumers
+// wait for their inputs.
+//
+// The grid is split into `ngrp` column groups of CTAs (group g holds the kv
+// heads [g*n_kv/ngrp, (g+1)*n_kv/ngrp) and the matching columns of Wo, and
+// one ngrp-th of the FFN columns):
 //
 //   per layer l:  QKV   rows of [Wq;Wk;Wv] . RMSNorm(x)        -> qkv (+ bias)
 //                 ATTN  (kv head, position split) units: RoPE(q), RoPE(k),
-//                       K/V row `pos` stored as F16, partial softmax (m, l, acc);
-//                       the last split of a kv head merges the partials -> attn
-//                 O     rows of Wo . attn                       -> x += ...
+//                       K/V row `pos` stored as F16, partial softmax (m, l, acc)
+//                 O     every CTA of group g merges the partials of its heads
+//                       and multiplies them by its rows of g's columns of Wo
+//                       -> adds to the residual accumulator (one word per row)
 //                 GU    rows of [Wgate|Wup] . RMSNorm(x)        -> u = silu(gate) * up
-//                 DOWN  rows of Wdown . u                       -> x += ...
+//                       (group g computes its ffn/ngrp columns of u)
+//                 DOWN  every CTA of group g multiplies g's part of u by its
+//                       rows of g's columns of Wdown -> adds to the residual
 //   LOGITS  rows of Wout . RMSNorm(x) -> logits, argmax (first index of the max)
 //
 // Steps follow "The Forward Pass in Java", Example 13 (Llama.forward).  The
 // attention split and merge is the flash-decoding rearrangement of the same
-// softmax (max-subtracted partial sums combined with exp(m_s - M) weights).
+// softmax (max-subtracted partial sums combined with exp(m_s - M) weights);
+// splitting the O and down products by column groups only regroups their sums.
 //
 // A matrix row is reduced by a "team" of lanes, each holding 32 elements of
-// the activation vector in registers (loaded straight from L2 at the start of
-// the phase, normalised in registers); rows up to 1024 elements are part of a
-// warp, longer rows whole warps that meet at their own named barrier and take
-// two rows per pass.  Each CTA keeps the residual-stream rows it owns in
-// shared memory, so no phase reads back what it wrote.
+// the activation vector in registers; rows up to 1024 elements are part of a
+// warp, longer rows whole warps that take four rows per pass.  Every CTA keeps
+// the whole residual stream in shared memory and adds each layer's two
+// accumulated updates to it in the same order, so all CTAs hold the same bits.
 //
 // Every wait is bounded; on expiry the error word is set, the producer drains
 // its copies in flight, and the CTA exits.
+#include <algorithm>
+
 #include "llm_internal.cuh"
 
 namespace llm {
@@ -65,20 +75,32 @@ __device__ __forceinline__ bool bounded_wait(Ready ready, int* err) {
     }
 }
 
+__device__ __forceinline__ bool tagged2_ready(const ulonglong2& w, unsigned tag) {
+    return ((unsigned)(w.x >> 32) == tag) & ((unsigned)(w.y >> 32) == tag);
+}
+
 // Tagged elements once they carry `tag` (the step's): four consecutive ones
-// (16-byte aligned), or one.  After a timeout (the error word is set) the
-// values read as zero; every later wait of the step then gives up at once.
+// (16-byte aligned), two, or one.  After a timeout (the error word is set)
+// the values read as zero; every later wait of the step then gives up at once.
 __device__ __forceinline__ float4 poll4(const unsigned long long* a, unsigned tag, int* err) {
     ulonglong2 w0, w1;
     const auto ready = [&] {
         w0 = ld_tagged2(a);
         w1 = ld_tagged2(a + 2);
-        return ((unsigned)(w0.x >> 32) == tag) & ((unsigned)(w0.y >> 32) == tag) & ((unsigned)(w1.x >> 32) == tag) &
-               ((unsigned)(w1.y >> 32) == tag);
+        return tagged2_ready(w0, tag) & tagged2_ready(w1, tag);
     };
     if (!bounded_wait(ready, err)) return make_float4(0.f, 0.f, 0.f, 0.f);
     return make_float4(__uint_as_float((unsigned)w0.x), __uint_as_float((unsigned)w0.y),
                        __uint_as_float((unsigned)w1.x), __uint_as_float((unsigned)w1.y));
+}
+__device__ __forceinline__ float2 poll2(const unsigned long long* a, unsigned tag, int* err) {
+    ulonglong2 w;
+    const auto ready = [&] {
+        w = ld_tagged2(a);
+        return tagged2_ready(w, tag);
+    };
+    if (!bounded_wait(ready, err)) return make_float2(0.f, 0.f);
+    return make_float2(__uint_as_float((unsigned)w.x), __uint_as_float((unsigned)w.y));
 }
 __device__ __forceinline__ float poll1(const unsigned long long* a, unsigned tag, int* err) {
     unsigned long long w;
@@ -88,6 +110,19 @@ __device__ __forceinline__ float poll1(const unsigned long long* a, unsigned tag
     };
     if (!bounded_wait(ready, err)) return 0.f;
     return __uint_as_float((unsigned)w);
+}
+
+// Four residual-accumulator words (16-byte aligned) once `n` groups have
+// added to each: their sums, as floats.
+__device__ __forceinline__ float4 poll_acc4(const unsigned long long* a, unsigned n, int* err) {
+    ulonglong2 w0, w1;
+    const auto ready = [&] {
+        w0 = ld_tagged2(a);
+        w1 = ld_tagged2(a + 2);
+        return (acc_count(w0.x) == n) & (acc_count(w0.y) == n) & (acc_count(w1.x) == n) & (acc_count(w1.y) == n);
+    };
+    if (!bounded_wait(ready, err)) return make_float4(0.f, 0.f, 0.f, 0.f);
+    return make_float4(acc_value(w0.x), acc_value(w0.y), acc_value(w1.x), acc_value(w1.y));
 }
 
 // Shared-memory regions, addressed from the dynamic smem base with the
@@ -101,13 +136,15 @@ struct Smem {
     __device__ __forceinline__ float* xs() const { return reinterpret_cast<float*>(base + p.off_xs); }
     // [rows of this CTA][warps of a team] partial dots of multi-warp teams
     __device__ __forceinline__ float* rowp() const { return reinterpret_cast<float*>(base + p.off_red); }
+    // the residual stream [dim]; in the logits phase, that phase's row partials
+    __device__ __forceinline__ float* res() const { return reinterpret_cast<float*>(base + p.off_res); }
     __device__ __forceinline__ float* rope_c() const { return reinterpret_cast<float*>(base + p.off_rope); }
     __device__ __forceinline__ float* rope_s() const { return rope_c() + 128; }
-    // [2 * kConsumers] attention split combine
+    // [2 * kConsumers] attention split combine, merge partial sums
     __device__ __forceinline__ float* comb() const { return reinterpret_cast<float*>(base + p.off_comb); }
-    // [kOwnFloats] residual rows this CTA owns, then [kOwnFloats] its QKV bias rows
-    __device__ __forceinline__ float* xown() const { return reinterpret_cast<float*>(base + p.off_own); }
-    __device__ __forceinline__ float* bias() const { return xown() + kOwnFloats; }
+    // [kOwnFloats] the CTA's QKV bias rows / (gate, up) sums; then [kOwnFloats] merge weights
+    __device__ __forceinline__ float* bias() const { return reinterpret_cast<float*>(base + p.off_own); }
+    __device__ __forceinline__ float* aux() const { return bias() + kOwnFloats; }
     // the next RMSNorm's gains, fetched ahead of their phase (swizzled like the staged vector)
     __device__ __forceinline__ float* gains() const { return reinterpret_cast<float*>(base + p.off_gain); }
     __device__ __forceinline__ uint64_t* full() const { return reinterpret_cast<uint64_t*>(base + p.off_bar); }
@@ -121,10 +158,22 @@ struct Smem {
 
 // ------------------------------------------------------------ schedule --
 // Both roles walk the same sequence of chunks; these helpers define it.
-__device__ __forceinline__ void cta_rows(int rows, int& r0, int& r1) {
-    const long long b = blockIdx.x, G = gridDim.x;
-    r0 = (int)(rows * b / G);
-    r1 = (int)(rows * (b + 1) / G);
+__device__ __forceinline__ void share(int n, int j, int parts, int& a, int& b) {
+    a = (int)((long long)n * j / parts);
+    b = (int)((long long)n * (j + 1) / parts);
+}
+__device__ __forceinline__ void cta_rows(int rows, int& r0, int& r1) { share(rows, blockIdx.x, gridDim.x, r0, r1); }
+
+// This CTA's column group: group g is CTAs [g*G/ngrp, (g+1)*G/ngrp); j is the
+// CTA's index in it and n its size.
+struct Part {
+    int g, j, n;
+};
+__device__ __forceinline__ Part cta_part(int ngrp) {
+    const long long G = gridDim.x, b = blockIdx.x;
+    const int g = (int)((ngrp * (b + 1) - 1) / G);
+    const int f0 = (int)(g * G / ngrp), f1 = (int)((g + 1) * G / ngrp);
+    return Part{g, (int)b - f0, f1 - f0};
 }
 
 __device__ __forceinline__ void unit_range(const StepParams& p, int unit, int S, int& g, int& s, int& t0, int& t1) {
@@ -150,6 +199,14 @@ struct RingPos {
     }
 };
 
+__device__ __forceinline__ const char* layer_map(const StepParams& p, int layer, int which) {
+    return reinterpret_cast<const char*>(p.kv_maps) + ((size_t)kMapsPerLayer * layer + which) * 128;
+}
+
+// First scale column of group g's scale box (the group's first scale rounded
+// down to a multiple of 8, a 16-byte boundary).
+__device__ __forceinline__ int gview_scale_x(const GView& v, int g) { return (g * (v.m.cols / 32)) & ~7; }
+
 // ------------------------------------------------------------ producer --
 struct Producer {
     const StepParams& p;
@@ -157,7 +214,6 @@ struct Producer {
     RingPos rp;
     long long it = 0;
     bool dead = false;
-    long long waited = 0;  // trace builds: cycles spent waiting for free slots
 
     __device__ Producer(const StepParams& p_, Smem& s_) : p(p_), sm(s_) {}
 
@@ -168,16 +224,10 @@ struct Producer {
         if (rp.count >= p.ns) {
             const uint32_t par = rp.phase ^ 1u;
             uint64_t* bar = &sm.empty()[slot];
-#ifdef LLM_TRACE
-            const long long tw0 = clock64();
-#endif
             if (!bounded_wait([&] { return mbar_test_wait(bar, par); }, p.err)) {
                 dead = true;
                 return nullptr;
             }
-#ifdef LLM_TRACE
-            waited += clock64() - tw0;
-#endif
         }
         return sm.ring() + (size_t)slot * kSlotBytes;
     }
@@ -187,43 +237,48 @@ struct Producer {
         it++;
     }
 
-    __device__ void gemv(const DMat& m, int wtype, int tk) {
+    // Rows [r0, r1) of m (single rows) as whole rows, m.rpc per chunk.
+    __device__ void rows(const DMat& m, int wtype, int r0, int r1, int tk) {
         if (dead) return;
         trace_mark(p, tk);
-        int r0, r1;                                   // rows, or super-rows when m.pair
-        cta_rows(m.rows, r0, r1);
-        if (m.pair == 2) { r0 *= 2; r1 *= 2; }        // pairs streamed as single rows
-        const int per = m.pair == 1 ? 2 : 1;
         const size_t rowq = (size_t)row_qbytes(m, wtype);
         const int rowd = wtype == LLM_Q8_0 ? 2 * m.dstride : 0;
         for (int r = r0; r < r1; r += m.rpc) {
-            const int n = min(m.rpc, r1 - r) * per;  // matrix rows in this chunk
+            const int n = min(m.rpc, r1 - r);
             int slot;
             uint8_t* dst = acquire(slot);
             if (!dst) return;
             const uint32_t bq = (uint32_t)(n * rowq), bd = (uint32_t)(n * rowd);
             mbar_arrive_expect_tx(&sm.full()[slot], bq + bd);
-            bulk_g2s(dst, m.q + (size_t)r * per * rowq, bq, &sm.full()[slot]);
-            if (bd)
-                bulk_g2s(dst + bq, reinterpret_cast<const uint8_t*>(m.d) + (size_t)r * per * rowd, bd,
-                         &sm.full()[slot]);
-            if (r == r0 && tk < 448) trace_mark(p, 640 + (tk - 256) / 8 * 4 + ((tk - 256) % 8 == 0 ? 0 : (tk - 256) % 8 - 1));
+            bulk_g2s(dst, m.q + (size_t)r * rowq, bq, &sm.full()[slot]);
+            if (bd) bulk_g2s(dst + bq, reinterpret_cast<const uint8_t*>(m.d) + (size_t)r * rowd, bd, &sm.full()[slot]);
             issued();
         }
-#ifdef LLM_TRACE
-        if (p.trace && tk < 448)
-            p.trace[(size_t)blockIdx.x * kTraceSlots + 896 + (tk - 256) / 8 * 4 + ((tk - 256) % 8 == 0 ? 0 : (tk - 256) % 8 - 1)] = waited;
-        waited = 0;
-#endif
+    }
+
+    // Rows [r0, r1) of group g's column block of a matrix, v.R rows per chunk
+    // (TMA boxes; rows past the matrix's end read as zero).
+    __device__ void view(const GView& v, const char* mq, const char* md, int g, int r0, int r1, int tk) {
+        if (dead) return;
+        trace_mark(p, tk);
+        const int y = g * (v.m.cols / v.U), sx = gview_scale_x(v, g);
+        for (int r = r0; r < r1; r += v.R) {
+            int slot;
+            uint8_t* dst = acquire(slot);
+            if (!dst) return;
+            mbar_arrive_expect_tx(&sm.full()[slot], (uint32_t)v.box_bytes);
+            tma_3d_g2s(dst, mq, 0, y, r, &sm.full()[slot]);
+            if (v.rowd) tma_2d_g2s(dst + v.sboff, md, sx, r, &sm.full()[slot]);
+            issued();
+        }
     }
 
     __device__ void attention(int layer) {
         if (dead) return;
         trace_mark(p, 256 + 8 * layer + 1);
         const int S = p.splits, units = p.n_kv * S, P = p.attn_rows;
-        const char* maps = reinterpret_cast<const char*>(p.kv_maps);
-        const void* kmap = maps + (size_t)(2 * layer) * 128;
-        const void* vmap = maps + (size_t)(2 * layer + 1) * 128;
+        const void* kmap = layer_map(p, layer, 0);
+        const void* vmap = layer_map(p, layer, 1);
         const uint32_t half_bytes = (uint32_t)(P * p.hd * 2);
         const int W = p.attn_w, nsub = p.hd / W;                   // sub-tiles of [P][W] per tile
         for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
@@ -265,17 +320,15 @@ struct Consumer {
     Smem& sm;
     RingPos rp;            // next slot to consume
     int tid, warp, lane;
-    int own0, own1;        // residual rows this CTA owns (rows of Wo and Wdown)
     unsigned tag;          // this step's tag of the tagged vectors
-    int tk = -1;           // trace slot of the current GEMV's first chunk
-    long long waited = 0;  // trace builds: cycles spent waiting for ring slots
+    unsigned long long* delta;   // this step's parity of the residual accumulators
 
     __device__ Consumer(const StepParams& p_, Smem& s_) : p(p_), sm(s_) {
         tid = threadIdx.x;
         warp = tid >> 5;
         lane = tid & 31;
-        cta_rows(p.dim, own0, own1);
         tag = __ldcg(p.epoch) + 1u;
+        delta = p.delta + (size_t)(tag & 1u) * p.n_layers * 2 * p.dim;
     }
 
     // element offsets of the tagged vectors within a layer's set
@@ -284,6 +337,14 @@ struct Consumer {
     // layer l's tagged vector at element offset `off` of its set
     __device__ __forceinline__ unsigned long long* tv(int l, long long off) const {
         return p.tv + (long long)l * tl().stride + off;
+    }
+    // layer l's attention partials
+    __device__ __forceinline__ unsigned long long* part(int l) const {
+        return p.part + (long long)l * part_words_per_layer(p.n_heads, p.max_splits, p.hd);
+    }
+    // layer l's residual accumulator after the attention block (0) or the FFN (1)
+    __device__ __forceinline__ unsigned long long* acc(int l, int which) const {
+        return delta + ((size_t)l * 2 + which) * p.dim;
     }
 
     __device__ bool aborted() const { return *(volatile int*)&sm.misc()[0] != 0; }
@@ -294,13 +355,7 @@ struct Consumer {
         slot = rp.slot;
         const uint32_t par = rp.phase;
         uint64_t* bar = &sm.full()[slot];
-#ifdef LLM_TRACE
-        const long long tw0 = clock64();
-#endif
         if (!bounded_wait([&] { return mbar_test_wait(bar, par); }, p.err)) sm.misc()[0] = 1;
-#ifdef LLM_TRACE
-        waited += clock64() - tw0;
-#endif
         return sm.ring() + (size_t)slot * kSlotBytes;
     }
 
@@ -311,8 +366,8 @@ struct Consumer {
     }
 
     // Start copying a norm's gains (n floats, n % 4 == 0) into shared memory;
-    // lane_x waits for them.  Each 16-byte word w lands at the swizzled word
-    // (w & ~7) + ((w & 7) ^ ((w >> 3) & 7)), as the staged vectors do.
+    // lanes_prep waits for them.  Each 16-byte word w lands at the swizzled
+    // word (w & ~7) + ((w & 7) ^ ((w >> 3) & 7)), as the staged vectors do.
     __device__ void prefetch_gains(const float* g, int n) {
         float4* dst = reinterpret_cast<float4*>(sm.gains());
         for (int i = tid; i < n / 4; i += kConsumers)
@@ -538,42 +593,37 @@ __device__ __forceinline__ void lane_rows(const uint32_t (&w)[N], const uint32_t
 // ------------------------------------------------------------------ GEMV --
 // The epilogue of a GEMV phase, chosen at run time (all phases share one
 // copy of the GEMV code):
-//   kStore     out[r] = v (+ bias of this CTA's row r), tagged
-//   kResidual  out[r] = own[r] + v, the owned rows kept in shared memory
-//   kSwiGLU    u[i] = silu(gate_i) * up_i ("The Forward Pass in Java",
-//              Example 8): the (gate, up) sums of interleaved rows 2i, 2i+1
-//              are parked in shared memory and the nonlinearity is applied
-//              to all of the CTA's rows at once when the phase finishes
-//   kLogits    logits[r] = v, keeping this thread's best (value, first index)
+//   kStore   out[r] = v (+ bias of this CTA's row r), tagged
+//   kSwiGLU  u[i] = silu(gate_i) * up_i ("The Forward Pass in Java",
+//            Example 8): the (gate, up) sums of interleaved rows 2i, 2i+1
+//            are parked in shared memory and the nonlinearity is applied to
+//            all of the CTA's rows at once when the phase finishes
+//   kLogits  logits[r] = v, keeping this thread's best (value, first index)
+//   kAccum   v added to row r's residual accumulator word (fixed point)
 struct Epi {
-    enum : int { kStore, kResidual, kSwiGLU, kLogits };
+    enum : int { kStore, kSwiGLU, kLogits, kAccum };
     int kind;
-    unsigned long long* out;      // tagged output vector (store, residual, swiglu)
+    unsigned long long* out;      // tagged output vector (store, swiglu) or accumulator words (accum)
     const float* bias;            // store: smem bias indexed from `base`, or nullptr
-    float* sm;                    // residual: owned rows; swiglu: (gate, up) sums
-    int base;                     // first row (store), first owned row (residual), first super-row (swiglu)
+    float* sm;                    // swiglu: (gate, up) sums
+    int base;                     // first row (store), first super-row (swiglu)
     int end;                      // swiglu: end super-row
     unsigned tag;
     float* logits;
+    int* err;
     unsigned long long best;
     __device__ void row(int r, float v) {
         if (kind == kStore) {
             st_tagged(out + r, bias ? v + bias[r - base] : v, tag);
-        } else if (kind == kResidual) {
-            const float y = sm[r - base] + v;
-            sm[r - base] = y;
-            st_tagged(out + r, y, tag);
         } else if (kind == kSwiGLU) {
             sm[r - 2 * base] = v;                 // row r: gate (even) or up (odd) of super-row r / 2
+        } else if (kind == kAccum) {
+            acc_add(out + r, v, err);
         } else {
             __stcg(logits + r, v);
             const unsigned long long k = argmax_key(v, r);
             best = k > best ? k : best;
         }
-    }
-    __device__ void pair(int i, float g, float up) {
-        sm[2 * (i - base)] = g;
-        sm[2 * (i - base) + 1] = up;
     }
     __device__ void finish(Consumer& c) {
         if (kind != kSwiGLU) return;
@@ -586,23 +636,14 @@ struct Epi {
     }
 };
 
-// Where a GEMV phase takes its activation vector: a tagged vector (written
-// by this step) or the embedding row of `token`, optionally RMSNormed with
-// gains g ("The Forward Pass in Java", Example 4: y = (x * scale) * g with
-// scale = 1/sqrt(mean(x^2) + eps), the sum of squares a float tree sum).
-struct XSrc {
-    const unsigned long long* x;  // tagged; nullptr: the embedding row
-    const float* g;               // nullptr: no norm
-    int n;                        // length of the vector
-};
-
-// Lane layout of a plan: team, lane index within the team, row half (pair).
+// Lane layout of a plan: team, lane index within the team (= the lane's
+// 32-column block of the row), first column, 16-byte words of the row.
 struct Lanes {
-    int team, lit, hsel, clit, col0, nseg;
+    int team, lit, col0, nseg;
     bool active;
 };
 
-template <int DT, bool PAIR>
+template <int DT>
 __device__ __forceinline__ Lanes lane_layout(const Consumer& c, const DMat& m) {
     constexpr int ES = DT == LLM_Q8_0 ? 1 : (DT == LLM_F16 ? 2 : 4);
     Lanes L;
@@ -615,11 +656,8 @@ __device__ __forceinline__ Lanes lane_layout(const Consumer& c, const DMat& m) {
         L.team = c.warp / wpr;
         L.lit = (c.warp % wpr) * 32 + c.lane;
     }
-    const int half = PAIR ? tw / 2 : tw;
-    L.hsel = PAIR ? L.lit / half : 0;
-    L.clit = L.lit - L.hsel * half;
     L.active = L.team < m.teams;
-    L.col0 = L.clit * kLaneElems;
+    L.col0 = L.lit * kLaneElems;
     L.nseg = L.active && L.col0 < m.cols ? min(kLaneElems, m.cols - L.col0) * ES / 16 : 0;
     return L;
 }
@@ -636,144 +674,231 @@ __device__ __forceinline__ void xreg_from_words(Word w, XReg<DT>& xr) {
     }
 }
 
-// xr <- the lane's 32 activations, normed when src.g is set ("The Forward
-// Pass in Java", Example 4: y = (x * scale) * g, scale = 1/sqrt(mean(x^2) +
-// eps), the sum of squares a float tree sum).  Every consumer thread must call
-// this (it synchronises).  The vector is staged in the scratch region with
-// coalesced loads (each 16-byte word w of the 128-byte slice s at word s*8 +
-// (w ^ (s & 7)), so that the lanes' reads of their own slices fall in distinct
-// banks), normed in place by the threads that staged it, and each lane then
-// reads its slice from shared memory.  This keeps the L2 requests per line of
-// the (freshly written, grid-wide read) vector at one per CTA.  A vector longer
-// than the region is staged in region-sized pieces, one after the other; only
-// the FFN-length input of the down projection is that long (every normed
-// vector and the embedding row have length dim, which always fits).
-template <int DT, bool PAIR>
-__device__ __forceinline__ void lane_x(Consumer& c, const Lanes& L, const XSrc& src, int token, XReg<DT>& xr) {
-    const int col0 = L.col0;
-    const bool have = L.active && col0 < src.n;
-    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4* xv = reinterpret_cast<float4*>(c.sm.xs());
-    auto sw = [](int i) { return (i & ~7) + ((i & 7) ^ ((i >> 3) & 7)); };
-    const int piece = c.p.scratch_floats & ~31;          // floats per staging pass (whole slices)
-    for (int base = 0; base < src.n; base += piece) {
-        const int len = min(piece, src.n - base), ngr = len / 4;
-        float ss = 0.f;
-        if (src.x) {
-            const unsigned long long* xsrc = src.x + base;
-            for (int i = c.tid; i < ngr; i += kConsumers) {
-                const float4 v = poll4(xsrc + 4 * i, c.tag, c.p.err);
-                ss += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
-                xv[sw(i)] = v;
-            }
+// The staging region holds a phase's activation vector as 16-byte words;
+// word i of the 128-byte slice s = i / 8 sits at word s*8 + ((i & 7) ^ (s & 7)),
+// so that the lanes' reads of their own slices fall in distinct banks.
+__device__ __forceinline__ int swz(int i) { return (i & ~7) + ((i & 7) ^ ((i >> 3) & 7)); }
+
+// Staging sources.  Each thread stages the 4-element groups i = tid, tid +
+// kConsumers, ... (the same set in every phase, so a thread finds the
+// residual values it keeps where it left them).
+//
+// The residual stream: x = x + (the update the block before added to the
+// accumulator words d, once all ngrp groups have added), or at layer 0 the
+// embedding row of `token` ("The Forward Pass in Java", Example 3: a copy of
+// that row).  Kept in the residual region and staged; returns the thread's
+// sum of squares of the staged values (for the RMSNorm that follows).
+template <int DT>
+__device__ float stage_residual(Consumer& c, const unsigned long long* d, int token, float4* xv) {
+    const StepParams& p = c.p;
+    float4* res = reinterpret_cast<float4*>(c.sm.res());
+    const int ngr = p.dim / 4;
+    float ss = 0.f;
+    for (int i = c.tid; i < ngr; i += kConsumers) {
+        float4 x;
+        if (d) {
+            const float4 u = poll_acc4(d + 4 * i, (unsigned)p.ngrp, p.err);
+            const float4 r = res[i];
+            x = make_float4(__fadd_rn(r.x, u.x), __fadd_rn(r.y, u.y), __fadd_rn(r.z, u.z), __fadd_rn(r.w, u.w));
         } else {
-            for (int i = c.tid; i < ngr; i += kConsumers) {
-                const int e = base + 4 * i;
-                const float4 v = make_float4(weight_at<DT>(c.p.embd, token, e), weight_at<DT>(c.p.embd, token, e + 1),
-                                             weight_at<DT>(c.p.embd, token, e + 2), weight_at<DT>(c.p.embd, token, e + 3));
-                ss += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
-                xv[sw(i)] = v;
-            }
+            const int e = 4 * i;
+            x = make_float4(weight_at<DT>(p.embd, token, e), weight_at<DT>(p.embd, token, e + 1),
+                            weight_at<DT>(p.embd, token, e + 2), weight_at<DT>(p.embd, token, e + 3));
         }
-        if (src.g) {
-            // (normed vectors are staged in one piece)
-            cp_async_wait_all();                         // this thread's part of the gains (fetched ahead)
-            const float tot = c.warps_total(ss);        // synchronises the consumers
-            const float scale = 1.0f / sqrtf(tot / (float)src.n + c.p.eps);
-            // each thread norms the groups it staged (their gains are the ones it fetched)
-            const float4* g4 = reinterpret_cast<const float4*>(c.sm.gains());
-            for (int i = c.tid; i < ngr; i += kConsumers) {
-                const float4 x = xv[sw(i)], g = g4[sw(i)];
-                xv[sw(i)] = make_float4(__fmul_rn(__fmul_rn(x.x, scale), g.x), __fmul_rn(__fmul_rn(x.y, scale), g.y),
-                                        __fmul_rn(__fmul_rn(x.z, scale), g.z), __fmul_rn(__fmul_rn(x.w, scale), g.w));
-            }
-        }
-        // lanes whose slice lies in this piece (slices never straddle pieces)
-        const int sl = (col0 - base) >> 5;
-        const bool mine = col0 >= base && col0 < base + len;
-        if constexpr (DT == LLM_Q8_0) {
-            // every staged group becomes its share of its block's digit record
-            for (int i0 = c.tid - c.lane; i0 < ngr; i0 += kConsumers) {
-                const int i = i0 + c.lane;
-                const bool valid = i < ngr;
-                convert_group(xv, i >> 3, i & 7, valid, valid ? xv[sw(i)] : zero);
-            }
-            consumer_sync();
-            if (mine && have) {
-                const uint4* rec = reinterpret_cast<const uint4*>(xv + sl * 8);
-                const int rot = sl & 7;
+        res[i] = x;
+        ss += (x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w);
+        xv[swz(i)] = x;
+    }
+    return ss;
+}
+
+// n elements (n % 4 == 0) of a tagged vector of this step.
+__device__ void stage_tagged(Consumer& c, const unsigned long long* src, int n, float4* xv) {
+    for (int i = c.tid; i < n / 4; i += kConsumers) xv[swz(i)] = poll4(src + 4 * i, c.tag, c.p.err);
+}
+
+// The attention output of group g's heads, merged from the position splits'
+// partials (m_s, l_s, acc_s): per head M = max_s m_s, w_s = e^(m_s - M) /
+// sum_s' e^(m_s' - M) l_s', o = sum_s w_s acc_s.  Weights: one warp per head,
+// one lane per split.  Weighted sums: thread (pair e2 of the group's outputs,
+// split class sg) takes the splits s = sg, sg + NSG, ... in ascending order;
+// the classes' sums are then added in class order (the same bits on every
+// CTA of the group and in every run).  A thread issues its first eight loads
+// before it waits on any of them.
+__device__ void stage_merged(Consumer& c, int layer, int g, float4* xv) {
+    const StepParams& p = c.p;
+    const int HG = p.n_heads / p.ngrp, hd = p.hd, S = p.splits, MS = p.max_splits;
+    const int h0 = g * HG, GDG = HG * hd;
+    const unsigned long long* pacc = c.part(layer);
+    const unsigned long long* pml = pacc + (size_t)p.n_heads * MS * hd;
+    float* wgt = c.sm.aux();                                       // [HG][S]
+    float* comb = c.sm.comb();                                     // [NSG][GDG]
+    const int NP = GDG / 2, NSG = kConsumers / NP;
+    const int e2 = c.tid % NP, sg = c.tid / NP;
+    const bool act = sg < NSG;
+    const int hh = (2 * e2) / hd, ii = (2 * e2) % hd;
+    const unsigned long long* src = pacc + (size_t)(h0 + hh) * MS * hd + ii;
+    constexpr int kB = 8;
+    ulonglong2 w[kB];
 #pragma unroll
-                for (int k = 0; k < 3; k++) {
-                    const uint4 a = rec[(2 * k) ^ rot], b = rec[(2 * k + 1) ^ rot];
-                    xr.d[k][0] = a.x; xr.d[k][1] = a.y; xr.d[k][2] = a.z; xr.d[k][3] = a.w;
-                    xr.d[k][4] = b.x; xr.d[k][5] = b.y; xr.d[k][6] = b.z; xr.d[k][7] = b.w;
-                }
-                xr.inv = __uint_as_float(rec[6 ^ rot].x);
-            } else if (base == 0) {
+    for (int k = 0; k < kB; k++) {
+        const int s = sg + k * NSG;
+        if (act && s < S) w[k] = ld_tagged2(src + (size_t)s * hd);
+    }
+    for (int h = c.warp; h < HG; h += kConsumerWarps) {
+        const bool has = c.lane < S;
+        const float2 ml = has ? poll2(pml + 2 * ((size_t)(h0 + h) * MS + c.lane), c.tag, p.err)
+                              : make_float2(-INFINITY, 0.f);
+        const float M = warp_max(ml.x);
+        const float wv = has && ml.x != -INFINITY ? expf(ml.x - M) : 0.f;
+        const float Ls = warp_sum(wv * ml.y);
+        if (has) wgt[h * S + c.lane] = wv / Ls;
+    }
 #pragma unroll
-                for (int k = 0; k < 8; k++) xr.d[0][k] = xr.d[1][k] = xr.d[2][k] = 0u;
-                xr.inv = 0.f;
-            }
-        } else {
-            consumer_sync();
-            if (mine) {
-                const float4* x4 = xv + sl * 8;
-                const int rot = sl & 7;
-                xreg_from_words<DT>([&](int k) { return have && col0 + 4 * k < src.n ? x4[k ^ rot] : zero; }, xr);
-            } else if (base == 0 && !have) {
-                xreg_from_words<DT>([&](int) { return zero; }, xr);
+    for (int k = 0; k < kB; k++) {
+        const int s = sg + k * NSG;
+        if (act && s < S && !tagged2_ready(w[k], c.tag)) {
+            const float2 v = poll2(src + (size_t)s * hd, c.tag, p.err);
+            w[k].x = __float_as_uint(v.x);
+            w[k].y = __float_as_uint(v.y);
+        }
+    }
+    consumer_sync();                                               // weights
+    float ox = 0.f, oy = 0.f;
+    if (act) {
+        const float* wh = wgt + hh * S;
+#pragma unroll
+        for (int k = 0; k < kB; k++) {
+            const int s = sg + k * NSG;
+            if (s < S) {
+                ox = fmaf(wh[s], __uint_as_float((unsigned)w[k].x), ox);
+                oy = fmaf(wh[s], __uint_as_float((unsigned)w[k].y), oy);
             }
         }
-        if (base + len < src.n) consumer_sync();       // the next piece overwrites the region
+        for (int s = sg + kB * NSG; s < S; s += NSG) {
+            const float2 v = poll2(src + (size_t)s * hd, c.tag, p.err);
+            ox = fmaf(wh[s], v.x, ox);
+            oy = fmaf(wh[s], v.y, oy);
+        }
+        comb[sg * GDG + 2 * e2] = ox;
+        comb[sg * GDG + 2 * e2 + 1] = oy;
+    }
+    consumer_sync();
+    for (int q = c.tid; q < GDG / 4; q += kConsumers) {
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < NSG; k++) {
+            const float4 v = reinterpret_cast<const float4*>(comb + k * GDG)[q];
+            o.x += v.x;
+            o.y += v.y;
+            o.z += v.z;
+            o.w += v.w;
+        }
+        xv[swz(q)] = o;
     }
 }
 
-// The CTA's rows of m, chunk by chunk from the ring (the plan in DMat).
-// Multi-warp teams take two rows per pass: their partial dots are reduced with
-// one butterfly (lanes 0-15 for the first row, 16-31 for the second) and each
-// warp parks its part of the two rows in shared memory; after the last chunk
-// the consumers finish all rows at once (parts added in warp order, so the
-// result does not depend on timing) and apply the phase's epilogue.
-template <int DT, bool PAIR>
-__device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const XSrc& src, int token, Epi& epi) {
+// xr <- the lane's 32 activations of the staged vector (n elements),
+// normed first when `gains` is set ("The Forward Pass in Java", Example 4:
+// y = (x * scale) * g, scale = 1/sqrt(mean(x^2) + eps), the sum of squares a
+// float tree sum; the gains were fetched ahead with cp.async).  Each thread
+// norms the groups it staged; Q8_0 phases then turn every staged 32-element
+// block into its digit record (convert_group), again on the groups the
+// thread staged.  Every consumer thread must call this (it synchronises).
+template <int DT>
+__device__ void lanes_prep(Consumer& c, const Lanes& L, int n, const float* gains, float ss, XReg<DT>& xr) {
+    const int ngr = n / 4;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4* xv = reinterpret_cast<float4*>(c.sm.xs());
+    if (gains) {
+        cp_async_wait_all();                         // this thread's part of the gains
+        const float tot = c.warps_total(ss);         // synchronises the consumers
+        const float scale = 1.0f / sqrtf(tot / (float)n + c.p.eps);
+        const float4* g4 = reinterpret_cast<const float4*>(gains);
+        for (int i = c.tid; i < ngr; i += kConsumers) {
+            const float4 x = xv[swz(i)], g = g4[swz(i)];
+            xv[swz(i)] = make_float4(__fmul_rn(__fmul_rn(x.x, scale), g.x), __fmul_rn(__fmul_rn(x.y, scale), g.y),
+                                     __fmul_rn(__fmul_rn(x.z, scale), g.z), __fmul_rn(__fmul_rn(x.w, scale), g.w));
+        }
+    }
+    const int col0 = L.col0;
+    const bool have = L.active && col0 < n;
+    const int sl = col0 >> 5;
+    if constexpr (DT == LLM_Q8_0) {
+        for (int i0 = c.tid - c.lane; i0 < ngr; i0 += kConsumers) {
+            const int i = i0 + c.lane;
+            const bool valid = i < ngr;
+            convert_group(xv, i >> 3, i & 7, valid, valid ? xv[swz(i)] : zero);
+        }
+        consumer_sync();
+        if (have) {
+            const uint4* rec = reinterpret_cast<const uint4*>(xv + sl * 8);
+            const int rot = sl & 7;
+#pragma unroll
+            for (int k = 0; k < 3; k++) {
+                const uint4 a = rec[(2 * k) ^ rot], b = rec[(2 * k + 1) ^ rot];
+                xr.d[k][0] = a.x; xr.d[k][1] = a.y; xr.d[k][2] = a.z; xr.d[k][3] = a.w;
+                xr.d[k][4] = b.x; xr.d[k][5] = b.y; xr.d[k][6] = b.z; xr.d[k][7] = b.w;
+            }
+            xr.inv = __uint_as_float(rec[6 ^ rot].x);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; k++) xr.d[0][k] = xr.d[1][k] = xr.d[2][k] = 0u;
+            xr.inv = 0.f;
+        }
+    } else {
+        consumer_sync();
+        const float4* x4 = xv + sl * 8;
+        const int rot = sl & 7;
+        xreg_from_words<DT>([&](int k) { return have && col0 + 4 * k < n ? x4[k ^ rot] : zero; }, xr);
+    }
+}
+
+// Where a chunk's rows sit in its ring slot.
+struct ChunkGeo {
+    int rowq, rowd;   // bytes per row of values, of Q8_0 scales
+    int sfix;         // >= 0: the scales start at this byte offset; < 0: right after the chunk's values
+    int soff;         // byte offset of the row's first scale within a scale row
+    int rpc;          // rows per chunk
+};
+
+__device__ __forceinline__ ChunkGeo rows_geo(const DMat& m, int wtype) {
+    return ChunkGeo{row_qbytes(m, wtype), wtype == LLM_Q8_0 ? 2 * m.dstride : 0, -1, 0, m.rpc};
+}
+__device__ __forceinline__ ChunkGeo view_geo(const GView& v, int g) {
+    return ChunkGeo{v.rowq, v.rowd, v.sboff, v.rowd ? (g * (v.m.cols / 32) - gview_scale_x(v, g)) * 2 : 0, v.R};
+}
+
+// Rows [r0, r1) of m, chunk by chunk from the ring (the plan in m, the chunk
+// layout in ck).  Multi-warp teams take four (Q8_0) or two rows per pass:
+// their partial dots are reduced with one transposed butterfly and each warp
+// parks its part of the rows in `rowp`; after the last chunk the consumers
+// finish all rows at once (parts added in warp order, so the result does not
+// depend on timing) and apply the phase's epilogue.
+template <int DT>
+__device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const ChunkGeo& ck, int r0, int r1,
+                                             const Lanes& L, const XReg<DT>& xr, float* rowp, Epi& epi) {
     constexpr int ES = DT == LLM_Q8_0 ? 1 : (DT == LLM_F16 ? 2 : 4);
-    const Lanes L = lane_layout<DT, PAIR>(c, m);
-    XReg<DT> xr;
-    lane_x<DT, PAIR>(c, L, src, token, xr);
-    if (c.tid == 0 && c.tk >= 0) trace_mark(c.p, c.tk - 160 + 512);
     const int tw = m.tw, teams = m.teams;
-    int r0, r1;
-    cta_rows(m.rows, r0, r1);
-    if (m.pair == 2) { r0 *= 2; r1 *= 2; }            // pairs reduced as single rows
-    const int per = PAIR ? 2 : 1;
-    const int rowq = row_qbytes(m, DT);
-    const int rowd = DT == LLM_Q8_0 ? 2 * m.dstride : 0;
-    const int xoff = L.col0 * ES, soff = L.clit * 2;
-    for (int r = r0; r < r1; r += m.rpc) {
-        const int n = min(m.rpc, r1 - r);
+    const int xoff = L.col0 * ES, soff = ck.soff + L.lit * 2;
+    for (int r = r0; r < r1; r += ck.rpc) {
+        const int n = min(ck.rpc, r1 - r);
         int slot;
         const uint8_t* buf = c.next_slot(slot);
-        if (c.tid == 0 && r == r0 && c.tk >= 0) trace_mark(c.p, c.tk);
-        const uint8_t* sbase = buf + (size_t)n * per * rowq;
+        const uint8_t* sbase = buf + (ck.sfix >= 0 ? ck.sfix : n * ck.rowq);
         const uint32_t sbuf = smem_addr(buf), ssc = smem_addr(sbase);
         if (tw <= 32) {
-            const int half = PAIR ? tw / 2 : tw;
             const int wteam = c.warp * (32 / tw);
             for (int j = 0; wteam + j * teams < n; j++) {
                 const int rr = L.team + j * teams;
                 const bool real = L.active && rr < n;
-                const int mrow = (real ? rr : 0) * per + L.hsel;
-                float v = real ? lane_row<DT>(buf + (size_t)mrow * rowq + xoff, sbase + mrow * rowd + soff, xr, L.nseg)
+                const int mrow = real ? rr : 0;
+                float v = real ? lane_row<DT>(buf + (size_t)mrow * ck.rowq + xoff, sbase + mrow * ck.rowd + soff, xr,
+                                              L.nseg)
                                : 0.f;
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1)
-                    if (o < half) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if constexpr (PAIR) {
-                    const float up = __shfl_down_sync(0xffffffffu, v, half);
-                    if (real && L.lit == 0) epi.pair(r + rr, v, up);
-                } else {
-                    if (real && L.lit == 0) epi.row(r + rr, v);
-                }
+                    if (o < tw) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (real && L.lit == 0) epi.row(r + rr, v);
             }
         } else if (L.active) {
             // whole-warp teams: RPP consecutive rows per pass; each warp parks
@@ -782,16 +907,16 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
             // lanes 8k..8k+7 (RPP 4) or 16k..16k+15 (RPP 2) end with row k.
             constexpr int RPP = RowsPerPass<DT>::value;
             const int wpr = tw / 32, wi = c.warp % wpr;
-            float* rp = c.sm.rowp() + (size_t)(r - r0) * wpr + wi;
+            float* rp = rowp + (size_t)(r - r0) * wpr + wi;
             for (int j = 0;; j++) {
                 const int rbase = (L.team + j * teams) * RPP;
                 if (rbase >= n) break;
                 uint32_t wq[RPP], ws[RPP];
 #pragma unroll
                 for (int k = 0; k < RPP; k++) {
-                    const int mr = min(rbase + k, n - 1) * per + L.hsel;
-                    wq[k] = sbuf + (uint32_t)(mr * rowq + xoff);
-                    ws[k] = ssc + (uint32_t)(mr * rowd + soff);
+                    const int mr = min(rbase + k, n - 1);
+                    wq[k] = sbuf + (uint32_t)(mr * ck.rowq + xoff);
+                    ws[k] = ssc + (uint32_t)(mr * ck.rowd + soff);
                 }
                 float v[RPP];
                 lane_rows<DT, RPP>(wq, ws, xr, L.nseg, v);
@@ -821,28 +946,16 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const X
         // finish every row: the warps' parts added in warp order
         const int wpr = tw / 32;
         consumer_sync();
-        const float* rp = c.sm.rowp();
         for (int i = c.tid; i < r1 - r0; i += kConsumers) {
-            if constexpr (PAIR) {
-                float g = 0.f, up = 0.f;
-                for (int k = 0; k < wpr / 2; k++) g += rp[i * wpr + k];
-                for (int k = wpr / 2; k < wpr; k++) up += rp[i * wpr + k];
-                epi.pair(r0 + i, g, up);
-            } else {
-                float t = 0.f;
-                for (int k = 0; k < wpr; k++) t += rp[i * wpr + k];
-                epi.row(r0 + i, t);
-            }
+            float t = 0.f;
+            for (int k = 0; k < wpr; k++) t += rowp[i * wpr + k];
+            epi.row(r0 + i, t);
         }
     }
     epi.finish(c);
-    // narrow teams have no finishing barrier: the next phase's staging must
-    // not overwrite the staged vector (or the gains) while a warp still reads it
-    if (tw <= 32) consumer_sync();
-#ifdef LLM_TRACE
-    if (c.tid == 0 && c.tk >= 0 && c.p.trace) c.p.trace[(size_t)blockIdx.x * kTraceSlots + c.tk - 160 + 768] = c.waited;
-    c.waited = 0;
-#endif
+    // the next phase's staging must not overwrite what a warp still reads
+    // (the gains, the (gate, up) sums, the row partials)
+    consumer_sync();
 }
 
 // ------------------------------------------------------------------ RoPE --
@@ -941,58 +1054,6 @@ __device__ void attention_prologue(Consumer& c, const LayerDev& L, int layer, in
     consumer_sync();                                               // kp, vp visible
 }
 
-// After the unit's partial is stored: the last unit of kv head g (an
-// acquire-release counter) merges the splits in one round of loads and
-// writes the heads' tagged output.
-__device__ void attention_merge(Consumer& c, int layer, int g) {
-    const StepParams& p = c.p;
-    Smem& sm = c.sm;
-    const int tid = c.tid, warp = c.warp, lane = c.lane;
-    const int hd = p.hd, gq = p.n_heads / p.n_kv, h0 = g * gq, GD = gq * hd, S = p.splits;
-    const float* part_acc = p.attn_part;
-    const float* part_ml = p.attn_part + (size_t)p.n_heads * p.max_splits * hd;
-    unsigned* mc = p.counters + n_phase_counters(p.n_layers) + layer * p.n_kv + g;
-    if (tid == 0) sm.misc()[1] = atom_add_acq_rel(mc, 1u) == (unsigned)(S - 1);
-    consumer_sync();
-    if (sm.misc()[1]) {
-        if (tid == 0) trace_mark(p, 576 + 4 * layer + 2);
-        // weights per head, one warp per head and one split per lane (S <= 32)
-        const int MS = p.max_splits;
-        float* wgt = sm.comb();                                    // [gq][S]
-        if (warp < gq) {
-            const bool has = lane < S;
-            const float2 mv = has ? __ldcg(reinterpret_cast<const float2*>(part_ml) + (size_t)(h0 + warp) * MS + lane)
-                                  : make_float2(-INFINITY, 0.f);
-            const float M = warp_max(mv.x);
-            const float w = has && mv.x != -INFINITY ? expf(mv.x - M) : 0.f;
-            const float Ls = warp_sum(w * mv.y);
-            if (has) wgt[warp * S + lane] = w / Ls;
-        }
-        // every thread loads its elements' partial sums meanwhile (all splits at once)
-        for (int e0 = 0; e0 < GD; e0 += kConsumers) {
-            const int e = e0 + tid;
-            const int hh = e < GD ? e / hd : 0, ii = e < GD ? e % hd : 0;
-            const float* src = part_acc + (size_t)(h0 + hh) * MS * hd + ii;
-            float av[32];
-#pragma unroll
-            for (int k = 0; k < 32; k++) av[k] = e < GD && k < S ? __ldcg(src + (size_t)k * hd) : 0.f;
-            consumer_sync();                                       // weights ready
-            if (e < GD) {
-                float v = 0.f;
-#pragma unroll
-                for (int k = 0; k < 32; k++)
-                    if (k < S) v = fmaf(wgt[hh * S + k], av[k], v);
-                st_tagged(c.tv(layer, c.tl().attn) + (h0 + hh) * hd + ii, v, c.tag);
-            }
-        }
-        if (tid == 0) trace_mark(p, 576 + 4 * layer + 3);
-    }
-    consumer_sync();
-}
-
-// Scalar form (any head_dim and group size): scores one thread per (head,
-// position), softmax one warp per head, the weighted V sum split over
-// threads by output pair and position stride.
 __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int unit) {
     const StepParams& p = c.p;
     Smem& sm = c.sm;
@@ -1109,18 +1170,20 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
         sm.comb()[sp * GD + 2 * o2 + 1] = acc.y;
     }
     consumer_sync();
-    float* part_acc = p.attn_part;
-    float* part_ml = p.attn_part + (size_t)p.n_heads * p.max_splits * hd;
+    unsigned long long* part_acc = c.part(layer);
+    unsigned long long* part_ml = part_acc + (size_t)p.n_heads * p.max_splits * hd;
     for (int oo = tid; oo < GD; oo += kConsumers) {
         float v = 0.f;
         for (int k = 0; k < NSPLIT; k++) v += sm.comb()[k * GD + oo];
         const int hh = oo / hd, ii = oo % hd;
         const size_t hs = (size_t)(h0 + hh) * p.max_splits + s;
-        __stcg(part_acc + hs * hd + ii, v);
-        if (ii == 0) __stcg(reinterpret_cast<float2*>(part_ml) + hs, make_float2(ml[hh], ml[gq + hh]));
+        st_tagged(part_acc + hs * hd + ii, v, c.tag);
+        if (ii == 0) {
+            st_tagged(part_ml + 2 * hs, ml[hh], c.tag);
+            st_tagged(part_ml + 2 * hs + 1, ml[gq + hh], c.tag);
+        }
     }
     consumer_sync();                                               // comb, scratch free
-    attention_merge(c, layer, g);
     return true;
 }
 
@@ -1129,7 +1192,6 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
 // 64, else hd), each written by TMA with the swizzle of its row width (128,
 // 64 or 32 bytes: address bits 7.. XORed into the chunk bits 4..; none for
 // other widths).  The ring is 1024-byte aligned, so the pattern computed on
-// the address is the one the copy used.
 template <int HD>
 __device__ __forceinline__ uint32_t kv_chunk(uint32_t tile, int P, int r, int ch) {
     constexpr int W = HD % 64 == 0 ? 64 : HD;
@@ -1276,16 +1338,18 @@ __device__ bool attention_unit_mma(Consumer& c, const LayerDev& L, int layer, in
             }
         }
     }
+    unsigned long long* part_acc = c.part(layer);
+    unsigned long long* part_ml = part_acc + (size_t)p.n_heads * p.max_splits * HD;
     if (!buf) {                                                    // no positions: an empty partial
         for (int oo = tid; oo < GD; oo += kConsumers) {
             const size_t hs = (size_t)(h0 + oo / HD) * p.max_splits + s;
-            __stcg(p.attn_part + hs * HD + oo % HD, 0.f);
-            if (oo % HD == 0)
-                __stcg(reinterpret_cast<float2*>(p.attn_part + (size_t)p.n_heads * p.max_splits * HD) + hs,
-                       make_float2(-INFINITY, 0.f));
+            st_tagged(part_acc + hs * HD + oo % HD, 0.f, c.tag);
+            if (oo % HD == 0) {
+                st_tagged(part_ml + 2 * hs, -INFINITY, c.tag);
+                st_tagged(part_ml + 2 * hs + 1, 0.f, c.tag);
+            }
         }
         consumer_sync();
-        attention_merge(c, layer, g);
         return true;
     }
     // the warps' partials, in the last slot (its tile is no longer read)
@@ -1304,8 +1368,6 @@ __device__ bool attention_unit_mma(Consumer& c, const LayerDev& L, int layer, in
         wpart[warp * WS + hq * (HD + 2) + HD + 1] = l_run;
     }
     consumer_sync();
-    float* part_acc = p.attn_part;
-    float* part_ml = p.attn_part + (size_t)p.n_heads * p.max_splits * HD;
     for (int oo = tid; oo < GD; oo += kConsumers) {
         const int hh = oo / HD, ii = oo % HD;
         float M = -INFINITY;
@@ -1318,14 +1380,16 @@ __device__ bool attention_unit_mma(Consumer& c, const LayerDev& L, int layer, in
             l = fmaf(f, wpart[w * WS + hh * (HD + 2) + HD + 1], l);
         }
         const size_t hs = (size_t)(h0 + hh) * p.max_splits + s;
-        __stcg(part_acc + hs * HD + ii, v);
-        if (ii == 0) __stcg(reinterpret_cast<float2*>(part_ml) + hs, make_float2(M, l));
+        st_tagged(part_acc + hs * HD + ii, v, c.tag);
+        if (ii == 0) {
+            st_tagged(part_ml + 2 * hs, M, c.tag);
+            st_tagged(part_ml + 2 * hs + 1, l, c.tag);
+        }
     }
     fence_proxy_async_smem();                                      // the slot's next fill is a TMA write
     consumer_sync();
     c.release(slot);
     if (tid == 0) trace_mark(p, 576 + 4 * layer + 1);
-    attention_merge(c, layer, g);
     return true;
 }
 
@@ -1340,7 +1404,6 @@ __device__ bool attention_any(Consumer& c, const LayerDev& L, int layer, int uni
     }
     return attention_unit(c, L, layer, unit);
 }
-
 // ----------------------------------------------------------------- kernel --
 template <int DT>
 __device__ bool consumer_main(const StepParams& p, Smem& sm) {
@@ -1351,84 +1414,124 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, kErrToken);
         token = 0;
     }
+    // this CTA's share of the other parity's accumulators (the next step's)
+    {
+        unsigned long long* other = p.delta + (size_t)((c.tag & 1u) ^ 1u) * p.n_layers * 2 * p.dim;
+        int z0, z1;
+        cta_rows(p.n_layers * 2 * p.dim, z0, z1);
+        for (int i = z0 + tid; i < z1; i += kConsumers) other[i] = 0ull;
+    }
     c.prefetch_gains(p.layers[0].attn_norm, p.dim);
     rope_table(p, sm, tid);
-    // this CTA's residual rows start as the embedding row's values
-    for (int i = c.own0 + tid; i < c.own1; i += kConsumers) sm.xown()[i - c.own0] = weight_at<DT>(p.embd, token, i);
-    // Phases wait for their inputs through the tags of the vectors they read;
-    // the only counters left are the attention merges and the end of the step.
+    const Part pt = cta_part(p.ngrp);
+    const int fdg = p.dv.m.cols;
+    int rg0, rg1;            // this CTA's rows of its group's Wo and Wdown column blocks
+    share(p.dim, pt.j, pt.n, rg0, rg1);
+    int u0, u1;              // this CTA's FFN columns (gate/up super-rows)
+    share(fdg, pt.j, pt.n, u0, u1);
+    u0 += pt.g * fdg;
+    u1 += pt.g * fdg;
+    float4* xv = reinterpret_cast<float4*>(sm.xs());
     // Every GEMV phase (QKV, O, GU, DOWN of each layer, then the logits) goes
     // through the one call site below, so the kernel holds one copy of the
     // GEMV code.
+    enum { kSrcResidual, kSrcTagged, kSrcMerged };
     const int nph = 4 * p.n_layers + 1;
     unsigned long long best = 0ull;
     for (int ph = 0; ph < nph; ph++) {
         const int l = ph >> 2, k = ph & 3;
         const bool last = ph == nph - 1;
         const LayerDev& L = p.layers[last ? p.n_layers - 1 : l];
-        const DMat* m;
-        XSrc src;
+        DMat m;
+        ChunkGeo ck;
+        int r0, r1, n, src;
+        const unsigned long long* sv = nullptr;   // residual: accumulator words (nullptr: embedding); tagged: vector
+        const float* gains = nullptr;
+        float* rowp = sm.rowp();
         Epi e{};
         e.tag = c.tag;
+        e.err = p.err;
         if (last) {
             // ---- LOGITS + argmax
             if (tid == 0) trace_mark(p, 240);
-            c.tk = -1;
-            m = &p.out;
-            src = XSrc{c.tv(p.n_layers - 1, c.tl().xd), p.out_norm, p.dim};
+            m = p.out;
+            cta_rows(m.rows, r0, r1);
+            ck = rows_geo(m, DT);
+            src = kSrcResidual;
+            sv = c.acc(p.n_layers - 1, 1);
+            n = p.dim;
+            gains = sm.gains();
+            rowp = sm.res();                       // the residual is dead once staged
             e.kind = Epi::kLogits;
             e.logits = p.logits;
         } else if (k == 0) {
             // ---- QKV
-            int q0, q1;
-            cta_rows(L.qkv.rows, q0, q1);
-            if (L.qkv_bias)
-                for (int i = tid; i < q1 - q0; i += kConsumers) sm.bias()[i] = __ldg(L.qkv_bias + q0 + i);
             if (tid == 0) trace_mark(p, 10 * l);
-            c.tk = 160 + 4 * l;
-            m = &L.qkv;
-            src = XSrc{l == 0 ? nullptr : c.tv(l - 1, c.tl().xd), L.attn_norm, p.dim};
+            m = L.qkv;
+            cta_rows(m.rows, r0, r1);
+            ck = rows_geo(m, DT);
+            if (L.qkv_bias)
+                for (int i = tid; i < r1 - r0; i += kConsumers) sm.bias()[i] = __ldg(L.qkv_bias + r0 + i);
+            src = kSrcResidual;
+            sv = l == 0 ? nullptr : c.acc(l - 1, 1);
+            n = p.dim;
+            gains = sm.gains();
             e.kind = Epi::kStore;
             e.out = c.tv(l, c.tl().qkv);
             e.bias = L.qkv_bias ? sm.bias() : nullptr;
-            e.base = q0;
+            e.base = r0;
         } else if (k == 1) {
-            // ---- ATTN, then O
+            // ---- ATTN, then O (this CTA's rows of its group's columns of Wo)
             if (tid == 0) trace_mark(p, 10 * l + 2);
             const int units = p.n_kv * p.splits;
             for (int unit = blockIdx.x; unit < units; unit += G)
                 if (!attention_any(c, L, l, unit)) return false;
             if (tid == 0) trace_mark(p, 10 * l + 3);
-            if (tid == 0) trace_mark(p, 10 * l + 4);
-            c.tk = 160 + 4 * l + 1;
-            m = &L.o;
-            src = XSrc{c.tv(l, c.tl().attn), nullptr, p.q_dim};
-            e.kind = Epi::kResidual;
-            e.out = c.tv(l, c.tl().xo);
-            e.sm = sm.xown();
-            e.base = c.own0;
+            m = p.ov.m;
+            r0 = rg0;
+            r1 = rg1;
+            ck = view_geo(p.ov, pt.g);
+            src = kSrcMerged;
+            n = m.cols;
+            e.kind = Epi::kAccum;
+            e.out = c.acc(l, 0);
         } else if (k == 2) {
-            // ---- GU
+            // ---- GU (this CTA's FFN columns)
             if (tid == 0) trace_mark(p, 10 * l + 6);
-            c.tk = 160 + 4 * l + 2;
-            m = &L.gu;
-            src = XSrc{c.tv(l, c.tl().xo), L.ffn_norm, p.dim};
+            m = L.gu;
+            r0 = 2 * u0;
+            r1 = 2 * u1;
+            ck = rows_geo(m, DT);
+            src = kSrcResidual;
+            sv = c.acc(l, 0);
+            n = p.dim;
+            gains = sm.gains();
             e.kind = Epi::kSwiGLU;
             e.out = c.tv(l, c.tl().u);
             e.sm = sm.bias();
-            cta_rows(L.gu.rows, e.base, e.end);
+            e.base = u0;
+            e.end = u1;
         } else {
-            // ---- DOWN
+            // ---- DOWN (this CTA's rows of its group's columns of Wdown)
             if (tid == 0) trace_mark(p, 10 * l + 8);
-            c.tk = 160 + 4 * l + 3;
-            m = &L.down;
-            src = XSrc{c.tv(l, c.tl().u), nullptr, p.ffn};
-            e.kind = Epi::kResidual;
-            e.out = c.tv(l, c.tl().xd);
-            e.sm = sm.xown();
-            e.base = c.own0;
+            m = p.dv.m;
+            r0 = rg0;
+            r1 = rg1;
+            ck = view_geo(p.dv, pt.g);
+            src = kSrcTagged;
+            sv = c.tv(l, c.tl().u) + (size_t)pt.g * fdg;
+            n = fdg;
+            e.kind = Epi::kAccum;
+            e.out = c.acc(l, 1);
         }
-        gemv_consume<DT, false>(c, *m, src, token, e);
+        float ss = 0.f;
+        if (src == kSrcResidual) ss = stage_residual<DT>(c, sv, token, xv);
+        else if (src == kSrcTagged) stage_tagged(c, sv, n, xv);
+        else stage_merged(c, l, pt.g, xv);
+        const Lanes Ln = lane_layout<DT>(c, m);
+        XReg<DT> xr;
+        lanes_prep<DT>(c, Ln, n, gains, ss, xr);
+        gemv_consume<DT>(c, m, ck, r0, r1, Ln, xr, rowp, e);
         if (last) {
             best = e.best;
         } else {
@@ -1456,15 +1559,14 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         sm.misc()[1] = (old == (unsigned)(G - 1));
     }
     consumer_sync();
-    if (sm.misc()[1]) {
+    if (sm.misc()[1] && tid == 0) {
         // every CTA has passed its last wait: publish the argmax, re-arm the
-        // counters, and make this step's tag the last completed one
+        // counter, and make this step's tag the last completed one
         __threadfence();
-        if (tid == 0) *p.token_out = argmax_key_index(atomicExch(p.best, 0ull));
-        if (tid == 0) *p.epoch = c.tag;
-        if (tid == 0) trace_mark(p, 242);
-        const int nc = n_phase_counters(p.n_layers) + p.n_layers * p.n_kv;
-        for (int i = tid; i < nc; i += kConsumers) p.counters[i] = 0u;
+        *p.token_out = argmax_key_index(atomicExch(p.best, 0ull));
+        *p.epoch = c.tag;
+        *fin = 0u;
+        trace_mark(p, 242);
     }
     return true;
 }
@@ -1472,16 +1574,27 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
 template <int DT>
 __device__ void producer_main(const StepParams& p, Smem& sm) {
     Producer pr(p, sm);
+    const Part pt = cta_part(p.ngrp);
+    const int fdg = p.dv.m.cols;
+    int rg0, rg1, u0, u1;
+    share(p.dim, pt.j, pt.n, rg0, rg1);
+    share(fdg, pt.j, pt.n, u0, u1);
+    u0 += pt.g * fdg;
+    u1 += pt.g * fdg;
     for (int l = 0; l < p.n_layers && !pr.dead; l++) {
         const LayerDev& L = p.layers[l];
-        pr.gemv(L.qkv, DT, 256 + 8 * l);
+        int q0, q1;
+        cta_rows(L.qkv.rows, q0, q1);
+        pr.rows(L.qkv, DT, q0, q1, 256 + 8 * l);
         pr.attention(l);
-        pr.gemv(L.o, DT, 256 + 8 * l + 2);
-        pr.gemv(L.gu, DT, 256 + 8 * l + 3);
-        pr.gemv(L.down, DT, 256 + 8 * l + 4);
+        pr.view(p.ov, layer_map(p, l, 2), layer_map(p, l, 3), pt.g, rg0, rg1, 256 + 8 * l + 2);
+        pr.rows(L.gu, DT, 2 * u0, 2 * u1, 256 + 8 * l + 3);
+        pr.view(p.dv, layer_map(p, l, 4), layer_map(p, l, 5), pt.g, rg0, rg1, 256 + 8 * l + 4);
         trace_mark(p, 256 + 8 * l + 5);
     }
-    pr.gemv(p.out, DT, 448);
+    int o0, o1;
+    cta_rows(p.out.rows, o0, o1);
+    pr.rows(p.out, DT, o0, o1, 448);
     trace_mark(p, 449);
     pr.drain();   // on success every chunk was consumed and the waits return at once
 }
@@ -1545,10 +1658,53 @@ bool matrix_plan(DMat& m, int wtype, bool pair) {
     return true;
 }
 
-// Shared-memory geometry of the step kernel for a model.  Returns false if the
-// model does not fit the kernel's limits.
-bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int n_kv, int hd, int rope_dims,
-                   int rowp_floats, size_t* smem_bytes) {
+// Column-group view of a [rows x cols] matrix split into ngrp groups of
+// cols/ngrp columns, each CTA taking at most max_rows rows of its group.
+// Returns false if the groups do not fit the kernel's limits.
+bool gview_plan(GView& v, int wtype, int rows, int cols, int ngrp, int max_rows) {
+    if (cols % ngrp) return false;
+    const int gc = cols / ngrp;
+    const int es = wtype == LLM_Q8_0 ? 1 : (wtype == LLM_F16 ? 2 : 4);
+    v = GView{};
+    v.m.rows = rows;
+    v.m.cols = gc;
+    v.m.dstride = 0;
+    if (!matrix_plan(v.m, wtype, false)) return false;
+    v.U = gc % 32 == 0 ? 32 : 16 / es;
+    if (wtype == LLM_Q8_0 && gc % 32) return false;
+    if (gc % v.U || cols % v.U || gc / v.U > 256) return false;
+    v.rowq = gc * es;
+    v.rowd = 0;
+    if (wtype == LLM_Q8_0) {
+        const int cb = gc / 32;
+        int extra = 0;
+        for (int g = 0; g < ngrp; g++) extra = std::max(extra, (g * cb) % 8);
+        const int sb = (cb + extra + 7) & ~7;
+        if (sb > 256) return false;
+        v.rowd = sb * 2;
+    }
+    const int per = v.rowq + v.rowd;
+    if (max_rows < 1) max_rows = 1;
+    const int chunks = (int)(((long long)max_rows * per + (kSlotBytes - 1024) - 1) / (kSlotBytes - 1024));
+    int R = (max_rows + chunks - 1) / chunks;
+    if (R > 256) R = 256;
+    auto al128 = [](int b) { return (b + 127) & ~127; };
+    while (R > 1 && al128(R * v.rowq) + R * v.rowd > kSlotBytes) R--;
+    if (al128(R * v.rowq) + R * v.rowd > kSlotBytes) return false;
+    v.R = R;
+    v.m.rpc = R;
+    v.sboff = al128(R * v.rowq);
+    v.box_bytes = R * v.rowq + R * v.rowd;
+    return true;
+}
+
+// Shared-memory geometry of the step kernel for a model.  stage_floats: the
+// longest vector a GEMV phase stages (dim, or a group's Wo / Wdown columns);
+// rowp_floats / rowp_logits: row partials of multi-warp teams (the logits
+// phase keeps them in the residual region).  Returns false if the model does
+// not fit the kernel's limits.
+bool step_geometry(StepParams& p, int dim, int stage_floats, int n_heads, int n_kv, int hd, int rope_dims,
+                   int rowp_floats, int rowp_logits, size_t* smem_bytes) {
     const int gq = n_heads / n_kv;
     // KV rows per slot: K and V tiles of P rows fill a slot, at most 256 (a TMA
     // box side), and the unit's scores (2 * gq * P floats) stay within 8 KB
@@ -1565,24 +1721,16 @@ bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int 
     // q_s, kf, kp/vp; the scalar form adds its score buffers
     const size_t attn_scratch =
         sizeof(float) * (size_t)(GD + 2 * hd) + (p.attn_mma ? 0 : sizeof(float) * (size_t)(2 * gq * P + 4 * gq));
-    // the scratch region also stages the activation vectors of the GEMV
-    // phases: always those of length dim and q_dim, the FFN one as well when
-    // that still leaves a 192 KB ring
     auto slices = [](int n) { return (size_t)((n + 31) & ~31) * sizeof(float); };
-    const size_t stage = slices(dim > q_dim ? dim : q_dim);
     size_t xs = attn_scratch;
-    xs = xs > stage ? xs : stage;
+    xs = std::max(xs, slices(std::max(dim, stage_floats)));
     auto al = [](size_t b) { return (b + 127) & ~(size_t)127; };
-    const size_t tpart = sizeof(float) * (size_t)rowp_floats;
+    const size_t tpart = sizeof(float) * (size_t)std::max(rowp_floats, 1);
+    const size_t res = sizeof(float) * (size_t)std::max(dim, rowp_logits);
     const size_t gain_bytes = slices(dim);
-    auto fixed_for = [&](size_t x) {
-        return al(x) + al(tpart) + al(2 * 128 * 4) + al(2 * kConsumers * 4) + al(2 * kOwnFloats * 4) + al(gain_bytes) +
-               2048;                                            // barriers and flags; the ring's alignment
-    };
     if (rope_dims / 2 > 128 || GD > 2 * kConsumers || GD % 2) return false;
-    const size_t xs_ffn = xs > slices(ffn) ? xs : slices(ffn);
-    if (((long long)kMaxSmem - (long long)fixed_for(xs_ffn)) / kSlotBytes * kSlotBytes >= 196608) xs = xs_ffn;
-    const size_t fixed = fixed_for(xs);
+    const size_t fixed = al(xs) + al(tpart) + al(res) + al(2 * 128 * 4) + al(2 * kConsumers * 4) +
+                         al(2 * kOwnFloats * 4) + al(gain_bytes) + 2048;   // barriers and flags; the ring's alignment
     long long ns = ((long long)kMaxSmem - (long long)fixed) / kSlotBytes;
     if (ns > 8) ns = 8;
     if (ns < 2) return false;
@@ -1592,6 +1740,7 @@ bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int 
     p.scratch_floats = (int)(xs / sizeof(float));
     p.off_xs = (int)off; off += al(xs);
     p.off_red = (int)off; off += al(tpart);
+    p.off_res = (int)off; off += al(res);
     p.off_rope = (int)off; off += al(2 * 128 * 4);
     p.off_comb = (int)off; off += al(2 * kConsumers * 4);
     p.off_own = (int)off; off += al(2 * kOwnFloats * 4);

@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -15,9 +16,10 @@
 #include "llm_internal.cuh"
 
 namespace llm {
-bool step_geometry(StepParams& p, int dim, int q_dim, int ffn, int n_heads, int n_kv, int hd, int rope_dims,
-                   int rowp_floats, size_t* smem_bytes);
+bool step_geometry(StepParams& p, int dim, int stage_floats, int n_heads, int n_kv, int hd, int rope_dims,
+                   int rowp_floats, int rowp_logits, size_t* smem_bytes);
 bool matrix_plan(DMat& m, int wtype, bool pair);
+bool gview_plan(GView& v, int wtype, int rows, int cols, int ngrp, int max_rows);
 const void* step_kernel_ptr(int wtype);
 void launch_kv_store(cudaStream_t st, __half* kc, __half* vc, int pos, int kv_dim, const float* k, const float* v);
 void launch_dequant_rows(cudaStream_t st, int wtype, const DMat& m, int row0, int n_rows, float* out);
@@ -36,10 +38,11 @@ struct llm_handle {
     cudaStream_t st = nullptr;
     int device = 0, sms = 0;
     int q_dim = 0, kv_dim = 0, max_splits = 1;
+    int ngrp = 1;                    // column groups of the decode step's O and down products
     size_t smem = 0;
     const void* kernel = nullptr;
     StepParams geo{};                // shared-memory geometry of the step kernel
-    CUtensorMap* kv_maps = nullptr;  // device array [2 * n_layers]
+    CUtensorMap* kv_maps = nullptr;  // device array [kMapsPerLayer * n_layers]
     float theta_scale = 0.f, attn_div = 0.f;
 
     uint8_t* arena = nullptr;        // weights in the library layout
@@ -54,8 +57,12 @@ struct llm_handle {
 
     unsigned long long* tv = nullptr;  // tagged activation vectors of every layer
     size_t tv_words = 0;
+    unsigned long long* part = nullptr;  // tagged attention partials of every layer
+    size_t part_words = 0;
+    unsigned long long* delta = nullptr; // residual accumulators, two parities
+    size_t delta_words = 0;
     unsigned* epoch = nullptr;          // tag of the last completed step
-    float *logits = nullptr, *attn_part = nullptr;
+    float* logits = nullptr;
     unsigned long long* best = nullptr;
     unsigned* counters = nullptr;
     int n_counters = 0;
@@ -361,27 +368,59 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
     CKC(cudaMalloc(&h->d_layers, sizeof(LayerDev) * L));
     CKC(cudaMemcpyAsync(h->d_layers, h->layers.data(), sizeof(LayerDev) * L, cudaMemcpyHostToDevice, h->st));
 
+    // ---- column groups of the decode step: the largest divisor of n_kv up
+    // to 8 (else the smallest above) whose Wo and Wdown column blocks have
+    // whole Q8_0 blocks (rows of 16-byte words for F16/F32) and whose merged
+    // attention output fits the kernel's pairs of consumer threads
+    {
+        const int unit = c.wtype == LLM_Q8_0 ? 32 : (c.wtype == LLM_F16 ? 8 : 4);
+        auto fits = [&](int n) {
+            return c.n_kv_heads % n == 0 && q % n == 0 && f % n == 0 && (q / n) % unit == 0 && (f / n) % unit == 0 &&
+                   q / n <= 2 * kConsumers && n <= h->sms;
+        };
+        int ng = 0;
+        for (int n = 1; n <= c.n_kv_heads && n <= 8; n++)
+            if (fits(n)) ng = n;
+        for (int n = 9; !ng && n <= c.n_kv_heads; n++)
+            if (fits(n)) ng = n;
+        if (!ng)
+            return create_failed(h, fail(h, LLM_ERR_UNSUPPORTED,
+                                         "no column grouping of the output and down projections fits this shape"));
+        h->ngrp = ng;
+    }
+    const int gdg = q / h->ngrp, fdg = f / h->ngrp;
+    const int min_gsz = h->sms / h->ngrp;                      // CTAs in the smallest group
+    const int view_rows = (d + min_gsz - 1) / min_gsz;         // most rows a CTA takes of a group's columns
+    if (!gview_plan(h->geo.ov, c.wtype, d, q, h->ngrp, view_rows) ||
+        !gview_plan(h->geo.dv, c.wtype, d, f, h->ngrp, view_rows))
+        return create_failed(h, fail(h, LLM_ERR_UNSUPPORTED, "no streaming plan for the output or down projection"));
+
     // ---- activations
     // position splits per kv head: enough units to cover every SM, at most 32
-    // (the merge takes one split per lane)
+    // (the merge takes one split per lane) and at most 256 weights per group
     {
         int ms = h->sms / c.n_kv_heads;
         if (ms > 32) ms = 32;
+        const int hg = c.n_heads / h->ngrp;
+        if (ms > kOwnFloats / hg) ms = kOwnFloats / hg;
         h->max_splits = ms > 1 ? ms : 1;
     }
-    h->n_counters = n_phase_counters(L) + L * c.n_kv_heads;
+    h->n_counters = 1;
     size_t a = 0;
     auto take = [&](size_t b) { size_t o = a; a += align256(b); return o; };
     h->tv_words = (size_t)L * (size_t)tv_layout(d, q, kv, f).stride;
-    const size_t o_tv = take(h->tv_words * 8), o_epoch = take(4), o_logits = take((size_t)c.vocab * 4),
-                 o_part = take((size_t)c.n_heads * h->max_splits * (c.head_dim + 2) * 4), o_best = take(8),
+    h->part_words = (size_t)L * (size_t)part_words_per_layer(c.n_heads, h->max_splits, c.head_dim);
+    h->delta_words = (size_t)2 * L * 2 * d;
+    const size_t o_tv = take(h->tv_words * 8), o_part = take(h->part_words * 8), o_delta = take(h->delta_words * 8),
+                 o_epoch = take(4), o_logits = take((size_t)c.vocab * 4), o_best = take(8),
                  o_ctr = take((size_t)h->n_counters * 4), o_err = take(4), o_tin = take(4), o_tout = take(4);
     CKC(cudaMalloc(&h->act, a));
     CKC(cudaMemsetAsync(h->act, 0, a, h->st));
     h->tv = (unsigned long long*)(h->act + o_tv);
+    h->part = (unsigned long long*)(h->act + o_part);
+    h->delta = (unsigned long long*)(h->act + o_delta);
     h->epoch = (unsigned*)(h->act + o_epoch);
     h->logits = (float*)(h->act + o_logits);
-    h->attn_part = (float*)(h->act + o_part);
     h->best = (unsigned long long*)(h->act + o_best);
     h->counters = (unsigned*)(h->act + o_ctr);
     h->err = (int*)(h->act + o_err);
@@ -396,26 +435,28 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
     h->theta_scale = (float)pow((double)c.rope_base, -2.0 / (double)c.rope_dims);
     h->attn_div = (float)sqrt((double)c.head_dim);
     h->kernel = step_kernel_ptr(c.wtype);
-    // row partials a CTA keeps for one GEMV phase: its rows times the warps of a team
-    int rowp_floats = 0;
+    // row partials a CTA keeps for one GEMV phase (multi-warp teams): its rows
+    // times the warps of a team; the logits phase's are kept apart
+    int rowp_floats = 0, rowp_logits = 0;
     {
-        const DMat* mats[5] = {&h->layers[0].qkv, &h->layers[0].o, &h->layers[0].gu, &h->layers[0].down, &h->out};
-        for (const DMat* m : mats) {
-            const int rows = (m->rows + h->sms - 1) / h->sms * (m->pair == 2 ? 2 : 1);
-            const int parts = m->tw > 32 ? m->tw / 32 : 1;
-            if (rows * parts > rowp_floats) rowp_floats = rows * parts;
-        }
+        auto parts = [](const DMat& m) { return m.tw > 32 ? m.tw / 32 : 0; };
+        const DMat& Q = h->layers[0].qkv;
+        const DMat& GU = h->layers[0].gu;
+        rowp_floats = std::max(rowp_floats, (Q.rows + h->sms - 1) / h->sms * parts(Q));
+        rowp_floats = std::max(rowp_floats, 2 * ((fdg + min_gsz - 1) / min_gsz) * parts(GU));
+        rowp_floats = std::max(rowp_floats, view_rows * parts(h->geo.ov.m));
+        rowp_floats = std::max(rowp_floats, view_rows * parts(h->geo.dv.m));
+        rowp_logits = (h->out.rows + h->sms - 1) / h->sms * parts(h->out);
     }
-    if (!step_geometry(h->geo, d, q, f, c.n_heads, c.n_kv_heads, c.head_dim, c.rope_dims, rowp_floats,
-                       &h->smem))
+    if (!step_geometry(h->geo, d, std::max(gdg, fdg), c.n_heads, c.n_kv_heads, c.head_dim, c.rope_dims, rowp_floats,
+                       rowp_logits, &h->smem))
         return create_failed(h, fail(h, LLM_ERR_UNSUPPORTED, "the step's shared-memory layout does not fit"));
     // per-CTA shares that live in shared memory, and every matrix's plan
-    if ((d + h->sms - 1) / h->sms > kOwnFloats || (q + 2 * kv + h->sms - 1) / h->sms > kOwnFloats ||
-        2 * ((f + h->sms - 1) / h->sms) > kOwnFloats)
+    if ((q + 2 * kv + h->sms - 1) / h->sms > kOwnFloats || 2 * ((fdg + min_gsz - 1) / min_gsz) > kOwnFloats)
         return create_failed(h, fail(h, LLM_ERR_UNSUPPORTED, "a CTA's share of a vector exceeds %d floats", kOwnFloats));
     for (int l = 0; l < L; l++) {
         const LayerDev& D = h->layers[l];
-        if (!D.qkv.rpc || !D.o.rpc || !D.gu.rpc || !D.down.rpc)
+        if (!D.qkv.rpc || !D.gu.rpc)
             return create_failed(h, fail(h, LLM_ERR_UNSUPPORTED, "layer %d: no streaming plan for a matrix", l));
     }
     if (!h->embd.rpc || !h->out.rpc)
@@ -425,10 +466,12 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
     CKC(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->kernel, kBlock, h->smem));
     if (per_sm < 1) return create_failed(h, fail(h, LLM_ERR_UNSUPPORTED, "the step kernel cannot be resident"));
 
-    // 2-D tensor maps of every layer's K and V cache: [max_seq][kv_dim] F16,
+    // Tensor maps of every layer: the K and V cache ([max_seq][kv_dim] F16,
     // box [attn_rows][attn_w], read by the step kernel's TMA tile loads; the
     // tensor-core attention reads its tiles with ldmatrix, so they are
-    // swizzled by their row width (128, 64 or 32 bytes)
+    // swizzled by their row width: 128, 64 or 32 bytes), then the column-group
+    // views of Wo and Wdown (values as a 3-D view {U, cols/U, rows}, Q8_0
+    // scales as a 2-D view {dstride, rows}; rows past the end read as zero).
     {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q_res;
@@ -436,8 +479,32 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
         if (!fn || q_res != cudaDriverEntryPointSuccess)
             return create_failed(h, fail(h, LLM_ERR_CUDA, "cuTensorMapEncodeTiled is not available"));
         auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-        std::vector<CUtensorMap> maps((size_t)2 * L);
-        for (int l = 0; l < L; l++)
+        std::vector<CUtensorMap> maps((size_t)kMapsPerLayer * L);
+        memset(maps.data(), 0, sizeof(CUtensorMap) * maps.size());
+        const int es = c.wtype == LLM_Q8_0 ? 1 : (c.wtype == LLM_F16 ? 2 : 4);
+        const CUtensorMapDataType vdt = c.wtype == LLM_Q8_0 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                        : c.wtype == LLM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        auto value_view = [&](CUtensorMap* m, const DMat& w, const GView& v) {
+            cuuint64_t gdim[3] = {(cuuint64_t)v.U, (cuuint64_t)(w.cols / v.U), (cuuint64_t)w.rows};
+            cuuint64_t gstride[2] = {(cuuint64_t)v.U * es, (cuuint64_t)w.cols * es};
+            cuuint32_t box[3] = {(cuuint32_t)v.U, (cuuint32_t)(v.m.cols / v.U), (cuuint32_t)v.R};
+            cuuint32_t estride[3] = {1, 1, 1};
+            return encode(m, vdt, 3, (void*)w.q, gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        };
+        auto scale_view = [&](CUtensorMap* m, const DMat& w, const GView& v) {
+            cuuint64_t gdim[2] = {(cuuint64_t)w.dstride, (cuuint64_t)w.rows};
+            cuuint64_t gstride[1] = {(cuuint64_t)w.dstride * 2};
+            cuuint32_t box[2] = {(cuuint32_t)(v.rowd / 2), (cuuint32_t)v.R};
+            cuuint32_t estride[2] = {1, 1};
+            return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (void*)w.d, gdim, gstride, box, estride,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        };
+        for (int l = 0; l < L; l++) {
+            CUtensorMap* lm = &maps[(size_t)kMapsPerLayer * l];
             for (int which = 0; which < 2; which++) {
                 void* base = which ? (void*)h->layers[l].vc : (void*)h->layers[l].kc;
                 cuuint64_t gdim[2] = {(cuuint64_t)kv, (cuuint64_t)c.max_seq};
@@ -450,13 +517,21 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
                                                : row_bytes == 64  ? CU_TENSOR_MAP_SWIZZLE_64B
                                                : row_bytes == 32  ? CU_TENSOR_MAP_SWIZZLE_32B
                                                                   : CU_TENSOR_MAP_SWIZZLE_NONE;
-                CUresult r = encode(&maps[(size_t)2 * l + which], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, gdim,
-                                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                CUresult r = encode(&lm[which], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, gdim, gstride, box, estride,
+                                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
                 if (r != CUDA_SUCCESS)
-                    return create_failed(h, fail(h, LLM_ERR_CUDA, "cuTensorMapEncodeTiled of layer %d: error %d", l,
+                    return create_failed(h, fail(h, LLM_ERR_CUDA, "cuTensorMapEncodeTiled (KV) of layer %d: error %d", l,
                                                  (int)r));
             }
+            CUresult r = value_view(&lm[2], h->layers[l].o, h->geo.ov);
+            if (r == CUDA_SUCCESS) r = value_view(&lm[4], h->layers[l].down, h->geo.dv);
+            if (r == CUDA_SUCCESS && c.wtype == LLM_Q8_0) r = scale_view(&lm[3], h->layers[l].o, h->geo.ov);
+            if (r == CUDA_SUCCESS && c.wtype == LLM_Q8_0) r = scale_view(&lm[5], h->layers[l].down, h->geo.dv);
+            if (r != CUDA_SUCCESS)
+                return create_failed(h, fail(h, LLM_ERR_CUDA, "cuTensorMapEncodeTiled (Wo / Wdown) of layer %d: error %d",
+                                             l, (int)r));
+        }
         CKC(cudaMalloc(&h->kv_maps, sizeof(CUtensorMap) * maps.size()));
         CKC(cudaMemcpyAsync(h->kv_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice,
                             h->st));
@@ -468,7 +543,9 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
 #undef CKC
 }
 
-static int launch_step(llm_handle* h, const int* token_dev, int pos, int* argmax_dev) {
+// The step's parameters: the handle's model, layout and buffers (the
+// no-alloc step then points the working memory elsewhere).
+static StepParams step_params(const llm_handle* h, const int* token_dev, int pos, int* argmax_dev) {
     const llm_config& c = h->cfg;
     StepParams p = h->geo;
     p.layers = h->d_layers;
@@ -480,13 +557,18 @@ static int launch_step(llm_handle* h, const int* token_dev, int pos, int* argmax
     p.rope_freqs = h->rope_freqs;
     p.n_layers = c.n_layers; p.dim = c.dim; p.n_heads = c.n_heads; p.n_kv = c.n_kv_heads; p.hd = c.head_dim;
     p.ffn = c.ffn_dim; p.vocab = c.vocab; p.max_seq = c.max_seq; p.rope_dims = c.rope_dims; p.neox = c.rope_neox;
-    p.q_dim = h->q_dim; p.kv_dim = h->kv_dim;
+    p.q_dim = h->q_dim; p.kv_dim = h->kv_dim; p.ngrp = h->ngrp;
     p.eps = c.eps; p.theta_scale = h->theta_scale; p.attn_div = h->attn_div;
-    p.tv = h->tv; p.epoch = h->epoch; p.logits = h->logits; p.attn_part = h->attn_part;
+    p.tv = h->tv; p.part = h->part; p.delta = h->delta; p.epoch = h->epoch; p.logits = h->logits;
     p.max_splits = h->max_splits; p.best = h->best; p.counters = h->counters; p.err = h->err;
     p.token_in = token_dev; p.token_out = argmax_dev; p.pos = pos;
-    int s = (pos + 1 + 15) / 16;
+    const int s = (pos + 1 + 15) / 16;
     p.splits = s < 1 ? 1 : (s > h->max_splits ? h->max_splits : s);
+    return p;
+}
+
+static int launch_step(llm_handle* h, const int* token_dev, int pos, int* argmax_dev) {
+    StepParams p = step_params(h, token_dev, pos, argmax_dev);
     void* args[] = {&p};
     CK(h, cudaLaunchCooperativeKernel(h->kernel, dim3(h->sms), dim3(kBlock), args, h->smem, h->st));
     h->launches++;
@@ -499,6 +581,10 @@ static int read_device_error(llm_handle* h) {
     const int e = h->pinned->err;
     if (e & kErrTimeout) { h->broken = true; return fail(h, LLM_ERR_DEVICE_TIMEOUT, "a bounded device wait expired"); }
     if (e & kErrToken) { h->broken = true; return fail(h, LLM_ERR_OUT_OF_RANGE, "a device-side token was out of range"); }
+    if (e & kErrRange) {
+        h->broken = true;
+        return fail(h, LLM_ERR_NONFINITE, "a residual update was not finite or not below 2^15 in magnitude");
+    }
     return LLM_OK;
 }
 
@@ -509,7 +595,10 @@ extern "C" int llm_reset(llm_handle* h) {
     CK(h, cudaMemsetAsync(h->counters, 0, (size_t)h->n_counters * 4, h->st));
     CK(h, cudaMemsetAsync(h->best, 0, 8, h->st));
     // a step that stopped early may have left words with the next step's tag
+    // and accumulator words half added
     CK(h, cudaMemsetAsync(h->tv, 0, h->tv_words * 8, h->st));
+    CK(h, cudaMemsetAsync(h->part, 0, h->part_words * 8, h->st));
+    CK(h, cudaMemsetAsync(h->delta, 0, h->delta_words * 8, h->st));
     CK(h, cudaMemsetAsync(h->epoch, 0, 4, h->st));
     CK(h, cudaStreamSynchronize(h->st));
     h->broken = false;
@@ -691,6 +780,7 @@ extern "C" const char* llm_status_string(int s) {
         case LLM_ERR_NO_MEMORY: return "device allocation failed";
         case LLM_ERR_DEVICE_TIMEOUT: return "device wait timed out";
         case LLM_ERR_STATE: return "invalid handle state";
+        case LLM_ERR_NONFINITE: return "a non-finite or out-of-range value in the residual stream";
         default: return "unknown status";
     }
 }
@@ -725,18 +815,20 @@ size_t scratch_align(size_t b) { return (b + 255) & ~(size_t)255; }
 
 // Scratch layout of a handle's step: offsets in bytes, total in *bytes.
 struct ScratchLayout {
-    size_t epoch, tv, tv_bytes, part, best, counters, err, total;
+    size_t epoch, tv, tv_bytes, part, part_bytes, delta, delta_bytes, best, counters, err, total;
 };
 
 ScratchLayout scratch_layout(const llm_handle* h) {
-    const llm_config& c = h->cfg;
     ScratchLayout s{};
     size_t o = 0;
     auto take = [&](size_t b) { size_t at = o; o += scratch_align(b); return at; };
     s.epoch = take(4);                                  // shared by every handle: tags only grow
     s.tv_bytes = h->tv_words * 8;
     s.tv = take(s.tv_bytes);
-    s.part = take((size_t)c.n_heads * h->max_splits * (c.head_dim + 2) * 4);
+    s.part_bytes = h->part_words * 8;
+    s.part = take(s.part_bytes);
+    s.delta_bytes = h->delta_words * 8;
+    s.delta = take(s.delta_bytes);                      // cleared before every call
     s.best = take(8);                                   // these three must start at zero
     s.counters = take((size_t)h->n_counters * 4);
     s.err = take(4);
@@ -772,33 +864,22 @@ extern "C" int llm_decode_step_noalloc(llm_handle* h, const int32_t* token_dev, 
         }
         base = static_cast<unsigned char*>(g_scratch_addr[h->device]);
     }
-    // argmax key, grid counters and error word start at zero (contiguous)
+    // argmax key, grid counter and error word start at zero (contiguous); the
+    // residual accumulators too (another handle's steps cleared only their
+    // own layout's words)
     CK(h, cudaMemsetAsync(base + sl.best, 0, sl.err + 4 - sl.best, h->st));
+    CK(h, cudaMemsetAsync(base + sl.delta, 0, sl.delta_bytes, h->st));
 
-    const llm_config& c = h->cfg;
-    StepParams p = h->geo;
-    p.layers = h->d_layers;
-    p.kv_maps = h->kv_maps;
+    StepParams p = step_params(h, token_dev, pos, argmax_dev);
     p.trace = nullptr;
-    p.embd = h->embd;
-    p.out = h->out;
-    p.out_norm = h->out_norm;
-    p.rope_freqs = h->rope_freqs;
-    p.n_layers = c.n_layers; p.dim = c.dim; p.n_heads = c.n_heads; p.n_kv = c.n_kv_heads; p.hd = c.head_dim;
-    p.ffn = c.ffn_dim; p.vocab = c.vocab; p.max_seq = c.max_seq; p.rope_dims = c.rope_dims; p.neox = c.rope_neox;
-    p.q_dim = h->q_dim; p.kv_dim = h->kv_dim;
-    p.eps = c.eps; p.theta_scale = h->theta_scale; p.attn_div = h->attn_div;
     p.tv = reinterpret_cast<unsigned long long*>(base + sl.tv);
+    p.part = reinterpret_cast<unsigned long long*>(base + sl.part);
+    p.delta = reinterpret_cast<unsigned long long*>(base + sl.delta);
     p.epoch = reinterpret_cast<unsigned*>(base + sl.epoch);
     p.logits = logits_dev;
-    p.attn_part = reinterpret_cast<float*>(base + sl.part);
-    p.max_splits = h->max_splits;
     p.best = reinterpret_cast<unsigned long long*>(base + sl.best);
     p.counters = reinterpret_cast<unsigned*>(base + sl.counters);
     p.err = reinterpret_cast<int*>(base + sl.err);
-    p.token_in = token_dev; p.token_out = argmax_dev; p.pos = pos;
-    const int s = (pos + 1 + 15) / 16;
-    p.splits = s < 1 ? 1 : (s > h->max_splits ? h->max_splits : s);
     void* args[] = {&p};
     CK(h, cudaLaunchCooperativeKernel(h->kernel, dim3(h->sms), dim3(kBlock), args, h->smem, h->st));
     h->launches++;
@@ -808,9 +889,14 @@ extern "C" int llm_decode_step_noalloc(llm_handle* h, const int32_t* token_dev, 
     if (e) {
         // a step that stopped early may have left words with the next step's tag
         CK(h, cudaMemsetAsync(base + sl.tv, 0, sl.tv_bytes, h->st));
+        CK(h, cudaMemsetAsync(base + sl.part, 0, sl.part_bytes, h->st));
         CK(h, cudaStreamSynchronize(h->st));
     }
     if (e & kErrTimeout) { h->broken = true; return fail(h, LLM_ERR_DEVICE_TIMEOUT, "a bounded device wait expired"); }
     if (e & kErrToken) { h->broken = true; return fail(h, LLM_ERR_OUT_OF_RANGE, "the device-side token was out of range"); }
+    if (e & kErrRange) {
+        h->broken = true;
+        return fail(h, LLM_ERR_NONFINITE, "a residual update was not finite or not below 2^15 in magnitude");
+    }
     return LLM_OK;
 }

@@ -22,7 +22,7 @@ __host__ __device__ inline int max_blocks_per_thread(int wtype) { return wtype =
 constexpr int kMaxSmem = 232448;                  // 227 KB opt-in dynamic shared memory per CTA
 
 // Device error word bits (sticky until llm_reset).
-enum : int { kErrNone = 0, kErrTimeout = 1, kErrToken = 2 };
+enum : int { kErrNone = 0, kErrTimeout = 1, kErrToken = 2, kErrRange = 4 };
 
 // A weight matrix in the library's layout.  Q8_0: row r is `cols` int8 quants
 // at q + r*cols, and cols/32
@@ -42,11 +42,29 @@ struct DMat {
     int rpc, tw, teams, pair;
 };
 
+// A column-group view of a row-major matrix (Wo, Wdown in the decode step):
+// the grid is split into `ngrp` groups of CTAs and group g multiplies columns
+// [g*m.cols, (g+1)*m.cols) of the matrix (m.cols = the group's width) by its
+// own part of the input vector.  A CTA streams rows of its group's column block
+// with TMA: the values as a 3-D tensor view {U, cols/U, rows} (one box of
+// {U, m.cols/U, R} per chunk) and, for Q8_0, the scales as a 2-D view
+// {dstride, rows} (a box of {SB, R} starting at the group's first scale
+// rounded down to a multiple of 8, so the box starts on a 16-byte boundary).
+struct GView {
+    DMat m;          // streaming plan for m.cols columns (rows = the matrix's rows)
+    int R;           // rows per chunk (the boxes' height)
+    int U;           // elements in the innermost dimension of the value view
+    int rowq;        // bytes of one row of the value box (m.cols * element size)
+    int rowd;        // bytes of one row of the scale box (SB * 2), Q8_0
+    int sboff;       // byte offset of the scale box in a ring slot
+    int box_bytes;   // bytes one chunk delivers (both boxes)
+};
+
 struct LayerDev {
     DMat qkv;                 // rows: q (n_heads*hd), k (kv_dim), v (kv_dim)
-    DMat o;                   // [q_dim -> dim]
+    DMat o;                   // [q_dim -> dim], row-major (prefill, test hooks)
     DMat gu;                  // interleaved: row 2i = gate row i, row 2i+1 = up row i
-    DMat down;                // [ffn -> dim]
+    DMat down;                // [ffn -> dim], row-major (prefill, test hooks)
     const float* attn_norm;
     const float* ffn_norm;
     const float* qkv_bias;    // [q_dim + 2 kv_dim] or nullptr
@@ -54,32 +72,41 @@ struct LayerDev {
     __half* vc;
 };
 
-// Counters of one step: the logits phase, then one merge counter per
-// (layer, kv head).  All zero between steps.
+// Counters of one step: the end-of-step count only (zero between steps).
 //
 // Activation vectors that cross the grid are tagged: each element is one
 // 64-bit word, the float's bits in the low half and the step's tag in the high
 // half, written with one store.  A reader waits until the words it needs carry
 // the current tag, so the data is its own ready flag (no separate counter, no
-// release/acquire round trip).  Each layer has its own set of vectors, each
-// written exactly once per step:
-//   qkv [q_dim + 2 kv_dim], attn [q_dim], xo [dim] (residual after the
-//   attention block), u [ffn] (silu(gate) * up), xd [dim] (residual after the
-//   feed-forward block).
+// release/acquire round trip).  Each layer has its own set, each written
+// exactly once per step: qkv [q_dim + 2 kv_dim], u [ffn] (silu(gate) * up),
+// and the attention partials of every (head, split).
+//
+// The residual stream is updated through accumulator words: the O and down
+// projections of column group g add their partial sums as
+// (1 << 56) + round(v * 2^32) with red.add.u64, so a word holds the number of
+// groups that have added (top 8 bits) and the exact fixed-point sum of their
+// parts (integer addition: the same bits whatever the arrival order).  A
+// reader waits until the count equals the number of groups, then adds the sum
+// to the residual it keeps in shared memory.  Two parities (the step's tag
+// parity) of [n_layers][2][dim] words; each step clears the other parity.
 struct StepParams {
     const LayerDev* layers;
-    const void* kv_maps;      // CUtensorMap[2 * n_layers]: K and V cache of each layer, box [attn_rows][hd]
+    const void* kv_maps;      // CUtensorMap[kMapsPerLayer * n_layers]: K, V, O values, O scales, down values, down scales
+    GView ov, dv;             // column-group views of Wo and Wdown (same geometry in every layer)
     DMat embd;
     DMat out;
     const float* out_norm;
     const float* rope_freqs;  // [rope_dims/2] or nullptr
     int n_layers, dim, n_heads, n_kv, hd, ffn, vocab, max_seq, rope_dims, neox, q_dim, kv_dim;
+    int ngrp;                 // column groups (divides n_kv)
     float eps, theta_scale, attn_div;
 
     unsigned long long* tv;   // tagged vectors, n_layers sets (tv_elems_per_layer words each)
+    unsigned long long* part; // tagged attention partials, n_layers sets (part_words_per_layer each)
+    unsigned long long* delta;// residual accumulators [2][n_layers][2][dim]
     unsigned* epoch;          // tag of the last completed step; this step writes epoch + 1
     float* logits;            // [vocab]
-    float* attn_part;         // acc [n_heads][max_splits][hd], then (m, l) [n_heads][max_splits][2]
     int max_splits;
     unsigned long long* best; // packed argmax of the step
     unsigned* counters;
@@ -95,11 +122,19 @@ struct StepParams {
     int attn_rows;            // KV rows per ring slot
     int attn_mma;             // attention on tensor cores (mma.sync): head_dim in {32, 48, 64}, gq <= 4
     int attn_w;               // KV tile sub-tile width (elements): 64 when head_dim % 64 == 0 on the mma path, else head_dim
-    int off_xs, off_red, off_rope, off_comb, off_bar, off_misc, off_own, off_gain;
-    int scratch_floats;       // floats of the attention scratch region (xs)
+    int off_xs, off_red, off_res, off_rope, off_comb, off_bar, off_misc, off_own, off_gain;
+    int scratch_floats;       // floats of the staging / attention scratch region (xs)
 
     unsigned long long* trace;  // [gridDim.x][kTraceSlots] phase stamps, or nullptr (LLM_TRACE builds)
 };
+constexpr int kMapsPerLayer = 6;
+
+// Attention partials of one layer: acc [n_heads][max_splits][hd], then (m, l)
+// [n_heads][max_splits][2] (tagged words).
+__host__ __device__ inline long long part_words_per_layer(int n_heads, int max_splits, int hd) {
+    long long w = (long long)n_heads * max_splits * (hd + 2);
+    return w + (w & 1);
+}
 
 // Phase trace (compiled in with -DLLM_TRACE): per CTA, %globaltimer stamps (ns).
 //   consumer  10*l + {0..9}: start/end of QKV, ATTN, O, GU, DOWN of layer l
@@ -119,17 +154,16 @@ __host__ __device__ inline int n_phase_counters(int) { return 1; }
 
 // Tagged-vector set of one layer: element offsets of its vectors.
 struct TvLayout {
-    long long qkv, attn, xo, u, xd, stride;
+    long long qkv, u, stride;
 };
 __host__ __device__ inline TvLayout tv_layout(int dim, int q_dim, int kv_dim, int ffn) {
+    (void)dim;
     TvLayout t;
     t.qkv = 0;
-    t.attn = t.qkv + q_dim + 2LL * kv_dim;
-    t.xo = t.attn + q_dim;
-    t.u = t.xo + dim;
-    t.xd = t.u + ffn;
-    t.stride = t.xd + dim;
-    t.stride += t.stride & 1;          // 16-byte aligned sets
+    t.u = t.qkv + q_dim + 2LL * kv_dim;
+    t.u += t.u & 1;                    // 16-byte aligned vectors
+    t.stride = t.u + ffn;
+    t.stride += t.stride & 1;
     return t;
 }
 
@@ -298,6 +332,34 @@ __device__ __forceinline__ void tma_2d_g2s(void* dst, const void* tmap, int x, i
         "[%4];" ::"r"(smem_addr(dst)),
         "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar))
         : "memory");
+}
+
+// 3-D tiled tensor copy global -> shared (box of the tensor map at (x, y, z)).
+__device__ __forceinline__ void tma_3d_g2s(void* dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_addr(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Residual accumulator words: (contributions << 56) + fixed-point sum (scale
+// 2^32).  A contribution must stay below 2^15 in magnitude so that the sum of
+// up to 255 of them never reaches the count bits.
+constexpr float kAccScale = 4294967296.0f;       // 2^32
+constexpr float kAccInvScale = 2.3283064365386963e-10f;   // 2^-32
+constexpr float kAccLimit = 32768.0f;             // 2^15
+__device__ __forceinline__ void acc_add(unsigned long long* a, float v, int* err) {
+    long long fx = 0;
+    if (fabsf(v) < kAccLimit) fx = __float2ll_rn(v * kAccScale);
+    else atomicOr(err, kErrRange);                 // also NaN
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(a), "l"((1ull << 56) + (unsigned long long)fx)
+                 : "memory");
+}
+__device__ __forceinline__ unsigned acc_count(unsigned long long w) { return (unsigned)((w + (1ull << 55)) >> 56); }
+__device__ __forceinline__ float acc_value(unsigned long long w) {
+    const unsigned long long c = (w + (1ull << 55)) >> 56;
+    return __ll2float_rn((long long)(w - (c << 56))) * kAccInvScale;
 }
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
