@@ -52,6 +52,14 @@ __device__ __forceinline__ void trace_mark(const StepParams& p, int k) {
 #else
 __device__ __forceinline__ void trace_mark(const StepParams&, int) {}
 #endif
+// Fine-grained marks inside the phases of one layer (trace builds): thread
+// 0's time at step i of a phase, at slot c.fine + i (c.fine < 0: off).
+#ifdef LLM_TRACE
+#define FMARK(c, i) \
+    do { if ((c).fine >= 0 && (c).tid == 0) trace_mark((c).p, (c).fine + (i)); } while (0)
+#else
+#define FMARK(c, i) do { } while (0)
+#endif
 
 // Spin until ready() holds.  The deadline (SM cycle counter) and the error
 // word (a global load) are checked only every 256 polls, so a wait that ends
@@ -214,6 +222,7 @@ struct Producer {
     RingPos rp;
     long long it = 0;
     bool dead = false;
+    long long waited = 0;  // trace builds: SM cycles spent waiting for free slots
 
     __device__ Producer(const StepParams& p_, Smem& s_) : p(p_), sm(s_) {}
 
@@ -224,10 +233,16 @@ struct Producer {
         if (rp.count >= p.ns) {
             const uint32_t par = rp.phase ^ 1u;
             uint64_t* bar = &sm.empty()[slot];
-            if (!bounded_wait([&] { return mbar_test_wait(bar, par); }, p.err)) {
+#ifdef LLM_TRACE
+            const long long tw0 = clock64();
+#endif
+            if (!bounded_wait([&] { return mbar_sleep_wait(bar, par); }, p.err)) {
                 dead = true;
                 return nullptr;
             }
+#ifdef LLM_TRACE
+            waited += clock64() - tw0;
+#endif
         }
         return sm.ring() + (size_t)slot * kSlotBytes;
     }
@@ -235,6 +250,19 @@ struct Producer {
     __device__ __forceinline__ void issued() {
         rp.advance(p.ns);
         it++;
+    }
+
+    // trace builds: the cycles waited for free slots during the phase with
+    // producer trace slot tk (256 + 8 l + {0, 2, 3, 4}), at 896 + 4 l + j
+    __device__ __forceinline__ void note_wait(int tk) {
+#ifdef LLM_TRACE
+        if (p.trace && tk >= 256 && tk < 448) {
+            const int l = (tk - 256) / 8, k = (tk - 256) % 8;
+            const int j = k == 0 ? 0 : k - 1;
+            p.trace[(size_t)blockIdx.x * kTraceSlots + 896 + 4 * l + j] = waited;
+        }
+        waited = 0;
+#endif
     }
 
     // Rows [r0, r1) of m (single rows) as whole rows, m.rpc per chunk.
@@ -254,6 +282,7 @@ struct Producer {
             if (bd) bulk_g2s(dst + bq, reinterpret_cast<const uint8_t*>(m.d) + (size_t)r * rowd, bd, &sm.full()[slot]);
             issued();
         }
+        note_wait(tk);
     }
 
     // Rows [r0, r1) of group g's column block of a matrix, v.R rows per chunk
@@ -271,6 +300,7 @@ struct Producer {
             if (v.rowd) tma_2d_g2s(dst + v.sboff, md, sx, r, &sm.full()[slot]);
             issued();
         }
+        note_wait(tk);
     }
 
     __device__ void attention(int layer) {
@@ -296,6 +326,7 @@ struct Producer {
                 issued();
             }
         }
+        note_wait(-1);
     }
 
     __device__ void drain() {
@@ -322,6 +353,8 @@ struct Consumer {
     int tid, warp, lane;
     unsigned tag;          // this step's tag of the tagged vectors
     unsigned long long* delta;   // this step's parity of the residual accumulators
+    long long waited = 0;        // trace builds: SM cycles spent waiting for full ring slots
+    int fine = -1;               // trace builds: first slot of this phase's fine marks, or -1
 
     __device__ Consumer(const StepParams& p_, Smem& s_) : p(p_), sm(s_) {
         tid = threadIdx.x;
@@ -355,7 +388,13 @@ struct Consumer {
         slot = rp.slot;
         const uint32_t par = rp.phase;
         uint64_t* bar = &sm.full()[slot];
-        if (!bounded_wait([&] { return mbar_test_wait(bar, par); }, p.err)) sm.misc()[0] = 1;
+#ifdef LLM_TRACE
+        const long long tw0 = clock64();
+#endif
+        if (!bounded_wait([&] { return mbar_sleep_wait(bar, par); }, p.err)) sm.misc()[0] = 1;
+#ifdef LLM_TRACE
+        waited += clock64() - tw0;
+#endif
         return sm.ring() + (size_t)slot * kSlotBytes;
     }
 
@@ -366,7 +405,7 @@ struct Consumer {
     }
 
     // Start copying a norm's gains (n floats, n % 4 == 0) into shared memory;
-    // lanes_prep waits for them.  Each 16-byte word w lands at the swizzled
+    // stage_residual waits for them.  Each 16-byte word w lands at the swizzled
     // word (w & ~7) + ((w & 7) ^ ((w >> 3) & 7)), as the staged vectors do.
     __device__ void prefetch_gains(const float* g, int n) {
         float4* dst = reinterpret_cast<float4*>(sm.gains());
@@ -441,6 +480,11 @@ __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
+// An int below 2^22 in magnitude as a float, exactly: placed in the mantissa
+// of 1.5 * 2^23 by an integer add and taken out by a float subtraction (two
+// full-rate operations instead of a conversion).
+__device__ __forceinline__ float small_i2f(int a) { return __int_as_float(a + 0x4B400000) - 12582912.0f; }
+
 // sum_j qs_j X_j of one block (two 16-byte words of quants), in float: each
 // digit's sum is an exact integer below 2^21 in magnitude.
 __device__ __forceinline__ float q8_block_sum(const uint4 (&w)[2], const XReg<LLM_Q8_0>& xr) {
@@ -452,7 +496,7 @@ __device__ __forceinline__ float q8_block_sum(const uint4 (&w)[2], const XReg<LL
         a1 = dp4a_su(u[i], xr.d[1][i], a1);
         a2 = dp4a_ss(u[i], xr.d[2][i], a2);
     }
-    return fmaf(fmaf((float)a2, 256.f, (float)a1), 256.f, (float)a0);
+    return fmaf(fmaf(small_i2f(a2), 256.f, small_i2f(a1)), 256.f, small_i2f(a0));
 }
 
 // One staged group (four floats, word w of 32-element block b of the staging
@@ -565,15 +609,20 @@ __device__ __forceinline__ float lds_half(uint32_t a) {
 // N rows at once: every shared-memory word of the N rows is loaded before the
 // arithmetic starts, so the load latency is paid once.  Rows are given by
 // their shared-memory addresses (quants or values w, Q8_0 scale sc).
+// Q8_0: a lane reads its block's two 16-byte words in the order (sw, 1 - sw)
+// with sw = bit 2 of the lane, so that the eight lanes of a quarter warp,
+// whose blocks lie 32 bytes apart, touch all 32 banks once (the lane's digit
+// words are permuted the same way when they are loaded, see lanes_prep).
 template <int DT, int N>
 __device__ __forceinline__ void lane_rows(const uint32_t (&w)[N], const uint32_t (&sc)[N], const XReg<DT>& xr,
-                                          int nseg, float (&v)[N]) {
+                                          int nseg, int sw, float (&v)[N]) {
     constexpr int NS = LaneDot<DT>::kSeg;
     uint4 a[N][NS];
 #pragma unroll
     for (int r = 0; r < N; r++)
 #pragma unroll
-        for (int s = 0; s < NS; s++) a[r][s] = s < nseg ? lds128(w[r] + 16 * s) : make_uint4(0u, 0u, 0u, 0u);
+        for (int s = 0; s < NS; s++)
+            a[r][s] = s < nseg ? lds128(w[r] + 16 * (DT == LLM_Q8_0 ? (s ^ sw) : s)) : make_uint4(0u, 0u, 0u, 0u);
     if constexpr (DT == LLM_Q8_0) {
         float dq[N];
 #pragma unroll
@@ -612,7 +661,9 @@ struct Epi {
     float* logits;
     int* err;
     unsigned long long best;
+    float scale;                  // the RMSNorm scale of a normed phase (its vector is x * g), else 1
     __device__ void row(int r, float v) {
+        v *= scale;
         if (kind == kStore) {
             st_tagged(out + r, bias ? v + bias[r - base] : v, tag);
         } else if (kind == kSwiGLU) {
@@ -679,42 +730,75 @@ __device__ __forceinline__ void xreg_from_words(Word w, XReg<DT>& xr) {
 // so that the lanes' reads of their own slices fall in distinct banks.
 __device__ __forceinline__ int swz(int i) { return (i & ~7) + ((i & 7) ^ ((i >> 3) & 7)); }
 
+// One staged 4-element group (group i of the vector, valid when i < the
+// vector's groups): Q8_0 phases turn it straight into its share of its
+// 32-element block's digit record (convert_group; the block's 8 groups are
+// lanes 8j..8j+7 of one warp, so every lane of the warp calls this), the
+// others store the floats.
+template <int DT>
+__device__ __forceinline__ void stage_group(float4* xv, int i, bool valid, float4 v) {
+    if constexpr (DT == LLM_Q8_0) {
+        convert_group(xv, i >> 3, i & 7, valid, v);
+    } else {
+        if (valid) xv[swz(i)] = v;
+    }
+}
+
 // Staging sources.  Each thread stages the 4-element groups i = tid, tid +
 // kConsumers, ... (the same set in every phase, so a thread finds the
-// residual values it keeps where it left them).
+// residual values it keeps where it left them); the loops run warp by warp.
 //
 // The residual stream: x = x + (the update the block before added to the
 // accumulator words d, once all ngrp groups have added), or at layer 0 the
 // embedding row of `token` ("The Forward Pass in Java", Example 3: a copy of
-// that row).  Kept in the residual region and staged; returns the thread's
-// sum of squares of the staged values (for the RMSNorm that follows).
+// that row).  Kept in the residual region.  A normed phase stages x * g (the
+// norm's gains, fetched ahead) and leaves the norm's scale to the rows'
+// epilogue ("The Forward Pass in Java", Example 4: y = (x * scale) * g, and
+// W y = scale * W (x * g)); returns the thread's sum of squares of x.
 template <int DT>
-__device__ float stage_residual(Consumer& c, const unsigned long long* d, int token, float4* xv) {
+__device__ float stage_residual(Consumer& c, const unsigned long long* d, int token, bool norm, float4* xv) {
     const StepParams& p = c.p;
     float4* res = reinterpret_cast<float4*>(c.sm.res());
+    const float4* g4 = reinterpret_cast<const float4*>(c.sm.gains());
     const int ngr = p.dim / 4;
     float ss = 0.f;
-    for (int i = c.tid; i < ngr; i += kConsumers) {
-        float4 x;
-        if (d) {
-            const float4 u = poll_acc4(d + 4 * i, (unsigned)p.ngrp, p.err);
-            const float4 r = res[i];
-            x = make_float4(__fadd_rn(r.x, u.x), __fadd_rn(r.y, u.y), __fadd_rn(r.z, u.z), __fadd_rn(r.w, u.w));
-        } else {
-            const int e = 4 * i;
-            x = make_float4(weight_at<DT>(p.embd, token, e), weight_at<DT>(p.embd, token, e + 1),
-                            weight_at<DT>(p.embd, token, e + 2), weight_at<DT>(p.embd, token, e + 3));
+    if (norm) cp_async_wait_all();                     // this thread's part of the gains
+    for (int i0 = c.tid - c.lane; i0 < ngr; i0 += kConsumers) {
+        const int i = i0 + c.lane;
+        const bool valid = i < ngr;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid) {
+            if (d) {
+                const float4 u = poll_acc4(d + 4 * i, (unsigned)p.ngrp, p.err);
+                const float4 r = res[i];
+                x = make_float4(__fadd_rn(r.x, u.x), __fadd_rn(r.y, u.y), __fadd_rn(r.z, u.z), __fadd_rn(r.w, u.w));
+            } else {
+                const int e = 4 * i;
+                x = make_float4(weight_at<DT>(p.embd, token, e), weight_at<DT>(p.embd, token, e + 1),
+                                weight_at<DT>(p.embd, token, e + 2), weight_at<DT>(p.embd, token, e + 3));
+            }
+            res[i] = x;
+            ss += (x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w);
+            if (norm) {
+                const float4 g = g4[swz(i)];
+                x = make_float4(__fmul_rn(x.x, g.x), __fmul_rn(x.y, g.y), __fmul_rn(x.z, g.z), __fmul_rn(x.w, g.w));
+            }
         }
-        res[i] = x;
-        ss += (x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w);
-        xv[swz(i)] = x;
+        stage_group<DT>(xv, i, valid, x);
     }
     return ss;
 }
 
 // n elements (n % 4 == 0) of a tagged vector of this step.
+template <int DT>
 __device__ void stage_tagged(Consumer& c, const unsigned long long* src, int n, float4* xv) {
-    for (int i = c.tid; i < n / 4; i += kConsumers) xv[swz(i)] = poll4(src + 4 * i, c.tag, c.p.err);
+    const int ngr = n / 4;
+    for (int i0 = c.tid - c.lane; i0 < ngr; i0 += kConsumers) {
+        const int i = i0 + c.lane;
+        const bool valid = i < ngr;
+        const float4 v = valid ? poll4(src + 4 * i, c.tag, c.p.err) : make_float4(0.f, 0.f, 0.f, 0.f);
+        stage_group<DT>(xv, i, valid, v);
+    }
 }
 
 // The attention output of group g's heads, merged from the position splits'
@@ -725,6 +809,7 @@ __device__ void stage_tagged(Consumer& c, const unsigned long long* src, int n, 
 // the classes' sums are then added in class order (the same bits on every
 // CTA of the group and in every run).  A thread issues its first eight loads
 // before it waits on any of them.
+template <int DT>
 __device__ void stage_merged(Consumer& c, int layer, int g, float4* xv) {
     const StepParams& p = c.p;
     const int HG = p.n_heads / p.ngrp, hd = p.hd, S = p.splits, MS = p.max_splits;
@@ -764,6 +849,7 @@ __device__ void stage_merged(Consumer& c, int layer, int g, float4* xv) {
         }
     }
     consumer_sync();                                               // weights
+    if (c.tid == 0) trace_mark(p, 576 + 4 * layer + 2);
     float ox = 0.f, oy = 0.f;
     if (act) {
         const float* wh = wgt + hh * S;
@@ -784,52 +870,51 @@ __device__ void stage_merged(Consumer& c, int layer, int g, float4* xv) {
         comb[sg * GDG + 2 * e2 + 1] = oy;
     }
     consumer_sync();
-    for (int q = c.tid; q < GDG / 4; q += kConsumers) {
+    const int ngr = GDG / 4;
+    for (int q0 = c.tid - c.lane; q0 < ngr; q0 += kConsumers) {
+        const int q = q0 + c.lane;
+        const bool valid = q < ngr;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k = 0; k < NSG; k++) {
-            const float4 v = reinterpret_cast<const float4*>(comb + k * GDG)[q];
-            o.x += v.x;
-            o.y += v.y;
-            o.z += v.z;
-            o.w += v.w;
+        if (valid) {
+            for (int k = 0; k < NSG; k++) {
+                const float4 v = reinterpret_cast<const float4*>(comb + k * GDG)[q];
+                o.x += v.x;
+                o.y += v.y;
+                o.z += v.z;
+                o.w += v.w;
+            }
         }
-        xv[swz(q)] = o;
+        stage_group<DT>(xv, q, valid, o);
     }
 }
 
-// xr <- the lane's 32 activations of the staged vector (n elements),
-// normed first when `gains` is set ("The Forward Pass in Java", Example 4:
-// y = (x * scale) * g, scale = 1/sqrt(mean(x^2) + eps), the sum of squares a
-// float tree sum; the gains were fetched ahead with cp.async).  Each thread
-// norms the groups it staged; Q8_0 phases then turn every staged 32-element
-// block into its digit record (convert_group), again on the groups the
-// thread staged.  Every consumer thread must call this (it synchronises).
+// xr <- the lane's 32 activations of the staged vector (n elements; Q8_0: its
+// block's digit record).  A normed phase's warps first pool their sums of
+// squares (pass norm and the thread's sum ss); returns the norm's scale
+// 1/sqrt(mean(x^2) + eps) ("The Forward Pass in Java", Example 4; the sum of
+// squares a float tree sum), or 1.  Every consumer thread must call this (it
+// synchronises).
 template <int DT>
-__device__ void lanes_prep(Consumer& c, const Lanes& L, int n, const float* gains, float ss, XReg<DT>& xr) {
-    const int ngr = n / 4;
+__device__ float lanes_prep(Consumer& c, const Lanes& L, int n, bool norm, float ss, XReg<DT>& xr) {
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
     float4* xv = reinterpret_cast<float4*>(c.sm.xs());
-    if (gains) {
-        cp_async_wait_all();                         // this thread's part of the gains
-        const float tot = c.warps_total(ss);         // synchronises the consumers
-        const float scale = 1.0f / sqrtf(tot / (float)n + c.p.eps);
-        const float4* g4 = reinterpret_cast<const float4*>(gains);
-        for (int i = c.tid; i < ngr; i += kConsumers) {
-            const float4 x = xv[swz(i)], g = g4[swz(i)];
-            xv[swz(i)] = make_float4(__fmul_rn(__fmul_rn(x.x, scale), g.x), __fmul_rn(__fmul_rn(x.y, scale), g.y),
-                                     __fmul_rn(__fmul_rn(x.z, scale), g.z), __fmul_rn(__fmul_rn(x.w, scale), g.w));
-        }
+    FMARK(c, 1);
+    if (norm) {
+        const float w = warp_sum(ss);
+        if (c.lane == 0) c.sm.fred()[c.warp] = w;
+    }
+    consumer_sync();
+    FMARK(c, 4);
+    float scale = 1.0f;
+    if (norm) {
+        float tot = 0.f;
+        for (int w = 0; w < kConsumerWarps; w++) tot += c.sm.fred()[w];
+        scale = 1.0f / sqrtf(tot / (float)n + c.p.eps);
     }
     const int col0 = L.col0;
     const bool have = L.active && col0 < n;
     const int sl = col0 >> 5;
     if constexpr (DT == LLM_Q8_0) {
-        for (int i0 = c.tid - c.lane; i0 < ngr; i0 += kConsumers) {
-            const int i = i0 + c.lane;
-            const bool valid = i < ngr;
-            convert_group(xv, i >> 3, i & 7, valid, valid ? xv[swz(i)] : zero);
-        }
-        consumer_sync();
         if (have) {
             const uint4* rec = reinterpret_cast<const uint4*>(xv + sl * 8);
             const int rot = sl & 7;
@@ -840,17 +925,27 @@ __device__ void lanes_prep(Consumer& c, const Lanes& L, int n, const float* gain
                 xr.d[k][4] = b.x; xr.d[k][5] = b.y; xr.d[k][6] = b.z; xr.d[k][7] = b.w;
             }
             xr.inv = __uint_as_float(rec[6 ^ rot].x);
+            if ((c.lane >> 2) & 1) {               // the order lane_rows reads this lane's quant words in
+#pragma unroll
+                for (int k = 0; k < 3; k++)
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const uint32_t t = xr.d[k][i];
+                        xr.d[k][i] = xr.d[k][i + 4];
+                        xr.d[k][i + 4] = t;
+                    }
+            }
         } else {
 #pragma unroll
             for (int k = 0; k < 8; k++) xr.d[0][k] = xr.d[1][k] = xr.d[2][k] = 0u;
             xr.inv = 0.f;
         }
     } else {
-        consumer_sync();
         const float4* x4 = xv + sl * 8;
         const int rot = sl & 7;
         xreg_from_words<DT>([&](int k) { return have && col0 + 4 * k < n ? x4[k ^ rot] : zero; }, xr);
     }
+    return scale;
 }
 
 // Where a chunk's rows sit in its ring slot.
@@ -876,18 +971,27 @@ __device__ __forceinline__ ChunkGeo view_geo(const GView& v, int g) {
 // depend on timing) and apply the phase's epilogue.
 template <int DT>
 __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const ChunkGeo& ck, int r0, int r1,
-                                             const Lanes& L, const XReg<DT>& xr, float* rowp, Epi& epi) {
+                                             const Lanes& L, const XReg<DT>& xr, float* rowp, Epi& epi, int tk) {
     constexpr int ES = DT == LLM_Q8_0 ? 1 : (DT == LLM_F16 ? 2 : 4);
+    constexpr int RPP = RowsPerPass<DT>::value;
     const int tw = m.tw, teams = m.teams;
     const int xoff = L.col0 * ES, soff = ck.soff + L.lit * 2;
+    const int sw = DT == LLM_Q8_0 ? (c.lane >> 2) & 1 : 0;
+    const int wl = tw < 32 ? tw : 32;                 // lanes of a team within one warp
+    const int wpr = tw > 32 ? tw / 32 : 1;            // warps of a team
+    // the warp's first team decides how many passes the warp makes (every lane
+    // of a warp takes part in the shuffles of every pass)
+    const int wteam = tw <= 32 ? c.warp * (32 / tw) : c.warp / wpr;
     for (int r = r0; r < r1; r += ck.rpc) {
         const int n = min(ck.rpc, r1 - r);
         int slot;
         const uint8_t* buf = c.next_slot(slot);
+        if (r == r0 && tk >= 0 && c.tid == 0) trace_mark(c.p, tk);
+        FMARK(c, 6 + 2 * min((r - r0) / ck.rpc, 3));
         const uint8_t* sbase = buf + (ck.sfix >= 0 ? ck.sfix : n * ck.rowq);
         const uint32_t sbuf = smem_addr(buf), ssc = smem_addr(sbase);
-        if (tw <= 32) {
-            const int wteam = c.warp * (32 / tw);
+        if (wl < RPP) {
+            // teams narrower than the rows of a pass: one row per team and pass
             for (int j = 0; wteam + j * teams < n; j++) {
                 const int rr = L.team + j * teams;
                 const bool real = L.active && rr < n;
@@ -895,22 +999,22 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const C
                 float v = real ? lane_row<DT>(buf + (size_t)mrow * ck.rowq + xoff, sbase + mrow * ck.rowd + soff, xr,
                                               L.nseg)
                                : 0.f;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    if (o < tw) v += __shfl_xor_sync(0xffffffffu, v, o);
+                for (int o = wl >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
                 if (real && L.lit == 0) epi.row(r + rr, v);
             }
-        } else if (L.active) {
-            // whole-warp teams: RPP consecutive rows per pass; each warp parks
-            // its part of the rows' dots, the rows are finished after the last
-            // chunk.  A transposed butterfly reduces the RPP values at once:
-            // lanes 8k..8k+7 (RPP 4) or 16k..16k+15 (RPP 2) end with row k.
-            constexpr int RPP = RowsPerPass<DT>::value;
-            const int wpr = tw / 32, wi = c.warp % wpr;
-            float* rp = rowp + (size_t)(r - r0) * wpr + wi;
+        } else {
+            // RPP consecutive rows per team and pass.  A transposed butterfly
+            // over the team's wl lanes reduces the RPP values at once: the
+            // first step (distance wl/2) halves the values a lane carries, the
+            // second (RPP 4, distance wl/4) halves them again, the rest are
+            // plain; lane t of the team ends with row k = its bits at wl/2
+            // (and wl/4).  Whole-warp teams of several warps park each warp's
+            // part and finish the rows after the last chunk.
+            const int h = wl >> 1, q = wl >> 2;
+            float* rp = rowp + (size_t)(r - r0) * wpr + (tw > 32 ? c.warp % wpr : 0);
             for (int j = 0;; j++) {
+                if ((wteam + j * teams) * RPP >= n) break;
                 const int rbase = (L.team + j * teams) * RPP;
-                if (rbase >= n) break;
                 uint32_t wq[RPP], ws[RPP];
 #pragma unroll
                 for (int k = 0; k < RPP; k++) {
@@ -919,33 +1023,38 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const C
                     ws[k] = ssc + (uint32_t)(mr * ck.rowd + soff);
                 }
                 float v[RPP];
-                lane_rows<DT, RPP>(wq, ws, xr, L.nseg, v);
+                lane_rows<DT, RPP>(wq, ws, xr, L.active && rbase < n ? L.nseg : 0, sw, v);
                 float keep;
+                int k, lo;
                 if constexpr (RPP == 4) {
-                    const bool u16 = (c.lane & 16) != 0;
-                    const float a0 = (u16 ? v[2] : v[0]) + __shfl_xor_sync(0xffffffffu, u16 ? v[0] : v[2], 16);
-                    const float a1 = (u16 ? v[3] : v[1]) + __shfl_xor_sync(0xffffffffu, u16 ? v[1] : v[3], 16);
-                    const bool u8 = (c.lane & 8) != 0;
-                    keep = (u8 ? a1 : a0) + __shfl_xor_sync(0xffffffffu, u8 ? a0 : a1, 8);
-#pragma unroll
-                    for (int o = 4; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+                    const bool u1 = (c.lane & h) != 0;
+                    const float a0 = (u1 ? v[2] : v[0]) + __shfl_xor_sync(0xffffffffu, u1 ? v[0] : v[2], h);
+                    const float a1 = (u1 ? v[3] : v[1]) + __shfl_xor_sync(0xffffffffu, u1 ? v[1] : v[3], h);
+                    const bool u2 = (c.lane & q) != 0;
+                    keep = (u2 ? a1 : a0) + __shfl_xor_sync(0xffffffffu, u2 ? a0 : a1, q);
+                    for (int o = q >> 1; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+                    k = (u1 ? 2 : 0) + (u2 ? 1 : 0);
+                    lo = q;
                 } else {
-                    keep = c.lane < 16 ? v[0] : v[1];
-                    keep += __shfl_xor_sync(0xffffffffu, c.lane < 16 ? v[1] : v[0], 16);
-#pragma unroll
-                    for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+                    const bool u1 = (c.lane & h) != 0;
+                    keep = (u1 ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, u1 ? v[0] : v[1], h);
+                    for (int o = h >> 1; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+                    k = u1 ? 1 : 0;
+                    lo = h;
                 }
-                constexpr int G = 32 / RPP;                    // lanes holding one row's sum
-                const int k = RPP == 4 ? (c.lane >> 4) * 2 + ((c.lane >> 3) & 1) : c.lane >> 4;
-                if ((c.lane & (G - 1)) == 0 && rbase + k < n) rp[(rbase + k) * wpr] = keep;
+                if ((c.lane & (lo - 1)) == 0 && L.active && rbase + k < n) {
+                    if (tw > 32) rp[(rbase + k) * wpr] = keep;
+                    else epi.row(r + rbase + k, keep);
+                }
             }
         }
         c.release(slot);
+        FMARK(c, 7 + 2 * min((r - r0) / ck.rpc, 3));
     }
     if (tw > 32) {
         // finish every row: the warps' parts added in warp order
-        const int wpr = tw / 32;
         consumer_sync();
+        FMARK(c, 14);
         for (int i = c.tid; i < r1 - r0; i += kConsumers) {
             float t = 0.f;
             for (int k = 0; k < wpr; k++) t += rowp[i * wpr + k];
@@ -956,6 +1065,11 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const C
     // the next phase's staging must not overwrite what a warp still reads
     // (the gains, the (gate, up) sums, the row partials)
     consumer_sync();
+    FMARK(c, 15);
+#ifdef LLM_TRACE
+    if (c.tid == 0 && tk >= 0 && c.p.trace) c.p.trace[(size_t)blockIdx.x * kTraceSlots + tk - 160 + 768] = c.waited;
+    c.waited = 0;
+#endif
 }
 
 // ------------------------------------------------------------------ RoPE --
@@ -1524,14 +1638,21 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
             e.kind = Epi::kAccum;
             e.out = c.acc(l, 1);
         }
+#ifdef LLM_TRACE
+        c.fine = !last && l == 8 ? 960 + 16 * k : -1;
+#endif
+        FMARK(c, 0);
         float ss = 0.f;
-        if (src == kSrcResidual) ss = stage_residual<DT>(c, sv, token, xv);
-        else if (src == kSrcTagged) stage_tagged(c, sv, n, xv);
-        else stage_merged(c, l, pt.g, xv);
+        if (src == kSrcResidual) ss = stage_residual<DT>(c, sv, token, gains != nullptr, xv);
+        else if (src == kSrcTagged) stage_tagged<DT>(c, sv, n, xv);
+        else stage_merged<DT>(c, l, pt.g, xv);
         const Lanes Ln = lane_layout<DT>(c, m);
         XReg<DT> xr;
-        lanes_prep<DT>(c, Ln, n, gains, ss, xr);
-        gemv_consume<DT>(c, m, ck, r0, r1, Ln, xr, rowp, e);
+        e.scale = lanes_prep<DT>(c, Ln, n, gains != nullptr, ss, xr);
+        FMARK(c, 5);
+        const int jt = last ? -1 : k;                               // trace: QKV 0, O 1, GU 2, DOWN 3
+        if (tid == 0 && jt >= 0) trace_mark(p, 512 + 4 * l + jt);
+        gemv_consume<DT>(c, m, ck, r0, r1, Ln, xr, rowp, e, jt >= 0 ? 160 + 4 * l + jt : -1);
         if (last) {
             best = e.best;
         } else {
@@ -1641,7 +1762,8 @@ bool matrix_plan(DMat& m, int wtype, bool pair) {
     int teams, rows_per_pass;
     if (tw <= 32) {
         teams = kConsumerWarps * (32 / tw);
-        rows_per_pass = teams;
+        const int rpp = wtype == LLM_Q8_0 ? RowsPerPass<LLM_Q8_0>::value : 2;
+        rows_per_pass = tw >= rpp ? teams * rpp : teams;
     } else {
         if (tw / 32 > kConsumerWarps) return false;
         teams = kConsumerWarps / (tw / 32);

@@ -264,6 +264,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Wait for a phase with the thread suspended (up to about 1 us per call) until
+// the phase completes: a waiting warp then takes no issue slots from the
+// warps that share its SM sub-partition.
+__device__ __forceinline__ bool mbar_sleep_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(1000u)
+        : "memory");
+    return ok != 0;
+}
+
 // Non-blocking probe of a phase: never suspends the thread, so a spin on it
 // sees the phase complete as soon as it does.
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
@@ -347,19 +362,34 @@ __device__ __forceinline__ void tma_3d_g2s(void* dst, const void* tmap, int x, i
 // 2^32).  A contribution must stay below 2^15 in magnitude so that the sum of
 // up to 255 of them never reaches the count bits.
 constexpr float kAccScale = 4294967296.0f;       // 2^32
-constexpr float kAccInvScale = 2.3283064365386963e-10f;   // 2^-32
 constexpr float kAccLimit = 32768.0f;             // 2^15
+// round(v * 2^32) as a 64-bit integer for |v| < 2^15, in 32-bit operations
+// (64-bit conversions run on the FP64 pipe, which is slow on this part): the
+// scaled value is an exact float; below 2^31 it rounds to an int32, above it
+// is already an integer and splits exactly into 2^16 * q + rem.
+__device__ __forceinline__ long long acc_fixed(float v) {
+    const float t = v * kAccScale;
+    if (fabsf(t) < 2147483648.0f) return (long long)__float2int_rn(t);
+    const int q = __float2int_rz(t * 1.52587890625e-05f);         // t / 2^16, truncated
+    const float rem = fmaf(-(float)q, 65536.0f, t);                // exact
+    return (long long)q * 65536 + (long long)__float2int_rn(rem);
+}
 __device__ __forceinline__ void acc_add(unsigned long long* a, float v, int* err) {
     long long fx = 0;
-    if (fabsf(v) < kAccLimit) fx = __float2ll_rn(v * kAccScale);
+    if (fabsf(v) < kAccLimit) fx = acc_fixed(v);
     else atomicOr(err, kErrRange);                 // also NaN
     asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(a), "l"((1ull << 56) + (unsigned long long)fx)
                  : "memory");
 }
 __device__ __forceinline__ unsigned acc_count(unsigned long long w) { return (unsigned)((w + (1ull << 55)) >> 56); }
+// The word's sum times 2^-32 as a float: magnitude split into 32-bit halves
+// (each converted exactly or rounded once, then one fused multiply-add).
 __device__ __forceinline__ float acc_value(unsigned long long w) {
     const unsigned long long c = (w + (1ull << 55)) >> 56;
-    return __ll2float_rn((long long)(w - (c << 56))) * kAccInvScale;
+    const long long v = (long long)(w - (c << 56));
+    const unsigned long long a = v < 0 ? (unsigned long long)(-v) : (unsigned long long)v;
+    const float f = __fadd_rn(__uint2float_rn((unsigned)(a >> 32)), __uint2float_rn((unsigned)a) * 2.3283064365386963e-10f);
+    return v < 0 ? -f : f;
 }
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
