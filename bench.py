@@ -37,6 +37,10 @@ import synth  # noqa: E402
 METRIC = "decode tok/s @batch1 (Llama-3.2-1B-shape Q8_0, ctx 4k); % HBM roofline"
 POS = 4095
 CFG = synth.LLAMA1B_Q8
+# decode workloads: (model, label); the headline is the 1B shape at pos 4095
+DECODE_MODELS = {"llama1b_q8": (synth.LLAMA1B_Q8, "llama-3.2-1b-shape q8_0"),
+                 "llama7b_q8": (synth.LLAMA7B_Q8, "llama-2-7b-shape q8_0")}
+DTYPE = "q8_0 weights x 24-bit block fixed-point activations (dp4a), f32 accumulate"
 KERNEL_SOURCES = ["llama_decode_forward_gb300/csrc/decode_step.cu", "llama_decode_forward_gb300/csrc/llm_internal.cuh"]
 
 
@@ -161,22 +165,30 @@ def job_throughput(world: int, steps: int, seconds: float) -> float:
 
 
 # --------------------------------------------------------- CPU baseline --
-def cpu_oracle_sample(W, tok: int, budget_s: float = 12.0, min_steps: int = 1, max_steps: int | None = None):
-    """The oracle (single thread) on the same workload: decode steps at pos
-    4095 after the same 4095 pre-filled rows, as many as fit in the budget."""
+def cpu_oracle_sample(W, tok: int, budget_s: float = 12.0, min_steps: int = 1, max_steps: int | None = None,
+                      cfg=None, pos: int = POS, threads: int = 1):
+    """The oracle on the same workload: decode steps at `pos` after the same
+    pre-filled rows, as many as fit in the budget; on one thread, or with
+    `threads` > 1 its row-split variant (bitwise the same results)."""
     import oracle
-    ora = oracle.OracleModel(CFG, W, max_seq=POS + 1)
-    for l in range(CFG.n_layers):
+    cfg = cfg or CFG
+    ora = oracle.OracleModel(cfg, W, max_seq=pos + 1)
+    for l in range(cfg.n_layers):
         for which in (0, 1):
-            ora.set_kv_rows_f16(l, which, synth.kv_rows(CFG, l, which, POS))
-    n, t0 = 0, time.perf_counter()
-    while True:
-        ora.forward(tok, POS)
-        n += 1
-        el = time.perf_counter() - t0
-        if (n >= min_steps and el >= budget_s) or (max_steps and n >= max_steps):
-            break
-    ora.close()
+            if pos:
+                ora.set_kv_rows_f16(l, which, synth.kv_rows(cfg, l, which, pos))
+    oracle.set_threads(threads)
+    try:
+        n, t0 = 0, time.perf_counter()
+        while True:
+            ora.forward(tok, pos)
+            n += 1
+            el = time.perf_counter() - t0
+            if (n >= min_steps and el >= budget_s) or (max_steps and n >= max_steps):
+                break
+    finally:
+        oracle.set_threads(1)
+        ora.close()
     return n, el
 
 
@@ -194,7 +206,8 @@ def run_reference(args):
     v = n / el
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": args.gpus, "steps": n,
             "warmup": warm, "ms_per_step": 1000.0 * el / n, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random Q8_0 weights and KV rows)",
+            "vs_baseline": None, "dtype": "q8_0 weights x f32 activations, f32 accumulate",
+            "data": "synthetic (seeded random Q8_0 weights and KV rows)",
             "config": {"workload": "llama-3.2-1b-shape q8_0 decode, batch 1, step at pos 4095 (ctx 4096)",
                        "pos": POS, "implementation": "CPU oracle (plain C, single thread)"},
             "cpu_baseline": {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle",
@@ -205,6 +218,13 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- ours --
+def percentiles(xs) -> dict:
+    """Median and the 10th / 90th percentiles of per-launch times (ms)."""
+    a = np.sort(np.asarray(xs, dtype=np.float64))
+    q = lambda f: float(np.quantile(a, f))
+    return {"median": q(0.5), "p10": q(0.1), "p90": q(0.9), "n": int(a.size)}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -218,22 +238,27 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.cuda.current_device()
 
-    W = synth.make_weights(CFG)
+    cfg, label = DECODE_MODELS[args.model]
+    pos = POS if args.pos is None else args.pos
+    headline = args.model == "llama1b_q8" and pos == POS
+    cfg = cfg.scaled(max_seq=max(cfg.max_seq if headline else 0, pos + 1))
+    W = synth.make_weights(cfg)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
-        dec = L.Decoder(CFG, W, stream=stream.cuda_stream)
-        for l in range(CFG.n_layers):
+        dec = L.Decoder(cfg, W, stream=stream.cuda_stream)
+        for l in range(cfg.n_layers):
             k, v = dec.kv_tensors(l)
             for which, t in ((0, k), (1, v)):
-                rows = synth.kv_rows(CFG, l, which, POS)
-                t[:POS].copy_(torch.from_numpy(rows.view(np.int16)).to("cuda"))
+                if pos:
+                    rows = synth.kv_rows(cfg, l, which, pos)
+                    t[:pos].copy_(torch.from_numpy(rows.view(np.int16)).to("cuda"))
     torch.cuda.synchronize()
-    tok = int(synth.prompt(CFG, 1)[0])
+    tok = int(synth.prompt(cfg, 1)[0])
     token_dev = torch.tensor([tok], dtype=torch.int32, device="cuda")
     argmax_dev = torch.zeros(1, dtype=torch.int32, device="cuda")
 
     def step():
-        L.llm_decode_step_async(dec.h, token_dev, POS, argmax_dev)
+        L.llm_decode_step_async(dec.h, token_dev, pos, argmax_dev)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -270,46 +295,57 @@ def run_ours(args):
     value = job_throughput(world, args.steps, total_ms / 1000.0)
 
     # end to end through the synchronous C-ABI call, pinned host buffers
-    logits_pin = torch.empty(CFG.vocab, dtype=torch.float32, pin_memory=True)
+    logits_pin = torch.empty(cfg.vocab, dtype=torch.float32, pin_memory=True)
     logits_np = logits_pin.numpy()
     for _ in range(max(args.warmup, 3)):
-        L.llm_decode_step(dec.h, tok, POS, logits_np)
+        L.llm_decode_step(dec.h, tok, pos, logits_np)
     if world > 1:
         dist.barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        L.llm_decode_step(dec.h, tok, POS, logits_np)
+        L.llm_decode_step(dec.h, tok, pos, logits_np)
     e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, world, "cuda")
     e2e = job_throughput(world, args.steps, e2e_s)
 
-    nbytes = algorithmic_bytes(CFG, POS)
+    nbytes = algorithmic_bytes(cfg, pos)
     kern_ms = statistics.mean(per_launch)
     peaks = measured_peaks()
     achieved = nbytes / (kern_ms / 1000.0) / 1e9
-    traffic = stored_traffic()
+    traffic = stored_traffic() if headline else None
+    pct = percentiles(per_launch)
     line = {
-        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if headline else f"decode tok/s @batch1 ({label}, step at pos {pos}); % HBM roofline",
+        "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
         "data": "synthetic (seeded random Q8_0 weights and KV rows)",
-        "config": {"workload": "llama-3.2-1b-shape q8_0 decode, batch 1, step at pos 4095 (ctx 4096)",
-                   "n_layers": CFG.n_layers, "dim": CFG.dim, "vocab": CFG.vocab, "pos": POS,
-                   "bytes_per_step": nbytes, "l2": "working set 1.45 GB > 129 MB L2; no flush",
+        "config": {"workload": f"{label} decode, batch 1, step at pos {pos} (ctx {pos + 1})",
+                   "n_layers": cfg.n_layers, "dim": cfg.dim, "vocab": cfg.vocab, "pos": pos,
+                   "bytes_per_step": nbytes,
+                   "l2": f"working set {nbytes / 1e9:.2f} GB > 129 MB L2; no flush",
                    "parallelism": f"replicas x{world}"},
+        "launch_ms": pct,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "kernel": "decode_step_kernel<Q8_0> (whole step, one launch)",
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
-                     "frac_of_8tbs_nominal": achieved / 8000.0},
-        "e2e": {"value": e2e, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4 + 4 + 4 * CFG.vocab},
+                     "frac_of_8tbs_nominal": achieved / 8000.0,
+                     "frac_at_median_launch": nbytes / (pct["median"] / 1000.0) / 1e9 / peaks["hbm_gbs"]},
+        "e2e": {"value": e2e, "unit": "tok/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4 + 4 + 4 * cfg.vocab},
         "gpu_launches": launches,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        n, el = cpu_oracle_sample(W, tok, budget_s=args.cpu_budget)
+        n, el = cpu_oracle_sample(W, tok, budget_s=args.cpu_budget, cfg=cfg, pos=pos)
         line["cpu_baseline"] = {"value": n / el, "unit": "tok/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{n} full decode steps at pos 4095 of the same model, 1 thread, {el:.1f} s"}
+                                "sample": f"{n} full decode steps at pos {pos} of the same model, 1 thread, {el:.1f} s"}
+        cores = os.cpu_count() or 1
+        n, el = cpu_oracle_sample(W, tok, budget_s=args.cpu_budget, cfg=cfg, pos=pos, threads=cores)
+        line["cpu_baseline_all_cores"] = {
+            "value": n / el, "unit": "tok/s", "cores": cores, "kind": "oracle (row-split over the host cores)",
+            "sample": f"{n} full decode steps at pos {pos} of the same model, {cores} threads, {el:.1f} s "
+                      "(each output element computed by one thread: bitwise the single-thread result)"}
     dec.close()
     if world > 1:
         dist.barrier()
@@ -390,6 +426,10 @@ def main():
                     help="decode (the headline line) or the optional batched-prefill line")
     ap.add_argument("--prefill-weights", choices=sorted(PREFILL_CFGS), default="f16",
                     help="weight type of the prefill line's model")
+    ap.add_argument("--model", choices=sorted(DECODE_MODELS), default="llama1b_q8",
+                    help="decode workload's model: the Llama-3.2-1B shape (the headline) or the Llama-2-7B shape")
+    ap.add_argument("--pos", type=int, default=None,
+                    help="position of the timed decode step (rows 0..pos-1 pre-filled); default 4095")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

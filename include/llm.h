@@ -149,8 +149,11 @@ int llm_prefill(llm_handle *h, const int32_t *tokens_host, int32_t n, int32_t po
  * enqueued steps (DEVICE_TIMEOUT, OUT_OF_RANGE) or CUDA. */
 int llm_sync(llm_handle *h);
 
-/* DEVICE pointer to the logits of the latest step (vocab floats); valid until
- * the next step on the handle and the handle's destruction. */
+/* DEVICE pointer to the handle's logits buffer (vocab floats): the logits of
+ * the latest llm_decode_step / llm_decode_step_async / llm_generate /
+ * llm_prefill on the handle; llm_decode_step_noalloc writes the caller's
+ * buffer instead and leaves this one untouched.  Valid until the next step on
+ * the handle and the handle's destruction. */
 const float *llm_logits_device(const llm_handle *h);
 
 /* The handle's model shape (the llm_config it was created with; for a handle
@@ -176,6 +179,24 @@ int llm_test_kv_store(llm_handle *h, int layer, int32_t pos, const float *k_dev,
  * 4 w_gate, 5 w_up, 6 w_down (of `layer`), 7 tok_embd, 8 output.  Synchronous. */
 int llm_test_dequant_rows(llm_handle *h, int which, int layer, int32_t row0, int32_t n_rows, float *out_dev);
 
+/* Test hook: one matrix-vector product of the decode step on a given input,
+ * run by the step's own device code (activation staging — for Q8_0 the
+ * per-32-element fixed-point digit records —, the shared-memory weight ring
+ * and the row reduction), so that its arithmetic can be checked element by
+ * element.  which: 0 [wq;wk;wv] of `layer` (x_dev: dim floats; y_dev:
+ * n_heads*head_dim + 2*n_kv_heads*head_dim), 1 wo (x_dev: n_heads*head_dim;
+ * y_dev: llm_column_groups(h) * dim floats, group g's partial product over
+ * its columns [g*c, (g+1)*c), c = n_heads*head_dim/groups, at g*dim), 2 the
+ * interleaved gate/up rows (x_dev: dim; y_dev: 2*ffn_dim, row 2i gate i,
+ * row 2i+1 up i), 3 w_down (x_dev: ffn_dim; y_dev: groups * dim, as for wo),
+ * 4 the logits matrix (x_dev: dim; y_dev: vocab).  DEVICE F32 buffers.
+ * Synchronous.  Errors: INVALID_ARG, OUT_OF_RANGE (layer), STATE, CUDA. */
+int llm_test_gemv(llm_handle *h, int which, int layer, const float *x_dev, float *y_dev);
+
+/* The number of column groups the decode step splits the output and down
+ * projections into (a divisor of n_kv_heads), or INVALID_ARG for NULL. */
+int llm_column_groups(const llm_handle *h);
+
 /* Phase trace of the last decode step: copies sms * 1024 %globaltimer stamps
  * (nanoseconds, uint64, per CTA: the start and end of every phase of every
  * layer, as laid out in the library's trace table) to `host` (HOST, caller
@@ -184,18 +205,20 @@ int llm_test_dequant_rows(llm_handle *h, int which, int layer, int32_t row0, int
 int llm_trace_read(llm_handle *h, uint64_t *host, int32_t *sms);
 
 /* One decode step like llm_decode_step_async, but its working memory (the
- * tagged activation vectors of every layer, attention partials, grid
- * counters, argmax and error words) lives in a fixed 16 MiB device array inside the
- * library rather than in buffers of the handle, so the call allocates no
- * memory of any kind.  The described decode pass has no counterpart of this
+ * tagged activation vectors and attention partials of every layer, the
+ * residual accumulators, the grid counter, argmax and error words) lives in
+ * a fixed 16 MiB device array inside the library rather than in buffers of
+ * the handle, so the call allocates no memory of any kind.  The described decode pass has no counterpart of this
  * call: it exists for callers that may not allocate device memory while
  * serving (a process whose remaining device memory is owned by its own pool
  * and cannot grow after start-up).
  *   token_dev   DEVICE int32, the input token (read by the kernel).
  *   pos         position of the token, in [0, max_seq).
- *   logits_dev  DEVICE float[vocab], written with the step's logits.
+ *   logits_dev  DEVICE float[vocab], written with the step's logits (the
+ *               handle's own logits buffer, llm_logits_device, is untouched).
  *   argmax_dev  DEVICE int32, written with the first index of the max logit.
- * The handle's KV cache row `pos` is written as by llm_decode_step.
+ * The handle's KV cache row `pos` is written as by llm_decode_step, and the
+ * step computes the same bits as llm_decode_step (the same kernel).
  * Synchronous: returns after the step has finished on the handle's stream.
  * Errors: LLM_ERR_INVALID_ARG for NULL pointers, LLM_ERR_OUT_OF_RANGE for a
  * bad pos (or a device-side token out of range, after which the handle needs

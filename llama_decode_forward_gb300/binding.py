@@ -63,6 +63,8 @@ _SIGS = {
     "llm_kv_view": ([_vp, _int, ctypes.POINTER(_vp), ctypes.POINTER(_vp)], _int),
     "llm_test_kv_store": ([_vp, _int, _i32, _vp, _vp], _int),
     "llm_test_dequant_rows": ([_vp, _int, _int, _i32, _i32, _vp], _int),
+    "llm_test_gemv": ([_vp, _int, _int, _vp, _vp], _int),
+    "llm_column_groups": ([_vp], _int),
     "llm_trace_read": ([_vp, _vp, ctypes.POINTER(_i32)], _int),
     "llm_decode_step_noalloc": ([_vp, _vp, _i32, _vp, _vp], _int),
     "llm_launch_count": ([_vp], ctypes.c_int64),
@@ -205,6 +207,14 @@ def llm_test_kv_store(h, layer: int, pos: int, k_dev, v_dev):
 
 def llm_test_dequant_rows(h, which: int, layer: int, row0: int, n_rows: int, out_dev):
     _check(_lib.llm_test_dequant_rows(h, which, layer, row0, n_rows, _ptr(out_dev)), h)
+
+
+def llm_test_gemv(h, which: int, layer: int, x_dev, y_dev):
+    _check(_lib.llm_test_gemv(h, which, layer, _ptr(x_dev), _ptr(y_dev)), h)
+
+
+def llm_column_groups(h) -> int:
+    return int(_lib.llm_column_groups(h))
 
 
 def llm_decode_step_noalloc(h, token_dev, pos: int, logits_dev, argmax_dev):

@@ -43,6 +43,19 @@ def up_to_date(lib: str = LIB) -> bool:
     return all(os.path.getmtime(s) <= t for s in _inputs())
 
 
+def compile_command(src: str, obj: str, trace: bool = False, verbose: bool = False) -> list[str]:
+    """The nvcc command that compiles one source for sm_103a."""
+    cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *(["-DLLM_TRACE"] if trace else []), "-c", src, "-o", obj]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    return cmd
+
+
+def link_command(objs: list[str], out: str) -> list[str]:
+    """The nvcc command that links the objects into the shared library."""
+    return [_nvcc(), *ARCH, "-shared", "-o", out, *objs]
+
+
 def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
     """Compile every .cu under csrc/ (in parallel) and link the shared library
     (with trace=True, the phase-trace variant)."""
@@ -50,14 +63,10 @@ def build(force: bool = False, verbose: bool = False, trace: bool = False) -> st
     if not force and up_to_date(lib):
         return lib
     os.makedirs(out_dir, exist_ok=True)
-    nvcc = _nvcc()
-    defs = ["-DLLM_TRACE"] if trace else []
 
     def compile_one(src):
         obj = os.path.join(out_dir, os.path.splitext(os.path.basename(src))[0] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *defs, "-c", src, "-o", obj]
-        if verbose:
-            cmd.insert(1, "-Xptxas=-v")
+        cmd = compile_command(src, obj, trace, verbose)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -68,7 +77,7 @@ def build(force: bool = False, verbose: bool = False, trace: bool = False) -> st
     with ThreadPoolExecutor(max_workers=min(8, len(sources()))) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = lib + f".tmp{os.getpid()}"
-    r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+    r = subprocess.run(link_command(objs, tmp), capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, lib)

@@ -1894,6 +1894,88 @@ __global__ void dequant_rows_kernel(DMat m, int row0, int n_rows, float* out) {
         out[e] = weight_at<DT>(m, row0 + (int)(e / m.cols), (int)(e % m.cols));
 }
 
+// The decode step's GEMV on a given vector: the same staging (digit records
+// for Q8_0), lane registers, ring and gemv_consume as the step, with the
+// matrix chosen by `which` (0 QKV, 1 Wo by column groups, 2 gate/up, 3 Wdown
+// by column groups, 4 the logits matrix).  x: the product's input vector (F32);
+// y: its rows, or for 1 and 3 [ngrp][dim] the column groups' partial
+// products.  No grid-wide dependency: every CTA computes its own rows.
+template <int DT>
+__global__ void __launch_bounds__(kBlock, 1) gemv_test_kernel(const __grid_constant__ StepParams p, int which,
+                                                              int layer, const float* x, float* y) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    Smem sm(reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023), p);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.ns; i++) {
+            mbar_init(&sm.full()[i], 1);
+            mbar_init(&sm.empty()[i], kConsumerWarps);
+        }
+        sm.misc()[0] = 0;
+        sm.misc()[1] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const LayerDev& L = p.layers[layer];
+    const Part pt = cta_part(p.ngrp);
+    const GView* v = which == 1 ? &p.ov : which == 3 ? &p.dv : nullptr;
+    const DMat& m = v ? v->m : which == 0 ? L.qkv : which == 2 ? L.gu : p.out;
+    int r0, r1, n;
+    const float* xs = x;
+    float* ys = y;
+    if (v) {
+        share(p.dim, pt.j, pt.n, r0, r1);
+        n = m.cols;
+        xs = x + (size_t)pt.g * n;
+        ys = y + (size_t)pt.g * p.dim;
+    } else {
+        cta_rows(m.rows, r0, r1);
+        if (which == 2) { r0 *= 2; r1 *= 2; }   // gate/up: super-rows, streamed as single rows
+        n = p.dim;
+    }
+    if (threadIdx.x >= kConsumers) {
+        if (threadIdx.x == kConsumers) {
+            Producer pr(p, sm);
+            if (v) pr.view(*v, layer_map(p, layer, which == 1 ? 2 : 4), layer_map(p, layer, which == 1 ? 3 : 5), pt.g, r0,
+                           r1, -1);
+            else pr.rows(m, DT, r0, r1, -1);
+            pr.drain();
+        }
+        __syncwarp();
+    } else {
+        Consumer c(p, sm);
+        float4* xv = reinterpret_cast<float4*>(sm.xs());
+        const int ngr = n / 4;
+        for (int i0 = c.tid - c.lane; i0 < ngr; i0 += kConsumers) {
+            const int i = i0 + c.lane;
+            const bool valid = i < ngr;
+            stage_group<DT>(xv, i, valid,
+                            valid ? reinterpret_cast<const float4*>(xs)[i] : make_float4(0.f, 0.f, 0.f, 0.f));
+        }
+        const Lanes Ln = lane_layout<DT>(c, m);
+        XReg<DT> xr;
+        Epi e{};
+        e.kind = Epi::kLogits;
+        e.logits = ys;
+        e.err = p.err;
+        e.scale = lanes_prep<DT>(c, Ln, n, false, 0.f, xr);
+        const ChunkGeo ck = v ? view_geo(*v, pt.g) : rows_geo(m, DT);
+        gemv_consume<DT>(c, m, ck, r0, r1, Ln, xr, which == 4 ? sm.res() : sm.rowp(), e, -1);
+    }
+    block_join();
+}
+
+cudaError_t launch_gemv_test(cudaStream_t st, int wtype, const StepParams& p, int which, int layer, const float* x,
+                             float* y, int sms, size_t smem) {
+    const void* fn = wtype == LLM_Q8_0 ? (const void*)gemv_test_kernel<LLM_Q8_0>
+                     : wtype == LLM_F16 ? (const void*)gemv_test_kernel<LLM_F16>
+                                        : (const void*)gemv_test_kernel<LLM_F32>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    StepParams q = p;
+    void* args[] = {&q, &which, &layer, &x, &y};
+    return cudaLaunchKernel(fn, dim3(sms), dim3(kBlock), args, smem, st);
+}
+
 void launch_kv_store(cudaStream_t st, __half* kc, __half* vc, int pos, int kv_dim, const float* k, const float* v) {
     kv_store_kernel<<<(kv_dim + 255) / 256, 256, 0, st>>>(kc, vc, pos, kv_dim, k, v);
 }

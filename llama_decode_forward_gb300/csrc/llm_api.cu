@@ -23,6 +23,8 @@ bool gview_plan(GView& v, int wtype, int rows, int cols, int ngrp, int max_rows)
 const void* step_kernel_ptr(int wtype);
 void launch_kv_store(cudaStream_t st, __half* kc, __half* vc, int pos, int kv_dim, const float* k, const float* v);
 void launch_dequant_rows(cudaStream_t st, int wtype, const DMat& m, int row0, int n_rows, float* out);
+cudaError_t launch_gemv_test(cudaStream_t st, int wtype, const StepParams& p, int which, int layer, const float* x,
+                             float* y, int sms, size_t smem);
 }  // namespace llm
 
 using namespace llm;
@@ -756,6 +758,21 @@ extern "C" int llm_test_dequant_rows(llm_handle* h, int which, int layer, int32_
     CK(h, cudaStreamSynchronize(h->st));
     return LLM_OK;
 }
+
+extern "C" int llm_test_gemv(llm_handle* h, int which, int layer, const float* x_dev, float* y_dev) {
+    if (!h || !x_dev || !y_dev) return LLM_ERR_INVALID_ARG;
+    if (which < 0 || which > 4) return fail(h, LLM_ERR_INVALID_ARG, "which = %d", which);
+    if (layer < 0 || layer >= h->cfg.n_layers) return fail(h, LLM_ERR_OUT_OF_RANGE, "layer %d", layer);
+    if (h->broken) return fail(h, LLM_ERR_STATE, "handle has a device error; call llm_reset");
+    StepParams p = step_params(h, h->tok_in, 0, h->tok_out);
+    p.trace = nullptr;
+    CK(h, launch_gemv_test(h->st, h->cfg.wtype, p, which, layer, x_dev, y_dev, h->sms, h->smem));
+    h->launches++;
+    CK(h, cudaStreamSynchronize(h->st));
+    return read_device_error(h);
+}
+
+extern "C" int llm_column_groups(const llm_handle* h) { return h ? h->ngrp : LLM_ERR_INVALID_ARG; }
 
 extern "C" int llm_trace_read(llm_handle* h, uint64_t* host, int32_t* sms) {
     if (!h || !host || !sms) return LLM_ERR_INVALID_ARG;

@@ -24,7 +24,7 @@ F32, F16, Q8_0 = 0, 1, 8
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LOCK = threading.Lock()
 _LIB = None
-CFLAGS = ["-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared"]
+CFLAGS = ["-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp"]
 
 
 def build(force: bool = False) -> str:
@@ -91,6 +91,7 @@ def load(path: str):
     L.orc_argmax.argtypes = [vp, i]
     L.orc_argmax.restype = i
     L.orc_matvec_llamacpp.argtypes = [vp, vp, i, vp, i, i]
+    L.orc_set_threads.argtypes = [i]
     L.orc_attention_llamacpp.argtypes = [vp, vp, vp, vp, i, i, i, i]
     return L
 
@@ -125,6 +126,29 @@ def f32_to_f16(x) -> np.ndarray:
     L = lib()
     a = _f32(x).ravel()
     return np.array([L.orc_f32_to_f16(float(v)) for v in a], dtype=np.uint16)
+
+
+def set_threads(n: int) -> None:
+    """1 (the default): the oracle runs on the calling thread.  n > 1: the
+    rows of every matrix product and the heads of attention are split over n
+    OpenMP threads (each output element still computed by one thread in the
+    same order, so every result is bitwise the single-thread one)."""
+    lib().orc_set_threads(int(n))
+
+
+class threads:
+    """Context manager: the oracle on n threads inside the block, 1 after."""
+
+    def __init__(self, n: int | None = None):
+        self.n = n or os.cpu_count() or 1
+
+    def __enter__(self):
+        set_threads(self.n)
+        return self
+
+    def __exit__(self, *exc):
+        set_threads(1)
+        return False
 
 
 def dequant_row(w: np.ndarray, wtype: int, row: int, cols: int) -> np.ndarray:

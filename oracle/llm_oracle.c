@@ -105,22 +105,34 @@ void orc_rmsnorm(float *out, const float *x, const float *g, int n, float eps) {
     }
 }
 
+/* ------------------------------------------------------------- threads --
+ * Off by default (1).  With n > 1 the rows of each matrix product and the
+ * heads of attention are split over n threads; every output element is still
+ * computed by one thread in the same order, so results do not change. */
+static int orc_threads_ = 1;
+
+void orc_set_threads(int n) { orc_threads_ = n > 1 ? n : 1; }
+
 /* ---------------------------------------------------------------- GEMV --
  * "The Forward Pass in Java", Example 5: out[r] = sum_i W[r*cols+i] * x[i],
  * a GGUF tensor with dims [cols, rows] storing row r at r*cols; the sum runs
  * in float from i = 0.  Rows are decoded one at a time (decoding is exact, so
  * this equals decoding the whole tensor first). */
 void orc_matvec(float *out, const void *w, int wtype, const float *x, int rows, int cols) {
-    float *row = (float *)malloc(sizeof(float) * (size_t)cols);
-    for (int r = 0; r < rows; r++) {
-        const float *wr;
-        if (wtype == ORC_F32) wr = (const float *)w + (int64_t)r * cols;
-        else { orc_dequant_row(w, wtype, r, cols, row); wr = row; }
-        float s = 0.0f;
-        for (int i = 0; i < cols; i++) { float p = wr[i] * x[i]; s = s + p; }
-        out[r] = s;
+#pragma omp parallel num_threads(orc_threads_) if (orc_threads_ > 1)
+    {
+        float *row = (float *)malloc(sizeof(float) * (size_t)cols);
+#pragma omp for schedule(static)
+        for (int r = 0; r < rows; r++) {
+            const float *wr;
+            if (wtype == ORC_F32) wr = (const float *)w + (int64_t)r * cols;
+            else { orc_dequant_row(w, wtype, r, cols, row); wr = row; }
+            float s = 0.0f;
+            for (int i = 0; i < cols; i++) { float p = wr[i] * x[i]; s = s + p; }
+            out[r] = s;
+        }
+        free(row);
     }
-    free(row);
 }
 
 /* ---------------------------------------------------------------- RoPE --
@@ -173,10 +185,13 @@ static float round_f16(float v) { return orc_f16_to_f32(orc_f32_to_f16(v)); }
 static void attention(float *out, const float *q, const float *kcache, const float *vcache,
                       int n_heads, int n_kv_heads, int head_dim, int pos, int llamacpp) {
     int kv_dim = n_kv_heads * head_dim, group = n_heads / n_kv_heads;
-    float *att = (float *)malloc(sizeof(float) * (size_t)(pos + 1));
-    float *qh = (float *)malloc(sizeof(float) * (size_t)head_dim);
     float sq = (float)sqrt((double)head_dim);
     for (int i = 0; i < n_heads * head_dim; i++) out[i] = 0.0f;
+#pragma omp parallel num_threads(orc_threads_) if (orc_threads_ > 1)
+    {
+    float *att = (float *)malloc(sizeof(float) * (size_t)(pos + 1));
+    float *qh = (float *)malloc(sizeof(float) * (size_t)head_dim);
+#pragma omp for schedule(static)
     for (int h = 0; h < n_heads; h++) {
         int kv_off = (h / group) * head_dim;
         for (int i = 0; i < head_dim; i++) qh[i] = llamacpp ? round_f16(q[h * head_dim + i]) : q[h * head_dim + i];
@@ -200,6 +215,7 @@ static void attention(float *out, const float *q, const float *kcache, const flo
     }
     free(qh);
     free(att);
+    }
 }
 
 void orc_attention(float *out, const float *q, const float *kcache, const float *vcache,

@@ -1,8 +1,8 @@
 /*
  * CPU oracle for the batch-1 Llama decode forward pass.
  *
- * TEST INFRASTRUCTURE ONLY.  This is a plain, slow, single-threaded C
- * evaluation of what the GPU library computes, written from the method's
+ * TEST INFRASTRUCTURE ONLY.  This is a plain, slow C evaluation (single
+ * threaded unless orc_set_threads says otherwise) of what the GPU library computes, written from the method's
  * definition so that the CUDA path can be checked against it.  Only the test
  * suite, the package smoke check and the benchmark's CPU-baseline leg may load
  * it.  It shares no code, header, table or helper with the CUDA library.
@@ -78,6 +78,13 @@ typedef struct orc_model orc_model;
  * ffn_norm-l, ffn_gate-l, ffn_up-l, ffn_swiglu-l, ffn_out-l, l_out-l,
  * result_norm, result_output).  `layer` is -1 outside the layer loop. */
 typedef void (*orc_trace_fn)(const char *name, int layer, const float *v, int n, void *user);
+
+/* ---- threads ----
+ * 1 (the default): everything on the calling thread.  n > 1: the rows of
+ * every matrix product and the heads of attention are split over n OpenMP
+ * threads; each output element is still computed by one thread in the same
+ * order, so every result is bitwise the single-thread one. */
+void orc_set_threads(int n);
 
 /* ---- model ---- */
 orc_model *orc_create(const orc_config *cfg, const orc_weights *w);  /* NULL on bad config */

@@ -21,15 +21,20 @@ def test_exports_every_declared_symbol():
 
 
 def test_library_is_built_for_sm_103a():
-    out = subprocess.run(["/usr/local/cuda/bin/cuobjdump", "--list-elf", L.LIBRARY_PATH], capture_output=True,
-                         text=True)
-    if out.returncode != 0:
-        pytest.skip("cuobjdump unavailable")
-    assert "sm_103a" in out.stdout
+    """Every compile and the link pass exactly one -gencode pair, sm_103a
+    machine code from compute_103a (no other architecture, no PTX to JIT)."""
+    from llama_decode_forward_gb300 import build as B
+    want = ["-gencode", "arch=compute_103a,code=sm_103a"]
+    for cmd in [B.compile_command(s, "x.o") for s in B.sources()] + [B.link_command(["x.o"], "lib.so")]:
+        i = cmd.index("-gencode")
+        assert cmd[i:i + 2] == want, cmd
+        assert cmd.count("-gencode") == 1 and not any("-arch" in a for a in cmd), cmd
+    assert B.compile_command("a.cu", "a.o", trace=True)[-4:-2] == ["-c", "a.cu"]
+    assert "-DLLM_TRACE" in B.compile_command("a.cu", "a.o", trace=True)
 
 
 def test_status_strings():
-    for s in range(0, -8, -1):
+    for s in range(0, -9, -1):
         assert L.llm_status_string(s) not in ("", "unknown status")
     assert L.llm_status_string(-99) == "unknown status"
 

@@ -87,7 +87,8 @@ def test_llama1b_q8_0_step_at_context(lib, pos):
     dec = lib.Decoder(cfg, W)
     prefill_kv_both(cfg.scaled(max_seq=pos + 1), ora, dec, pos)
     tok = int(synth.prompt(cfg, 1)[0])
-    ref = ora.forward(tok, pos)
+    with oracle.threads():
+        ref = ora.forward(tok, pos)
     logits = np.empty(cfg.vocab, np.float32)
     am = lib.llm_decode_step(dec.h, tok, pos, logits)
     check_logits(logits, ref, cfg.wtype, f"pos {pos}")
@@ -95,14 +96,20 @@ def test_llama1b_q8_0_step_at_context(lib, pos):
         assert margin(ref) < TOL[cfg.wtype]
 
 
-def test_qwen2_f16_decode_steps(lib):
-    """Qwen2-style F16 (NEOX, biases, tied): token-by-token prompt then greedy steps."""
-    run_stream_workload(lib, synth.QWEN2_F16.scaled(max_seq=64), 16, 8)
+def test_qwen2_f16_prefill_512_and_128_greedy_steps(lib):
+    """Qwen2-style F16 (NEOX, biases, tied), as the workload states: a
+    512-token batched prefill (tensor-core GEMMs) from seeded uniform token
+    ids, then 128 greedy decode steps; teacher-forced logits at every step and
+    the free-running stream against the oracle (run on every host core, which
+    gives the single-thread oracle's bits)."""
+    with oracle.threads():
+        run_stream_workload(lib, synth.QWEN2_F16.scaled(max_seq=640), 512, 128)
 
 
-@pytest.mark.parametrize("ctx", [1, 1024])
+@pytest.mark.parametrize("ctx", [1, 1024, 4096, 16384])
 def test_llama7b_q8_0_step_at_context(lib, ctx):
-    """Llama-2-7B shape, Q8_0: one step at pos ctx-1."""
+    """Llama-2-7B shape, Q8_0: one step at pos ctx-1 after ctx-1 seeded cache
+    rows (the context sweep of the workload)."""
     cfg = synth.LLAMA7B_Q8
     pos = ctx - 1
     W = synth.make_weights(cfg)
@@ -111,7 +118,19 @@ def test_llama7b_q8_0_step_at_context(lib, ctx):
     if pos:
         prefill_kv_both(cfg.scaled(max_seq=ctx), ora, dec, pos)
     tok = int(synth.prompt(cfg, 1)[0])
-    ref = ora.forward(tok, pos)
+    with oracle.threads():
+        ref = ora.forward(tok, pos)
     logits = np.empty(cfg.vocab, np.float32)
-    lib.llm_decode_step(dec.h, tok, pos, logits)
+    am = lib.llm_decode_step(dec.h, tok, pos, logits)
     check_logits(logits, ref, cfg.wtype, f"ctx {ctx}")
+    if am != oracle.argmax(ref):
+        assert margin(ref) < TOL[cfg.wtype]
+    # the K/V rows the step wrote at pos, against the oracle's (layer 0 and the last)
+    for l in (0, cfg.n_layers - 1):
+        k, v = dec.kv_tensors(l)
+        for which, t in ((0, k), (1, v)):
+            g = t[pos].cpu().numpy().view(np.float16).astype(np.float64)
+            r = ora.kv(l, which)[pos].astype(np.float64)
+            assert np.max(np.abs(g - r)) <= TOL[cfg.wtype], (l, which)
+    ora.close()
+    dec.close()
