@@ -1482,23 +1482,33 @@ __device__ bool attention_unit_mma(Consumer& c, const LayerDev& L, int layer, in
         wpart[warp * WS + hq * (HD + 2) + HD + 1] = l_run;
     }
     consumer_sync();
-    for (int oo = tid; oo < GD; oo += kConsumers) {
-        const int hh = oo / HD, ii = oo % HD;
-        float M = -INFINITY;
-        for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, wpart[w * WS + hh * (HD + 2) + HD]);
-        float v = 0.f, l = 0.f;
-        for (int w = 0; w < kConsumerWarps; w++) {
-            const float mw = wpart[w * WS + hh * (HD + 2) + HD];
-            const float f = mw == -INFINITY ? 0.f : expf(mw - M);
-            v = fmaf(f, wpart[w * WS + hh * (HD + 2) + ii], v);
-            l = fmaf(f, wpart[w * WS + hh * (HD + 2) + HD + 1], l);
-        }
-        const size_t hs = (size_t)(h0 + hh) * p.max_splits + s;
-        st_tagged(part_acc + hs * HD + ii, v, c.tag);
-        if (ii == 0) {
+    // the warps' rescale factors, once per (head, warp): warp hh takes head hh,
+    // lane w warp w's running max; M = the head's max, f_w = e^(m_w - M), and
+    // the head's sum l = sum_w f_w l_w (warp order) with its (m, l) stored
+    float* fw = sm.comb();                                         // [gq][kConsumerWarps]
+    if (warp < gq) {
+        const int hh = warp;
+        const float mw = lane < kConsumerWarps ? wpart[lane * WS + hh * (HD + 2) + HD] : -INFINITY;
+        const float M = warp_max(mw);
+        const float f = mw == -INFINITY ? 0.f : expf(mw - M);
+        if (lane < kConsumerWarps) fw[hh * kConsumerWarps + lane] = f;
+        __syncwarp();
+        if (lane == 0) {
+            float l = 0.f;
+            for (int w = 0; w < kConsumerWarps; w++) l = fmaf(fw[hh * kConsumerWarps + w], wpart[w * WS + hh * (HD + 2) + HD + 1], l);
+            const size_t hs = (size_t)(h0 + hh) * p.max_splits + s;
             st_tagged(part_ml + 2 * hs, M, c.tag);
             st_tagged(part_ml + 2 * hs + 1, l, c.tag);
         }
+    }
+    consumer_sync();
+    for (int oo = tid; oo < GD; oo += kConsumers) {
+        const int hh = oo / HD, ii = oo % HD;
+        float v = 0.f;
+#pragma unroll 5
+        for (int w = 0; w < kConsumerWarps; w++) v = fmaf(fw[hh * kConsumerWarps + w], wpart[w * WS + hh * (HD + 2) + ii], v);
+        const size_t hs = (size_t)(h0 + hh) * p.max_splits + s;
+        st_tagged(part_acc + hs * HD + ii, v, c.tag);
     }
     fence_proxy_async_smem();                                      // the slot's next fill is a TMA write
     consumer_sync();
