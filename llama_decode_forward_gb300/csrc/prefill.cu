@@ -445,6 +445,215 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 2-D map of a [rows][K] F16 matrix, box 64 x box_rows, 128-byte swizzle.
+// ------------------------------------------------ attention on tensor cores --
+// Causal attention of 16 prompt rows of one kv head over the cache ("The
+// Forward Pass in Java", Example 11; "What a Llama model computes, and why"
+// §4: row i attends to positions 0..pos0+i), one warp per query head of the
+// kv head.  Scores and the weighted V sum are mma.sync m16n8k16 products on
+// F16 parts: q and the probabilities are split into hi = their F16 rounding
+// and lo = the rest rounded to F16, so each product of a part with an F16 K
+// or V element is exact and the two parts add up in the F32 accumulator
+// (the same arithmetic as the decode step's attention).  The online softmax
+// (running max and sum per row, rescaled accumulators) runs on the
+// accumulator fragments; K and V arrive in 64-position tiles, double
+// buffered with cp.async, in rows padded to HD + 8 halves so that ldmatrix
+// reads them without bank conflicts.  The output row is divided by its sum
+// and rounded to F16 (the O projection's operand).
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half a, __half b) {
+    return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
+}
+
+constexpr int kAttnKT = 64;                      // cache positions per K/V tile
+
+template <int HD>
+__global__ void __launch_bounds__(256) attention_mma_kernel(const float* QKV, int n, int pos0, int n_heads, int n_kv,
+                                                            float attn_div, const __half* kc, const __half* vc,
+                                                            __half* A) {
+    constexpr int PITCH = HD + 8;                // halves per shared-memory row
+    extern __shared__ __align__(16) __half kvs[];   // [2 buffers][K, V][kAttnKT][PITCH]
+    const int gq = n_heads / n_kv, q_dim = n_heads * HD, kv_dim = n_kv * HD, row_w = q_dim + 2 * kv_dim;
+    const int ntile = (n + 15) / 16;
+    const int qt = ntile - 1 - (int)blockIdx.x;  // the longest rows first
+    const int g = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = g * gq + warp;
+    const int t0 = qt * 16;
+    const int r = lane >> 2, t = lane & 3;
+    const int n_pos = pos0 + min(t0 + 16, n);    // positions the tile's last row attends to
+    // this thread's two rows; rows past the batch take the last row's causal limit (never stored)
+    const int R0 = min(t0 + r, n - 1), R1 = min(t0 + r + 8, n - 1);
+    // q fragments: element (row t0 + r + 8 (j & 1), column ks*16 + 8 (j >> 1) + 2t + {0, 1})
+    uint32_t qhi[HD / 16][4], qlo[HD / 16][4];
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ks++)
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int row = (j & 1) ? R1 : R0, col = ks * 16 + (j >> 1) * 8 + 2 * t;
+            const float2 x = *reinterpret_cast<const float2*>(QKV + (size_t)row * row_w + h * HD + col);
+            const __half hx = __float2half_rn(x.x), hy = __float2half_rn(x.y);
+            qhi[ks][j] = h2_bits(hx, hy);
+            qlo[ks][j] = h2_bits(__float2half_rn(x.x - __half2float(hx)), __float2half_rn(x.y - __half2float(hy)));
+        }
+    float o[HD / 8][4];
+#pragma unroll
+    for (int nt = 0; nt < HD / 8; nt++) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    const int ntiles = (n_pos + kAttnKT - 1) / kAttnKT;
+    auto load_tile = [&](int c, int buf) {
+        __half* ks_ = kvs + (size_t)(buf * 2) * kAttnKT * PITCH;
+        __half* vs_ = ks_ + kAttnKT * PITCH;
+        constexpr int W = HD / 8;                // 16-byte words per row
+        for (int e = threadIdx.x; e < kAttnKT * W; e += blockDim.x) {
+            const int pr = e / W, w = e % W;
+            const int pos = min(c * kAttnKT + pr, n_pos - 1);   // rows past n_pos repeat a valid row (masked)
+            const size_t src = (size_t)pos * kv_dim + (size_t)g * HD + w * 8;
+            cp_async16(ks_ + pr * PITCH + w * 8, kc + src);
+            cp_async16(vs_ + pr * PITCH + w * 8, vc + src);
+        }
+        cp_async_commit();
+    };
+    load_tile(0, 0);
+    for (int c = 0; c < ntiles; c++) {
+        if (c + 1 < ntiles) {
+            load_tile(c + 1, (c + 1) & 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            cp_async_wait_all();
+        }
+        __syncthreads();
+        const __half* ks_ = kvs + (size_t)((c & 1) * 2) * kAttnKT * PITCH;
+        const __half* vs_ = ks_ + kAttnKT * PITCH;
+        const uint32_t kbase = smem_addr(ks_), vbase = smem_addr(vs_);
+        for (int sub = 0; sub < kAttnKT / 16; sub++) {
+            const int p0 = c * kAttnKT + sub * 16;
+            if (p0 >= n_pos) break;
+            // scores of positions p0 + 8 nt + 2t + {0, 1}, rows r and r + 8
+            float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                const int mi = lane >> 3, ri = lane & 7;
+                const uint32_t krow = kbase + (uint32_t)((sub * 16 + ri + (mi >= 2 ? 8 : 0)) * PITCH * 2);
+#pragma unroll
+                for (int ks = 0; ks < HD / 16; ks++) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(krow + (uint32_t)((ks * 16 + (mi & 1) * 8) * 2), b0, b1, b2, b3);
+                    mma16816(s[0], qhi[ks], b0, b1);
+                    mma16816(s[0], qlo[ks], b0, b1);
+                    mma16816(s[1], qhi[ks], b2, b3);
+                    mma16816(s[1], qlo[ks], b2, b3);
+                }
+            }
+            float mt0 = -INFINITY, mt1 = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; nt++)
+#pragma unroll
+                for (int k = 0; k < 2; k++) {
+                    const int P = p0 + nt * 8 + 2 * t + k;
+                    s[nt][k] = P <= pos0 + R0 ? __fdiv_rn(s[nt][k], attn_div) : -INFINITY;
+                    s[nt][2 + k] = P <= pos0 + R1 ? __fdiv_rn(s[nt][2 + k], attn_div) : -INFINITY;
+                    mt0 = fmaxf(mt0, s[nt][k]);
+                    mt1 = fmaxf(mt1, s[nt][2 + k]);
+                }
+            mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, 1));
+            mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, 2));
+            mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, 1));
+            mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, 2));
+            const float mn0 = fmaxf(m0, mt0), mn1 = fmaxf(m1, mt1);
+            const float c0 = expf(m0 - mn0), c1 = expf(m1 - mn1);   // 0 on the first tile (m = -inf)
+            float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; nt++)
+#pragma unroll
+                for (int k = 0; k < 2; k++) {
+                    s[nt][k] = expf(s[nt][k] - mn0);
+                    s[nt][2 + k] = expf(s[nt][2 + k] - mn1);
+                    ls0 += s[nt][k];
+                    ls1 += s[nt][2 + k];
+                }
+            ls0 += __shfl_xor_sync(0xffffffffu, ls0, 1);
+            ls0 += __shfl_xor_sync(0xffffffffu, ls0, 2);
+            ls1 += __shfl_xor_sync(0xffffffffu, ls1, 1);
+            ls1 += __shfl_xor_sync(0xffffffffu, ls1, 2);
+            l0 = l0 * c0 + ls0;
+            l1 = l1 * c1 + ls1;
+            m0 = mn0;
+            m1 = mn1;
+#pragma unroll
+            for (int nt = 0; nt < HD / 8; nt++) {
+                o[nt][0] *= c0;
+                o[nt][1] *= c0;
+                o[nt][2] *= c1;
+                o[nt][3] *= c1;
+            }
+            // probabilities as A fragments (the accumulator layout is the A layout): hi and lo parts
+            uint32_t phi[4], plo[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const float x = s[j >> 1][(j & 1) * 2], y = s[j >> 1][(j & 1) * 2 + 1];
+                const __half hx = __float2half_rn(x), hy = __float2half_rn(y);
+                phi[j] = h2_bits(hx, hy);
+                plo[j] = h2_bits(__float2half_rn(x - __half2float(hx)), __float2half_rn(y - __half2float(hy)));
+            }
+            {
+                const int mi = lane >> 3, ri = lane & 7;
+                const uint32_t vrow = vbase + (uint32_t)((sub * 16 + ri + (mi & 1) * 8) * PITCH * 2);
+#pragma unroll
+                for (int nt = 0; nt < HD / 8; nt += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vrow + (uint32_t)(((nt + (mi >> 1)) * 8) * 2), b0, b1, b2, b3);
+                    mma16816(o[nt], phi, b0, b1);
+                    mma16816(o[nt], plo, b0, b1);
+                    mma16816(o[nt + 1], phi, b2, b3);
+                    mma16816(o[nt + 1], plo, b2, b3);
+                }
+            }
+        }
+        __syncthreads();                         // the buffer is reloaded two tiles later
+    }
+    const float i0 = 1.0f / l0, i1 = 1.0f / l1;
+    const int row0 = t0 + r, row1 = t0 + r + 8;
+#pragma unroll
+    for (int nt = 0; nt < HD / 8; nt++) {
+        const int col = h * HD + nt * 8 + 2 * t;
+        if (row0 < n)
+            *reinterpret_cast<__half2*>(A + (size_t)row0 * q_dim + col) =
+                __floats2half2_rn(o[nt][0] * i0, o[nt][1] * i0);
+        if (row1 < n)
+            *reinterpret_cast<__half2*>(A + (size_t)row1 * q_dim + col) =
+                __floats2half2_rn(o[nt][2] * i1, o[nt][3] * i1);
+    }
+}
+
+// The tensor-core attention for the head sizes it is instantiated for and up
+// to 8 query heads per kv head; other shapes keep attention_rows_kernel.
+bool attention_mma_launch(cudaStream_t st, const float* QKV, int n, int pos0, int n_heads, int n_kv, int hd,
+                          float attn_div, const __half* kc, const __half* vc, __half* A, cudaError_t* e) {
+    const int gq = n_heads / n_kv;
+    if (gq > 8 || !(hd == 32 || hd == 64 || hd == 128)) return false;
+    const dim3 grid((n + 15) / 16, n_kv), block(32 * gq);
+    const size_t smem = (size_t)2 * 2 * kAttnKT * (hd + 8) * sizeof(__half);
+    const void* fn = hd == 32 ? (const void*)attention_mma_kernel<32>
+                     : hd == 64 ? (const void*)attention_mma_kernel<64>
+                                : (const void*)attention_mma_kernel<128>;
+    if (smem > 48 * 1024) {
+        *e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (*e != cudaSuccess) return true;
+    }
+    if (hd == 32) attention_mma_kernel<32><<<grid, block, smem, st>>>(QKV, n, pos0, n_heads, n_kv, attn_div, kc, vc, A);
+    else if (hd == 64) attention_mma_kernel<64><<<grid, block, smem, st>>>(QKV, n, pos0, n_heads, n_kv, attn_div, kc, vc, A);
+    else attention_mma_kernel<128><<<grid, block, smem, st>>>(QKV, n, pos0, n_heads, n_kv, attn_div, kc, vc, A);
+    *e = cudaGetLastError();
+    return true;
+}
+
 bool gemm_map(CUtensorMap* m, const void* base, int K, int rows, int box_rows = 128) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
@@ -568,9 +777,15 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
             rope_kv_rows_kernel<<<nb, 128, 0, c.st>>>(QKV, nb, p0, c.n_heads, c.n_kv, c.hd, c.rope_dims, c.neox,
                                                       c.theta_scale, c.rope_freqs, L.kc, L.vc);
             PF_CK(cudaGetLastError(), "RoPE and KV append");
-            attention_rows_kernel<<<dim3(nb, c.n_kv), 128, attn_smem, c.st>>>(QKV, nb, p0, c.n_heads, c.n_kv, c.hd,
-                                                                              c.attn_div, L.kc, L.vc, Ah);
-            PF_CK(cudaGetLastError(), "attention");
+            {
+                cudaError_t ea = cudaSuccess;
+                if (!attention_mma_launch(c.st, QKV, nb, p0, c.n_heads, c.n_kv, c.hd, c.attn_div, L.kc, L.vc, Ah, &ea)) {
+                    attention_rows_kernel<<<dim3(nb, c.n_kv), 128, attn_smem, c.st>>>(QKV, nb, p0, c.n_heads, c.n_kv,
+                                                                                      c.hd, c.attn_div, L.kc, L.vc, Ah);
+                    ea = cudaGetLastError();
+                }
+                PF_CK(ea, "attention");
+            }
             GemmOut oo{nullptr, nullptr, X, nullptr};
             if (!(wm = weights(l, 1, L.o, L.o.rows, c.q_dim, 64))) { *msg = "O weights"; return cudaErrorInvalidValue; }
             PF_CK((gemm<64, kEpiResidual>(c.st, mAh, *wm, oo, nb, c.dim, c.q_dim, c.err)), "O GEMM");
