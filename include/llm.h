@@ -54,6 +54,21 @@ typedef enum {
                                      outputs are invalid and the handle needs llm_reset */
 } llm_status;
 
+/* Rounding of the decode step ("What a Llama model computes, and why" §8).
+ * LLM_NUMERICS_EXACT: every matrix product takes its F32 input vector as it
+ * is (Q8_0 rows meet the activations as 24-bit block fixed point, about what
+ * an F32 sum keeps), and attention's q and probabilities stay F32.
+ * LLM_NUMERICS_LLAMACPP: llama.cpp's rounding points.  A Q8_0 product first
+ * quantizes its input to Q8_0 blocks (d = amax/127 stored as F16, each
+ * element x/d rounded half away from zero) and sums the blocks' integer dots
+ * times d_w*d_x; an F16 product rounds its input to F16; attention rounds q
+ * to F16 and each probability e_t/sum to F16 after the normaliser over all
+ * positions (so the step streams the K rows twice).  RMSNorm's scale is
+ * applied before the rounding ((x * scale) * g).  llm_prefill is not
+ * affected by this field.  Slower than EXACT; meant for comparing with
+ * llama.cpp's outputs. */
+typedef enum { LLM_NUMERICS_EXACT = 0, LLM_NUMERICS_LLAMACPP = 1 } llm_numerics;
+
 /* Model shape ("The Forward Pass in Java", Example 1, Config record).
  * head_dim * n_heads must equal dim; n_heads must be a multiple of n_kv_heads;
  * rope_dims is even and <= head_dim (dims beyond it are not rotated);
@@ -66,6 +81,7 @@ typedef struct {
     float rope_base;    /* RoPE frequency base */
     int rope_neox;      /* 0: pairs (2i, 2i+1) (llama); 1: pairs (i, i + rope_dims/2) (qwen2) */
     int wtype;          /* llm_dtype of every matrix, the embedding and the output */
+    int numerics;       /* llm_numerics of the decode step (0, the zero-initialised default: exact) */
 } llm_config;
 
 /* One layer's tensors, all DEVICE pointers in GGUF layout ("The Forward Pass

@@ -18,13 +18,14 @@ LLM_F32, LLM_F16, LLM_Q8_0 = 0, 1, 8
 LLM_OK = 0
 LLM_ERR_INVALID_ARG, LLM_ERR_UNSUPPORTED, LLM_ERR_OUT_OF_RANGE = -1, -2, -3
 LLM_ERR_CUDA, LLM_ERR_NO_MEMORY, LLM_ERR_DEVICE_TIMEOUT, LLM_ERR_STATE, LLM_ERR_NONFINITE = -4, -5, -6, -7, -8
+LLM_NUMERICS_EXACT, LLM_NUMERICS_LLAMACPP = 0, 1
 
 
 class llm_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("n_layers", "dim", "n_heads", "n_kv_heads", "head_dim", "ffn_dim",
                                             "vocab", "max_seq", "rope_dims")] + \
                [("eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("rope_neox", ctypes.c_int),
-                ("wtype", ctypes.c_int)]
+                ("wtype", ctypes.c_int), ("numerics", ctypes.c_int)]
 
 
 class llm_layer_weights(ctypes.Structure):
@@ -253,7 +254,7 @@ def config_struct(cfg) -> llm_config:
     return llm_config(n_layers=cfg.n_layers, dim=cfg.dim, n_heads=cfg.n_heads, n_kv_heads=cfg.n_kv_heads,
                       head_dim=cfg.head_dim, ffn_dim=cfg.ffn_dim, vocab=cfg.vocab, max_seq=cfg.max_seq,
                       rope_dims=cfg.rope_dims, eps=cfg.eps, rope_base=cfg.rope_base, rope_neox=int(cfg.rope_neox),
-                      wtype=int(cfg.wtype))
+                      wtype=int(cfg.wtype), numerics=int(getattr(cfg, "numerics", LLM_NUMERICS_EXACT)))
 
 
 class DeviceWeights:

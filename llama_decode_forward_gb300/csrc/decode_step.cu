@@ -40,6 +40,7 @@
 // Every wait is bounded; on expiry the error word is set, the producer drains
 // its copies in flight, and the CTA exits.
 #include <algorithm>
+#include <type_traits>
 
 #include "llm_internal.cuh"
 
@@ -159,6 +160,7 @@ struct Smem {
     __device__ __forceinline__ uint64_t* empty() const { return full() + p.ns; }
     __device__ __forceinline__ int* misc() const { return reinterpret_cast<int*>(base + p.off_misc); }   // [0] abort, [1] flag
     __device__ __forceinline__ float* fred() const { return reinterpret_cast<float*>(base + p.off_misc + 64); }
+    __device__ __forceinline__ double* fred_d() const { return reinterpret_cast<double*>(base + p.off_misc + 64); }
     __device__ __forceinline__ unsigned long long* best() const {
         return reinterpret_cast<unsigned long long*>(base + p.off_misc + 64 + 8 * (kConsumerWarps + 2));
     }
@@ -303,7 +305,10 @@ struct Producer {
         note_wait(tk);
     }
 
-    __device__ void attention(int layer) {
+    // The K and V tiles of this CTA's attention units, chunk by chunk; with
+    // two_pass (llama.cpp rounding) each unit's K tiles alone first, then its
+    // K and V tiles again.
+    __device__ void attention(int layer, bool two_pass) {
         if (dead) return;
         trace_mark(p, 256 + 8 * layer + 1);
         const int S = p.splits, units = p.n_kv * S, P = p.attn_rows;
@@ -314,16 +319,21 @@ struct Producer {
         for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
             int g, s, t0, t1;
             unit_range(p, unit, S, g, s, t0, t1);
-            for (int c0 = t0; c0 < t1; c0 += P) {
-                int slot;
-                uint8_t* dst = acquire(slot);
-                if (!dst) return;
-                mbar_arrive_expect_tx(&sm.full()[slot], 2 * half_bytes);
-                for (int j = 0; j < nsub; j++) {
-                    tma_2d_g2s(dst + (size_t)j * P * W * 2, kmap, g * p.hd + j * W, c0, &sm.full()[slot]);
-                    tma_2d_g2s(dst + half_bytes + (size_t)j * P * W * 2, vmap, g * p.hd + j * W, c0, &sm.full()[slot]);
+            for (int pass = two_pass ? 0 : 1; pass < 2; pass++) {
+                const bool with_v = pass == 1;
+                for (int c0 = t0; c0 < t1; c0 += P) {
+                    int slot;
+                    uint8_t* dst = acquire(slot);
+                    if (!dst) return;
+                    mbar_arrive_expect_tx(&sm.full()[slot], with_v ? 2 * half_bytes : half_bytes);
+                    for (int j = 0; j < nsub; j++) {
+                        tma_2d_g2s(dst + (size_t)j * P * W * 2, kmap, g * p.hd + j * W, c0, &sm.full()[slot]);
+                        if (with_v)
+                            tma_2d_g2s(dst + half_bytes + (size_t)j * P * W * 2, vmap, g * p.hd + j * W, c0,
+                                       &sm.full()[slot]);
+                    }
+                    issued();
                 }
-                issued();
             }
         }
         note_wait(-1);
@@ -533,6 +543,38 @@ __device__ __forceinline__ void convert_group(float4* xv, int b, int w, bool val
     }
 }
 
+// The llama.cpp reading of a Q8_0 product ("What a Llama model computes, and
+// why" §8): the block's activations are themselves quantized to Q8_0 first,
+// d = amax / 127 kept as F16 and q_j = x_j * (1/d) rounded half away from
+// zero (|q_j| <= 127; d = 0 gives q = 0).  The same digit record carries it:
+// q_j as the signed top digit with the two low digits zero, and
+// d_F16 * 2^-16 in place of 2^-e, so the three-digit dot returns
+// d_F16 * sum_j qs_j q_j (the integer dot scaled by the block's F16 d).
+__device__ __forceinline__ void convert_group_q8(float4* xv, int b, int w, bool valid, float4 v) {
+    float m = valid ? fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) : 0.f;
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    const float d = __fdiv_rn(m, 127.0f);
+    const float id = d != 0.f ? __frcp_rn(d) : 0.f;
+    auto q = [&](float x) { return (uint32_t)(int)roundf(__fmul_rn(x, id)) & 0xFFu; };
+    const uint32_t b2 = q(v.x) | (q(v.y) << 8) | (q(v.z) << 16) | (q(v.w) << 24);
+    if (valid) {
+        uint32_t* blk = reinterpret_cast<uint32_t*>(xv + 8 * b);
+        const int r = b & 7;
+        blk[4 * ((0 + (w >> 2)) ^ r) + (w & 3)] = 0u;
+        blk[4 * ((2 + (w >> 2)) ^ r) + (w & 3)] = 0u;
+        blk[4 * ((4 + (w >> 2)) ^ r) + (w & 3)] = b2;
+        if (w == 0) {
+            const float dx = __half2float(__float2half_rn(d));
+            reinterpret_cast<uint4*>(blk)[6 ^ r] = make_uint4(__float_as_uint(dx * (1.0f / 65536.0f)), 0u, 0u, 0u);
+        }
+    }
+}
+
+// x rounded to F16 (to nearest even) and widened back.
+__device__ __forceinline__ float f16_round(float x) { return __half2float(__float2half_rn(x)); }
+
 template <int DT>
 struct LaneDot;
 
@@ -676,12 +718,15 @@ struct Epi {
             best = k > best ? k : best;
         }
     }
+    // LC (llama.cpp rounding): e^-g taken in double and rounded to float, as
+    // the oracle takes it, so the product's input rounds from the same value
+    template <bool LC>
     __device__ void finish(Consumer& c) {
         if (kind != kSwiGLU) return;
         consumer_sync();
         for (int k = c.tid; k < end - base; k += kConsumers) {
             const float g = sm[2 * k], up = sm[2 * k + 1];
-            const float e = expf(-g);
+            const float e = LC ? (float)exp(-(double)g) : expf(-g);
             st_tagged(out + base + k, __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), up), c.tag);
         }
     }
@@ -732,14 +777,17 @@ __device__ __forceinline__ int swz(int i) { return (i & ~7) + ((i & 7) ^ ((i >> 
 
 // One staged 4-element group (group i of the vector, valid when i < the
 // vector's groups): Q8_0 phases turn it straight into its share of its
-// 32-element block's digit record (convert_group; the block's 8 groups are
-// lanes 8j..8j+7 of one warp, so every lane of the warp calls this), the
-// others store the floats.
-template <int DT>
+// 32-element block's digit record (convert_group, or convert_group_q8 under
+// llama.cpp rounding, LC; the block's 8 groups are lanes 8j..8j+7 of one
+// warp, so every lane of the warp calls this), the others store the floats
+// (F16 phases under LC rounded to F16 first).
+template <int DT, bool LC>
 __device__ __forceinline__ void stage_group(float4* xv, int i, bool valid, float4 v) {
     if constexpr (DT == LLM_Q8_0) {
-        convert_group(xv, i >> 3, i & 7, valid, v);
+        if constexpr (LC) convert_group_q8(xv, i >> 3, i & 7, valid, v);
+        else convert_group(xv, i >> 3, i & 7, valid, v);
     } else {
+        if constexpr (LC && DT == LLM_F16) v = make_float4(f16_round(v.x), f16_round(v.y), f16_round(v.z), f16_round(v.w));
         if (valid) xv[swz(i)] = v;
     }
 }
@@ -754,14 +802,21 @@ __device__ __forceinline__ void stage_group(float4* xv, int i, bool valid, float
 // that row).  Kept in the residual region.  A normed phase stages x * g (the
 // norm's gains, fetched ahead) and leaves the norm's scale to the rows'
 // epilogue ("The Forward Pass in Java", Example 4: y = (x * scale) * g, and
-// W y = scale * W (x * g)); returns the thread's sum of squares of x.
-template <int DT>
-__device__ float stage_residual(Consumer& c, const unsigned long long* d, int token, bool norm, float4* xv) {
+// W y = scale * W (x * g)); returns the thread's sum of squares of x.  Under
+// llama.cpp rounding (LC) a normed phase stages nothing here: its input is
+// rounded after the scale is applied, so lanes_prep stages (x * scale) * g.
+// The sum of squares of a norm: float, or double under llama.cpp rounding
+// (LC), where the norm's scale is formed as the oracle forms it, in double.
+template <bool LC>
+using NormSum = std::conditional_t<LC, double, float>;
+
+template <int DT, bool LC>
+__device__ NormSum<LC> stage_residual(Consumer& c, const unsigned long long* d, int token, bool norm, float4* xv) {
     const StepParams& p = c.p;
     float4* res = reinterpret_cast<float4*>(c.sm.res());
     const float4* g4 = reinterpret_cast<const float4*>(c.sm.gains());
     const int ngr = p.dim / 4;
-    float ss = 0.f;
+    NormSum<LC> ss = 0;
     if (norm) cp_async_wait_all();                     // this thread's part of the gains
     for (int i0 = c.tid - c.lane; i0 < ngr; i0 += kConsumers) {
         const int i = i0 + c.lane;
@@ -778,26 +833,29 @@ __device__ float stage_residual(Consumer& c, const unsigned long long* d, int to
                                 weight_at<DT>(p.embd, token, e + 2), weight_at<DT>(p.embd, token, e + 3));
             }
             res[i] = x;
-            ss += (x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w);
-            if (norm) {
+            if constexpr (LC)
+                ss += ((double)x.x * x.x + (double)x.y * x.y) + ((double)x.z * x.z + (double)x.w * x.w);
+            else
+                ss += (x.x * x.x + x.y * x.y) + (x.z * x.z + x.w * x.w);
+            if (norm && !LC) {
                 const float4 g = g4[swz(i)];
                 x = make_float4(__fmul_rn(x.x, g.x), __fmul_rn(x.y, g.y), __fmul_rn(x.z, g.z), __fmul_rn(x.w, g.w));
             }
         }
-        stage_group<DT>(xv, i, valid, x);
+        if (!LC || !norm) stage_group<DT, LC>(xv, i, valid, x);
     }
     return ss;
 }
 
 // n elements (n % 4 == 0) of a tagged vector of this step.
-template <int DT>
+template <int DT, bool LC>
 __device__ void stage_tagged(Consumer& c, const unsigned long long* src, int n, float4* xv) {
     const int ngr = n / 4;
     for (int i0 = c.tid - c.lane; i0 < ngr; i0 += kConsumers) {
         const int i = i0 + c.lane;
         const bool valid = i < ngr;
         const float4 v = valid ? poll4(src + 4 * i, c.tag, c.p.err) : make_float4(0.f, 0.f, 0.f, 0.f);
-        stage_group<DT>(xv, i, valid, v);
+        stage_group<DT, LC>(xv, i, valid, v);
     }
 }
 
@@ -808,8 +866,10 @@ __device__ void stage_tagged(Consumer& c, const unsigned long long* src, int n, 
 // split class sg) takes the splits s = sg, sg + NSG, ... in ascending order;
 // the classes' sums are then added in class order (the same bits on every
 // CTA of the group and in every run).  A thread issues its first eight loads
-// before it waits on any of them.
-template <int DT>
+// before it waits on any of them.  Under llama.cpp rounding (LC) the splits'
+// partials are already normalised by the head's global sum (each probability
+// was rounded to F16 after it), so every weight w_s is 1.
+template <int DT, bool LC>
 __device__ void stage_merged(Consumer& c, int layer, int g, float4* xv) {
     const StepParams& p = c.p;
     const int HG = p.n_heads / p.ngrp, hd = p.hd, S = p.splits, MS = p.max_splits;
@@ -832,6 +892,10 @@ __device__ void stage_merged(Consumer& c, int layer, int g, float4* xv) {
     }
     for (int h = c.warp; h < HG; h += kConsumerWarps) {
         const bool has = c.lane < S;
+        if constexpr (LC) {
+            if (has) wgt[h * S + c.lane] = 1.0f;
+            continue;
+        }
         const float2 ml = has ? poll2(pml + 2 * ((size_t)(h0 + h) * MS + c.lane), c.tag, p.err)
                               : make_float2(-INFINITY, 0.f);
         const float M = warp_max(ml.x);
@@ -884,7 +948,7 @@ __device__ void stage_merged(Consumer& c, int layer, int g, float4* xv) {
                 o.w += v.w;
             }
         }
-        stage_group<DT>(xv, q, valid, o);
+        stage_group<DT, LC>(xv, q, valid, o);
     }
 }
 
@@ -892,24 +956,56 @@ __device__ void stage_merged(Consumer& c, int layer, int g, float4* xv) {
 // block's digit record).  A normed phase's warps first pool their sums of
 // squares (pass norm and the thread's sum ss); returns the norm's scale
 // 1/sqrt(mean(x^2) + eps) ("The Forward Pass in Java", Example 4; the sum of
-// squares a float tree sum), or 1.  Every consumer thread must call this (it
-// synchronises).
-template <int DT>
-__device__ float lanes_prep(Consumer& c, const Lanes& L, int n, bool norm, float ss, XReg<DT>& xr) {
+// squares a float tree sum), or 1.  Under llama.cpp rounding (LC) a normed
+// phase's input y = (x * scale) * g is formed and staged here (from the
+// residual and the gains each thread left in shared memory; the same groups
+// as stage_residual) and 1 is returned.  Every consumer thread must call this
+// (it synchronises).
+template <int DT, bool LC>
+__device__ float lanes_prep(Consumer& c, const Lanes& L, int n, bool norm, NormSum<LC> ss, XReg<DT>& xr) {
     const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
     float4* xv = reinterpret_cast<float4*>(c.sm.xs());
     FMARK(c, 1);
     if (norm) {
-        const float w = warp_sum(ss);
-        if (c.lane == 0) c.sm.fred()[c.warp] = w;
+        const NormSum<LC> w = warp_sum(ss);
+        if (c.lane == 0) {
+            if constexpr (LC) c.sm.fred_d()[c.warp] = w;
+            else c.sm.fred()[c.warp] = w;
+        }
     }
     consumer_sync();
     FMARK(c, 4);
     float scale = 1.0f;
     if (norm) {
-        float tot = 0.f;
-        for (int w = 0; w < kConsumerWarps; w++) tot += c.sm.fred()[w];
-        scale = 1.0f / sqrtf(tot / (float)n + c.p.eps);
+        if constexpr (LC) {
+            double tot = 0.0;
+            for (int w = 0; w < kConsumerWarps; w++) tot += c.sm.fred_d()[w];
+            scale = (float)(1.0 / sqrt(tot / (double)n + (double)c.p.eps));
+        } else {
+            float tot = 0.f;
+            for (int w = 0; w < kConsumerWarps; w++) tot += c.sm.fred()[w];
+            scale = 1.0f / sqrtf(tot / (float)n + c.p.eps);
+        }
+    }
+    if constexpr (LC) {
+        if (norm) {
+            const float4* res = reinterpret_cast<const float4*>(c.sm.res());
+            const float4* g4 = reinterpret_cast<const float4*>(c.sm.gains());
+            const int ngr = n / 4;
+            for (int i0 = c.tid - c.lane; i0 < ngr; i0 += kConsumers) {
+                const int i = i0 + c.lane;
+                const bool valid = i < ngr;
+                float4 y = zero;
+                if (valid) {
+                    const float4 x = res[i], g = g4[swz(i)];
+                    y = make_float4(__fmul_rn(__fmul_rn(x.x, scale), g.x), __fmul_rn(__fmul_rn(x.y, scale), g.y),
+                                    __fmul_rn(__fmul_rn(x.z, scale), g.z), __fmul_rn(__fmul_rn(x.w, scale), g.w));
+                }
+                stage_group<DT, LC>(xv, i, valid, y);
+            }
+            consumer_sync();
+            scale = 1.0f;
+        }
     }
     const int col0 = L.col0;
     const bool have = L.active && col0 < n;
@@ -969,7 +1065,7 @@ __device__ __forceinline__ ChunkGeo view_geo(const GView& v, int g) {
 // parks its part of the rows in `rowp`; after the last chunk the consumers
 // finish all rows at once (parts added in warp order, so the result does not
 // depend on timing) and apply the phase's epilogue.
-template <int DT>
+template <int DT, bool LC>
 __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const ChunkGeo& ck, int r0, int r1,
                                              const Lanes& L, const XReg<DT>& xr, float* rowp, Epi& epi, int tk) {
     constexpr int ES = DT == LLM_Q8_0 ? 1 : (DT == LLM_F16 ? 2 : 4);
@@ -1061,7 +1157,7 @@ __device__ __forceinline__ void gemv_consume(Consumer& c, const DMat& m, const C
             epi.row(r0 + i, t);
         }
     }
-    epi.finish(c);
+    epi.template finish<LC>(c);
     // the next phase's staging must not overwrite what a warp still reads
     // (the gains, the (gate, up) sums, the row partials)
     consumer_sync();
@@ -1112,18 +1208,21 @@ __device__ __forceinline__ void store_kv(__half* kc, __half* vc, int pos, int kv
 // ("The Forward Pass in Java", Example 11: scores q.k / sqrt(hd), softmax over
 // the positions, weighted sum of the V rows).  The unit keeps a running max m
 // and sum l per head across its chunks (online softmax) and writes its partial
-// (m, l, acc): acc[h][d] at attn_part[(h*max_splits + s)*hd + d], (m, l) at
-// attn_part[n_heads*max_splits*hd + 2*(h*max_splits + s)].  The last unit of
-// a kv head to finish merges its splits: per head M = max_s m_s,
+// (m, l, acc): acc[h][d] at part[(h*max_splits + s)*hd + d], (m, l) at
+// part[n_heads*max_splits*hd + 2*(h*max_splits + s)].  The O phase merges the
+// splits (stage_merged): per head M = max_s m_s,
 // w_s = e^(m_s - M) / sum_s' e^(m_s' - M) l_s', attn = sum_s w_s acc_s.
 //
 // Scratch shared by both forms of the unit: q_s [gq][hd] (rotated q, F32),
 // kf [hd] (this position's k, F32), kp and vp [hd] each (its K and V rows,
 // F16); the scalar form's score buffers follow.
 
-// q of the unit's heads, rotated, into q_s; the writer (the unit that holds
-// this step's position) rotates k, rounds K and V to F16 into kp/vp and
-// stores them in the cache.  Ends with the scratch visible to all consumers.
+// q of the unit's heads, rotated, into q_s (under llama.cpp rounding, LC,
+// then rounded to F16: the q.k products take an F16 q); the writer (the unit
+// that holds this step's position) rotates k, rounds K and V to F16 into
+// kp/vp and stores them in the cache.  Ends with the scratch visible to all
+// consumers.
+template <bool LC>
 __device__ void attention_prologue(Consumer& c, const LayerDev& L, int layer, int g, bool writer) {
     const StepParams& p = c.p;
     Smem& sm = c.sm;
@@ -1160,6 +1259,8 @@ __device__ void attention_prologue(Consumer& c, const LayerDev& L, int layer, in
     if (writer)
         for (int i = tid; i < p.rope_dims / 2; i += kConsumers) rope_apply(p, sm, kf, i);
     consumer_sync();
+    if constexpr (LC)
+        for (int i = tid; i < GD; i += kConsumers) q_s[i] = f16_round(q_s[i]);
     if (writer && tid < hd) {
         const __half kh = __float2half_rn(kf[tid]);
         kp[tid] = kh;
@@ -1168,6 +1269,17 @@ __device__ void attention_prologue(Consumer& c, const LayerDev& L, int layer, in
     consumer_sync();                                               // kp, vp visible
 }
 
+// Scalar form (any head size).  Under llama.cpp rounding (LC) the unit makes
+// two passes over its positions ("What a Llama model computes, and why" §8:
+// each probability is rounded to F16 after division by the softmax sum over
+// all positions, so that sum must be known first).  Pass 0 reads only the K
+// tiles and finds the unit's (m, l); the units of a kv head exchange them
+// (tagged words after the (m, l) partials; every unit runs on its own CTA, all
+// resident, and each reaches the exchange without waiting on another unit),
+// and each forms the head's M = max_s m_s and L = sum_s e^(m_s - M) l_s from
+// the same values in the same order.  Pass 1 recomputes the scores, takes
+// p_t = f16(e^(s_t - M) / L) and accumulates p_t V_t with no rescaling.
+template <bool LC>
 __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int unit) {
     const StepParams& p = c.p;
     Smem& sm = c.sm;
@@ -1180,11 +1292,11 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
     __half* kp = reinterpret_cast<__half*>(q_s + GD + hd);         // [hd] this position's K row (F16)
     __half* vp = kp + hd;                                          // [hd] this position's V row (F16)
     float* sc = q_s + GD + 2 * hd;                                 // [2][gq][P] scores, then probabilities
-    float* ml = sc + 2 * gq * P;                                   // [2][gq] running max m, sum l
+    float* ml = sc + 2 * gq * P;                                   // [2][gq] running max m, sum l (LC pass 1: M, L)
     float* corr = ml + 2 * gq;                                     // [2][gq] rescale of the chunk's old sums
 
     const bool writer = t0 <= p.pos && p.pos < t1;
-    attention_prologue(c, L, layer, g, writer);
+    attention_prologue<LC>(c, L, layer, g, writer);
     if (tid < gq) { ml[tid] = -INFINITY; ml[gq + tid] = 0.f; }     // read after the first chunk's scores sync
     // PV work split: thread t accumulates the output pair o2 = t % (GD/2)
     // (elements 2*o2, 2*o2+1) over positions with index % NSPLIT == t / (GD/2).
@@ -1196,87 +1308,138 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
     const int nh2 = hd / 2;
     const int prow = p.pos - t0;                                   // this step's position within the unit
     float2 acc = make_float2(0.f, 0.f);
+    unsigned long long* part_acc = c.part(layer);
+    unsigned long long* part_ml = part_acc + (size_t)p.n_heads * p.max_splits * hd;
 
     int ci = 0;
-    for (int c0 = t0; c0 < t1; c0 += P, ci++) {
-        const int np = min(P, t1 - c0);
-        int slot;
-        const uint8_t* buf = c.next_slot(slot);
-        const __half* ks = reinterpret_cast<const __half*>(buf);
-        const __half* vs = ks + (size_t)P * hd;
-        float* scb = sc + (ci & 1) * gq * P;
-        float* corrb = corr + (ci & 1) * gq;
-        // scores: thread (h, position); the K row of this step's position is
-        // the one just computed, not the copy the tile load may have read.
-        // Four partial sums; the start column rotates with the lane so that a
-        // warp's reads fall in different banks.
-        for (int idx = tid; idx < gq * np; idx += kConsumers) {
-            const int h = idx / np, pp = idx % np;
-            const float2* q2 = reinterpret_cast<const float2*>(q_s + h * hd);
-            const __half2* k2 = reinterpret_cast<const __half2*>(
-                writer && c0 + pp - t0 == prow ? kp : ks + (size_t)pp * hd);
-            float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
-            int j = lane % nh2;
-            int k = 0;
-            for (; k + 4 <= nh2; k += 4) {
-                const int j1 = j + 1 == nh2 ? 0 : j + 1;
-                const int j2 = j1 + 1 == nh2 ? 0 : j1 + 1;
-                const int j3 = j2 + 1 == nh2 ? 0 : j2 + 1;
-                a0 = __ffma2_rn(__half22float2(k2[j]), q2[j], a0);
-                a1 = __ffma2_rn(__half22float2(k2[j1]), q2[j1], a1);
-                a2 = __ffma2_rn(__half22float2(k2[j2]), q2[j2], a2);
-                a3 = __ffma2_rn(__half22float2(k2[j3]), q2[j3], a3);
-                j = j3 + 1 == nh2 ? 0 : j3 + 1;
+    for (int pass = 0; pass < (LC ? 2 : 1); pass++) {
+        const bool pv = !LC || pass == 1;                          // this pass accumulates P.V
+        if (LC && pass == 1) {
+            // exchange the splits' (m, l) and form each head's (M, L)
+            consumer_sync();                                       // ml (also when the unit has no positions)
+            unsigned long long* stats = part_ml + 2 * (size_t)p.n_heads * p.max_splits;
+            for (int h = warp; h < gq; h += kConsumerWarps) {
+                const size_t hb = (size_t)(h0 + h) * p.max_splits;
+                const float mo = ml[h], lo = ml[gq + h];
+                if (lane == 0) {
+                    st_tagged(stats + 2 * (hb + s), mo, c.tag);
+                    st_tagged(stats + 2 * (hb + s) + 1, lo, c.tag);
+                }
+                float2 v = make_float2(-INFINITY, 0.f);
+                if (lane < S) v = lane == s ? make_float2(mo, lo) : poll2(stats + 2 * (hb + lane), c.tag, p.err);
+                const float M = warp_max(v.x);
+                const float Ls = warp_sum(v.x == -INFINITY ? 0.f : (float)exp((double)(v.x - M)) * v.y);
+                __syncwarp();
+                if (lane == 0) { ml[h] = M; ml[gq + h] = Ls; }
             }
-            for (; k < nh2; k++) {
-                a0 = __ffma2_rn(__half22float2(k2[j]), q2[j], a0);
-                j = j + 1 == nh2 ? 0 : j + 1;
-            }
-            const float2 a = make_float2((a0.x + a1.x) + (a2.x + a3.x), (a0.y + a1.y) + (a2.y + a3.y));
-            scb[h * P + pp] = __fdiv_rn(a.x + a.y, p.attn_div);
+            consumer_sync();
+            if (c.aborted()) return false;
         }
-        consumer_sync();
-        if (c.aborted()) return false;
-        if (warp < gq) {
-            const int h = warp;
-            float mloc = -INFINITY;
-            for (int pp = lane; pp < np; pp += 32) mloc = fmaxf(mloc, scb[h * P + pp]);
-            mloc = warp_max(mloc);
-            const float mold = ml[h], mnew = fmaxf(mold, mloc);
-            float sum = 0.f;
-            for (int pp = lane; pp < np; pp += 32) {
-                const float e = expf(scb[h * P + pp] - mnew);
-                scb[h * P + pp] = e;
-                sum += e;
+        for (int c0 = t0; c0 < t1; c0 += P, ci++) {
+            const int np = min(P, t1 - c0);
+            int slot;
+            const uint8_t* buf = c.next_slot(slot);
+            const __half* ks = reinterpret_cast<const __half*>(buf);
+            const __half* vs = ks + (size_t)P * hd;
+            float* scb = sc + (ci & 1) * gq * P;
+            float* corrb = corr + (ci & 1) * gq;
+            // scores: thread (h, position); the K row of this step's position is
+            // the one just computed, not the copy the tile load may have read.
+            // Four partial sums; the start column rotates with the lane so that a
+            // warp's reads fall in different banks.
+            for (int idx = tid; idx < gq * np; idx += kConsumers) {
+                const int h = idx / np, pp = idx % np;
+                const float2* q2 = reinterpret_cast<const float2*>(q_s + h * hd);
+                const __half2* k2 = reinterpret_cast<const __half2*>(
+                    writer && c0 + pp - t0 == prow ? kp : ks + (size_t)pp * hd);
+                if constexpr (LC) {
+                    // F16 q times F16 k: every product exact, summed in float in
+                    // dimension order (the oracle's sum, to the bit)
+                    float a = 0.f;
+                    for (int j = 0; j < nh2; j++) {
+                        const float2 kk = __half22float2(k2[j]), qq = q2[j];
+                        a = fmaf(qq.x, kk.x, a);
+                        a = fmaf(qq.y, kk.y, a);
+                    }
+                    scb[h * P + pp] = __fdiv_rn(a, p.attn_div);
+                    continue;
+                }
+                float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+                int j = lane % nh2;
+                int k = 0;
+                for (; k + 4 <= nh2; k += 4) {
+                    const int j1 = j + 1 == nh2 ? 0 : j + 1;
+                    const int j2 = j1 + 1 == nh2 ? 0 : j1 + 1;
+                    const int j3 = j2 + 1 == nh2 ? 0 : j2 + 1;
+                    a0 = __ffma2_rn(__half22float2(k2[j]), q2[j], a0);
+                    a1 = __ffma2_rn(__half22float2(k2[j1]), q2[j1], a1);
+                    a2 = __ffma2_rn(__half22float2(k2[j2]), q2[j2], a2);
+                    a3 = __ffma2_rn(__half22float2(k2[j3]), q2[j3], a3);
+                    j = j3 + 1 == nh2 ? 0 : j3 + 1;
+                }
+                for (; k < nh2; k++) {
+                    a0 = __ffma2_rn(__half22float2(k2[j]), q2[j], a0);
+                    j = j + 1 == nh2 ? 0 : j + 1;
+                }
+                const float2 a = make_float2((a0.x + a1.x) + (a2.x + a3.x), (a0.y + a1.y) + (a2.y + a3.y));
+                scb[h * P + pp] = __fdiv_rn(a.x + a.y, p.attn_div);
             }
-            sum = warp_sum(sum);
-            if (lane == 0) {
-                const float cr = expf(mold - mnew);       // 0 on the first chunk (mold = -inf)
-                ml[h] = mnew;
-                ml[gq + h] = ml[gq + h] * cr + sum;
-                corrb[h] = cr;
+            consumer_sync();
+            if (c.aborted()) return false;
+            if (warp < gq) {
+                const int h = warp;
+                if (LC && pv) {
+                    // the head's global (M, L): e_t = e^(s_t - M) taken in double and
+                    // rounded to float (as the oracle takes it), p_t = f16(e_t / L),
+                    // no rescaling
+                    const float M = ml[h], Ls = ml[gq + h];
+                    for (int pp = lane; pp < np; pp += 32) {
+                        const float e = (float)exp((double)__fsub_rn(scb[h * P + pp], M));
+                        scb[h * P + pp] = f16_round(__fdiv_rn(e, Ls));
+                    }
+                    if (lane == 0) corrb[h] = 1.0f;
+                } else {
+                    auto ex = [](float d) { return LC ? (float)exp((double)d) : expf(d); };
+                    float mloc = -INFINITY;
+                    for (int pp = lane; pp < np; pp += 32) mloc = fmaxf(mloc, scb[h * P + pp]);
+                    mloc = warp_max(mloc);
+                    const float mold = ml[h], mnew = fmaxf(mold, mloc);
+                    float sum = 0.f;
+                    for (int pp = lane; pp < np; pp += 32) {
+                        const float e = ex(__fsub_rn(scb[h * P + pp], mnew));
+                        scb[h * P + pp] = e;
+                        sum += e;
+                    }
+                    sum = warp_sum(sum);
+                    if (lane == 0) {
+                        const float cr = ex(mold - mnew);          // 0 on the first chunk (mold = -inf)
+                        ml[h] = mnew;
+                        ml[gq + h] = ml[gq + h] * cr + sum;
+                        corrb[h] = cr;
+                    }
+                }
             }
+            consumer_sync();
+            if (pv && pv_active) {
+                const float cr = corrb[oh];
+                float2 v0 = make_float2(acc.x * cr, acc.y * cr), v1 = make_float2(0.f, 0.f), v2 = v1, v3 = v1;
+                const float* e = scb + oh * P;
+                auto vrow = [&](int pp) {
+                    const __half* r = writer && c0 + pp - t0 == prow ? vp : vs + (size_t)pp * hd;
+                    return __half22float2(*reinterpret_cast<const __half2*>(r + oi));
+                };
+                int pp = sp;
+                for (; pp + 3 * NSPLIT < np; pp += 4 * NSPLIT) {
+                    v0 = __ffma2_rn(make_float2(e[pp], e[pp]), vrow(pp), v0);
+                    v1 = __ffma2_rn(make_float2(e[pp + NSPLIT], e[pp + NSPLIT]), vrow(pp + NSPLIT), v1);
+                    v2 = __ffma2_rn(make_float2(e[pp + 2 * NSPLIT], e[pp + 2 * NSPLIT]), vrow(pp + 2 * NSPLIT), v2);
+                    v3 = __ffma2_rn(make_float2(e[pp + 3 * NSPLIT], e[pp + 3 * NSPLIT]), vrow(pp + 3 * NSPLIT), v3);
+                }
+                for (; pp < np; pp += NSPLIT) v0 = __ffma2_rn(make_float2(e[pp], e[pp]), vrow(pp), v0);
+                acc = make_float2((v0.x + v1.x) + (v2.x + v3.x), (v0.y + v1.y) + (v2.y + v3.y));
+            }
+            c.release(slot);
         }
-        consumer_sync();
-        if (pv_active) {
-            const float cr = corrb[oh];
-            float2 v0 = make_float2(acc.x * cr, acc.y * cr), v1 = make_float2(0.f, 0.f), v2 = v1, v3 = v1;
-            const float* e = scb + oh * P;
-            auto vrow = [&](int pp) {
-                const __half* r = writer && c0 + pp - t0 == prow ? vp : vs + (size_t)pp * hd;
-                return __half22float2(*reinterpret_cast<const __half2*>(r + oi));
-            };
-            int pp = sp;
-            for (; pp + 3 * NSPLIT < np; pp += 4 * NSPLIT) {
-                v0 = __ffma2_rn(make_float2(e[pp], e[pp]), vrow(pp), v0);
-                v1 = __ffma2_rn(make_float2(e[pp + NSPLIT], e[pp + NSPLIT]), vrow(pp + NSPLIT), v1);
-                v2 = __ffma2_rn(make_float2(e[pp + 2 * NSPLIT], e[pp + 2 * NSPLIT]), vrow(pp + 2 * NSPLIT), v2);
-                v3 = __ffma2_rn(make_float2(e[pp + 3 * NSPLIT], e[pp + 3 * NSPLIT]), vrow(pp + 3 * NSPLIT), v3);
-            }
-            for (; pp < np; pp += NSPLIT) v0 = __ffma2_rn(make_float2(e[pp], e[pp]), vrow(pp), v0);
-            acc = make_float2((v0.x + v1.x) + (v2.x + v3.x), (v0.y + v1.y) + (v2.y + v3.y));
-        }
-        c.release(slot);
     }
     // combine the PV position splits and write this unit's partial
     if (pv_active) {
@@ -1284,8 +1447,6 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
         sm.comb()[sp * GD + 2 * o2 + 1] = acc.y;
     }
     consumer_sync();
-    unsigned long long* part_acc = c.part(layer);
-    unsigned long long* part_ml = part_acc + (size_t)p.n_heads * p.max_splits * hd;
     for (int oo = tid; oo < GD; oo += kConsumers) {
         float v = 0.f;
         for (int k = 0; k < NSPLIT; k++) v += sm.comb()[k * GD + oo];
@@ -1349,7 +1510,7 @@ __device__ bool attention_unit_mma(Consumer& c, const LayerDev& L, int layer, in
     const __half* kp = reinterpret_cast<const __half*>(q_s + GD + HD);
     const __half* vp = kp + HD;
     const bool writer = t0 <= p.pos && p.pos < t1;
-    attention_prologue(c, L, layer, g, writer);
+    attention_prologue<false>(c, L, layer, g, writer);
     if (tid == 0) trace_mark(p, 576 + 4 * layer);
 
     // A fragments of q: row r = lane / 4 is part (r & 1) of head r / 2
@@ -1517,7 +1678,9 @@ __device__ bool attention_unit_mma(Consumer& c, const LayerDev& L, int layer, in
     return true;
 }
 
+template <bool LC>
 __device__ bool attention_any(Consumer& c, const LayerDev& L, int layer, int unit) {
+    if constexpr (LC) return attention_unit<true>(c, L, layer, unit);   // the two-pass scalar form
     if (c.p.attn_mma) {
         switch (c.p.hd) {
             case 32: return attention_unit_mma<32>(c, L, layer, unit);
@@ -1526,10 +1689,10 @@ __device__ bool attention_any(Consumer& c, const LayerDev& L, int layer, int uni
             default: break;
         }
     }
-    return attention_unit(c, L, layer, unit);
+    return attention_unit<false>(c, L, layer, unit);
 }
 // ----------------------------------------------------------------- kernel --
-template <int DT>
+template <int DT, bool LC>
 __device__ bool consumer_main(const StepParams& p, Smem& sm) {
     Consumer c(p, sm);
     const int tid = c.tid, G = gridDim.x;
@@ -1609,7 +1772,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
             if (tid == 0) trace_mark(p, 10 * l + 2);
             const int units = p.n_kv * p.splits;
             for (int unit = blockIdx.x; unit < units; unit += G)
-                if (!attention_any(c, L, l, unit)) return false;
+                if (!attention_any<LC>(c, L, l, unit)) return false;
             if (tid == 0) trace_mark(p, 10 * l + 3);
             m = p.ov.m;
             r0 = rg0;
@@ -1652,17 +1815,17 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
         c.fine = !last && l == 8 ? 960 + 16 * k : -1;
 #endif
         FMARK(c, 0);
-        float ss = 0.f;
-        if (src == kSrcResidual) ss = stage_residual<DT>(c, sv, token, gains != nullptr, xv);
-        else if (src == kSrcTagged) stage_tagged<DT>(c, sv, n, xv);
-        else stage_merged<DT>(c, l, pt.g, xv);
+        NormSum<LC> ss = 0;
+        if (src == kSrcResidual) ss = stage_residual<DT, LC>(c, sv, token, gains != nullptr, xv);
+        else if (src == kSrcTagged) stage_tagged<DT, LC>(c, sv, n, xv);
+        else stage_merged<DT, LC>(c, l, pt.g, xv);
         const Lanes Ln = lane_layout<DT>(c, m);
         XReg<DT> xr;
-        e.scale = lanes_prep<DT>(c, Ln, n, gains != nullptr, ss, xr);
+        e.scale = lanes_prep<DT, LC>(c, Ln, n, gains != nullptr, ss, xr);
         FMARK(c, 5);
         const int jt = last ? -1 : k;                               // trace: QKV 0, O 1, GU 2, DOWN 3
         if (tid == 0 && jt >= 0) trace_mark(p, 512 + 4 * l + jt);
-        gemv_consume<DT>(c, m, ck, r0, r1, Ln, xr, rowp, e, jt >= 0 ? 160 + 4 * l + jt : -1);
+        gemv_consume<DT, LC>(c, m, ck, r0, r1, Ln, xr, rowp, e, jt >= 0 ? 160 + 4 * l + jt : -1);
         if (last) {
             best = e.best;
         } else {
@@ -1702,7 +1865,7 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
     return true;
 }
 
-template <int DT>
+template <int DT, bool LC>
 __device__ void producer_main(const StepParams& p, Smem& sm) {
     Producer pr(p, sm);
     const Part pt = cta_part(p.ngrp);
@@ -1717,7 +1880,7 @@ __device__ void producer_main(const StepParams& p, Smem& sm) {
         int q0, q1;
         cta_rows(L.qkv.rows, q0, q1);
         pr.rows(L.qkv, DT, q0, q1, 256 + 8 * l);
-        pr.attention(l);
+        pr.attention(l, LC);
         pr.view(p.ov, layer_map(p, l, 2), layer_map(p, l, 3), pt.g, rg0, rg1, 256 + 8 * l + 2);
         pr.rows(L.gu, DT, 2 * u0, 2 * u1, 256 + 8 * l + 3);
         pr.view(p.dv, layer_map(p, l, 4), layer_map(p, l, 5), pt.g, rg0, rg1, 256 + 8 * l + 4);
@@ -1730,7 +1893,7 @@ __device__ void producer_main(const StepParams& p, Smem& sm) {
     pr.drain();   // on success every chunk was consumed and the waits return at once
 }
 
-template <int DT>
+template <int DT, bool LC>
 __global__ void __launch_bounds__(kBlock, 1) decode_step_kernel(const __grid_constant__ StepParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the ring starts on a 1024-byte boundary (the swizzled KV tiles rely on it)
@@ -1746,10 +1909,10 @@ __global__ void __launch_bounds__(kBlock, 1) decode_step_kernel(const __grid_con
     }
     __syncthreads();
     if (threadIdx.x >= kConsumers) {
-        if (threadIdx.x == kConsumers) producer_main<DT>(p, sm);
+        if (threadIdx.x == kConsumers) producer_main<DT, LC>(p, sm);
         __syncwarp();
     } else {
-        consumer_main<DT>(p, sm);
+        consumer_main<DT, LC>(p, sm);
     }
     block_join();
 }
@@ -1836,7 +1999,7 @@ bool gview_plan(GView& v, int wtype, int rows, int cols, int ngrp, int max_rows)
 // phase keeps them in the residual region).  Returns false if the model does
 // not fit the kernel's limits.
 bool step_geometry(StepParams& p, int dim, int stage_floats, int n_heads, int n_kv, int hd, int rope_dims,
-                   int rowp_floats, int rowp_logits, size_t* smem_bytes) {
+                   int rowp_floats, int rowp_logits, bool llamacpp, size_t* smem_bytes) {
     const int gq = n_heads / n_kv;
     // KV rows per slot: K and V tiles of P rows fill a slot, at most 256 (a TMA
     // box side), and the unit's scores (2 * gq * P floats) stay within 8 KB
@@ -1847,8 +2010,9 @@ bool step_geometry(StepParams& p, int dim, int stage_floats, int n_heads, int n_
     if (P < 8) return false;
     const int GD = gq * hd;
     // tensor-core attention for the head sizes it is instantiated for
-    // (head_dim 128 would need more registers than the kernel has to spare)
-    p.attn_mma = (hd == 32 || hd == 48 || hd == 64) && gq <= 4;
+    // (head_dim 128 would need more registers than the kernel has to spare);
+    // llama.cpp rounding takes the two-pass scalar form
+    p.attn_mma = !llamacpp && (hd == 32 || hd == 48 || hd == 64) && gq <= 4;
     p.attn_w = p.attn_mma && hd % 64 == 0 ? 64 : hd;
     // q_s, kf, kp/vp; the scalar form adds its score buffers
     const size_t attn_scratch =
@@ -1883,11 +2047,18 @@ bool step_geometry(StepParams& p, int dim, int stage_floats, int n_heads, int n_
     return *smem_bytes <= (size_t)kMaxSmem;
 }
 
-const void* step_kernel_ptr(int wtype) {
+const void* step_kernel_ptr(int wtype, bool llamacpp) {
+    if (llamacpp) {
+        switch (wtype) {
+            case LLM_Q8_0: return (const void*)decode_step_kernel<LLM_Q8_0, true>;
+            case LLM_F16: return (const void*)decode_step_kernel<LLM_F16, true>;
+            default: return (const void*)decode_step_kernel<LLM_F32, true>;
+        }
+    }
     switch (wtype) {
-        case LLM_Q8_0: return (const void*)decode_step_kernel<LLM_Q8_0>;
-        case LLM_F16: return (const void*)decode_step_kernel<LLM_F16>;
-        default: return (const void*)decode_step_kernel<LLM_F32>;
+        case LLM_Q8_0: return (const void*)decode_step_kernel<LLM_Q8_0, false>;
+        case LLM_F16: return (const void*)decode_step_kernel<LLM_F16, false>;
+        default: return (const void*)decode_step_kernel<LLM_F32, false>;
     }
 }
 
@@ -1909,8 +2080,10 @@ __global__ void dequant_rows_kernel(DMat m, int row0, int n_rows, float* out) {
 // matrix chosen by `which` (0 QKV, 1 Wo by column groups, 2 gate/up, 3 Wdown
 // by column groups, 4 the logits matrix).  x: the product's input vector (F32);
 // y: its rows, or for 1 and 3 [ngrp][dim] the column groups' partial
-// products.  No grid-wide dependency: every CTA computes its own rows.
-template <int DT>
+// products.  LC: the staging of llama.cpp rounding (x quantized to Q8_0
+// blocks, or rounded to F16).  No grid-wide dependency: every CTA computes
+// its own rows.
+template <int DT, bool LC>
 __global__ void __launch_bounds__(kBlock, 1) gemv_test_kernel(const __grid_constant__ StepParams p, int which,
                                                               int layer, const float* x, float* y) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1958,8 +2131,8 @@ __global__ void __launch_bounds__(kBlock, 1) gemv_test_kernel(const __grid_const
         for (int i0 = c.tid - c.lane; i0 < ngr; i0 += kConsumers) {
             const int i = i0 + c.lane;
             const bool valid = i < ngr;
-            stage_group<DT>(xv, i, valid,
-                            valid ? reinterpret_cast<const float4*>(xs)[i] : make_float4(0.f, 0.f, 0.f, 0.f));
+            stage_group<DT, LC>(xv, i, valid,
+                                valid ? reinterpret_cast<const float4*>(xs)[i] : make_float4(0.f, 0.f, 0.f, 0.f));
         }
         const Lanes Ln = lane_layout<DT>(c, m);
         XReg<DT> xr;
@@ -1967,18 +2140,21 @@ __global__ void __launch_bounds__(kBlock, 1) gemv_test_kernel(const __grid_const
         e.kind = Epi::kLogits;
         e.logits = ys;
         e.err = p.err;
-        e.scale = lanes_prep<DT>(c, Ln, n, false, 0.f, xr);
+        e.scale = lanes_prep<DT, LC>(c, Ln, n, false, 0.f, xr);
         const ChunkGeo ck = v ? view_geo(*v, pt.g) : rows_geo(m, DT);
-        gemv_consume<DT>(c, m, ck, r0, r1, Ln, xr, which == 4 ? sm.res() : sm.rowp(), e, -1);
+        gemv_consume<DT, LC>(c, m, ck, r0, r1, Ln, xr, which == 4 ? sm.res() : sm.rowp(), e, -1);
     }
     block_join();
 }
 
-cudaError_t launch_gemv_test(cudaStream_t st, int wtype, const StepParams& p, int which, int layer, const float* x,
-                             float* y, int sms, size_t smem) {
-    const void* fn = wtype == LLM_Q8_0 ? (const void*)gemv_test_kernel<LLM_Q8_0>
-                     : wtype == LLM_F16 ? (const void*)gemv_test_kernel<LLM_F16>
-                                        : (const void*)gemv_test_kernel<LLM_F32>;
+cudaError_t launch_gemv_test(cudaStream_t st, int wtype, bool llamacpp, const StepParams& p, int which, int layer,
+                             const float* x, float* y, int sms, size_t smem) {
+    const void* fn = llamacpp ? (wtype == LLM_Q8_0 ? (const void*)gemv_test_kernel<LLM_Q8_0, true>
+                                 : wtype == LLM_F16 ? (const void*)gemv_test_kernel<LLM_F16, true>
+                                                    : (const void*)gemv_test_kernel<LLM_F32, true>)
+                              : (wtype == LLM_Q8_0 ? (const void*)gemv_test_kernel<LLM_Q8_0, false>
+                                 : wtype == LLM_F16 ? (const void*)gemv_test_kernel<LLM_F16, false>
+                                                    : (const void*)gemv_test_kernel<LLM_F32, false>);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     StepParams q = p;

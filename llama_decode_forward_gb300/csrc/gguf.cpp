@@ -550,6 +550,7 @@ extern "C" int llm_gguf_config(const llm_gguf* g, int32_t max_seq, llm_config* c
     cfg->rope_base = (float)base;
     cfg->rope_neox = a == "qwen2";
     cfg->wtype = embd->type;
+    cfg->numerics = LLM_NUMERICS_EXACT;
     return LLM_OK;
 }
 

@@ -17,14 +17,14 @@
 
 namespace llm {
 bool step_geometry(StepParams& p, int dim, int stage_floats, int n_heads, int n_kv, int hd, int rope_dims,
-                   int rowp_floats, int rowp_logits, size_t* smem_bytes);
+                   int rowp_floats, int rowp_logits, bool llamacpp, size_t* smem_bytes);
 bool matrix_plan(DMat& m, int wtype, bool pair);
 bool gview_plan(GView& v, int wtype, int rows, int cols, int ngrp, int max_rows);
-const void* step_kernel_ptr(int wtype);
+const void* step_kernel_ptr(int wtype, bool llamacpp);
 void launch_kv_store(cudaStream_t st, __half* kc, __half* vc, int pos, int kv_dim, const float* k, const float* v);
 void launch_dequant_rows(cudaStream_t st, int wtype, const DMat& m, int row0, int n_rows, float* out);
-cudaError_t launch_gemv_test(cudaStream_t st, int wtype, const StepParams& p, int which, int layer, const float* x,
-                             float* y, int sms, size_t smem);
+cudaError_t launch_gemv_test(cudaStream_t st, int wtype, bool llamacpp, const StepParams& p, int which, int layer,
+                             const float* x, float* y, int sms, size_t smem);
 }  // namespace llm
 
 using namespace llm;
@@ -191,6 +191,8 @@ static int validate_config(const llm_config* c, llm_handle* h) {
     if (c->rope_dims <= 0 || c->rope_dims % 2 || c->rope_dims > c->head_dim)
         return fail(h, LLM_ERR_INVALID_ARG, "rope_dims must be even and in (0, head_dim]");
     if (!(c->eps >= 0.f) || !(c->rope_base > 0.f)) return fail(h, LLM_ERR_INVALID_ARG, "bad eps or rope_base");
+    if (c->numerics != LLM_NUMERICS_EXACT && c->numerics != LLM_NUMERICS_LLAMACPP)
+        return fail(h, LLM_ERR_INVALID_ARG, "numerics must be LLM_NUMERICS_EXACT or LLM_NUMERICS_LLAMACPP");
     if (c->wtype != LLM_F32 && c->wtype != LLM_F16 && c->wtype != LLM_Q8_0)
         return fail(h, LLM_ERR_UNSUPPORTED, "weight type %d not supported", c->wtype);
     const int mult = c->wtype == LLM_Q8_0 ? 32 : (c->wtype == LLM_F16 ? 8 : 4);
@@ -436,7 +438,7 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
 
     h->theta_scale = (float)pow((double)c.rope_base, -2.0 / (double)c.rope_dims);
     h->attn_div = (float)sqrt((double)c.head_dim);
-    h->kernel = step_kernel_ptr(c.wtype);
+    h->kernel = step_kernel_ptr(c.wtype, c.numerics == LLM_NUMERICS_LLAMACPP);
     // row partials a CTA keeps for one GEMV phase (multi-warp teams): its rows
     // times the warps of a team; the logits phase's are kept apart
     int rowp_floats = 0, rowp_logits = 0;
@@ -451,7 +453,7 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
         rowp_logits = (h->out.rows + h->sms - 1) / h->sms * parts(h->out);
     }
     if (!step_geometry(h->geo, d, std::max(gdg, fdg), c.n_heads, c.n_kv_heads, c.head_dim, c.rope_dims, rowp_floats,
-                       rowp_logits, &h->smem))
+                       rowp_logits, c.numerics == LLM_NUMERICS_LLAMACPP, &h->smem))
         return create_failed(h, fail(h, LLM_ERR_UNSUPPORTED, "the step's shared-memory layout does not fit"));
     // per-CTA shares that live in shared memory, and every matrix's plan
     if ((q + 2 * kv + h->sms - 1) / h->sms > kOwnFloats || 2 * ((fdg + min_gsz - 1) / min_gsz) > kOwnFloats)
@@ -766,7 +768,8 @@ extern "C" int llm_test_gemv(llm_handle* h, int which, int layer, const float* x
     if (h->broken) return fail(h, LLM_ERR_STATE, "handle has a device error; call llm_reset");
     StepParams p = step_params(h, h->tok_in, 0, h->tok_out);
     p.trace = nullptr;
-    CK(h, launch_gemv_test(h->st, h->cfg.wtype, p, which, layer, x_dev, y_dev, h->sms, h->smem));
+    CK(h, launch_gemv_test(h->st, h->cfg.wtype, h->cfg.numerics == LLM_NUMERICS_LLAMACPP, p, which, layer, x_dev,
+                           y_dev, h->sms, h->smem));
     h->launches++;
     CK(h, cudaStreamSynchronize(h->st));
     return read_device_error(h);

@@ -130,9 +130,11 @@ struct StepParams {
 constexpr int kMapsPerLayer = 6;
 
 // Attention partials of one layer: acc [n_heads][max_splits][hd], then (m, l)
-// [n_heads][max_splits][2] (tagged words).
+// [n_heads][max_splits][2], then the score statistics the llama.cpp-rounding
+// step exchanges before its second pass [n_heads][max_splits][2] (tagged
+// words).
 __host__ __device__ inline long long part_words_per_layer(int n_heads, int max_splits, int hd) {
-    long long w = (long long)n_heads * max_splits * (hd + 2);
+    long long w = (long long)n_heads * max_splits * (hd + 4);
     return w + (w & 1);
 }
 
@@ -396,6 +398,12 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
 __device__ __forceinline__ void block_join() { asm volatile("bar.sync 2, %0;" ::"n"(kBlock) : "memory"); }
 
 __device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;

@@ -119,6 +119,7 @@ class ModelConfig:
     bias: bool = False
     rope_freqs: bool = False          # pass explicit (unit) frequency factors
     number: int = 0                   # workload number, picks the seeds
+    numerics: int = 0                 # llm_numerics of the library handle (0 exact, 1 llama.cpp rounding)
 
     @property
     def rope_dims(self) -> int:

@@ -65,6 +65,8 @@ def _weights(n_layers=2, null_field=None):
     (dict(wtype=L.LLM_F16, ffn_dim=100), L.LLM_ERR_UNSUPPORTED),
     (dict(dim=4 * 320, head_dim=320, ffn_dim=96), L.LLM_ERR_UNSUPPORTED),   # head_dim > 256
     (dict(max_seq=-1), L.LLM_ERR_INVALID_ARG),
+    (dict(numerics=2), L.LLM_ERR_INVALID_ARG),
+    (dict(numerics=-1), L.LLM_ERR_INVALID_ARG),
 ])
 def test_create_rejects_bad_config(kw, status):
     with pytest.raises(L.LlmError) as e:
