@@ -41,6 +41,7 @@ CFG = synth.LLAMA1B_Q8
 DECODE_MODELS = {"llama1b_q8": (synth.LLAMA1B_Q8, "llama-3.2-1b-shape q8_0"),
                  "llama7b_q8": (synth.LLAMA7B_Q8, "llama-2-7b-shape q8_0")}
 DTYPE = "q8_0 weights x 24-bit block fixed-point activations (dp4a), f32 accumulate"
+DTYPE_LLAMACPP = "q8_0 weights x q8_0-quantized activations (dp4a), f32 accumulate; f16 attention probabilities"
 KERNEL_SOURCES = ["llama_decode_forward_gb300/csrc/decode_step.cu", "llama_decode_forward_gb300/csrc/llm_internal.cuh"]
 
 
@@ -172,7 +173,7 @@ def cpu_oracle_sample(W, tok: int, budget_s: float = 12.0, min_steps: int = 1, m
     `threads` > 1 its row-split variant (bitwise the same results)."""
     import oracle
     cfg = cfg or CFG
-    ora = oracle.OracleModel(cfg, W, max_seq=pos + 1)
+    ora = oracle.OracleModel(cfg, W, max_seq=pos + 1, llamacpp_rounding=bool(getattr(cfg, "numerics", 0)))
     for l in range(cfg.n_layers):
         for which in (0, 1):
             if pos:
@@ -240,8 +241,9 @@ def run_ours(args):
 
     cfg, label = DECODE_MODELS[args.model]
     pos = POS if args.pos is None else args.pos
-    headline = args.model == "llama1b_q8" and pos == POS
-    cfg = cfg.scaled(max_seq=max(cfg.max_seq if headline else 0, pos + 1))
+    lc = args.numerics == "llamacpp"
+    headline = args.model == "llama1b_q8" and pos == POS and not lc
+    cfg = cfg.scaled(max_seq=max(cfg.max_seq if headline else 0, pos + 1), numerics=int(lc))
     W = synth.make_weights(cfg)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
@@ -315,12 +317,14 @@ def run_ours(args):
     traffic = stored_traffic() if headline else None
     pct = percentiles(per_launch)
     line = {
-        "metric": METRIC if headline else f"decode tok/s @batch1 ({label}, step at pos {pos}); % HBM roofline",
+        "metric": METRIC if headline else (f"decode tok/s @batch1 ({label}, step at pos {pos}"
+                                           f"{', llama.cpp rounding' if lc else ''}); % HBM roofline"),
         "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_LLAMACPP if lc else DTYPE,
         "data": "synthetic (seeded random Q8_0 weights and KV rows)",
-        "config": {"workload": f"{label} decode, batch 1, step at pos {pos} (ctx {pos + 1})",
+        "config": {"workload": f"{label} decode, batch 1, step at pos {pos} (ctx {pos + 1})"
+                               + (", llama.cpp rounding" if lc else ""),
                    "n_layers": cfg.n_layers, "dim": cfg.dim, "vocab": cfg.vocab, "pos": pos,
                    "bytes_per_step": nbytes,
                    "l2": f"working set {nbytes / 1e9:.2f} GB > 129 MB L2; no flush",
@@ -328,7 +332,7 @@ def run_ours(args):
         "launch_ms": pct,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "decode_step_kernel<Q8_0> (whole step, one launch)",
+                     "kernel": f"decode_step_kernel<Q8_0{', llama.cpp rounding' if lc else ''}> (whole step, one launch)",
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
                      "frac_of_8tbs_nominal": achieved / 8000.0,
                      "frac_at_median_launch": nbytes / (pct["median"] / 1000.0) / 1e9 / peaks["hbm_gbs"]},
@@ -441,6 +445,8 @@ def main():
                     help="weight type of the prefill line's model")
     ap.add_argument("--model", choices=sorted(DECODE_MODELS), default="llama1b_q8",
                     help="decode workload's model: the Llama-3.2-1B shape (the headline) or the Llama-2-7B shape")
+    ap.add_argument("--numerics", choices=["exact", "llamacpp"], default="exact",
+                    help="the decode step's rounding (llm_config.numerics); llamacpp is not the headline")
     ap.add_argument("--pos", type=int, default=None,
                     help="position of the timed decode step (rows 0..pos-1 pre-filled); default 4095")
     args = ap.parse_args()
