@@ -49,9 +49,12 @@ typedef enum {
     LLM_ERR_NO_MEMORY = -5,       /* device allocation failed */
     LLM_ERR_DEVICE_TIMEOUT = -6,  /* a bounded wait inside a kernel gave up; the step's outputs are invalid */
     LLM_ERR_STATE = -7,           /* call not valid in the handle's state (e.g. after a device error) */
-    LLM_ERR_NONFINITE = -8        /* a residual-stream update was NaN, infinite or not below 2^15 in
+    LLM_ERR_NONFINITE = -8,       /* a residual-stream update was NaN, infinite or not below 2^15 in
                                      magnitude (the decode step's fixed-point accumulators); the step's
                                      outputs are invalid and the handle needs llm_reset */
+    LLM_ERR_CHECK = -9            /* libraries built with LLM_CHECKED only: a device-side index check of
+                                     the decode step failed and the access it guarded was skipped; the
+                                     step's outputs are invalid and the handle needs llm_reset */
 } llm_status;
 
 /* Rounding of the decode step ("What a Llama model computes, and why" §8).
@@ -209,6 +212,37 @@ int llm_test_dequant_rows(llm_handle *h, int which, int layer, int32_t row0, int
  * Synchronous.  Errors: INVALID_ARG, OUT_OF_RANGE (layer), STATE, CUDA. */
 int llm_test_gemv(llm_handle *h, int which, int layer, const float *x_dev, float *y_dev);
 
+/* 1 if this library was built with LLM_CHECKED (device-side index checks on
+ * the decode step's global writes and weight-stream ranges, reporting
+ * LLM_ERR_CHECK instead of trapping), else 0. */
+int llm_checked_build(void);
+
+/* Test hook of LLM_CHECKED builds: the index check of the decode step's
+ * logits writes accepts only indices below `limit` (0 restores vocab), so a
+ * test can see a failing check reported as LLM_ERR_CHECK with the writes past
+ * `limit` skipped.  Errors: UNSUPPORTED in other builds, OUT_OF_RANGE. */
+int llm_test_logits_limit(llm_handle *h, int32_t limit);
+
+/* Test hook: allocation failure.  The nth device or pinned-host allocation
+ * the library makes from now on (in llm_create, llm_create_from_gguf or
+ * llm_prefill's workspace) fails as if the device were out of memory, once;
+ * 0 disarms.  The failing call returns LLM_ERR_NO_MEMORY and releases what it
+ * had allocated.  Process-wide.  Errors: INVALID_ARG for nth < 0. */
+int llm_test_fail_alloc(int32_t nth);
+
+/* Test hook: guard bands.  The KV cache, the activation buffer and the
+ * prefill workspace are allocated with 4096 bytes more on each side, filled
+ * with 0xA5.  Returns how many of those bytes differ from 0xA5 (0: no kernel
+ * wrote past either end of these buffers), or a negative status.
+ * Synchronous. */
+int64_t llm_test_guards(llm_handle *h);
+
+/* Test hook: overwrites the guard byte adjacent to one end of a guarded
+ * buffer (band 2b: before buffer b, 2b+1: after it; b = 0 KV cache,
+ * 1 activations, 2 prefill workspace once allocated), so that a test can see
+ * llm_test_guards report it.  Synchronous.  Errors: OUT_OF_RANGE. */
+int llm_test_poke_guard(llm_handle *h, int band);
+
 /* The number of column groups the decode step splits the output and down
  * projections into (a divisor of n_kv_heads), or INVALID_ARG for NULL. */
 int llm_column_groups(const llm_handle *h);
@@ -251,7 +285,13 @@ int llm_decode_step_noalloc(llm_handle *h, const int32_t *token_dev, int32_t pos
 /* Number of kernel launches enqueued on the handle's stream so far (all calls). */
 int64_t llm_launch_count(const llm_handle *h);
 
-/* Releases every device buffer of the handle (after waiting for its stream). */
+/* Releases every device buffer of the handle (after waiting for its stream).
+ * The library keeps a set of the handles llm_create returned and that are
+ * not yet destroyed: every call refuses any other pointer with
+ * LLM_ERR_INVALID_ARG (llm_logits_device returns NULL, llm_launch_count 0),
+ * and llm_destroy of such a pointer (a second destroy, NULL) does nothing.
+ * A pointer that a later llm_create happens to return again names that new
+ * handle. */
 void llm_destroy(llm_handle *h);
 
 const char *llm_status_string(int status);

@@ -18,6 +18,7 @@ LLM_F32, LLM_F16, LLM_Q8_0 = 0, 1, 8
 LLM_OK = 0
 LLM_ERR_INVALID_ARG, LLM_ERR_UNSUPPORTED, LLM_ERR_OUT_OF_RANGE = -1, -2, -3
 LLM_ERR_CUDA, LLM_ERR_NO_MEMORY, LLM_ERR_DEVICE_TIMEOUT, LLM_ERR_STATE, LLM_ERR_NONFINITE = -4, -5, -6, -7, -8
+LLM_ERR_CHECK = -9
 LLM_NUMERICS_EXACT, LLM_NUMERICS_LLAMACPP = 0, 1
 
 
@@ -86,6 +87,11 @@ _SIGS = {
     "llm_create_from_gguf": ([_vp, _i32, _vp, ctypes.POINTER(_vp), ctypes.c_char_p, ctypes.c_size_t], _int),
     "llm_status_string": ([_int], ctypes.c_char_p),
     "llm_last_error": ([_vp], ctypes.c_char_p),
+    "llm_test_fail_alloc": ([_i32], _int),
+    "llm_checked_build": ([], _int),
+    "llm_test_logits_limit": ([_vp, _i32], _int),
+    "llm_test_guards": ([_vp], ctypes.c_int64),
+    "llm_test_poke_guard": ([_vp, _int], _int),
 }
 
 
@@ -99,7 +105,14 @@ def declared_symbols(header: str | None = None) -> list[str]:
 
 
 def load_library(path: str | None = None):
-    lib = ctypes.CDLL(path or _build.build())
+    """The library at `path`, or the in-tree build: LLM_DECODE_VARIANT=checked
+    (device-side index checks) or =trace (phase stamps) selects a variant."""
+    if path is None:
+        variant = os.environ.get("LLM_DECODE_VARIANT", "")
+        if variant not in ("", "checked", "trace"):
+            raise ValueError(f"LLM_DECODE_VARIANT={variant!r}: expected checked or trace")
+        path = _build.build(checked=variant == "checked", trace=variant == "trace")
+    lib = ctypes.CDLL(path)
     for name, (args, res) in _SIGS.items():
         fn = getattr(lib, name)
         fn.argtypes = args
@@ -216,6 +229,31 @@ def llm_test_gemv(h, which: int, layer: int, x_dev, y_dev):
 
 def llm_column_groups(h) -> int:
     return int(_lib.llm_column_groups(h))
+
+
+def llm_checked_build() -> bool:
+    return bool(_lib.llm_checked_build())
+
+
+def llm_test_logits_limit(h, limit: int) -> None:
+    _check(_lib.llm_test_logits_limit(h, int(limit)), h)
+
+
+def llm_test_fail_alloc(nth: int) -> None:
+    _check(_lib.llm_test_fail_alloc(int(nth)))
+
+
+def llm_test_guards(h) -> int:
+    """Changed guard-band bytes around the handle's KV cache, activations
+    and prefill workspace (0 when intact)."""
+    n = int(_lib.llm_test_guards(h))
+    if n < 0:
+        _check(n, h)
+    return n
+
+
+def llm_test_poke_guard(h, band: int) -> None:
+    _check(_lib.llm_test_poke_guard(h, int(band)), h)
 
 
 def llm_decode_step_noalloc(h, token_dev, pos: int, logits_dev, argmax_dev):

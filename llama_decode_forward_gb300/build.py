@@ -16,6 +16,10 @@ LIB = os.path.join(OUT_DIR, "libllmdecode.so")
 # kernel also records per-CTA phase timestamps readable with llm_trace_read.
 TRACE_DIR = os.path.join(OUT_DIR, "trace")
 TRACE_LIB = os.path.join(TRACE_DIR, "libllmdecode_trace.so")
+# Variant with device-side index checks (-DLLM_CHECKED): same ABI; a failed
+# check skips the access and the call returns LLM_ERR_CHECK.
+CHECKED_DIR = os.path.join(OUT_DIR, "checked")
+CHECKED_LIB = os.path.join(CHECKED_DIR, "libllmdecode_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               f"-I{os.path.join(ROOT, 'include')}"]
@@ -43,9 +47,11 @@ def up_to_date(lib: str = LIB) -> bool:
     return all(os.path.getmtime(s) <= t for s in _inputs())
 
 
-def compile_command(src: str, obj: str, trace: bool = False, verbose: bool = False) -> list[str]:
+def compile_command(src: str, obj: str, trace: bool = False, verbose: bool = False,
+                    checked: bool = False) -> list[str]:
     """The nvcc command that compiles one source for sm_103a."""
-    cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *(["-DLLM_TRACE"] if trace else []), "-c", src, "-o", obj]
+    cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *(["-DLLM_TRACE"] if trace else []), *(["-DLLM_CHECKED"] if checked else []),
+           "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     return cmd
@@ -56,17 +62,20 @@ def link_command(objs: list[str], out: str) -> list[str]:
     return [_nvcc(), *ARCH, "-shared", "-o", out, *objs]
 
 
-def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, trace: bool = False, checked: bool = False) -> str:
     """Compile every .cu under csrc/ (in parallel) and link the shared library
-    (with trace=True, the phase-trace variant)."""
-    lib, out_dir = (TRACE_LIB, TRACE_DIR) if trace else (LIB, OUT_DIR)
+    (with trace=True, the phase-trace variant; with checked=True, the
+    index-checked variant)."""
+    if trace and checked:
+        raise ValueError("one variant at a time")
+    lib, out_dir = (TRACE_LIB, TRACE_DIR) if trace else (CHECKED_LIB, CHECKED_DIR) if checked else (LIB, OUT_DIR)
     if not force and up_to_date(lib):
         return lib
     os.makedirs(out_dir, exist_ok=True)
 
     def compile_one(src):
         obj = os.path.join(out_dir, os.path.splitext(os.path.basename(src))[0] + ".o")
-        cmd = compile_command(src, obj, trace, verbose)
+        cmd = compile_command(src, obj, trace, verbose, checked)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -85,4 +94,5 @@ def build(force: bool = False, verbose: bool = False, trace: bool = False) -> st
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, trace="--trace" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, trace="--trace" in sys.argv,
+                checked="--checked" in sys.argv))

@@ -65,7 +65,10 @@ __device__ __forceinline__ void trace_mark(const StepParams&, int) {}
 // Spin until ready() holds.  The deadline (SM cycle counter) and the error
 // word (a global load) are checked only every 256 polls, so a wait that ends
 // reacts within a few hundred cycles.  Returns false on expiry (after setting
-// the error word) or when another CTA has already reported a timeout.
+// the error word) or when another CTA has already reported a timeout.  (A
+// failed index check of LLM_CHECKED builds does not end waits: data it kept
+// from being written makes its readers time out, and writes nobody waits
+// for, such as the logits, leave the rest of the step intact.)
 constexpr long long kWaitLimitCycles = 4000000000ll;   // about 2 s at 2 GHz
 
 template <class Ready>
@@ -270,6 +273,11 @@ struct Producer {
     // Rows [r0, r1) of m (single rows) as whole rows, m.rpc per chunk.
     __device__ void rows(const DMat& m, int wtype, int r0, int r1, int tk) {
         if (dead) return;
+        // a pair matrix counts super-rows and streams single rows
+        if (!LLM_IN_BOUNDS(p.err, r0 >= 0 && r1 <= m.rows * (m.pair ? 2 : 1))) {
+            dead = true;                      // the consumers' waits for these chunks time out
+            return;
+        }
         trace_mark(p, tk);
         const size_t rowq = (size_t)row_qbytes(m, wtype);
         const int rowd = wtype == LLM_Q8_0 ? 2 * m.dstride : 0;
@@ -291,6 +299,10 @@ struct Producer {
     // (TMA boxes; rows past the matrix's end read as zero).
     __device__ void view(const GView& v, const char* mq, const char* md, int g, int r0, int r1, int tk) {
         if (dead) return;
+        if (!LLM_IN_BOUNDS(p.err, r0 >= 0 && r1 <= v.m.rows && g >= 0 && g < p.ngrp)) {
+            dead = true;
+            return;
+        }
         trace_mark(p, tk);
         const int y = g * (v.m.cols / v.U), sx = gview_scale_x(v, g);
         for (int r = r0; r < r1; r += v.R) {
@@ -384,6 +396,11 @@ struct Consumer {
     // layer l's attention partials
     __device__ __forceinline__ unsigned long long* part(int l) const {
         return p.part + (long long)l * part_words_per_layer(p.n_heads, p.max_splits, p.hd);
+    }
+    // a tagged attention partial or statistic of this step (index-checked in
+    // LLM_CHECKED builds)
+    __device__ __forceinline__ void st_part(unsigned long long* a, float v) const {
+        if (LLM_IN_BOUNDS(p.err, a >= p.part && a < p.part + p.part_words)) st_tagged(a, v, tag);
     }
     // layer l's residual accumulator after the attention block (0) or the FFN (1)
     __device__ __forceinline__ unsigned long long* acc(int l, int which) const {
@@ -704,16 +721,19 @@ struct Epi {
     int* err;
     unsigned long long best;
     float scale;                  // the RMSNorm scale of a normed phase (its vector is x * g), else 1
+    const unsigned long long* lo; // LLM_CHECKED builds: out + r must lie in [lo, lo + n);
+    long long n;                  // logits: r < n
     __device__ void row(int r, float v) {
         v *= scale;
         if (kind == kStore) {
-            st_tagged(out + r, bias ? v + bias[r - base] : v, tag);
+            if (LLM_IN_BOUNDS(err, out + r >= lo && out + r < lo + n))
+                st_tagged(out + r, bias ? v + bias[r - base] : v, tag);
         } else if (kind == kSwiGLU) {
             sm[r - 2 * base] = v;                 // row r: gate (even) or up (odd) of super-row r / 2
         } else if (kind == kAccum) {
-            acc_add(out + r, v, err);
+            if (LLM_IN_BOUNDS(err, out + r >= lo && out + r < lo + n)) acc_add(out + r, v, err);
         } else {
-            __stcg(logits + r, v);
+            if (LLM_IN_BOUNDS(err, r >= 0 && r < n)) __stcg(logits + r, v);
             const unsigned long long k = argmax_key(v, r);
             best = k > best ? k : best;
         }
@@ -727,7 +747,8 @@ struct Epi {
         for (int k = c.tid; k < end - base; k += kConsumers) {
             const float g = sm[2 * k], up = sm[2 * k + 1];
             const float e = LC ? (float)exp(-(double)g) : expf(-g);
-            st_tagged(out + base + k, __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), up), c.tag);
+            if (LLM_IN_BOUNDS(err, out + base + k >= lo && out + base + k < lo + n))
+                st_tagged(out + base + k, __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), up), c.tag);
         }
     }
 };
@@ -1202,6 +1223,11 @@ __device__ __forceinline__ void store_kv(__half* kc, __half* vc, int pos, int kv
     kc[e] = k;
     vc[e] = v;
 }
+__device__ __forceinline__ void store_kv_checked(const StepParams& p, __half* kc, __half* vc, int g, int i, __half k,
+                                                 __half v) {
+    if (LLM_IN_BOUNDS(p.err, p.pos >= 0 && p.pos < p.max_seq && g * p.hd + i < p.kv_dim))
+        store_kv(kc, vc, p.pos, p.kv_dim, g * p.hd, i, k, v);
+}
 
 // ------------------------------------------------------------- attention --
 // One unit = the positions [t0, t1) of kv head g, for its gq query heads
@@ -1264,7 +1290,7 @@ __device__ void attention_prologue(Consumer& c, const LayerDev& L, int layer, in
     if (writer && tid < hd) {
         const __half kh = __float2half_rn(kf[tid]);
         kp[tid] = kh;
-        store_kv(L.kc, L.vc, p.pos, p.kv_dim, g * hd, tid, kh, vp[tid]);
+        store_kv_checked(p, L.kc, L.vc, g, tid, kh, vp[tid]);
     }
     consumer_sync();                                               // kp, vp visible
 }
@@ -1322,13 +1348,13 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
                 const size_t hb = (size_t)(h0 + h) * p.max_splits;
                 const float mo = ml[h], lo = ml[gq + h];
                 if (lane == 0) {
-                    st_tagged(stats + 2 * (hb + s), mo, c.tag);
-                    st_tagged(stats + 2 * (hb + s) + 1, lo, c.tag);
+                    c.st_part(stats + 2 * (hb + s), mo);
+                    c.st_part(stats + 2 * (hb + s) + 1, lo);
                 }
                 float2 v = make_float2(-INFINITY, 0.f);
                 if (lane < S) v = lane == s ? make_float2(mo, lo) : poll2(stats + 2 * (hb + lane), c.tag, p.err);
                 const float M = warp_max(v.x);
-                const float Ls = warp_sum(v.x == -INFINITY ? 0.f : (float)exp((double)(v.x - M)) * v.y);
+                const float Ls = warp_sum(v.x == -INFINITY ? 0.f : expf(v.x - M) * v.y);
                 __syncwarp();
                 if (lane == 0) { ml[h] = M; ml[gq + h] = Ls; }
             }
@@ -1352,18 +1378,6 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
                 const float2* q2 = reinterpret_cast<const float2*>(q_s + h * hd);
                 const __half2* k2 = reinterpret_cast<const __half2*>(
                     writer && c0 + pp - t0 == prow ? kp : ks + (size_t)pp * hd);
-                if constexpr (LC) {
-                    // F16 q times F16 k: every product exact, summed in float in
-                    // dimension order (the oracle's sum, to the bit)
-                    float a = 0.f;
-                    for (int j = 0; j < nh2; j++) {
-                        const float2 kk = __half22float2(k2[j]), qq = q2[j];
-                        a = fmaf(qq.x, kk.x, a);
-                        a = fmaf(qq.y, kk.y, a);
-                    }
-                    scb[h * P + pp] = __fdiv_rn(a, p.attn_div);
-                    continue;
-                }
                 float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
                 int j = lane % nh2;
                 int k = 0;
@@ -1389,30 +1403,25 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
             if (warp < gq) {
                 const int h = warp;
                 if (LC && pv) {
-                    // the head's global (M, L): e_t = e^(s_t - M) taken in double and
-                    // rounded to float (as the oracle takes it), p_t = f16(e_t / L),
-                    // no rescaling
+                    // the head's global (M, L): p_t = f16(e^(s_t - M) / L), no rescaling
                     const float M = ml[h], Ls = ml[gq + h];
-                    for (int pp = lane; pp < np; pp += 32) {
-                        const float e = (float)exp((double)__fsub_rn(scb[h * P + pp], M));
-                        scb[h * P + pp] = f16_round(__fdiv_rn(e, Ls));
-                    }
+                    for (int pp = lane; pp < np; pp += 32)
+                        scb[h * P + pp] = f16_round(__fdiv_rn(expf(__fsub_rn(scb[h * P + pp], M)), Ls));
                     if (lane == 0) corrb[h] = 1.0f;
                 } else {
-                    auto ex = [](float d) { return LC ? (float)exp((double)d) : expf(d); };
                     float mloc = -INFINITY;
                     for (int pp = lane; pp < np; pp += 32) mloc = fmaxf(mloc, scb[h * P + pp]);
                     mloc = warp_max(mloc);
                     const float mold = ml[h], mnew = fmaxf(mold, mloc);
                     float sum = 0.f;
                     for (int pp = lane; pp < np; pp += 32) {
-                        const float e = ex(__fsub_rn(scb[h * P + pp], mnew));
+                        const float e = expf(scb[h * P + pp] - mnew);
                         scb[h * P + pp] = e;
                         sum += e;
                     }
                     sum = warp_sum(sum);
                     if (lane == 0) {
-                        const float cr = ex(mold - mnew);          // 0 on the first chunk (mold = -inf)
+                        const float cr = expf(mold - mnew);       // 0 on the first chunk (mold = -inf)
                         ml[h] = mnew;
                         ml[gq + h] = ml[gq + h] * cr + sum;
                         corrb[h] = cr;
@@ -1452,10 +1461,10 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
         for (int k = 0; k < NSPLIT; k++) v += sm.comb()[k * GD + oo];
         const int hh = oo / hd, ii = oo % hd;
         const size_t hs = (size_t)(h0 + hh) * p.max_splits + s;
-        st_tagged(part_acc + hs * hd + ii, v, c.tag);
+        c.st_part(part_acc + hs * hd + ii, v);
         if (ii == 0) {
-            st_tagged(part_ml + 2 * hs, ml[hh], c.tag);
-            st_tagged(part_ml + 2 * hs + 1, ml[gq + hh], c.tag);
+            c.st_part(part_ml + 2 * hs, ml[hh]);
+            c.st_part(part_ml + 2 * hs + 1, ml[gq + hh]);
         }
     }
     consumer_sync();                                               // comb, scratch free
@@ -1618,10 +1627,10 @@ __device__ bool attention_unit_mma(Consumer& c, const LayerDev& L, int layer, in
     if (!buf) {                                                    // no positions: an empty partial
         for (int oo = tid; oo < GD; oo += kConsumers) {
             const size_t hs = (size_t)(h0 + oo / HD) * p.max_splits + s;
-            st_tagged(part_acc + hs * HD + oo % HD, 0.f, c.tag);
+            c.st_part(part_acc + hs * HD + oo % HD, 0.f);
             if (oo % HD == 0) {
-                st_tagged(part_ml + 2 * hs, -INFINITY, c.tag);
-                st_tagged(part_ml + 2 * hs + 1, 0.f, c.tag);
+                c.st_part(part_ml + 2 * hs, -INFINITY);
+                c.st_part(part_ml + 2 * hs + 1, 0.f);
             }
         }
         consumer_sync();
@@ -1658,8 +1667,8 @@ __device__ bool attention_unit_mma(Consumer& c, const LayerDev& L, int layer, in
             float l = 0.f;
             for (int w = 0; w < kConsumerWarps; w++) l = fmaf(fw[hh * kConsumerWarps + w], wpart[w * WS + hh * (HD + 2) + HD + 1], l);
             const size_t hs = (size_t)(h0 + hh) * p.max_splits + s;
-            st_tagged(part_ml + 2 * hs, M, c.tag);
-            st_tagged(part_ml + 2 * hs + 1, l, c.tag);
+            c.st_part(part_ml + 2 * hs, M);
+            c.st_part(part_ml + 2 * hs + 1, l);
         }
     }
     consumer_sync();
@@ -1669,7 +1678,7 @@ __device__ bool attention_unit_mma(Consumer& c, const LayerDev& L, int layer, in
 #pragma unroll 5
         for (int w = 0; w < kConsumerWarps; w++) v = fmaf(fw[hh * kConsumerWarps + w], wpart[w * WS + hh * (HD + 2) + ii], v);
         const size_t hs = (size_t)(h0 + hh) * p.max_splits + s;
-        st_tagged(part_acc + hs * HD + ii, v, c.tag);
+        c.st_part(part_acc + hs * HD + ii, v);
     }
     fence_proxy_async_smem();                                      // the slot's next fill is a TMA write
     consumer_sync();
@@ -1810,6 +1819,15 @@ __device__ bool consumer_main(const StepParams& p, Smem& sm) {
             n = fdg;
             e.kind = Epi::kAccum;
             e.out = c.acc(l, 1);
+        }
+        if (e.kind == Epi::kAccum) {
+            e.lo = p.delta;
+            e.n = p.delta_words;
+        } else if (e.kind == Epi::kLogits) {
+            e.n = p.logits_limit;
+        } else {
+            e.lo = p.tv;
+            e.n = p.tv_words;
         }
 #ifdef LLM_TRACE
         c.fine = !last && l == 8 ? 960 + 16 * k : -1;
@@ -2139,6 +2157,7 @@ __global__ void __launch_bounds__(kBlock, 1) gemv_test_kernel(const __grid_const
         Epi e{};
         e.kind = Epi::kLogits;
         e.logits = ys;
+        e.n = v ? p.dim : m.rows;
         e.err = p.err;
         e.scale = lanes_prep<DT, LC>(c, Ln, n, false, 0.f, xr);
         const ChunkGeo ck = v ? view_geo(*v, pt.g) : rows_geo(m, DT);

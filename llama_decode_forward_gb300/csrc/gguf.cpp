@@ -22,6 +22,7 @@
 
 namespace llm {
 int check_shape(const llm_config* c, std::string* why);   // llm_api.cu: llm_create's shape checks
+cudaError_t dev_alloc(void** p, size_t bytes);             // llm_api.cu: the library's device allocations
 }
 
 namespace {
@@ -645,7 +646,7 @@ extern "C" int llm_create_from_gguf(const llm_gguf* g, int32_t max_seq, llm_stre
     }
     uint8_t* stage = nullptr;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t ce = cudaMalloc(&stage, total ? total : 256);
+    cudaError_t ce = llm::dev_alloc(reinterpret_cast<void**>(&stage), total ? total : 256);
     if (ce != cudaSuccess) {
         put_err(err, err_len, "staging %zu bytes: %s", total, cudaGetErrorString(ce));
         return ce == cudaErrorMemoryAllocation ? LLM_ERR_NO_MEMORY : LLM_ERR_CUDA;

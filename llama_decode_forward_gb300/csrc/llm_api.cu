@@ -6,8 +6,10 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <string>
+#include <unordered_set>
 #include <vector>
 
 #include <cuda.h>
@@ -28,6 +30,68 @@ cudaError_t launch_gemv_test(cudaStream_t st, int wtype, bool llamacpp, const St
 }  // namespace llm
 
 using namespace llm;
+
+// ------------------------------------------------------------ allocations --
+// Every device and pinned-host allocation of the library goes through these
+// two functions.  llm_test_fail_alloc(n) arms a countdown: the n-th
+// allocation from then on fails with cudaErrorMemoryAllocation without
+// calling CUDA (and disarms the countdown), so tests can make each allocation
+// of llm_create or llm_prefill fail in turn.
+static std::atomic<int> g_fail_countdown{0};
+
+static bool injected_failure() {
+    int n = g_fail_countdown.load();
+    while (n > 0 && !g_fail_countdown.compare_exchange_weak(n, n - 1)) {}
+    return n == 1;
+}
+
+namespace llm {
+cudaError_t dev_alloc(void** p, size_t bytes) {
+    if (injected_failure()) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(p, bytes);
+}
+}  // namespace llm
+
+static cudaError_t host_alloc(void** p, size_t bytes) {
+    if (injected_failure()) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMallocHost(p, bytes);
+}
+
+// Guard bands: the KV cache, the activations and the prefill workspace are
+// allocated with kGuardBytes more on each side, filled with kGuardByte; the
+// buffer proper starts kGuardBytes into the allocation (256-byte alignment
+// kept).  llm_test_guards counts guard bytes that changed: a kernel that
+// wrote past either end of one of these buffers shows up there.
+constexpr size_t kGuardBytes = 4096;
+constexpr int kGuardByte = 0xA5;
+
+struct Guarded {
+    uint8_t* raw = nullptr;   // the allocation (freed with cudaFree)
+    size_t bytes = 0;         // the buffer proper
+    uint8_t* ptr() const { return raw ? raw + kGuardBytes : nullptr; }
+};
+
+static cudaError_t guarded_alloc(Guarded& g, size_t bytes, cudaStream_t st) {
+    void* raw = nullptr;
+    cudaError_t e = dev_alloc(&raw, bytes + 2 * kGuardBytes);
+    if (e != cudaSuccess) return e;
+    g.raw = static_cast<uint8_t*>(raw);
+    g.bytes = bytes;
+    e = cudaMemsetAsync(g.raw, kGuardByte, kGuardBytes, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(g.raw + kGuardBytes + bytes, kGuardByte, kGuardBytes, st);
+    return e;
+}
+
+static void guarded_free(Guarded& g) {
+    cudaFree(g.raw);
+    g = Guarded{};
+}
 
 struct HostPinned {
     int token_in;
@@ -51,6 +115,7 @@ struct llm_handle {
     size_t arena_bytes = 0;
     __half* kv = nullptr;            // [n_layers][2][max_seq][kv_dim]
     uint8_t* act = nullptr;          // activations, counters, partials
+    Guarded kv_mem, act_mem, ws_mem; // the guarded allocations behind kv, act and prefill_ws
     std::vector<LayerDev> layers;
     LayerDev* d_layers = nullptr;
     DMat embd{}, out{};
@@ -80,6 +145,7 @@ struct llm_handle {
     unsigned long long* trace = nullptr;   // LLM_TRACE builds: [sms][kTraceSlots]
     void* prefill_ws = nullptr;      // prefill workspace (lazily sized)
     size_t prefill_ws_bytes = 0;
+    int test_logits_limit = 0;       // llm_test_logits_limit: > 0 narrows the checked logits bound
 };
 
 // --------------------------------------------------------------- helpers --
@@ -231,16 +297,37 @@ static void free_handle(llm_handle* h) {
     if (!h) return;
     if (h->st) cudaStreamSynchronize(h->st);
     cudaFree(h->arena);
-    cudaFree(h->kv);
-    cudaFree(h->act);
+    guarded_free(h->kv_mem);
+    guarded_free(h->act_mem);
     cudaFree(h->d_layers);
     cudaFree(h->kv_maps);
-    cudaFree(h->prefill_ws);
+    guarded_free(h->ws_mem);
     cudaFree(h->trace);
     if (h->pinned) cudaFreeHost(h->pinned);
     cudaGetLastError();
     delete h;
 }
+
+// ----------------------------------------------------------- live handles --
+// Every handle llm_create returned that llm_destroy has not freed.  The entry
+// points refuse any other pointer with LLM_ERR_INVALID_ARG before touching
+// it, so a second llm_destroy or a call on a destroyed handle does nothing
+// (a pointer that a later llm_create happens to receive again names that new
+// handle).
+static std::mutex g_live_mu;
+static std::unordered_set<const llm_handle*>& live_set() {
+    static std::unordered_set<const llm_handle*> s;
+    return s;
+}
+static bool alive(const llm_handle* h) {
+    if (!h) return false;
+    std::lock_guard<std::mutex> g(g_live_mu);
+    return live_set().count(h) != 0;
+}
+#define LIVE_OR_RETURN(h)                           \
+    do {                                            \
+        if (!alive(h)) return LLM_ERR_INVALID_ARG;  \
+    } while (0)
 
 namespace llm {
 // The shape checks of llm_create, for callers that want them before moving
@@ -310,7 +397,7 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
     if (w->output) bytes += align256(mat_bytes(c.wtype, c.vocab, d)) + 512;
     bytes += align256((size_t)d * 4) + align256((size_t)c.rope_dims * 2 + 4);
     h->arena_bytes = bytes;
-    CKC(cudaMalloc(&h->arena, bytes));
+    CKC(dev_alloc((void**)&h->arena, bytes));
 
     size_t off = 0;
     h->layers.resize(L);
@@ -363,13 +450,14 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
 
     // ---- KV cache
     const size_t kv_bytes = (size_t)L * 2 * c.max_seq * kv * sizeof(__half);
-    CKC(cudaMalloc(&h->kv, kv_bytes));
+    CKC(guarded_alloc(h->kv_mem, kv_bytes, h->st));
+    h->kv = reinterpret_cast<__half*>(h->kv_mem.ptr());
     CKC(cudaMemsetAsync(h->kv, 0, kv_bytes, h->st));
     for (int l = 0; l < L; l++) {
         h->layers[l].kc = h->kv + (size_t)(2 * l) * c.max_seq * kv;
         h->layers[l].vc = h->layers[l].kc + (size_t)c.max_seq * kv;
     }
-    CKC(cudaMalloc(&h->d_layers, sizeof(LayerDev) * L));
+    CKC(dev_alloc((void**)&h->d_layers, sizeof(LayerDev) * L));
     CKC(cudaMemcpyAsync(h->d_layers, h->layers.data(), sizeof(LayerDev) * L, cudaMemcpyHostToDevice, h->st));
 
     // ---- column groups of the decode step: the largest divisor of n_kv up
@@ -418,7 +506,8 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
     const size_t o_tv = take(h->tv_words * 8), o_part = take(h->part_words * 8), o_delta = take(h->delta_words * 8),
                  o_epoch = take(4), o_logits = take((size_t)c.vocab * 4), o_best = take(8),
                  o_ctr = take((size_t)h->n_counters * 4), o_err = take(4), o_tin = take(4), o_tout = take(4);
-    CKC(cudaMalloc(&h->act, a));
+    CKC(guarded_alloc(h->act_mem, a, h->st));
+    h->act = h->act_mem.ptr();
     CKC(cudaMemsetAsync(h->act, 0, a, h->st));
     h->tv = (unsigned long long*)(h->act + o_tv);
     h->part = (unsigned long long*)(h->act + o_part);
@@ -430,9 +519,9 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
     h->err = (int*)(h->act + o_err);
     h->tok_in = (int*)(h->act + o_tin);
     h->tok_out = (int*)(h->act + o_tout);
-    CKC(cudaMallocHost(&h->pinned, sizeof(HostPinned)));
+    CKC(host_alloc((void**)&h->pinned, sizeof(HostPinned)));
 #ifdef LLM_TRACE
-    CKC(cudaMalloc(&h->trace, (size_t)h->sms * kTraceSlots * 8));
+    CKC(dev_alloc((void**)&h->trace, (size_t)h->sms * kTraceSlots * 8));
     CKC(cudaMemsetAsync(h->trace, 0, (size_t)h->sms * kTraceSlots * 8, h->st));
 #endif
 
@@ -536,12 +625,16 @@ extern "C" int llm_create(const llm_config* cfg, const llm_weights* w, llm_strea
                 return create_failed(h, fail(h, LLM_ERR_CUDA, "cuTensorMapEncodeTiled (Wo / Wdown) of layer %d: error %d",
                                              l, (int)r));
         }
-        CKC(cudaMalloc(&h->kv_maps, sizeof(CUtensorMap) * maps.size()));
+        CKC(dev_alloc((void**)&h->kv_maps, sizeof(CUtensorMap) * maps.size()));
         CKC(cudaMemcpyAsync(h->kv_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice,
                             h->st));
     }
     CKC(cudaStreamSynchronize(h->st));
     t_create_error.clear();
+    {
+        std::lock_guard<std::mutex> g(g_live_mu);
+        live_set().insert(h);
+    }
     *out = h;
     return LLM_OK;
 #undef CKC
@@ -568,6 +661,10 @@ static StepParams step_params(const llm_handle* h, const int* token_dev, int pos
     p.token_in = token_dev; p.token_out = argmax_dev; p.pos = pos;
     const int s = (pos + 1 + 15) / 16;
     p.splits = s < 1 ? 1 : (s > h->max_splits ? h->max_splits : s);
+    p.tv_words = (long long)h->tv_words;
+    p.part_words = (long long)h->part_words;
+    p.delta_words = (long long)h->delta_words;
+    p.logits_limit = h->test_logits_limit > 0 ? h->test_logits_limit : c.vocab;
     return p;
 }
 
@@ -579,21 +676,37 @@ static int launch_step(llm_handle* h, const int* token_dev, int pos, int* argmax
     return LLM_OK;
 }
 
+// The status of a device error word: the first of timeout, token, range,
+// check that is set, with every set condition named in the message.
+static int device_error_status(llm_handle* h, int e) {
+    if (!e) return LLM_OK;
+    h->broken = true;
+    std::string why;
+    auto add = [&](int bit, const char* text) {
+        if (!(e & bit)) return;
+        if (!why.empty()) why += "; ";
+        why += text;
+    };
+    add(kErrTimeout, "a bounded device wait expired");
+    add(kErrToken, "a device-side token was out of range");
+    add(kErrRange, "a residual update was not finite or not below 2^15 in magnitude");
+    add(kErrCheck, "a device-side index check failed and its access was skipped");
+    const int status = e & kErrTimeout ? LLM_ERR_DEVICE_TIMEOUT
+                       : e & kErrToken ? LLM_ERR_OUT_OF_RANGE
+                       : e & kErrRange ? LLM_ERR_NONFINITE
+                       : e & kErrCheck ? LLM_ERR_CHECK
+                                       : LLM_ERR_CUDA;
+    return fail(h, status, "%s", why.c_str());
+}
+
 static int read_device_error(llm_handle* h) {
     CK(h, cudaMemcpyAsync(&h->pinned->err, h->err, 4, cudaMemcpyDeviceToHost, h->st));
     CK(h, cudaStreamSynchronize(h->st));
-    const int e = h->pinned->err;
-    if (e & kErrTimeout) { h->broken = true; return fail(h, LLM_ERR_DEVICE_TIMEOUT, "a bounded device wait expired"); }
-    if (e & kErrToken) { h->broken = true; return fail(h, LLM_ERR_OUT_OF_RANGE, "a device-side token was out of range"); }
-    if (e & kErrRange) {
-        h->broken = true;
-        return fail(h, LLM_ERR_NONFINITE, "a residual update was not finite or not below 2^15 in magnitude");
-    }
-    return LLM_OK;
+    return device_error_status(h, h->pinned->err);
 }
 
 extern "C" int llm_reset(llm_handle* h) {
-    if (!h) return LLM_ERR_INVALID_ARG;
+    LIVE_OR_RETURN(h);
     CK(h, cudaStreamSynchronize(h->st));
     CK(h, cudaMemsetAsync(h->err, 0, 4, h->st));
     CK(h, cudaMemsetAsync(h->counters, 0, (size_t)h->n_counters * 4, h->st));
@@ -610,7 +723,7 @@ extern "C" int llm_reset(llm_handle* h) {
 }
 
 extern "C" int llm_decode_step(llm_handle* h, int32_t token, int32_t pos, float* logits_host, int32_t* argmax_host) {
-    if (!h) return LLM_ERR_INVALID_ARG;
+    LIVE_OR_RETURN(h);
     if (h->broken) return fail(h, LLM_ERR_STATE, "handle has a device error; call llm_reset");
     if (token < 0 || token >= h->cfg.vocab) return fail(h, LLM_ERR_OUT_OF_RANGE, "token %d not in [0, %d)", token, h->cfg.vocab);
     if (pos < 0 || pos >= h->cfg.max_seq) return fail(h, LLM_ERR_OUT_OF_RANGE, "pos %d not in [0, %d)", pos, h->cfg.max_seq);
@@ -627,14 +740,16 @@ extern "C" int llm_decode_step(llm_handle* h, int32_t token, int32_t pos, float*
 }
 
 extern "C" int llm_decode_step_async(llm_handle* h, const int32_t* token_dev, int32_t pos, int32_t* argmax_dev) {
-    if (!h || !token_dev || !argmax_dev) return fail(h, LLM_ERR_INVALID_ARG, "NULL argument");
+    LIVE_OR_RETURN(h);
+    if (!token_dev || !argmax_dev) return fail(h, LLM_ERR_INVALID_ARG, "NULL argument");
     if (h->broken) return fail(h, LLM_ERR_STATE, "handle has a device error; call llm_reset");
     if (pos < 0 || pos >= h->cfg.max_seq) return fail(h, LLM_ERR_OUT_OF_RANGE, "pos %d not in [0, %d)", pos, h->cfg.max_seq);
     return launch_step(h, token_dev, pos, argmax_dev);
 }
 
 extern "C" int llm_generate(llm_handle* h, int32_t token, int32_t pos, int32_t n_steps, int32_t* tokens_dev) {
-    if (!h || !tokens_dev || n_steps < 0) return fail(h, LLM_ERR_INVALID_ARG, "bad argument");
+    LIVE_OR_RETURN(h);
+    if (!tokens_dev || n_steps < 0) return fail(h, LLM_ERR_INVALID_ARG, "bad argument");
     if (h->broken) return fail(h, LLM_ERR_STATE, "handle has a device error; call llm_reset");
     if (token < 0 || token >= h->cfg.vocab) return fail(h, LLM_ERR_OUT_OF_RANGE, "token %d not in [0, %d)", token, h->cfg.vocab);
     if (pos < 0 || (long long)pos + n_steps > h->cfg.max_seq)
@@ -651,7 +766,8 @@ extern "C" int llm_generate(llm_handle* h, int32_t token, int32_t pos, int32_t n
 
 extern "C" int llm_prefill(llm_handle* h, const int32_t* tokens_host, int32_t n, int32_t pos0, float* logits_host,
                            int32_t* argmax_host) {
-    if (!h || !tokens_host || n <= 0) return fail(h, LLM_ERR_INVALID_ARG, "bad argument");
+    LIVE_OR_RETURN(h);
+    if (!tokens_host || n <= 0) return fail(h, LLM_ERR_INVALID_ARG, "bad argument");
     if (h->broken) return fail(h, LLM_ERR_STATE, "handle has a device error; call llm_reset");
     if (pos0 < 0 || (long long)pos0 + n > h->cfg.max_seq)
         return fail(h, LLM_ERR_OUT_OF_RANGE, "positions %d..%d exceed max_seq %d", pos0, pos0 + n - 1, h->cfg.max_seq);
@@ -671,10 +787,12 @@ extern "C" int llm_prefill(llm_handle* h, const int32_t* tokens_host, int32_t n,
         // F16 weights: tensor-core batches of up to kPrefillRows tokens
         const size_t need = prefill_workspace_bytes(pc);
         if (h->prefill_ws_bytes < need) {
-            cudaFree(h->prefill_ws);
+            CK(h, cudaStreamSynchronize(h->st));
+            guarded_free(h->ws_mem);
             h->prefill_ws = nullptr;
             h->prefill_ws_bytes = 0;
-            CK(h, cudaMalloc(&h->prefill_ws, need));
+            CK(h, guarded_alloc(h->ws_mem, need, h->st));
+            h->prefill_ws = h->ws_mem.ptr();
             h->prefill_ws_bytes = need;
         }
         const char* what = "";
@@ -701,21 +819,21 @@ extern "C" int llm_prefill(llm_handle* h, const int32_t* tokens_host, int32_t n,
 }
 
 extern "C" int llm_sync(llm_handle* h) {
-    if (!h) return LLM_ERR_INVALID_ARG;
+    LIVE_OR_RETURN(h);
     CK(h, cudaStreamSynchronize(h->st));
     return read_device_error(h);
 }
 
-extern "C" const float* llm_logits_device(const llm_handle* h) { return h ? h->logits : nullptr; }
+extern "C" const float* llm_logits_device(const llm_handle* h) { return alive(h) ? h->logits : nullptr; }
 
 extern "C" int llm_get_config(const llm_handle* h, llm_config* out) {
-    if (!h || !out) return LLM_ERR_INVALID_ARG;
+    if (!alive(h) || !out) return LLM_ERR_INVALID_ARG;
     *out = h->cfg;
     return LLM_OK;
 }
 
 extern "C" int llm_kv_view(llm_handle* h, int layer, uint16_t** k_dev, uint16_t** v_dev) {
-    if (!h || !k_dev || !v_dev) return LLM_ERR_INVALID_ARG;
+    if (!alive(h) || !k_dev || !v_dev) return LLM_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.n_layers) return fail(h, LLM_ERR_OUT_OF_RANGE, "layer %d", layer);
     *k_dev = reinterpret_cast<uint16_t*>(h->layers[layer].kc);
     *v_dev = reinterpret_cast<uint16_t*>(h->layers[layer].vc);
@@ -723,7 +841,7 @@ extern "C" int llm_kv_view(llm_handle* h, int layer, uint16_t** k_dev, uint16_t*
 }
 
 extern "C" int llm_test_kv_store(llm_handle* h, int layer, int32_t pos, const float* k_dev, const float* v_dev) {
-    if (!h || !k_dev || !v_dev) return LLM_ERR_INVALID_ARG;
+    if (!alive(h) || !k_dev || !v_dev) return LLM_ERR_INVALID_ARG;
     if (layer < 0 || layer >= h->cfg.n_layers || pos < 0 || pos >= h->cfg.max_seq)
         return fail(h, LLM_ERR_OUT_OF_RANGE, "layer %d / pos %d", layer, pos);
     launch_kv_store(h->st, h->layers[layer].kc, h->layers[layer].vc, pos, h->kv_dim, k_dev, v_dev);
@@ -734,7 +852,7 @@ extern "C" int llm_test_kv_store(llm_handle* h, int layer, int32_t pos, const fl
 }
 
 extern "C" int llm_test_dequant_rows(llm_handle* h, int which, int layer, int32_t row0, int32_t n_rows, float* out_dev) {
-    if (!h || !out_dev || n_rows < 0) return LLM_ERR_INVALID_ARG;
+    if (!alive(h) || !out_dev || n_rows < 0) return LLM_ERR_INVALID_ARG;
     if (which < 7 && (layer < 0 || layer >= h->cfg.n_layers)) return fail(h, LLM_ERR_OUT_OF_RANGE, "layer %d", layer);
     const llm_config& c = h->cfg;
     DMat m{};
@@ -762,7 +880,7 @@ extern "C" int llm_test_dequant_rows(llm_handle* h, int which, int layer, int32_
 }
 
 extern "C" int llm_test_gemv(llm_handle* h, int which, int layer, const float* x_dev, float* y_dev) {
-    if (!h || !x_dev || !y_dev) return LLM_ERR_INVALID_ARG;
+    if (!alive(h) || !x_dev || !y_dev) return LLM_ERR_INVALID_ARG;
     if (which < 0 || which > 4) return fail(h, LLM_ERR_INVALID_ARG, "which = %d", which);
     if (layer < 0 || layer >= h->cfg.n_layers) return fail(h, LLM_ERR_OUT_OF_RANGE, "layer %d", layer);
     if (h->broken) return fail(h, LLM_ERR_STATE, "handle has a device error; call llm_reset");
@@ -775,10 +893,75 @@ extern "C" int llm_test_gemv(llm_handle* h, int which, int layer, const float* x
     return read_device_error(h);
 }
 
-extern "C" int llm_column_groups(const llm_handle* h) { return h ? h->ngrp : LLM_ERR_INVALID_ARG; }
+extern "C" int llm_test_logits_limit(llm_handle* h, int32_t limit) {
+    LIVE_OR_RETURN(h);
+#ifdef LLM_CHECKED
+    if (limit < 0 || limit > h->cfg.vocab) return fail(h, LLM_ERR_OUT_OF_RANGE, "limit %d", limit);
+    h->test_logits_limit = limit;
+    return LLM_OK;
+#else
+    (void)limit;
+    return fail(h, LLM_ERR_UNSUPPORTED, "not an LLM_CHECKED build");
+#endif
+}
+
+extern "C" int llm_checked_build(void) {
+#ifdef LLM_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+extern "C" int llm_test_fail_alloc(int32_t nth) {
+    if (nth < 0) return LLM_ERR_INVALID_ARG;
+    g_fail_countdown.store(nth);
+    return LLM_OK;
+}
+
+// The guarded buffers of a handle, in the order llm_test_poke_guard numbers
+// their bands: KV cache, activations, prefill workspace (when allocated).
+static int guarded_buffers(const llm_handle* h, const Guarded** out) {
+    int n = 0;
+    out[n++] = &h->kv_mem;
+    out[n++] = &h->act_mem;
+    if (h->ws_mem.raw) out[n++] = &h->ws_mem;
+    return n;
+}
+
+extern "C" int64_t llm_test_guards(llm_handle* h) {
+    LIVE_OR_RETURN(h);
+    const Guarded* g[3];
+    const int n = guarded_buffers(h, g);
+    std::vector<uint8_t> band(kGuardBytes);
+    int64_t changed = 0;
+    CK(h, cudaStreamSynchronize(h->st));
+    for (int i = 0; i < n; i++)
+        for (int side = 0; side < 2; side++) {
+            const uint8_t* src = g[i]->raw + (side ? kGuardBytes + g[i]->bytes : 0);
+            CK(h, cudaMemcpy(band.data(), src, kGuardBytes, cudaMemcpyDeviceToHost));
+            for (size_t k = 0; k < kGuardBytes; k++) changed += band[k] != (uint8_t)kGuardByte;
+        }
+    return changed;
+}
+
+extern "C" int llm_test_poke_guard(llm_handle* h, int band) {
+    LIVE_OR_RETURN(h);
+    const Guarded* g[3];
+    const int n = guarded_buffers(h, g);
+    if (band < 0 || band >= 2 * n) return fail(h, LLM_ERR_OUT_OF_RANGE, "guard band %d of %d", band, 2 * n);
+    const Guarded& b = *g[band / 2];
+    // the byte next to the buffer: the one an off-by-one write would hit
+    uint8_t* at = band % 2 ? b.raw + kGuardBytes + b.bytes : b.raw + kGuardBytes - 1;
+    CK(h, cudaStreamSynchronize(h->st));
+    CK(h, cudaMemset(at, 0x5A, 1));
+    return LLM_OK;
+}
+
+extern "C" int llm_column_groups(const llm_handle* h) { return alive(h) ? h->ngrp : LLM_ERR_INVALID_ARG; }
 
 extern "C" int llm_trace_read(llm_handle* h, uint64_t* host, int32_t* sms) {
-    if (!h || !host || !sms) return LLM_ERR_INVALID_ARG;
+    if (!alive(h) || !host || !sms) return LLM_ERR_INVALID_ARG;
     if (!h->trace) return LLM_ERR_UNSUPPORTED;
     *sms = h->sms;
     CK(h, cudaMemcpyAsync(host, h->trace, (size_t)h->sms * kTraceSlots * 8, cudaMemcpyDeviceToHost, h->st));
@@ -786,9 +969,15 @@ extern "C" int llm_trace_read(llm_handle* h, uint64_t* host, int32_t* sms) {
     return LLM_OK;
 }
 
-extern "C" int64_t llm_launch_count(const llm_handle* h) { return h ? h->launches : 0; }
+extern "C" int64_t llm_launch_count(const llm_handle* h) { return alive(h) ? h->launches : 0; }
 
-extern "C" void llm_destroy(llm_handle* h) { free_handle(h); }
+extern "C" void llm_destroy(llm_handle* h) {
+    {
+        std::lock_guard<std::mutex> g(g_live_mu);
+        if (!h || !live_set().erase(h)) return;   // NULL, already destroyed, or never created
+    }
+    free_handle(h);
+}
 
 extern "C" const char* llm_status_string(int s) {
     switch (s) {
@@ -801,11 +990,15 @@ extern "C" const char* llm_status_string(int s) {
         case LLM_ERR_DEVICE_TIMEOUT: return "device wait timed out";
         case LLM_ERR_STATE: return "invalid handle state";
         case LLM_ERR_NONFINITE: return "a non-finite or out-of-range value in the residual stream";
+        case LLM_ERR_CHECK: return "a device-side index check failed (LLM_CHECKED build)";
         default: return "unknown status";
     }
 }
 
-extern "C" const char* llm_last_error(const llm_handle* h) { return h ? h->last_error.c_str() : t_create_error.c_str(); }
+extern "C" const char* llm_last_error(const llm_handle* h) {
+    if (!h) return t_create_error.c_str();
+    return alive(h) ? h->last_error.c_str() : "not a live handle";
+}
 
 // ------------------------------------------------------- no-alloc step --
 // A decode step whose working memory (residual stream, q/k/v, attention
@@ -859,7 +1052,7 @@ ScratchLayout scratch_layout(const llm_handle* h) {
 
 extern "C" int llm_decode_step_noalloc(llm_handle* h, const int32_t* token_dev, int32_t pos, float* logits_dev,
                                        int32_t* argmax_dev) {
-    if (!h) return LLM_ERR_INVALID_ARG;
+    LIVE_OR_RETURN(h);
     if (!token_dev || !logits_dev || !argmax_dev) return fail(h, LLM_ERR_INVALID_ARG, "NULL argument");
     if (h->broken) return fail(h, LLM_ERR_STATE, "handle has a device error; call llm_reset");
     if (pos < 0 || pos >= h->cfg.max_seq) return fail(h, LLM_ERR_OUT_OF_RANGE, "pos %d not in [0, %d)", pos, h->cfg.max_seq);
@@ -912,11 +1105,5 @@ extern "C" int llm_decode_step_noalloc(llm_handle* h, const int32_t* token_dev, 
         CK(h, cudaMemsetAsync(base + sl.part, 0, sl.part_bytes, h->st));
         CK(h, cudaStreamSynchronize(h->st));
     }
-    if (e & kErrTimeout) { h->broken = true; return fail(h, LLM_ERR_DEVICE_TIMEOUT, "a bounded device wait expired"); }
-    if (e & kErrToken) { h->broken = true; return fail(h, LLM_ERR_OUT_OF_RANGE, "the device-side token was out of range"); }
-    if (e & kErrRange) {
-        h->broken = true;
-        return fail(h, LLM_ERR_NONFINITE, "a residual update was not finite or not below 2^15 in magnitude");
-    }
-    return LLM_OK;
+    return device_error_status(h, e);
 }

@@ -22,7 +22,16 @@ __host__ __device__ inline int max_blocks_per_thread(int wtype) { return wtype =
 constexpr int kMaxSmem = 232448;                  // 227 KB opt-in dynamic shared memory per CTA
 
 // Device error word bits (sticky until llm_reset).
-enum : int { kErrNone = 0, kErrTimeout = 1, kErrToken = 2, kErrRange = 4 };
+enum : int { kErrNone = 0, kErrTimeout = 1, kErrToken = 2, kErrRange = 4, kErrCheck = 8 };
+
+// Index checks of LLM_CHECKED builds: a check that fails records kErrCheck in
+// the error word and the access it guards is skipped (no trap).  Other builds
+// compile the checks away.
+#ifdef LLM_CHECKED
+#define LLM_IN_BOUNDS(err, cond) ((cond) ? true : (atomicOr((err), kErrCheck), false))
+#else
+#define LLM_IN_BOUNDS(err, cond) true
+#endif
 
 // A weight matrix in the library's layout.  Q8_0: row r is `cols` int8 quants
 // at q + r*cols, and cols/32
@@ -116,6 +125,9 @@ struct StepParams {
     int* token_out;
     int pos;
     int splits;               // attention splits per kv head for this pos
+    // sizes the index checks of LLM_CHECKED builds hold the step's accesses to
+    long long tv_words, part_words, delta_words;
+    int logits_limit;         // logits the step may write (vocab)
 
     // shared-memory geometry (bytes from the dynamic smem base)
     int ns;                   // ring slots

@@ -31,10 +31,16 @@ def test_library_is_built_for_sm_103a():
         assert cmd.count("-gencode") == 1 and not any("-arch" in a for a in cmd), cmd
     assert B.compile_command("a.cu", "a.o", trace=True)[-4:-2] == ["-c", "a.cu"]
     assert "-DLLM_TRACE" in B.compile_command("a.cu", "a.o", trace=True)
+    checked = B.compile_command("a.cu", "a.o", checked=True)
+    assert "-DLLM_CHECKED" in checked and "-DLLM_TRACE" not in checked
+    assert "-DLLM_CHECKED" not in B.compile_command("a.cu", "a.o")
+    assert B.CHECKED_LIB != B.LIB and B.TRACE_LIB != B.LIB
+    with pytest.raises(ValueError):
+        B.build(trace=True, checked=True)
 
 
 def test_status_strings():
-    for s in range(0, -9, -1):
+    for s in range(0, -10, -1):
         assert L.llm_status_string(s) not in ("", "unknown status")
     assert L.llm_status_string(-99) == "unknown status"
 
