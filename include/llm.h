@@ -212,6 +212,29 @@ int llm_test_dequant_rows(llm_handle *h, int which, int layer, int32_t row0, int
  * Synchronous.  Errors: INVALID_ARG, OUT_OF_RANGE (layer), STATE, CUDA. */
 int llm_test_gemv(llm_handle *h, int which, int layer, const float *x_dev, float *y_dev);
 
+/* Named intermediates of the handle's last llm_decode_step (or
+ * llm_decode_step_async / llm_generate step), read back from the buffers the
+ * step exchanges them through, for layer-by-layer checks like those of "The
+ * Forward Pass in Java", Example 11 (llama.cpp's tensor names):
+ *   LLM_DEBUG_Q / _K / _V   q, k, v after their biases, before RoPE
+ *                           (n_heads*head_dim / n_kv_heads*head_dim values);
+ *                           v is llama.cpp's Vcur
+ *   LLM_DEBUG_ATTN_OUT      attn_out: the output projection's update of the
+ *                           residual stream (dim values)
+ *   LLM_DEBUG_FFN_SWIGLU    ffn_swiglu: silu(gate) * up (ffn_dim values)
+ *   LLM_DEBUG_FFN_OUT       ffn_out: the down projection's update (dim)
+ * The updates are the decode step's fixed-point sums (2^-32 steps) rounded to
+ * float.  host: HOST float[n], n the tensor's length.  Synchronous.
+ * Errors: INVALID_ARG (which, NULL, n), OUT_OF_RANGE (layer), STATE when no
+ * step ran since create or llm_reset, or the values are not all from the
+ * last decode step (llm_prefill and llm_decode_step_noalloc do not write these
+ * buffers). */
+enum {
+    LLM_DEBUG_Q = 0, LLM_DEBUG_K = 1, LLM_DEBUG_V = 2,
+    LLM_DEBUG_ATTN_OUT = 3, LLM_DEBUG_FFN_SWIGLU = 4, LLM_DEBUG_FFN_OUT = 5
+};
+int llm_debug_tensor(llm_handle *h, int layer, int which, float *host, int32_t n);
+
 /* 1 if this library was built with LLM_CHECKED (device-side index checks on
  * the decode step's global writes and weight-stream ranges, reporting
  * LLM_ERR_CHECK instead of trapping), else 0. */

@@ -20,6 +20,7 @@ LLM_ERR_INVALID_ARG, LLM_ERR_UNSUPPORTED, LLM_ERR_OUT_OF_RANGE = -1, -2, -3
 LLM_ERR_CUDA, LLM_ERR_NO_MEMORY, LLM_ERR_DEVICE_TIMEOUT, LLM_ERR_STATE, LLM_ERR_NONFINITE = -4, -5, -6, -7, -8
 LLM_ERR_CHECK = -9
 LLM_NUMERICS_EXACT, LLM_NUMERICS_LLAMACPP = 0, 1
+LLM_DEBUG_Q, LLM_DEBUG_K, LLM_DEBUG_V, LLM_DEBUG_ATTN_OUT, LLM_DEBUG_FFN_SWIGLU, LLM_DEBUG_FFN_OUT = range(6)
 
 
 class llm_config(ctypes.Structure):
@@ -89,6 +90,7 @@ _SIGS = {
     "llm_last_error": ([_vp], ctypes.c_char_p),
     "llm_test_fail_alloc": ([_i32], _int),
     "llm_checked_build": ([], _int),
+    "llm_debug_tensor": ([_vp, _int, _int, _vp, _i32], _int),
     "llm_test_logits_limit": ([_vp, _i32], _int),
     "llm_test_guards": ([_vp], ctypes.c_int64),
     "llm_test_poke_guard": ([_vp, _int], _int),
@@ -229,6 +231,17 @@ def llm_test_gemv(h, which: int, layer: int, x_dev, y_dev):
 
 def llm_column_groups(h) -> int:
     return int(_lib.llm_column_groups(h))
+
+
+def llm_debug_tensor(h, layer: int, which: int) -> np.ndarray:
+    """One named intermediate of the last decode step (LLM_DEBUG_*)."""
+    c = llm_get_config(h)
+    q_dim, kv_dim = c.n_heads * c.head_dim, c.n_kv_heads * c.head_dim
+    n = {LLM_DEBUG_Q: q_dim, LLM_DEBUG_K: kv_dim, LLM_DEBUG_V: kv_dim, LLM_DEBUG_ATTN_OUT: c.dim,
+         LLM_DEBUG_FFN_SWIGLU: c.ffn_dim, LLM_DEBUG_FFN_OUT: c.dim}.get(which, 0)
+    out = np.empty(max(n, 1), np.float32)
+    _check(_lib.llm_debug_tensor(h, int(layer), int(which), out.ctypes.data, n), h)
+    return out[:n]
 
 
 def llm_checked_build() -> bool:

@@ -893,6 +893,59 @@ extern "C" int llm_test_gemv(llm_handle* h, int which, int layer, const float* x
     return read_device_error(h);
 }
 
+// Named intermediates of the last decode step, read back from the buffers the
+// step kernel exchanges them through: the tagged Q/K/V and SwiGLU vectors,
+// and the residual accumulator words of the attention and FFN updates.
+extern "C" int llm_debug_tensor(llm_handle* h, int layer, int which, float* host, int32_t n) {
+    LIVE_OR_RETURN(h);
+    if (!host) return fail(h, LLM_ERR_INVALID_ARG, "NULL host buffer");
+    if (layer < 0 || layer >= h->cfg.n_layers) return fail(h, LLM_ERR_OUT_OF_RANGE, "layer %d", layer);
+    const llm_config& c = h->cfg;
+    const TvLayout tl = tv_layout(c.dim, h->q_dim, h->kv_dim, c.ffn_dim);
+    long long off;
+    int len;
+    bool tagged = true;
+    switch (which) {
+        case LLM_DEBUG_Q: off = tl.qkv; len = h->q_dim; break;
+        case LLM_DEBUG_K: off = tl.qkv + h->q_dim; len = h->kv_dim; break;
+        case LLM_DEBUG_V: off = tl.qkv + h->q_dim + h->kv_dim; len = h->kv_dim; break;
+        case LLM_DEBUG_FFN_SWIGLU: off = tl.u; len = c.ffn_dim; break;
+        case LLM_DEBUG_ATTN_OUT: off = 0; len = c.dim; tagged = false; break;
+        case LLM_DEBUG_FFN_OUT: off = 1; len = c.dim; tagged = false; break;
+        default: return fail(h, LLM_ERR_INVALID_ARG, "which %d", which);
+    }
+    if (n != len) return fail(h, LLM_ERR_INVALID_ARG, "tensor %d has %d values, buffer %d", which, len, n);
+    CK(h, cudaStreamSynchronize(h->st));
+    unsigned epoch = 0;
+    CK(h, cudaMemcpy(&epoch, h->epoch, 4, cudaMemcpyDeviceToHost));
+    if (epoch == 0) return fail(h, LLM_ERR_STATE, "no decode step has run on this handle since its reset");
+    std::vector<unsigned long long> w(len);
+    const unsigned long long* src;
+    if (tagged) {
+        src = h->tv + (long long)layer * tl.stride + off;
+    } else {
+        // the step's parity of [2][n_layers][2][dim]; word (layer, off)
+        src = h->delta + (size_t)(epoch & 1u) * c.n_layers * 2 * c.dim + ((size_t)layer * 2 + off) * c.dim;
+    }
+    CK(h, cudaMemcpy(w.data(), src, (size_t)len * 8, cudaMemcpyDeviceToHost));
+    for (int i = 0; i < len; i++) {
+        if (tagged) {
+            if ((unsigned)(w[i] >> 32) != epoch)
+                return fail(h, LLM_ERR_STATE, "value %d of tensor %d is not from the last decode step", i, which);
+            const uint32_t bits = (uint32_t)w[i];
+            memcpy(&host[i], &bits, 4);
+        } else {
+            // (count << 56) + round(v * 2^32): the count rounds to the nearest multiple of 2^56
+            const unsigned long long cnt = (w[i] + (1ull << 55)) >> 56;
+            if (cnt != (unsigned long long)h->ngrp)
+                return fail(h, LLM_ERR_STATE, "accumulator %d of tensor %d holds %llu of %d parts", i, which, cnt, h->ngrp);
+            const long long v = (long long)(w[i] - (cnt << 56));
+            host[i] = (float)ldexp((double)v, -32);
+        }
+    }
+    return LLM_OK;
+}
+
 extern "C" int llm_test_logits_limit(llm_handle* h, int32_t limit) {
     LIVE_OR_RETURN(h);
 #ifdef LLM_CHECKED
