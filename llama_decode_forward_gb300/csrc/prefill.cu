@@ -21,6 +21,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <string>
 #include <vector>
 
@@ -32,18 +33,25 @@ namespace {
 
 constexpr int kGBM = 128, kGBK = 64;
 constexpr int kGABytes = kGBM * kGBK * 2;
-// Tile width BN and ring depth: 96 KB of stages, so two CTAs share an SM.
-template <int BN>
-struct GemmTile {
-    static constexpr int kStages = BN == 64 ? 4 : 3;
-    static constexpr int kStageBytes = kGABytes + BN * kGBK * 2;
-    static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
-};
+// GEMM tile widths: the Q/K/V output, the dim-wide outputs (O, down: 64 wide
+// so that a 512-token batch still has 128 tiles), the gate/up output
+constexpr int kBnQkv = 128, kBnNarrow = 64, kBnWide = 256;
 constexpr long long kSpinLimit = 200000000ll;   // mbarrier polls before a wait gives up
 
 __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t par, int* err) {
     for (long long i = 0; i < kSpinLimit; i++)
         if (mbar_test_wait(bar, par)) return true;
+    atomicOr(err, kErrTimeout);
+    return false;
+}
+
+// The same wait with the threads suspended between probes (about 1 us at
+// most per probe): for warps that wait through a whole main loop, whose
+// polling would otherwise take shared-memory bandwidth from the tensor cores.
+constexpr long long kSleepLimit = 4000000ll;    // suspended probes before a wait gives up (a few seconds)
+__device__ __forceinline__ bool sleep_parity(uint64_t* bar, uint32_t par, int* err) {
+    for (long long i = 0; i < kSleepLimit; i++)
+        if (mbar_sleep_wait(bar, par)) return true;
     atomicOr(err, kErrTimeout);
     return false;
 }
@@ -69,120 +77,314 @@ struct GemmOut {
     __half* hout;        // kEpiSwiGLU: [M][N/2] f16, silu(acc[2i]) * acc[2i+1]
 };
 
-template <int BN, int EPI>
-__global__ void __launch_bounds__(128, 2) gemm_f16_kernel(const __grid_constant__ CUtensorMap ma,
-                                                          const __grid_constant__ CUtensorMap mb, GemmOut o, int M,
-                                                          int N, int K, int* err) {
-    constexpr int kGStages = GemmTile<BN>::kStages, kGStageBytes = GemmTile<BN>::kStageBytes, kGBN = BN;
+// Q8_0 weights of a GEMM: the FP16 scales of the library layout (row r's
+// block b at d[r * dstride + b]); the int8 quants come through a tensor map.
+struct GemmScales {
+    const __half* d;
+    int dstride;
+};
+
+// Shared-memory plan of the GEMM: a ring of kStages stages (A tile, W tile
+// as F16, and for Q8_0 weights the W tile's int8 quants), then the
+// epilogue's transpose buffers and the barriers.
+template <int BN, bool Q8>
+struct GemmPlan {
+    static constexpr int kBBytes = BN * kGBK * 2;
+    static constexpr int kQBytes = Q8 ? BN * kGBK : 0;
+    static constexpr int kStageBytes = kGABytes + kBBytes + kQBytes;
+    static constexpr int kStages = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
+    static constexpr int kEpiWarps = 4;
+    static constexpr int kConvWarps = Q8 ? 4 : 0;
+    static constexpr int kThreads = 32 * (2 + kEpiWarps + kConvWarps);
+    static constexpr int kTransBytes = kEpiWarps * 32 * 33 * 4;
+    static constexpr int kBarBytes = 8 * (3 * kStages + 4 + 1) + 16;
+    static constexpr int kSmem = kStages * kStageBytes + kTransBytes + kBarBytes + 1024;
+};
+
+// One F16 value of the W tile in the 128-byte-swizzled K-major layout the
+// MMA descriptors describe: row r's 64 values fill 128 bytes at r * 128, its
+// 16-byte chunk c at chunk position c ^ (r & 7).
+__device__ __forceinline__ uint32_t sw128_chunk(uint32_t tile, int r, int c) {
+    return tile + (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) * 16);
+}
+
+// Four int8 quants (one word) times the scale pair d2, as two F16 pairs: the
+// quant q becomes the F16 value 1152 + q exactly (bytes 0x64, q ^ 0x80: 1024
+// + (q + 128)), 1152 is subtracted exactly, and the product d * q is rounded
+// once to nearest even by the F16 multiply.
+__device__ __forceinline__ void q4_to_f16(uint32_t w, __half2 d2, uint32_t& lo, uint32_t& hi) {
+    const uint32_t x = w ^ 0x80808080u;
+    const __half2 off = __half2half2(__ushort_as_half((unsigned short)0x6480));   // 1152
+    const uint32_t ua = __byte_perm(x, 0x64646464u, 0x4140u), ub = __byte_perm(x, 0x64646464u, 0x4342u);
+    __half2 a = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&ua), off), d2);
+    __half2 b = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&ub), off), d2);
+    lo = *reinterpret_cast<const uint32_t*>(&a);
+    hi = *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// C[M][N] = A[M][K] . W[N][K]^T, persistent and warp-specialised, one CTA per
+// SM:
+//   warp 0     TMA producer (one lane): per k-step the 128 x 64 A tile and
+//              the BN x 64 W tile (F16; for Q8_0 weights its int8 quants)
+//              into the ring stage;
+//   warp 1     allocates 2 * BN TMEM columns (two accumulators) and issues
+//              tcgen05.mma (M 128, N BN, K 16) from one lane, committing each
+//              stage back to the producer and each finished tile to the
+//              epilogue;
+//   warps 2-5  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 of the
+//              finished accumulator (tcgen05.ld) while the next tile's MMAs
+//              run in the other one, transposes each 32 x 32 block through
+//              shared memory and writes rows with the lanes along the columns;
+//   warps 6-9  (Q8_0) expand each stage's quants to F16 (d * q rounded to
+//              nearest even, as an F16 matrix of the weights would hold)
+//              into the stage's W tile.
+// Tile t (t = blockIdx.x, + gridDim.x, ...) is row block t % Mt, column block
+// t / Mt: CTAs working at the same time share W tiles.  Every wait is
+// bounded (kErrTimeout, then the role stops).
+template <int BN, int EPI, bool Q8>
+__global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb, GemmScales ws,
+                GemmOut o, int M, int N, int K, int* err) {
+    using G = GemmPlan<BN, Q8>;
+    constexpr int S = G::kStages;
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + kGStages * kGStageBytes);
-    uint64_t* empty = full + kGStages;
-    uint64_t* done = empty + kGStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    float* trans = reinterpret_cast<float*>(sm + S * G::kStageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S * G::kStageBytes + G::kTransBytes);
+    uint64_t* empty = full + S;
+    uint64_t* conv = empty + S;          // Q8_0: the stage's W tile is expanded
+    uint64_t* accf = conv + S;           // [2] accumulator b holds a finished tile
+    uint64_t* acce = accf + 2;           // [2] accumulator b has been read
+    uint64_t* fin = acce + 2;            // every MMA issued has completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * kGBM, n0 = blockIdx.x * kGBN;
+    const int Mt = (M + kGBM - 1) / kGBM, Nt = (N + BN - 1) / BN, tiles = Mt * Nt, nk = K / kGBK;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kGStages; s++) {
+        for (int s = 0; s < S; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&conv[s], G::kConvWarps > 0 ? G::kConvWarps : 1);
         }
-        mbar_init(done, 1);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], G::kEpiWarps);
+        }
+        mbar_init(fin, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) {
+    if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
-                     "r"(kGBN));
+                     "r"(2 * BN));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;");
     const uint32_t tmem = *tmem_slot;
-    // instruction descriptor: F32 accumulator, F16 A and B, both K-major, N = 128, M = 128
-    const uint32_t idesc = (1u << 4) | ((uint32_t)(kGBN >> 3) << 17) | ((uint32_t)(kGBM >> 4) << 24);
-    const int nk = K / kGBK;
-    if (threadIdx.x == 0) {
-        bool ok = true;
-        for (int kt = 0; kt < nk + kGStages && ok; kt++) {
-            if (kt < nk) {                                          // load k-tile kt
-                const int s = kt % kGStages;
-                if (kt >= kGStages) ok = wait_parity(&empty[s], ((kt / kGStages) - 1) & 1, err);
-                if (!ok) break;
-                uint8_t* st = sm + s * kGStageBytes;
-                mbar_arrive_expect_tx(&full[s], kGStageBytes);
-                tma_2d_g2s(st, &ma, kt * kGBK, m0, &full[s]);
-                tma_2d_g2s(st + kGABytes, &mb, kt * kGBK, n0, &full[s]);
-            }
-            const int kc = kt - (kGStages - 1);                    // multiply k-tile kc
-            if (kc >= 0 && kc < nk) {
-                const int s = kc % kGStages;
-                ok = wait_parity(&full[s], (kc / kGStages) & 1, err);
-                if (!ok) break;
-                asm volatile("tcgen05.fence::after_thread_sync;");
-                uint8_t* st = sm + s * kGStageBytes;
-                const uint64_t da = umma_desc_sw128(st), db = umma_desc_sw128(st + kGABytes);
-#pragma unroll
-                for (int kk = 0; kk < kGBK / 16; kk++) {
-                    const uint32_t accumulate = (kc > 0 || kk > 0) ? 1u : 0u;
-                    asm volatile(
-                        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-                        "l"(da + 2 * kk), "l"(db + 2 * kk), "r"(idesc), "r"(accumulate));
+
+    if (warp == 0) {
+        // ---- producer
+        if (lane == 0) {
+            long long it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                const int m0 = (t % Mt) * kGBM, n0 = (t / Mt) * BN;
+                for (int kt = 0; kt < nk && ok; kt++, it++) {
+                    const int s = (int)(it % S);
+                    if (!(ok = wait_parity(&empty[s], (uint32_t)(((it / S) & 1) ^ 1), err))) break;
+                    uint8_t* st = sm + s * G::kStageBytes;
+                    mbar_arrive_expect_tx(&full[s], (uint32_t)(kGABytes + (Q8 ? G::kQBytes : G::kBBytes)));
+                    tma_2d_g2s(st, &ma, kt * kGBK, m0, &full[s]);
+                    tma_2d_g2s(st + kGABytes + (Q8 ? G::kBBytes : 0), &mb, kt * kGBK, n0, &full[s]);
                 }
+            }
+            // the last copies have landed before the CTA can exit (at once when
+            // the MMAs consumed them)
+            for (long long k = it - 1; k >= 0 && k >= it - S; k--)
+                wait_parity(&full[(int)(k % S)], (uint32_t)((k / S) & 1), err);
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer
+        if (lane == 0) {
+            // F32 accumulator, F16 A and B, both K-major, N = BN, M = 128
+            const uint32_t idesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kGBM >> 4) << 24);
+            long long it = 0;
+            bool ok = true;
+            int j = 0;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, j++) {
+                const int b = j & 1;
+                if (!(ok = wait_parity(&acce[b], (uint32_t)(((j >> 1) & 1) ^ 1), err))) break;
+                asm volatile("tcgen05.fence::after_thread_sync;");
+                const uint32_t dacc = tmem + (uint32_t)(b * BN);
+                for (int kt = 0; kt < nk; kt++, it++) {
+                    const int s = (int)(it % S);
+                    const uint32_t par = (uint32_t)((it / S) & 1);
+                    if (!(ok = wait_parity(&full[s], par, err))) break;
+                    if (Q8 && !(ok = wait_parity(&conv[s], par, err))) break;
+                    asm volatile("tcgen05.fence::after_thread_sync;");
+                    uint8_t* st = sm + s * G::kStageBytes;
+                    const uint64_t da = umma_desc_sw128(st), db = umma_desc_sw128(st + kGABytes);
+#pragma unroll
+                    for (int kk = 0; kk < kGBK / 16; kk++) {
+                        const uint32_t accumulate = (kt > 0 || kk > 0) ? 1u : 0u;
+                        asm volatile(
+                            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dacc),
+                            "l"(da + 2 * kk), "l"(db + 2 * kk), "r"(idesc), "r"(accumulate));
+                    }
+                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                     smem_addr(&empty[s]))
+                                 : "memory");
+                }
+                if (!ok) break;
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                 smem_addr(&empty[s]))
+                                 smem_addr(&accf[b]))
                              : "memory");
             }
+            // every MMA issued has completed before the accumulators are freed
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                             smem_addr(fin))
+                         : "memory");
+            wait_parity(fin, 0, err);
         }
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                         smem_addr(done))
-                     : "memory");
-    }
-    __syncwarp();
-    wait_parity(done, 0, err);
-    asm volatile("tcgen05.fence::after_thread_sync;");
-    // epilogue: warp w owns TMEM lanes (rows) 32w..32w+31, 32 columns per load
-    const int row = m0 + warp * 32 + lane;
-    for (int c0 = 0; c0 < kGBN; c0 += 32) {
-        uint32_t v[32];
-        const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0;
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
-              "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
-              "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
-              "=r"(v[30]), "=r"(v[31])
-            : "r"(taddr));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (row < M) {
-            const int cb = n0 + c0;
-            if constexpr (EPI == kEpiBias) {
+    } else if (warp < 2 + G::kEpiWarps) {
+        // ---- epilogue
+        const int q = warp & 3;                                   // TMEM lanes 32q .. 32q+31
+        float* tb = trans + (warp - 2) * 32 * 33;
+        int j = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, j++) {
+            const int b = j & 1;
+            const int m0 = (t % Mt) * kGBM, n0 = (t / Mt) * BN;
+            if (!sleep_parity(&accf[b], (uint32_t)((j >> 1) & 1), err)) break;
+            asm volatile("tcgen05.fence::after_thread_sync;");
+            const int rbase = m0 + q * 32;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c0);
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                    "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                      "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+                      "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]),
+                      "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]),
+                      "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                    : "r"(taddr));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                // row `lane` of this 32 x 32 block, transposed through shared memory
+                if constexpr (EPI == kEpiSwiGLU) {
+                    // columns 2i (gate) and 2i+1 (up) of the interleaved matrix
 #pragma unroll
-                for (int j = 0; j < 32; j++)
-                    if (cb + j < N) o.out[(size_t)row * N + cb + j] = __uint_as_float(v[j]) + (o.bias ? o.bias[cb + j] : 0.f);
-            } else if constexpr (EPI == kEpiResidual) {
-#pragma unroll
-                for (int j = 0; j < 32; j++)
-                    if (cb + j < N) o.resid[(size_t)row * N + cb + j] += __uint_as_float(v[j]);
-            } else {
-                // columns 2i (gate) and 2i+1 (up) of the interleaved matrix
-#pragma unroll
-                for (int j = 0; j < 32; j += 2)
-                    if (cb + j + 1 < N) {
-                        const float g = __uint_as_float(v[j]), up = __uint_as_float(v[j + 1]);
+                    for (int i = 0; i < 16; i++) {
+                        const float g = __uint_as_float(v[2 * i]), up = __uint_as_float(v[2 * i + 1]);
                         const float e = expf(-g);
-                        o.hout[(size_t)row * (N / 2) + (cb + j) / 2] =
-                            __float2half_rn(__fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), up));
+                        tb[lane * 33 + i] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), up);
                     }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; i++) tb[lane * 33 + i] = __uint_as_float(v[i]);
+                }
+                __syncwarp();
+                if constexpr (EPI == kEpiSwiGLU) {
+                    // two rows of 16 F16 outputs per pass
+                    const int oc = (n0 + c0) / 2 + (lane & 15);
+#pragma unroll 4
+                    for (int r2 = 0; r2 < 32; r2 += 2) {
+                        const int r = r2 + (lane >> 4), row = rbase + r;
+                        if (row < M && 2 * oc + 1 < N)
+                            o.hout[(size_t)row * (N / 2) + oc] = __float2half_rn(tb[r * 33 + (lane & 15)]);
+                    }
+                } else if constexpr (EPI == kEpiBias) {
+                    const int col = n0 + c0 + lane;
+                    const float bias = o.bias && col < N ? o.bias[col] : 0.f;
+#pragma unroll 4
+                    for (int r = 0; r < 32; r++) {
+                        const int row = rbase + r;
+                        if (row < M && col < N) o.out[(size_t)row * N + col] = tb[r * 33 + lane] + bias;
+                    }
+                } else {
+                    // the 32 residual values are all loaded before any is stored
+                    // (one memory latency per block, not one per row)
+                    const int col = n0 + c0 + lane;
+                    float old[32];
+#pragma unroll
+                    for (int r = 0; r < 32; r++) {
+                        const int row = rbase + r;
+                        old[r] = row < M && col < N ? __ldcg(o.resid + (size_t)row * N + col) : 0.f;
+                    }
+#pragma unroll
+                    for (int r = 0; r < 32; r++) {
+                        const int row = rbase + r;
+                        if (row < M && col < N) o.resid[(size_t)row * N + col] = old[r] + tb[r * 33 + lane];
+                    }
+                }
+                __syncwarp();
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[b]);
+        }
+    } else if constexpr (Q8) {
+        // ---- Q8_0 expansion: the W tile's BN rows x 4 pairs of 16-byte
+        // output chunks are items i = c + 128 k of the 128 converter threads
+        // (row i % BN, pair i / BN): 16 quants in, 16 F16 values out.  A
+        // thread's items lie in kRows rows (c + 128 j); each row's two block
+        // scales of a k-step are one 4-byte word, loaded a k-step ahead.
+        const int c = threadIdx.x - 32 * (2 + G::kEpiWarps);
+        constexpr int kItems = BN * 4 / 128;
+        constexpr int kRows = BN > 128 ? BN / 128 : 1;
+        long long it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            const int n0 = (t / Mt) * BN;
+            const uint32_t* drow[kRows];
+#pragma unroll
+            for (int j = 0; j < kRows; j++) {
+                const int wrow = n0 + (c + 128 * j) % BN;
+                drow[j] = wrow < N ? reinterpret_cast<const uint32_t*>(ws.d + (size_t)wrow * ws.dstride) : nullptr;
+            }
+            uint32_t dnext[kRows];
+#pragma unroll
+            for (int j = 0; j < kRows; j++) dnext[j] = drow[j] ? __ldg(drow[j]) : 0u;
+            for (int kt = 0; kt < nk; kt++, it++) {
+                uint32_t dcur[kRows];
+#pragma unroll
+                for (int j = 0; j < kRows; j++) {
+                    dcur[j] = dnext[j];
+                    dnext[j] = drow[j] && kt + 1 < nk ? __ldg(drow[j] + kt + 1) : 0u;
+                }
+                const int s = (int)(it % S);
+                if (!(ok = sleep_parity(&full[s], (uint32_t)((it / S) & 1), err))) break;
+                uint8_t* st = sm + s * G::kStageBytes;
+                const uint32_t btile = smem_addr(st + kGABytes);
+                const uint8_t* qtile = st + kGABytes + G::kBBytes;
+#pragma unroll
+                for (int k = 0; k < kItems; k++) {
+                    const int i = c + 128 * k, r = i % BN, pair = i / BN;
+                    const uint32_t dw = dcur[BN > 128 ? k % kRows : 0];
+                    const __half d = __ushort_as_half((unsigned short)(pair < 2 ? dw & 0xFFFFu : dw >> 16));
+                    const __half2 d2 = __half2half2(d);
+                    const uint4 qv = *reinterpret_cast<const uint4*>(qtile + r * kGBK + pair * 16);
+                    uint32_t h[8];
+                    q4_to_f16(qv.x, d2, h[0], h[1]);
+                    q4_to_f16(qv.y, d2, h[2], h[3]);
+                    q4_to_f16(qv.z, d2, h[4], h[5]);
+                    q4_to_f16(qv.w, d2, h[6], h[7]);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sw128_chunk(btile, r, 2 * pair)),
+                                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sw128_chunk(btile, r, 2 * pair + 1)),
+                                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]) : "memory");
+                }
+                fence_proxy_async_smem();                               // the MMA reads the tile
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&conv[s]);
             }
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kGBN));
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BN));
 }
 
 // Embedding rows of the batch: F16 widened, or Q8_0 decoded as d * qs (both
@@ -202,28 +404,6 @@ __global__ void embed_rows_kernel(const int* tok, int n, DMat embd, int wtype, i
 }
 
 // A Q8_0 matrix (library layout) expanded to F16 for the tensor-core GEMMs:
-// d * qs, exact in F32, rounded to nearest even (the prefill's operand
-// precision; the decode step keeps the exact values).  8 values per thread.
-__global__ void q8_to_f16_kernel(DMat m, int rows, __half* out) {
-    const long long groups = (long long)rows * m.cols / 8;
-    for (long long gidx = blockIdx.x * (long long)blockDim.x + threadIdx.x; gidx < groups;
-         gidx += (long long)gridDim.x * blockDim.x) {
-        const long long e = gidx * 8;
-        const long long r = e / m.cols;
-        const int c = (int)(e - r * m.cols);
-        const float d = __half2float(m.d[r * m.dstride + c / 32]);
-        const uint2 qv = *reinterpret_cast<const uint2*>(m.q + e);
-        const uint32_t w[2] = {qv.x, qv.y};
-        __half h[8];
-#pragma unroll
-        for (int k = 0; k < 8; k++) {
-            const int q = (int)(int8_t)((w[k / 4] >> (8 * (k % 4))) & 0xFFu);
-            h[k] = __float2half_rn(__fmul_rn(d, (float)q));
-        }
-        *reinterpret_cast<uint4*>(out + e) = *reinterpret_cast<const uint4*>(h);
-    }
-}
-
 // RMSNorm of every row ("The Forward Pass in Java", Example 4: y = (x*scale)*g,
 // scale = 1/sqrt(mean(x^2) + eps)); the GEMM operand is y rounded to F16.
 __global__ void rmsnorm_rows_f16_kernel(const float* X, int n, int dim, const float* g, float eps, __half* Y) {
@@ -666,18 +846,35 @@ bool gemm_map(CUtensorMap* m, const void* base, int K, int rows, int box_rows = 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int EPI>
-cudaError_t gemm(cudaStream_t st, const CUtensorMap& ma, const CUtensorMap& mb, const GemmOut& o, int M, int N, int K,
-                 int* err) {
+// The int8 quants of a Q8_0 matrix in the library layout ([rows][K], K
+// contiguous) as BN x 64 boxes, no swizzle.
+bool q8_map(CUtensorMap* m, const void* base, int K, int rows, int box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)K};
+    cuuint32_t box[2] = {(cuuint32_t)kGBK, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One GEMM: min(tiles, SMs) persistent CTAs.  mb: the F16 weight tiles, or
+// for Q8 the quant tiles (scales in ws).
+template <int BN, int EPI, bool Q8>
+cudaError_t gemm(cudaStream_t st, int sms, const CUtensorMap& ma, const CUtensorMap& mb, GemmScales ws,
+                 const GemmOut& o, int M, int N, int K, int* err) {
+    using G = GemmPlan<BN, Q8>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_f16_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             GemmTile<BN>::kSmem);
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, EPI, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             G::kSmem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    dim3 grid((N + BN - 1) / BN, (M + kGBM - 1) / kGBM);
-    gemm_f16_kernel<BN, EPI><<<grid, 128, GemmTile<BN>::kSmem, st>>>(ma, mb, o, M, N, K, err);
+    const int tiles = ((M + kGBM - 1) / kGBM) * ((N + BN - 1) / BN);
+    gemm_kernel<BN, EPI, Q8><<<tiles < sms ? tiles : sms, G::kThreads, G::kSmem, st>>>(ma, mb, ws, o, M, N, K, err);
     return cudaGetLastError();
 }
 
@@ -688,21 +885,11 @@ bool prefill_supported(const PrefillCtx& c) {
            c.n_heads / c.n_kv * c.hd <= 8 * 128 && c.rope_dims / 2 <= 128;
 }
 
-// The largest layer matrix (elements): the F16 expansion of a Q8_0 one.
-static size_t prefill_expand_elems(const PrefillCtx& c) {
-    size_t m = (size_t)(c.q_dim + 2 * c.kv_dim) * c.dim;
-    m = std::max(m, (size_t)c.dim * c.q_dim);
-    m = std::max(m, (size_t)2 * c.ffn * c.dim);
-    m = std::max(m, (size_t)c.dim * c.ffn);
-    return m;
-}
-
 size_t prefill_workspace_bytes(const PrefillCtx& c) {
     const size_t M = kPrefillRows;
     auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
-    const size_t expand = c.wtype == LLM_Q8_0 ? al(prefill_expand_elems(c) * 2) : 0;
     return al(M * 4) + al(M * c.dim * 4) + al(M * c.dim * 2) + al(M * (c.q_dim + 2 * c.kv_dim) * 4) +
-           al(M * c.q_dim * 2) + al(M * c.ffn * 2) + al((size_t)c.dim * 4) + expand;
+           al(M * c.q_dim * 2) + al(M * c.ffn * 2) + al((size_t)c.dim * 4);
 }
 
 // Runs the batch; `ws` holds prefill_workspace_bytes(c).  Returns a CUDA error
@@ -718,7 +905,6 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
     __half* Ah = reinterpret_cast<__half*>(w); w += al(M * c.q_dim * 2);
     __half* Hh = reinterpret_cast<__half*>(w); w += al(M * c.ffn * 2);
     float* ylast = reinterpret_cast<float*>(w); w += al((size_t)c.dim * 4);
-    __half* Wx = c.wtype == LLM_Q8_0 ? reinterpret_cast<__half*>(w) : nullptr;   // F16 expansion of a Q8_0 matrix
     cudaError_t e;
 #define PF_CK(call, what)                 \
     do {                                  \
@@ -732,28 +918,37 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
         *msg = "tensor map of an activation operand";
         return cudaErrorInvalidValue;
     }
-    // weight operands: the F16 matrices themselves, or (Q8_0) each matrix
-    // expanded to F16 into Wx just before its GEMM
-    std::vector<CUtensorMap> mw(c.wtype == LLM_F16 ? (size_t)4 * c.n_layers : 0);
-    for (int l = 0; l < (int)mw.size() / 4; l++) {
+    // weight operands: the F16 matrices, or the int8 quants of the Q8_0 ones
+    // (expanded to F16 tile by tile inside the GEMM), per layer: QKV, O,
+    // gate/up (single rows), down; box heights = the GEMMs' tile widths
+    const bool q8 = c.wtype == LLM_Q8_0;
+    std::vector<CUtensorMap> mw((size_t)4 * c.n_layers);
+    for (int l = 0; l < c.n_layers; l++) {
         const LayerDev& L = c.layers[l];
-        if (!gemm_map(&mw[4 * l + 0], L.qkv.q, c.dim, L.qkv.rows, 64) ||
-            !gemm_map(&mw[4 * l + 1], L.o.q, c.q_dim, L.o.rows, 64) ||
-            !gemm_map(&mw[4 * l + 2], L.gu.q, c.dim, 2 * L.gu.rows, 128) ||
-            !gemm_map(&mw[4 * l + 3], L.down.q, c.ffn, L.down.rows, 64)) {
+        auto map = [&](CUtensorMap* m, const DMat& d, int K, int rows, int box) {
+            return q8 ? q8_map(m, d.q, K, rows, box) : gemm_map(m, d.q, K, rows, box);
+        };
+        if (!map(&mw[4 * l + 0], L.qkv, c.dim, L.qkv.rows, kBnQkv) ||
+            !map(&mw[4 * l + 1], L.o, c.q_dim, L.o.rows, kBnNarrow) ||
+            !map(&mw[4 * l + 2], L.gu, c.dim, 2 * L.gu.rows, kBnWide) ||
+            !map(&mw[4 * l + 3], L.down, c.ffn, L.down.rows, kBnNarrow)) {
             *msg = "tensor map of a weight matrix";
             return cudaErrorInvalidValue;
         }
     }
-    CUtensorMap mq;
-    auto weights = [&](int l, int which, const DMat& m, int rows, int K, int box) -> const CUtensorMap* {
-        if (c.wtype == LLM_F16) return &mw[4 * l + which];
-        const long long groups = (long long)rows * K / 8;
-        const int blocks = (int)std::min<long long>((groups + 255) / 256, (long long)c.sms * 16);
-        q8_to_f16_kernel<<<blocks, 256, 0, c.st>>>(m, rows, Wx);
-        if (cudaGetLastError() != cudaSuccess || !gemm_map(&mq, Wx, K, rows, box)) return nullptr;
-        return &mq;
+    auto run = [&](auto bn, auto epi, const CUtensorMap& ma, const CUtensorMap& mb, const DMat& wm, const GemmOut& o,
+                   int M, int N, int K) -> cudaError_t {
+        constexpr int BN = decltype(bn)::value, EPI = decltype(epi)::value;
+        const GemmScales sc{wm.d, wm.dstride};
+        return q8 ? gemm<BN, EPI, true>(c.st, c.sms, ma, mb, sc, o, M, N, K, c.err)
+                  : gemm<BN, EPI, false>(c.st, c.sms, ma, mb, sc, o, M, N, K, c.err);
     };
+    using Qkv = std::integral_constant<int, kBnQkv>;
+    using Narrow = std::integral_constant<int, kBnNarrow>;
+    using Wide = std::integral_constant<int, kBnWide>;
+    using EBias = std::integral_constant<int, kEpiBias>;
+    using EResid = std::integral_constant<int, kEpiResidual>;
+    using ESwi = std::integral_constant<int, kEpiSwiGLU>;
     const int gq = c.n_heads / c.n_kv;
     const int attn_smem = (int)(2 * sizeof(__half) * kAttnTile * c.hd +
                                 sizeof(float) * ((size_t)gq * c.hd + (size_t)gq * kAttnTile + 3 * gq));
@@ -770,10 +965,8 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
             const LayerDev& L = c.layers[l];
             rmsnorm_rows_f16_kernel<<<nb, 256, 0, c.st>>>(X, nb, c.dim, L.attn_norm, c.eps, Xh);
             PF_CK(cudaGetLastError(), "attention RMSNorm");
-            const CUtensorMap* wm;
             GemmOut oq{QKV, L.qkv_bias, nullptr, nullptr};
-            if (!(wm = weights(l, 0, L.qkv, L.qkv.rows, c.dim, 64))) { *msg = "QKV weights"; return cudaErrorInvalidValue; }
-            PF_CK((gemm<64, kEpiBias>(c.st, mXh, *wm, oq, nb, L.qkv.rows, c.dim, c.err)), "QKV GEMM");
+            PF_CK(run(Qkv{}, EBias{}, mXh, mw[4 * l + 0], L.qkv, oq, nb, L.qkv.rows, c.dim), "QKV GEMM");
             rope_kv_rows_kernel<<<nb, 128, 0, c.st>>>(QKV, nb, p0, c.n_heads, c.n_kv, c.hd, c.rope_dims, c.neox,
                                                       c.theta_scale, c.rope_freqs, L.kc, L.vc);
             PF_CK(cudaGetLastError(), "RoPE and KV append");
@@ -787,16 +980,13 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
                 PF_CK(ea, "attention");
             }
             GemmOut oo{nullptr, nullptr, X, nullptr};
-            if (!(wm = weights(l, 1, L.o, L.o.rows, c.q_dim, 64))) { *msg = "O weights"; return cudaErrorInvalidValue; }
-            PF_CK((gemm<64, kEpiResidual>(c.st, mAh, *wm, oo, nb, c.dim, c.q_dim, c.err)), "O GEMM");
+            PF_CK(run(Narrow{}, EResid{}, mAh, mw[4 * l + 1], L.o, oo, nb, c.dim, c.q_dim), "O GEMM");
             rmsnorm_rows_f16_kernel<<<nb, 256, 0, c.st>>>(X, nb, c.dim, L.ffn_norm, c.eps, Xh);
             PF_CK(cudaGetLastError(), "FFN RMSNorm");
             GemmOut og{nullptr, nullptr, nullptr, Hh};
-            if (!(wm = weights(l, 2, L.gu, 2 * L.gu.rows, c.dim, 128))) { *msg = "gate/up weights"; return cudaErrorInvalidValue; }
-            PF_CK((gemm<128, kEpiSwiGLU>(c.st, mXh, *wm, og, nb, 2 * L.gu.rows, c.dim, c.err)), "gate/up GEMM");
+            PF_CK(run(Wide{}, ESwi{}, mXh, mw[4 * l + 2], L.gu, og, nb, 2 * L.gu.rows, c.dim), "gate/up GEMM");
             GemmOut od{nullptr, nullptr, X, nullptr};
-            if (!(wm = weights(l, 3, L.down, L.down.rows, c.ffn, 64))) { *msg = "down weights"; return cudaErrorInvalidValue; }
-            PF_CK((gemm<64, kEpiResidual>(c.st, mHh, *wm, od, nb, c.dim, c.ffn, c.err)), "down GEMM");
+            PF_CK(run(Narrow{}, EResid{}, mHh, mw[4 * l + 3], L.down, od, nb, c.dim, c.ffn), "down GEMM");
         }
         if (b0 + nb == n) {
             final_norm_kernel<<<1, 256, 0, c.st>>>(X + (size_t)(nb - 1) * c.dim, c.dim, c.out_norm, c.eps, ylast);
