@@ -6,17 +6,18 @@
 // The projections are tensor-core GEMMs on the 5th-generation tensor cores:
 // C[M][N] = A[M][K] . W[N][K]^T with A the token rows (F16, rounded to
 // nearest even from the F32 activations) and W a weight matrix in the
-// library's row layout (F16, K contiguous; a Q8_0 matrix is first expanded
-// to F16, d * qs rounded to nearest even), F32 accumulation in tensor
-// memory.  One CTA computes one 128 x BN tile (BN 64 for the narrow outputs,
-// 128 for the wide gate/up one; two CTAs per SM): thread 0 streams 128 x 64
-// tiles of A and BN x 64 tiles of W into a ring with 2-D TMA (128-byte
-// swizzle) and issues tcgen05.mma (M 128, N BN, K 16) into a TMEM accumulator; the four
-// warps then read their 32 rows back with tcgen05.ld and apply the epilogue
-// (bias, residual add, or SwiGLU over the interleaved gate/up columns).
+// library's row layout (F16, K contiguous; Q8_0 tiles are expanded to F16,
+// d * qs rounded to nearest even, in shared memory), F32 accumulation in
+// tensor memory.  The GEMM kernel is persistent and warp-specialised (one
+// CTA per SM; gemm_kernel below): a TMA producer warp, an MMA-issuing warp
+// with two TMEM accumulators, four epilogue warps (bias, residual add, or
+// SwiGLU over the interleaved gate/up columns, written through a
+// shared-memory transpose), and for Q8_0 four warps that expand the quants.
 //
-// The per-row steps (embedding, RMSNorm, RoPE + KV append, attention over the
-// cache, the last row's logits and argmax) are plain CUDA kernels.
+// Causal attention over the cache runs on mma.sync tensor-core tiles
+// (attention_mma_kernel); the per-row steps (embedding, RMSNorm, the batch's
+// RoPE table, RoPE + KV append, the last row's logits and argmax) are plain
+// CUDA kernels.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -50,8 +51,10 @@ __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t par, int* er
 // polling would otherwise take shared-memory bandwidth from the tensor cores.
 constexpr long long kSleepLimit = 4000000ll;    // suspended probes before a wait gives up (a few seconds)
 __device__ __forceinline__ bool sleep_parity(uint64_t* bar, uint32_t par, int* err) {
-    for (long long i = 0; i < kSleepLimit; i++)
+    for (long long i = 0; i < kSleepLimit; i++) {
         if (mbar_sleep_wait(bar, par)) return true;
+        if ((i & 63) == 63 && (*(volatile int*)err & kErrTimeout)) return false;   // another wait gave up
+    }
     atomicOr(err, kErrTimeout);
     return false;
 }
@@ -138,9 +141,9 @@ __device__ __forceinline__ void q4_to_f16(uint32_t w, __half2 d2, uint32_t& lo, 
 //   warps 6-9  (Q8_0) expand each stage's quants to F16 (d * q rounded to
 //              nearest even, as an F16 matrix of the weights would hold)
 //              into the stage's W tile.
-// Tile t (t = blockIdx.x, + gridDim.x, ...) is row block t % Mt, column block
-// t / Mt: CTAs working at the same time share W tiles.  Every wait is
-// bounded (kErrTimeout, then the role stops).
+// Tile t (t = blockIdx.x, + gridDim.x, ...) is row block t % Mt of column
+// block t / Mt, so CTAs working at the same time share W tiles through L2.
+// Every wait is bounded (kErrTimeout, then the role stops).
 template <int BN, int EPI, bool Q8>
 __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb, GemmScales ws,
@@ -158,7 +161,10 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
     uint64_t* fin = acce + 2;            // every MMA issued has completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int Mt = (M + kGBM - 1) / kGBM, Nt = (N + BN - 1) / BN, tiles = Mt * Nt, nk = K / kGBK;
+    const int Mt = (M + kGBM - 1) / kGBM, Nt = (N + BN - 1) / BN, nk = K / kGBK;
+    const int t_first = (int)blockIdx.x, t_step = (int)gridDim.x, t_count = Mt * Nt;
+    auto tile_m0 = [&](int t) { return (t % Mt) * kGBM; };
+    auto tile_n0 = [&](int t) { return (t / Mt) * BN; };
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; s++) {
             mbar_init(&full[s], 1);
@@ -187,8 +193,8 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
         if (lane == 0) {
             long long it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-                const int m0 = (t % Mt) * kGBM, n0 = (t / Mt) * BN;
+            for (int t = t_first; t < t_count && ok; t += t_step) {
+                const int m0 = tile_m0(t), n0 = tile_n0(t);
                 for (int kt = 0; kt < nk && ok; kt++, it++) {
                     const int s = (int)(it % S);
                     if (!(ok = wait_parity(&empty[s], (uint32_t)(((it / S) & 1) ^ 1), err))) break;
@@ -211,7 +217,7 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
             long long it = 0;
             bool ok = true;
             int j = 0;
-            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, j++) {
+            for (int t = t_first; t < t_count && ok; t += t_step, j++) {
                 const int b = j & 1;
                 if (!(ok = wait_parity(&acce[b], (uint32_t)(((j >> 1) & 1) ^ 1), err))) break;
                 asm volatile("tcgen05.fence::after_thread_sync;");
@@ -252,9 +258,9 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
         const int q = warp & 3;                                   // TMEM lanes 32q .. 32q+31
         float* tb = trans + (warp - 2) * 32 * 33;
         int j = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x, j++) {
+        for (int t = t_first; t < t_count; t += t_step, j++) {
             const int b = j & 1;
-            const int m0 = (t % Mt) * kGBM, n0 = (t / Mt) * BN;
+            const int m0 = tile_m0(t), n0 = tile_n0(t);
             if (!sleep_parity(&accf[b], (uint32_t)((j >> 1) & 1), err)) break;
             asm volatile("tcgen05.fence::after_thread_sync;");
             const int rbase = m0 + q * 32;
@@ -304,19 +310,22 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
                         if (row < M && col < N) o.out[(size_t)row * N + col] = tb[r * 33 + lane] + bias;
                     }
                 } else {
-                    // the 32 residual values are all loaded before any is stored
-                    // (one memory latency per block, not one per row)
+                    // 16 residual values are loaded before any is stored (one
+                    // memory latency per 16 rows, not one per row)
                     const int col = n0 + c0 + lane;
-                    float old[32];
+#pragma unroll 1
+                    for (int h = 0; h < 32; h += 16) {
+                        float old[16];
 #pragma unroll
-                    for (int r = 0; r < 32; r++) {
-                        const int row = rbase + r;
-                        old[r] = row < M && col < N ? __ldcg(o.resid + (size_t)row * N + col) : 0.f;
-                    }
+                        for (int r = 0; r < 16; r++) {
+                            const int row = rbase + h + r;
+                            old[r] = row < M && col < N ? __ldcg(o.resid + (size_t)row * N + col) : 0.f;
+                        }
 #pragma unroll
-                    for (int r = 0; r < 32; r++) {
-                        const int row = rbase + r;
-                        if (row < M && col < N) o.resid[(size_t)row * N + col] = old[r] + tb[r * 33 + lane];
+                        for (int r = 0; r < 16; r++) {
+                            const int row = rbase + h + r;
+                            if (row < M && col < N) o.resid[(size_t)row * N + col] = old[r] + tb[(h + r) * 33 + lane];
+                        }
                     }
                 }
                 __syncwarp();
@@ -336,8 +345,8 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
         constexpr int kRows = BN > 128 ? BN / 128 : 1;
         long long it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-            const int n0 = (t / Mt) * BN;
+        for (int t = t_first; t < t_count && ok; t += t_step) {
+            const int n0 = tile_n0(t);
             const uint32_t* drow[kRows];
 #pragma unroll
             for (int j = 0; j < kRows; j++) {
@@ -406,52 +415,69 @@ __global__ void embed_rows_kernel(const int* tok, int n, DMat embd, int wtype, i
 // A Q8_0 matrix (library layout) expanded to F16 for the tensor-core GEMMs:
 // RMSNorm of every row ("The Forward Pass in Java", Example 4: y = (x*scale)*g,
 // scale = 1/sqrt(mean(x^2) + eps)); the GEMM operand is y rounded to F16.
+// One warp per row, 8 values per 16-byte step (dim % 8 == 0).
 __global__ void rmsnorm_rows_f16_kernel(const float* X, int n, int dim, const float* g, float eps, __half* Y) {
-    const int i = blockIdx.x;
+    const int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (i >= n) return;
-    const float* x = X + (size_t)i * dim;
+    const float4* x4 = reinterpret_cast<const float4*>(X + (size_t)i * dim);
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    const int n8 = dim / 8;
     float ss = 0.f;
-    for (int d = threadIdx.x; d < dim; d += blockDim.x) ss += x[d] * x[d];
-    __shared__ float red[32];
+    for (int k = lane; k < n8; k += 32) {
+        const float4 a = x4[2 * k], b = x4[2 * k + 1];
+        ss += (a.x * a.x + a.y * a.y) + (a.z * a.z + a.w * a.w) + ((b.x * b.x + b.y * b.y) + (b.z * b.z + b.w * b.w));
+    }
     ss = warp_sum(ss);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-    __syncthreads();
-    float tot = 0.f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += red[w];
-    const float scale = 1.0f / sqrtf(tot / (float)dim + eps);
-    for (int d = threadIdx.x; d < dim; d += blockDim.x)
-        Y[(size_t)i * dim + d] = __float2half_rn(__fmul_rn(__fmul_rn(x[d], scale), g[d]));
+    const float scale = 1.0f / sqrtf(ss / (float)dim + eps);
+    uint4* y4 = reinterpret_cast<uint4*>(Y + (size_t)i * dim);
+    for (int k = lane; k < n8; k += 32) {
+        const float4 a = x4[2 * k], b = x4[2 * k + 1], ga = g4[2 * k], gb = g4[2 * k + 1];
+        auto y = [&](float x, float gg) { return __float2half_rn(__fmul_rn(__fmul_rn(x, scale), gg)); };
+        const __half2 h0 = __halves2half2(y(a.x, ga.x), y(a.y, ga.y)), h1 = __halves2half2(y(a.z, ga.z), y(a.w, ga.w));
+        const __half2 h2 = __halves2half2(y(b.x, gb.x), y(b.y, gb.y)), h3 = __halves2half2(y(b.z, gb.z), y(b.w, gb.w));
+        y4[k] = make_uint4(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1),
+                           *reinterpret_cast<const uint32_t*>(&h2), *reinterpret_cast<const uint32_t*>(&h3));
+    }
 }
 
-// RoPE of q and k of row i at position pos0+i with the decode step's float
-// angle chain ("The Forward Pass in Java", Example 6; frequency factors per
-// "What a Llama model computes, and why" §2.4), then the F16 K and V rows of
-// that position ("The Forward Pass in Java", Examples 7 and 10).
+// cos and sin of every (row, pair) of the batch, tab[(i * half + j) * 2 + {0,
+// 1}]: the decode step's float angle chain ("The Forward Pass in Java",
+// Example 6: theta starts at the position and is multiplied by theta_scale
+// once per pair; frequency factors per "What a Llama model computes, and
+// why" §2.4), cos/sin taken in double.  The angles depend only on the
+// position, so one table serves every layer of the batch.
+__global__ void rope_table_kernel(float* tab, int n, int pos0, int half, float theta_scale, const float* freqs) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= n * half) return;
+    const int i = e / half, j = e % half;
+    float th = (float)(pos0 + i);
+    for (int k = 0; k < j; k++) th = __fmul_rn(th, theta_scale);
+    if (freqs) th = __fdiv_rn(th, freqs[j]);
+    double sv, cv;
+    sincos((double)th, &sv, &cv);
+    tab[2 * e] = (float)cv;
+    tab[2 * e + 1] = (float)sv;
+}
+
+// RoPE of q and k of row i at position pos0+i with the batch's angle table,
+// then the F16 K and V rows of that position ("The Forward Pass in Java",
+// Examples 7 and 10).
 __global__ void rope_kv_rows_kernel(float* QKV, int n, int pos0, int n_heads, int n_kv, int hd, int rope_dims, int neox,
-                                    float theta_scale, const float* freqs, __half* kc, __half* vc) {
+                                    const float* tab, __half* kc, __half* vc) {
     const int i = blockIdx.x;
     if (i >= n) return;
     const int pos = pos0 + i;
     const int q_dim = n_heads * hd, kv_dim = n_kv * hd, half = rope_dims / 2;
     float* row = QKV + (size_t)i * (q_dim + 2 * kv_dim);
-    __shared__ float cs[128], sn[128];
-    for (int j = threadIdx.x; j < half; j += blockDim.x) {
-        float th = (float)pos;
-        for (int k = 0; k < j; k++) th = __fmul_rn(th, theta_scale);
-        if (freqs) th = __fdiv_rn(th, freqs[j]);
-        double s, c;
-        sincos((double)th, &s, &c);
-        cs[j] = (float)c;
-        sn[j] = (float)s;
-    }
-    __syncthreads();
+    const float2* cs = reinterpret_cast<const float2*>(tab) + (size_t)i * half;
     for (int t = threadIdx.x; t < (n_heads + n_kv) * half; t += blockDim.x) {
         const int head = t / half, j = t % half;
         float* v = head < n_heads ? row + head * hd : row + q_dim + (head - n_heads) * hd;
         const int a = neox ? j : 2 * j, b = neox ? j + half : 2 * j + 1;
+        const float2 r = cs[j];
         const float x0 = v[a], x1 = v[b];
-        v[a] = __fsub_rn(__fmul_rn(x0, cs[j]), __fmul_rn(x1, sn[j]));
-        v[b] = __fadd_rn(__fmul_rn(x0, sn[j]), __fmul_rn(x1, cs[j]));
+        v[a] = __fsub_rn(__fmul_rn(x0, r.x), __fmul_rn(x1, r.y));
+        v[b] = __fadd_rn(__fmul_rn(x0, r.y), __fmul_rn(x1, r.x));
     }
     __syncthreads();
     for (int e = threadIdx.x; e < kv_dim; e += blockDim.x) {
@@ -637,8 +663,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // (running max and sum per row, rescaled accumulators) runs on the
 // accumulator fragments; K and V arrive in 64-position tiles, double
 // buffered with cp.async, in rows padded to HD + 8 halves so that ldmatrix
-// reads them without bank conflicts.  The output row is divided by its sum
-// and rounded to F16 (the O projection's operand).
+// reads them without bank conflicts.  Each head has `split` warps: warp
+// (head, sp) takes the 16-position sub-tiles whose index is sp modulo split,
+// and at the end warp sp = 0 folds the others' (max, sum, accumulators) into
+// its own in the order sp = 1, 2, ... (the same bits in every run).  The
+// output row is divided by its sum and rounded to F16 (the O projection's
+// operand).
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
@@ -654,17 +684,19 @@ __device__ __forceinline__ uint32_t h2_bits(__half a, __half b) {
 constexpr int kAttnKT = 64;                      // cache positions per K/V tile
 
 template <int HD>
-__global__ void __launch_bounds__(256) attention_mma_kernel(const float* QKV, int n, int pos0, int n_heads, int n_kv,
+__global__ void __launch_bounds__(HD == 128 ? 256 : 512) attention_mma_kernel(const float* QKV, int n, int pos0,
+                                                                              int n_heads, int n_kv,
                                                             float attn_div, const __half* kc, const __half* vc,
-                                                            __half* A) {
+                                                            __half* A, int split) {
     constexpr int PITCH = HD + 8;                // halves per shared-memory row
-    extern __shared__ __align__(16) __half kvs[];   // [2 buffers][K, V][kAttnKT][PITCH]
+    extern __shared__ __align__(16) __half kvs[];   // [2 buffers][K, V][kAttnKT][PITCH]; then the warps' partials
     const int gq = n_heads / n_kv, q_dim = n_heads * HD, kv_dim = n_kv * HD, row_w = q_dim + 2 * kv_dim;
     const int ntile = (n + 15) / 16;
     const int qt = ntile - 1 - (int)blockIdx.x;  // the longest rows first
     const int g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = g * gq + warp;
+    const int hq = warp % gq, sp = warp / gq;
+    const int h = g * gq + hq;
     const int t0 = qt * 16;
     const int r = lane >> 2, t = lane & 3;
     const int n_pos = pos0 + min(t0 + 16, n);    // positions the tile's last row attends to
@@ -716,6 +748,7 @@ __global__ void __launch_bounds__(256) attention_mma_kernel(const float* QKV, in
         for (int sub = 0; sub < kAttnKT / 16; sub++) {
             const int p0 = c * kAttnKT + sub * 16;
             if (p0 >= n_pos) break;
+            if ((c * (kAttnKT / 16) + sub) % split != sp) continue;
             // scores of positions p0 + 8 nt + 2t + {0, 1}, rows r and r + 8
             float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             {
@@ -798,6 +831,42 @@ __global__ void __launch_bounds__(256) attention_mma_kernel(const float* QKV, in
         }
         __syncthreads();                         // the buffer is reloaded two tiles later
     }
+    // fold the head's other warps into warp sp = 0, in the order sp = 1, 2, ...
+    if (split > 1) {
+        constexpr int NV = HD / 2 + 4;           // a lane's accumulators, then m0, m1, l0, l1
+        float* part = reinterpret_cast<float*>(kvs);   // the K/V tiles are no longer read
+        if (sp > 0) {
+            float* pw = part + (size_t)((sp - 1) * gq + hq) * NV * 32 + lane;
+#pragma unroll
+            for (int nt = 0; nt < HD / 8; nt++)
+#pragma unroll
+                for (int k = 0; k < 4; k++) pw[(nt * 4 + k) * 32] = o[nt][k];
+            pw[(HD / 2) * 32] = m0;
+            pw[(HD / 2 + 1) * 32] = m1;
+            pw[(HD / 2 + 2) * 32] = l0;
+            pw[(HD / 2 + 3) * 32] = l1;
+        }
+        __syncthreads();
+        if (sp > 0) return;
+        for (int k2 = 1; k2 < split; k2++) {
+            const float* pw = part + (size_t)((k2 - 1) * gq + hq) * NV * 32 + lane;
+            const float om0 = pw[(HD / 2) * 32], om1 = pw[(HD / 2 + 1) * 32];
+            const float M0 = fmaxf(m0, om0), M1 = fmaxf(m1, om1);
+            const float a0 = m0 == -INFINITY ? 0.f : expf(m0 - M0), b0 = om0 == -INFINITY ? 0.f : expf(om0 - M0);
+            const float a1 = m1 == -INFINITY ? 0.f : expf(m1 - M1), b1 = om1 == -INFINITY ? 0.f : expf(om1 - M1);
+            l0 = l0 * a0 + pw[(HD / 2 + 2) * 32] * b0;
+            l1 = l1 * a1 + pw[(HD / 2 + 3) * 32] * b1;
+            m0 = M0;
+            m1 = M1;
+#pragma unroll
+            for (int nt = 0; nt < HD / 8; nt++) {
+                o[nt][0] = o[nt][0] * a0 + pw[(nt * 4 + 0) * 32] * b0;
+                o[nt][1] = o[nt][1] * a0 + pw[(nt * 4 + 1) * 32] * b0;
+                o[nt][2] = o[nt][2] * a1 + pw[(nt * 4 + 2) * 32] * b1;
+                o[nt][3] = o[nt][3] * a1 + pw[(nt * 4 + 3) * 32] * b1;
+            }
+        }
+    }
     const float i0 = 1.0f / l0, i1 = 1.0f / l1;
     const int row0 = t0 + r, row1 = t0 + r + 8;
 #pragma unroll
@@ -818,8 +887,13 @@ bool attention_mma_launch(cudaStream_t st, const float* QKV, int n, int pos0, in
                           float attn_div, const __half* kc, const __half* vc, __half* A, cudaError_t* e) {
     const int gq = n_heads / n_kv;
     if (gq > 8 || !(hd == 32 || hd == 64 || hd == 128)) return false;
-    const dim3 grid((n + 15) / 16, n_kv), block(32 * gq);
-    const size_t smem = (size_t)2 * 2 * kAttnKT * (hd + 8) * sizeof(__half);
+    // warps per head: up to 4, at most 16 warps a block (8 for head_dim 128,
+    // whose accumulators need twice the registers)
+    const int split = std::max(1, std::min(4, (hd == 128 ? 8 : 16) / gq));
+    const dim3 grid((n + 15) / 16, n_kv), block(32 * gq * split);
+    const size_t kv_bytes = (size_t)2 * 2 * kAttnKT * (hd + 8) * sizeof(__half);
+    const size_t part_bytes = (size_t)(split - 1) * gq * (hd / 2 + 4) * 32 * sizeof(float);
+    const size_t smem = std::max(kv_bytes, part_bytes);
     const void* fn = hd == 32 ? (const void*)attention_mma_kernel<32>
                      : hd == 64 ? (const void*)attention_mma_kernel<64>
                                 : (const void*)attention_mma_kernel<128>;
@@ -827,9 +901,12 @@ bool attention_mma_launch(cudaStream_t st, const float* QKV, int n, int pos0, in
         *e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (*e != cudaSuccess) return true;
     }
-    if (hd == 32) attention_mma_kernel<32><<<grid, block, smem, st>>>(QKV, n, pos0, n_heads, n_kv, attn_div, kc, vc, A);
-    else if (hd == 64) attention_mma_kernel<64><<<grid, block, smem, st>>>(QKV, n, pos0, n_heads, n_kv, attn_div, kc, vc, A);
-    else attention_mma_kernel<128><<<grid, block, smem, st>>>(QKV, n, pos0, n_heads, n_kv, attn_div, kc, vc, A);
+    if (hd == 32)
+        attention_mma_kernel<32><<<grid, block, smem, st>>>(QKV, n, pos0, n_heads, n_kv, attn_div, kc, vc, A, split);
+    else if (hd == 64)
+        attention_mma_kernel<64><<<grid, block, smem, st>>>(QKV, n, pos0, n_heads, n_kv, attn_div, kc, vc, A, split);
+    else
+        attention_mma_kernel<128><<<grid, block, smem, st>>>(QKV, n, pos0, n_heads, n_kv, attn_div, kc, vc, A, split);
     *e = cudaGetLastError();
     return true;
 }
@@ -889,7 +966,7 @@ size_t prefill_workspace_bytes(const PrefillCtx& c) {
     const size_t M = kPrefillRows;
     auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
     return al(M * 4) + al(M * c.dim * 4) + al(M * c.dim * 2) + al(M * (c.q_dim + 2 * c.kv_dim) * 4) +
-           al(M * c.q_dim * 2) + al(M * c.ffn * 2) + al((size_t)c.dim * 4);
+           al(M * c.q_dim * 2) + al(M * c.ffn * 2) + al((size_t)c.dim * 4) + al(M * (c.rope_dims / 2) * 8);
 }
 
 // Runs the batch; `ws` holds prefill_workspace_bytes(c).  Returns a CUDA error
@@ -905,6 +982,7 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
     __half* Ah = reinterpret_cast<__half*>(w); w += al(M * c.q_dim * 2);
     __half* Hh = reinterpret_cast<__half*>(w); w += al(M * c.ffn * 2);
     float* ylast = reinterpret_cast<float*>(w); w += al((size_t)c.dim * 4);
+    float* rtab = reinterpret_cast<float*>(w); w += al(M * (c.rope_dims / 2) * 8);   // the batch's cos/sin table
     cudaError_t e;
 #define PF_CK(call, what)                 \
     do {                                  \
@@ -961,14 +1039,21 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
         PF_CK(cudaMemcpyAsync(tok, tokens_host + b0, (size_t)nb * 4, cudaMemcpyHostToDevice, c.st), "token upload");
         embed_rows_kernel<<<nb, 256, 0, c.st>>>(tok, nb, c.embd, c.wtype, c.dim, X);
         PF_CK(cudaGetLastError(), "embedding");
+        {
+            const int cells = nb * (c.rope_dims / 2);
+            rope_table_kernel<<<(cells + 255) / 256, 256, 0, c.st>>>(rtab, nb, p0, c.rope_dims / 2, c.theta_scale,
+                                                                     c.rope_freqs);
+            PF_CK(cudaGetLastError(), "RoPE table");
+        }
+        const int norm_blocks = (nb + 7) / 8;
         for (int l = 0; l < c.n_layers; l++) {
             const LayerDev& L = c.layers[l];
-            rmsnorm_rows_f16_kernel<<<nb, 256, 0, c.st>>>(X, nb, c.dim, L.attn_norm, c.eps, Xh);
+            rmsnorm_rows_f16_kernel<<<norm_blocks, 256, 0, c.st>>>(X, nb, c.dim, L.attn_norm, c.eps, Xh);
             PF_CK(cudaGetLastError(), "attention RMSNorm");
             GemmOut oq{QKV, L.qkv_bias, nullptr, nullptr};
             PF_CK(run(Qkv{}, EBias{}, mXh, mw[4 * l + 0], L.qkv, oq, nb, L.qkv.rows, c.dim), "QKV GEMM");
-            rope_kv_rows_kernel<<<nb, 128, 0, c.st>>>(QKV, nb, p0, c.n_heads, c.n_kv, c.hd, c.rope_dims, c.neox,
-                                                      c.theta_scale, c.rope_freqs, L.kc, L.vc);
+            rope_kv_rows_kernel<<<nb, 128, 0, c.st>>>(QKV, nb, p0, c.n_heads, c.n_kv, c.hd, c.rope_dims, c.neox, rtab,
+                                                      L.kc, L.vc);
             PF_CK(cudaGetLastError(), "RoPE and KV append");
             {
                 cudaError_t ea = cudaSuccess;
@@ -981,7 +1066,7 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
             }
             GemmOut oo{nullptr, nullptr, X, nullptr};
             PF_CK(run(Narrow{}, EResid{}, mAh, mw[4 * l + 1], L.o, oo, nb, c.dim, c.q_dim), "O GEMM");
-            rmsnorm_rows_f16_kernel<<<nb, 256, 0, c.st>>>(X, nb, c.dim, L.ffn_norm, c.eps, Xh);
+            rmsnorm_rows_f16_kernel<<<norm_blocks, 256, 0, c.st>>>(X, nb, c.dim, L.ffn_norm, c.eps, Xh);
             PF_CK(cudaGetLastError(), "FFN RMSNorm");
             GemmOut og{nullptr, nullptr, nullptr, Hh};
             PF_CK(run(Wide{}, ESwi{}, mXh, mw[4 * l + 2], L.gu, og, nb, 2 * L.gu.rows, c.dim), "gate/up GEMM");
