@@ -97,7 +97,7 @@ struct GemmPlan {
     static constexpr int kStageBytes = kGABytes + kBBytes + kQBytes;
     static constexpr int kStages = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
     static constexpr int kEpiWarps = 4;
-    static constexpr int kConvWarps = Q8 ? 4 : 0;
+    static constexpr int kConvWarps = Q8 ? 8 : 0;
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kConvWarps);
     static constexpr int kTransBytes = kEpiWarps * 32 * 33 * 4;
     static constexpr int kBarBytes = 8 * (3 * kStages + 4 + 1) + 16;
@@ -336,13 +336,15 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
         }
     } else if constexpr (Q8) {
         // ---- Q8_0 expansion: the W tile's BN rows x 4 pairs of 16-byte
-        // output chunks are items i = c + 128 k of the 128 converter threads
+        // output chunks are items i = c + kCT k of the kCT converter threads
         // (row i % BN, pair i / BN): 16 quants in, 16 F16 values out.  A
-        // thread's items lie in kRows rows (c + 128 j); each row's two block
+        // thread's items lie in kRows rows (c + kCT j); each row's two block
         // scales of a k-step are one 4-byte word, loaded a k-step ahead.
+        constexpr int kCT = 32 * G::kConvWarps;
         const int c = threadIdx.x - 32 * (2 + G::kEpiWarps);
-        constexpr int kItems = BN * 4 / 128;
-        constexpr int kRows = BN > 128 ? BN / 128 : 1;
+        constexpr int kItems = BN * 4 / kCT;
+        constexpr int kRows = kCT >= BN ? 1 : BN / kCT;
+        static_assert(kItems >= 1 && (BN * 4) % kCT == 0, "converter items");
         long long it = 0;
         bool ok = true;
         for (int t = t_first; t < t_count && ok; t += t_step) {
@@ -350,7 +352,7 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
             const uint32_t* drow[kRows];
 #pragma unroll
             for (int j = 0; j < kRows; j++) {
-                const int wrow = n0 + (c + 128 * j) % BN;
+                const int wrow = n0 + (c + kCT * j) % BN;
                 drow[j] = wrow < N ? reinterpret_cast<const uint32_t*>(ws.d + (size_t)wrow * ws.dstride) : nullptr;
             }
             uint32_t dnext[kRows];
@@ -370,8 +372,8 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
                 const uint8_t* qtile = st + kGABytes + G::kBBytes;
 #pragma unroll
                 for (int k = 0; k < kItems; k++) {
-                    const int i = c + 128 * k, r = i % BN, pair = i / BN;
-                    const uint32_t dw = dcur[BN > 128 ? k % kRows : 0];
+                    const int i = c + kCT * k, r = i % BN, pair = i / BN;
+                    const uint32_t dw = dcur[k % kRows];
                     const __half d = __ushort_as_half((unsigned short)(pair < 2 ? dw & 0xFFFFu : dw >> 16));
                     const __half2 d2 = __half2half2(d);
                     const uint4 qv = *reinterpret_cast<const uint4*>(qtile + r * kGBK + pair * 16);
