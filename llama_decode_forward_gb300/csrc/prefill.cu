@@ -34,8 +34,12 @@ namespace {
 
 constexpr int kGBM = 128, kGBK = 64;
 constexpr int kGABytes = kGBM * kGBK * 2;
-// GEMM tile widths: the Q/K/V output, the dim-wide outputs (O, down: 64 wide
-// so that a 512-token batch still has 128 tiles), the gate/up output
+// GEMM tile widths (multiples of 16, the MMA's N step), measured on a
+// 512-token batch of the 1B shape: Q/K/V (3072 rows: 96 tiles of 128; 96-wide
+// tiles were 7 % faster with F16 weights but slower with Q8_0, whose
+// expansion then has half the converter warps), the dim-wide outputs O and
+// down (2048: 128 tiles of 64), gate/up (16384: 256 tiles of 256; 296 tiles
+// of 224 were slower)
 constexpr int kBnQkv = 128, kBnNarrow = 64, kBnWide = 256;
 constexpr long long kSpinLimit = 200000000ll;   // mbarrier polls before a wait gives up
 
@@ -97,7 +101,12 @@ struct GemmPlan {
     static constexpr int kStageBytes = kGABytes + kBBytes + kQBytes;
     static constexpr int kStages = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
     static constexpr int kEpiWarps = 4;
-    static constexpr int kConvWarps = Q8 ? 8 : 0;
+    // Q8_0 converter warps: 8, or 4 when the tile's BN x 4 work items do not
+    // split evenly over 256 threads
+    static constexpr int kConvWarps = !Q8 ? 0 : (BN * 4) % 256 == 0 ? 8 : 4;
+    // TMEM columns of the two accumulators (a power of two of at least 32)
+    static constexpr int kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
+                                     : 2 * BN <= 256 ? 256 : 512;
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kConvWarps);
     static constexpr int kTransBytes = kEpiWarps * 32 * 33 * 4;
     static constexpr int kBarBytes = 8 * (3 * kStages + 4 + 1) + 16;
@@ -180,7 +189,7 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
-                     "r"(2 * BN));
+                     "r"(G::kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
@@ -337,13 +346,16 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
     } else if constexpr (Q8) {
         // ---- Q8_0 expansion: the W tile's BN rows x 4 pairs of 16-byte
         // output chunks are items i = c + kCT k of the kCT converter threads
-        // (row i % BN, pair i / BN): 16 quants in, 16 F16 values out.  A
-        // thread's items lie in kRows rows (c + kCT j); each row's two block
-        // scales of a k-step are one 4-byte word, loaded a k-step ahead.
+        // (row i % BN, pair i / BN): 16 quants in, 16 F16 values out.  Each
+        // item's row has its two block scales of a k-step in one 4-byte
+        // word, loaded a k-step ahead.
         constexpr int kCT = 32 * G::kConvWarps;
         const int c = threadIdx.x - 32 * (2 + G::kEpiWarps);
         constexpr int kItems = BN * 4 / kCT;
-        constexpr int kRows = kCT >= BN ? 1 : BN / kCT;
+        // one scale word per distinct row: all items of a thread share row
+        // c % BN when kCT is a multiple of BN, else each item has its own
+        constexpr bool kSameRow = kCT % BN == 0;
+        constexpr int kRows = kSameRow ? 1 : kItems;
         static_assert(kItems >= 1 && (BN * 4) % kCT == 0, "converter items");
         long long it = 0;
         bool ok = true;
@@ -352,7 +364,7 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
             const uint32_t* drow[kRows];
 #pragma unroll
             for (int j = 0; j < kRows; j++) {
-                const int wrow = n0 + (c + kCT * j) % BN;
+                const int wrow = n0 + (c + kCT * j) % BN;           // item j's row
                 drow[j] = wrow < N ? reinterpret_cast<const uint32_t*>(ws.d + (size_t)wrow * ws.dstride) : nullptr;
             }
             uint32_t dnext[kRows];
@@ -373,7 +385,7 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < kItems; k++) {
                     const int i = c + kCT * k, r = i % BN, pair = i / BN;
-                    const uint32_t dw = dcur[k % kRows];
+                    const uint32_t dw = dcur[kSameRow ? 0 : k];
                     const __half d = __ushort_as_half((unsigned short)(pair < 2 ? dw & 0xFFFFu : dw >> 16));
                     const __half2 d2 = __half2half2(d);
                     const uint4 qv = *reinterpret_cast<const uint4*>(qtile + r * kGBK + pair * 16);
@@ -395,7 +407,8 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
-    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BN));
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(G::kTmemCols));
 }
 
 // Embedding rows of the batch: F16 widened, or Q8_0 decoded as d * qs (both
