@@ -438,6 +438,9 @@ __global__ void rmsnorm_rows_f16_kernel(const float* X, int n, int dim, const fl
     const float4* g4 = reinterpret_cast<const float4*>(g);
     const int n8 = dim / 8;
     float ss = 0.f;
+    // unrolled so that a lane's loads are in flight together (one memory
+    // latency per eight groups, not one per group)
+#pragma unroll 8
     for (int k = lane; k < n8; k += 32) {
         const float4 a = x4[2 * k], b = x4[2 * k + 1];
         ss += (a.x * a.x + a.y * a.y) + (a.z * a.z + a.w * a.w) + ((b.x * b.x + b.y * b.y) + (b.z * b.z + b.w * b.w));
@@ -445,6 +448,7 @@ __global__ void rmsnorm_rows_f16_kernel(const float* X, int n, int dim, const fl
     ss = warp_sum(ss);
     const float scale = 1.0f / sqrtf(ss / (float)dim + eps);
     uint4* y4 = reinterpret_cast<uint4*>(Y + (size_t)i * dim);
+#pragma unroll 8
     for (int k = lane; k < n8; k += 32) {
         const float4 a = x4[2 * k], b = x4[2 * k + 1], ga = g4[2 * k], gb = g4[2 * k + 1];
         auto y = [&](float x, float gg) { return __float2half_rn(__fmul_rn(__fmul_rn(x, scale), gg)); };
@@ -485,6 +489,7 @@ __global__ void rope_kv_rows_kernel(float* QKV, int n, int pos0, int n_heads, in
     const int q_dim = n_heads * hd, kv_dim = n_kv * hd, half = rope_dims / 2;
     float* row = QKV + (size_t)i * (q_dim + 2 * kv_dim);
     const float2* cs = reinterpret_cast<const float2*>(tab) + (size_t)i * half;
+#pragma unroll 4
     for (int t = threadIdx.x; t < (n_heads + n_kv) * half; t += blockDim.x) {
         const int head = t / half, j = t % half;
         float* v = head < n_heads ? row + head * hd : row + q_dim + (head - n_heads) * hd;
@@ -495,6 +500,7 @@ __global__ void rope_kv_rows_kernel(float* QKV, int n, int pos0, int n_heads, in
         v[b] = __fadd_rn(__fmul_rn(x0, r.y), __fmul_rn(x1, r.x));
     }
     __syncthreads();
+#pragma unroll 4
     for (int e = threadIdx.x; e < kv_dim; e += blockDim.x) {
         kc[(size_t)pos * kv_dim + e] = __float2half_rn(row[q_dim + e]);
         vc[(size_t)pos * kv_dim + e] = __float2half_rn(row[q_dim + kv_dim + e]);
@@ -684,8 +690,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // its own in the order sp = 1, 2, ... (the same bits in every run).  The
 // output row is divided by its sum and rounded to F16 (the O projection's
 // operand).
+// (not volatile: a pure function of its operands, so the compiler may
+// interleave independent accumulation chains)
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -696,7 +704,7 @@ __device__ __forceinline__ uint32_t h2_bits(__half a, __half b) {
     return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
 }
 
-constexpr int kAttnKT = 64;                      // cache positions per K/V tile
+constexpr int kAttnKT = 128;                     // cache positions per K/V tile
 
 template <int HD>
 __global__ void __launch_bounds__(HD == 128 ? 256 : 512) attention_mma_kernel(const float* QKV, int n, int pos0,
@@ -735,6 +743,11 @@ __global__ void __launch_bounds__(HD == 128 ? 256 : 512) attention_mma_kernel(co
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
     const int ntiles = (n_pos + kAttnKT - 1) / kAttnKT;
+    // score / sqrt(head_dim): a power-of-two divisor (head_dim 64, 256, ...)
+    // divides exactly as a multiply by its reciprocal (the same bits)
+    const bool div_pow2 = (__float_as_uint(attn_div) & 0x007FFFFFu) == 0u;
+    const float inv_div = __frcp_rn(attn_div);
+    auto scale_score = [&](float x) { return div_pow2 ? __fmul_rn(x, inv_div) : __fdiv_rn(x, attn_div); };
     auto load_tile = [&](int c, int buf) {
         __half* ks_ = kvs + (size_t)(buf * 2) * kAttnKT * PITCH;
         __half* vs_ = ks_ + kAttnKT * PITCH;
@@ -760,10 +773,11 @@ __global__ void __launch_bounds__(HD == 128 ? 256 : 512) attention_mma_kernel(co
         const __half* ks_ = kvs + (size_t)((c & 1) * 2) * kAttnKT * PITCH;
         const __half* vs_ = ks_ + kAttnKT * PITCH;
         const uint32_t kbase = smem_addr(ks_), vbase = smem_addr(vs_);
-        for (int sub = 0; sub < kAttnKT / 16; sub++) {
+        // this warp's sub-tiles of the tile: global index = sp modulo split
+        const int sub0 = ((sp - c * (kAttnKT / 16)) % split + split) % split;
+        for (int sub = sub0; sub < kAttnKT / 16; sub += split) {
             const int p0 = c * kAttnKT + sub * 16;
             if (p0 >= n_pos) break;
-            if ((c * (kAttnKT / 16) + sub) % split != sp) continue;
             // scores of positions p0 + 8 nt + 2t + {0, 1}, rows r and r + 8
             float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             {
@@ -774,8 +788,8 @@ __global__ void __launch_bounds__(HD == 128 ? 256 : 512) attention_mma_kernel(co
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(krow + (uint32_t)((ks * 16 + (mi & 1) * 8) * 2), b0, b1, b2, b3);
                     mma16816(s[0], qhi[ks], b0, b1);
-                    mma16816(s[0], qlo[ks], b0, b1);
                     mma16816(s[1], qhi[ks], b2, b3);
+                    mma16816(s[0], qlo[ks], b0, b1);
                     mma16816(s[1], qlo[ks], b2, b3);
                 }
             }
@@ -785,8 +799,8 @@ __global__ void __launch_bounds__(HD == 128 ? 256 : 512) attention_mma_kernel(co
 #pragma unroll
                 for (int k = 0; k < 2; k++) {
                     const int P = p0 + nt * 8 + 2 * t + k;
-                    s[nt][k] = P <= pos0 + R0 ? __fdiv_rn(s[nt][k], attn_div) : -INFINITY;
-                    s[nt][2 + k] = P <= pos0 + R1 ? __fdiv_rn(s[nt][2 + k], attn_div) : -INFINITY;
+                    s[nt][k] = P <= pos0 + R0 ? scale_score(s[nt][k]) : -INFINITY;
+                    s[nt][2 + k] = P <= pos0 + R1 ? scale_score(s[nt][2 + k]) : -INFINITY;
                     mt0 = fmaxf(mt0, s[nt][k]);
                     mt1 = fmaxf(mt1, s[nt][2 + k]);
                 }
@@ -838,8 +852,8 @@ __global__ void __launch_bounds__(HD == 128 ? 256 : 512) attention_mma_kernel(co
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4_t(vrow + (uint32_t)(((nt + (mi >> 1)) * 8) * 2), b0, b1, b2, b3);
                     mma16816(o[nt], phi, b0, b1);
-                    mma16816(o[nt], plo, b0, b1);
                     mma16816(o[nt + 1], phi, b2, b3);
+                    mma16816(o[nt], plo, b0, b1);
                     mma16816(o[nt + 1], plo, b2, b3);
                 }
             }
