@@ -1229,6 +1229,14 @@ __device__ __forceinline__ void store_kv_checked(const StepParams& p, __half* kc
         store_kv(kc, vc, p.pos, p.kv_dim, g * p.hd, i, k, v);
 }
 
+// score / sqrt(head_dim) ("The Forward Pass in Java", Example 11): a
+// power-of-two divisor (head_dim 64, 256, ...) divides exactly as a multiply
+// by its reciprocal, the same bits as the IEEE division at a fraction of the
+// instructions.
+__device__ __forceinline__ float attn_scale(float x, float div) {
+    return (__float_as_uint(div) & 0x007FFFFFu) == 0u ? __fmul_rn(x, __frcp_rn(div)) : __fdiv_rn(x, div);
+}
+
 // ------------------------------------------------------------- attention --
 // One unit = the positions [t0, t1) of kv head g, for its gq query heads
 // ("The Forward Pass in Java", Example 11: scores q.k / sqrt(hd), softmax over
@@ -1396,7 +1404,7 @@ __device__ bool attention_unit(Consumer& c, const LayerDev& L, int layer, int un
                     j = j + 1 == nh2 ? 0 : j + 1;
                 }
                 const float2 a = make_float2((a0.x + a1.x) + (a2.x + a3.x), (a0.y + a1.y) + (a2.y + a3.y));
-                scb[h * P + pp] = __fdiv_rn(a.x + a.y, p.attn_div);
+                scb[h * P + pp] = attn_scale(a.x + a.y, p.attn_div);
             }
             consumer_sync();
             if (c.aborted()) return false;
@@ -1584,7 +1592,7 @@ __device__ bool attention_unit_mma(Consumer& c, const LayerDev& L, int layer, in
                 for (int k = 0; k < 2; k++) {
                     const float v = sc[ns][k] + __shfl_xor_sync(0xffffffffu, sc[ns][k], 4);   // hi + lo
                     const int pos = pj + 8 * ns + 2 * t + k;
-                    e[ns][k] = pos < np ? __fdiv_rn(v, p.attn_div) : -INFINITY;
+                    e[ns][k] = pos < np ? attn_scale(v, p.attn_div) : -INFINITY;
                     mt = fmaxf(mt, e[ns][k]);
                 }
             mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
