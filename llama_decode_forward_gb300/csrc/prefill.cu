@@ -624,23 +624,34 @@ __global__ void logits_kernel(DMat out, int wtype, const float* y, int dim, int 
     for (int r = blockIdx.x * wpb + warp; r < vocab; r += gridDim.x * wpb) {
         float s = 0.f;
         if (wtype == LLM_Q8_0) {
-            // lane takes 32-element blocks lane, lane + 32, ...: the block sum times its scale
+            // 16 quants per lane and step, the warp's 512 bytes contiguous:
+            // half a 32-element block times that block's scale (rows are
+            // multiples of 32 elements, the quant rows 16-byte aligned)
             const uint8_t* q = out.q + (size_t)r * out.cols;
-            for (int b = lane; b < dim / 32; b += 32) {
+            const __half* d = out.d + (size_t)r * out.dstride;
+#pragma unroll 4
+            for (int e = 16 * lane; e < dim; e += 512) {
+                const uint4 w = *reinterpret_cast<const uint4*>(q + e);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
                 float t = 0.f;
-                for (int k = 0; k < 32; k += 4) {
-                    const uint32_t w4 = *reinterpret_cast<const uint32_t*>(q + b * 32 + k);
 #pragma unroll
-                    for (int j = 0; j < 4; j++) t = fmaf((float)(int)(int8_t)((w4 >> (8 * j)) & 0xFFu), ys[b * 32 + k + j], t);
-                }
-                s = fmaf(__half2float(out.d[(size_t)r * out.dstride + b]), t, s);
+                for (int j = 0; j < 16; j++)
+                    t = fmaf((float)(int)(int8_t)((ws[j >> 2] >> (8 * (j & 3))) & 0xFFu), ys[e + j], t);
+                s = fmaf(__half2float(d[e >> 5]), t, s);
             }
         } else {
+            // 8 F16 values per lane and step (16 bytes), 512 bytes per warp
             const __half* w = reinterpret_cast<const __half*>(out.q) + (size_t)r * out.cols;
-            for (int d = 2 * lane; d < dim; d += 64) {
-                const float2 wv = __half22float2(*reinterpret_cast<const __half2*>(w + d));
-                s = fmaf(wv.x, ys[d], s);
-                s = fmaf(wv.y, ys[d + 1], s);
+#pragma unroll 4
+            for (int e = 8 * lane; e < dim; e += 256) {
+                const uint4 v = *reinterpret_cast<const uint4*>(w + e);
+                const uint32_t vs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&vs[j]));
+                    s = fmaf(f.x, ys[e + 2 * j], s);
+                    s = fmaf(f.y, ys[e + 2 * j + 1], s);
+                }
             }
         }
         s = warp_sum(s);
