@@ -85,7 +85,8 @@ struct GemmOut {
 };
 
 // Q8_0 weights of a GEMM: the FP16 scales of the library layout (row r's
-// block b at d[r * dstride + b]); the int8 quants come through a tensor map.
+// block b at d[r * dstride + b]; d 16-byte aligned, dstride the block count
+// rounded up to a multiple of 8); the int8 quants come through a tensor map.
 struct GemmScales {
     const __half* d;
     int dstride;
@@ -94,23 +95,31 @@ struct GemmScales {
 // Shared-memory plan of the GEMM: a ring of kStages stages (A tile, W tile
 // as F16, and for Q8_0 weights the W tile's int8 quants), then the
 // epilogue's transpose buffers and the barriers.
+//
+// F16 weights: a stage is the A tile and the F16 W tile.  Q8_0 weights: a
+// stage is the A tile and the W tile's int8 quants; the converters expand the
+// quants into one of kWBufs F16 W buffers outside the ring (so the ring keeps
+// more stages, and the expansions run ahead of the MMAs).
 template <int BN, bool Q8>
 struct GemmPlan {
-    static constexpr int kBBytes = BN * kGBK * 2;
+    static constexpr int kBBytes = BN * kGBK * 2;                 // one F16 W tile
     static constexpr int kQBytes = Q8 ? BN * kGBK : 0;
-    static constexpr int kStageBytes = kGABytes + kBBytes + kQBytes;
-    static constexpr int kStages = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
+    static constexpr int kStageBytes = kGABytes + (Q8 ? kQBytes : kBBytes);
     static constexpr int kEpiWarps = 4;
     // Q8_0 converter warps: 8, or 4 when the tile's BN x 4 work items do not
     // split evenly over 256 threads
     static constexpr int kConvWarps = !Q8 ? 0 : (BN * 4) % 256 == 0 ? 8 : 4;
+    static constexpr int kWBufs = 2;                               // F16 W buffers (Q8_0)
+    static constexpr int kWBufBytes = Q8 ? kWBufs * kBBytes : 0;
+    static constexpr int kStages =
+        (200 * 1024 - kWBufBytes) / kStageBytes > 8 ? 8 : (200 * 1024 - kWBufBytes) / kStageBytes;
     // TMEM columns of the two accumulators (a power of two of at least 32)
     static constexpr int kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128
                                      : 2 * BN <= 256 ? 256 : 512;
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kConvWarps);
     static constexpr int kTransBytes = kEpiWarps * 32 * 33 * 4;
-    static constexpr int kBarBytes = 8 * (3 * kStages + 4 + 1) + 16;
-    static constexpr int kSmem = kStages * kStageBytes + kTransBytes + kBarBytes + 1024;
+    static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kWBufs + 4 + 1) + 16;
+    static constexpr int kSmem = kStages * kStageBytes + kWBufBytes + kTransBytes + kBarBytes + 1024;
 };
 
 // One F16 value of the W tile in the 128-byte-swizzled K-major layout the
@@ -119,6 +128,11 @@ struct GemmPlan {
 __device__ __forceinline__ uint32_t sw128_chunk(uint32_t tile, int r, int c) {
     return tile + (uint32_t)r * 128u + (uint32_t)((c ^ (r & 7)) * 16);
 }
+
+// Byte offset of 16-byte chunk c (0..3) of row r in a tile of 64-byte rows
+// loaded with the 64-byte TMA swizzle (address bits 4-5 XOR bits 7-8): eight
+// consecutive rows' chunk c then fall in eight different bank groups.
+__device__ __forceinline__ int sw64_chunk(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
 
 // Four int8 quants (one word) times the scale pair d2, as two F16 pairs: the
 // quant q becomes the F16 value 1152 + q exactly (bytes 0x64, q ^ 0x80: 1024
@@ -161,11 +175,14 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
     constexpr int S = G::kStages;
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-    float* trans = reinterpret_cast<float*>(sm + S * G::kStageBytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S * G::kStageBytes + G::kTransBytes);
+    constexpr int WB = G::kWBufs;
+    uint8_t* wbuf = sm + S * G::kStageBytes;                       // Q8_0: [WB] F16 W tiles
+    float* trans = reinterpret_cast<float*>(wbuf + G::kWBufBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(wbuf + G::kWBufBytes + G::kTransBytes);
     uint64_t* empty = full + S;
-    uint64_t* conv = empty + S;          // Q8_0: the stage's W tile is expanded
-    uint64_t* accf = conv + S;           // [2] accumulator b holds a finished tile
+    uint64_t* wfull = empty + S;         // [WB] Q8_0: W buffer b holds an expanded tile
+    uint64_t* wempty = wfull + WB;       // [WB] Q8_0: the MMAs reading W buffer b are done
+    uint64_t* accf = wempty + WB;        // [2] accumulator b holds a finished tile
     uint64_t* acce = accf + 2;           // [2] accumulator b has been read
     uint64_t* fin = acce + 2;            // every MMA issued has completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
@@ -178,7 +195,10 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
         for (int s = 0; s < S; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&conv[s], G::kConvWarps > 0 ? G::kConvWarps : 1);
+        }
+        for (int b = 0; b < WB; b++) {
+            mbar_init(&wfull[b], G::kConvWarps > 0 ? G::kConvWarps : 1);
+            mbar_init(&wempty[b], 1);
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(&accf[b], 1);
@@ -210,7 +230,7 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
                     uint8_t* st = sm + s * G::kStageBytes;
                     mbar_arrive_expect_tx(&full[s], (uint32_t)(kGABytes + (Q8 ? G::kQBytes : G::kBBytes)));
                     tma_2d_g2s(st, &ma, kt * kGBK, m0, &full[s]);
-                    tma_2d_g2s(st + kGABytes + (Q8 ? G::kBBytes : 0), &mb, kt * kGBK, n0, &full[s]);
+                    tma_2d_g2s(st + kGABytes, &mb, kt * kGBK, n0, &full[s]);   // the W tile (F16 or quants)
                 }
             }
             // the last copies have landed before the CTA can exit (at once when
@@ -234,11 +254,13 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
                 for (int kt = 0; kt < nk; kt++, it++) {
                     const int s = (int)(it % S);
                     const uint32_t par = (uint32_t)((it / S) & 1);
+                    const int wb = (int)(it % WB);
                     if (!(ok = wait_parity(&full[s], par, err))) break;
-                    if (Q8 && !(ok = wait_parity(&conv[s], par, err))) break;
+                    if (Q8 && !(ok = wait_parity(&wfull[wb], (uint32_t)((it / WB) & 1), err))) break;
                     asm volatile("tcgen05.fence::after_thread_sync;");
                     uint8_t* st = sm + s * G::kStageBytes;
-                    const uint64_t da = umma_desc_sw128(st), db = umma_desc_sw128(st + kGABytes);
+                    const uint64_t da = umma_desc_sw128(st),
+                                   db = umma_desc_sw128(Q8 ? wbuf + wb * G::kBBytes : st + kGABytes);
 #pragma unroll
                     for (int kk = 0; kk < kGBK / 16; kk++) {
                         const uint32_t accumulate = (kt > 0 || kk > 0) ? 1u : 0u;
@@ -250,6 +272,10 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
                     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                                      smem_addr(&empty[s]))
                                  : "memory");
+                    if (Q8)
+                        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                         smem_addr(&wempty[wb]))
+                                     : "memory");
                 }
                 if (!ok) break;
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -348,7 +374,9 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
         // output chunks are items i = c + kCT k of the kCT converter threads
         // (row i % BN, pair i / BN): 16 quants in, 16 F16 values out.  Each
         // item's row has its two block scales of a k-step in one 4-byte
-        // word, loaded a k-step ahead.
+        // word; the words of four k-steps are one 16-byte load (a row's
+        // scales start 16-byte aligned and are padded to a multiple of 8
+        // blocks), issued four k-steps before the first of them is used.
         constexpr int kCT = 32 * G::kConvWarps;
         const int c = threadIdx.x - 32 * (2 + G::kEpiWarps);
         constexpr int kItems = BN * 4 / kCT;
@@ -367,28 +395,40 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
                 const int wrow = n0 + (c + kCT * j) % BN;           // item j's row
                 drow[j] = wrow < N ? reinterpret_cast<const uint32_t*>(ws.d + (size_t)wrow * ws.dstride) : nullptr;
             }
-            uint32_t dnext[kRows];
+            uint4 dq[kRows], dqn[kRows];
+            const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int j = 0; j < kRows; j++) dnext[j] = drow[j] ? __ldg(drow[j]) : 0u;
+            for (int j = 0; j < kRows; j++) {
+                dqn[j] = drow[j] ? __ldg(reinterpret_cast<const uint4*>(drow[j])) : zero4;
+                dq[j] = zero4;
+            }
             for (int kt = 0; kt < nk; kt++, it++) {
+                if ((kt & 3) == 0) {
+#pragma unroll
+                    for (int j = 0; j < kRows; j++) {
+                        dq[j] = dqn[j];
+                        dqn[j] = drow[j] && kt + 4 < nk ? __ldg(reinterpret_cast<const uint4*>(drow[j] + kt + 4)) : zero4;
+                    }
+                }
                 uint32_t dcur[kRows];
 #pragma unroll
                 for (int j = 0; j < kRows; j++) {
-                    dcur[j] = dnext[j];
-                    dnext[j] = drow[j] && kt + 1 < nk ? __ldg(drow[j] + kt + 1) : 0u;
+                    const uint4 v = dq[j];
+                    dcur[j] = (kt & 2) ? ((kt & 1) ? v.w : v.z) : ((kt & 1) ? v.y : v.x);
                 }
-                const int s = (int)(it % S);
+                const int s = (int)(it % S), wb = (int)(it % WB);
                 if (!(ok = sleep_parity(&full[s], (uint32_t)((it / S) & 1), err))) break;
+                if (!(ok = sleep_parity(&wempty[wb], (uint32_t)(((it / WB) & 1) ^ 1), err))) break;
                 uint8_t* st = sm + s * G::kStageBytes;
-                const uint32_t btile = smem_addr(st + kGABytes);
-                const uint8_t* qtile = st + kGABytes + G::kBBytes;
+                const uint32_t btile = smem_addr(wbuf + wb * G::kBBytes);
+                const uint8_t* qtile = st + kGABytes;
 #pragma unroll
                 for (int k = 0; k < kItems; k++) {
                     const int i = c + kCT * k, r = i % BN, pair = i / BN;
                     const uint32_t dw = dcur[kSameRow ? 0 : k];
                     const __half d = __ushort_as_half((unsigned short)(pair < 2 ? dw & 0xFFFFu : dw >> 16));
                     const __half2 d2 = __half2half2(d);
-                    const uint4 qv = *reinterpret_cast<const uint4*>(qtile + r * kGBK + pair * 16);
+                    const uint4 qv = *reinterpret_cast<const uint4*>(qtile + sw64_chunk(r, pair));
                     uint32_t h[8];
                     q4_to_f16(qv.x, d2, h[0], h[1]);
                     q4_to_f16(qv.y, d2, h[2], h[3]);
@@ -401,7 +441,7 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
                 }
                 fence_proxy_async_smem();                               // the MMA reads the tile
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&conv[s]);
+                if (lane == 0) mbar_arrive(&wfull[wb]);
             }
         }
     }
@@ -964,7 +1004,7 @@ bool gemm_map(CUtensorMap* m, const void* base, int K, int rows, int box_rows = 
 }
 
 // The int8 quants of a Q8_0 matrix in the library layout ([rows][K], K
-// contiguous) as BN x 64 boxes, no swizzle.
+// contiguous) as BN x 64 boxes, 64-byte swizzle (sw64_chunk).
 bool q8_map(CUtensorMap* m, const void* base, int K, int rows, int box_rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
@@ -973,7 +1013,7 @@ bool q8_map(CUtensorMap* m, const void* base, int K, int rows, int box_rows) {
     cuuint32_t box[2] = {(cuuint32_t)kGBK, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), gdim, gstride, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
