@@ -377,15 +377,19 @@ def prefill_flops(cfg, n: int) -> float:
 
 def run_prefill(args):
     """Optional line (not the headline): a 1B-shape model's 512-token batched
-    prefill (the Qwen2-style F16 model, or Llama 3.2 Q8_0 whose matrices are
-    expanded to F16 before each GEMM), tokens per second and tensor-core
-    TFLOP/s."""
+    prefill (the Qwen2-style F16 model, or Llama 3.2 Q8_0 whose quants are
+    expanded to F16 tile by tile inside each GEMM, or with --prefill-f16-copy
+    read from the handle's F16 copy of the layer matrices), tokens per second
+    and tensor-core TFLOP/s."""
     import torch
     import llama_decode_forward_gb300 as L
     base = PREFILL_CFGS[args.prefill_weights]
     cfg = base.scaled(max_seq=PREFILL_N + 128)
     W = synth.make_weights(cfg)
     dec = L.Decoder(cfg, W)
+    copy = args.prefill_f16_copy and args.prefill_weights == "q8_0"
+    if copy:
+        L.llm_prefill_f16_copy(dec.h)
     toks = synth.prompt(cfg, PREFILL_N)
     logits = np.empty(cfg.vocab, np.float32)
     for _ in range(max(args.warmup, 3)):
@@ -418,7 +422,9 @@ def run_prefill(args):
             "warmup": max(args.warmup, 3), "ms_per_step": 1000.0 * el / args.steps, "higher_is_better": True,
             "dtype": "f16 operands, f32 accumulate",
             "data": f"synthetic (seeded random {args.prefill_weights.upper()} weights and tokens)",
-            "config": {"workload": f"{base.name} prefill, 512 tokens", "flops_per_prefill": fl},
+            "config": {"workload": f"{base.name} prefill, 512 tokens", "flops_per_prefill": fl,
+                       "q8_0_operands": ("F16 copy of the layer matrices (llm_prefill_f16_copy)" if copy
+                                         else "expanded inside each GEMM") if args.prefill_weights == "q8_0" else None},
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak if peak else None,
                          "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops; f16 taken equal)"},
@@ -443,6 +449,8 @@ def main():
                     help="decode (the headline line) or the optional batched-prefill line")
     ap.add_argument("--prefill-weights", choices=sorted(PREFILL_CFGS), default="f16",
                     help="weight type of the prefill line's model")
+    ap.add_argument("--prefill-f16-copy", action="store_true",
+                    help="Q8_0 prefill line: give the handle its F16 copy of the layer matrices first")
     ap.add_argument("--model", choices=sorted(DECODE_MODELS), default="llama1b_q8",
                     help="decode workload's model: the Llama-3.2-1B shape (the headline) or the Llama-2-7B shape")
     ap.add_argument("--numerics", choices=["exact", "llamacpp"], default="exact",

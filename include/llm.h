@@ -164,6 +164,19 @@ int llm_generate(llm_handle *h, int32_t token, int32_t pos, int32_t n_steps, int
 int llm_prefill(llm_handle *h, const int32_t *tokens_host, int32_t n, int32_t pos0,
                 float *logits_host, int32_t *argmax_host);
 
+/* enable != 0: gives a Q8_0 handle an F16 copy of its layer matrices (QKV, O,
+ * gate/up, down), each value d*q rounded to nearest even: the values the
+ * batched prefill's GEMMs otherwise expand from the quants tile by tile.
+ * Later llm_prefill calls read the copy instead, with the same results bit
+ * for bit and the GEMMs at the speed of F16 weights; the decode step still
+ * streams the Q8_0 matrices.  Costs 2 bytes of device memory per layer
+ * weight (about 2 GB for a 1B model); enabling twice keeps one copy.
+ * enable == 0 frees the copy (waiting for the handle's stream first).
+ * Asynchronous on the handle's stream.  Errors: UNSUPPORTED for F16 or F32
+ * weights or a model whose prefill runs token by token, NO_MEMORY (nothing
+ * kept), CUDA. */
+int llm_prefill_f16_copy(llm_handle *h, int enable);
+
 /* Waits for the handle's stream and reports a device-side error of the
  * enqueued steps (DEVICE_TIMEOUT, OUT_OF_RANGE) or CUDA. */
 int llm_sync(llm_handle *h);

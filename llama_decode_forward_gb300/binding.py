@@ -94,6 +94,7 @@ _SIGS = {
     "llm_test_logits_limit": ([_vp, _i32], _int),
     "llm_test_guards": ([_vp], ctypes.c_int64),
     "llm_test_poke_guard": ([_vp, _int], _int),
+    "llm_prefill_f16_copy": ([_vp, _int], _int),
 }
 
 
@@ -201,6 +202,12 @@ def llm_prefill(h, tokens_host, pos0: int, logits_host: np.ndarray | None = None
     _check_logits_buffer(h, logits_host)
     _check(_lib.llm_prefill(h, t.ctypes.data, t.size, int(pos0), _ptr(logits_host), ctypes.addressof(out)), h)
     return out.value
+
+
+def llm_prefill_f16_copy(h, enable: bool = True) -> None:
+    """Keep (or free) the F16 copy of a Q8_0 handle's layer matrices that the
+    batched prefill's GEMMs then read."""
+    _check(_lib.llm_prefill_f16_copy(h, 1 if enable else 0), h)
 
 
 def llm_sync(h):

@@ -145,6 +145,8 @@ struct llm_handle {
     unsigned long long* trace = nullptr;   // LLM_TRACE builds: [sms][kTraceSlots]
     void* prefill_ws = nullptr;      // prefill workspace (lazily sized)
     size_t prefill_ws_bytes = 0;
+    __half* f16_copy = nullptr;      // llm_prefill_f16_copy: F16 copy of the Q8_0 layer matrices
+    size_t f16_copy_bytes = 0;
     int test_logits_limit = 0;       // llm_test_logits_limit: > 0 narrows the checked logits bound
 };
 
@@ -302,6 +304,7 @@ static void free_handle(llm_handle* h) {
     cudaFree(h->d_layers);
     cudaFree(h->kv_maps);
     guarded_free(h->ws_mem);
+    cudaFree(h->f16_copy);
     cudaFree(h->trace);
     if (h->pinned) cudaFreeHost(h->pinned);
     cudaGetLastError();
@@ -764,6 +767,56 @@ extern "C" int llm_generate(llm_handle* h, int32_t token, int32_t pos, int32_t n
     return LLM_OK;
 }
 
+static PrefillCtx prefill_ctx(const llm_handle* h) {
+    PrefillCtx pc{};
+    pc.st = h->st; pc.sms = h->sms; pc.wtype = h->cfg.wtype;
+    pc.n_layers = h->cfg.n_layers; pc.dim = h->cfg.dim; pc.n_heads = h->cfg.n_heads; pc.n_kv = h->cfg.n_kv_heads;
+    pc.hd = h->cfg.head_dim; pc.ffn = h->cfg.ffn_dim; pc.vocab = h->cfg.vocab; pc.rope_dims = h->cfg.rope_dims;
+    pc.neox = h->cfg.rope_neox; pc.q_dim = h->q_dim; pc.kv_dim = h->kv_dim;
+    pc.eps = h->cfg.eps; pc.theta_scale = h->theta_scale; pc.attn_div = h->attn_div;
+    pc.layers = h->layers.data(); pc.embd = h->embd; pc.out = h->out; pc.out_norm = h->out_norm;
+    pc.rope_freqs = h->rope_freqs; pc.logits = h->logits; pc.argmax_dev = h->tok_out; pc.best = h->best; pc.err = h->err;
+    pc.f16_copy = h->f16_copy;
+    return pc;
+}
+
+extern "C" int llm_prefill_f16_copy(llm_handle* h, int enable) {
+    LIVE_OR_RETURN(h);
+    if (!enable) {
+        if (h->f16_copy) {
+            CK(h, cudaStreamSynchronize(h->st));
+            CK(h, cudaFree(h->f16_copy));
+            h->f16_copy = nullptr;
+            h->f16_copy_bytes = 0;
+        }
+        return LLM_OK;
+    }
+    if (h->f16_copy) return LLM_OK;
+    PrefillCtx pc = prefill_ctx(h);
+    if (h->cfg.wtype != LLM_Q8_0)
+        return fail(h, LLM_ERR_UNSUPPORTED, "an F16 prefill copy is for Q8_0 weights only");
+    if (!prefill_supported(pc))
+        return fail(h, LLM_ERR_UNSUPPORTED, "this model's prefill runs the decode step token by token");
+    const size_t bytes = prefill_f16_copy_bytes(pc);
+    void* p = nullptr;
+    if (dev_alloc(&p, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(h, LLM_ERR_NO_MEMORY, "allocating the %zu-byte F16 prefill copy", bytes);
+    }
+    int launches = 0;
+    const cudaError_t e = prefill_make_f16_copy(pc, static_cast<__half*>(p), &launches);
+    h->launches += launches;
+    if (e == cudaSuccess) {
+        h->f16_copy = static_cast<__half*>(p);
+        h->f16_copy_bytes = bytes;
+        return LLM_OK;
+    }
+    cudaStreamSynchronize(h->st);
+    cudaFree(p);
+    cudaGetLastError();
+    return fail(h, LLM_ERR_CUDA, "F16 prefill copy: %s", cudaGetErrorString(e));
+}
+
 extern "C" int llm_prefill(llm_handle* h, const int32_t* tokens_host, int32_t n, int32_t pos0, float* logits_host,
                            int32_t* argmax_host) {
     LIVE_OR_RETURN(h);
@@ -775,14 +828,7 @@ extern "C" int llm_prefill(llm_handle* h, const int32_t* tokens_host, int32_t n,
         if (tokens_host[i] < 0 || tokens_host[i] >= h->cfg.vocab)
             return fail(h, LLM_ERR_OUT_OF_RANGE, "token %d not in [0, %d)", tokens_host[i], h->cfg.vocab);
     int rc;
-    PrefillCtx pc{};
-    pc.st = h->st; pc.sms = h->sms; pc.wtype = h->cfg.wtype;
-    pc.n_layers = h->cfg.n_layers; pc.dim = h->cfg.dim; pc.n_heads = h->cfg.n_heads; pc.n_kv = h->cfg.n_kv_heads;
-    pc.hd = h->cfg.head_dim; pc.ffn = h->cfg.ffn_dim; pc.vocab = h->cfg.vocab; pc.rope_dims = h->cfg.rope_dims;
-    pc.neox = h->cfg.rope_neox; pc.q_dim = h->q_dim; pc.kv_dim = h->kv_dim;
-    pc.eps = h->cfg.eps; pc.theta_scale = h->theta_scale; pc.attn_div = h->attn_div;
-    pc.layers = h->layers.data(); pc.embd = h->embd; pc.out = h->out; pc.out_norm = h->out_norm;
-    pc.rope_freqs = h->rope_freqs; pc.logits = h->logits; pc.argmax_dev = h->tok_out; pc.best = h->best; pc.err = h->err;
+    const PrefillCtx pc = prefill_ctx(h);
     if (prefill_supported(pc)) {
         // F16 weights: tensor-core batches of up to kPrefillRows tokens
         const size_t need = prefill_workspace_bytes(pc);

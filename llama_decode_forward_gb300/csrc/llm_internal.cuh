@@ -196,9 +196,14 @@ struct PrefillCtx {
     int* argmax_dev;                         // the last token's argmax
     unsigned long long* best;                // argmax key, zero before and after
     int* err;                                // device error word
+    const __half* f16_copy;                  // Q8_0: the F16 copy of the layer matrices, or nullptr
 };
 bool prefill_supported(const PrefillCtx& c);
 size_t prefill_workspace_bytes(const PrefillCtx& c);
+// The F16 copy of a Q8_0 model's layer matrices for the prefill GEMMs: its
+// size, and its expansion (asynchronous on c.st; *launches counts kernels).
+size_t prefill_f16_copy_bytes(const PrefillCtx& c);
+cudaError_t prefill_make_f16_copy(const PrefillCtx& c, __half* dst, int* launches);
 cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_host, int n, int pos0, const char** msg);
 
 __host__ __device__ inline int dtype_bytes_x16(int wtype) {   // bytes per element, times 16

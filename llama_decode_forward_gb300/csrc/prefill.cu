@@ -704,6 +704,31 @@ __global__ void logits_kernel(DMat out, int wtype, const float* y, int dim, int 
     if (lane == 0 && key) atomicMax(best, key);
 }
 
+// The F16 copy of a Q8_0 matrix (rows x cols, cols a multiple of 64): each
+// thread expands one 16-value chunk with q4_to_f16, the routine the GEMM's
+// converter warps use, so the copy holds the very values those warps write
+// into shared memory (d * q rounded to nearest even).
+__global__ void q8_expand_kernel(const uint8_t* __restrict__ q, const __half* __restrict__ d, int dstride, int rows,
+                                 int cols, __half* __restrict__ y) {
+    const int chunks = cols / 16;
+    const long long total = (long long)rows * chunks;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const long long r = e / chunks;
+        const int c = (int)(e % chunks);
+        const __half2 d2 = __half2half2(d[r * dstride + c / 2]);
+        const uint4 qv = *reinterpret_cast<const uint4*>(q + r * cols + c * 16);
+        uint4 a, b;
+        q4_to_f16(qv.x, d2, a.x, a.y);
+        q4_to_f16(qv.y, d2, a.z, a.w);
+        q4_to_f16(qv.z, d2, b.x, b.y);
+        q4_to_f16(qv.w, d2, b.z, b.w);
+        uint4* out = reinterpret_cast<uint4*>(y + r * cols + c * 16);
+        out[0] = a;
+        out[1] = b;
+    }
+}
+
 __global__ void argmax_publish_kernel(unsigned long long* best, int* out) {
     *out = argmax_key_index(*best);
     *best = 0ull;
@@ -1042,6 +1067,52 @@ bool prefill_supported(const PrefillCtx& c) {
            c.n_heads / c.n_kv * c.hd <= 8 * 128 && c.rope_dims / 2 <= 128;
 }
 
+// The four GEMM weight matrices of layer l (QKV, O, gate/up as single rows,
+// down): their rows and columns, and their element offsets in the F16 copy
+// (each matrix starts 256-byte aligned).
+static void copy_shape(const PrefillCtx& c, int l, int k, int* rows, int* cols) {
+    const LayerDev& L = c.layers[l];
+    switch (k) {
+        case 0: *rows = L.qkv.rows; *cols = c.dim; break;
+        case 1: *rows = L.o.rows; *cols = c.q_dim; break;
+        case 2: *rows = 2 * L.gu.rows; *cols = c.dim; break;
+        default: *rows = L.down.rows; *cols = c.ffn; break;
+    }
+}
+
+static size_t copy_offset(const PrefillCtx& c, int l, int k) {
+    size_t off = 0;
+    for (int i = 0; i < 4 * l + k; i++) {
+        int rows, cols;
+        copy_shape(c, i / 4, i % 4, &rows, &cols);
+        off += ((size_t)rows * cols + 127) & ~(size_t)127;
+    }
+    return off;
+}
+
+size_t prefill_f16_copy_bytes(const PrefillCtx& c) { return copy_offset(c, c.n_layers, 0) * sizeof(__half); }
+
+cudaError_t prefill_make_f16_copy(const PrefillCtx& c, __half* dst, int* launches) {
+    *launches = 0;
+    if (c.wtype != LLM_Q8_0) return cudaErrorInvalidValue;
+    for (int l = 0; l < c.n_layers; l++) {
+        const LayerDev& L = c.layers[l];
+        const DMat* m[4] = {&L.qkv, &L.o, &L.gu, &L.down};
+        for (int k = 0; k < 4; k++) {
+            int rows, cols;
+            copy_shape(c, l, k, &rows, &cols);
+            const long long chunks = (long long)rows * (cols / 16);
+            const int blocks = (int)((chunks + 255) / 256 < 65535 ? (chunks + 255) / 256 : 65535);
+            q8_expand_kernel<<<blocks, 256, 0, c.st>>>(static_cast<const uint8_t*>(m[k]->q), m[k]->d, m[k]->dstride,
+                                                      rows, cols, dst + copy_offset(c, l, k));
+            ++*launches;
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return cudaSuccess;
+}
+
 size_t prefill_workspace_bytes(const PrefillCtx& c) {
     const size_t M = kPrefillRows;
     auto al = [](size_t b) { return (b + 255) & ~(size_t)255; };
@@ -1076,22 +1147,25 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
         *msg = "tensor map of an activation operand";
         return cudaErrorInvalidValue;
     }
-    // weight operands: the F16 matrices, or the int8 quants of the Q8_0 ones
-    // (expanded to F16 tile by tile inside the GEMM), per layer: QKV, O,
-    // gate/up (single rows), down; box heights = the GEMMs' tile widths
-    const bool q8 = c.wtype == LLM_Q8_0;
+    // weight operands: the F16 matrices, the F16 copy of the Q8_0 ones, or
+    // the int8 quants of the Q8_0 ones (expanded to F16 tile by tile inside
+    // the GEMM), per layer: QKV, O, gate/up (single rows), down; box heights =
+    // the GEMMs' tile widths
+    const bool q8 = c.wtype == LLM_Q8_0 && !c.f16_copy;
     std::vector<CUtensorMap> mw((size_t)4 * c.n_layers);
+    static constexpr int kBox[4] = {kBnQkv, kBnNarrow, kBnWide, kBnNarrow};
     for (int l = 0; l < c.n_layers; l++) {
         const LayerDev& L = c.layers[l];
-        auto map = [&](CUtensorMap* m, const DMat& d, int K, int rows, int box) {
-            return q8 ? q8_map(m, d.q, K, rows, box) : gemm_map(m, d.q, K, rows, box);
-        };
-        if (!map(&mw[4 * l + 0], L.qkv, c.dim, L.qkv.rows, kBnQkv) ||
-            !map(&mw[4 * l + 1], L.o, c.q_dim, L.o.rows, kBnNarrow) ||
-            !map(&mw[4 * l + 2], L.gu, c.dim, 2 * L.gu.rows, kBnWide) ||
-            !map(&mw[4 * l + 3], L.down, c.ffn, L.down.rows, kBnNarrow)) {
-            *msg = "tensor map of a weight matrix";
-            return cudaErrorInvalidValue;
+        const DMat* dm[4] = {&L.qkv, &L.o, &L.gu, &L.down};
+        for (int k = 0; k < 4; k++) {
+            int rows, cols;
+            copy_shape(c, l, k, &rows, &cols);
+            const void* base = c.f16_copy ? static_cast<const void*>(c.f16_copy + copy_offset(c, l, k)) : dm[k]->q;
+            if (!(q8 ? q8_map(&mw[4 * l + k], base, cols, rows, kBox[k])
+                     : gemm_map(&mw[4 * l + k], base, cols, rows, kBox[k]))) {
+                *msg = "tensor map of a weight matrix";
+                return cudaErrorInvalidValue;
+            }
         }
     }
     auto run = [&](auto bn, auto epi, const CUtensorMap& ma, const CUtensorMap& mb, const DMat& wm, const GemmOut& o,
