@@ -43,6 +43,36 @@ constexpr int kGABytes = kGBM * kGBK * 2;
 constexpr int kBnQkv = 128, kBnNarrow = 64, kBnWide = 256;
 constexpr long long kSpinLimit = 200000000ll;   // mbarrier polls before a wait gives up
 
+// Programmatic dependent launch.  Every kernel of the batched prefill is
+// launched with programmatic stream serialization (launch_dep) and lets the
+// next kernel be scheduled as soon as all its own CTAs are running
+// (griddep_launch); each waits for the whole previous kernel to complete, its
+// memory visible (griddep_wait), before it touches activations.  So a
+// kernel's launch and setup overlap the tail of the one before, and nothing
+// else changes.  (Without the launch attribute both are no-ops.)
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_entry() {
+    griddep_launch();
+    griddep_wait();
+}
+
+// A launch with programmatic stream serialization (see griddep_entry).
+template <class... KArgs, class... Args>
+cudaError_t launch_dep(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t par, int* err) {
     for (long long i = 0; i < kSpinLimit; i++)
         if (mbar_test_wait(bar, par)) return true;
@@ -173,6 +203,7 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
                 GemmOut o, int M, int N, int K, int* err) {
     using G = GemmPlan<BN, Q8>;
     constexpr int S = G::kStages;
+    griddep_launch();
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
     constexpr int WB = G::kWBufs;
@@ -216,6 +247,7 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;");
     const uint32_t tmem = *tmem_slot;
+    griddep_wait();                      // the barriers and TMEM were set up while the previous kernel finished
 
     if (warp == 0) {
         // ---- producer
@@ -454,6 +486,7 @@ __global__ void __launch_bounds__(GemmPlan<BN, Q8>::kThreads, 1)
 // Embedding rows of the batch: F16 widened, or Q8_0 decoded as d * qs (both
 // exact in F32; Q8_0 quants are stored as int8).
 __global__ void embed_rows_kernel(const int* tok, int n, DMat embd, int wtype, int dim, float* X) {
+    griddep_entry();
     const int i = blockIdx.x;
     if (i >= n) return;
     const size_t r = (size_t)tok[i];
@@ -472,6 +505,7 @@ __global__ void embed_rows_kernel(const int* tok, int n, DMat embd, int wtype, i
 // scale = 1/sqrt(mean(x^2) + eps)); the GEMM operand is y rounded to F16.
 // One warp per row, 8 values per 16-byte step (dim % 8 == 0).
 __global__ void rmsnorm_rows_f16_kernel(const float* X, int n, int dim, const float* g, float eps, __half* Y) {
+    griddep_entry();
     const int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (i >= n) return;
     const float4* x4 = reinterpret_cast<const float4*>(X + (size_t)i * dim);
@@ -506,6 +540,7 @@ __global__ void rmsnorm_rows_f16_kernel(const float* X, int n, int dim, const fl
 // why" §2.4), cos/sin taken in double.  The angles depend only on the
 // position, so one table serves every layer of the batch.
 __global__ void rope_table_kernel(float* tab, int n, int pos0, int half, float theta_scale, const float* freqs) {
+    griddep_entry();
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= n * half) return;
     const int i = e / half, j = e % half;
@@ -523,6 +558,7 @@ __global__ void rope_table_kernel(float* tab, int n, int pos0, int half, float t
 // Examples 7 and 10).
 __global__ void rope_kv_rows_kernel(float* QKV, int n, int pos0, int n_heads, int n_kv, int hd, int rope_dims, int neox,
                                     const float* tab, __half* kc, __half* vc) {
+    griddep_entry();
     const int i = blockIdx.x;
     if (i >= n) return;
     const int pos = pos0 + i;
@@ -557,6 +593,7 @@ constexpr int kAttnTile = 128;
 __global__ void __launch_bounds__(128) attention_rows_kernel(const float* QKV, int n, int pos0, int n_heads, int n_kv,
                                                              int hd, float attn_div, const __half* kc,
                                                              const __half* vc, __half* A) {
+    griddep_entry();
     const int i = blockIdx.x, g = blockIdx.y;
     if (i >= n) return;
     const int gq = n_heads / n_kv, q_dim = n_heads * hd, kv_dim = n_kv * hd, GD = gq * hd;
@@ -642,6 +679,7 @@ __global__ void __launch_bounds__(128) attention_rows_kernel(const float* QKV, i
 // The last row: RMSNorm in F32 (as the decode step), logits of every vocabulary
 // row (F16 output matrix), argmax key of each warp's rows.
 __global__ void final_norm_kernel(const float* x, int dim, const float* g, float eps, float* y) {
+    griddep_entry();
     float ss = 0.f;
     for (int d = threadIdx.x; d < dim; d += blockDim.x) ss += x[d] * x[d];
     __shared__ float red[32];
@@ -656,6 +694,7 @@ __global__ void final_norm_kernel(const float* x, int dim, const float* g, float
 
 __global__ void logits_kernel(DMat out, int wtype, const float* y, int dim, int vocab, float* logits,
                               unsigned long long* best) {
+    griddep_entry();
     extern __shared__ float ys[];
     for (int d = threadIdx.x; d < dim; d += blockDim.x) ys[d] = y[d];
     __syncthreads();
@@ -730,6 +769,7 @@ __global__ void q8_expand_kernel(const uint8_t* __restrict__ q, const __half* __
 }
 
 __global__ void argmax_publish_kernel(unsigned long long* best, int* out) {
+    griddep_entry();
     *out = argmax_key_index(*best);
     *best = 0ull;
 }
@@ -787,6 +827,7 @@ __global__ void __launch_bounds__(HD == 128 ? 256 : 512) attention_mma_kernel(co
                                                                               int n_heads, int n_kv,
                                                             float attn_div, const __half* kc, const __half* vc,
                                                             __half* A, int split) {
+    griddep_entry();
     constexpr int PITCH = HD + 8;                // halves per shared-memory row
     extern __shared__ __align__(16) __half kvs[];   // [2 buffers][K, V][kAttnKT][PITCH]; then the warps' partials
     const int gq = n_heads / n_kv, q_dim = n_heads * HD, kv_dim = n_kv * HD, row_w = q_dim + 2 * kv_dim;
@@ -1006,13 +1047,8 @@ bool attention_mma_launch(cudaStream_t st, const float* QKV, int n, int pos0, in
         *e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (*e != cudaSuccess) return true;
     }
-    if (hd == 32)
-        attention_mma_kernel<32><<<grid, block, smem, st>>>(QKV, n, pos0, n_heads, n_kv, attn_div, kc, vc, A, split);
-    else if (hd == 64)
-        attention_mma_kernel<64><<<grid, block, smem, st>>>(QKV, n, pos0, n_heads, n_kv, attn_div, kc, vc, A, split);
-    else
-        attention_mma_kernel<128><<<grid, block, smem, st>>>(QKV, n, pos0, n_heads, n_kv, attn_div, kc, vc, A, split);
-    *e = cudaGetLastError();
+    auto k = hd == 32 ? attention_mma_kernel<32> : hd == 64 ? attention_mma_kernel<64> : attention_mma_kernel<128>;
+    *e = launch_dep(k, grid, block, smem, st, QKV, n, pos0, n_heads, n_kv, attn_div, kc, vc, A, split);
     return true;
 }
 
@@ -1056,8 +1092,8 @@ cudaError_t gemm(cudaStream_t st, int sms, const CUtensorMap& ma, const CUtensor
         attr = true;
     }
     const int tiles = ((M + kGBM - 1) / kGBM) * ((N + BN - 1) / BN);
-    gemm_kernel<BN, EPI, Q8><<<tiles < sms ? tiles : sms, G::kThreads, G::kSmem, st>>>(ma, mb, ws, o, M, N, K, err);
-    return cudaGetLastError();
+    return launch_dep(gemm_kernel<BN, EPI, Q8>, dim3(tiles < sms ? tiles : sms), dim3(G::kThreads), (size_t)G::kSmem, st,
+                      ma, mb, ws, o, M, N, K, err);
 }
 
 }  // namespace
@@ -1191,50 +1227,51 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
         const int nb = n - b0 < kPrefillRows ? n - b0 : kPrefillRows;
         const int p0 = pos0 + b0;
         PF_CK(cudaMemcpyAsync(tok, tokens_host + b0, (size_t)nb * 4, cudaMemcpyHostToDevice, c.st), "token upload");
-        embed_rows_kernel<<<nb, 256, 0, c.st>>>(tok, nb, c.embd, c.wtype, c.dim, X);
-        PF_CK(cudaGetLastError(), "embedding");
+        PF_CK(launch_dep(embed_rows_kernel, dim3(nb), dim3(256), 0, c.st, tok, nb, c.embd, c.wtype, c.dim, X),
+              "embedding");
         {
             const int cells = nb * (c.rope_dims / 2);
-            rope_table_kernel<<<(cells + 255) / 256, 256, 0, c.st>>>(rtab, nb, p0, c.rope_dims / 2, c.theta_scale,
-                                                                     c.rope_freqs);
-            PF_CK(cudaGetLastError(), "RoPE table");
+            PF_CK(launch_dep(rope_table_kernel, dim3((cells + 255) / 256), dim3(256), 0, c.st, rtab, nb, p0,
+                             c.rope_dims / 2, c.theta_scale, c.rope_freqs),
+                  "RoPE table");
         }
         const int norm_blocks = (nb + 7) / 8;
         for (int l = 0; l < c.n_layers; l++) {
             const LayerDev& L = c.layers[l];
-            rmsnorm_rows_f16_kernel<<<norm_blocks, 256, 0, c.st>>>(X, nb, c.dim, L.attn_norm, c.eps, Xh);
-            PF_CK(cudaGetLastError(), "attention RMSNorm");
+            PF_CK(launch_dep(rmsnorm_rows_f16_kernel, dim3(norm_blocks), dim3(256), 0, c.st, X, nb, c.dim, L.attn_norm,
+                             c.eps, Xh),
+                  "attention RMSNorm");
             GemmOut oq{QKV, L.qkv_bias, nullptr, nullptr};
             PF_CK(run(Qkv{}, EBias{}, mXh, mw[4 * l + 0], L.qkv, oq, nb, L.qkv.rows, c.dim), "QKV GEMM");
-            rope_kv_rows_kernel<<<nb, 128, 0, c.st>>>(QKV, nb, p0, c.n_heads, c.n_kv, c.hd, c.rope_dims, c.neox, rtab,
-                                                      L.kc, L.vc);
-            PF_CK(cudaGetLastError(), "RoPE and KV append");
+            PF_CK(launch_dep(rope_kv_rows_kernel, dim3(nb), dim3(128), 0, c.st, QKV, nb, p0, c.n_heads, c.n_kv, c.hd,
+                             c.rope_dims, c.neox, rtab, L.kc, L.vc),
+                  "RoPE and KV append");
             {
                 cudaError_t ea = cudaSuccess;
                 if (!attention_mma_launch(c.st, QKV, nb, p0, c.n_heads, c.n_kv, c.hd, c.attn_div, L.kc, L.vc, Ah, &ea)) {
-                    attention_rows_kernel<<<dim3(nb, c.n_kv), 128, attn_smem, c.st>>>(QKV, nb, p0, c.n_heads, c.n_kv,
-                                                                                      c.hd, c.attn_div, L.kc, L.vc, Ah);
-                    ea = cudaGetLastError();
+                    ea = launch_dep(attention_rows_kernel, dim3(nb, c.n_kv), dim3(128), (size_t)attn_smem, c.st, QKV,
+                                    nb, p0, c.n_heads, c.n_kv, c.hd, c.attn_div, L.kc, L.vc, Ah);
                 }
                 PF_CK(ea, "attention");
             }
             GemmOut oo{nullptr, nullptr, X, nullptr};
             PF_CK(run(Narrow{}, EResid{}, mAh, mw[4 * l + 1], L.o, oo, nb, c.dim, c.q_dim), "O GEMM");
-            rmsnorm_rows_f16_kernel<<<norm_blocks, 256, 0, c.st>>>(X, nb, c.dim, L.ffn_norm, c.eps, Xh);
-            PF_CK(cudaGetLastError(), "FFN RMSNorm");
+            PF_CK(launch_dep(rmsnorm_rows_f16_kernel, dim3(norm_blocks), dim3(256), 0, c.st, X, nb, c.dim, L.ffn_norm,
+                             c.eps, Xh),
+                  "FFN RMSNorm");
             GemmOut og{nullptr, nullptr, nullptr, Hh};
             PF_CK(run(Wide{}, ESwi{}, mXh, mw[4 * l + 2], L.gu, og, nb, 2 * L.gu.rows, c.dim), "gate/up GEMM");
             GemmOut od{nullptr, nullptr, X, nullptr};
             PF_CK(run(Narrow{}, EResid{}, mHh, mw[4 * l + 3], L.down, od, nb, c.dim, c.ffn), "down GEMM");
         }
         if (b0 + nb == n) {
-            final_norm_kernel<<<1, 256, 0, c.st>>>(X + (size_t)(nb - 1) * c.dim, c.dim, c.out_norm, c.eps, ylast);
-            PF_CK(cudaGetLastError(), "final RMSNorm");
-            logits_kernel<<<c.sms * 4, 256, (size_t)c.dim * 4, c.st>>>(c.out, c.wtype, ylast, c.dim, c.vocab, c.logits,
-                                                                       c.best);
-            PF_CK(cudaGetLastError(), "logits");
-            argmax_publish_kernel<<<1, 1, 0, c.st>>>(c.best, c.argmax_dev);
-            PF_CK(cudaGetLastError(), "argmax");
+            PF_CK(launch_dep(final_norm_kernel, dim3(1), dim3(256), 0, c.st, (const float*)(X + (size_t)(nb - 1) * c.dim),
+                             c.dim, c.out_norm, c.eps, ylast),
+                  "final RMSNorm");
+            PF_CK(launch_dep(logits_kernel, dim3(c.sms * 4), dim3(256), (size_t)c.dim * 4, c.st, c.out, c.wtype,
+                             (const float*)ylast, c.dim, c.vocab, c.logits, c.best),
+                  "logits");
+            PF_CK(launch_dep(argmax_publish_kernel, dim3(1), dim3(1), 0, c.st, c.best, c.argmax_dev), "argmax");
         }
     }
 #undef PF_CK
