@@ -832,198 +832,207 @@ __global__ void __launch_bounds__(HD == 128 ? 256 : 512) attention_mma_kernel(co
     extern __shared__ __align__(16) __half kvs[];   // [2 buffers][K, V][kAttnKT][PITCH]; then the warps' partials
     const int gq = n_heads / n_kv, q_dim = n_heads * HD, kv_dim = n_kv * HD, row_w = q_dim + 2 * kv_dim;
     const int ntile = (n + 15) / 16;
-    const int qt = ntile - 1 - (int)blockIdx.x;  // the longest rows first
-    const int g = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int hq = warp % gq, sp = warp / gq;
-    const int h = g * gq + hq;
-    const int t0 = qt * 16;
-    const int r = lane >> 2, t = lane & 3;
-    const int n_pos = pos0 + min(t0 + 16, n);    // positions the tile's last row attends to
-    // this thread's two rows; rows past the batch take the last row's causal limit (never stored)
-    const int R0 = min(t0 + r, n - 1), R1 = min(t0 + r + 8, n - 1);
-    // q fragments: element (row t0 + r + 8 (j & 1), column ks*16 + 8 (j >> 1) + 2t + {0, 1})
-    uint32_t qhi[HD / 16][4], qlo[HD / 16][4];
-#pragma unroll
-    for (int ks = 0; ks < HD / 16; ks++)
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            const int row = (j & 1) ? R1 : R0, col = ks * 16 + (j >> 1) * 8 + 2 * t;
-            const float2 x = *reinterpret_cast<const float2*>(QKV + (size_t)row * row_w + h * HD + col);
-            const __half hx = __float2half_rn(x.x), hy = __float2half_rn(x.y);
-            qhi[ks][j] = h2_bits(hx, hy);
-            qlo[ks][j] = h2_bits(__float2half_rn(x.x - __half2float(hx)), __float2half_rn(x.y - __half2float(hy)));
+    // two query tiles per block, the longest with the shortest (tiles
+    // ntile-1-i and i): equal work in every block, one wave of blocks
+    const int bx = (int)blockIdx.x;
+    for (int pass = 0; pass < 2; pass++) {
+        const int qt = pass == 0 ? ntile - 1 - bx : bx;
+        if (pass == 1) {
+            if (qt >= ntile - 1 - bx) break;
+            __syncthreads();                         // the fold's reads of the reused K/V buffer are done
         }
-    float o[HD / 8][4];
-#pragma unroll
-    for (int nt = 0; nt < HD / 8; nt++) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-    const int ntiles = (n_pos + kAttnKT - 1) / kAttnKT;
-    // score / sqrt(head_dim): a power-of-two divisor (head_dim 64, 256, ...)
-    // divides exactly as a multiply by its reciprocal (the same bits)
-    const bool div_pow2 = (__float_as_uint(attn_div) & 0x007FFFFFu) == 0u;
-    const float inv_div = __frcp_rn(attn_div);
-    auto scale_score = [&](float x) { return div_pow2 ? __fmul_rn(x, inv_div) : __fdiv_rn(x, attn_div); };
-    auto load_tile = [&](int c, int buf) {
-        __half* ks_ = kvs + (size_t)(buf * 2) * kAttnKT * PITCH;
-        __half* vs_ = ks_ + kAttnKT * PITCH;
-        constexpr int W = HD / 8;                // 16-byte words per row
-        for (int e = threadIdx.x; e < kAttnKT * W; e += blockDim.x) {
-            const int pr = e / W, w = e % W;
-            const int pos = min(c * kAttnKT + pr, n_pos - 1);   // rows past n_pos repeat a valid row (masked)
-            const size_t src = (size_t)pos * kv_dim + (size_t)g * HD + w * 8;
-            cp_async16(ks_ + pr * PITCH + w * 8, kc + src);
-            cp_async16(vs_ + pr * PITCH + w * 8, vc + src);
-        }
-        cp_async_commit();
-    };
-    load_tile(0, 0);
-    for (int c = 0; c < ntiles; c++) {
-        if (c + 1 < ntiles) {
-            load_tile(c + 1, (c + 1) & 1);
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-        } else {
-            cp_async_wait_all();
-        }
-        __syncthreads();
-        const __half* ks_ = kvs + (size_t)((c & 1) * 2) * kAttnKT * PITCH;
-        const __half* vs_ = ks_ + kAttnKT * PITCH;
-        const uint32_t kbase = smem_addr(ks_), vbase = smem_addr(vs_);
-        // this warp's sub-tiles of the tile: global index = sp modulo split
-        const int sub0 = ((sp - c * (kAttnKT / 16)) % split + split) % split;
-        for (int sub = sub0; sub < kAttnKT / 16; sub += split) {
-            const int p0 = c * kAttnKT + sub * 16;
-            if (p0 >= n_pos) break;
-            // scores of positions p0 + 8 nt + 2t + {0, 1}, rows r and r + 8
-            float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            {
-                const int mi = lane >> 3, ri = lane & 7;
-                const uint32_t krow = kbase + (uint32_t)((sub * 16 + ri + (mi >= 2 ? 8 : 0)) * PITCH * 2);
-#pragma unroll
-                for (int ks = 0; ks < HD / 16; ks++) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(krow + (uint32_t)((ks * 16 + (mi & 1) * 8) * 2), b0, b1, b2, b3);
-                    mma16816(s[0], qhi[ks], b0, b1);
-                    mma16816(s[1], qhi[ks], b2, b3);
-                    mma16816(s[0], qlo[ks], b0, b1);
-                    mma16816(s[1], qlo[ks], b2, b3);
-                }
-            }
-            float mt0 = -INFINITY, mt1 = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < 2; nt++)
-#pragma unroll
-                for (int k = 0; k < 2; k++) {
-                    const int P = p0 + nt * 8 + 2 * t + k;
-                    s[nt][k] = P <= pos0 + R0 ? scale_score(s[nt][k]) : -INFINITY;
-                    s[nt][2 + k] = P <= pos0 + R1 ? scale_score(s[nt][2 + k]) : -INFINITY;
-                    mt0 = fmaxf(mt0, s[nt][k]);
-                    mt1 = fmaxf(mt1, s[nt][2 + k]);
-                }
-            mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, 1));
-            mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, 2));
-            mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, 1));
-            mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, 2));
-            const float mn0 = fmaxf(m0, mt0), mn1 = fmaxf(m1, mt1);
-            const float c0 = expf(m0 - mn0), c1 = expf(m1 - mn1);   // 0 on the first tile (m = -inf)
-            float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 2; nt++)
-#pragma unroll
-                for (int k = 0; k < 2; k++) {
-                    s[nt][k] = expf(s[nt][k] - mn0);
-                    s[nt][2 + k] = expf(s[nt][2 + k] - mn1);
-                    ls0 += s[nt][k];
-                    ls1 += s[nt][2 + k];
-                }
-            ls0 += __shfl_xor_sync(0xffffffffu, ls0, 1);
-            ls0 += __shfl_xor_sync(0xffffffffu, ls0, 2);
-            ls1 += __shfl_xor_sync(0xffffffffu, ls1, 1);
-            ls1 += __shfl_xor_sync(0xffffffffu, ls1, 2);
-            l0 = l0 * c0 + ls0;
-            l1 = l1 * c1 + ls1;
-            m0 = mn0;
-            m1 = mn1;
-#pragma unroll
-            for (int nt = 0; nt < HD / 8; nt++) {
-                o[nt][0] *= c0;
-                o[nt][1] *= c0;
-                o[nt][2] *= c1;
-                o[nt][3] *= c1;
-            }
-            // probabilities as A fragments (the accumulator layout is the A layout): hi and lo parts
-            uint32_t phi[4], plo[4];
-#pragma unroll
+        const int g = blockIdx.y;
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int hq = warp % gq, sp = warp / gq;
+        const int h = g * gq + hq;
+        const int t0 = qt * 16;
+        const int r = lane >> 2, t = lane & 3;
+        const int n_pos = pos0 + min(t0 + 16, n);    // positions the tile's last row attends to
+        // this thread's two rows; rows past the batch take the last row's causal limit (never stored)
+        const int R0 = min(t0 + r, n - 1), R1 = min(t0 + r + 8, n - 1);
+        // q fragments: element (row t0 + r + 8 (j & 1), column ks*16 + 8 (j >> 1) + 2t + {0, 1})
+        uint32_t qhi[HD / 16][4], qlo[HD / 16][4];
+    #pragma unroll
+        for (int ks = 0; ks < HD / 16; ks++)
+    #pragma unroll
             for (int j = 0; j < 4; j++) {
-                const float x = s[j >> 1][(j & 1) * 2], y = s[j >> 1][(j & 1) * 2 + 1];
-                const __half hx = __float2half_rn(x), hy = __float2half_rn(y);
-                phi[j] = h2_bits(hx, hy);
-                plo[j] = h2_bits(__float2half_rn(x - __half2float(hx)), __float2half_rn(y - __half2float(hy)));
+                const int row = (j & 1) ? R1 : R0, col = ks * 16 + (j >> 1) * 8 + 2 * t;
+                const float2 x = *reinterpret_cast<const float2*>(QKV + (size_t)row * row_w + h * HD + col);
+                const __half hx = __float2half_rn(x.x), hy = __float2half_rn(x.y);
+                qhi[ks][j] = h2_bits(hx, hy);
+                qlo[ks][j] = h2_bits(__float2half_rn(x.x - __half2float(hx)), __float2half_rn(x.y - __half2float(hy)));
             }
-            {
-                const int mi = lane >> 3, ri = lane & 7;
-                const uint32_t vrow = vbase + (uint32_t)((sub * 16 + ri + (mi & 1) * 8) * PITCH * 2);
-#pragma unroll
-                for (int nt = 0; nt < HD / 8; nt += 2) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(vrow + (uint32_t)(((nt + (mi >> 1)) * 8) * 2), b0, b1, b2, b3);
-                    mma16816(o[nt], phi, b0, b1);
-                    mma16816(o[nt + 1], phi, b2, b3);
-                    mma16816(o[nt], plo, b0, b1);
-                    mma16816(o[nt + 1], plo, b2, b3);
+        float o[HD / 8][4];
+    #pragma unroll
+        for (int nt = 0; nt < HD / 8; nt++) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+        const int ntiles = (n_pos + kAttnKT - 1) / kAttnKT;
+        // score / sqrt(head_dim): a power-of-two divisor (head_dim 64, 256, ...)
+        // divides exactly as a multiply by its reciprocal (the same bits)
+        const bool div_pow2 = (__float_as_uint(attn_div) & 0x007FFFFFu) == 0u;
+        const float inv_div = __frcp_rn(attn_div);
+        auto scale_score = [&](float x) { return div_pow2 ? __fmul_rn(x, inv_div) : __fdiv_rn(x, attn_div); };
+        auto load_tile = [&](int c, int buf) {
+            __half* ks_ = kvs + (size_t)(buf * 2) * kAttnKT * PITCH;
+            __half* vs_ = ks_ + kAttnKT * PITCH;
+            constexpr int W = HD / 8;                // 16-byte words per row
+            for (int e = threadIdx.x; e < kAttnKT * W; e += blockDim.x) {
+                const int pr = e / W, w = e % W;
+                const int pos = min(c * kAttnKT + pr, n_pos - 1);   // rows past n_pos repeat a valid row (masked)
+                const size_t src = (size_t)pos * kv_dim + (size_t)g * HD + w * 8;
+                cp_async16(ks_ + pr * PITCH + w * 8, kc + src);
+                cp_async16(vs_ + pr * PITCH + w * 8, vc + src);
+            }
+            cp_async_commit();
+        };
+        load_tile(0, 0);
+        for (int c = 0; c < ntiles; c++) {
+            if (c + 1 < ntiles) {
+                load_tile(c + 1, (c + 1) & 1);
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
+            } else {
+                cp_async_wait_all();
+            }
+            __syncthreads();
+            const __half* ks_ = kvs + (size_t)((c & 1) * 2) * kAttnKT * PITCH;
+            const __half* vs_ = ks_ + kAttnKT * PITCH;
+            const uint32_t kbase = smem_addr(ks_), vbase = smem_addr(vs_);
+            // this warp's sub-tiles of the tile: global index = sp modulo split
+            const int sub0 = ((sp - c * (kAttnKT / 16)) % split + split) % split;
+            for (int sub = sub0; sub < kAttnKT / 16; sub += split) {
+                const int p0 = c * kAttnKT + sub * 16;
+                if (p0 >= n_pos) break;
+                // scores of positions p0 + 8 nt + 2t + {0, 1}, rows r and r + 8
+                float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                {
+                    const int mi = lane >> 3, ri = lane & 7;
+                    const uint32_t krow = kbase + (uint32_t)((sub * 16 + ri + (mi >= 2 ? 8 : 0)) * PITCH * 2);
+    #pragma unroll
+                    for (int ks = 0; ks < HD / 16; ks++) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(krow + (uint32_t)((ks * 16 + (mi & 1) * 8) * 2), b0, b1, b2, b3);
+                        mma16816(s[0], qhi[ks], b0, b1);
+                        mma16816(s[1], qhi[ks], b2, b3);
+                        mma16816(s[0], qlo[ks], b0, b1);
+                        mma16816(s[1], qlo[ks], b2, b3);
+                    }
+                }
+                float mt0 = -INFINITY, mt1 = -INFINITY;
+    #pragma unroll
+                for (int nt = 0; nt < 2; nt++)
+    #pragma unroll
+                    for (int k = 0; k < 2; k++) {
+                        const int P = p0 + nt * 8 + 2 * t + k;
+                        s[nt][k] = P <= pos0 + R0 ? scale_score(s[nt][k]) : -INFINITY;
+                        s[nt][2 + k] = P <= pos0 + R1 ? scale_score(s[nt][2 + k]) : -INFINITY;
+                        mt0 = fmaxf(mt0, s[nt][k]);
+                        mt1 = fmaxf(mt1, s[nt][2 + k]);
+                    }
+                mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, 1));
+                mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, 2));
+                mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, 1));
+                mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, 2));
+                const float mn0 = fmaxf(m0, mt0), mn1 = fmaxf(m1, mt1);
+                const float c0 = expf(m0 - mn0), c1 = expf(m1 - mn1);   // 0 on the first tile (m = -inf)
+                float ls0 = 0.f, ls1 = 0.f;
+    #pragma unroll
+                for (int nt = 0; nt < 2; nt++)
+    #pragma unroll
+                    for (int k = 0; k < 2; k++) {
+                        s[nt][k] = expf(s[nt][k] - mn0);
+                        s[nt][2 + k] = expf(s[nt][2 + k] - mn1);
+                        ls0 += s[nt][k];
+                        ls1 += s[nt][2 + k];
+                    }
+                ls0 += __shfl_xor_sync(0xffffffffu, ls0, 1);
+                ls0 += __shfl_xor_sync(0xffffffffu, ls0, 2);
+                ls1 += __shfl_xor_sync(0xffffffffu, ls1, 1);
+                ls1 += __shfl_xor_sync(0xffffffffu, ls1, 2);
+                l0 = l0 * c0 + ls0;
+                l1 = l1 * c1 + ls1;
+                m0 = mn0;
+                m1 = mn1;
+    #pragma unroll
+                for (int nt = 0; nt < HD / 8; nt++) {
+                    o[nt][0] *= c0;
+                    o[nt][1] *= c0;
+                    o[nt][2] *= c1;
+                    o[nt][3] *= c1;
+                }
+                // probabilities as A fragments (the accumulator layout is the A layout): hi and lo parts
+                uint32_t phi[4], plo[4];
+    #pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const float x = s[j >> 1][(j & 1) * 2], y = s[j >> 1][(j & 1) * 2 + 1];
+                    const __half hx = __float2half_rn(x), hy = __float2half_rn(y);
+                    phi[j] = h2_bits(hx, hy);
+                    plo[j] = h2_bits(__float2half_rn(x - __half2float(hx)), __float2half_rn(y - __half2float(hy)));
+                }
+                {
+                    const int mi = lane >> 3, ri = lane & 7;
+                    const uint32_t vrow = vbase + (uint32_t)((sub * 16 + ri + (mi & 1) * 8) * PITCH * 2);
+    #pragma unroll
+                    for (int nt = 0; nt < HD / 8; nt += 2) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(vrow + (uint32_t)(((nt + (mi >> 1)) * 8) * 2), b0, b1, b2, b3);
+                        mma16816(o[nt], phi, b0, b1);
+                        mma16816(o[nt + 1], phi, b2, b3);
+                        mma16816(o[nt], plo, b0, b1);
+                        mma16816(o[nt + 1], plo, b2, b3);
+                    }
+                }
+            }
+            __syncthreads();                         // the buffer is reloaded two tiles later
+        }
+        // fold the head's other warps into warp sp = 0, in the order sp = 1, 2, ...
+        if (split > 1) {
+            constexpr int NV = HD / 2 + 4;           // a lane's accumulators, then m0, m1, l0, l1
+            float* part = reinterpret_cast<float*>(kvs);   // the K/V tiles are no longer read
+            if (sp > 0) {
+                float* pw = part + (size_t)((sp - 1) * gq + hq) * NV * 32 + lane;
+    #pragma unroll
+                for (int nt = 0; nt < HD / 8; nt++)
+    #pragma unroll
+                    for (int k = 0; k < 4; k++) pw[(nt * 4 + k) * 32] = o[nt][k];
+                pw[(HD / 2) * 32] = m0;
+                pw[(HD / 2 + 1) * 32] = m1;
+                pw[(HD / 2 + 2) * 32] = l0;
+                pw[(HD / 2 + 3) * 32] = l1;
+            }
+            __syncthreads();
+            if (sp > 0) continue;                    // warp 0 of the head folds and stores
+            for (int k2 = 1; k2 < split; k2++) {
+                const float* pw = part + (size_t)((k2 - 1) * gq + hq) * NV * 32 + lane;
+                const float om0 = pw[(HD / 2) * 32], om1 = pw[(HD / 2 + 1) * 32];
+                const float M0 = fmaxf(m0, om0), M1 = fmaxf(m1, om1);
+                const float a0 = m0 == -INFINITY ? 0.f : expf(m0 - M0), b0 = om0 == -INFINITY ? 0.f : expf(om0 - M0);
+                const float a1 = m1 == -INFINITY ? 0.f : expf(m1 - M1), b1 = om1 == -INFINITY ? 0.f : expf(om1 - M1);
+                l0 = l0 * a0 + pw[(HD / 2 + 2) * 32] * b0;
+                l1 = l1 * a1 + pw[(HD / 2 + 3) * 32] * b1;
+                m0 = M0;
+                m1 = M1;
+    #pragma unroll
+                for (int nt = 0; nt < HD / 8; nt++) {
+                    o[nt][0] = o[nt][0] * a0 + pw[(nt * 4 + 0) * 32] * b0;
+                    o[nt][1] = o[nt][1] * a0 + pw[(nt * 4 + 1) * 32] * b0;
+                    o[nt][2] = o[nt][2] * a1 + pw[(nt * 4 + 2) * 32] * b1;
+                    o[nt][3] = o[nt][3] * a1 + pw[(nt * 4 + 3) * 32] * b1;
                 }
             }
         }
-        __syncthreads();                         // the buffer is reloaded two tiles later
-    }
-    // fold the head's other warps into warp sp = 0, in the order sp = 1, 2, ...
-    if (split > 1) {
-        constexpr int NV = HD / 2 + 4;           // a lane's accumulators, then m0, m1, l0, l1
-        float* part = reinterpret_cast<float*>(kvs);   // the K/V tiles are no longer read
-        if (sp > 0) {
-            float* pw = part + (size_t)((sp - 1) * gq + hq) * NV * 32 + lane;
-#pragma unroll
-            for (int nt = 0; nt < HD / 8; nt++)
-#pragma unroll
-                for (int k = 0; k < 4; k++) pw[(nt * 4 + k) * 32] = o[nt][k];
-            pw[(HD / 2) * 32] = m0;
-            pw[(HD / 2 + 1) * 32] = m1;
-            pw[(HD / 2 + 2) * 32] = l0;
-            pw[(HD / 2 + 3) * 32] = l1;
+        const float i0 = 1.0f / l0, i1 = 1.0f / l1;
+        const int row0 = t0 + r, row1 = t0 + r + 8;
+    #pragma unroll
+        for (int nt = 0; nt < HD / 8; nt++) {
+            const int col = h * HD + nt * 8 + 2 * t;
+            if (row0 < n)
+                *reinterpret_cast<__half2*>(A + (size_t)row0 * q_dim + col) =
+                    __floats2half2_rn(o[nt][0] * i0, o[nt][1] * i0);
+            if (row1 < n)
+                *reinterpret_cast<__half2*>(A + (size_t)row1 * q_dim + col) =
+                    __floats2half2_rn(o[nt][2] * i1, o[nt][3] * i1);
         }
-        __syncthreads();
-        if (sp > 0) return;
-        for (int k2 = 1; k2 < split; k2++) {
-            const float* pw = part + (size_t)((k2 - 1) * gq + hq) * NV * 32 + lane;
-            const float om0 = pw[(HD / 2) * 32], om1 = pw[(HD / 2 + 1) * 32];
-            const float M0 = fmaxf(m0, om0), M1 = fmaxf(m1, om1);
-            const float a0 = m0 == -INFINITY ? 0.f : expf(m0 - M0), b0 = om0 == -INFINITY ? 0.f : expf(om0 - M0);
-            const float a1 = m1 == -INFINITY ? 0.f : expf(m1 - M1), b1 = om1 == -INFINITY ? 0.f : expf(om1 - M1);
-            l0 = l0 * a0 + pw[(HD / 2 + 2) * 32] * b0;
-            l1 = l1 * a1 + pw[(HD / 2 + 3) * 32] * b1;
-            m0 = M0;
-            m1 = M1;
-#pragma unroll
-            for (int nt = 0; nt < HD / 8; nt++) {
-                o[nt][0] = o[nt][0] * a0 + pw[(nt * 4 + 0) * 32] * b0;
-                o[nt][1] = o[nt][1] * a0 + pw[(nt * 4 + 1) * 32] * b0;
-                o[nt][2] = o[nt][2] * a1 + pw[(nt * 4 + 2) * 32] * b1;
-                o[nt][3] = o[nt][3] * a1 + pw[(nt * 4 + 3) * 32] * b1;
-            }
-        }
-    }
-    const float i0 = 1.0f / l0, i1 = 1.0f / l1;
-    const int row0 = t0 + r, row1 = t0 + r + 8;
-#pragma unroll
-    for (int nt = 0; nt < HD / 8; nt++) {
-        const int col = h * HD + nt * 8 + 2 * t;
-        if (row0 < n)
-            *reinterpret_cast<__half2*>(A + (size_t)row0 * q_dim + col) =
-                __floats2half2_rn(o[nt][0] * i0, o[nt][1] * i0);
-        if (row1 < n)
-            *reinterpret_cast<__half2*>(A + (size_t)row1 * q_dim + col) =
-                __floats2half2_rn(o[nt][2] * i1, o[nt][3] * i1);
     }
 }
 
@@ -1036,7 +1045,7 @@ bool attention_mma_launch(cudaStream_t st, const float* QKV, int n, int pos0, in
     // warps per head: up to 4, at most 16 warps a block (8 for head_dim 128,
     // whose accumulators need twice the registers)
     const int split = std::max(1, std::min(4, (hd == 128 ? 8 : 16) / gq));
-    const dim3 grid((n + 15) / 16, n_kv), block(32 * gq * split);
+    const dim3 grid(((n + 15) / 16 + 1) / 2, n_kv), block(32 * gq * split);   // two query tiles per block
     const size_t kv_bytes = (size_t)2 * 2 * kAttnKT * (hd + 8) * sizeof(__half);
     const size_t part_bytes = (size_t)(split - 1) * gq * (hd / 2 + 4) * 32 * sizeof(float);
     const size_t smem = std::max(kv_bytes, part_bytes);
