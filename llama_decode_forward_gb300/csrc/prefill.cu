@@ -696,7 +696,12 @@ __global__ void logits_kernel(DMat out, int wtype, const float* y, int dim, int 
                               unsigned long long* best) {
     griddep_entry();
     extern __shared__ float ys[];
-    for (int d = threadIdx.x; d < dim; d += blockDim.x) ys[d] = y[d];
+    // Q8_0: y[e] for e = 512 it + 16 l + 4 k + c sits at float4 (4 it + k) * 32 + l,
+    // component c, so the 32 lanes' float4 reads of one k are 512 contiguous
+    // bytes (the plain layout put lanes 16 floats apart: 16-way bank
+    // conflicts on every read); F16: the plain layout
+    for (int e = threadIdx.x; e < dim; e += blockDim.x)
+        ys[wtype == LLM_Q8_0 ? (((e >> 9) * 4 + ((e >> 2) & 3)) * 32 + ((e >> 4) & 31)) * 4 + (e & 3) : e] = y[e];
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
     unsigned long long key = 0ull;
@@ -712,10 +717,16 @@ __global__ void logits_kernel(DMat out, int wtype, const float* y, int dim, int 
             for (int e = 16 * lane; e < dim; e += 512) {
                 const uint4 w = *reinterpret_cast<const uint4*>(q + e);
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                const float4* y4 = reinterpret_cast<const float4*>(ys) + (size_t)(e >> 9) * 128 + lane;
                 float t = 0.f;
 #pragma unroll
-                for (int j = 0; j < 16; j++)
-                    t = fmaf((float)(int)(int8_t)((ws[j >> 2] >> (8 * (j & 3))) & 0xFFu), ys[e + j], t);
+                for (int k = 0; k < 4; k++) {
+                    const float4 v = y4[32 * k];
+                    const float yv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int c = 0; c < 4; c++)
+                        t = fmaf((float)(int)(int8_t)((ws[k] >> (8 * c)) & 0xFFu), yv[c], t);
+                }
                 s = fmaf(__half2float(d[e >> 5]), t, s);
             }
         } else {
@@ -1277,8 +1288,8 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
             PF_CK(launch_dep(final_norm_kernel, dim3(1), dim3(256), 0, c.st, (const float*)(X + (size_t)(nb - 1) * c.dim),
                              c.dim, c.out_norm, c.eps, ylast),
                   "final RMSNorm");
-            PF_CK(launch_dep(logits_kernel, dim3(c.sms * 4), dim3(256), (size_t)c.dim * 4, c.st, c.out, c.wtype,
-                             (const float*)ylast, c.dim, c.vocab, c.logits, c.best),
+            PF_CK(launch_dep(logits_kernel, dim3(c.sms * 4), dim3(256), (size_t)((c.dim + 511) & ~511) * 4, c.st,
+                             c.out, c.wtype, (const float*)ylast, c.dim, c.vocab, c.logits, c.best),
                   "logits");
             PF_CK(launch_dep(argmax_publish_kernel, dim3(1), dim3(1), 0, c.st, c.best, c.argmax_dev), "argmax");
         }
