@@ -123,4 +123,6 @@ def test_null_handle_calls_are_rejected():
     assert L.binding._lib.llm_decode_step(None, 0, 0, None, None) == L.LLM_ERR_INVALID_ARG
     assert L.binding._lib.llm_launch_count(None) == 0
     assert L.binding._lib.llm_get_config(None, None) == L.LLM_ERR_INVALID_ARG
+    assert L.binding._lib.llm_prefill_f16_copy(None, 1) == L.LLM_ERR_INVALID_ARG
+    assert L.binding._lib.llm_prefill_f16_copy(None, 0) == L.LLM_ERR_INVALID_ARG
     L.binding._lib.llm_destroy(None)
