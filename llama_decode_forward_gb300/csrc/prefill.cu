@@ -7,17 +7,20 @@
 // C[M][N] = A[M][K] . W[N][K]^T with A the token rows (F16, rounded to
 // nearest even from the F32 activations) and W a weight matrix in the
 // library's row layout (F16, K contiguous; Q8_0 tiles are expanded to F16,
-// d * qs rounded to nearest even, in shared memory), F32 accumulation in
-// tensor memory.  The GEMM kernel is persistent and warp-specialised (one
-// CTA per SM; gemm_kernel below): a TMA producer warp, an MMA-issuing warp
-// with two TMEM accumulators, four epilogue warps (bias, residual add, or
-// SwiGLU over the interleaved gate/up columns, written through a
-// shared-memory transpose), and for Q8_0 four warps that expand the quants.
+// d * qs rounded to nearest even, in shared memory, or read from the
+// handle's F16 copy of the matrices made by q8_expand_kernel), F32
+// accumulation in tensor memory.  The GEMM kernel is persistent and
+// warp-specialised (one CTA per SM; gemm_kernel below): a TMA producer warp,
+// an MMA-issuing warp with two TMEM accumulators, four epilogue warps (bias,
+// residual add, or SwiGLU over the interleaved gate/up columns, written
+// through a shared-memory transpose), and for Q8_0 four or eight warps that
+// expand the quants.
 //
 // Causal attention over the cache runs on mma.sync tensor-core tiles
-// (attention_mma_kernel); the per-row steps (embedding, RMSNorm, the batch's
-// RoPE table, RoPE + KV append, the last row's logits and argmax) are plain
-// CUDA kernels.
+// (attention_mma_kernel, two query tiles per block); the per-row steps
+// (embedding, RMSNorm, the batch's RoPE table, RoPE + KV append, the last
+// row's logits and argmax) are plain CUDA kernels.  Every kernel of a batch
+// is a programmatic dependent launch (launch_dep, griddep_entry).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
