@@ -1258,11 +1258,14 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
                              c.rope_dims / 2, c.theta_scale, c.rope_freqs),
                   "RoPE table");
         }
-        const int norm_blocks = (nb + 7) / 8;
+        // RMSNorm: one warp per row, two rows per block, so a batch's rows
+        // spread over every SM (the row stream is bound by each SM's intake)
+        constexpr int kNormRows = 2;
+        const int norm_blocks = (nb + kNormRows - 1) / kNormRows;
         for (int l = 0; l < c.n_layers; l++) {
             const LayerDev& L = c.layers[l];
-            PF_CK(launch_dep(rmsnorm_rows_f16_kernel, dim3(norm_blocks), dim3(256), 0, c.st, X, nb, c.dim, L.attn_norm,
-                             c.eps, Xh),
+            PF_CK(launch_dep(rmsnorm_rows_f16_kernel, dim3(norm_blocks), dim3(32 * kNormRows), 0, c.st, X, nb, c.dim,
+                             L.attn_norm, c.eps, Xh),
                   "attention RMSNorm");
             GemmOut oq{QKV, L.qkv_bias, nullptr, nullptr};
             PF_CK(run(Qkv{}, EBias{}, mXh, mw[4 * l + 0], L.qkv, oq, nb, L.qkv.rows, c.dim), "QKV GEMM");
@@ -1279,8 +1282,8 @@ cudaError_t prefill_f16(const PrefillCtx& c, void* ws, const int32_t* tokens_hos
             }
             GemmOut oo{nullptr, nullptr, X, nullptr};
             PF_CK(run(Narrow{}, EResid{}, mAh, mw[4 * l + 1], L.o, oo, nb, c.dim, c.q_dim), "O GEMM");
-            PF_CK(launch_dep(rmsnorm_rows_f16_kernel, dim3(norm_blocks), dim3(256), 0, c.st, X, nb, c.dim, L.ffn_norm,
-                             c.eps, Xh),
+            PF_CK(launch_dep(rmsnorm_rows_f16_kernel, dim3(norm_blocks), dim3(32 * kNormRows), 0, c.st, X, nb, c.dim,
+                             L.ffn_norm, c.eps, Xh),
                   "FFN RMSNorm");
             GemmOut og{nullptr, nullptr, nullptr, Hh};
             PF_CK(run(Wide{}, ESwi{}, mXh, mw[4 * l + 2], L.gu, og, nb, 2 * L.gu.rows, c.dim), "gate/up GEMM");
